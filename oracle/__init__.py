@@ -1,0 +1,135 @@
+"""fp64 CPU oracle for KDA (Kimi Delta Attention) -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+``cpu_baseline`` / reference leg may import this package.  It shares no code
+with the CUDA path (no kernels, headers, helpers or constants), and the CUDA
+path never imports it.
+
+Two independent formulations of the same result:
+
+* :func:`kda_fwd` / :func:`kda_bwd` -- the plain token-by-token recurrence and
+  its hand-derived backward, in C (``kda_oracle.c``), threaded over
+  (sequence, value head).  This is *the* oracle.
+* :mod:`oracle.chunked` -- the chunk-wise WY/UT form (chunk-local gate
+  cumsum, decayed beta*K*K^T block, (I+L)^-1, w/u, inter-chunk state scan,
+  output, and the reverse state-gradient scan with the intra-chunk backward),
+  written in numpy fp64 with the pairwise decays formed directly.  It is used to
+  pin the token loop and to give per-chunk intermediates.
+
+Array layout (numpy float64): q,k [B,T,H,K]; v,dO [B,T,HV,V]; g [B,T,HV,K];
+beta [B,T,HV]; h0,dhT [N,HV,K,V].  ``cu_seqlens`` (int [N+1]) requires B == 1.
+Parity unpinned by the pages: they print no worked example, so every pin is
+mathematical (closed forms, invariants, finite differences, brute force,
+autograd of a naive loop); see ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libkda_oracle.so")
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (plain -O2, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+                               "-lm", "-lpthread"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            i64, i32 = ctypes.c_int64, ctypes.c_int
+            lib.kda_oracle_fwd.argtypes = [i64, i32, i32, i32, i32, i32, ip] + [dp] * 8 + [i32]
+            lib.kda_oracle_fwd.restype = i32
+            lib.kda_oracle_bwd.argtypes = [i64, i32, i32, i32, i32, i32, ip] + [dp] * 16 + [i32]
+            lib.kda_oracle_bwd.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _c64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _offsets(B, T, cu_seqlens):
+    if cu_seqlens is None:
+        return np.ascontiguousarray(np.arange(B + 1, dtype=np.int32) * T)
+    assert B == 1, "packed batches use B == 1"
+    return np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+
+
+def kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, output_final_state=True, nthreads=0):
+    """Token-by-token KDA forward.  Returns (o [B,T,HV,V], hT [N,HV,K,V] or None)."""
+    lib = _load()
+    q, k, v, g, beta, h0 = map(_c64, (q, k, v, g, beta, h0))
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    cu = _offsets(B, T, cu_seqlens)
+    N = len(cu) - 1
+    o = np.zeros((B, T, HV, V))
+    hT = np.zeros((N, HV, K, V)) if output_final_state else None
+    st = lib.kda_oracle_fwd(B * T, N, H, HV, K, V, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                            _p(q), _p(k), _p(v), _p(g), _p(beta), _p(h0), _p(o), _p(hT), nthreads)
+    if st != 0:
+        raise RuntimeError(f"kda_oracle_fwd failed ({st})")
+    return o, hT
+
+
+def kda_bwd(q, k, v, g, beta, h0, do, dhT, cu_seqlens=None, nthreads=0):
+    """Token-by-token KDA backward.  Returns dict dq, dk, dv, dg, dbeta, dh0."""
+    lib = _load()
+    q, k, v, g, beta, h0, do, dhT = map(_c64, (q, k, v, g, beta, h0, do, dhT))
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    cu = _offsets(B, T, cu_seqlens)
+    N = len(cu) - 1
+    out = dict(dq=np.zeros((B, T, H, K)), dk=np.zeros((B, T, H, K)), dv=np.zeros((B, T, HV, V)),
+               dg=np.zeros((B, T, HV, K)), dbeta=np.zeros((B, T, HV)), dh0=np.zeros((N, HV, K, V)))
+    dqp = np.zeros((B * T, HV, K))
+    dkp = np.zeros((B * T, HV, K))
+    st = lib.kda_oracle_bwd(B * T, N, H, HV, K, V, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                            _p(q), _p(k), _p(v), _p(g), _p(beta), _p(h0), _p(do), _p(dhT),
+                            _p(out["dq"]), _p(out["dk"]), _p(out["dv"]), _p(out["dg"]),
+                            _p(out["dbeta"]), _p(out["dh0"]), _p(dqp), _p(dkp), nthreads)
+    if st != 0:
+        raise RuntimeError(f"kda_oracle_bwd failed ({st})")
+    return out
+
+
+def rel_rms(x, ref) -> float:
+    """Relative RMS error ||x - ref||_2 / ||ref||_2 (the relative-RMS check style
+    of FLA's KDA tests).  A zero reference requires x == 0 exactly."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = float(np.sqrt(np.sum(ref * ref)))
+    num = float(np.sqrt(np.sum((x - ref) ** 2)))
+    if den == 0.0:
+        return 0.0 if num == 0.0 else float("inf")
+    return num / den

@@ -1,0 +1,275 @@
+"""Pins for the fp64 oracle: checks against facts fixed by the mathematics,
+not by the oracle itself (closed forms, invariants, finite differences,
+library autograd of a naive loop, an independent chunked formulation, and a
+hand-derived worked example).  CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import chunked
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_problem(rng, B=1, T=7, H=1, HV=1, K=3, V=2, h0=True, gscale=1.0):
+    q = rng.standard_normal((B, T, H, K))
+    k = rng.standard_normal((B, T, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, HV, V))
+    g = -gscale * np.log1p(np.exp(rng.standard_normal((B, T, HV, K))))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((B, T, HV))))
+    return q, k, v, g, beta
+
+
+def test_handcalc_golden():
+    vals = {}
+    with open(os.path.join(GOLDEN, "kda_handcalc_T3_K2_V1.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                name, *xs = line.split()
+                vals[name] = np.array([float(x) for x in xs])
+    K, V = int(vals["K"][0]), int(vals["V"][0])
+    T = 3
+    q = vals["q"].reshape(1, T, 1, K)
+    k = vals["k"].reshape(1, T, 1, K)
+    v = vals["v"].reshape(1, T, 1, V)
+    g = vals["g"].reshape(1, T, 1, K)
+    beta = vals["beta"].reshape(1, T, 1)
+    h0 = vals["h0"].reshape(1, 1, K, V)
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, h0)
+    np.testing.assert_allclose(o.reshape(-1) * math.sqrt(K), vals["o_times_sqrtK"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(hT.reshape(-1), vals["hT"], rtol=0, atol=1e-13)
+
+
+def test_no_gate_no_beta_state_unchanged_and_closed_form_grads():
+    """g = 0, beta = 0: S never changes, o_t = h0^T q_t / sqrt(K); the
+    gradients have closed forms."""
+    rng = np.random.default_rng(1)
+    B, T, H, HV, K, V = 1, 9, 1, 1, 4, 3
+    q, k, v, _, _ = rand_problem(rng, B, T, H, HV, K, V)
+    g = np.zeros((B, T, HV, K))
+    beta = np.zeros((B, T, HV))
+    h0 = rng.standard_normal((1, HV, K, V))
+    do = rng.standard_normal((B, T, HV, V))
+    dhT = rng.standard_normal((1, HV, K, V))
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, h0)
+    assert np.array_equal(hT, h0)
+    qs = q[0, :, 0] / math.sqrt(K)
+    np.testing.assert_allclose(o[0, :, 0], qs @ h0[0, 0], rtol=1e-14, atol=1e-14)
+    gr = oracle.kda_bwd(q, k, v, g, beta, h0, do, dhT)
+    assert np.all(gr["dv"] == 0)
+    np.testing.assert_allclose(gr["dq"][0, :, 0], do[0, :, 0] @ h0[0, 0].T / math.sqrt(K), atol=1e-13)
+    np.testing.assert_allclose(gr["dh0"][0, 0], dhT[0, 0] + qs.T @ do[0, :, 0], atol=1e-13)
+    # dbeta_t = (v_t - h0^T k_t) . (dS_t^T k_t), dS_t = dhT + sum_{s>=t} q~_s dO_s^T
+    for t in range(T):
+        dS = dhT[0, 0] + qs[t:].T @ do[0, t:, 0]
+        kt = k[0, t, 0]
+        want = (v[0, t, 0] - h0[0, 0].T @ kt) @ (dS.T @ kt)
+        assert abs(gr["dbeta"][0, t, 0] - want) < 1e-12
+
+
+def test_beta_zero_pure_decay_closed_form():
+    """beta = 0: S_t = diag(2^(g_1+..+g_t)) h0."""
+    rng = np.random.default_rng(2)
+    B, T, H, HV, K, V = 1, 6, 1, 1, 5, 2
+    q, k, v, g, _ = rand_problem(rng, B, T, H, HV, K, V)
+    beta = np.zeros((B, T, HV))
+    h0 = rng.standard_normal((1, HV, K, V))
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, h0)
+    G = np.cumsum(g[0, :, 0], axis=0)
+    for t in range(T):
+        S = np.exp2(G[t])[:, None] * h0[0, 0]
+        np.testing.assert_allclose(o[0, t, 0], S.T @ q[0, t, 0] / math.sqrt(K), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(hT[0, 0], np.exp2(G[-1])[:, None] * h0[0, 0], rtol=1e-13)
+
+
+def test_orthonormal_keys_write_exactly():
+    """g = 0, beta = 1, orthonormal keys, h0 = 0: the delta rule stores v_t
+    exactly (S^T k_t = v_t), so S = sum_s k_s v_s^T and o is causal linear
+    attention over the written pairs."""
+    rng = np.random.default_rng(3)
+    K, V, T = 6, 4, 5
+    Qm, _ = np.linalg.qr(rng.standard_normal((K, K)))
+    k = Qm[:, :T].T.reshape(1, T, 1, K)
+    q = rng.standard_normal((1, T, 1, K))
+    v = rng.standard_normal((1, T, 1, V))
+    g = np.zeros((1, T, 1, K))
+    beta = np.ones((1, T, 1))
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, None)
+    S = hT[0, 0]
+    for t in range(T):
+        np.testing.assert_allclose(S.T @ k[0, t, 0], v[0, t, 0], atol=1e-13)
+        want = sum((q[0, t, 0] @ k[0, s, 0]) * v[0, s, 0] for s in range(t + 1)) / math.sqrt(K)
+        np.testing.assert_allclose(o[0, t, 0], want, atol=1e-13)
+
+
+def test_scalar_case_closed_form():
+    """K = V = 1: s_t = a_t s + beta k (v - a_t s k) = alpha_t s + b_t with
+    alpha_t = a_t (1 - beta k^2), b_t = beta k v; a first-order linear
+    recurrence with the textbook solution s_T = (prod alpha) s_0 + sum_t b_t prod_{u>t} alpha_u."""
+    rng = np.random.default_rng(4)
+    T = 11
+    q = rng.standard_normal((1, T, 1, 1))
+    k = rng.standard_normal((1, T, 1, 1))
+    v = rng.standard_normal((1, T, 1, 1))
+    g = -np.abs(rng.standard_normal((1, T, 1, 1)))
+    beta = rng.uniform(0, 1, (1, T, 1))
+    h0 = rng.standard_normal((1, 1, 1, 1))
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, h0)
+    a = np.exp2(g.reshape(T))
+    kk, vv, bb = k.reshape(T), v.reshape(T), beta.reshape(T)
+    alpha = a * (1 - bb * kk * kk)
+    b = bb * kk * vv
+    for t in range(T):
+        s = np.prod(alpha[: t + 1]) * h0.item() + sum(b[u] * np.prod(alpha[u + 1: t + 1]) for u in range(t + 1))
+        assert abs(o[0, t, 0, 0] - s * q[0, t, 0, 0]) < 1e-13
+    assert abs(hT.item() - (np.prod(alpha) * h0.item() + sum(b[u] * np.prod(alpha[u + 1:]) for u in range(T)))) < 1e-13
+
+
+def test_empty_slots_pass_state_bitwise_and_split_invariance():
+    rng = np.random.default_rng(5)
+    T, H, HV, K, V = 40, 1, 2, 4, 3
+    q, k, v, g, beta = rand_problem(rng, 1, T, H, HV, K, V)
+    cu = [0, 0, 17, 17, 40, 40]
+    N = len(cu) - 1
+    h0 = rng.standard_normal((N, HV, K, V))
+    do = rng.standard_normal((1, T, HV, V))
+    dhT = rng.standard_normal((N, HV, K, V))
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, h0, cu)
+    gr = oracle.kda_bwd(q, k, v, g, beta, h0, do, dhT, cu)
+    for n in (0, 2, 4):  # empty slots
+        assert np.array_equal(hT[n], h0[n])
+        assert np.array_equal(gr["dh0"][n], dhT[n])
+    # split sequence [17, 40) at 29: run [17, 29), feed its final state as the
+    # initial state of [29, 40); must equal the unsplit run of [17, 40)
+    o_u, hT_u = oracle.kda_fwd(q, k, v, g, beta, np.stack([h0[1], h0[3]]), [0, 17, 40])
+    o_a, hT_a = oracle.kda_fwd(q, k, v, g, beta, np.stack([h0[1], h0[3]]), [0, 17, 29])
+    o_b, hT_b = oracle.kda_fwd(q, k, v, g, beta, np.stack([h0[1], hT_a[1]]), [0, 29, 40])
+    # the same operations on the same numbers: bitwise equal
+    assert np.array_equal(o_a[0, 17:29], o_u[0, 17:29])
+    assert np.array_equal(o_b[0, 29:40], o_u[0, 29:40])
+    assert np.array_equal(hT_b[1], hT_u[1])
+    # and the split changes nothing in the backward either
+    gu = oracle.kda_bwd(q, k, v, g, beta, np.stack([h0[1], h0[3]]), do, np.stack([dhT[1], dhT[3]]),
+                        [0, 17, 40])
+    gb = oracle.kda_bwd(q, k, v, g, beta, np.stack([h0[1], hT_a[1]]), do, np.stack([dhT[1], dhT[3]]),
+                        [0, 29, 40])
+    ga = oracle.kda_bwd(q, k, v, g, beta, np.stack([h0[1], h0[3]]), do, np.stack([dhT[1], gb["dh0"][1]]),
+                        [0, 17, 29])
+    for key in ("dv", "dg", "dbeta", "dq", "dk"):
+        np.testing.assert_allclose(gb[key][0, 29:40], gu[key][0, 29:40], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(ga[key][0, 17:29], gu[key][0, 17:29], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ga["dh0"][1], gu["dh0"][1], rtol=1e-12, atol=1e-13)
+
+
+def test_gva_head_map_contiguous_groups():
+    """HV = 2H: value head j reads q/k head j // 2 (contiguous groups)."""
+    rng = np.random.default_rng(6)
+    T, H, HV, K, V = 12, 2, 4, 3, 2
+    q, k, v, g, beta = rand_problem(rng, 1, T, H, HV, K, V)
+    h0 = rng.standard_normal((1, HV, K, V))
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, h0)
+    for j in range(HV):
+        h = j // 2
+        oj, hTj = oracle.kda_fwd(q[:, :, h:h + 1], k[:, :, h:h + 1], v[:, :, j:j + 1],
+                                 g[:, :, j:j + 1], beta[:, :, j:j + 1], h0[:, j:j + 1])
+        assert np.array_equal(oj[:, :, 0], o[:, :, j])
+        assert np.array_equal(hTj[:, 0], hT[:, j])
+
+
+@pytest.mark.parametrize("chunk", [1, 16, 64])
+def test_chunked_formulation_agrees(chunk):
+    rng = np.random.default_rng(7)
+    T, H, HV, K, V = 150, 1, 2, 8, 6
+    q, k, v, g, beta = rand_problem(rng, 1, T, H, HV, K, V, gscale=2.0)
+    cu = [0, 5, 5, 70, 150]
+    N = len(cu) - 1
+    h0 = rng.standard_normal((N, HV, K, V))
+    do = rng.standard_normal((1, T, HV, V))
+    dhT = rng.standard_normal((N, HV, K, V))
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, h0, cu)
+    o2, hT2 = chunked.kda_chunked_fwd(q, k, v, g, beta, h0, cu, chunk=chunk)
+    assert oracle.rel_rms(o2, o) < 1e-12 and oracle.rel_rms(hT2, hT) < 1e-12
+    gr = oracle.kda_bwd(q, k, v, g, beta, h0, do, dhT, cu)
+    gr2 = chunked.kda_chunked_bwd(q, k, v, g, beta, h0, do, dhT, cu, chunk=chunk)
+    for key in gr:
+        assert oracle.rel_rms(gr2[key], gr[key]) < 1e-11, key
+
+
+def test_finite_differences_every_gradient():
+    """Central differences (fp64) of L = <o, W> + <hT, Wh> against the
+    hand-derived backward, for every input element, GVA + an empty slot."""
+    rng = np.random.default_rng(8)
+    T, H, HV, K, V = 6, 1, 2, 3, 2
+    q, k, v, g, beta = rand_problem(rng, 1, T, H, HV, K, V)
+    cu = [0, 2, 2, 6]
+    N = 3
+    h0 = rng.standard_normal((N, HV, K, V))
+    W = rng.standard_normal((1, T, HV, V))
+    Wh = rng.standard_normal((N, HV, K, V))
+
+    def loss(q, k, v, g, beta, h0):
+        o, hT = oracle.kda_fwd(q, k, v, g, beta, h0, cu, nthreads=1)
+        return float(np.sum(o * W) + np.sum(hT * Wh))
+
+    gr = oracle.kda_bwd(q, k, v, g, beta, h0, W, Wh, cu, nthreads=1)
+    args = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0)
+    names = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta", h0="dh0")
+    eps = 1e-6
+    for name, arr in args.items():
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = loss(**args)
+            arr[idx] = old - eps
+            lm = loss(**args)
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        err = np.max(np.abs(fd - gr[names[name]])) / max(1.0, np.max(np.abs(fd)))
+        assert err < 1e-7, (name, err)
+
+
+def test_backward_matches_torch_autograd_of_naive_loop():
+    """torch.autograd (a library routine) differentiates a naive fp64 loop;
+    the oracle's hand-derived backward must agree."""
+    rng = np.random.default_rng(9)
+    T, H, HV, K, V = 20, 2, 4, 5, 3
+    q, k, v, g, beta = rand_problem(rng, 1, T, H, HV, K, V)
+    h0 = rng.standard_normal((1, HV, K, V))
+    do = rng.standard_normal((1, T, HV, V))
+    dhT = rng.standard_normal((1, HV, K, V))
+    tq, tk, tv, tg, tb, th = (torch.tensor(x, requires_grad=True) for x in (q, k, v, g, beta, h0))
+    outs = []
+    finals = []
+    for j in range(HV):
+        hh = j // (HV // H)
+        S = th[0, j]
+        oj = []
+        for t in range(T):
+            S = torch.exp2(tg[0, t, j])[:, None] * S
+            e = S.T @ tk[0, t, hh]
+            d = tb[0, t, j] * (tv[0, t, j] - e)
+            S = S + torch.outer(tk[0, t, hh], d)
+            oj.append(S.T @ tq[0, t, hh] / math.sqrt(K))
+        outs.append(torch.stack(oj))
+        finals.append(S)
+    o = torch.stack(outs, dim=1)[None]
+    hT = torch.stack(finals)[None]
+    L = (o * torch.tensor(do)).sum() + (hT * torch.tensor(dhT)).sum()
+    L.backward()
+    gr = oracle.kda_bwd(q, k, v, g, beta, h0, do, dhT)
+    for t_, key in ((tq, "dq"), (tk, "dk"), (tv, "dv"), (tg, "dg"), (tb, "dbeta"), (th, "dh0")):
+        np.testing.assert_allclose(gr[key], t_.grad.numpy(), rtol=1e-11, atol=1e-12, err_msg=key)
+
+
+def test_rel_rms_definition():
+    assert oracle.rel_rms([3.0, 4.0], [3.0, 4.0]) == 0.0
+    assert abs(oracle.rel_rms([3.0, 5.0], [3.0, 4.0]) - 0.2) < 1e-15
+    assert oracle.rel_rms([0.0], [0.0]) == 0.0
+    assert oracle.rel_rms([1e-30], [0.0]) == float("inf")
