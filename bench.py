@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark: chunked KDA forward + backward on one GB300 (or N replicas).
+
+One step = kda_chunk_fwd + kda_chunk_bwd through the C ABI on the dense
+training layer (B=8, T=4096, H=HV=32, K=V=128, bf16 q/k/v, fp32 g/beta, no
+initial or final state), inputs resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 it runs under torchrun, one replica per rank (no collective in the
+op: independent batches, weak scaling); rank 0 prints the max-over-ranks time.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload), as the slow reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_rule_42_gb300 import _lib, inputs  # noqa: E402
+from gated_delta_rule_42_gb300.ops import make_inputs_struct  # noqa: E402
+
+METRIC = "chunk_kda fwd+bwd tokens/s on 1 GB300 (bf16, K=V=128); % of roofline"
+WORKLOAD_CFG = 2  # the dense training layer
+L2_BYTES = 126 * 2 ** 20
+
+
+# --------------------------------------------------------------------------
+# algorithmic cost model (per token, whole layer): the bytes every step must
+# move at minimum (inputs read once, outputs written once, states) and the
+# flops of the chunked algorithm without recompute (triangular products at half)
+# --------------------------------------------------------------------------
+def algorithmic_bytes(cfg):
+    e = 2 if cfg.dtype == torch.bfloat16 else 4
+    H, HV, K, V = cfg.H, cfg.HV, cfg.K, cfg.V
+    inp = 2 * H * K * e + HV * V * e + 4 * HV * K + 4 * HV
+    fwd = inp + HV * V * e
+    bwd = inp + HV * V * e + 2 * H * K * e + HV * V * e + 4 * HV * K + 4 * HV
+    toks = cfg.valid_tokens
+    state = 4 * cfg.N * HV * K * V
+    st_f = (state if cfg.h0 is not None else 0) + (state if cfg.output_final_state else 0)
+    st_b = (state if cfg.h0 is not None else 0) + (2 * state if cfg.output_final_state else 0) + \
+        (state if cfg.h0 is not None else 0)
+    return dict(fwd=fwd * toks + st_f, bwd=bwd * toks + st_b, total=(fwd + bwd) * toks + st_f + st_b,
+                per_token_head=(fwd + bwd) / HV)
+
+
+def algorithmic_flops(cfg, C=64):
+    d = cfg.K
+    per = 18 * d * d + 15 * C * d + 2 * C * C
+    return per * cfg.valid_tokens * cfg.HV
+
+
+# Interface bytes per launch of each kernel (what the kernel must read and
+# write by its own contract), per token of the layer.  Used for the dominant
+# kernel's roofline.
+def kernel_bytes_per_token(name, cfg):
+    e = 2 if cfg.dtype == torch.bfloat16 else 4
+    H, HV, K, V = cfg.H, cfg.HV, cfg.K, cfg.V
+    qk, vv, g, b = H * K * e, HV * V * e, 4 * HV * K, 4 * HV
+    f32K, f32V, cc, hh = 4 * HV * K, 4 * HV * V, 4 * HV * 64, 4 * HV * K * V / 64
+    table = {
+        "simple_intra_kernel": 2 * qk + vv + g + b + 2 * f32K + 2 * cc + f32K + f32V,
+        "simple_scan_kernel": qk + 2 * f32K + f32V + hh + f32V,
+        "simple_output_kernel": qk + f32K + cc + f32V + hh + vv,
+        "simple_dh_scan_kernel": 2 * qk + 2 * f32K + cc + vv + hh + f32V,
+        "simple_bwd_intra_kernel": 3 * qk - qk + vv + vv + b + f32K + 2 * cc + 2 * hh + 2 * f32V
+        + vv + b + g + 2 * f32K + 2 * f32K,
+        "group_reduce_kernel": 2 * f32K + 2 * qk,
+    }
+    return table.get(name)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sust=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+# --------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+# --------------------------------------------------------------------------
+class Runner:
+    """Preallocated device buffers and the two C-ABI calls of one step."""
+
+    def __init__(self, cfg, device):
+        self.lib = _lib.load()
+        self.cfg = cfg
+        self.dev = device
+        d = cfg.to(device)
+        self.d = d
+        self.s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+        s = self.s
+        self.o = torch.empty_like(d.v)
+        self.hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=device)
+                   if cfg.output_final_state else None)
+        self.dq, self.dk, self.dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
+        self.dg, self.db = torch.empty_like(d.g), torch.empty_like(d.beta)
+        self.dh0 = torch.empty_like(d.h0) if d.h0 is not None else None
+        need = max(self.lib.kda_chunk_fwd_workspace_size(ctypes.byref(s)),
+                   self.lib.kda_chunk_bwd_workspace_size(ctypes.byref(s)))
+        self.ws = torch.empty(need + 256, dtype=torch.uint8, device=device)
+        p = self.ws.data_ptr()
+        self.wp = ctypes.c_void_p((p + 255) & ~255)
+        self.wb = need
+        self.stream = torch.cuda.current_stream(device)
+        self.sp = ctypes.c_void_p(self.stream.cuda_stream)
+
+    @staticmethod
+    def _p(t):
+        return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+    def step(self):
+        p, lib, s = self._p, self.lib, self.s
+        _lib.check(lib, lib.kda_chunk_fwd(ctypes.byref(s), p(self.o), p(self.hT), self.wp, self.wb, self.sp))
+        _lib.check(lib, lib.kda_chunk_bwd(ctypes.byref(s), p(self.d.do), p(self.d.dhT), p(self.dq), p(self.dk),
+                                          p(self.dv), p(self.dg), p(self.db), p(self.dh0), self.wp, self.wb,
+                                          self.sp))
+
+
+def timed(fn, steps, stream):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def e2e_measure(cfg, runner, steps):
+    """Same step through the public API with HOST buffers: pinned host inputs
+    copied in and every output copied out inside the timed region."""
+    d = runner.d
+    host_in = {k: getattr(cfg, k).pin_memory() for k in ("q", "k", "v", "g", "beta", "do")
+               if getattr(cfg, k) is not None}
+    for k in ("h0", "dhT"):
+        if getattr(cfg, k) is not None:
+            host_in[k] = getattr(cfg, k).pin_memory()
+    outs = [runner.o, runner.dq, runner.dk, runner.dv, runner.dg, runner.db] + \
+        [t for t in (runner.hT, runner.dh0) if t is not None]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        for k, t in host_in.items():
+            getattr(d, k).copy_(t, non_blocking=True)
+        runner.step()
+        for dst, src in zip(host_out, outs):
+            dst.copy_(src, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    ms = timed(one, steps, runner.stream)
+    return ms / steps, h2d, d2h
+
+
+def kernel_split(runner, steps):
+    """Per-kernel device time (CUDA events on the launching stream)."""
+    lib = runner.lib
+    _lib.timing_collect(lib)
+    lib.kda_timing_enable(1)
+    for _ in range(steps):
+        runner.step()
+    torch.cuda.synchronize()
+    lib.kda_timing_enable(0)
+    return _lib.timing_collect(lib)
+
+
+def oracle_sample(cfg, units):
+    """fp64 slices of batch row 0 holding ``units`` value heads (rounded up to
+    whole q/k head groups), for the oracle."""
+    r = cfg.HV // cfg.H
+    hs = list(range((min(units, cfg.HV) + r - 1) // r))
+    js = list(range(hs[0] * r, (hs[-1] + 1) * r))
+    off = cfg.offsets()
+    a, b = int(off[0]), int(off[1])
+    sl = {}
+    for k in ("q", "k", "v", "g", "beta", "do"):
+        x = getattr(cfg, k)
+        y = x.reshape(cfg.B * cfg.T, *x.shape[2:])[a:b]
+        y = y[:, hs] if k in ("q", "k") else y[:, js]
+        sl[k] = np.ascontiguousarray(y.to(torch.float64).numpy()[None])
+    return sl, len(js), b - a
+
+
+def run_oracle(sl, cores):
+    import oracle
+    oracle.kda_fwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], None, None, False, nthreads=cores)
+    oracle.kda_bwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], None, sl["do"], None, nthreads=cores)
+
+
+def cpu_baseline(cfg):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample:
+    whole (sequence, value head) units of the same workload, fwd + bwd."""
+    cores = os.cpu_count() or 1
+    sl, nj, L = oracle_sample(cfg, 2 * cores)
+    t0 = time.perf_counter()
+    run_oracle(sl, cores)
+    dt = time.perf_counter() - t0
+    value = L * nj / cfg.HV / dt  # a layer token needs all HV value heads
+    return dict(value=round(value, 2), unit="tokens/s", cores=cores, kind="oracle",
+                sample=f"batch row 0, {nj} of {cfg.HV} value heads x {L} tokens, fwd+bwd in fp64 "
+                       f"({dt:.1f} s); tokens/s = tokens x heads / HV / seconds")
+
+
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=WORKLOAD_CFG)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return reference_arm(args, warmup)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
+    runner = Runner(cfg, dev)
+    for _ in range(warmup):
+        runner.step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    n0 = runner.lib.kda_launch_count()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms = timed(runner.step, args.steps, runner.stream)
+    if dist:
+        dist.barrier()
+    launches = runner.lib.kda_launch_count() - n0
+    ck = clocks.stop() if rank == 0 else None
+    t = torch.tensor([ms], device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+
+    split = kernel_split(runner, max(3, min(args.steps, 10)))
+    e2e = None if args.no_e2e else e2e_measure(cfg, runner, max(3, min(args.steps, 10)))
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    peaks = load_peaks()
+    ms_step = ms / args.steps
+    toks = cfg.valid_tokens
+    value = toks * world / (ms_step / 1e3)
+    ab = algorithmic_bytes(cfg)
+    af = algorithmic_flops(cfg)
+    t_hbm = ab["total"] / (peaks["hbm"] * 1e9)
+    t_tc = af / (peaks["bf16_sust"] * 1e12 if peaks.get("bf16_sust") else peaks["bf16"] * 1e12)
+    roof_s = max(t_hbm, t_tc)
+
+    # dominant kernel
+    steps_split = max(3, min(args.steps, 10))
+    per_step = {k: v[0] / steps_split for k, v in split.items()}
+    dom = max(split, key=lambda k: split[k][0])
+    dom_ms, dom_n = split[dom]
+    bpt = kernel_bytes_per_token(dom, cfg)
+    achieved = (bpt * toks / (dom_ms / dom_n / 1e3) / 1e9) if bpt else None
+    roof = dict(kernel=dom, bound="hbm", achieved=None if achieved is None else round(achieved, 1),
+                peak=peaks["hbm"], unit="GB/s",
+                frac=None if achieved is None else round(achieved / peaks["hbm"], 4),
+                traffic=None, launch_ms=round(dom_ms / dom_n, 4),
+                peak_source=f"{peaks['src']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["src"] == "measured"
+                else "fallback 6.8 TB/s")
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "H": cfg.H, "HV": cfg.HV, "K": cfg.K,
+                   "V": cfg.V, "global_batch": cfg.B * world, "seq_len": cfg.T,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"inputs {ab['fwd'] / 1e9:.2f} GB read per step > L2 (no flush)"},
+        "roofline": roof,
+        "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                          "algorithmic_bytes": ab["total"], "algorithmic_flops": af,
+                          "roofline_ms": round(roof_s * 1e3, 4),
+                          "achieved_GBps": round(ab["total"] / (ms_step / 1e3) / 1e9, 1),
+                          "frac": round(roof_s / (ms_step / 1e3), 4),
+                          "peaks": {"hbm_gbs": peaks["hbm"], "bf16_tflops": peaks["bf16"],
+                                    "source": peaks["src"]}},
+        "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(per_step.items(), key=lambda x: -x[1])},
+        "gpu_launches": int(launches),
+        "clocks": ck,
+    }
+    if e2e is not None:
+        e_ms, h2d, d2h = e2e
+        out["e2e"] = {"value": round(toks / (e_ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(e_ms, 3),
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def reference_arm(args, warmup):
+    """The oracle, as it stands, on the host cores: each step is a bounded
+    sample of the workload (batch row 0, a few value heads, fwd+bwd)."""
+    cfg = inputs.make_config(args.config)
+    cores = os.cpu_count() or 1
+    sl, nj, L = oracle_sample(cfg, max(2, cores // 4))
+    for _ in range(warmup):
+        run_oracle(sl, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle(sl, cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = L * nj / cfg.HV / dt
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+           "n_gpus": 0, "steps": args.steps, "warmup": warmup, "ms_per_step": round(dt * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "H": cfg.H, "HV": cfg.HV,
+                      "K": cfg.K, "V": cfg.V, "parallelism": "host threads"},
+           "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": f"per step: batch row 0, {nj} of {cfg.HV} value heads x {L} tokens, "
+                                      f"fwd+bwd fp64; tokens/s = tokens x heads / HV / seconds"},
+           "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,202 @@
+// C ABI of libkda: argument validation, workspace layout and dispatch.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+thread_local char g_err[512] = "";
+
+kda_status fail(kda_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+kda_status cuda_fail(cudaError_t e, const char *where) {
+  return fail(KDA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Checks every host-visible property of the problem and fills P.
+kda_status validate(const kda_inputs *in, Problem &P) {
+  if (in == nullptr) return fail(KDA_ERR_INVALID_ARG, "inputs is NULL");
+  if (in->B < 1 || in->T < 0 || in->H < 1 || in->HV < 1 || in->K < 1 || in->V < 1)
+    return fail(KDA_ERR_INVALID_ARG, "sizes must be positive (B=%d T=%d H=%d HV=%d K=%d V=%d)",
+                in->B, in->T, in->H, in->HV, in->K, in->V);
+  if (in->HV % in->H != 0)
+    return fail(KDA_ERR_INVALID_ARG, "HV (%d) must be a multiple of H (%d)", in->HV, in->H);
+  if (in->K > kMaxDim || in->V > kMaxDim)
+    return fail(KDA_ERR_UNSUPPORTED, "K=%d V=%d: head dims above %d are not implemented", in->K,
+                in->V, kMaxDim);
+  if (in->HV > 65535) return fail(KDA_ERR_UNSUPPORTED, "HV=%d above 65535", in->HV);
+  if (in->dtype != KDA_F32 && in->dtype != KDA_BF16)
+    return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)in->dtype);
+  const int64_t Ttot = (int64_t)in->B * in->T;
+  if (Ttot * (in->HV > in->H ? in->HV : in->H) * kMaxDim >= ((int64_t)1 << 46))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  if (in->cu_seqlens != nullptr) {
+    if (in->B != 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens requires B == 1 (B=%d)", in->B);
+    if (in->N < 0) return fail(KDA_ERR_INVALID_ARG, "N=%d must be >= 0", in->N);
+  } else if (in->N != in->B) {
+    return fail(KDA_ERR_INVALID_ARG, "dense batch: N (%d) must equal B (%d)", in->N, in->B);
+  }
+  if (in->N > (1 << 24)) return fail(KDA_ERR_UNSUPPORTED, "N=%d too large", in->N);
+  if (Ttot > 0 && (in->q == nullptr || in->k == nullptr || in->v == nullptr ||
+                   in->g == nullptr || in->beta == nullptr))
+    return fail(KDA_ERR_INVALID_ARG, "q, k, v, g and beta are required");
+  P.B = in->B;
+  P.T = in->T;
+  P.H = in->H;
+  P.HV = in->HV;
+  P.K = in->K;
+  P.V = in->V;
+  P.N = in->N;
+  P.Ttot = Ttot;
+  const int64_t per = ((int64_t)in->T + kChunk - 1) / kChunk;
+  const int64_t nc = in->cu_seqlens != nullptr ? per + in->N : per * in->B;
+  if (nc >= (1 << 30)) return fail(KDA_ERR_UNSUPPORTED, "too many chunks");
+  P.NC = (int)nc;
+  P.bf16 = in->dtype == KDA_BF16;
+  P.q = in->q;
+  P.k = in->k;
+  P.v = in->v;
+  P.g = in->g;
+  P.beta = in->beta;
+  P.h0 = in->h0;
+  P.cu = in->cu_seqlens;
+  return KDA_OK;
+}
+
+// Workspace regions, in order.  Returns the total size; with base != NULL
+// also fills W.
+size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
+  const size_t slots = (size_t)P.NC * P.HV;
+  const size_t K = P.K, V = P.V, C = kChunk;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return base ? (void *)(base + at) : nullptr;
+  };
+  Workspace w;
+  memset(&w, 0, sizeof(w));
+  w.seq = (int4 *)take(sizeof(int4) * (size_t)(P.N > 0 ? P.N : 1));
+  w.chunk = (int4 *)take(sizeof(int4) * (size_t)(P.NC > 0 ? P.NC : 1));
+  w.flags = (int *)take(sizeof(int) * 4);
+  w.G = (float *)take(sizeof(float) * slots * C * K);
+  w.Aqk = (float *)take(sizeof(float) * slots * C * C);
+  w.A = (float *)take(sizeof(float) * slots * C * C);
+  w.w = (float *)take(sizeof(float) * slots * C * K);
+  w.u = (float *)take(sizeof(float) * slots * C * V);
+  w.h = (float *)take(sizeof(float) * slots * K * V);
+  w.delta = (float *)take(sizeof(float) * slots * C * V);
+  if (backward) {
+    w.dh = (float *)take(sizeof(float) * slots * K * V);
+    w.ddelta = (float *)take(sizeof(float) * slots * C * V);
+    w.dqp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
+    w.dkp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
+    w.dw = (float *)take(sizeof(float) * slots * C * K);
+  }
+  if (W) *W = w;
+  return off;
+}
+
+kda_status check_ws(size_t need, void *ws, size_t bytes) {
+  if (need == 0) return KDA_OK;
+  if (ws == nullptr) return fail(KDA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+  if (bytes < need)
+    return fail(KDA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", bytes, need);
+  if (((uintptr_t)ws & 255) != 0) return fail(KDA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+  return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+size_t kda_chunk_fwd_workspace_size(const kda_inputs *in) {
+  Problem P{};
+  if (validate(in, P) != KDA_OK) return 0;
+  return layout(P, false, nullptr, nullptr);
+}
+
+size_t kda_chunk_bwd_workspace_size(const kda_inputs *in) {
+  Problem P{};
+  if (validate(in, P) != KDA_OK) return 0;
+  return layout(P, true, nullptr, nullptr);
+}
+
+kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  g_err[0] = 0;
+  Problem P{};
+  kda_status st = validate(in, P);
+  if (st != KDA_OK) return st;
+  if (P.Ttot > 0 && o == nullptr) return fail(KDA_ERR_INVALID_ARG, "o is NULL");
+  const size_t need = layout(P, false, nullptr, nullptr);
+  if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
+  if (P.N == 0) return KDA_OK;
+  Workspace W;
+  layout(P, false, (char *)workspace, &W);
+  cudaError_t e = simple_forward(P, W, o, hT, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd");
+  return KDA_OK;
+}
+
+kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT, void *dq,
+                         void *dk, void *dv, float *dg, float *dbeta, float *dh0,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+  g_err[0] = 0;
+  Problem P{};
+  kda_status st = validate(in, P);
+  if (st != KDA_OK) return st;
+  if (P.Ttot > 0 && (dO == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+                     dg == nullptr || dbeta == nullptr))
+    return fail(KDA_ERR_INVALID_ARG, "dO, dq, dk, dv, dg and dbeta are required");
+  const size_t need = layout(P, true, nullptr, nullptr);
+  if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
+  if (P.N == 0) return KDA_OK;
+  Workspace W;
+  layout(P, true, (char *)workspace, &W);
+  cudaError_t e = simple_backward(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_bwd");
+  return KDA_OK;
+}
+
+kda_status kda_recurrent_fwd(const kda_inputs *in, void *o, float *hT, void *stream) {
+  g_err[0] = 0;
+  Problem P{};
+  kda_status st = validate(in, P);
+  if (st != KDA_OK) return st;
+  if (P.Ttot > 0 && o == nullptr) return fail(KDA_ERR_INVALID_ARG, "o is NULL");
+  cudaError_t e = launch_recurrent(P, o, hT, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_recurrent_fwd");
+  return KDA_OK;
+}
+
+const char *kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported problem";
+    case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KDA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char *kda_last_error(void) { return g_err; }
+
+int kda_version(void) { return 100; }
+
+}  // extern "C"

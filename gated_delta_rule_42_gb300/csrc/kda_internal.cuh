@@ -1,0 +1,81 @@
+// Internal definitions shared by the CUDA translation units of libkda.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kChunk = 64;    // tokens per chunk
+constexpr int kMaxDim = 128;  // largest K and V the kernels are built for
+
+// A chunk-table entry: the chunk's logical sequence n (-1 = unused slot), its
+// first packed token, its length (1..64) and its index inside the sequence.
+// A sequence entry: first packed token, length, first chunk, number of chunks.
+struct Problem {
+  int B, T, H, HV, K, V, N;
+  int64_t Ttot;  // rows of the packed token axis (B*T)
+  int NC;        // chunk-table capacity, an upper bound on the number of chunks
+  bool bf16;
+  const void *q, *k, *v;
+  const float *g, *beta, *h0;
+  const int32_t *cu;
+};
+
+// Device workspace, carved from the caller's buffer.  Per-(chunk, value head)
+// slots are indexed slot = chunk * HV + j.
+struct Workspace {
+  int4 *seq;     // [N]
+  int4 *chunk;   // [NC]
+  int *flags;    // [0] = number of chunks, [1] = malformed-offsets flag
+  float *G;      // [slot][64][K]   chunk-local inclusive gate cumsum
+  float *Aqk;    // [slot][64][64]  lower (incl. diagonal) decayed q~ k^T
+  float *A;      // [slot][64][64]  (I + L)^-1
+  float *w;      // [slot][64][K]
+  float *u;      // [slot][64][V]
+  float *h;      // [slot][K][V]    state at chunk start
+  float *delta;  // [slot][64][V]   u - w h
+  // backward only
+  float *dh;     // [slot][K][V]    gradient of the chunk-end state
+  float *ddelta; // [slot][64][V]
+  float *dqp;    // [Ttot][HV][K]   per-value-head dq~ partials
+  float *dkp;    // [Ttot][HV][K]
+  float *dw;     // [slot][64][K]
+};
+
+// --- element access -------------------------------------------------------
+__device__ __forceinline__ float ldf(const float *p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16 *p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void stf(float *p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void stf(__nv_bfloat16 *p, int64_t i, float x) {
+  p[i] = __float2bfloat16_rn(x);
+}
+
+// --- launch instrumentation (instrument.cu) -----------------------------------
+void inst_begin(const char *name, cudaStream_t s);
+void inst_end(cudaStream_t s);
+// Wraps one kernel launch: counts it and, when timing is on, brackets it with events.
+#define KDA_LAUNCH(name, stream, ...)  \
+  do {                                 \
+    ::kda::inst_begin(name, stream);   \
+    __VA_ARGS__;                       \
+    ::kda::inst_end(stream);           \
+  } while (0)
+
+// --- host-side launchers (defined in the .cu files) ---------------------------
+cudaError_t launch_chunk_map(const Problem &P, const Workspace &W, cudaStream_t s);
+// map + intra + scan: fills G, Aqk, A, w, u, h, delta; writes hT if not NULL
+cudaError_t simple_prepare(const Problem &P, const Workspace &W, float *hT, cudaStream_t s);
+cudaError_t simple_forward(const Problem &P, const Workspace &W, void *o, float *hT,
+                           cudaStream_t s);
+cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO,
+                            const float *dhT, void *dq, void *dk, void *dv, float *dg,
+                            float *dbeta, float *dh0, cudaStream_t s);
+cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,164 @@
+"""PyTorch-facing entry points: ``chunk_kda`` (autograd) and ``recurrent_kda``.
+
+The signatures follow the KDA contract of "kda in torchtitan (training)"
+(pytorch/torchtitan PR #4164, agent note on ``recurrent_kda``):
+``(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
+output_final_state=False) -> (output, final_state)`` where ``gate`` is the
+per-token log2 decay, queries are scaled by 1/sqrt(K) internally,
+``cu_seqlens`` is a device int32 offset array (repeated offsets are empty
+slots) and states are fp32 with one entry per logical sequence.
+
+PyTorch provides device memory and the current stream; every step of the
+computation runs in libkda's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+__all__ = ["chunk_kda", "recurrent_kda", "chunk_kda_fwd", "chunk_kda_bwd", "make_inputs_struct"]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tensor(name, t, dtype, device, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None):
+    """Validate the tensors and build the C ``kda_inputs`` struct."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("KDA kernels run on CUDA tensors only")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _check_tensor("q", q, q.dtype, dev)
+    _check_tensor("k", k, q.dtype, dev, (B, T, H, K))
+    _check_tensor("v", v, q.dtype, dev, (B, T, HV, V))
+    _check_tensor("g", g, torch.float32, dev, (B, T, HV, K))
+    _check_tensor("beta", beta, torch.float32, dev, (B, T, HV))
+    if cu_seqlens is not None:
+        _check_tensor("cu_seqlens", cu_seqlens, torch.int32, dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if initial_state is not None:
+        _check_tensor("initial_state", initial_state, torch.float32, dev, (N, HV, K, V))
+    s = _lib.KdaInputs()
+    s.B, s.T, s.H, s.HV, s.K, s.V, s.N = B, T, H, HV, K, V, N
+    s.dtype = _lib.KDA_BF16 if q.dtype == torch.bfloat16 else _lib.KDA_F32
+    s.q, s.k, s.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    s.g, s.beta = g.data_ptr(), beta.data_ptr()
+    s.h0 = None if initial_state is None else initial_state.data_ptr()
+    s.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
+    return s
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    ws = torch.empty(max(nbytes, 256) + 256, dtype=torch.uint8, device=device)
+    return ws
+
+
+def _aligned(ws: torch.Tensor):
+    p = ws.data_ptr()
+    return ctypes.c_void_p((p + 255) & ~255), ws.numel() - (((p + 255) & ~255) - p)
+
+
+def chunk_kda_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_final_state=False,
+                  workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    lib = _lib.load()
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens)
+    o = torch.empty_like(v)
+    hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
+          if output_final_state else None)
+    need = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s))
+    if workspace is None or workspace.numel() < need + 256:
+        workspace = _workspace(need, q.device)
+    wp, wb = _aligned(workspace)
+    _lib.check(lib, lib.kda_chunk_fwd(ctypes.byref(s), _ptr(o), _ptr(hT), wp, wb, _stream(q.device)))
+    return o, hT
+
+
+def chunk_kda_bwd(q, k, v, g, beta, initial_state, cu_seqlens, do, dht,
+                  workspace: Optional[torch.Tensor] = None, need_dh0: bool = True):
+    lib = _lib.load()
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens)
+    _check_tensor("do", do, q.dtype, q.device, tuple(v.shape))
+    if dht is not None:
+        _check_tensor("dht", dht, torch.float32, q.device, (s.N, s.HV, s.K, s.V))
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dg = torch.empty_like(g)
+    db = torch.empty_like(beta)
+    dh0 = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
+           if need_dh0 else None)
+    need = lib.kda_chunk_bwd_workspace_size(ctypes.byref(s))
+    if workspace is None or workspace.numel() < need + 256:
+        workspace = _workspace(need, q.device)
+    wp, wb = _aligned(workspace)
+    _lib.check(lib, lib.kda_chunk_bwd(ctypes.byref(s), _ptr(do), _ptr(dht), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), wp, wb,
+                                      _stream(q.device)))
+    return dq, dk, dv, dg, db, dh0
+
+
+class ChunkKDAFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, output_final_state):
+        o, hT = chunk_kda_fwd(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+        ctx.has_h0 = initial_state is not None
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        q, k, v, g, beta, h0, cu = ctx.saved_tensors
+        do = do.contiguous()
+        dht = None if dht is None else dht.contiguous()
+        dq, dk, dv, dg, db, dh0 = chunk_kda_bwd(q, k, v, g, beta, h0, cu, do, dht,
+                                                need_dh0=ctx.has_h0)
+        return dq, dk, dv, dg, db, dh0, None, None
+
+
+def chunk_kda(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, output_final_state=False):
+    """Chunked KDA forward (with autograd).  Returns (o, final_state or None)."""
+    return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state)
+
+
+def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
+                  output_final_state=False):
+    """Token-by-token KDA forward for inference (fp32 arithmetic).  Rejects
+    inputs that require grad: train through :func:`chunk_kda`."""
+    if any(t is not None and t.requires_grad for t in (q, k, v, gate, beta, initial_state)):
+        raise RuntimeError("recurrent_kda is inference-only; use chunk_kda for training")
+    lib = _lib.load()
+    s = make_inputs_struct(q, k, v, gate, beta, initial_state, cu_seqlens)
+    o = torch.empty_like(v)
+    hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
+          if output_final_state else None)
+    _lib.check(lib, lib.kda_recurrent_fwd(ctypes.byref(s), _ptr(o), _ptr(hT), _stream(q.device)))
+    return o, hT

@@ -1,0 +1,149 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) chunked KDA library (libkda.so).
+ *
+ * KDA (Kimi Delta Attention) is a gated delta-rule recurrence with a
+ * per-channel decay.  For every logical sequence n and value head j an fp32
+ * state S[K][V] evolves token by token:
+ *     S <- diag(2^g_t) S                       (g_t: per-token, per-channel log2 decay)
+ *     S <- S + beta_t k_t (v_t - S^T k_t)^T    (delta-rule write, prediction from the decayed state)
+ *     o_t = S^T (q_t / sqrt(K))                (read-out from the updated state)
+ * The chunked entry points evaluate this exactly (up to rounding) in chunks of
+ * 64 tokens: a chunk-local gate cumsum, the strictly-lower decayed beta*K*K^T
+ * block L and its unit-lower inverse A = (I+L)^-1, w = A(beta k 2^G),
+ * u = A(beta v), an inter-chunk state scan and the output o = (q 2^G) h + Aqk(u - w h).
+ * This is the sub-kernel decomposition of the FLA KDA/GDN pipeline
+ * (chunk_scaled_dot_kkt / solve_tril / recompute_w_u / fwd_h / fwd_o, and
+ * bwd_dhu / bwd_dqkwg / bwd_dv_local / wy_bwd for the backward) named in
+ * "[Fix] Use unit KDA gate scale when A_log is omitted"
+ * (fla-org/flash-linear-attention PR #1294, commit log, GDN per-kernel tests).
+ *
+ * Argument contract (mirrors the recurrent_kda / chunk_kda contract in
+ * "kda in torchtitan (training)", pytorch/torchtitan PR #4164, agent note):
+ *   - the gate g is the PER-TOKEN log2 decay (the library does the chunk cumsum);
+ *   - queries are scaled by 1/sqrt(K) internally;
+ *   - cu_seqlens is a DEVICE int32 array of N+1 non-decreasing offsets with
+ *     cu_seqlens[0] == 0 and cu_seqlens[N] <= T; repeated offsets are empty
+ *     slots whose state passes through bitwise (hT[n] = h0[n], dh0[n] = dhT[n]);
+ *     tokens at or after cu_seqlens[N] are outside the contract: never read for
+ *     a result and never written;
+ *   - states are fp32 with one leading entry per logical sequence.
+ *
+ * Layouts (row-major, all DEVICE pointers):
+ *   q, k, dq, dk   [B][T][H][K]      dtype
+ *   v, o, dO, dv   [B][T][HV][V]     dtype
+ *   g, dg          [B][T][HV][K]     fp32
+ *   beta, dbeta    [B][T][HV]        fp32
+ *   h0,hT,dhT,dh0  [N][HV][K][V]     fp32
+ * Value head j reads query/key head j / (HV/H) (contiguous groups).
+ * dq and dk are summed over the HV/H value heads that share a q/k head.
+ *
+ * Ownership: the caller allocates every input, output and workspace buffer;
+ * the library never allocates or frees device memory, never synchronises and
+ * never reads device data on the host.  Work is enqueued on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream).  The backward recomputes
+ * everything it needs from the inputs: no forward context is saved.
+ *
+ * Errors: arguments the host can check are validated before anything is
+ * enqueued and reported synchronously (KDA_ERR_INVALID_ARG,
+ * KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE); nothing is launched in that case.
+ * A failed launch returns KDA_ERR_CUDA.  kda_last_error() returns a message
+ * for the last failure on the calling thread.  The values inside cu_seqlens
+ * live on the device and are a precondition: they are not checked.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null required pointer, bad sizes, HV % H != 0, ... */
+  KDA_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement     */
+  KDA_ERR_WORKSPACE = 3,   /* workspace pointer NULL or smaller than required  */
+  KDA_ERR_CUDA = 4         /* a CUDA launch or API call failed                 */
+} kda_status;
+
+typedef enum kda_dtype {
+  KDA_F32 = 0,  /* q, k, v (and o, dO, dq, dk, dv) in fp32: fp32 arithmetic throughout */
+  KDA_BF16 = 1  /* q, k, v (and o, dO, dq, dk, dv) in bf16: fp32 accumulation          */
+} kda_dtype;
+
+/* Problem description shared by every entry point. */
+typedef struct kda_inputs {
+  int B, T;         /* batch and (padded) tokens per batch row; B must be 1 with cu_seqlens */
+  int H, HV;        /* query/key heads and value heads; HV must be a multiple of H          */
+  int K, V;         /* key and value head dims: 1..128 each (bf16 fast path: K = V = 128)    */
+  int N;            /* logical sequences: B when cu_seqlens is NULL, else len(cu_seqlens)-1   */
+  kda_dtype dtype;  /* element type of q, k, v, o, dO, dq, dk, dv                            */
+  const void *q, *k, *v;
+  const float *g;           /* per-token log2 decay (typically <= 0)                         */
+  const float *beta;        /* per (token, value head) write strength                        */
+  const float *h0;          /* initial states [N][HV][K][V], or NULL for zeros               */
+  const int32_t *cu_seqlens;/* device [N+1] packed offsets, or NULL for a dense batch         */
+} kda_inputs;
+
+/* Bytes of device workspace kda_chunk_fwd needs for this problem (256-byte
+ * aligned base required).  Returns 0 if the problem is invalid. */
+size_t kda_chunk_fwd_workspace_size(const kda_inputs *in);
+
+/* Chunked forward.  Writes o [B][T][HV][V] (dtype) for every valid token and,
+ * if hT is not NULL, the final states hT [N][HV][K][V] (fp32).
+ * workspace: device scratch of at least kda_chunk_fwd_workspace_size() bytes;
+ * its contents on entry do not matter and are clobbered. */
+kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace kda_chunk_bwd needs. */
+size_t kda_chunk_bwd_workspace_size(const kda_inputs *in);
+
+/* Chunked backward with state recompute.  Given dO [B][T][HV][V] (dtype) and the
+ * final-state gradient dhT [N][HV][K][V] (fp32, NULL = zero), writes
+ * dq, dk [B][T][H][K] (dtype), dv [B][T][HV][V] (dtype), dg [B][T][HV][K] (fp32,
+ * gradient w.r.t. the log2 gate), dbeta [B][T][HV] (fp32) for every valid token
+ * and, if dh0 is not NULL, dh0 [N][HV][K][V] (fp32). */
+kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT, void *dq,
+                         void *dk, void *dv, float *dg, float *dbeta, float *dh0,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Token-by-token recurrent forward (inference): one sequential pass per
+ * (sequence, value head), fp32 state and fp32 arithmetic whatever the dtype,
+ * no workspace.  Same arguments and results as kda_chunk_fwd, as in the
+ * recurrent_kda entry point of "kda in torchtitan (training)". */
+kda_status kda_recurrent_fwd(const kda_inputs *in, void *o, float *hT, void *stream);
+
+/* Static description of a status code. */
+const char *kda_status_string(kda_status s);
+
+/* Message describing the last failure on the calling thread ("" if none). */
+const char *kda_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int kda_version(void);
+
+/* ---- instrumentation (benchmarks and profiling; no counterpart on the pages) ----
+ * Every kernel the library launches is counted.  While timing is enabled, a
+ * CUDA event pair is recorded on the launching stream around each launch. */
+
+/* Kernels launched by this library in this process so far. */
+unsigned long long kda_launch_count(void);
+
+/* Turns per-launch event timing on (1) or off (0); returns the previous state. */
+int kda_timing_enable(int on);
+
+/* Waits for every recorded event pair, sums the elapsed times per kernel name and
+ * clears the records.  Fills up to max_kernels entries: names (each name_stride
+ * bytes, NUL-terminated), total milliseconds and launch counts.  Returns the
+ * number of distinct kernels seen (may exceed max_kernels). */
+int kda_timing_collect(int max_kernels, char *names, size_t name_stride, double *total_ms,
+                       int *launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

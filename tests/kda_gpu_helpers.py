@@ -1,0 +1,181 @@
+"""Helpers for the GPU parity tests: call libkda through its C ABI with
+NaN-poisoned outputs and workspace, run the oracle on the same inputs (whole
+problem, or sampled (sequence, q/k head) units of a large one), compare."""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+import oracle
+from gated_delta_rule_42_gb300 import _lib
+from gated_delta_rule_42_gb300.ops import make_inputs_struct
+
+# tolerances (relative RMS): fp32 inputs 1e-5 everywhere; bf16 inputs 5e-3 on
+# o / final state, 1e-2 on every gradient
+TOL = {torch.float32: dict(fwd=1e-5, bwd=1e-5), torch.bfloat16: dict(fwd=5e-3, bwd=1e-2)}
+
+
+def _nan_like(shape, dtype, dev):
+    return torch.full(shape, float("nan"), dtype=dtype, device=dev)
+
+
+def _poisoned_ws(nbytes, dev):
+    ws = torch.full((nbytes + 512,), 255, dtype=torch.uint8, device=dev)
+    p = ws.data_ptr()
+    a = (p + 255) & ~255
+    return ws, ctypes.c_void_p(a), nbytes + 512 - (a - p)
+
+
+def gpu_fwd(inp, dev="cuda", lib=None):
+    """kda_chunk_fwd on the inputs (moved to dev); returns CPU o, hT."""
+    lib = lib or _lib.load()
+    d = inp.to(dev)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+    o = _nan_like(d.v.shape, d.dtype, dev)
+    hT = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if inp.output_final_state else None
+    need = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s))
+    ws, wp, wb = _poisoned_ws(need, dev)
+    st = lib.kda_chunk_fwd(ctypes.byref(s), ctypes.c_void_p(o.data_ptr()),
+                           None if hT is None else ctypes.c_void_p(hT.data_ptr()), wp, wb,
+                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    _lib.check(lib, st)
+    torch.cuda.synchronize()
+    return o.cpu(), (None if hT is None else hT.cpu())
+
+
+def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True):
+    lib = lib or _lib.load()
+    d = inp.to(dev)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+    out = dict(dq=_nan_like(d.q.shape, d.dtype, dev), dk=_nan_like(d.k.shape, d.dtype, dev),
+               dv=_nan_like(d.v.shape, d.dtype, dev), dg=_nan_like(d.g.shape, torch.float32, dev),
+               dbeta=_nan_like(d.beta.shape, torch.float32, dev))
+    out["dh0"] = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if want_dh0 else None
+    need = lib.kda_chunk_bwd_workspace_size(ctypes.byref(s))
+    ws, wp, wb = _poisoned_ws(need, dev)
+
+    def p(t):
+        return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+    st = lib.kda_chunk_bwd(ctypes.byref(s), p(d.do), p(d.dhT), p(out["dq"]), p(out["dk"]),
+                           p(out["dv"]), p(out["dg"]), p(out["dbeta"]), p(out["dh0"]), wp, wb,
+                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    _lib.check(lib, st)
+    torch.cuda.synchronize()
+    return {k: (None if v is None else v.cpu()) for k, v in out.items()}
+
+
+def gpu_recurrent(inp, dev="cuda", lib=None):
+    lib = lib or _lib.load()
+    d = inp.to(dev)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+    o = _nan_like(d.v.shape, d.dtype, dev)
+    hT = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if inp.output_final_state else None
+    st = lib.kda_recurrent_fwd(ctypes.byref(s), ctypes.c_void_p(o.data_ptr()),
+                               None if hT is None else ctypes.c_void_p(hT.data_ptr()),
+                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    _lib.check(lib, st)
+    torch.cuda.synchronize()
+    return o.cpu(), (None if hT is None else hT.cpu())
+
+
+def oracle_fwd(inp):
+    f = inp.f64()
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
+    return oracle.kda_fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], cu, True)
+
+
+def oracle_bwd(inp):
+    f = inp.f64()
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
+    return oracle.kda_bwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], f["do"], f["dhT"], cu)
+
+
+def valid_mask(inp):
+    """Boolean [B*T] of tokens inside the contract."""
+    m = np.zeros(inp.B * inp.T, dtype=bool)
+    off = inp.offsets()
+    for n in range(len(off) - 1):
+        m[off[n]:off[n + 1]] = True
+    return m
+
+
+def tok(x, inp):
+    """[B,T,...] -> [B*T,...] as fp64 numpy."""
+    x = x.detach().cpu()
+    if x.dtype != torch.float64:
+        x = x.to(torch.float64)
+    return x.numpy().reshape(inp.B * inp.T, *x.shape[2:])
+
+
+def assert_rel(name, got, ref, tol):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values (unwritten or overflow)"
+    err = oracle.rel_rms(got, ref)
+    assert err <= tol, f"{name}: rel-RMS {err:.3e} > {tol:.1e}"
+    return err
+
+
+def check_fwd(inp, o, hT, ref_o, ref_hT, tol):
+    m = valid_mask(inp)
+    errs = {"o": assert_rel("o", tok(o, inp)[m], ref_o.reshape(inp.B * inp.T, -1, inp.V)[m], tol)}
+    if (~m).any():  # outside the contract: never written
+        assert torch.isnan(o.reshape(inp.B * inp.T, -1)[torch.from_numpy(~m)]).all(), "tail written"
+    if hT is not None:
+        errs["hT"] = assert_rel("hT", hT.numpy(), ref_hT, tol)
+        for n in empty_slots(inp):
+            want = inp.h0[n] if inp.h0 is not None else torch.zeros_like(hT[n])
+            assert torch.equal(hT[n], want), f"empty slot {n} state not passed through bitwise"
+    return errs
+
+
+def check_bwd(inp, gr, ref, tol):
+    m = valid_mask(inp)
+    errs = {}
+    for key in ("dq", "dk", "dv", "dg", "dbeta"):
+        g = tok(gr[key], inp)
+        errs[key] = assert_rel(key, g[m], ref[key].reshape(g.shape)[m], tol)
+        if (~m).any():
+            assert torch.isnan(gr[key].reshape(inp.B * inp.T, -1)[torch.from_numpy(~m)]).all(), \
+                f"{key}: tail written"
+    if gr.get("dh0") is not None:
+        errs["dh0"] = assert_rel("dh0", gr["dh0"].numpy(), ref["dh0"], tol)
+        for n in empty_slots(inp):
+            want = inp.dhT[n] if inp.dhT is not None else torch.zeros_like(gr["dh0"][n])
+            assert torch.equal(gr["dh0"][n], want), f"empty slot {n} dh0 not passed through bitwise"
+    return errs
+
+
+def empty_slots(inp):
+    off = inp.offsets()
+    return [n for n in range(len(off) - 1) if off[n] == off[n + 1]]
+
+
+def sample_units(inp, units):
+    """Oracle on sampled (sequence n, q/k head hq) units of a large problem
+    (all HV/H value heads of the group, so dq and dk are complete).
+    Returns a list of (n, hq, js, t0, t1, (o, hT), bwd dict)."""
+    B, T, H, HV = inp.B, inp.T, inp.H, inp.HV
+    r = HV // H
+    off = inp.offsets()
+
+    def sl(x, t0, t1, cols):
+        if x is None:
+            return None
+        y = x.reshape(B * T, *x.shape[2:])[t0:t1][:, cols]
+        return y.to(torch.float64).numpy()[None]
+
+    out = []
+    for n, hq in units:
+        t0, t1 = int(off[n]), int(off[n + 1])
+        js = list(range(hq * r, (hq + 1) * r))
+        q, k = sl(inp.q, t0, t1, [hq]), sl(inp.k, t0, t1, [hq])
+        v, g, beta, do = (sl(x, t0, t1, js) for x in (inp.v, inp.g, inp.beta, inp.do))
+        h0 = None if inp.h0 is None else inp.h0[n:n + 1][:, js].to(torch.float64).numpy()
+        dhT = None if inp.dhT is None else inp.dhT[n:n + 1][:, js].to(torch.float64).numpy()
+        o, hT = oracle.kda_fwd(q, k, v, g, beta, h0, None, True)
+        gr = oracle.kda_bwd(q, k, v, g, beta, h0, do, dhT)
+        out.append((n, hq, js, t0, t1, (o, hT), gr))
+    return out

@@ -1,0 +1,81 @@
+"""The C-ABI library loads, exports every symbol include/kda.h declares, and
+rejects bad arguments on the host (no GPU is touched: validation happens before
+anything is enqueued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_42_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.kda_version() >= 100
+
+
+def _inputs(**kw):
+    s = _lib.KdaInputs()
+    s.B, s.T, s.H, s.HV, s.K, s.V, s.N, s.dtype = 1, 128, 2, 4, 64, 64, 1, _lib.KDA_BF16
+    for f in ("q", "k", "v", "g", "beta"):
+        setattr(s, f, 0x1000)
+    for key, val in kw.items():
+        setattr(s, key, val)
+    return s
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(HV=3), _lib.KDA_ERR_INVALID_ARG),
+    (dict(K=256), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(V=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(N=2), _lib.KDA_ERR_INVALID_ARG),             # dense: N must equal B
+    (dict(B=2, N=2, cu_seqlens=0x2000), _lib.KDA_ERR_INVALID_ARG),  # packed needs B == 1
+    (dict(q=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dtype=7), _lib.KDA_ERR_INVALID_ARG),
+])
+def test_host_validation(lib, kw, status):
+    s = _inputs(**kw)
+    st = lib.kda_chunk_fwd(ctypes.byref(s), ctypes.c_void_p(0x3000), None, None, 0, None)
+    assert st == status, lib.kda_last_error()
+    assert lib.kda_last_error().decode() != ""
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(s)) == 0
+
+
+def test_workspace_checks(lib):
+    s = _inputs()
+    need_f = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s))
+    need_b = lib.kda_chunk_bwd_workspace_size(ctypes.byref(s))
+    assert 0 < need_f < need_b
+    st = lib.kda_chunk_fwd(ctypes.byref(s), ctypes.c_void_p(0x3000), None, None, need_f, None)
+    assert st == _lib.KDA_ERR_WORKSPACE
+    st = lib.kda_chunk_fwd(ctypes.byref(s), ctypes.c_void_p(0x3000), None, ctypes.c_void_p(0x10000),
+                           need_f - 1, None)
+    assert st == _lib.KDA_ERR_WORKSPACE
+    st = lib.kda_chunk_fwd(ctypes.byref(s), ctypes.c_void_p(0x3000), None, ctypes.c_void_p(0x10010),
+                           need_f, None)
+    assert st == _lib.KDA_ERR_WORKSPACE  # misaligned
+    st = lib.kda_chunk_bwd(ctypes.byref(s), None, None, None, None, None, None, None, None, None, 0, None)
+    assert st == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for st in range(5):
+        assert lib.kda_status_string(st).decode()
