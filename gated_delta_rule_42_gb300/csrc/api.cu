@@ -1,6 +1,7 @@
 // C ABI of libkda: argument validation, workspace layout and dispatch.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "kda_internal.cuh"
@@ -76,6 +77,11 @@ kda_status validate(const kda_inputs *in, Problem &P) {
 
 // Workspace regions, in order.  Returns the total size; with base != NULL
 // also fills W.
+bool use_tc(const Problem &P) {
+  const char *f = getenv("KDA_FORCE_SIMPLE");
+  return tc_eligible(P) && !(f != nullptr && f[0] == '1');
+}
+
 size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   const size_t slots = (size_t)P.NC * P.HV;
   const size_t K = P.K, V = P.V, C = kChunk;
@@ -90,6 +96,10 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   w.seq = (int4 *)take(sizeof(int4) * (size_t)(P.N > 0 ? P.N : 1));
   w.chunk = (int4 *)take(sizeof(int4) * (size_t)(P.NC > 0 ? P.NC : 1));
   w.flags = (int *)take(sizeof(int) * 4);
+  if (!backward && use_tc(P)) {  // the fused forward keeps everything on chip
+    if (W) *W = w;
+    return off;
+  }
   w.G = (float *)take(sizeof(float) * slots * C * K);
   w.Aqk = (float *)take(sizeof(float) * slots * C * C);
   w.A = (float *)take(sizeof(float) * slots * C * C);
@@ -148,7 +158,8 @@ kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspa
   if (P.N == 0) return KDA_OK;
   Workspace W;
   layout(P, false, (char *)workspace, &W);
-  cudaError_t e = simple_forward(P, W, o, hT, (cudaStream_t)stream);
+  cudaError_t e = use_tc(P) ? tc_forward(P, W, o, hT, nullptr, W.flags + 2, (cudaStream_t)stream)
+                            : simple_forward(P, W, o, hT, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd");
   return KDA_OK;
 }

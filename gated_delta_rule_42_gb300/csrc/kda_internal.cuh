@@ -77,5 +77,11 @@ cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO
                             const float *dhT, void *dq, void *dk, void *dv, float *dg,
                             float *dbeta, float *dh0, cudaStream_t s);
 cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t s);
+// bf16, K = V = 128 tensor-core forward; with hstates != NULL writes the
+// chunk-start states (bf16 [chunk][HV][K][V]) instead of the output.
+cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, void *hstates,
+                       int *err, cudaStream_t s);
+// true when the tensor-core kernels handle this problem
+inline bool tc_eligible(const Problem &P) { return P.bf16 && P.K == 128 && P.V == 128; }
 
 }  // namespace kda

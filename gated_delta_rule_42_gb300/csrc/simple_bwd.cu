@@ -29,7 +29,7 @@ size_t dh_smem(int K) {
   return sizeof(float) * (K * kBV + 2 * kChunk * K + 2 * kChunk * kBV + K);
 }
 size_t bwd_intra_smem(int K) {
-  return sizeof(float) * (4 * K * kLDT + 5 * kChunk * kChunk + 2 * kChunk + K);
+  return sizeof(float) * (4 * K * kLDT + 5 * kChunk * kChunk + 2 * kChunk);
 }
 
 template <typename Tin>
@@ -156,7 +156,6 @@ simple_bwd_intra_kernel(Problem P, Workspace W, const Tin *__restrict__ dO, Tin 
   float *sT = sdQK + kChunk * kChunk;   // [64][64] A^T dA
   float *sb = sT + kChunk * kChunk;     // [64]
   float *sdb = sb + kChunk;             // [64]
-  float *sGl = sdb + kChunk;            // [K]
 
   for (int idx = tid; idx < kChunk * K; idx += kThreads) {
     const int r = idx / K, cc = idx - r * K;
@@ -180,9 +179,12 @@ simple_bwd_intra_kernel(Problem P, Workspace W, const Tin *__restrict__ dO, Tin 
     sb[tid] = (tid < len) ? P.beta[(int64_t)(t0 + tid) * HV + j] : 0.f;
     sdb[tid] = 0.f;
   }
-  for (int cc = tid; cc < K; cc += kThreads) sGl[cc] = 0.f;
   __syncthreads();
 
+  // Every reduction below runs in a fixed order (no float atomics), so the
+  // results are bitwise reproducible.
+  const int warp = tid >> 5, lane = tid & 31;
+  float *sc = sdQK;  // [64][K] scratch for P1-P2; aliases sdQK and sT, unused until P3
   // P1: terms through h and dh' (thread per (r, c))
   for (int idx = tid; idx < len * K; idx += kThreads) {
     const int r = idx / K, cc = idx - r * K;
@@ -202,17 +204,19 @@ simple_bwd_intra_kernel(Problem P, Workspace W, const Tin *__restrict__ dO, Tin 
     dka[ei] = dKh * e;
     dga[ei] = kLn2 * (dQg * qg - dKh * kh);
     dws[r * K + cc] = dwv;
-    atomicAdd(&sGl[cc], kLn2 * dKh * kh);
+    sc[r * K + cc] = kLn2 * dKh * kh;
   }
   __syncthreads();
   // P2: the decay of the carried state, d(2^G_last) = rowsum(dh' .* h)
   for (int cc = tid; cc < K; cc += kThreads) {
     float s = 0.f;
     for (int x = 0; x < V; ++x) s = fmaf(dhs[(size_t)cc * V + x], hs[(size_t)cc * V + x], s);
+    float acc = 0.f;
+    for (int r = 0; r < len; ++r) acc += sc[r * K + cc];
     const float Gl = sG[cc * kLDT + len - 1];
-    const float tot = sGl[cc] + kLn2 * exp2f(Gl) * s;
-    dga[((int64_t)(t0 + len - 1) * HV + j) * K + cc] += tot;
+    dga[((int64_t)(t0 + len - 1) * HV + j) * K + cc] += acc + kLn2 * exp2f(Gl) * s;
   }
+  __syncthreads();
   // P3: dA and dAqk (thread per (r, i))
   for (int p = tid; p < kChunk * kChunk; p += kThreads) {
     const int r = p >> 6, i = p & 63;
@@ -229,25 +233,28 @@ simple_bwd_intra_kernel(Problem P, Workspace W, const Tin *__restrict__ dO, Tin 
     sdQK[p] = aq;
   }
   __syncthreads();
-  // P4: d(beta v) = A^T dD -> dv, dbeta
-  for (int idx = tid; idx < len * V; idx += kThreads) {
-    const int r = idx / V, x = idx - r * V;
-    float s = 0.f;
-    for (int i = r; i < len; ++i) s = fmaf(sA[i * kChunk + r], dDs[i * V + x], s);
-    const int64_t e = ((int64_t)(t0 + r) * HV + j) * V + x;
-    stf(dv, e, sb[r] * s);
-    atomicAdd(&sdb[r], s * ldf(v, e));
-  }
-  // P5: d(beta k 2^G) = A^T dw -> dk, dbeta, dG
-  for (int idx = tid; idx < len * K; idx += kThreads) {
-    const int r = idx / K, cc = idx - r * K;
-    float s = 0.f;
-    for (int i = r; i < len; ++i) s = fmaf(sA[i * kChunk + r], dws[i * K + cc], s);
-    const float kd = sKd[cc * kLDT + r];
-    const int64_t ei = ((int64_t)(t0 + r) * HV + j) * K + cc;
-    dka[ei] += sb[r] * exp2f(sG[cc * kLDT + r]) * s;
-    dga[ei] += kLn2 * sb[r] * s * kd;
-    atomicAdd(&sdb[r], s * kd);
+  // P4/P5 (one warp per row r): d(beta v) = A^T dD -> dv, dbeta;
+  // d(beta k 2^G) = A^T dw -> dk, dbeta, dG
+  for (int r = warp; r < len; r += kThreads / 32) {
+    float part = 0.f;
+    for (int x = lane; x < V; x += 32) {
+      float s = 0.f;
+      for (int i = r; i < len; ++i) s = fmaf(sA[i * kChunk + r], dDs[i * V + x], s);
+      const int64_t e = ((int64_t)(t0 + r) * HV + j) * V + x;
+      stf(dv, e, sb[r] * s);
+      part = fmaf(s, ldf(v, e), part);
+    }
+    for (int cc = lane; cc < K; cc += 32) {
+      float s = 0.f;
+      for (int i = r; i < len; ++i) s = fmaf(sA[i * kChunk + r], dws[i * K + cc], s);
+      const float kd = sKd[cc * kLDT + r];
+      const int64_t ei = ((int64_t)(t0 + r) * HV + j) * K + cc;
+      dka[ei] += sb[r] * exp2f(sG[cc * kLDT + r]) * s;
+      dga[ei] += kLn2 * sb[r] * s * kd;
+      part = fmaf(s, kd, part);
+    }
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) sdb[r] += part;
   }
   // P6: T = A^T dA
   for (int p = tid; p < kChunk * kChunk; p += kThreads) {
@@ -266,16 +273,18 @@ simple_bwd_intra_kernel(Problem P, Workspace W, const Tin *__restrict__ dO, Tin 
     sdA[p] = -s;
   }
   __syncthreads();
-  // P7: dbeta from L = beta * KK
-  for (int p = tid; p < kChunk * kChunk; p += kThreads) {
-    const int r = p >> 6, i = p & 63;
-    if (i < r && r < len) {
+  // P7 (one warp per row r): dbeta from L = beta * KK
+  for (int r = warp; r < len; r += kThreads / 32) {
+    float part = 0.f;
+    for (int i = lane; i < r; i += 32) {
       float kk = 0.f;
       for (int cc = 0; cc < K; ++cc)
         kk = fmaf(sk[cc * kLDT + r] * sk[cc * kLDT + i],
                   exp2f(sG[cc * kLDT + r] - sG[cc * kLDT + i]), kk);
-      atomicAdd(&sdb[r], sdA[p] * kk);
+      part = fmaf(sdA[r * kChunk + i], kk, part);
     }
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) sdb[r] += part;
   }
   // P8: row-side pairwise sums (thread per (r, c))
   for (int idx = tid; idx < len * K; idx += kThreads) {

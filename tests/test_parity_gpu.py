@@ -152,3 +152,12 @@ def test_cuda_graph_replay_with_mutated_offsets():
         ref_inp.cu_seqlens = torch.tensor(cu, dtype=torch.int32)
         ro, rhT = H.oracle_fwd(ref_inp)
         H.check_fwd(ref_inp, o.cpu(), hT.cpu(), ro, rhT, H.TOL[torch.bfloat16]["fwd"])
+
+
+def test_backward_is_bitwise_deterministic():
+    inp = inputs.make_inputs(B=1, T=300, H=2, HV=4, K=128, V=128, dtype=torch.bfloat16, seed=9,
+                             cu_seqlens=[0, 130, 130, 300])
+    a = H.gpu_bwd(inp)
+    b = H.gpu_bwd(inp)
+    for key in a:
+        assert torch.equal(a[key], b[key]), key
