@@ -180,12 +180,19 @@ class Runner:
     def _p(t):
         return None if t is None else ctypes.c_void_p(t.data_ptr())
 
-    def step(self):
+    def fwd(self):
         p, lib, s = self._p, self.lib, self.s
         _lib.check(lib, lib.kda_chunk_fwd(ctypes.byref(s), p(self.o), p(self.hT), self.wp, self.wb, self.sp))
+
+    def bwd(self):
+        p, lib, s = self._p, self.lib, self.s
         _lib.check(lib, lib.kda_chunk_bwd(ctypes.byref(s), p(self.d.do), p(self.d.dhT), p(self.dq), p(self.dk),
                                           p(self.dv), p(self.dg), p(self.db), p(self.dh0), self.wp, self.wb,
                                           self.sp))
+
+    def step(self):
+        self.fwd()
+        self.bwd()
 
 
 def timed(fn, steps, stream):
@@ -286,6 +293,8 @@ def main():
     ap.add_argument("--config", type=int, default=WORKLOAD_CFG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["step", "fwd", "bwd"], default="step",
+                    help="time only the forward or only the backward call (profiling aid)")
     args = ap.parse_args()
     warmup = max(args.warmup, 3)
 
@@ -308,6 +317,9 @@ def main():
 
     cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
     runner = Runner(cfg, dev)
+    if args.only != "step":  # profiling aid: time one half of the step only
+        runner.step = runner.fwd if args.only == "fwd" else runner.bwd
+        args.no_e2e = args.no_cpu_baseline = True
     for _ in range(warmup):
         runner.step()
     torch.cuda.synchronize()
