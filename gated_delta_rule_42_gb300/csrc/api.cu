@@ -96,9 +96,27 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   w.seq = (int4 *)take(sizeof(int4) * (size_t)(P.N > 0 ? P.N : 1));
   w.chunk = (int4 *)take(sizeof(int4) * (size_t)(P.NC > 0 ? P.NC : 1));
   w.flags = (int *)take(sizeof(int) * 4);
-  if (!backward && use_tc(P)) {  // the fused forward keeps everything on chip
+  if (use_tc(P)) {
+    if (backward) {  // tensor-core backward: per-slot bf16 / fp32 intermediates
+      w.tc_hs = (__nv_bfloat16 *)take(2 * slots * K * V);
+      w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);
+      w.tc_dd = (__nv_bfloat16 *)take(2 * slots * C * V);
+      w.tc_dx = (__nv_bfloat16 *)take(2 * slots * C * V);
+      w.tc_A = (__nv_bfloat16 *)take(2 * slots * C * C);
+      w.tc_dqg = (float *)take(4 * slots * C * K);
+      w.tc_dbk = (float *)take(4 * slots * C * K);
+      w.tc_dkh = (float *)take(4 * slots * K * C);
+      w.tc_dat = (float *)take(4 * slots * C * C);
+      w.tc_dqkt = (float *)take(4 * slots * C * C);
+      w.tc_dbx = (float *)take(4 * slots * C);
+      w.tc_dgl = (float *)take(4 * slots * K);
+      if (P.HV != P.H) {
+        w.dqp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
+        w.dkp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
+      }
+    }
     if (W) *W = w;
-    return off;
+    return off;  // the fused forward keeps everything on chip
   }
   w.G = (float *)take(sizeof(float) * slots * C * K);
   w.Aqk = (float *)take(sizeof(float) * slots * C * C);
@@ -179,7 +197,18 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
   if (P.N == 0) return KDA_OK;
   Workspace W;
   layout(P, true, (char *)workspace, &W);
-  cudaError_t e = simple_backward(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, (cudaStream_t)stream);
+  cudaError_t e;
+  if (use_tc(P)) {
+    cudaStream_t s = (cudaStream_t)stream;
+    int *err = W.flags + 2;
+    e = tc_forward(P, W, nullptr, nullptr, W.tc_hs, err, s);
+    if (e == cudaSuccess) e = tc_backward_scan(P, W, dO, dhT, dh0, err, s);
+    if (e == cudaSuccess) e = tc_backward_gemm(P, W, dO, dv, err, s);
+    if (e == cudaSuccess) e = tc_backward_chain(P, W, dq, dk, dg, dbeta, s);
+    if (e == cudaSuccess && P.HV != P.H) e = launch_group_reduce(P, W.dqp, W.dkp, dq, dk, s);
+  } else {
+    e = simple_backward(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_bwd");
   return KDA_OK;
 }

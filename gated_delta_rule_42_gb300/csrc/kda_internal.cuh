@@ -44,6 +44,19 @@ struct Workspace {
   float *dqp;    // [Ttot][HV][K]   per-value-head dq~ partials
   float *dkp;    // [Ttot][HV][K]
   float *dw;     // [slot][64][K]
+  // tensor-core backward (bf16, K = V = 128), per (chunk, value head) slot
+  __nv_bfloat16 *tc_hs;    // [slot][K][V]  chunk-start state (forward recompute)
+  __nv_bfloat16 *tc_dh;    // [slot][K][V]  gradient of the chunk-end state
+  __nv_bfloat16 *tc_dd;    // [slot][64][V] gradient of the deltas
+  __nv_bfloat16 *tc_dx;    // [slot][64][V] dX = A^T dD
+  __nv_bfloat16 *tc_A;     // [slot][64][64] (I + L)^-1
+  float *tc_dqg;           // [slot][64][K] dO h^T
+  float *tc_dbk;           // [slot][64][K] -dX h^T
+  float *tc_dkh;           // [slot][K][64] dKhat^T
+  float *tc_dat;           // [slot][64][64] dA^T
+  float *tc_dqkt;          // [slot][64][64] dAqk^T (unmasked)
+  float *tc_dbx;           // [slot][64] sum_v dX v
+  float *tc_dgl;           // [slot][K]  rowsum(dh' .* h)
 };
 
 // --- element access -------------------------------------------------------
@@ -81,6 +94,15 @@ cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t 
 // chunk-start states (bf16 [chunk][HV][K][V]) instead of the output.
 cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, void *hstates,
                        int *err, cudaStream_t s);
+cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,
+                             float *dh0, int *err, cudaStream_t s);
+cudaError_t tc_backward_gemm(const Problem &P, const Workspace &W, const void *dO, void *dv, int *err,
+                             cudaStream_t s);
+cudaError_t tc_backward_chain(const Problem &P, const Workspace &W, void *dq, void *dk, float *dg,
+                              float *dbeta, cudaStream_t s);
+// dq = (group sum of dqp) / sqrt(K), dk = group sum of dkp, over the HV/H value heads
+cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
+                                cudaStream_t s);
 // true when the tensor-core kernels handle this problem
 inline bool tc_eligible(const Problem &P) { return P.bf16 && P.K == 128 && P.V == 128; }
 

@@ -391,6 +391,21 @@ cudaError_t run_backward(const Problem &P, const Workspace &W, const void *dO, c
 
 }  // namespace
 
+cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
+                                cudaStream_t s) {
+  if (P.Ttot == 0) return cudaSuccess;
+  const int64_t total = P.Ttot * P.H * P.K;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (P.bf16)
+    KDA_LAUNCH("group_reduce_kernel", s, group_reduce_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+                                             P, dqp, dkp, (__nv_bfloat16 *)dq, (__nv_bfloat16 *)dk));
+  else
+    KDA_LAUNCH("group_reduce_kernel", s,
+               group_reduce_kernel<float><<<blocks, 256, 0, s>>>(P, dqp, dkp, (float *)dq, (float *)dk));
+  return cudaGetLastError();
+}
+
 cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO,
                             const float *dhT, void *dq, void *dk, void *dv, float *dg,
                             float *dbeta, float *dh0, cudaStream_t s) {

@@ -1,0 +1,242 @@
+// Reverse state-gradient scan of the bf16 chunked KDA backward (K = V = 128).
+//
+// One CTA walks the chunks of one (sequence, value head) from last to first,
+// holding dh' -- the gradient of the chunk-END state -- in fp32 registers
+// (thread = key channel c, half the value columns), starting from dhT (or 0).
+// Per chunk, after the V-independent phases (a) and (b) of tc_common.cuh
+// (recomputed from q, k, g, beta), on tcgen05:
+//   dD^T = dO^T Aqk + dh'^T Khat^T        dD = Aqk^T dO + Khat dh'   (deltas' gradient)
+//   dX^T = dD^T A                         dX = A^T dD                (through A = (I+L)^-1)
+//   dh  <- diag(2^G_last) dh' + Qg^T dO - Bk^T dX                    (gradient of the chunk-start state)
+// The last line is the reverse recurrence of FLA's bwd_dhu ("[Fix] Use unit KDA
+// gate scale when A_log is omitted", fla-org/flash-linear-attention PR #1294,
+// commit log: "the kernel's reverse state-gradient recurrence").  Every
+// operand is read straight from the row-major tiles through K- or MN-major
+// descriptors.  For the per-chunk gradient kernel the scan stores, per chunk:
+// dh' (bf16 [K][V]), dD and dX (bf16 [64][V]) and A (bf16 [64][64]); at the
+// start of the sequence it writes dh0 (fp32).
+#include "tc_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace umma;
+using namespace tc;
+
+constexpr uint32_t U_DH = 0, U_DDT = 32768, U_NDX = 49152;  // phase (c) use of the union
+constexpr uint32_t TMEM_COLS = 256;  // [0,64) dD^T, [64,128) dX^T, [128,256) dh update
+
+__global__ void __launch_bounds__(kThr, 1)
+kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__ dO,
+                       const float *__restrict__ dhT, float *__restrict__ dh0, int *err) {
+  extern __shared__ unsigned char smraw[];
+  unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(sm);
+  float *vec = (float *)(sm + OFF_VEC);
+  float *betab = (float *)(sm + OFF_BETA);
+  uint64_t *bar = (uint64_t *)(sm + OFF_MISC);
+  uint32_t *tslot = (uint32_t *)(sm + OFF_MISC + 8);
+  unsigned char *U = sm + OFF_U;
+
+  const int n = blockIdx.x, j = blockIdx.y;
+  const int HV = P.HV, h = j / (HV / P.H);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, vhalf = warp >> 2;
+  const int cown = quarter * 32 + lane;
+  const int4 si = W.seq[n];
+
+  if (tid == 0) {
+    bar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
+  uint32_t phase = 0;
+
+  float dreg[64];  // dh'[cown][64 * vhalf + x]
+  {
+    const size_t base = (((size_t)n * HV + j) * kD + cown) * kD + 64 * vhalf;
+#pragma unroll
+    for (int x = 0; x < 64; x += 4) {
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (dhT != nullptr) t = *reinterpret_cast<const float4 *>(dhT + base + x);
+      dreg[x] = t.x; dreg[x + 1] = t.y; dreg[x + 2] = t.z; dreg[x + 3] = t.w;
+    }
+  }
+
+  if (si.w > 0) {
+    const int4 chl = W.chunk[si.z + si.w - 1];
+    load_kqg(P, sm, chl.y, chl.z, j, h, betab, true);
+    load_rows(sbase + OFF_VRAW, dO, chl.y, chl.z, HV, j);
+    cp_commit();
+  }
+
+  for (int ci = si.w - 1; ci >= 0; --ci) {
+    const int cidx = si.z + ci;
+    const int4 ch = W.chunk[cidx];
+    const int len = ch.z;
+    const int buf = (si.w - 1 - ci) & 1;
+    const float *beta = betab + buf * kC;
+    const size_t slot = (size_t)cidx * HV + j;
+    cp_wait_all();
+    __syncthreads();
+
+    phase_a<true>(sm, len, beta);
+    if (ci > 0) {
+      const int4 pv = W.chunk[cidx - 1];
+      load_kqg(P, sm, pv.y, pv.z, j, h, betab + (buf ^ 1) * kC, true);
+      cp_commit();
+    }
+    phase_b<true>(sm, beta);
+
+    // ---------------- (c) ----------------
+    {
+      unsigned char *DH = U + U_DH;  // dh' row-major [c][v]
+#pragma unroll
+      for (int x8 = 0; x8 < 8; ++x8) {
+        float t[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = dreg[8 * x8 + e];
+        const uint4 u = pack8(t);
+        *reinterpret_cast<uint4 *>(DH + sw_chunk(cown, 8 * vhalf + x8, kD)) = u;
+        *reinterpret_cast<uint4 *>(W.tc_dh + (slot * kD + cown) * kD + 64 * vhalf + 8 * x8) = u;
+      }
+      // A for the per-chunk kernel, row-major bf16 [64][64]
+      for (int e = tid; e < kC * 8; e += kThr) {
+        const int r = e >> 3, jj = e & 7;
+        *reinterpret_cast<uint4 *>(W.tc_A + (slot * kC + r) * kC + jj * 8) =
+            *reinterpret_cast<const uint4 *>(sm + OFF_AM + sw_chunk(r, jj, kC));
+      }
+    }
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t aDH = sbase + OFF_U + U_DH, aDDT = sbase + OFF_U + U_DDT, aNDX = sbase + OFF_U + U_NDX;
+    if (tid == 0) {
+      // dD^T[v][r] = sum_i dO[i][v] Aqk[i][r] + sum_c dh'[c][v] Khat[r][c]   (M=128 v, N=64 r)
+      const uint32_t id1 = idesc(128, 64, 1, 1), id2 = idesc(128, 64, 1, 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma(tmem, desc_mn(sbase + OFF_VRAW, s, 8192), desc_mn(sbase + OFF_AQK, s, 8192), id1, s > 0);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) mma(tmem, desc_mn(aDH, s, 16384), desc_k16(sbase + OFF_KH, s, kC), id2, 1);
+      commit(bar);
+    }
+    bar_wait(bar, phase, err);
+    phase ^= 1;
+    fence_after();
+    {  // dD^T -> bf16 tile [v][r]; dD -> workspace, row-major [r][v]
+      const int v = cown, r0 = 32 * vhalf;
+      float d[32];
+      tmem_ld32(tq + (uint32_t)r0, d);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = d[q8 * 8 + e];
+        *reinterpret_cast<uint4 *>(U + U_DDT + sw_chunk(v, (r0 >> 3) + q8, kD)) = pack8(x);
+      }
+      __nv_bfloat16 *dst = W.tc_dd + slot * kC * kD + v;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dst[(r0 + e) * kD] = __float2bfloat16_rn(d[e]);
+    }
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (tid == 0) {  // dX^T[v][i] = sum_r dD^T[v][r] A[r][i]   (M=128 v, N=64 i, K=64 r)
+      const uint32_t id = idesc(128, 64, 0, 1);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) mma(tmem + 64, desc_k16(aDDT, s, kD), desc_mn(sbase + OFF_AM, s, 8192), id, s > 0);
+      commit(bar);
+    }
+    bar_wait(bar, phase, err);
+    phase ^= 1;
+    fence_after();
+    {  // -dX^T -> bf16 tile [v][i]; dX -> workspace, row-major [i][v]
+      const int v = cown, r0 = 32 * vhalf;
+      float d[32];
+      tmem_ld32(tq + 64u + (uint32_t)r0, d);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = -d[q8 * 8 + e];
+        *reinterpret_cast<uint4 *>(U + U_NDX + sw_chunk(v, (r0 >> 3) + q8, kD)) = pack8(x);
+      }
+      __nv_bfloat16 *dst = W.tc_dx + slot * kC * kD + v;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dst[(r0 + e) * kD] = __float2bfloat16_rn(d[e]);
+    }
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (tid == 0) {
+      // U[c][v] = sum_r Qg[r][c] dO[r][v] - sum_r Bk[r][c] dX[r][v]   (M=128 c, N=128 v, K=64 r)
+      const uint32_t id1 = idesc(128, 128, 1, 1), id2 = idesc(128, 128, 1, 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma(tmem + 128, desc_mn(sbase + OFF_QG, s, 8192), desc_mn(sbase + OFF_VRAW, s, 8192), id1, s > 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma(tmem + 128, desc_mn(sbase + OFF_BK, s, 8192), desc_k16(aNDX, s, kD), id2, 1);
+      commit(bar);
+    }
+    bar_wait(bar, phase, err);
+    phase ^= 1;
+    fence_after();
+    {
+      const float gl = vec[V_GAML * kD + cown];
+      float d[32];
+#pragma unroll
+      for (int hx = 0; hx < 2; ++hx) {
+        tmem_ld32(tq + 128u + (uint32_t)(64 * vhalf + 32 * hx), d);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dreg[32 * hx + e] = fmaf(gl, dreg[32 * hx + e], d[e]);
+      }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (ci > 0) {  // dO of this chunk consumed
+      const int4 pv = W.chunk[cidx - 1];
+      load_rows(sbase + OFF_VRAW, dO, pv.y, pv.z, HV, j);
+      cp_commit();
+    }
+  }
+
+  if (dh0 != nullptr) {
+    float *dst = dh0 + (((size_t)n * HV + j) * kD + cown) * kD + 64 * vhalf;
+#pragma unroll
+    for (int x = 0; x < 64; x += 4)
+      *reinterpret_cast<float4 *>(dst + x) = make_float4(dreg[x], dreg[x + 1], dreg[x + 2], dreg[x + 3]);
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    tmem_free(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,
+                             float *dh0, int *err, cudaStream_t s) {
+  if (P.N == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  KDA_LAUNCH("kda_bwd_scan_tc", s,
+             kda_bwd_scan_tc_kernel<<<dim3(P.N, P.HV), kThr, SMEM_BYTES, s>>>(
+                 P, W, (const __nv_bfloat16 *)dO, dhT, dh0, err));
+  return cudaGetLastError();
+}
+
+}  // namespace kda

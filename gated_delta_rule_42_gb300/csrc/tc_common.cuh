@@ -1,0 +1,333 @@
+// Shared pieces of the fused bf16 tensor-core KDA kernels (K = V = 128,
+// chunk 64): the shared-memory map, the asynchronous chunk loads, and the two
+// V-independent phases every chunk step needs:
+//  (a) chunk-local cumsum G of the log2 gate and the decay-scaled operand tiles;
+//  (b) the decayed Gram blocks L (strictly lower, beta-scaled) and Aqk (lower)
+//      on 16x16 warp MMAs, and A = (I + L)^-1 in fp32.
+//
+// Decay scaling.  2^(G_r - G_i) is split at the first row of each 16-token
+// block (ref): rows carry 2^(G_r - G_ref) <= 1 (tile Kr / Qr), columns carry
+// 2^(G_ref - G_i) <= 2^(15 |g|max) (tile Kc), and between blocks the per-channel
+// factor D_RI = 2^(G_ref(R) - G_ref(I)) <= 1 is applied to the column fragments
+// in registers.  Nothing overflows for gates >= -8 per token (log2 units).  The
+// chunk-level tiles Bk = beta k 2^G, Qg = q~ 2^G and Khat = k 2^(G_last - G)
+// only underflow where the true value is negligible.
+//
+// Every operand tile is 128-byte swizzled (see umma.cuh), so the same bytes
+// serve as a K-major or an MN-major tcgen05 operand and as an ldmatrix source.
+#pragma once
+
+#include "kda_internal.cuh"
+#include "umma.cuh"
+
+namespace kda {
+namespace tc {
+
+using namespace umma;
+
+constexpr int kC = 64;     // chunk
+constexpr int kD = 128;    // K = V
+constexpr int kThr = 256;  // 8 warps
+constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile
+
+// shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_KRAW = 0;       // k  [64][128] bf16
+constexpr uint32_t OFF_QRAW = 16384;   // q  [64][128]
+constexpr uint32_t OFF_VRAW = 32768;   // v (forward) or dO (backward) [64][128]
+constexpr uint32_t OFF_GRAW = 49152;   // g -> G  fp32 [64][132]
+constexpr uint32_t OFF_BK = 83968;     // beta k 2^G         [64 r][128 c]
+constexpr uint32_t OFF_QG = 100352;    // q~ 2^G             [64 r][128 c]
+constexpr uint32_t OFF_KH = 116736;    // k 2^(G_last - G)   [64 r][128 c]
+constexpr uint32_t OFF_AQK = 133120;   // Aqk                [64 r][64 i]
+constexpr uint32_t OFF_AM = 141312;    // A = (I + L)^-1     [64 r][64 i]
+constexpr uint32_t OFF_U = 149504;     // union (64 KB): phases (a)/(b) | phase (c)
+constexpr uint32_t U_KR = 0, U_QR = 16384, U_KC = 32768, U_LF = 49152;  // (a)/(b)
+constexpr uint32_t U_AF = 0, U_T = 16384;                              // (b) inverse scratch
+constexpr uint32_t OFF_VEC = 215040;   // fp32 vectors (20 rows of 128)
+constexpr uint32_t OFF_BETA = 225280;  // beta, two buffers of 64 fp32
+constexpr uint32_t OFF_MISC = 225792;  // mbarrier, tmem slot
+constexpr uint32_t SMEM_BYTES = 225792 + 64 + 1024;  // + alignment slack
+constexpr int V_GL = 0, V_GAML = 1, V_GREF = 2, V_EREF = 6, V_D = 10, V_LAM = 16;
+
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ void st_zero16(uint32_t dst) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};\n" ::"r"(dst), "r"(0u) : "memory");
+}
+__device__ __forceinline__ void st_bf2(unsigned char *tile, int r, int c, int R, float a, float b) {
+  *reinterpret_cast<uint32_t *>(tile + sw_off(r, c, R)) = pack_bf16(a, b);
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+  return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                    pack_bf16(x[6], x[7]));
+}
+__device__ __forceinline__ void unpack8(uint4 u, float (&x)[8]) {
+  float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y), c = unpack_bf16(u.z), d = unpack_bf16(u.w);
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+}
+
+// Descriptor of 16-row K slice s of an MN-major operand stored as a swizzled
+// tile whose rows are the K index (row stride 128 B) and whose columns are the
+// M (or N) index in 64-wide sub-tiles `lbo` bytes apart.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int s, uint32_t lbo) {
+  uint64_t d = (uint64_t)(((tile + (uint32_t)s * 2048u) >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// kind::f16 instruction descriptor with operand majors (0 = K-major, 1 = MN-major).
+__device__ __forceinline__ uint32_t idesc(int M, int N, int a_mn, int b_mn) {
+  return idesc_bf16(M, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
+}
+
+// Asynchronous loads of one chunk's rows of a [tokens][heads][128] bf16
+// tensor into a swizzled [64][128] tile; rows at or past len are zeroed.
+__device__ __forceinline__ void load_rows(uint32_t tile, const __nv_bfloat16 *src, int t0, int len,
+                                          int heads, int head) {
+  for (int it = threadIdx.x; it < kC * 16; it += kThr) {
+    const int r = it >> 4, jj = it & 15;
+    const uint32_t dst = tile + sw_chunk(r, jj, kC);
+    if (r < len) cp16(dst, src + ((size_t)(t0 + r) * heads + head) * kD + jj * 8);
+    else st_zero16(dst);
+  }
+}
+
+__device__ __forceinline__ void load_gate(uint32_t tile, const float *g, int t0, int len, int HV, int j) {
+  for (int it = threadIdx.x; it < kC * 32; it += kThr) {
+    const int r = it >> 5, jj = it & 31;
+    const uint32_t dst = tile + (uint32_t)(r * kGLD + jj * 4) * 4u;
+    if (r < len) cp16(dst, g + ((size_t)(t0 + r) * HV + j) * kD + jj * 4);
+    else st_zero16(dst);
+  }
+}
+
+// k, q (optional), g and beta of one chunk.
+__device__ __forceinline__ void load_kqg(const Problem &P, unsigned char *sm, int t0, int len, int j,
+                                         int h, float *beta_dst, bool with_q) {
+  const uint32_t base = smem_u32(sm);
+  load_rows(base + OFF_KRAW, (const __nv_bfloat16 *)P.k, t0, len, P.H, h);
+  if (with_q) load_rows(base + OFF_QRAW, (const __nv_bfloat16 *)P.q, t0, len, P.H, h);
+  load_gate(base + OFF_GRAW, P.g, t0, len, P.HV, j);
+  if (threadIdx.x < kC) beta_dst[threadIdx.x] = threadIdx.x < len ? P.beta[(size_t)(t0 + threadIdx.x) * P.HV + j] : 0.f;
+}
+
+// Phase (a).  Needs the k (and q) staging tiles, the gate tile and beta of the
+// chunk; ends with a __syncthreads.  Writes G (in place), the vectors, and the
+// tiles Kr, Kc, Bk, Khat (and Qr, Qg when kQ).
+template <bool kQ>
+__device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float *beta) {
+  const int tid = threadIdx.x;
+  float *G = (float *)(sm + OFF_GRAW);
+  float *vec = (float *)(sm + OFF_VEC);
+  unsigned char *U = sm + OFF_U;
+  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
+  if (tid < kD) {
+    const int c = tid;
+    float col[kC];
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < kC; ++r) col[r] = G[r * kGLD + c];
+#pragma unroll
+    for (int r = 0; r < kC; ++r) {
+      if (r < len) s += col[r];
+      col[r] = s;
+    }
+#pragma unroll
+    for (int r = 0; r < kC; ++r) G[r * kGLD + c] = col[r];
+    const float gl = s;
+    vec[V_GL * kD + c] = gl;
+    vec[V_GAML * kD + c] = exp2f(gl);
+    float gref[4];
+#pragma unroll
+    for (int R = 0; R < 4; ++R) {
+      gref[R] = (16 * R < len) ? col[16 * R] : gl;
+      vec[(V_GREF + R) * kD + c] = gref[R];
+      vec[(V_EREF + R) * kD + c] = exp2f(gref[R]);
+      vec[(V_LAM + R) * kD + c] = exp2f(gl - gref[R]);
+    }
+    int p = 0;
+#pragma unroll
+    for (int R = 1; R < 4; ++R)
+#pragma unroll
+      for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
+  }
+  __syncthreads();
+  // thread: 8 consecutive channels (one 16-byte chunk) of 4 consecutive rows
+  {
+    const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
+    float gref[8], eref[8], lam[8];
+#pragma unroll
+    for (int e = 0; e < 8; e += 4) {
+      *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (V_GREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(eref + e) = *reinterpret_cast<const float4 *>(vec + (V_EREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(lam + e) = *reinterpret_cast<const float4 *>(vec + (V_LAM + R) * kD + c0 + e);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = rg * 4 + rr;
+      const uint32_t off = sw_chunk(r, jj, kC);
+      float kv[8], qv[8], g[8], e1[8], e2[8], o[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + off), kv);
+      if (kQ) unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + off), qv);
+      *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGLD + c0);
+      *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGLD + c0 + 4);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        e1[e] = exp2f(g[e] - gref[e]);  // <= 1
+        e2[e] = exp2f(gref[e] - g[e]);  // >= 1
+      }
+      const float br = beta[r];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
+      *reinterpret_cast<uint4 *>(U + U_KR + off) = pack8(o);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
+      *reinterpret_cast<uint4 *>(U + U_KC + off) = pack8(o);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * e1[e] * eref[e];
+      *reinterpret_cast<uint4 *>(sm + OFF_BK + off) = pack8(o);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e] * lam[e];
+      *reinterpret_cast<uint4 *>(sm + OFF_KH + off) = pack8(o);
+      if (kQ) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
+        *reinterpret_cast<uint4 *>(U + U_QR + off) = pack8(o);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] *= eref[e];
+        *reinterpret_cast<uint4 *>(sm + OFF_QG + off) = pack8(o);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Phase (b).  Needs the tiles of phase (a); ends with a __syncthreads.  Writes
+// the A tile (and the Aqk tile when kQ).  Clobbers the union region.
+template <bool kQ>
+__device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_u32(sm);
+  const float *vec = (const float *)(sm + OFF_VEC);
+  unsigned char *U = sm + OFF_U;
+  float *Lf = (float *)(U + U_LF);
+  for (int pr = warp; pr < 16; pr += 8) {
+    const int R = pr >> 2, I = pr & 3;
+    float accL[2][4] = {}, accQ[2][4] = {};
+    if (I <= R) {
+      const float *Dv = (I < R) ? vec + (V_D + R * (R - 1) / 2 + I) * kD : nullptr;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        uint32_t ak[4], aq[4] = {0, 0, 0, 0}, b[4];
+        {
+          const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
+          ldsm_x4(sbase + OFF_U + U_KR + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
+          if (kQ) ldsm_x4(sbase + OFF_U + U_QR + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
+        }
+        {
+          const int mi = lane >> 3;
+          const int row = 16 * I + (lane & 7) + (mi >> 1) * 8, jj = 2 * s + (mi & 1);
+          ldsm_x4(sbase + OFF_U + U_KC + sw_chunk(row, jj, kC), b[0], b[1], b[2], b[3]);
+        }
+        if (Dv != nullptr) {
+          const int c0 = 16 * s + (lane & 3) * 2;
+          const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
+          const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 f = unpack_bf16(b[t]);
+            b[t] = (t & 1) ? pack_bf16(f.x * d89.x, f.y * d89.y) : pack_bf16(f.x * d01.x, f.y * d01.y);
+          }
+        }
+        mma16816(accL[0], ak, b[0], b[1]);
+        mma16816(accL[1], ak, b[2], b[3]);
+        if (kQ) {
+          mma16816(accQ[0], aq, b[0], b[1]);
+          mma16816(accQ[1], aq, b[2], b[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * R + (lane >> 2) + hh * 8;
+        const int i = 16 * I + nt * 8 + (lane & 3) * 2;
+        const float br = beta[r];
+        const float l0 = (i < r) ? br * accL[nt][2 * hh] : 0.f;
+        const float l1 = (i + 1 < r) ? br * accL[nt][2 * hh + 1] : 0.f;
+        *reinterpret_cast<float2 *>(Lf + r * kC + i) = make_float2(l0, l1);
+        if (kQ) {
+          const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
+          const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
+          st_bf2(sm + OFF_AQK, r, i, kC, a0, a1);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  float *Af = (float *)(U + U_AF);  // overwrites Kr (dead)
+  float *Tf = (float *)(U + U_T);   // overwrites Qr (dead)
+  if (warp < 4 && lane < 16) {
+    // diagonal block R = warp: lane i computes column i of (I + L_RR)^-1
+    const int R = warp, i = lane;
+    float a[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) a[m] = (m == i) ? 1.f : 0.f;
+#pragma unroll
+    for (int r = 1; r < 16; ++r) {
+      float s = a[r];
+#pragma unroll
+      for (int m = 0; m < r; ++m) s = fmaf(-Lf[(16 * R + r) * kC + 16 * R + m], a[m], s);
+      a[r] = s;
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) Af[(16 * R + m) * kC + 16 * R + i] = a[m];
+  }
+  for (int e = tid; e < 6 * 256; e += kThr) {  // strictly-upper blocks of A
+    const int b = e >> 8, w = e & 255;
+    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2);
+    const int I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
+    Af[(16 * R + (w >> 4)) * kC + 16 * I + (w & 15)] = 0.f;
+  }
+  __syncthreads();
+  // off-diagonal blocks by sub-diagonal level: A_RI = -A_RR sum_{M=I}^{R-1} L_RM A_MI
+#pragma unroll
+  for (int lvl = 1; lvl < 4; ++lvl) {
+    const int nb = 4 - lvl;
+    for (int e = tid; e < nb * 256; e += kThr) {
+      const int I = e >> 8, R = I + lvl, rr = (e >> 4) & 15, ii = e & 15;
+      float s = 0.f;
+      for (int M = I; M < R; ++M)
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          s = fmaf(Lf[(16 * R + rr) * kC + 16 * M + m], Af[(16 * M + m) * kC + 16 * I + ii], s);
+      Tf[(I * 16 + rr) * 16 + ii] = s;
+    }
+    __syncthreads();
+    for (int e = tid; e < nb * 256; e += kThr) {
+      const int I = e >> 8, R = I + lvl, rr = (e >> 4) & 15, ii = e & 15;
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) s = fmaf(Af[(16 * R + rr) * kC + 16 * R + m], Tf[(I * 16 + m) * 16 + ii], s);
+      Af[(16 * R + rr) * kC + 16 * I + ii] = -s;
+    }
+    __syncthreads();
+  }
+  for (int e = tid; e < kC * kC / 8; e += kThr) {  // A -> bf16 tile, 16-byte chunks
+    const int r = e >> 3, jj = e & 7;
+    float x[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) x[t] = Af[r * kC + jj * 8 + t];
+    *reinterpret_cast<uint4 *>(sm + OFF_AM + sw_chunk(r, jj, kC)) = pack8(x);
+  }
+  __syncthreads();
+}
+
+}  // namespace tc
+}  // namespace kda
