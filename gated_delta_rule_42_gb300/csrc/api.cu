@@ -146,6 +146,12 @@ kda_status check_ws(size_t need, void *ws, size_t bytes) {
 }
 
 }  // namespace
+
+void set_last_error(const char *msg) {
+  strncpy(g_err, msg, sizeof(g_err) - 1);
+  g_err[sizeof(g_err) - 1] = 0;
+}
+
 }  // namespace kda
 
 using namespace kda;

@@ -69,6 +69,9 @@ __device__ __forceinline__ void stf(__nv_bfloat16 *p, int64_t i, float x) {
   p[i] = __float2bfloat16_rn(x);
 }
 
+// Records the message kda_last_error() returns on the calling thread (api.cu).
+void set_last_error(const char *msg);
+
 // --- launch instrumentation (instrument.cu) -----------------------------------
 void inst_begin(const char *name, cudaStream_t s);
 void inst_end(cudaStream_t s);

@@ -125,6 +125,21 @@ const char *kda_last_error(void);
 /* Library ABI version (major * 100 + minor). */
 int kda_version(void);
 
+/* Chunked forward without a caller workspace (no counterpart on the pages).
+ * For callers that cannot allocate device memory -- a host program linked
+ * against this library alone, a runtime that plans every device byte at
+ * start-up and forbids allocation afterwards -- this runs kda_chunk_fwd on a
+ * scratch array that lives inside the library: 4 MiB of device memory per GPU
+ * that loads it, held until the process exits.  Same arguments and results as
+ * kda_chunk_fwd minus the workspace.  The first call on a device looks up the
+ * array's address with that device current; make it before any CUDA-graph
+ * capture.  All calls share the one array (it keeps the last call's contents;
+ * nothing in it must start at zero), so calls that may overlap on the GPU race:
+ * order them on one stream.  A problem whose workspace exceeds 4 MiB is
+ * rejected with KDA_ERR_WORKSPACE before anything is launched.  The library
+ * allocates nothing on this path. */
+kda_status kda_chunk_fwd_noalloc(const kda_inputs *in, void *o, float *hT, void *stream);
+
 /* ---- instrumentation (benchmarks and profiling; no counterpart on the pages) ----
  * Every kernel the library launches is counted.  While timing is enabled, a
  * CUDA event pair is recorded on the launching stream around each launch. */
