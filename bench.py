@@ -72,7 +72,17 @@ def kernel_bytes_per_token(name, cfg):
     H, HV, K, V = cfg.H, cfg.HV, cfg.K, cfg.V
     qk, vv, g, b = H * K * e, HV * V * e, 4 * HV * K, 4 * HV
     f32K, f32V, cc, hh = 4 * HV * K, 4 * HV * V, 4 * HV * 64, 4 * HV * K * V / 64
+    hs = 2 * HV * K * V / 64            # bf16 K x V state per chunk, per token
+    t16 = 16384 * HV / 64               # one 16 KB per-chunk tile (Aqk+A, X^T or D^T), per token
+    dgl = 4 * HV * K / 64               # fp32 K-vector per chunk, per token
     table = {
+        # tensor-core path (bf16, K = V = 128)
+        "kda_fwd_tc": 2 * qk + 2 * vv + g + b,
+        "kda_fwd_tc_states": 2 * qk + vv + g + b + hs + 3 * t16,
+        "kda_bwd_scan_tc": 2 * qk + g + b + vv + t16 + hs + 2 * vv,
+        "kda_bwd_gemm_tc": 2 * t16 + 2 * hs + 3 * vv + vv + b + vv + 3 * f32K + 2 * cc + b + dgl,
+        "kda_bwd_chain_tc": g + b + t16 / 2 + 3 * f32K + 2 * cc + 2 * qk + b + dgl + 2 * qk + g + b,
+        # fp32 path
         "simple_intra_kernel": 2 * qk + vv + g + b + 2 * f32K + 2 * cc + f32K + f32V,
         "simple_scan_kernel": qk + 2 * f32K + f32V + hh + f32V,
         "simple_output_kernel": qk + f32K + cc + f32V + hh + vv,
@@ -284,6 +294,19 @@ def cpu_baseline(cfg):
 
 
 # --------------------------------------------------------------------------
+def job_throughput(ms_local, tokens_per_rank, steps, dist=None, device="cpu"):
+    """Whole-job tokens/s for weak scaling: every rank processes tokens_per_rank
+    per step; the job's time is the slowest rank's (max over ranks).  Returns
+    (tokens/s, max ms over ranks for the timed steps)."""
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    world = 1
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        world = dist.get_world_size()
+    ms = float(t.item())
+    return tokens_per_rank * world / (ms / steps / 1e3), ms
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -336,13 +359,14 @@ def main():
         dist.barrier()
     launches = runner.lib.kda_launch_count() - n0
     ck = clocks.stop() if rank == 0 else None
-    t = torch.tensor([ms], device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
+    value, ms = job_throughput(ms, cfg.valid_tokens, args.steps, dist, device=dev)
 
     split = kernel_split(runner, max(3, min(args.steps, 10)))
-    e2e = None if args.no_e2e else e2e_measure(cfg, runner, max(3, min(args.steps, 10)))
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = e2e_measure(cfg, runner, max(3, min(args.steps, 10)))
+        e_value, e_ms = job_throughput(e_ms, cfg.valid_tokens, 1, dist, device=dev)  # ms per step, max over ranks
+        e2e = (e_value, e_ms, h2d, d2h)
 
     if rank != 0:
         if dist:
@@ -351,7 +375,6 @@ def main():
     peaks = load_peaks()
     ms_step = ms / args.steps
     toks = cfg.valid_tokens
-    value = toks * world / (ms_step / 1e3)
     ab = algorithmic_bytes(cfg)
     af = algorithmic_flops(cfg)
     t_hbm = ab["total"] / (peaks["hbm"] * 1e9)
@@ -393,8 +416,8 @@ def main():
         "clocks": ck,
     }
     if e2e is not None:
-        e_ms, h2d, d2h = e2e
-        out["e2e"] = {"value": round(toks / (e_ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(e_ms, 3),
+        e_value, e_ms, h2d, d2h = e2e
+        out["e2e"] = {"value": round(e_value, 1), "unit": "tokens/s", "ms_per_step": round(e_ms, 3),
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg)

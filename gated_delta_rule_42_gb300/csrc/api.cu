@@ -1,4 +1,5 @@
 // C ABI of libkda: argument validation, workspace layout and dispatch.
+#include <atomic>
 #include <stdarg.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -99,10 +100,12 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   if (use_tc(P)) {
     if (backward) {  // tensor-core backward: per-slot bf16 / fp32 intermediates
       w.tc_hs = (__nv_bfloat16 *)take(2 * slots * K * V);
+      w.tc_aqk_a = (unsigned char *)take(16384 * slots);
+      w.tc_xt = (unsigned char *)take(16384 * slots);
+      w.tc_dt = (unsigned char *)take(16384 * slots);
       w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);
       w.tc_dd = (__nv_bfloat16 *)take(2 * slots * C * V);
       w.tc_dx = (__nv_bfloat16 *)take(2 * slots * C * V);
-      w.tc_A = (__nv_bfloat16 *)take(2 * slots * C * C);
       w.tc_dqg = (float *)take(4 * slots * C * K);
       w.tc_dbk = (float *)take(4 * slots * C * K);
       w.tc_dkh = (float *)take(4 * slots * K * C);
@@ -147,6 +150,21 @@ kda_status check_ws(size_t need, void *ws, size_t bytes) {
 
 }  // namespace
 
+cudaError_t sm_count(int *out) {
+  static std::atomic<int> cached[64];  // zero-initialised; filled once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  *out = n;
+  return cudaSuccess;
+}
+
 void set_last_error(const char *msg) {
   strncpy(g_err, msg, sizeof(g_err) - 1);
   g_err[sizeof(g_err) - 1] = 0;
@@ -182,7 +200,7 @@ kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspa
   if (P.N == 0) return KDA_OK;
   Workspace W;
   layout(P, false, (char *)workspace, &W);
-  cudaError_t e = use_tc(P) ? tc_forward(P, W, o, hT, nullptr, W.flags + 2, (cudaStream_t)stream)
+  cudaError_t e = use_tc(P) ? tc_forward(P, W, o, hT, false, W.flags + 2, (cudaStream_t)stream)
                             : simple_forward(P, W, o, hT, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd");
   return KDA_OK;
@@ -207,7 +225,7 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
   if (use_tc(P)) {
     cudaStream_t s = (cudaStream_t)stream;
     int *err = W.flags + 2;
-    e = tc_forward(P, W, nullptr, nullptr, W.tc_hs, err, s);
+    e = tc_forward(P, W, nullptr, nullptr, true, err, s);
     if (e == cudaSuccess) e = tc_backward_scan(P, W, dO, dhT, dh0, err, s);
     if (e == cudaSuccess) e = tc_backward_gemm(P, W, dO, dv, err, s);
     if (e == cudaSuccess) e = tc_backward_chain(P, W, dq, dk, dg, dbeta, s);

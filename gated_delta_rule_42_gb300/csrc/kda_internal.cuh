@@ -45,11 +45,13 @@ struct Workspace {
   float *dkp;    // [Ttot][HV][K]
   float *dw;     // [slot][64][K]
   // tensor-core backward (bf16, K = V = 128), per (chunk, value head) slot
-  __nv_bfloat16 *tc_hs;    // [slot][K][V]  chunk-start state (forward recompute)
-  __nv_bfloat16 *tc_dh;    // [slot][K][V]  gradient of the chunk-end state
-  __nv_bfloat16 *tc_dd;    // [slot][64][V] gradient of the deltas
-  __nv_bfloat16 *tc_dx;    // [slot][64][V] dX = A^T dD
-  __nv_bfloat16 *tc_A;     // [slot][64][64] (I + L)^-1
+  __nv_bfloat16 *tc_hs;     // [slot][K][V]  chunk-start state (forward recompute)
+  unsigned char *tc_aqk_a;  // [slot] 16 KB: swizzled Aqk tile, then A = (I+L)^-1 tile
+  unsigned char *tc_xt;     // [slot] 16 KB: swizzled X^T tile [V][64]
+  unsigned char *tc_dt;     // [slot] 16 KB: swizzled D^T tile [V][64]
+  __nv_bfloat16 *tc_dh;     // [slot][K][V]  gradient of the chunk-end state
+  __nv_bfloat16 *tc_dd;     // [slot][64][V] gradient of the deltas
+  __nv_bfloat16 *tc_dx;     // [slot][64][V] dX = A^T dD
   float *tc_dqg;           // [slot][64][K] dO h^T
   float *tc_dbk;           // [slot][64][K] -dX h^T
   float *tc_dkh;           // [slot][K][64] dKhat^T
@@ -68,6 +70,9 @@ __device__ __forceinline__ void stf(float *p, int64_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16 *p, int64_t i, float x) {
   p[i] = __float2bfloat16_rn(x);
 }
+
+// Number of SMs of the current device, cached per device (api.cu).
+cudaError_t sm_count(int *out);
 
 // Records the message kda_last_error() returns on the calling thread (api.cu).
 void set_last_error(const char *msg);
@@ -93,9 +98,11 @@ cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO
                             const float *dhT, void *dq, void *dk, void *dv, float *dg,
                             float *dbeta, float *dh0, cudaStream_t s);
 cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t s);
-// bf16, K = V = 128 tensor-core forward; with hstates != NULL writes the
-// chunk-start states (bf16 [chunk][HV][K][V]) instead of the output.
-cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, void *hstates,
+// bf16, K = V = 128 tensor-core forward.  With states = true it runs in
+// "states" mode for the backward: no output; per (chunk, value head) slot it
+// saves the chunk-start state and the Aqk, A, X^T and D^T tiles to
+// W.tc_hs / tc_aqk_a / tc_xt / tc_dt.
+cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, bool states,
                        int *err, cudaStream_t s);
 cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,
                              float *dh0, int *err, cudaStream_t s);

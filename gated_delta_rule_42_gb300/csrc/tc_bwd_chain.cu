@@ -131,12 +131,15 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
 
   // ---- loads ----
   load_gate(sbase + C_G, P.g, t0, len, HV, j);
-  for (int it = tid; it < kC * 8; it += kThr) {
-    const int r = it >> 3, jj = it & 7;
-    cp16(sbase + C_A + sw_chunk(r, jj, kC), W.tc_A + (slot * kC + r) * kC + jj * 8);
+  {  // A, saved by the forward recompute in this kernel's swizzled layout (after the 8 KB Aqk tile)
+    const unsigned char *src = W.tc_aqk_a + slot * 16384 + 8192;
+    for (int it = tid; it < 512; it += kThr) cp16(sbase + C_A + it * 16, src + it * 16);
+  }
+  if (tid < kC) {
+    if (tid < len) cp4(smem_u32(beta + tid), P.beta + (size_t)(t0 + tid) * HV + j);
+    else beta[tid] = 0.f;
   }
   cp_commit();
-  if (tid < kC) beta[tid] = tid < len ? P.beta[(size_t)(t0 + tid) * HV + j] : 0.f;
   for (int it = tid; it < kC * 8; it += kThr) {  // dA^T, dAqk^T fp32 -> hi/lo bf16 tiles
     const int r = it >> 3, jj = it & 7;
     const float *a = W.tc_dat + (slot * kC + r) * kC + jj * 8;

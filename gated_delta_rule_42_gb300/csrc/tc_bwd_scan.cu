@@ -3,8 +3,9 @@
 // One CTA walks the chunks of one (sequence, value head) from last to first,
 // holding dh' -- the gradient of the chunk-END state -- in fp32 registers
 // (thread = key channel c, half the value columns), starting from dhT (or 0).
-// Per chunk, after the V-independent phases (a) and (b) of tc_common.cuh
-// (recomputed from q, k, g, beta), on tcgen05:
+// Per chunk, with the chunk-level tiles of phase (a) of tc_common.cuh rebuilt
+// from q, k, g, beta and the Aqk / A tiles saved by the forward recompute,
+// on tcgen05:
 //   dD^T = dO^T Aqk + dh'^T Khat^T        dD = Aqk^T dO + Khat dh'   (deltas' gradient)
 //   dX^T = dD^T A                         dX = A^T dD                (through A = (I+L)^-1)
 //   dh  <- diag(2^G_last) dh' + Qg^T dO - Bk^T dX                    (gradient of the chunk-start state)
@@ -13,8 +14,8 @@
 // commit log: "the kernel's reverse state-gradient recurrence").  Every
 // operand is read straight from the row-major tiles through K- or MN-major
 // descriptors.  For the per-chunk gradient kernel the scan stores, per chunk:
-// dh' (bf16 [K][V]), dD and dX (bf16 [64][V]) and A (bf16 [64][64]); at the
-// start of the sequence it writes dh0 (fp32).
+// dh' (bf16 [K][V]) and dD, dX (bf16 [64][V]); at the start of the sequence it
+// writes dh0 (fp32).
 #include "tc_common.cuh"
 
 namespace kda {
@@ -68,30 +69,34 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
     }
   }
 
+  // the saved Aqk and A tiles of one chunk (16 KB, verbatim) from the forward recompute
+  auto load_aqk_a = [&](int cidx) {
+    const unsigned char *src = W.tc_aqk_a + ((size_t)cidx * HV + j) * 16384;
+    for (int it = tid; it < 1024; it += kThr) cp16(sbase + OFF_AQK + it * 16, src + it * 16);
+  };
   if (si.w > 0) {
-    const int4 chl = W.chunk[si.z + si.w - 1];
-    load_kqg(P, sm, chl.y, chl.z, j, h, betab, true);
-    load_rows(sbase + OFF_VRAW, dO, chl.y, chl.z, HV, j);
+    const int2 chl = chunk_span(si, si.w - 1);
+    load_kqg(P, sm, chl.x, chl.y, j, h, betab, true);
+    load_rows(sbase + OFF_VRAW, dO, chl.x, chl.y, HV, j);
+    load_aqk_a(si.z + si.w - 1);
     cp_commit();
   }
 
   for (int ci = si.w - 1; ci >= 0; --ci) {
     const int cidx = si.z + ci;
-    const int4 ch = W.chunk[cidx];
-    const int len = ch.z;
+    const int len = chunk_span(si, ci).y;
     const int buf = (si.w - 1 - ci) & 1;
     const float *beta = betab + buf * kC;
     const size_t slot = (size_t)cidx * HV + j;
     cp_wait_all();
     __syncthreads();
 
-    phase_a<true>(sm, len, beta);
+    phase_a<true, false>(sm, len, beta);
     if (ci > 0) {
-      const int4 pv = W.chunk[cidx - 1];
-      load_kqg(P, sm, pv.y, pv.z, j, h, betab + (buf ^ 1) * kC, true);
+      const int2 pv = chunk_span(si, ci - 1);
+      load_kqg(P, sm, pv.x, pv.y, j, h, betab + (buf ^ 1) * kC, true);
       cp_commit();
     }
-    phase_b<true>(sm, beta);
 
     // ---------------- (c) ----------------
     {
@@ -104,12 +109,6 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
         const uint4 u = pack8(t);
         *reinterpret_cast<uint4 *>(DH + sw_chunk(cown, 8 * vhalf + x8, kD)) = u;
         *reinterpret_cast<uint4 *>(W.tc_dh + (slot * kD + cown) * kD + 64 * vhalf + 8 * x8) = u;
-      }
-      // A for the per-chunk kernel, row-major bf16 [64][64]
-      for (int e = tid; e < kC * 8; e += kThr) {
-        const int r = e >> 3, jj = e & 7;
-        *reinterpret_cast<uint4 *>(W.tc_A + (slot * kC + r) * kC + jj * 8) =
-            *reinterpret_cast<const uint4 *>(sm + OFF_AM + sw_chunk(r, jj, kC));
       }
     }
     fence_async_smem();
@@ -204,9 +203,10 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
     fence_before();
     __syncthreads();
     fence_after();
-    if (ci > 0) {  // dO of this chunk consumed
-      const int4 pv = W.chunk[cidx - 1];
-      load_rows(sbase + OFF_VRAW, dO, pv.y, pv.z, HV, j);
+    if (ci > 0) {  // dO, Aqk and A of this chunk consumed
+      const int2 pv = chunk_span(si, ci - 1);
+      load_rows(sbase + OFF_VRAW, dO, pv.x, pv.y, HV, j);
+      load_aqk_a(cidx - 1);
       cp_commit();
     }
   }

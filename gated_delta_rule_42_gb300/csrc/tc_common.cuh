@@ -52,6 +52,9 @@ constexpr int V_GL = 0, V_GAML = 1, V_GREF = 2, V_EREF = 6, V_D = 10, V_LAM = 16
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 __device__ __forceinline__ void st_zero16(uint32_t dst) {
@@ -106,20 +109,33 @@ __device__ __forceinline__ void load_gate(uint32_t tile, const float *g, int t0,
   }
 }
 
-// k, q (optional), g and beta of one chunk.
+// First token and length of chunk ci of a sequence whose table entry is
+// si = (first token, length, first chunk, chunk count): computed, not loaded,
+// so the sequential kernels never wait on the chunk table.
+__device__ __forceinline__ int2 chunk_span(const int4 &si, int ci) {
+  const int t = kC * ci;
+  return make_int2(si.x + t, min(kC, si.y - t));
+}
+
+// k, q (optional), g and beta of one chunk, all asynchronous (a plain load of
+// beta would stall its threads for a DRAM round trip in the middle of a chunk).
 __device__ __forceinline__ void load_kqg(const Problem &P, unsigned char *sm, int t0, int len, int j,
                                          int h, float *beta_dst, bool with_q) {
   const uint32_t base = smem_u32(sm);
   load_rows(base + OFF_KRAW, (const __nv_bfloat16 *)P.k, t0, len, P.H, h);
   if (with_q) load_rows(base + OFF_QRAW, (const __nv_bfloat16 *)P.q, t0, len, P.H, h);
   load_gate(base + OFF_GRAW, P.g, t0, len, P.HV, j);
-  if (threadIdx.x < kC) beta_dst[threadIdx.x] = threadIdx.x < len ? P.beta[(size_t)(t0 + threadIdx.x) * P.HV + j] : 0.f;
+  if (threadIdx.x < kC) {
+    if (threadIdx.x < len) cp4(smem_u32(beta_dst + threadIdx.x), P.beta + (size_t)(t0 + threadIdx.x) * P.HV + j);
+    else beta_dst[threadIdx.x] = 0.f;
+  }
 }
 
 // Phase (a).  Needs the k (and q) staging tiles, the gate tile and beta of the
 // chunk; ends with a __syncthreads.  Writes G (in place), the vectors, and the
-// tiles Kr, Kc, Bk, Khat (and Qr, Qg when kQ).
-template <bool kQ>
+// tiles Bk, Khat (and Qg when kQ); with kGram also the decay tiles Kr, Kc (and
+// Qr) that the Gram blocks of phase (b) need.
+template <bool kQ, bool kGram = true>
 __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float *beta) {
   const int tid = threadIdx.x;
   float *G = (float *)(sm + OFF_GRAW);
@@ -184,10 +200,10 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       const float br = beta[r];
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
-      *reinterpret_cast<uint4 *>(U + U_KR + off) = pack8(o);
+      if (kGram) *reinterpret_cast<uint4 *>(U + U_KR + off) = pack8(o);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
-      *reinterpret_cast<uint4 *>(U + U_KC + off) = pack8(o);
+      if (kGram) *reinterpret_cast<uint4 *>(U + U_KC + off) = pack8(o);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * e1[e] * eref[e];
       *reinterpret_cast<uint4 *>(sm + OFF_BK + off) = pack8(o);
@@ -197,7 +213,7 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       if (kQ) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
-        *reinterpret_cast<uint4 *>(U + U_QR + off) = pack8(o);
+        if (kGram) *reinterpret_cast<uint4 *>(U + U_QR + off) = pack8(o);
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] *= eref[e];
         *reinterpret_cast<uint4 *>(sm + OFF_QG + off) = pack8(o);

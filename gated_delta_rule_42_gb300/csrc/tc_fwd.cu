@@ -17,8 +17,9 @@
 // state held on chip across chunks as in the recurrent_kda kernel of "kda in
 // torchtitan (training)" (pytorch/torchtitan PR #4164).
 //
-// In "states" mode (no output) the kernel writes the chunk-start states h_c
-// (bf16, [chunk][HV][K][V]) for the backward pass instead.
+// In "states" mode (no output) the kernel saves, per chunk, what the backward
+// needs from the forward recompute: the chunk-start state h_c (bf16 row-major
+// [K][V]) and the swizzled tiles Aqk, A, X^T and D^T, copied verbatim.
 #include "tc_common.cuh"
 
 namespace kda {
@@ -33,7 +34,6 @@ constexpr uint32_t TMEM_COLS = 256;  // [0,64) X'^T / O^T, [64,128) D^T, [128,25
 struct FwdArgs {
   __nv_bfloat16 *o;   // [B*T][HV][V] or null
   float *hT;          // [N][HV][K][V] or null
-  __nv_bfloat16 *hs;  // chunk-start states [chunk][HV][K][V] (states mode)
   int *err;           // device error flag (a bounded wait gave up)
 };
 
@@ -79,27 +79,33 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
   }
 
   if (si.w > 0) {
-    const int4 ch0 = W.chunk[si.z];
-    load_kqg(P, sm, ch0.y, ch0.z, j, h, betab, kOut);
-    load_rows(sbase + OFF_VRAW, (const __nv_bfloat16 *)P.v, ch0.y, ch0.z, HV, j);
+    const int2 ch0 = chunk_span(si, 0);
+    load_kqg(P, sm, ch0.x, ch0.y, j, h, betab, true);
+    load_rows(sbase + OFF_VRAW, (const __nv_bfloat16 *)P.v, ch0.x, ch0.y, HV, j);
     cp_commit();
   }
 
   for (int ci = 0; ci < si.w; ++ci) {
     const int cidx = si.z + ci;
-    const int4 ch = W.chunk[cidx];
-    const int t0 = ch.y, len = ch.z;
+    const int2 ch = chunk_span(si, ci);
+    const int t0 = ch.x, len = ch.y;
+    const size_t slot = (size_t)cidx * HV + j;
     const float *beta = betab + (ci & 1) * kC;
     cp_wait_all();
     __syncthreads();
 
-    phase_a<kOut>(sm, len, beta);
+    phase_a<true>(sm, len, beta);
     if (ci + 1 < si.w) {  // staging k, q, g consumed: prefetch the next chunk's
-      const int4 nx = W.chunk[cidx + 1];
-      load_kqg(P, sm, nx.y, nx.z, j, h, betab + ((ci + 1) & 1) * kC, kOut);
+      const int2 nx = chunk_span(si, ci + 1);
+      load_kqg(P, sm, nx.x, nx.y, j, h, betab + ((ci + 1) & 1) * kC, true);
       cp_commit();
     }
-    phase_b<kOut>(sm, beta);
+    phase_b<true>(sm, beta);
+    if (!kOut) {  // Aqk and A tiles (adjacent, 16 KB) for the backward, verbatim
+      const uint4 *src = (const uint4 *)(sm + OFF_AQK);
+      uint4 *dst = (uint4 *)(W.tc_aqk_a + slot * 16384);
+      for (int e = tid; e < 1024; e += kThr) dst[e] = src[e];
+    }
 
     // ---------------- (c) state chain on tcgen05 ----------------
     {
@@ -111,8 +117,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
         for (int e = 0; e < 8; ++e) t[e] = hreg[8 * x8 + e];
         const uint4 u = pack8(t);
         *reinterpret_cast<uint4 *>(H + sw_chunk(cown, 8 * vhalf + x8, kD)) = u;
-        if (!kOut)
-          *reinterpret_cast<uint4 *>(args.hs + (((size_t)cidx * HV + j) * kD + cown) * kD + 64 * vhalf + 8 * x8) = u;
+        if (!kOut) *reinterpret_cast<uint4 *>(W.tc_hs + (slot * kD + cown) * kD + 64 * vhalf + 8 * x8) = u;
       }
     }
     fence_async_smem();
@@ -149,9 +154,14 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     fence_before();
     __syncthreads();
     fence_after();
+    if (!kOut) {  // X^T tile for the backward, verbatim
+      const uint4 *src = (const uint4 *)(U + U_XT);
+      uint4 *dst = (uint4 *)(W.tc_xt + slot * 16384);
+      for (int e = tid; e < 1024; e += kThr) dst[e] = src[e];
+    }
     if (ci + 1 < si.w) {  // v of this chunk consumed
-      const int4 nx = W.chunk[cidx + 1];
-      load_rows(sbase + OFF_VRAW, (const __nv_bfloat16 *)P.v, nx.y, nx.z, HV, j);
+      const int2 nx = chunk_span(si, ci + 1);
+      load_rows(sbase + OFF_VRAW, (const __nv_bfloat16 *)P.v, nx.x, nx.y, HV, j);
       cp_commit();
     }
     if (tid == 0) {  // D^T[v][r] = sum_i X^T[v][i] A[r][i]   (M=128 v, N=64 r, K=64 i)
@@ -179,6 +189,11 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     fence_before();
     __syncthreads();
     fence_after();
+    if (!kOut) {  // D^T tile for the backward, verbatim
+      const uint4 *src = (const uint4 *)(U + U_XT);
+      uint4 *dst = (uint4 *)(W.tc_dt + slot * 16384);
+      for (int e = tid; e < 1024; e += kThr) dst[e] = src[e];
+    }
     if (tid == 0) {
       if (kOut) {  // O^T[v][r] = sum_c h[c][v] Qg[r][c] + sum_i D^T[v][i] Aqk[r][i]
         const uint32_t id = idesc(128, 64, 1, 0), id2 = idesc(128, 64, 0, 0);
@@ -243,13 +258,13 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
 
 }  // namespace
 
-cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, void *hstates,
+cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, bool states,
                        int *err, cudaStream_t s) {
   cudaError_t e = launch_chunk_map(P, W, s);
   if (e != cudaSuccess || P.N == 0) return e;
-  FwdArgs a{(__nv_bfloat16 *)o, hT, (__nv_bfloat16 *)hstates, err};
+  FwdArgs a{(__nv_bfloat16 *)o, hT, err};
   const dim3 grid(P.N, P.HV);
-  if (hstates != nullptr) {
+  if (states) {
     e = cudaFuncSetAttribute(kda_fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
