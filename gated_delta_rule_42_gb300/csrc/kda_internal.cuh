@@ -54,7 +54,7 @@ struct Workspace {
   __nv_bfloat16 *tc_dx;     // [slot][64][V] dX = A^T dD
   float *tc_dqg;           // [slot][64][K] dO h^T
   float *tc_dbk;           // [slot][64][K] -dX h^T
-  float *tc_dkh;           // [slot][K][64] dKhat^T
+  float *tc_dkh;           // [slot][64][K] dKhat
   float *tc_dat;           // [slot][64][64] dA^T
   float *tc_dqkt;          // [slot][64][64] dAqk^T (unmasked)
   float *tc_dbx;           // [slot][64] sum_v dX v

@@ -33,7 +33,7 @@ constexpr uint32_t C_G = 0;          // G fp32 [64][132]
 constexpr uint32_t C_VEC = 33792;    // vectors (20 x 128 fp32)
 constexpr uint32_t C_BETA = 44032;   // beta [64]
 constexpr uint32_t C_RB = 44288;     // dbeta partials [2][64]
-constexpr uint32_t C_RC = 44800;     // column-sum partials [4][128]
+constexpr uint32_t C_RC = 44800;     // prefetched d(2^G_last) [128] and sum_v dX v [64]
 constexpr uint32_t C_KR = 47104;     // Kr  hi [64][128] | lo (+16 KB)
 constexpr uint32_t C_QR = 79872;     // Qr  hi | lo
 constexpr uint32_t C_KC = 112640;    // Kc  hi | lo
@@ -43,10 +43,20 @@ constexpr uint32_t C_DQK = 169984;   // dAqk^T [64 i][64 r] hi | lo
 constexpr uint32_t C_XB = 186368;    // X = beta dL [64 r][64 i] hi | lo
 constexpr uint32_t C_T = 202752;     // T = A^T dA [64 r][64 m] hi | lo
 constexpr uint32_t LO128 = 16384, LO64 = 8192;
-// after the chain products: dG split into Q (no exact cancellation) and P (its
-// chunk sum is exactly zero), fp32 [64][128] each, over the dead Kr / Qr tiles
-constexpr uint32_t C_DQS = C_KR;
-constexpr uint32_t C_DPS = C_QR;
+// after the pairwise chains (A, dL, dAqk, X and T dead): staging of the fp32
+// products of one 64-column pass, [64][PST_LD] each, then the per-block column
+// totals of the dg scan; d(2^G_last) and sum_v dX v are prefetched into the
+// dead T tile right after dL.
+constexpr uint32_t PST_LD = 68;                  // padded row stride (floats): conflict-free float2 reads
+constexpr uint32_t PST_BYTES = 64 * PST_LD * 4;  // 17408
+constexpr uint32_t C_PST = C_A;                  // dQg | dBk | dKhat staging (3 x 17408)
+constexpr uint32_t SQ_LD = 36;                   // row stride (floats) of the dG group tiles
+constexpr uint32_t C_SQ = C_PST + 3 * PST_BYTES;  // Q part of dG, one 32-column group [64][SQ_LD]
+constexpr uint32_t C_SP = C_SQ + 64 * SQ_LD * 4;  // P part
+constexpr uint32_t C_TOT = C_SP + 64 * SQ_LD * 4; // segment totals of Q, P [8][32] each; block totals of the Khat column term [4][32]
+constexpr uint32_t C_DGL = C_RC;                  // d(2^G_last) [128]
+constexpr uint32_t C_DBX = C_RC + 512;            // sum_v dX v [64]
+static_assert(C_TOT + (8 + 8 + 4) * 32 * 4 <= 219136, "group scratch overflows the map");
 constexpr uint32_t C_SMEM = 219136 + 1024;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -124,10 +134,9 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
   float *vec = (float *)(sm + C_VEC);
   float *beta = (float *)(sm + C_BETA);
   float *rb = (float *)(sm + C_RB);
-  float *rc = (float *)(sm + C_RC);
-  float *dQs = (float *)(sm + C_DQS), *dPs = (float *)(sm + C_DPS);
   const __nv_bfloat16 *kin = (const __nv_bfloat16 *)P.k, *qin = (const __nv_bfloat16 *)P.q;
   constexpr float qscale = 0.08838834764831845f;
+  KDA_PT_DECL;
 
   // ---- loads ----
   load_gate(sbase + C_G, P.g, t0, len, HV, j);
@@ -139,11 +148,23 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
     if (tid < len) cp4(smem_u32(beta + tid), P.beta + (size_t)(t0 + tid) * HV + j);
     else beta[tid] = 0.f;
   }
+  // Staged asynchronously in tiles that are written only later, so that no
+  // thread waits on a plain global load: dA^T, dAqk^T (fp32) in the Kr tile;
+  // raw k, q rows in the lo halves of Kc and Qr -- the decay-tile pass reads
+  // each 16-byte chunk there before the same thread overwrites it.
+  for (int it = tid; it < kC * 16; it += kThr) {
+    cp16(sbase + C_KR + it * 16, W.tc_dat + slot * kC * kC + it * 4);
+    cp16(sbase + C_KR + LO128 + it * 16, W.tc_dqkt + slot * kC * kC + it * 4);
+  }
+  load_rows(sbase + C_KC + LO128, kin, t0, len, H, h);
+  load_rows(sbase + C_QR + LO128, qin, t0, len, H, h);
   cp_commit();
+  cp_wait_all();
+  __syncthreads();
   for (int it = tid; it < kC * 8; it += kThr) {  // dA^T, dAqk^T fp32 -> hi/lo bf16 tiles
     const int r = it >> 3, jj = it & 7;
-    const float *a = W.tc_dat + (slot * kC + r) * kC + jj * 8;
-    const float *b = W.tc_dqkt + (slot * kC + r) * kC + jj * 8;
+    const float *a = (const float *)(sm + C_KR) + r * kC + jj * 8;
+    const float *b = (const float *)(sm + C_KR + LO128) + r * kC + jj * 8;
     float x[8], y[8];
 #pragma unroll
     for (int e = 0; e < 8; e += 4) {
@@ -162,8 +183,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
     *reinterpret_cast<uint4 *>(sm + C_DQK + off) = hi;
     *reinterpret_cast<uint4 *>(sm + C_DQK + LO64 + off) = lo;
   }
-  cp_wait_all();
-  __syncthreads();
+  KDA_PT(0);  // (the barrier after the cumsum also orders the Kr staging reads before the Kr writes)
 
   // ---- G, block references, decay tiles Kr, Qr, Kc (hi/lo) ----
   if (tid < kD) {
@@ -197,6 +217,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
   }
   __syncthreads();
+  KDA_PT(1);
   {
     const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
     float gref[8];
@@ -208,13 +229,8 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       const int r = rg * 4 + rr;
       const uint32_t off = sw_chunk(r, jj, kC);
       float kv[8], qv[8], o[8], e1[8], e2[8];
-      uint4 ku = make_uint4(0, 0, 0, 0), qu = make_uint4(0, 0, 0, 0);
-      if (r < len) {
-        ku = *reinterpret_cast<const uint4 *>(kin + ((size_t)(t0 + r) * H + h) * kD + c0);
-        qu = *reinterpret_cast<const uint4 *>(qin + ((size_t)(t0 + r) * H + h) * kD + c0);
-      }
-      unpack8(ku, kv);
-      unpack8(qu, qv);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + C_KC + LO128 + off), kv);  // raw k, q (zero past len)
+      unpack8(*reinterpret_cast<const uint4 *>(sm + C_QR + LO128 + off), qv);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float g = G[r * kGLD + c0 + e];
@@ -241,6 +257,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
   }
   __syncthreads();
 
+  KDA_PT(2);
   // ---- T = A^T dA  (T[r][m] = sum_i' A[i'][r] dA[i'][m]; dA[i'][m] = dA^T[m][i']) ----
   const int mt = warp >> 1, nh = warp & 1;  // 16-row block, 32-column half
   {
@@ -269,6 +286,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       }
   }
   __syncthreads();
+  KDA_PT(3);
   // ---- dL = -tril_{-1}(T A^T); X = beta dL ----
   {
     float acc[4][4] = {};
@@ -299,7 +317,11 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       }
   }
   __syncthreads();
+  if (tid < 32) cp16(sbase + C_DGL + tid * 16, W.tc_dgl + slot * kD + tid * 4);  // T is dead
+  else if (tid < 48) cp16(sbase + C_DBX + (tid - 32) * 16, W.tc_dbx + slot * kC + (tid - 32) * 4);
+  cp_commit();
 
+  KDA_PT(4);
   // ---- pairwise chains: warp owns rows 16B..16B+15 (as r and as i), columns ch0 .. ch0+63 ----
   // Block-pair products are formed in a temporary, scaled by the per-channel
   // factor D_RI in fp32, and added to the accumulators.
@@ -359,116 +381,186 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       }
     }
   }
-  __syncthreads();  // every warp is done with the decay tiles: Kr / Qr become the dG tiles
+  __syncthreads();  // every warp is done with the chain tiles: A .. X become the product staging
+  KDA_PT(5);
 
-  // ---- assembly (fragment element (r, c)) ----
-  const float *dqg = W.tc_dqg + slot * kC * kD, *dbk = W.tc_dbk + slot * kC * kD;
-  const float *dkh = W.tc_dkh + slot * kD * kC;  // [c][r]
+  // ---- assembly (fragment element (r, c)), in two passes of 32 columns per warp ----
+  // Per pass the products dQg, dBk, dKhat of the pass's 64 columns are staged
+  // in shared memory with one batch of asynchronous copies.  Raw k and q are
+  // not re-read: every term that needs them is a product with a decay factor
+  // that the hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2 already hold.
+  // dg = reverse cumsum of dG over the chunk runs as warp-shuffle scans over
+  // each warp's 16 rows plus per-block totals exchanged through shared memory.
+  float *sQ = (float *)(sm + C_SQ), *sP = (float *)(sm + C_SP);
+  float *totQ = (float *)(sm + C_TOT), *totP = totQ + 8 * 32, *totC = totP + 8 * 32;
+  const float *dglv = (const float *)(sm + C_DGL), *dbxv = (const float *)(sm + C_DBX);
+  const int i8 = lane >> 2, l4 = lane & 3, mid = len >> 1;
   float bpart[2] = {0.f, 0.f};
-  float cpart[8][2];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    cpart[nt][0] = cpart[nt][1] = 0.f;
+  for (int p = 0; p < 2; ++p) {
+    if (p == 1) __syncthreads();  // every warp is done with pass 0's staging
+    for (int it = tid; it < 3 * 1024; it += kThr) {
+      const int prod = it >> 10, w = it & 1023, r = w >> 4, seg = (w >> 3) & 1, jj = w & 7;
+      const float *src = (prod == 0 ? W.tc_dqg : prod == 1 ? W.tc_dbk : W.tc_dkh) +
+                         (slot * kC + r) * kD + 64 * seg + 32 * p + 4 * jj;
+      cp16(sbase + C_PST + (uint32_t)prod * PST_BYTES + (uint32_t)(r * PST_LD + 32 * seg + 4 * jj) * 4u, src);
+    }
+    cp_commit();
+    cp_wait_all();
+    __syncthreads();
+    KDA_PT(9);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int r = 16 * Bk + (lane >> 2) + 8 * hh;
-      const int c = ch0 + 8 * nt + (lane & 3) * 2;
-      const float br = beta[r];
-      float2 kv = make_float2(0.f, 0.f), qv = make_float2(0.f, 0.f);
-      if (r < len) {
-        kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(kin + ((size_t)(t0 + r) * H + h) * kD + c));
-        qv = unpack_bf16(*reinterpret_cast<const uint32_t *>(qin + ((size_t)(t0 + r) * H + h) * kD + c));
-      }
-      const float2 vq = *reinterpret_cast<const float2 *>(dqg + r * kD + c);
-      const float2 vb = *reinterpret_cast<const float2 *>(dbk + r * kD + c);
-      const float vk[2] = {dkh[c * kC + r], dkh[(c + 1) * kC + r]};
-      float dq2[2], dk2[2];
+    for (int gg = 0; gg < 2; ++gg) {
+      const int g = 2 * p + gg;
+      float qv[2][2][2], pv[2][2][2], cq[2][2];  // [nt of the group][hh][u], column sums [nt][u]
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int cc = c + u;
-        const float kk = u ? kv.y : kv.x, qq = (u ? qv.y : qv.x) * qscale;
-        const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = vk[u];
-        const float g = G[r * kGLD + cc], gref = vec[(V_GREF + Bk) * kD + cc];
-        const float e1 = exp2f(g - gref), e2 = exp2f(gref - g);
-        const float gam = e1 * vec[(V_EREF + Bk) * kD + cc], kh = e2 * vec[(V_LAM + Bk) * kD + cc];
-        const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
-        const float xI = xi[nt][2 * hh + u], yI = yi[nt][2 * hh + u];
-        dq2[u] = dQg * gam + e1 * yR;
-        dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * (xI + yI);
-        // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
-        dQs[r * kD + cc] = kLn2 * (dQg * qq * gam + br * dBk * kk * gam);
-        dPs[r * kD + cc] = kLn2 * (br * kk * e1 * xR + qq * e1 * yR - kk * e2 * (xI + yI) - dKh * kk * kh);
-        bpart[hh] += dBk * kk * gam + kk * e1 * xR;
-        cpart[nt][u] += dKh * kk * kh;
-      }
-      if (r < len) {
-        const size_t tok = (size_t)(t0 + r);
-        if (args.partial) {
-          float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
-          *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
-          *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
-        } else {
-          __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
-          __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
-          *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
-          *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
+      for (int ntl = 0; ntl < 2; ++ntl) {
+        const int nt = 2 * g + ntl;
+        const int c = ch0 + 8 * nt + 2 * l4;
+        const int lc = 32 * (ch0 >> 6) + 8 * nt - 32 * p + 2 * l4;  // column in the staging
+        const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
+        const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
+        const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
+        cq[ntl][0] = cq[ntl][1] = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * Bk + i8 + 8 * hh;
+          const float br = beta[r];
+          const uint32_t so = (uint32_t)(r * PST_LD + lc) * 4u;
+          const float2 vq = *reinterpret_cast<const float2 *>(sm + C_PST + so);
+          const float2 vb = *reinterpret_cast<const float2 *>(sm + C_PST + PST_BYTES + so);
+          const float2 vk = *reinterpret_cast<const float2 *>(sm + C_PST + 2 * PST_BYTES + so);
+          const uint32_t to = sw_off(r, c, kC);
+          const float2 krh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + to));
+          const float2 krl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + LO128 + to));
+          const float2 qrh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + to));
+          const float2 qrl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + LO128 + to));
+          const float2 kch = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + to));
+          const float2 kcl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + LO128 + to));
+          const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
+          float dq2[2], dk2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float Kr = u ? krh.y + krl.y : krh.x + krl.x;  // k e1
+            const float Qr = u ? qrh.y + qrl.y : qrh.x + qrl.x;  // q~ e1
+            const float Kc = u ? kch.y + kcl.y : kch.x + kcl.x;  // k e2
+            const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = u ? vk.y : vk.x;
+            const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
+            const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
+            const float e1 = exp2f(gg_ - gref), e2 = exp2f(gref - gg_);
+            const float gam = e1 * eref, kh = e2 * lam;
+            const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
+            const float xI = xi[nt][2 * hh + u], yI = yi[nt][2 * hh + u];
+            dq2[u] = dQg * gam + e1 * yR;
+            dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * (xI + yI);
+            // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
+            const bool in = r < len;
+            qv[ntl][hh][u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
+            pv[ntl][hh][u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * (xI + yI) - dKh * Kc * lam) : 0.f;
+            bpart[hh] += dBk * Kr * eref + Kr * xR;
+            cq[ntl][u] += dKh * Kc * lam;
+          }
+          if (r < len) {
+            const size_t tok = (size_t)(t0 + r);
+            if (args.partial) {
+              float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
+              *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
+              *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
+            } else {
+              __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
+              __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
+              *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
+              *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
+            }
+          }
         }
       }
+      KDA_PT(10);
+      // dG of this group's 32 columns -> shared memory, then the column scans
+#pragma unroll
+      for (int ntl = 0; ntl < 2; ++ntl) {
+        const int lc = 16 * (ch0 >> 6) + 8 * ntl + 2 * l4;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * Bk + i8 + 8 * hh;
+          *reinterpret_cast<float2 *>(sQ + r * SQ_LD + lc) = make_float2(qv[ntl][hh][0], qv[ntl][hh][1]);
+          *reinterpret_cast<float2 *>(sP + r * SQ_LD + lc) = make_float2(pv[ntl][hh][0], pv[ntl][hh][1]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {  // column sums of dKhat k khat over the warp's 16 rows
+          float cs = cq[ntl][u];
+          cs += __shfl_xor_sync(0xffffffffu, cs, 4);
+          cs += __shfl_xor_sync(0xffffffffu, cs, 8);
+          cs += __shfl_xor_sync(0xffffffffu, cs, 16);
+          if (i8 == 0) totC[Bk * 32 + lc + u] = cs;
+        }
+      }
+      __syncthreads();
+      KDA_PT(11);
+      {  // thread: one column of the group, one 8-row segment (warp = segment)
+        const int col = tid & 31, seg = warp;
+        const int cc = (col < 16) ? 16 * g + col : 64 + 16 * g + (col - 16);
+        float q8[8], p8[8], tq = 0.f, tp = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          q8[k] = sQ[(8 * seg + k) * SQ_LD + col];
+          p8[k] = sP[(8 * seg + k) * SQ_LD + col];
+          tq += q8[k];
+          tp += p8[k];
+        }
+        totQ[seg * 32 + col] = tq;
+        totP[seg * 32 + col] = tp;
+        __syncthreads();
+        float aq = 0.f, aps = 0.f, app = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          const float a = totQ[s2 * 32 + col], b = totP[s2 * 32 + col];
+          if (s2 > seg) { aq += a; aps += b; }
+          if (s2 < seg) app += b;
+        }
+        const float ks = totC[col] + totC[32 + col] + totC[64 + col] + totC[96 + col];
+        // dg_t = sum_{s>=t} dG_s: the Q part and the carried-state decay term
+        // from the chunk end; the zero-sum P part from whichever end is nearer
+        // (sum_{s>=t} P_s = -sum_{s<t} P_s, the Khat column sum counted at the
+        // last row), halving the cancelling terms it sums.
+        const float carried = kLn2 * vec[V_GAML * kD + cc] * dglv[cc];
+        float pre[8];
+        pre[0] = app;
+#pragma unroll
+        for (int k = 1; k < 8; ++k) pre[k] = pre[k - 1] + p8[k - 1];
+        float qs = aq, ps = aps + kLn2 * ks;
+#pragma unroll
+        for (int k = 7; k >= 0; --k) {
+          const int r = 8 * seg + k;
+          qs += q8[k];
+          ps += p8[k];
+          if (r < len)
+            args.dg[((size_t)(t0 + r) * HV + j) * kD + cc] = qs + carried + (r >= mid ? ps : -pre[k]);
+        }
+      }
+      KDA_PT(12);
     }
   }
+  KDA_PT(6);
   // dbeta partials: reduce over the 4 lanes sharing a row, then per column half
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     float v = bpart[hh];
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
-    if ((lane & 3) == 0) rb[(warp & 1) * kC + 16 * Bk + (lane >> 2) + 8 * hh] = v;
+    if (l4 == 0) rb[(warp & 1) * kC + 16 * Bk + i8 + 8 * hh] = v;
   }
-  // column sums of dKhat k khat over this warp's 16 rows
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float v = cpart[nt][u];
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
-      v += __shfl_xor_sync(0xffffffffu, v, 16);
-      if (lane < 4) rc[Bk * kD + ch0 + 8 * nt + lane * 2 + u] = v;
-    }
   __syncthreads();
+  KDA_PT(7);
   if (tid < kC && tid < len)
-    args.dbeta[(size_t)(t0 + tid) * HV + j] = W.tc_dbx[slot * kC + tid] + rb[tid] + rb[kC + tid];
-  if (tid < kD) {
-    // dg_t = sum_{s>=t} dG_s.  The Q part and the carried-state decay term
-    // accumulate from the chunk end; the zero-sum P part accumulates from
-    // whichever end is nearer (sum_{s>=t} P_s = -sum_{s<t} P_s), halving the
-    // number of cancelling terms each dg sums.
-    const int c = tid;
-    const float khsum = kLn2 * (rc[c] + rc[kD + c] + rc[2 * kD + c] + rc[3 * kD + c]);
-    const float carried = kLn2 * vec[V_GAML * kD + c] * W.tc_dgl[slot * kD + c];
-    const int mid = len >> 1;
-    float pf = 0.f;
-    for (int r = 0; r < mid; ++r) {  // dg_r for r < mid takes -sum_{s<r} P_s
-      const float p = dPs[r * kD + c];
-      dPs[r * kD + c] = -pf;
-      pf += p;
-    }
-    float qs = 0.f, ps = khsum;  // sum_{s>=t} P_s includes the Khat column sum at the last row
-    for (int r = len - 1; r >= 0; --r) {
-      qs += dQs[r * kD + c];
-      float pr;
-      if (r >= mid) {
-        ps += dPs[r * kD + c];
-        pr = ps;
-      } else {
-        pr = dPs[r * kD + c];
-      }
-      args.dg[((size_t)(t0 + r) * HV + j) * kD + c] = qs + carried + pr;
-    }
-  }
+    args.dbeta[(size_t)(t0 + tid) * HV + j] = dbxv[tid] + rb[tid] + rb[kC + tid];
+  KDA_PT(8);
+  KDA_PT_FLUSH;
 }
 
 }  // namespace
+
+KDA_PT_EXPORT(kda_debug_chain_phase_cycles)
 
 cudaError_t tc_backward_chain(const Problem &P, const Workspace &W, void *dq, void *dk, float *dg,
                               float *dbeta, cudaStream_t s) {

@@ -182,11 +182,12 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_gemm_tc_kernel(Problem P, Wor
           *reinterpret_cast<float4 *>(dst + 32 * hx + e) =
               make_float4(sg * d[e], sg * d[e + 1], sg * d[e + 2], sg * d[e + 3]);
       }
-      // dKhat^T [c][r] (lane c, 64 columns r: warps half 0 -> r 0..31, half 1 -> r 32..63)
+      // dKhat^T in TMEM (lane c, 64 columns r: warps half 0 -> r 0..31, half 1 -> r 32..63),
+      // stored as dKhat [r][c]: one coalesced 128-byte row segment per warp store
       tmem_ld32(tq + 256u + (uint32_t)(32 * half), d);
-      float *dk2 = W.tc_dkh + (slot * kD + lrow) * kC + 32 * half;
+      float *dk2 = W.tc_dkh + (slot * kC + 32 * half) * kD + lrow;
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4 *>(dk2 + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+      for (int e = 0; e < 32; ++e) dk2[e * kD] = d[e];
       // Z: lanes 0..63 (i), cols 64..127 (r) = dA^T [i][r]; lanes 64..127, cols 0..63 = dAqk^T [i][r]
       const uint32_t zc = lrow < 64 ? 64u : 0u;
       tmem_ld32(tq + 384u + zc + (uint32_t)(32 * half), d);

@@ -25,6 +25,57 @@ namespace tc {
 
 using namespace umma;
 
+// Phase timing (compile with -DKDA_PHASE_TIMING): thread 0 of every block
+// adds the clock64 cycles since its previous stamp to a shared-memory slot i
+// (KDA_PT(i)); KDA_PT_FLUSH adds the slots to kda_phase_cycles (one copy per
+// translation unit, read back by the KDA_PT_EXPORT function), so the totals
+// are sums over all blocks.  Off by default; it skips no work.
+#ifdef KDA_PHASE_TIMING
+static __device__ long long kda_phase_cycles[32];
+static __shared__ long long kda_pt_acc[33];  // [32] = time of the last stamp
+#define KDA_PT_ON (threadIdx.x == 0)
+#define KDA_PT_DECL                                             \
+  do {                                                          \
+    if (KDA_PT_ON) {                                            \
+      for (int i_ = 0; i_ < 32; ++i_) kda_pt_acc[i_] = 0;       \
+      kda_pt_acc[32] = clock64();                               \
+    }                                                           \
+  } while (0)
+#define KDA_PT(i)                                   \
+  do {                                              \
+    if (KDA_PT_ON) {                                \
+      const long long now_ = clock64();             \
+      kda_pt_acc[i] += now_ - kda_pt_acc[32];       \
+      kda_pt_acc[32] = now_;                        \
+    }                                               \
+  } while (0)
+#define KDA_PT_FLUSH                                                            \
+  do {                                                                          \
+    if (KDA_PT_ON)                                                              \
+      for (int i_ = 0; i_ < 32; ++i_)                                           \
+        atomicAdd((unsigned long long *)&kda_phase_cycles[i_], (unsigned long long)kda_pt_acc[i_]); \
+  } while (0)
+#define KDA_PT_EXPORT(name)                                                                      \
+  extern "C" int name(long long *out, int reset) {                                               \
+    if (cudaMemcpyFromSymbol(out, tc::kda_phase_cycles, sizeof(long long) * 32) != cudaSuccess) \
+      return 1;                                                                                  \
+    static const long long z[32] = {};                                                           \
+    if (reset && cudaMemcpyToSymbol(tc::kda_phase_cycles, z, sizeof(z)) != cudaSuccess) return 1; \
+    return 0;                                                                                    \
+  }
+#else
+#define KDA_PT_DECL \
+  do {              \
+  } while (0)
+#define KDA_PT(i) \
+  do {            \
+  } while (0)
+#define KDA_PT_FLUSH \
+  do {               \
+  } while (0)
+#define KDA_PT_EXPORT(name)
+#endif
+
 constexpr int kC = 64;     // chunk
 constexpr int kD = 128;    // K = V
 constexpr int kThr = 256;  // 8 warps
@@ -142,37 +193,57 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
   float *vec = (float *)(sm + OFF_VEC);
   unsigned char *U = sm + OFF_U;
   constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
-  if (tid < kD) {
-    const int c = tid;
-    float col[kC];
+  {  // two threads per channel (adjacent lanes), 32 rows each
+    const int c = tid >> 1, hf = tid & 1, r0 = 32 * hf, lane = tid & 31;
+    float col[32];
     float s = 0.f;
 #pragma unroll
-    for (int r = 0; r < kC; ++r) col[r] = G[r * kGLD + c];
+    for (int k = 0; k < 32; ++k) col[k] = G[(r0 + k) * kGLD + c];
 #pragma unroll
-    for (int r = 0; r < kC; ++r) {
-      if (r < len) s += col[r];
-      col[r] = s;
+    for (int k = 0; k < 32; ++k) {
+      if (r0 + k < len) s += col[k];
+      col[k] = s;
     }
+    const float lo_total = __shfl_sync(0xffffffffu, s, lane & ~1);
+    const float add = hf ? lo_total : 0.f;
 #pragma unroll
-    for (int r = 0; r < kC; ++r) G[r * kGLD + c] = col[r];
-    const float gl = s;
-    vec[V_GL * kD + c] = gl;
-    vec[V_GAML * kD + c] = exp2f(gl);
+    for (int k = 0; k < 32; ++k) {
+      col[k] += add;
+      G[(r0 + k) * kGLD + c] = col[k];
+    }
+    const float gl = __shfl_sync(0xffffffffu, s + add, lane | 1);
+    // block references: rows 0, 16 (lower partner) and 32, 48 (upper partner)
+    const float ga = (r0 < len) ? col[0] : gl, gb = (r0 + 16 < len) ? col[16] : gl;
     float gref[4];
-#pragma unroll
-    for (int R = 0; R < 4; ++R) {
-      gref[R] = (16 * R < len) ? col[16 * R] : gl;
-      vec[(V_GREF + R) * kD + c] = gref[R];
-      vec[(V_EREF + R) * kD + c] = exp2f(gref[R]);
-      vec[(V_LAM + R) * kD + c] = exp2f(gl - gref[R]);
+    gref[0] = __shfl_sync(0xffffffffu, ga, lane & ~1);
+    gref[1] = __shfl_sync(0xffffffffu, gb, lane & ~1);
+    gref[2] = __shfl_sync(0xffffffffu, ga, lane | 1);
+    gref[3] = __shfl_sync(0xffffffffu, gb, lane | 1);
+    if (hf == 0) {
+      vec[V_GL * kD + c] = gl;
+      vec[V_GAML * kD + c] = exp2f(gl);
     }
-    int p = 0;
 #pragma unroll
-    for (int R = 1; R < 4; ++R)
-#pragma unroll
-      for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
+    for (int q = 0; q < 2; ++q) {  // this partner's own two references (ga, gb)
+      const int R = 2 * hf + q;
+      const float gr = q ? gb : ga;
+      vec[(V_GREF + R) * kD + c] = gr;
+      vec[(V_EREF + R) * kD + c] = exp2f(gr);
+      vec[(V_LAM + R) * kD + c] = exp2f(gl - gr);
+    }
+    // D_RI = 2^(gref_R - gref_I) for the pairs (1,0) (2,0) (2,1) | (3,0) (3,1) (3,2)
+    if (hf == 0) {
+      vec[(V_D + 0) * kD + c] = exp2f(gref[1] - gref[0]);
+      vec[(V_D + 1) * kD + c] = exp2f(gref[2] - gref[0]);
+      vec[(V_D + 2) * kD + c] = exp2f(gref[2] - gref[1]);
+    } else {
+      vec[(V_D + 3) * kD + c] = exp2f(gref[3] - gref[0]);
+      vec[(V_D + 4) * kD + c] = exp2f(gref[3] - gref[1]);
+      vec[(V_D + 5) * kD + c] = exp2f(gref[3] - gref[2]);
+    }
   }
   __syncthreads();
+  KDA_PT(1);
   // thread: 8 consecutive channels (one 16-byte chunk) of 4 consecutive rows
   {
     const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
@@ -222,6 +293,11 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
   }
   __syncthreads();
 }
+
+// fp32 [64][64] scratch of phase (b) (L, then A): columns XOR-swizzled by
+// 4 * (row % 8), so reads of one column across 8 rows and float4 reads of four
+// consecutive columns are both free of bank conflicts.
+__device__ __forceinline__ int fsw(int r, int c) { return r * kC + (c ^ ((r & 7) << 2)); }
 
 // Phase (b).  Needs the tiles of phase (a); ends with a __syncthreads.  Writes
 // the A tile (and the Aqk tile when kQ).  Clobbers the union region.
@@ -277,7 +353,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
         const float br = beta[r];
         const float l0 = (i < r) ? br * accL[nt][2 * hh] : 0.f;
         const float l1 = (i + 1 < r) ? br * accL[nt][2 * hh + 1] : 0.f;
-        *reinterpret_cast<float2 *>(Lf + r * kC + i) = make_float2(l0, l1);
+        *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
         if (kQ) {
           const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
           const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
@@ -287,6 +363,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     }
   }
   __syncthreads();
+  KDA_PT(4);
   float *Af = (float *)(U + U_AF);  // overwrites Kr (dead)
   float *Tf = (float *)(U + U_T);   // overwrites Qr (dead)
   if (warp < 4 && lane < 16) {
@@ -299,39 +376,50 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     for (int r = 1; r < 16; ++r) {
       float s = a[r];
 #pragma unroll
-      for (int m = 0; m < r; ++m) s = fmaf(-Lf[(16 * R + r) * kC + 16 * R + m], a[m], s);
+      for (int m = 0; m < r; ++m) s = fmaf(-Lf[fsw(16 * R + r, 16 * R + m)], a[m], s);
       a[r] = s;
     }
 #pragma unroll
-    for (int m = 0; m < 16; ++m) Af[(16 * R + m) * kC + 16 * R + i] = a[m];
+    for (int m = 0; m < 16; ++m) Af[fsw(16 * R + m, 16 * R + i)] = a[m];
   }
   for (int e = tid; e < 6 * 256; e += kThr) {  // strictly-upper blocks of A
     const int b = e >> 8, w = e & 255;
     const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2);
     const int I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
-    Af[(16 * R + (w >> 4)) * kC + 16 * I + (w & 15)] = 0.f;
+    Af[fsw(16 * R + (w >> 4), 16 * I + (w & 15))] = 0.f;
   }
   __syncthreads();
-  // off-diagonal blocks by sub-diagonal level: A_RI = -A_RR sum_{M=I}^{R-1} L_RM A_MI
+  KDA_PT(5);
+  // off-diagonal blocks by sub-diagonal level: A_RI = -A_RR sum_{M=I}^{R-1} L_RM A_MI,
+  // each thread a 1 x 4 row segment (one broadcast L value per four FMAs)
 #pragma unroll
   for (int lvl = 1; lvl < 4; ++lvl) {
     const int nb = 4 - lvl;
-    for (int e = tid; e < nb * 256; e += kThr) {
-      const int I = e >> 8, R = I + lvl, rr = (e >> 4) & 15, ii = e & 15;
-      float s = 0.f;
+    for (int e = tid; e < nb * 64; e += kThr) {
+      const int I = e >> 6, R = I + lvl, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int M = I; M < R; ++M)
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-          s = fmaf(Lf[(16 * R + rr) * kC + 16 * M + m], Af[(16 * M + m) * kC + 16 * I + ii], s);
-      Tf[(I * 16 + rr) * 16 + ii] = s;
+        for (int m = 0; m < 16; ++m) {
+          const float l = Lf[fsw(16 * R + rr, 16 * M + m)];
+          const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(16 * M + m, 16 * I + i4));
+          acc.x = fmaf(l, a.x, acc.x); acc.y = fmaf(l, a.y, acc.y);
+          acc.z = fmaf(l, a.z, acc.z); acc.w = fmaf(l, a.w, acc.w);
+        }
+      *reinterpret_cast<float4 *>(Tf + (I * 16 + rr) * 16 + i4) = acc;
     }
     __syncthreads();
-    for (int e = tid; e < nb * 256; e += kThr) {
-      const int I = e >> 8, R = I + lvl, rr = (e >> 4) & 15, ii = e & 15;
-      float s = 0.f;
+    for (int e = tid; e < nb * 64; e += kThr) {
+      const int I = e >> 6, R = I + lvl, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 16; ++m) s = fmaf(Af[(16 * R + rr) * kC + 16 * R + m], Tf[(I * 16 + m) * 16 + ii], s);
-      Af[(16 * R + rr) * kC + 16 * I + ii] = -s;
+      for (int m = 0; m < 16; ++m) {
+        const float l = Af[fsw(16 * R + rr, 16 * R + m)];
+        const float4 t = *reinterpret_cast<const float4 *>(Tf + (I * 16 + m) * 16 + i4);
+        acc.x = fmaf(l, t.x, acc.x); acc.y = fmaf(l, t.y, acc.y);
+        acc.z = fmaf(l, t.z, acc.z); acc.w = fmaf(l, t.w, acc.w);
+      }
+      *reinterpret_cast<float4 *>(Af + fsw(16 * R + rr, 16 * I + i4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
   }
@@ -339,10 +427,11 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     const int r = e >> 3, jj = e & 7;
     float x[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) x[t] = Af[r * kC + jj * 8 + t];
+    for (int t = 0; t < 8; ++t) x[t] = Af[fsw(r, jj * 8 + t)];
     *reinterpret_cast<uint4 *>(sm + OFF_AM + sw_chunk(r, jj, kC)) = pack8(x);
   }
   __syncthreads();
+  KDA_PT(6);
 }
 
 }  // namespace tc

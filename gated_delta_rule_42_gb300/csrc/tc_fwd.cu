@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
   const uint32_t tmem = *tslot;
   const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
   uint32_t phase = 0;
+  KDA_PT_DECL;
 
   float hreg[64];  // h[cown][64 * vhalf + x]
   {
@@ -93,13 +94,16 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     const float *beta = betab + (ci & 1) * kC;
     cp_wait_all();
     __syncthreads();
+    KDA_PT(0);
 
     phase_a<true>(sm, len, beta);
+    KDA_PT(2);
     if (ci + 1 < si.w) {  // staging k, q, g consumed: prefetch the next chunk's
       const int2 nx = chunk_span(si, ci + 1);
       load_kqg(P, sm, nx.x, nx.y, j, h, betab + ((ci + 1) & 1) * kC, true);
       cp_commit();
     }
+    KDA_PT(3);
     phase_b<true>(sm, beta);
     if (!kOut) {  // Aqk and A tiles (adjacent, 16 KB) for the backward, verbatim
       const uint4 *src = (const uint4 *)(sm + OFF_AQK);
@@ -124,6 +128,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     fence_before();
     __syncthreads();
     fence_after();
+    KDA_PT(8);
     const uint32_t aH = sbase + OFF_U + U_H, aXT = sbase + OFF_U + U_XT;
     if (tid == 0) {  // X'^T[v][r] = sum_c h[c][v] Bk[r][c]   (M=128 v, N=64 r, K=128 c)
       const uint32_t id = idesc(128, 64, 1, 0);
@@ -134,6 +139,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     bar_wait(bar, phase, args.err);
     phase ^= 1;
     fence_after();
+    KDA_PT(9);
     {  // X^T[v][r] = beta_r v[r][v] - X'^T[v][r]  -> bf16 tile [v][r]
       const int v = cown, r0 = 32 * vhalf;
       float d[32];
@@ -154,6 +160,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     fence_before();
     __syncthreads();
     fence_after();
+    KDA_PT(10);
     if (!kOut) {  // X^T tile for the backward, verbatim
       const uint4 *src = (const uint4 *)(U + U_XT);
       uint4 *dst = (uint4 *)(W.tc_xt + slot * 16384);
@@ -173,6 +180,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     bar_wait(bar, phase, args.err);
     phase ^= 1;
     fence_after();
+    KDA_PT(11);
     {  // D^T -> bf16 tile [v][r] (reuses the X^T tile)
       const int v = cown, r0 = 32 * vhalf;
       float d[32];
@@ -189,6 +197,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     fence_before();
     __syncthreads();
     fence_after();
+    KDA_PT(12);
     if (!kOut) {  // D^T tile for the backward, verbatim
       const uint4 *src = (const uint4 *)(U + U_XT);
       uint4 *dst = (uint4 *)(W.tc_dt + slot * 16384);
@@ -212,6 +221,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     bar_wait(bar, phase, args.err);
     phase ^= 1;
     fence_after();
+    KDA_PT(13);
     if (kOut) {  // O^T -> staging tile [r][v], then coalesced 16-byte stores
       const int v = cown, r0 = 32 * vhalf;
       float d[32];
@@ -233,6 +243,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     fence_before();
     __syncthreads();
     fence_after();
+    KDA_PT(14);
     if (kOut) {
       const uint4 *Ot = (const uint4 *)(U + U_O);
       for (int it = tid; it < len * 16; it += kThr) {
@@ -240,6 +251,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
         *reinterpret_cast<uint4 *>(args.o + ((size_t)(t0 + r) * HV + j) * kD + jj * 8) = Ot[r * 16 + jj];
       }
     }
+    KDA_PT(15);
   }
 
   if (args.hT != nullptr) {
@@ -254,9 +266,12 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     fence_after();
     tmem_free(tmem, TMEM_COLS);
   }
+  KDA_PT_FLUSH;
 }
 
 }  // namespace
+
+KDA_PT_EXPORT(kda_debug_fwd_phase_cycles)
 
 cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, bool states,
                        int *err, cudaStream_t s) {
