@@ -1,6 +1,7 @@
 // Internal definitions shared by the CUDA translation units of libkda.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and its enums (types only; the encoder is reached through the runtime)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -70,6 +71,17 @@ __device__ __forceinline__ void stf(float *p, int64_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16 *p, int64_t i, float x) {
   p[i] = __float2bfloat16_rn(x);
 }
+
+// TMA tensor maps of one call's per-token tensors, passed to the sequential
+// kernels as a __grid_constant__ parameter (tma.cu).  k, q: [Ttot][H][128]
+// bf16 and v (or dO): [Ttot][HV][128] bf16 as 64 x 64 boxes with the 128-byte
+// swizzle of the operand tiles; g: [Ttot][HV][128] fp32 as 64-row x 128 boxes.
+struct TmaMaps {
+  CUtensorMap k, q, v, g;
+};
+// Encodes the maps (v may be NULL: no map).  Fails without launching anything
+// if the driver rejects a map (e.g. a base pointer not 16-byte aligned).
+cudaError_t make_tma_maps(const Problem &P, const void *v, TmaMaps *out);
 
 // Number of SMs of the current device, cached per device (api.cu).
 cudaError_t sm_count(int *out);

@@ -43,20 +43,29 @@ constexpr uint32_t C_DQK = 169984;   // dAqk^T [64 i][64 r] hi | lo
 constexpr uint32_t C_XB = 186368;    // X = beta dL [64 r][64 i] hi | lo
 constexpr uint32_t C_T = 202752;     // T = A^T dA [64 r][64 m] hi | lo
 constexpr uint32_t LO128 = 16384, LO64 = 8192;
-// after the pairwise chains (A, dL, dAqk, X and T dead): staging of the fp32
-// products of one 64-column pass, [64][PST_LD] each, then the per-block column
-// totals of the dg scan; d(2^G_last) and sum_v dX v are prefetched into the
-// dead T tile right after dL.
-constexpr uint32_t PST_LD = 68;                  // padded row stride (floats): conflict-free float2 reads
-constexpr uint32_t PST_BYTES = 64 * PST_LD * 4;  // 17408
-constexpr uint32_t C_PST = C_A;                  // dQg | dBk | dKhat staging (3 x 17408)
-constexpr uint32_t SQ_LD = 36;                   // row stride (floats) of the dG group tiles
-constexpr uint32_t C_SQ = C_PST + 3 * PST_BYTES;  // Q part of dG, one 32-column group [64][SQ_LD]
+// Product staging for the assembly, in four passes of 32 columns (16 per
+// column half), double-buffered: each pass holds dQg, dBk, dKhat as
+// [64][32] fp32 tiles with 16-byte chunks XOR-swizzled by row % 8 (8 KB each).
+// Buffer 0 lives in the A and T tiles (dead after dL, so pass 0 loads during
+// the pairwise chains); buffer 1 in the dL / dAqk tiles (dead after the
+// chains).  The dG tiles of a pass and the segment totals of its column scans
+// use the rest of the dead chain tiles; d(2^G_last) and sum_v dX v are
+// prefetched into the C_RC scratch right after dL.
+constexpr uint32_t ST_BYTES = 64 * 32 * 4;        // one staged [64][32] product
+constexpr uint32_t C_ST0_QB = C_T;                // pass buffer 0: dQg | dBk (16 KB)
+constexpr uint32_t C_ST0_K = C_A;                 //                dKhat (8 KB)
+constexpr uint32_t C_ST1 = C_DAB;                 // pass buffer 1: dQg | dBk | dKhat (24 KB)
+constexpr uint32_t SQ_LD = 36;                    // row stride (floats) of the dG pass tiles
+constexpr uint32_t C_SQ = C_ST1 + 3 * ST_BYTES;   // Q part of dG, one pass [64][SQ_LD]
 constexpr uint32_t C_SP = C_SQ + 64 * SQ_LD * 4;  // P part
-constexpr uint32_t C_TOT = C_SP + 64 * SQ_LD * 4; // segment totals of Q, P [8][32] each; block totals of the Khat column term [4][32]
+constexpr uint32_t C_TOT = C_SP + 64 * SQ_LD * 4; // segment totals of Q, P [8][32]; Khat column term [2][4][32]
 constexpr uint32_t C_DGL = C_RC;                  // d(2^G_last) [128]
 constexpr uint32_t C_DBX = C_RC + 512;            // sum_v dX v [64]
-static_assert(C_TOT + (8 + 8 + 4) * 32 * 4 <= 219136, "group scratch overflows the map");
+static_assert(C_TOT + (8 + 8 + 8) * 32 * 4 <= C_T, "pass scratch overlaps staging buffer 0");
+// byte offset of element (r, c) of a staged [64][32] product
+__device__ __forceinline__ uint32_t st_off(int r, int c) {
+  return (uint32_t)r * 128u + ((uint32_t)((c >> 2) ^ (r & 7)) << 4) + (uint32_t)(c & 3) * 4u;
+}
 constexpr uint32_t C_SMEM = 219136 + 1024;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -317,16 +326,28 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       }
   }
   __syncthreads();
-  if (tid < 32) cp16(sbase + C_DGL + tid * 16, W.tc_dgl + slot * kD + tid * 4);  // T is dead
+  // Asynchronous loads of product pass g (columns 16g .. 16g+15 of each half) into buffer g & 1.
+  auto stage = [&](int g) {
+    for (int it = tid; it < 3 * 512; it += kThr) {
+      const int prod = it >> 9, w = it & 511, r = w >> 3, q = w & 7;  // q: 16-byte chunk of the 32 columns
+      const int gc = 64 * (q >> 2) + 16 * g + 4 * (q & 3);            // first global column of the chunk
+      const float *src = (prod == 0 ? W.tc_dqg : prod == 1 ? W.tc_dbk : W.tc_dkh) + (slot * kC + r) * kD + gc;
+      const uint32_t base = (g & 1) ? C_ST1 + (uint32_t)prod * ST_BYTES
+                                    : (prod < 2 ? C_ST0_QB + (uint32_t)prod * ST_BYTES : C_ST0_K);
+      cp16(sbase + base + st_off(r, 4 * q), src);
+    }
+    cp_commit();
+  };
+  if (tid < 32) cp16(sbase + C_DGL + tid * 16, W.tc_dgl + slot * kD + tid * 4);
   else if (tid < 48) cp16(sbase + C_DBX + (tid - 32) * 16, W.tc_dbx + slot * kC + (tid - 32) * 4);
-  cp_commit();
+  stage(0);  // A and T are dead: pass 0 loads during the pairwise chains
 
   KDA_PT(4);
   // ---- pairwise chains: warp owns rows 16B..16B+15 (as r and as i), columns ch0 .. ch0+63 ----
   // Block-pair products are formed in a temporary, scaled by the per-channel
   // factor D_RI in fp32, and added to the accumulators.
   const int Bk = warp >> 1, ch0 = 64 * (warp & 1);
-  float xr[8][4] = {}, yr[8][4] = {}, xi[8][4] = {}, yi[8][4] = {};
+  float xr[8][4] = {}, yr[8][4] = {}, xyi[8][4] = {};  // xyi = xi + yi (only their sum is used)
   for (int I = 0; I <= Bk; ++I) {  // row side: R = Bk, I = 0..Bk
     const float *Dv = (I < Bk) ? vec + (V_D + Bk * (Bk - 1) / 2 + I) * kD : nullptr;
     uint32_t aLh[4], aLl[4], aQh[4], aQl[4];
@@ -369,55 +390,45 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       ldb_t(sbase + C_QR + LO128, kC, ch0 + 16 * nb, 16 * R, ql);
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        float tx[4] = {}, ty[4] = {};
+        float tx[4] = {};  // X Kr + dAqk Qr of this block pair, before the channel decay
         mma3(tx, aXh, aXl, kh[2 * t], kh[2 * t + 1], kl[2 * t], kl[2 * t + 1]);
-        mma3(ty, aQh, aQl, qh[2 * t], qh[2 * t + 1], ql[2 * t], ql[2 * t + 1]);
+        mma3(tx, aQh, aQl, qh[2 * t], qh[2 * t + 1], ql[2 * t], ql[2 * t + 1]);
         const int c = ch0 + 16 * nb + 8 * t + (lane & 3) * 2;
         const float d0 = Dv ? Dv[c] : 1.f, d1 = Dv ? Dv[c + 1] : 1.f;
-        float(&X)[4] = xi[2 * nb + t];
-        float(&Y)[4] = yi[2 * nb + t];
+        float(&X)[4] = xyi[2 * nb + t];
         X[0] = fmaf(d0, tx[0], X[0]); X[1] = fmaf(d1, tx[1], X[1]); X[2] = fmaf(d0, tx[2], X[2]); X[3] = fmaf(d1, tx[3], X[3]);
-        Y[0] = fmaf(d0, ty[0], Y[0]); Y[1] = fmaf(d1, ty[1], Y[1]); Y[2] = fmaf(d0, ty[2], Y[2]); Y[3] = fmaf(d1, ty[3], Y[3]);
       }
     }
   }
   __syncthreads();  // every warp is done with the chain tiles: A .. X become the product staging
   KDA_PT(5);
 
-  // ---- assembly (fragment element (r, c)), in two passes of 32 columns per warp ----
-  // Per pass the products dQg, dBk, dKhat of the pass's 64 columns are staged
-  // in shared memory with one batch of asynchronous copies.  Raw k and q are
-  // not re-read: every term that needs them is a product with a decay factor
-  // that the hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2 already hold.
-  // dg = reverse cumsum of dG over the chunk runs as warp-shuffle scans over
-  // each warp's 16 rows plus per-block totals exchanged through shared memory.
+  // ---- assembly (fragment element (r, c)), in four passes of 16 columns per warp ----
+  // Raw k and q are not re-read: every term that needs them is a product with
+  // a decay factor that the hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2 hold.
+  // dg = reverse cumsum of dG over the chunk runs per pass as column scans
+  // over 8-row segments with segment totals exchanged in shared memory.
   float *sQ = (float *)(sm + C_SQ), *sP = (float *)(sm + C_SP);
-  float *totQ = (float *)(sm + C_TOT), *totP = totQ + 8 * 32, *totC = totP + 8 * 32;
+  float *totQ = (float *)(sm + C_TOT), *totP = totQ + 8 * 32;
   const float *dglv = (const float *)(sm + C_DGL), *dbxv = (const float *)(sm + C_DBX);
   const int i8 = lane >> 2, l4 = lane & 3, mid = len >> 1;
   float bpart[2] = {0.f, 0.f};
+  stage(1);
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    if (p == 1) __syncthreads();  // every warp is done with pass 0's staging
-    for (int it = tid; it < 3 * 1024; it += kThr) {
-      const int prod = it >> 10, w = it & 1023, r = w >> 4, seg = (w >> 3) & 1, jj = w & 7;
-      const float *src = (prod == 0 ? W.tc_dqg : prod == 1 ? W.tc_dbk : W.tc_dkh) +
-                         (slot * kC + r) * kD + 64 * seg + 32 * p + 4 * jj;
-      cp16(sbase + C_PST + (uint32_t)prod * PST_BYTES + (uint32_t)(r * PST_LD + 32 * seg + 4 * jj) * 4u, src);
-    }
-    cp_commit();
-    cp_wait_all();
+  for (int g = 0; g < 4; ++g) {
+    if (g < 3) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+    else cp_wait_all();
     __syncthreads();
     KDA_PT(9);
-#pragma unroll
-    for (int gg = 0; gg < 2; ++gg) {
-      const int g = 2 * p + gg;
-      float qv[2][2][2], pv[2][2][2], cq[2][2];  // [nt of the group][hh][u], column sums [nt][u]
+    float *totC = totP + 8 * 32 + (g & 1) * 4 * 32;  // double-buffered: read after the next pass starts
+    const uint32_t bq = (g & 1) ? C_ST1 : C_ST0_QB, bb = bq + ST_BYTES, bk = (g & 1) ? C_ST1 + 2 * ST_BYTES : C_ST0_K;
+    {
+      float qv[2][2][2], pv[2][2][2], cq[2][2];  // [nt of the pass][hh][u], column sums [nt][u]
 #pragma unroll
       for (int ntl = 0; ntl < 2; ++ntl) {
         const int nt = 2 * g + ntl;
         const int c = ch0 + 8 * nt + 2 * l4;
-        const int lc = 32 * (ch0 >> 6) + 8 * nt - 32 * p + 2 * l4;  // column in the staging
+        const int lc = 16 * (ch0 >> 6) + 8 * ntl + 2 * l4;  // column in the staging
         const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
         const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
         const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
@@ -426,10 +437,10 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
         for (int hh = 0; hh < 2; ++hh) {
           const int r = 16 * Bk + i8 + 8 * hh;
           const float br = beta[r];
-          const uint32_t so = (uint32_t)(r * PST_LD + lc) * 4u;
-          const float2 vq = *reinterpret_cast<const float2 *>(sm + C_PST + so);
-          const float2 vb = *reinterpret_cast<const float2 *>(sm + C_PST + PST_BYTES + so);
-          const float2 vk = *reinterpret_cast<const float2 *>(sm + C_PST + 2 * PST_BYTES + so);
+          const uint32_t so = st_off(r, lc);
+          const float2 vq = *reinterpret_cast<const float2 *>(sm + bq + so);
+          const float2 vb = *reinterpret_cast<const float2 *>(sm + bb + so);
+          const float2 vk = *reinterpret_cast<const float2 *>(sm + bk + so);
           const uint32_t to = sw_off(r, c, kC);
           const float2 krh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + to));
           const float2 krl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + LO128 + to));
@@ -450,13 +461,13 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
             const float e1 = exp2f(gg_ - gref), e2 = exp2f(gref - gg_);
             const float gam = e1 * eref, kh = e2 * lam;
             const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
-            const float xI = xi[nt][2 * hh + u], yI = yi[nt][2 * hh + u];
+            const float xyI = xyi[nt][2 * hh + u];
             dq2[u] = dQg * gam + e1 * yR;
-            dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * (xI + yI);
+            dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * xyI;
             // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
             const bool in = r < len;
             qv[ntl][hh][u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
-            pv[ntl][hh][u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * (xI + yI) - dKh * Kc * lam) : 0.f;
+            pv[ntl][hh][u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * xyI - dKh * Kc * lam) : 0.f;
             bpart[hh] += dBk * Kr * eref + Kr * xR;
             cq[ntl][u] += dKh * Kc * lam;
           }
@@ -476,7 +487,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
         }
       }
       KDA_PT(10);
-      // dG of this group's 32 columns -> shared memory, then the column scans
+      // dG of this pass's 32 columns -> shared memory, then the column scans
 #pragma unroll
       for (int ntl = 0; ntl < 2; ++ntl) {
         const int lc = 16 * (ch0 >> 6) + 8 * ntl + 2 * l4;
@@ -495,9 +506,10 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
           if (i8 == 0) totC[Bk * 32 + lc + u] = cs;
         }
       }
-      __syncthreads();
+      __syncthreads();  // buffer g & 1 consumed; dG tiles complete
+      if (g + 2 < 4) stage(g + 2);
       KDA_PT(11);
-      {  // thread: one column of the group, one 8-row segment (warp = segment)
+      {  // thread: one column of the pass, one 8-row segment (warp = segment)
         const int col = tid & 31, seg = warp;
         const int cc = (col < 16) ? 16 * g + col : 64 + 16 * g + (col - 16);
         float q8[8], p8[8], tq = 0.f, tp = 0.f;

@@ -29,7 +29,8 @@ constexpr uint32_t TMEM_COLS = 256;  // [0,64) dD^T, [64,128) dX^T, [128,256) dh
 
 __global__ void __launch_bounds__(kThr, 1)
 kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__ dO,
-                       const float *__restrict__ dhT, float *__restrict__ dh0, int *err) {
+                       const float *__restrict__ dhT, float *__restrict__ dh0, int *err,
+                       const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
@@ -37,6 +38,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
   float *betab = (float *)(sm + OFF_BETA);
   uint64_t *bar = (uint64_t *)(sm + OFF_MISC);
   uint32_t *tslot = (uint32_t *)(sm + OFF_MISC + 8);
+  uint64_t *bar_kqg = (uint64_t *)(sm + OFF_MISC + 16);
   unsigned char *U = sm + OFF_U;
 
   const int n = blockIdx.x, j = blockIdx.y;
@@ -48,6 +50,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
 
   if (tid == 0) {
     bar_init(bar, 1);
+    bar_init(bar_kqg, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
@@ -56,7 +59,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
   fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
-  uint32_t phase = 0;
+  uint32_t phase = 0, kq_par = 0;
 
   float dreg[64];  // dh'[cown][64 * vhalf + x]
   {
@@ -76,7 +79,8 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
   };
   if (si.w > 0) {
     const int2 chl = chunk_span(si, si.w - 1);
-    load_kqg(P, sm, chl.x, chl.y, j, h, betab, true);
+    if (tid == 0) tma_kqg(maps, sbase, chl.x, h, j, true, bar_kqg);
+    load_beta(P, betab, chl.x, chl.y, j);
     load_rows(sbase + OFF_VRAW, dO, chl.x, chl.y, HV, j);
     load_aqk_a(si.z + si.w - 1);
     cp_commit();
@@ -88,13 +92,21 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
     const int buf = (si.w - 1 - ci) & 1;
     const float *beta = betab + buf * kC;
     const size_t slot = (size_t)cidx * HV + j;
-    cp_wait_all();
+    cp_wait_all();  // beta, dO, Aqk / A
+    bar_wait(bar_kqg, kq_par, err);
+    kq_par ^= 1;
+    if (len < kC) {  // rows past the sequence end hold other tokens: clear them
+      zero_tail(sm + OFF_KRAW, len);
+      zero_tail(sm + OFF_QRAW, len);
+      fence_async_smem();
+    }
     __syncthreads();
 
     phase_a<true, false>(sm, len, beta);
     if (ci > 0) {
       const int2 pv = chunk_span(si, ci - 1);
-      load_kqg(P, sm, pv.x, pv.y, j, h, betab + (buf ^ 1) * kC, true);
+      if (tid == 0) tma_kqg(maps, sbase, pv.x, h, j, true, bar_kqg);
+      load_beta(P, betab + (buf ^ 1) * kC, pv.x, pv.y, j);
       cp_commit();
     }
 
@@ -233,9 +245,11 @@ cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *d
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  TmaMaps maps;
+  if ((e = make_tma_maps(P, nullptr, &maps)) != cudaSuccess) return e;
   KDA_LAUNCH("kda_bwd_scan_tc", s,
              kda_bwd_scan_tc_kernel<<<dim3(P.N, P.HV), kThr, SMEM_BYTES, s>>>(
-                 P, W, (const __nv_bfloat16 *)dO, dhT, dh0, err));
+                 P, W, (const __nv_bfloat16 *)dO, dhT, dh0, err, maps));
   return cudaGetLastError();
 }
 

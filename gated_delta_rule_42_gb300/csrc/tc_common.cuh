@@ -79,13 +79,14 @@ static __shared__ long long kda_pt_acc[33];  // [32] = time of the last stamp
 constexpr int kC = 64;     // chunk
 constexpr int kD = 128;    // K = V
 constexpr int kThr = 256;  // 8 warps
-constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile
+constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile of the chain kernel
+constexpr int kGT = 128;   // row stride of the TMA-loaded gate tile of the sequential kernels
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_KRAW = 0;       // k  [64][128] bf16
 constexpr uint32_t OFF_QRAW = 16384;   // q  [64][128]
 constexpr uint32_t OFF_VRAW = 32768;   // v (forward) or dO (backward) [64][128]
-constexpr uint32_t OFF_GRAW = 49152;   // g -> G  fp32 [64][132]
+constexpr uint32_t OFF_GRAW = 49152;   // g -> G  fp32 [64][128] (dense rows: a TMA box)
 constexpr uint32_t OFF_BK = 83968;     // beta k 2^G         [64 r][128 c]
 constexpr uint32_t OFF_QG = 100352;    // q~ 2^G             [64 r][128 c]
 constexpr uint32_t OFF_KH = 116736;    // k 2^(G_last - G)   [64 r][128 c]
@@ -96,7 +97,7 @@ constexpr uint32_t U_KR = 0, U_QR = 16384, U_KC = 32768, U_LF = 49152;  // (a)/(
 constexpr uint32_t U_AF = 0, U_T = 16384;                              // (b) inverse scratch
 constexpr uint32_t OFF_VEC = 215040;   // fp32 vectors (20 rows of 128)
 constexpr uint32_t OFF_BETA = 225280;  // beta, two buffers of 64 fp32
-constexpr uint32_t OFF_MISC = 225792;  // mbarrier, tmem slot
+constexpr uint32_t OFF_MISC = 225792;  // mbarriers (MMA +0, k/q/g loads +16, v loads +24), tmem slot +8
 constexpr uint32_t SMEM_BYTES = 225792 + 64 + 1024;  // + alignment slack
 constexpr int V_GL = 0, V_GAML = 1, V_GREF = 2, V_EREF = 6, V_D = 10, V_LAM = 16;
 
@@ -168,17 +169,45 @@ __device__ __forceinline__ int2 chunk_span(const int4 &si, int ci) {
   return make_int2(si.x + t, min(kC, si.y - t));
 }
 
-// k, q (optional), g and beta of one chunk, all asynchronous (a plain load of
-// beta would stall its threads for a DRAM round trip in the middle of a chunk).
-__device__ __forceinline__ void load_kqg(const Problem &P, unsigned char *sm, int t0, int len, int j,
-                                         int h, float *beta_dst, bool with_q) {
-  const uint32_t base = smem_u32(sm);
-  load_rows(base + OFF_KRAW, (const __nv_bfloat16 *)P.k, t0, len, P.H, h);
-  if (with_q) load_rows(base + OFF_QRAW, (const __nv_bfloat16 *)P.q, t0, len, P.H, h);
-  load_gate(base + OFF_GRAW, P.g, t0, len, P.HV, j);
+// ---- TMA (bulk tensor) loads of the per-token tiles ----
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// Box (c0, c1, c2) of a 3-D tensor map into shared memory; completion counted on bar.
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::
+          "r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+// One swizzled [64][128] bf16 tile = two 64 x 64 boxes (channel offsets 0 and 64).
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, int head, int t0, uint64_t *bar) {
+  tma_load3(dst, map, 0, head, t0, bar);
+  tma_load3(dst + 8192, map, 64, head, t0, bar);
+}
+// k, q (when with_q) and the gate rows of one chunk, issued by one thread:
+// rows past the tensor end arrive as zeros, rows past the sequence end hold
+// the next tokens (zero_tail clears them where it matters).
+__device__ __forceinline__ void tma_kqg(const TmaMaps &M, uint32_t base, int t0, int h, int j, bool with_q,
+                                        uint64_t *bar) {
+  mbar_expect_tx(bar, (with_q ? 32768u : 16384u) + 32768u);
+  tma_tile(base + OFF_KRAW, &M.k, h, t0, bar);
+  if (with_q) tma_tile(base + OFF_QRAW, &M.q, h, t0, bar);
+  tma_load3(base + OFF_GRAW, &M.g, 0, j, t0, bar);
+}
+// Rows len..63 of a swizzled [64][128] bf16 tile -> 0 (after its load completed).
+__device__ __forceinline__ void zero_tail(unsigned char *tile, int len) {
+  for (int it = threadIdx.x; it < (kC - len) * 16; it += kThr) {
+    const int r = len + (it >> 4), q = it & 15;
+    *reinterpret_cast<uint4 *>(tile + (q >> 3) * 8192 + r * 128 + (q & 7) * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+// beta of one chunk (asynchronous; zero past len).
+__device__ __forceinline__ void load_beta(const Problem &P, float *dst, int t0, int len, int j) {
   if (threadIdx.x < kC) {
-    if (threadIdx.x < len) cp4(smem_u32(beta_dst + threadIdx.x), P.beta + (size_t)(t0 + threadIdx.x) * P.HV + j);
-    else beta_dst[threadIdx.x] = 0.f;
+    if (threadIdx.x < len) cp4(smem_u32(dst + threadIdx.x), P.beta + (size_t)(t0 + threadIdx.x) * P.HV + j);
+    else dst[threadIdx.x] = 0.f;
   }
 }
 
@@ -198,7 +227,7 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
     float col[32];
     float s = 0.f;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) col[k] = G[(r0 + k) * kGLD + c];
+    for (int k = 0; k < 32; ++k) col[k] = G[(r0 + k) * kGT + c];
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
       if (r0 + k < len) s += col[k];
@@ -209,7 +238,7 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
       col[k] += add;
-      G[(r0 + k) * kGLD + c] = col[k];
+      G[(r0 + k) * kGT + c] = col[k];
     }
     const float gl = __shfl_sync(0xffffffffu, s + add, lane | 1);
     // block references: rows 0, 16 (lower partner) and 32, 48 (upper partner)
@@ -261,8 +290,8 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       float kv[8], qv[8], g[8], e1[8], e2[8], o[8];
       unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + off), kv);
       if (kQ) unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + off), qv);
-      *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGLD + c0);
-      *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGLD + c0 + 4);
+      *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGT + c0);
+      *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + 4);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         e1[e] = exp2f(g[e] - gref[e]);  // <= 1

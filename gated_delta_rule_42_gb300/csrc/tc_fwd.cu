@@ -38,7 +38,8 @@ struct FwdArgs {
 };
 
 template <bool kOut>
-__global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args) {
+__global__ void __launch_bounds__(kThr, 1)
+kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
   float *betab = (float *)(sm + OFF_BETA);
   uint64_t *bar = (uint64_t *)(sm + OFF_MISC);
   uint32_t *tslot = (uint32_t *)(sm + OFF_MISC + 8);
+  uint64_t *bar_kqg = (uint64_t *)(sm + OFF_MISC + 16), *bar_v = (uint64_t *)(sm + OFF_MISC + 24);
   unsigned char *U = sm + OFF_U;
 
   const int n = blockIdx.x, j = blockIdx.y;
@@ -57,6 +59,8 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
 
   if (tid == 0) {
     bar_init(bar, 1);
+    bar_init(bar_kqg, 1);
+    bar_init(bar_v, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
@@ -65,7 +69,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
   fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
-  uint32_t phase = 0;
+  uint32_t phase = 0, kq_par = 0, v_par = 0;
   KDA_PT_DECL;
 
   float hreg[64];  // h[cown][64 * vhalf + x]
@@ -81,8 +85,12 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
 
   if (si.w > 0) {
     const int2 ch0 = chunk_span(si, 0);
-    load_kqg(P, sm, ch0.x, ch0.y, j, h, betab, true);
-    load_rows(sbase + OFF_VRAW, (const __nv_bfloat16 *)P.v, ch0.x, ch0.y, HV, j);
+    if (tid == 0) {
+      tma_kqg(maps, sbase, ch0.x, h, j, true, bar_kqg);
+      mbar_expect_tx(bar_v, 16384u);
+      tma_tile(sbase + OFF_VRAW, &maps.v, j, ch0.x, bar_v);
+    }
+    load_beta(P, betab, ch0.x, ch0.y, j);
     cp_commit();
   }
 
@@ -92,7 +100,14 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     const int t0 = ch.x, len = ch.y;
     const size_t slot = (size_t)cidx * HV + j;
     const float *beta = betab + (ci & 1) * kC;
-    cp_wait_all();
+    cp_wait_all();  // beta
+    bar_wait(bar_kqg, kq_par, args.err);
+    kq_par ^= 1;
+    if (len < kC) {  // rows past the sequence end hold other tokens: clear them
+      zero_tail(sm + OFF_KRAW, len);
+      zero_tail(sm + OFF_QRAW, len);
+      fence_async_smem();
+    }
     __syncthreads();
     KDA_PT(0);
 
@@ -100,7 +115,8 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     KDA_PT(2);
     if (ci + 1 < si.w) {  // staging k, q, g consumed: prefetch the next chunk's
       const int2 nx = chunk_span(si, ci + 1);
-      load_kqg(P, sm, nx.x, nx.y, j, h, betab + ((ci + 1) & 1) * kC, true);
+      if (tid == 0) tma_kqg(maps, sbase, nx.x, h, j, true, bar_kqg);
+      load_beta(P, betab + ((ci + 1) & 1) * kC, nx.x, nx.y, j);
       cp_commit();
     }
     KDA_PT(3);
@@ -112,6 +128,9 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
     }
 
     // ---------------- (c) state chain on tcgen05 ----------------
+    bar_wait(bar_v, v_par, args.err);
+    v_par ^= 1;
+    if (len < kC) zero_tail(sm + OFF_VRAW, len);  // (ordered before the MMAs by the barrier below)
     {
       unsigned char *H = U + U_H;  // h row-major [c][v], bf16
 #pragma unroll
@@ -166,10 +185,10 @@ __global__ void __launch_bounds__(kThr, 1) kda_fwd_tc_kernel(Problem P, Workspac
       uint4 *dst = (uint4 *)(W.tc_xt + slot * 16384);
       for (int e = tid; e < 1024; e += kThr) dst[e] = src[e];
     }
-    if (ci + 1 < si.w) {  // v of this chunk consumed
+    if (ci + 1 < si.w && tid == 0) {  // v of this chunk consumed
       const int2 nx = chunk_span(si, ci + 1);
-      load_rows(sbase + OFF_VRAW, (const __nv_bfloat16 *)P.v, nx.x, nx.y, HV, j);
-      cp_commit();
+      mbar_expect_tx(bar_v, 16384u);
+      tma_tile(sbase + OFF_VRAW, &maps.v, j, nx.x, bar_v);
     }
     if (tid == 0) {  // D^T[v][r] = sum_i X^T[v][i] A[r][i]   (M=128 v, N=64 r, K=64 i)
       const uint32_t id = idesc(128, 64, 0, 0);
@@ -278,17 +297,19 @@ cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT,
   cudaError_t e = launch_chunk_map(P, W, s);
   if (e != cudaSuccess || P.N == 0) return e;
   FwdArgs a{(__nv_bfloat16 *)o, hT, err};
+  TmaMaps maps;
+  if ((e = make_tma_maps(P, P.v, &maps)) != cudaSuccess) return e;
   const dim3 grid(P.N, P.HV);
   if (states) {
     e = cudaFuncSetAttribute(kda_fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    KDA_LAUNCH("kda_fwd_tc_states", s, kda_fwd_tc_kernel<false><<<grid, kThr, SMEM_BYTES, s>>>(P, W, a));
+    KDA_LAUNCH("kda_fwd_tc_states", s, kda_fwd_tc_kernel<false><<<grid, kThr, SMEM_BYTES, s>>>(P, W, a, maps));
   } else {
     e = cudaFuncSetAttribute(kda_fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    KDA_LAUNCH("kda_fwd_tc", s, kda_fwd_tc_kernel<true><<<grid, kThr, SMEM_BYTES, s>>>(P, W, a));
+    KDA_LAUNCH("kda_fwd_tc", s, kda_fwd_tc_kernel<true><<<grid, kThr, SMEM_BYTES, s>>>(P, W, a, maps));
   }
   return cudaGetLastError();
 }
