@@ -337,59 +337,55 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
   const float *vec = (const float *)(sm + OFF_VEC);
   unsigned char *U = sm + OFF_U;
   float *Lf = (float *)(U + U_LF);
-  for (int pr = warp; pr < 16; pr += 8) {
-    const int R = pr >> 2, I = pr & 3;
-    float accL[2][4] = {}, accQ[2][4] = {};
-    if (I <= R) {
-      const float *Dv = (I < R) ? vec + (V_D + R * (R - 1) / 2 + I) * kD : nullptr;
+  // Gram blocks: the 10 block pairs R >= I, each split into its two 8-column
+  // halves: 20 equal units over the 8 warps.
+  for (int u = warp; u < 20; u += 8) {
+    const int p = u >> 1, nt = u & 1;
+    const int R = p >= 6 ? 3 : p >= 3 ? 2 : p >= 1 ? 1 : 0, I = p - R * (R + 1) / 2;
+    const float *Dv = (I < R) ? vec + (V_D + R * (R - 1) / 2 + I) * kD : nullptr;
+    float accL[4] = {}, accQ[4] = {};
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        uint32_t ak[4], aq[4] = {0, 0, 0, 0}, b[4];
-        {
-          const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
-          ldsm_x4(sbase + OFF_U + U_KR + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
-          if (kQ) ldsm_x4(sbase + OFF_U + U_QR + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
-        }
-        {
-          const int mi = lane >> 3;
-          const int row = 16 * I + (lane & 7) + (mi >> 1) * 8, jj = 2 * s + (mi & 1);
-          ldsm_x4(sbase + OFF_U + U_KC + sw_chunk(row, jj, kC), b[0], b[1], b[2], b[3]);
-        }
-        if (Dv != nullptr) {
-          const int c0 = 16 * s + (lane & 3) * 2;
-          const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
-          const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float2 f = unpack_bf16(b[t]);
-            b[t] = (t & 1) ? pack_bf16(f.x * d89.x, f.y * d89.y) : pack_bf16(f.x * d01.x, f.y * d01.y);
-          }
-        }
-        mma16816(accL[0], ak, b[0], b[1]);
-        mma16816(accL[1], ak, b[2], b[3]);
-        if (kQ) {
-          mma16816(accQ[0], aq, b[0], b[1]);
-          mma16816(accQ[1], aq, b[2], b[3]);
-        }
+    for (int s = 0; s < 8; ++s) {
+      uint32_t ak[4], aq[4] = {0, 0, 0, 0}, b0, b1;
+      {
+        const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
+        ldsm_x4(sbase + OFF_U + U_KR + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
+        if (kQ) ldsm_x4(sbase + OFF_U + U_QR + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
       }
+      {
+        const int row = 16 * I + 8 * nt + (lane & 7), jj = 2 * s + ((lane >> 3) & 1);
+        ldsm_x2(sbase + OFF_U + U_KC + sw_chunk(row, jj, kC), b0, b1);
+      }
+      if (Dv != nullptr) {
+        const int c0 = 16 * s + (lane & 3) * 2;
+        const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
+        const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
+        const float2 f0 = unpack_bf16(b0), f1 = unpack_bf16(b1);
+        b0 = pack_bf16(f0.x * d01.x, f0.y * d01.y);
+        b1 = pack_bf16(f1.x * d89.x, f1.y * d89.y);
+      }
+      mma16816(accL, ak, b0, b1);
+      if (kQ) mma16816(accQ, aq, b0, b1);
     }
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * R + (lane >> 2) + hh * 8;
-        const int i = 16 * I + nt * 8 + (lane & 3) * 2;
-        const float br = beta[r];
-        const float l0 = (i < r) ? br * accL[nt][2 * hh] : 0.f;
-        const float l1 = (i + 1 < r) ? br * accL[nt][2 * hh + 1] : 0.f;
-        *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
-        if (kQ) {
-          const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
-          const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
-          st_bf2(sm + OFF_AQK, r, i, kC, a0, a1);
-        }
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = 16 * R + (lane >> 2) + hh * 8;
+      const int i = 16 * I + nt * 8 + (lane & 3) * 2;
+      const float br = beta[r];
+      const float l0 = (i < r) ? br * accL[2 * hh] : 0.f;
+      const float l1 = (i + 1 < r) ? br * accL[2 * hh + 1] : 0.f;
+      *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
+      if (kQ) {
+        const float a0 = (i <= r) ? accQ[2 * hh] : 0.f;
+        const float a1 = (i + 1 <= r) ? accQ[2 * hh + 1] : 0.f;
+        st_bf2(sm + OFF_AQK, r, i, kC, a0, a1);
       }
     }
+  }
+  if (kQ && tid < 6 * 32) {  // Aqk blocks above the diagonal (R < I) are zero
+    const int b = tid >> 5, w = tid & 31;
+    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
+    *reinterpret_cast<uint4 *>(sm + OFF_AQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   KDA_PT(4);
@@ -401,13 +397,12 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     float a[16];
 #pragma unroll
     for (int m = 0; m < 16; ++m) a[m] = (m == i) ? 1.f : 0.f;
+    // column-oriented substitution: once a[m] is final, subtract its multiples
+    // from every later row (independent updates: a short dependency chain)
 #pragma unroll
-    for (int r = 1; r < 16; ++r) {
-      float s = a[r];
+    for (int m = 0; m < 15; ++m)
 #pragma unroll
-      for (int m = 0; m < r; ++m) s = fmaf(-Lf[fsw(16 * R + r, 16 * R + m)], a[m], s);
-      a[r] = s;
-    }
+      for (int r = m + 1; r < 16; ++r) a[r] = fmaf(-Lf[fsw(16 * R + r, 16 * R + m)], a[m], a[r]);
 #pragma unroll
     for (int m = 0; m < 16; ++m) Af[fsw(16 * R + m, 16 * R + i)] = a[m];
   }
@@ -419,39 +414,58 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
   }
   __syncthreads();
   KDA_PT(5);
-  // off-diagonal blocks by sub-diagonal level: A_RI = -A_RR sum_{M=I}^{R-1} L_RM A_MI,
-  // each thread a 1 x 4 row segment (one broadcast L value per four FMAs)
+  // Off-diagonal blocks, 32-blocked: A = [[A1, 0], [A21, A2]] with A21 = -A2 L21 A1,
+  // where A1 = [[D0, 0], [-D1 L10 D0, D1]] and A2 likewise from D2, D3 (D_R the
+  // diagonal-block inverses above).  Each thread forms 1 x 4 row segments.
+  for (int e = tid; e < 2 * 64; e += kThr) {  // T_b = L_{R,R-1} D_{R-1} for R = 1, 3
+    const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int lvl = 1; lvl < 4; ++lvl) {
-    const int nb = 4 - lvl;
-    for (int e = tid; e < nb * 64; e += kThr) {
-      const int I = e >> 6, R = I + lvl, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int M = I; M < R; ++M)
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float l = Lf[fsw(16 * R + rr, 16 * M + m)];
-          const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(16 * M + m, 16 * I + i4));
-          acc.x = fmaf(l, a.x, acc.x); acc.y = fmaf(l, a.y, acc.y);
-          acc.z = fmaf(l, a.z, acc.z); acc.w = fmaf(l, a.w, acc.w);
-        }
-      *reinterpret_cast<float4 *>(Tf + (I * 16 + rr) * 16 + i4) = acc;
+    for (int m = 0; m < 16; ++m) {
+      const float l = Lf[fsw(16 * R + rr, 16 * (R - 1) + m)];
+      const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(16 * (R - 1) + m, 16 * (R - 1) + i4));
+      acc.x = fmaf(l, a.x, acc.x); acc.y = fmaf(l, a.y, acc.y);
+      acc.z = fmaf(l, a.z, acc.z); acc.w = fmaf(l, a.w, acc.w);
     }
-    __syncthreads();
-    for (int e = tid; e < nb * 64; e += kThr) {
-      const int I = e >> 6, R = I + lvl, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float l = Af[fsw(16 * R + rr, 16 * R + m)];
-        const float4 t = *reinterpret_cast<const float4 *>(Tf + (I * 16 + m) * 16 + i4);
-        acc.x = fmaf(l, t.x, acc.x); acc.y = fmaf(l, t.y, acc.y);
-        acc.z = fmaf(l, t.z, acc.z); acc.w = fmaf(l, t.w, acc.w);
-      }
-      *reinterpret_cast<float4 *>(Af + fsw(16 * R + rr, 16 * I + i4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    __syncthreads();
+    *reinterpret_cast<float4 *>(Tf + (b * 16 + rr) * 16 + i4) = acc;
   }
+  __syncthreads();
+  for (int e = tid; e < 2 * 64; e += kThr) {  // A_{R,R-1} = -D_R T_b
+    const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float l = Af[fsw(16 * R + rr, 16 * R + m)];
+      const float4 t = *reinterpret_cast<const float4 *>(Tf + (b * 16 + m) * 16 + i4);
+      acc.x = fmaf(l, t.x, acc.x); acc.y = fmaf(l, t.y, acc.y);
+      acc.z = fmaf(l, t.z, acc.z); acc.w = fmaf(l, t.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(Af + fsw(16 * R + rr, 16 * (R - 1) + i4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+  {
+    const int r = tid >> 3, c4 = (tid & 7) * 4;  // one 1 x 4 segment of a 32 x 32 block per thread
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {  // T2 = L21 A1  (A1 lower triangular: zeros above)
+      const float l = Lf[fsw(32 + r, m)];
+      const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(m, c4));
+      acc.x = fmaf(l, a.x, acc.x); acc.y = fmaf(l, a.y, acc.y);
+      acc.z = fmaf(l, a.z, acc.z); acc.w = fmaf(l, a.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(Tf + r * 32 + c4) = acc;
+    __syncthreads();
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {  // A21 = -A2 T2
+      const float l = Af[fsw(32 + r, 32 + m)];
+      const float4 t = *reinterpret_cast<const float4 *>(Tf + m * 32 + c4);
+      acc.x = fmaf(l, t.x, acc.x); acc.y = fmaf(l, t.y, acc.y);
+      acc.z = fmaf(l, t.z, acc.z); acc.w = fmaf(l, t.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(Af + fsw(32 + r, c4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
   for (int e = tid; e < kC * kC / 8; e += kThr) {  // A -> bf16 tile, 16-byte chunks
     const int r = e >> 3, jj = e & 7;
     float x[8];
