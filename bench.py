@@ -318,6 +318,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=["step", "fwd", "bwd"], default="step",
                     help="time only the forward or only the backward call (profiling aid)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="profiling aid: the dense workload with T replaced (e.g. 1024 for small ncu captures); "
+                         "the JSON line names the changed workload")
     args = ap.parse_args()
     warmup = max(args.warmup, 3)
 
@@ -338,7 +341,13 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
+    if args.seq_len is not None:  # profiling aid: same dense shape with another T
+        name, kw = inputs.CONFIGS[args.config]
+        assert kw.get("cu_seqlens") is None and "T" in kw, "--seq-len needs a dense configuration"
+        kw = dict(kw, T=args.seq_len)
+        cfg = inputs.make_inputs(seed=1000 + args.config + 7919 * rank, name=f"{name}_T{args.seq_len}", **kw)
+    else:
+        cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
     runner = Runner(cfg, dev)
     if args.only != "step":  # profiling aid: time one half of the step only
         runner.step = runner.fwd if args.only == "fwd" else runner.bwd

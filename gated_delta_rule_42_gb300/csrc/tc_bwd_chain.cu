@@ -32,8 +32,8 @@ using namespace tc;
 constexpr uint32_t C_G = 0;          // G fp32 [64][132]
 constexpr uint32_t C_VEC = 33792;    // vectors (20 x 128 fp32)
 constexpr uint32_t C_BETA = 44032;   // beta [64]
-constexpr uint32_t C_RB = 44288;     // dbeta partials [2][64]
-constexpr uint32_t C_RC = 44800;     // prefetched d(2^G_last) [128] and sum_v dX v [64]
+constexpr uint32_t C_RB = 44288;     // dbeta partials [4][64]
+constexpr uint32_t C_RC = 45312;     // prefetched d(2^G_last) [128] and sum_v dX v [64]
 constexpr uint32_t C_KR = 47104;     // Kr  hi [64][128] | lo (+16 KB)
 constexpr uint32_t C_QR = 79872;     // Qr  hi | lo
 constexpr uint32_t C_KC = 112640;    // Kc  hi | lo
@@ -58,10 +58,11 @@ constexpr uint32_t C_ST1 = C_DAB;                 // pass buffer 1: dQg | dBk | 
 constexpr uint32_t SQ_LD = 36;                    // row stride (floats) of the dG pass tiles
 constexpr uint32_t C_SQ = C_ST1 + 3 * ST_BYTES;   // Q part of dG, one pass [64][SQ_LD]
 constexpr uint32_t C_SP = C_SQ + 64 * SQ_LD * 4;  // P part
-constexpr uint32_t C_TOT = C_SP + 64 * SQ_LD * 4; // segment totals of Q, P [8][32]; Khat column term [2][4][32]
+constexpr uint32_t C_TOT = C_SP + 64 * SQ_LD * 4; // segment totals of Q, P [16][32]; Khat column term [2][4][32]
 constexpr uint32_t C_DGL = C_RC;                  // d(2^G_last) [128]
 constexpr uint32_t C_DBX = C_RC + 512;            // sum_v dX v [64]
-static_assert(C_TOT + (8 + 8 + 8) * 32 * 4 <= C_T, "pass scratch overlaps staging buffer 0");
+static_assert(C_TOT + (16 + 16 + 8) * 32 * 4 <= C_T, "pass scratch overlaps staging buffer 0");
+static_assert(C_RC + 768 <= C_KR, "prefetch scratch overlaps the Kr tile");
 // byte offset of element (r, c) of a staged [64][32] product
 __device__ __forceinline__ uint32_t st_off(int r, int c) {
   return (uint32_t)r * 128u + ((uint32_t)((c >> 2) ^ (r & 7)) << 4) + (uint32_t)(c & 3) * 4u;
@@ -128,7 +129,9 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
   mma16816(acc, al, bh0, bh1);
 }
 
-__global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Workspace W, ChainArgs args) {
+constexpr int kCT = 512;  // 16 warps: the assembly is latency-bound, so more warps hide more of it
+
+__global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Workspace W, ChainArgs args) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
@@ -148,10 +151,10 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
   KDA_PT_DECL;
 
   // ---- loads ----
-  load_gate(sbase + C_G, P.g, t0, len, HV, j);
+  load_gate<kCT>(sbase + C_G, P.g, t0, len, HV, j);
   {  // A, saved by the forward recompute in this kernel's swizzled layout (after the 8 KB Aqk tile)
     const unsigned char *src = W.tc_aqk_a + slot * 16384 + 8192;
-    for (int it = tid; it < 512; it += kThr) cp16(sbase + C_A + it * 16, src + it * 16);
+    for (int it = tid; it < 512; it += kCT) cp16(sbase + C_A + it * 16, src + it * 16);
   }
   if (tid < kC) {
     if (tid < len) cp4(smem_u32(beta + tid), P.beta + (size_t)(t0 + tid) * HV + j);
@@ -161,16 +164,16 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
   // thread waits on a plain global load: dA^T, dAqk^T (fp32) in the Kr tile;
   // raw k, q rows in the lo halves of Kc and Qr -- the decay-tile pass reads
   // each 16-byte chunk there before the same thread overwrites it.
-  for (int it = tid; it < kC * 16; it += kThr) {
+  for (int it = tid; it < kC * 16; it += kCT) {
     cp16(sbase + C_KR + it * 16, W.tc_dat + slot * kC * kC + it * 4);
     cp16(sbase + C_KR + LO128 + it * 16, W.tc_dqkt + slot * kC * kC + it * 4);
   }
-  load_rows(sbase + C_KC + LO128, kin, t0, len, H, h);
-  load_rows(sbase + C_QR + LO128, qin, t0, len, H, h);
+  load_rows<kCT>(sbase + C_KC + LO128, kin, t0, len, H, h);
+  load_rows<kCT>(sbase + C_QR + LO128, qin, t0, len, H, h);
   cp_commit();
   cp_wait_all();
   __syncthreads();
-  for (int it = tid; it < kC * 8; it += kThr) {  // dA^T, dAqk^T fp32 -> hi/lo bf16 tiles
+  for (int it = tid; it < kC * 8; it += kCT) {  // dA^T, dAqk^T fp32 -> hi/lo bf16 tiles
     const int r = it >> 3, jj = it & 7;
     const float *a = (const float *)(sm + C_KR) + r * kC + jj * 8;
     const float *b = (const float *)(sm + C_KR + LO128) + r * kC + jj * 8;
@@ -228,14 +231,14 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
   __syncthreads();
   KDA_PT(1);
   {
-    const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
+    const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 3;  // two rows per thread
     float gref[8];
 #pragma unroll
     for (int e = 0; e < 8; e += 4)
       *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (V_GREF + R) * kD + c0 + e);
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int r = rg * 4 + rr;
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = rg * 2 + rr;
       const uint32_t off = sw_chunk(r, jj, kC);
       float kv[8], qv[8], o[8], e1[8], e2[8];
       unpack8(*reinterpret_cast<const uint4 *>(sm + C_KC + LO128 + off), kv);  // raw k, q (zero past len)
@@ -268,29 +271,25 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
 
   KDA_PT(2);
   // ---- T = A^T dA  (T[r][m] = sum_i' A[i'][r] dA[i'][m]; dA[i'][m] = dA^T[m][i']) ----
-  const int mt = warp >> 1, nh = warp & 1;  // 16-row block, 32-column half
+  const int mt = warp >> 2, nq = warp & 3;  // 16-row block, 16-column quarter
   {
-    float acc[4][4] = {};
+    float acc[2][4] = {};
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      uint32_t a[4];
+      uint32_t a[4], bh[4], bl[4];
       lda_t(sbase + C_A, kC, 16 * mt, 16 * s, a);  // element (r, i') = A[i'][r]
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb) {
-        uint32_t bh[4], bl[4];
-        ldb(sbase + C_DAB, kC, 32 * nh + 16 * nb, 16 * s, bh);  // element (i', m) = dA^T[m][i']
-        ldb(sbase + C_DAB + LO64, kC, 32 * nh + 16 * nb, 16 * s, bl);
-        mma16816(acc[2 * nb], a, bh[0], bh[1]);
-        mma16816(acc[2 * nb], a, bl[0], bl[1]);
-        mma16816(acc[2 * nb + 1], a, bh[2], bh[3]);
-        mma16816(acc[2 * nb + 1], a, bl[2], bl[3]);
-      }
+      ldb(sbase + C_DAB, kC, 16 * nq, 16 * s, bh);  // element (i', m) = dA^T[m][i']
+      ldb(sbase + C_DAB + LO64, kC, 16 * nq, 16 * s, bl);
+      mma16816(acc[0], a, bh[0], bh[1]);
+      mma16816(acc[0], a, bl[0], bl[1]);
+      mma16816(acc[1], a, bh[2], bh[3]);
+      mma16816(acc[1], a, bl[2], bl[3]);
     }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * mt + (lane >> 2) + 8 * hh, m = 32 * nh + 8 * nt + (lane & 3) * 2;
+        const int r = 16 * mt + (lane >> 2) + 8 * hh, m = 16 * nq + 8 * nt + (lane & 3) * 2;
         st_split2(sm + C_T, LO64, r, m, kC, acc[nt][2 * hh], acc[nt][2 * hh + 1]);
       }
   }
@@ -298,39 +297,35 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
   KDA_PT(3);
   // ---- dL = -tril_{-1}(T A^T); X = beta dL ----
   {
-    float acc[4][4] = {};
+    float acc[2][4] = {};
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      uint32_t ah[4], al[4];
+      uint32_t ah[4], al[4], b[4];
       lda(sbase + C_T, kC, 16 * mt, 16 * s, ah);  // element (r, m) = T[r][m]
       lda(sbase + C_T + LO64, kC, 16 * mt, 16 * s, al);
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb) {
-        uint32_t b[4];
-        ldb(sbase + C_A, kC, 32 * nh + 16 * nb, 16 * s, b);  // element (m, i) = A[i][m]
-        mma16816(acc[2 * nb], ah, b[0], b[1]);
-        mma16816(acc[2 * nb], al, b[0], b[1]);
-        mma16816(acc[2 * nb + 1], ah, b[2], b[3]);
-        mma16816(acc[2 * nb + 1], al, b[2], b[3]);
-      }
+      ldb(sbase + C_A, kC, 16 * nq, 16 * s, b);  // element (m, i) = A[i][m]
+      mma16816(acc[0], ah, b[0], b[1]);
+      mma16816(acc[0], al, b[0], b[1]);
+      mma16816(acc[1], ah, b[2], b[3]);
+      mma16816(acc[1], al, b[2], b[3]);
     }
     __syncthreads();  // every warp has read dA^T: its tiles become dL
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * mt + (lane >> 2) + 8 * hh, i = 32 * nh + 8 * nt + (lane & 3) * 2;
+        const int r = 16 * mt + (lane >> 2) + 8 * hh, i = 16 * nq + 8 * nt + (lane & 3) * 2;
         const float d0 = (i < r) ? -acc[nt][2 * hh] : 0.f, d1 = (i + 1 < r) ? -acc[nt][2 * hh + 1] : 0.f;
         st_split2(sm + C_DAB, LO64, r, i, kC, d0, d1);
         st_split2(sm + C_XB, LO64, r, i, kC, beta[r] * d0, beta[r] * d1);
       }
   }
   __syncthreads();
-  // Asynchronous loads of product pass g (columns 16g .. 16g+15 of each half) into buffer g & 1.
+  // Asynchronous loads of product pass g (columns 32 q + 8 g .. +7 of each quarter q) into buffer g & 1.
   auto stage = [&](int g) {
-    for (int it = tid; it < 3 * 512; it += kThr) {
+    for (int it = tid; it < 3 * 512; it += kCT) {
       const int prod = it >> 9, w = it & 511, r = w >> 3, q = w & 7;  // q: 16-byte chunk of the 32 columns
-      const int gc = 64 * (q >> 2) + 16 * g + 4 * (q & 3);            // first global column of the chunk
+      const int gc = 32 * (q >> 1) + 8 * g + 4 * (q & 1);             // first global column of the chunk
       const float *src = (prod == 0 ? W.tc_dqg : prod == 1 ? W.tc_dbk : W.tc_dkh) + (slot * kC + r) * kD + gc;
       const uint32_t base = (g & 1) ? C_ST1 + (uint32_t)prod * ST_BYTES
                                     : (prod < 2 ? C_ST0_QB + (uint32_t)prod * ST_BYTES : C_ST0_K);
@@ -343,11 +338,11 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
   stage(0);  // A and T are dead: pass 0 loads during the pairwise chains
 
   KDA_PT(4);
-  // ---- pairwise chains: warp owns rows 16B..16B+15 (as r and as i), columns ch0 .. ch0+63 ----
+  // ---- pairwise chains: warp owns rows 16B..16B+15 (as r and as i), columns ch0 .. ch0+31 ----
   // Block-pair products are formed in a temporary, scaled by the per-channel
   // factor D_RI in fp32, and added to the accumulators.
-  const int Bk = warp >> 1, ch0 = 64 * (warp & 1);
-  float xr[8][4] = {}, yr[8][4] = {}, xyi[8][4] = {};  // xyi = xi + yi (only their sum is used)
+  const int Bk = warp >> 2, ch0 = 32 * (warp & 3);
+  float xr[4][4] = {}, yr[4][4] = {}, xyi[4][4] = {};  // xyi = xi + yi (only their sum is used)
   for (int I = 0; I <= Bk; ++I) {  // row side: R = Bk, I = 0..Bk
     const float *Dv = (I < Bk) ? vec + (V_D + Bk * (Bk - 1) / 2 + I) * kD : nullptr;
     uint32_t aLh[4], aLl[4], aQh[4], aQl[4];
@@ -356,7 +351,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
     lda_t(sbase + C_DQK, kC, 16 * Bk, 16 * I, aQh);  // dAqk[r][i] = dAqk^T[i][r]
     lda_t(sbase + C_DQK + LO64, kC, 16 * Bk, 16 * I, aQl);
 #pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
+    for (int nb = 0; nb < 2; ++nb) {
       uint32_t bh[4], bl[4];
       ldb_t(sbase + C_KC, kC, ch0 + 16 * nb, 16 * I, bh);  // element (i, c) = Kc[i][c]
       ldb_t(sbase + C_KC + LO128, kC, ch0 + 16 * nb, 16 * I, bl);
@@ -382,7 +377,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
     lda(sbase + C_DQK, kC, 16 * Bk, 16 * R, aQh);  // element (i, r) = dAqk^T[i][r]
     lda(sbase + C_DQK + LO64, kC, 16 * Bk, 16 * R, aQl);
 #pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
+    for (int nb = 0; nb < 2; ++nb) {
       uint32_t kh[4], kl[4], qh[4], ql[4];
       ldb_t(sbase + C_KR, kC, ch0 + 16 * nb, 16 * R, kh);  // element (r, c) = Kr[r][c]
       ldb_t(sbase + C_KR + LO128, kC, ch0 + 16 * nb, 16 * R, kl);
@@ -403,13 +398,13 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
   __syncthreads();  // every warp is done with the chain tiles: A .. X become the product staging
   KDA_PT(5);
 
-  // ---- assembly (fragment element (r, c)), in four passes of 16 columns per warp ----
+  // ---- assembly (fragment element (r, c)), in four passes of 8 columns per warp ----
   // Raw k and q are not re-read: every term that needs them is a product with
   // a decay factor that the hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2 hold.
   // dg = reverse cumsum of dG over the chunk runs per pass as column scans
-  // over 8-row segments with segment totals exchanged in shared memory.
+  // over 4-row segments with segment totals exchanged in shared memory.
   float *sQ = (float *)(sm + C_SQ), *sP = (float *)(sm + C_SP);
-  float *totQ = (float *)(sm + C_TOT), *totP = totQ + 8 * 32;
+  float *totQ = (float *)(sm + C_TOT), *totP = totQ + 16 * 32;
   const float *dglv = (const float *)(sm + C_DGL), *dbxv = (const float *)(sm + C_DBX);
   const int i8 = lane >> 2, l4 = lane & 3, mid = len >> 1;
   float bpart[2] = {0.f, 0.f};
@@ -420,15 +415,15 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
     else cp_wait_all();
     __syncthreads();
     KDA_PT(9);
-    float *totC = totP + 8 * 32 + (g & 1) * 4 * 32;  // double-buffered: read after the next pass starts
+    float *totC = totP + 16 * 32 + (g & 1) * 4 * 32;  // double-buffered: read after the next pass starts
     const uint32_t bq = (g & 1) ? C_ST1 : C_ST0_QB, bb = bq + ST_BYTES, bk = (g & 1) ? C_ST1 + 2 * ST_BYTES : C_ST0_K;
     {
-      float qv[2][2][2], pv[2][2][2], cq[2][2];  // [nt of the pass][hh][u], column sums [nt][u]
+      float qv[1][2][2], pv[1][2][2], cq[1][2];  // [nt of the pass][hh][u], column sums [nt][u]
 #pragma unroll
-      for (int ntl = 0; ntl < 2; ++ntl) {
-        const int nt = 2 * g + ntl;
+      for (int ntl = 0; ntl < 1; ++ntl) {
+        const int nt = g;
         const int c = ch0 + 8 * nt + 2 * l4;
-        const int lc = 16 * (ch0 >> 6) + 8 * ntl + 2 * l4;  // column in the staging
+        const int lc = 8 * (warp & 3) + 2 * l4;  // column in the staging
         const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
         const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
         const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
@@ -489,8 +484,8 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       KDA_PT(10);
       // dG of this pass's 32 columns -> shared memory, then the column scans
 #pragma unroll
-      for (int ntl = 0; ntl < 2; ++ntl) {
-        const int lc = 16 * (ch0 >> 6) + 8 * ntl + 2 * l4;
+      for (int ntl = 0; ntl < 1; ++ntl) {
+        const int lc = 8 * (warp & 3) + 2 * l4;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int r = 16 * Bk + i8 + 8 * hh;
@@ -509,14 +504,14 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
       __syncthreads();  // buffer g & 1 consumed; dG tiles complete
       if (g + 2 < 4) stage(g + 2);
       KDA_PT(11);
-      {  // thread: one column of the pass, one 8-row segment (warp = segment)
+      {  // thread: one column of the pass, one 4-row segment (warp = segment)
         const int col = tid & 31, seg = warp;
-        const int cc = (col < 16) ? 16 * g + col : 64 + 16 * g + (col - 16);
-        float q8[8], p8[8], tq = 0.f, tp = 0.f;
+        const int cc = 32 * (col >> 3) + 8 * g + (col & 7);
+        float q8[4], p8[4], tq = 0.f, tp = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          q8[k] = sQ[(8 * seg + k) * SQ_LD + col];
-          p8[k] = sP[(8 * seg + k) * SQ_LD + col];
+        for (int k = 0; k < 4; ++k) {
+          q8[k] = sQ[(4 * seg + k) * SQ_LD + col];
+          p8[k] = sP[(4 * seg + k) * SQ_LD + col];
           tq += q8[k];
           tp += p8[k];
         }
@@ -525,7 +520,7 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
         __syncthreads();
         float aq = 0.f, aps = 0.f, app = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) {
+        for (int s2 = 0; s2 < 16; ++s2) {
           const float a = totQ[s2 * 32 + col], b = totP[s2 * 32 + col];
           if (s2 > seg) { aq += a; aps += b; }
           if (s2 < seg) app += b;
@@ -536,14 +531,14 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
         // (sum_{s>=t} P_s = -sum_{s<t} P_s, the Khat column sum counted at the
         // last row), halving the cancelling terms it sums.
         const float carried = kLn2 * vec[V_GAML * kD + cc] * dglv[cc];
-        float pre[8];
+        float pre[4];
         pre[0] = app;
 #pragma unroll
-        for (int k = 1; k < 8; ++k) pre[k] = pre[k - 1] + p8[k - 1];
+        for (int k = 1; k < 4; ++k) pre[k] = pre[k - 1] + p8[k - 1];
         float qs = aq, ps = aps + kLn2 * ks;
 #pragma unroll
-        for (int k = 7; k >= 0; --k) {
-          const int r = 8 * seg + k;
+        for (int k = 3; k >= 0; --k) {
+          const int r = 4 * seg + k;
           qs += q8[k];
           ps += p8[k];
           if (r < len)
@@ -560,12 +555,12 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_chain_tc_kernel(Problem P, Wo
     float v = bpart[hh];
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
-    if (l4 == 0) rb[(warp & 1) * kC + 16 * Bk + i8 + 8 * hh] = v;
+    if (l4 == 0) rb[(warp & 3) * kC + 16 * Bk + i8 + 8 * hh] = v;
   }
   __syncthreads();
   KDA_PT(7);
   if (tid < kC && tid < len)
-    args.dbeta[(size_t)(t0 + tid) * HV + j] = dbxv[tid] + rb[tid] + rb[kC + tid];
+    args.dbeta[(size_t)(t0 + tid) * HV + j] = dbxv[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
   KDA_PT(8);
   KDA_PT_FLUSH;
 }
@@ -582,7 +577,7 @@ cudaError_t tc_backward_chain(const Problem &P, const Workspace &W, void *dq, vo
   if (e != cudaSuccess) return e;
   const bool partial = P.HV != P.H;
   ChainArgs a{partial ? (void *)W.dqp : dq, partial ? (void *)W.dkp : dk, dg, dbeta, partial};
-  KDA_LAUNCH("kda_bwd_chain_tc", s, kda_bwd_chain_tc_kernel<<<dim3(P.NC, P.HV), kThr, C_SMEM, s>>>(P, W, a));
+  KDA_LAUNCH("kda_bwd_chain_tc", s, kda_bwd_chain_tc_kernel<<<dim3(P.NC, P.HV), kCT, C_SMEM, s>>>(P, W, a));
   return cudaGetLastError();
 }
 

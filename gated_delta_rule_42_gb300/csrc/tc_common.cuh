@@ -142,9 +142,10 @@ __device__ __forceinline__ uint32_t idesc(int M, int N, int a_mn, int b_mn) {
 
 // Asynchronous loads of one chunk's rows of a [tokens][heads][128] bf16
 // tensor into a swizzled [64][128] tile; rows at or past len are zeroed.
+template <int NT = kThr>
 __device__ __forceinline__ void load_rows(uint32_t tile, const __nv_bfloat16 *src, int t0, int len,
                                           int heads, int head) {
-  for (int it = threadIdx.x; it < kC * 16; it += kThr) {
+  for (int it = threadIdx.x; it < kC * 16; it += NT) {
     const int r = it >> 4, jj = it & 15;
     const uint32_t dst = tile + sw_chunk(r, jj, kC);
     if (r < len) cp16(dst, src + ((size_t)(t0 + r) * heads + head) * kD + jj * 8);
@@ -152,8 +153,9 @@ __device__ __forceinline__ void load_rows(uint32_t tile, const __nv_bfloat16 *sr
   }
 }
 
+template <int NT = kThr>
 __device__ __forceinline__ void load_gate(uint32_t tile, const float *g, int t0, int len, int HV, int j) {
-  for (int it = threadIdx.x; it < kC * 32; it += kThr) {
+  for (int it = threadIdx.x; it < kC * 32; it += NT) {
     const int r = it >> 5, jj = it & 31;
     const uint32_t dst = tile + (uint32_t)(r * kGLD + jj * 4) * 4u;
     if (r < len) cp16(dst, g + ((size_t)(t0 + r) * HV + j) * kD + jj * 4);
