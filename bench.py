@@ -73,13 +73,14 @@ def kernel_bytes_per_token(name, cfg):
     qk, vv, g, b = H * K * e, HV * V * e, 4 * HV * K, 4 * HV
     f32K, f32V, cc, hh = 4 * HV * K, 4 * HV * V, 4 * HV * 64, 4 * HV * K * V / 64
     hs = 2 * HV * K * V / 64            # bf16 K x V state per chunk, per token
-    t16 = 16384 * HV / 64               # one 16 KB per-chunk tile (Aqk+A, X^T or D^T), per token
+    t16 = 16384 * HV / 64               # one 16 KB per-chunk tile (X^T or D^T), per token
+    rec = (65536 + 512) * HV / 64       # the per-chunk tile record (Bk, Qg, Khat, Aqk, A, 2^G_last), per token
     dgl = 4 * HV * K / 64               # fp32 K-vector per chunk, per token
     table = {
         # tensor-core path (bf16, K = V = 128)
         "kda_fwd_tc": 2 * qk + 2 * vv + g + b,
-        "kda_fwd_tc_states": 2 * qk + vv + g + b + hs + 3 * t16,
-        "kda_bwd_scan_tc": 2 * qk + g + b + vv + t16 + hs + 2 * vv,
+        "kda_fwd_tc_states": 2 * qk + vv + g + b + hs + rec + 2 * t16,
+        "kda_bwd_scan_tc": rec + vv + hs + 2 * vv,
         "kda_bwd_gemm_tc": 2 * t16 + 2 * hs + 3 * vv + vv + b + vv + 3 * f32K + 2 * cc + b + dgl,
         "kda_bwd_chain_tc": g + b + t16 / 2 + 3 * f32K + 2 * cc + 2 * qk + b + dgl + 2 * qk + g + b,
         # fp32 path

@@ -100,7 +100,7 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   if (use_tc(P)) {
     if (backward) {  // tensor-core backward: per-slot bf16 / fp32 intermediates
       w.tc_hs = (__nv_bfloat16 *)take(2 * slots * K * V);
-      w.tc_aqk_a = (unsigned char *)take(16384 * slots);
+      w.tc_tiles = (unsigned char *)take(kTileRecord * slots);
       w.tc_xt = (unsigned char *)take(16384 * slots);
       w.tc_dt = (unsigned char *)take(16384 * slots);
       w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);

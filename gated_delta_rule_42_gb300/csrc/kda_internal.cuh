@@ -12,6 +12,10 @@ namespace kda {
 
 constexpr int kChunk = 64;    // tokens per chunk
 constexpr int kMaxDim = 128;  // largest K and V the kernels are built for
+// Per-slot record of the chunk tiles the states pass saves for the reverse scan
+// and the gradient chain: Bk, Qg, Khat (16 KB each), Aqk, A (8 KB each), 2^G_last.
+constexpr size_t kTileRecord = 65536 + 512;
+constexpr size_t kTileRecA = 57344;  // offset of the A tile in the record
 
 // A chunk-table entry: the chunk's logical sequence n (-1 = unused slot), its
 // first packed token, its length (1..64) and its index inside the sequence.
@@ -47,7 +51,7 @@ struct Workspace {
   float *dw;     // [slot][64][K]
   // tensor-core backward (bf16, K = V = 128), per (chunk, value head) slot
   __nv_bfloat16 *tc_hs;     // [slot][K][V]  chunk-start state (forward recompute)
-  unsigned char *tc_aqk_a;  // [slot] 16 KB: swizzled Aqk tile, then A = (I+L)^-1 tile
+  unsigned char *tc_tiles;  // [slot] kTileRecord bytes: swizzled Bk | Qg | Khat | Aqk | A tiles, then 2^G_last (fp32 [K])
   unsigned char *tc_xt;     // [slot] 16 KB: swizzled X^T tile [V][64]
   unsigned char *tc_dt;     // [slot] 16 KB: swizzled D^T tile [V][64]
   __nv_bfloat16 *tc_dh;     // [slot][K][V]  gradient of the chunk-end state
@@ -113,7 +117,7 @@ cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t 
 // bf16, K = V = 128 tensor-core forward.  With states = true it runs in
 // "states" mode for the backward: no output; per (chunk, value head) slot it
 // saves the chunk-start state and the Aqk, A, X^T and D^T tiles to
-// W.tc_hs / tc_aqk_a / tc_xt / tc_dt.
+// W.tc_hs / tc_tiles / tc_xt / tc_dt.
 cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, bool states,
                        int *err, cudaStream_t s);
 cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,

@@ -152,8 +152,8 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Wor
 
   // ---- loads ----
   load_gate<kCT>(sbase + C_G, P.g, t0, len, HV, j);
-  {  // A, saved by the forward recompute in this kernel's swizzled layout (after the 8 KB Aqk tile)
-    const unsigned char *src = W.tc_aqk_a + slot * 16384 + 8192;
+  {  // A, saved by the forward recompute in this kernel's swizzled layout
+    const unsigned char *src = W.tc_tiles + slot * kTileRecord + kTileRecA;
     for (int it = tid; it < 512; it += kCT) cp16(sbase + C_A + it * 16, src + it * 16);
   }
   if (tid < kC) {

@@ -3,9 +3,9 @@
 // One CTA walks the chunks of one (sequence, value head) from last to first,
 // holding dh' -- the gradient of the chunk-END state -- in fp32 registers
 // (thread = key channel c, half the value columns), starting from dhT (or 0).
-// Per chunk, with the chunk-level tiles of phase (a) of tc_common.cuh rebuilt
-// from q, k, g, beta and the Aqk / A tiles saved by the forward recompute,
-// on tcgen05:
+// Per chunk, with the chunk tiles Bk = beta k 2^G, Qg = q~ 2^G, Khat =
+// k 2^(G_last - G), Aqk, A and 2^G_last saved by the forward recompute (one
+// bulk copy per chunk: the scan reads no q, k, g or beta), on tcgen05:
 //   dD^T = dO^T Aqk + dh'^T Khat^T        dD = Aqk^T dO + Khat dh'   (deltas' gradient)
 //   dX^T = dD^T A                         dX = A^T dD                (through A = (I+L)^-1)
 //   dh  <- diag(2^G_last) dh' + Qg^T dO - Bk^T dX                    (gradient of the chunk-start state)
@@ -29,20 +29,18 @@ constexpr uint32_t TMEM_COLS = 256;  // [0,64) dD^T, [64,128) dX^T, [128,256) dh
 
 __global__ void __launch_bounds__(kThr, 1)
 kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__ dO,
-                       const float *__restrict__ dhT, float *__restrict__ dh0, int *err,
-                       const __grid_constant__ TmaMaps maps) {
+                       const float *__restrict__ dhT, float *__restrict__ dh0, int *err) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
   float *vec = (float *)(sm + OFF_VEC);
-  float *betab = (float *)(sm + OFF_BETA);
   uint64_t *bar = (uint64_t *)(sm + OFF_MISC);
   uint32_t *tslot = (uint32_t *)(sm + OFF_MISC + 8);
-  uint64_t *bar_kqg = (uint64_t *)(sm + OFF_MISC + 16);
+  uint64_t *bar_t = (uint64_t *)(sm + OFF_MISC + 16);
   unsigned char *U = sm + OFF_U;
 
   const int n = blockIdx.x, j = blockIdx.y;
-  const int HV = P.HV, h = j / (HV / P.H);
+  const int HV = P.HV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, vhalf = warp >> 2;
   const int cown = quarter * 32 + lane;
@@ -50,7 +48,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
 
   if (tid == 0) {
     bar_init(bar, 1);
-    bar_init(bar_kqg, 1);
+    bar_init(bar_t, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
@@ -59,7 +57,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
   fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
-  uint32_t phase = 0, kq_par = 0;
+  uint32_t phase = 0, t_par = 0;
 
   float dreg[64];  // dh'[cown][64 * vhalf + x]
   {
@@ -72,43 +70,29 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
     }
   }
 
-  // the saved Aqk and A tiles of one chunk (16 KB, verbatim) from the forward recompute
-  auto load_aqk_a = [&](int cidx) {
-    const unsigned char *src = W.tc_aqk_a + ((size_t)cidx * HV + j) * 16384;
-    for (int it = tid; it < 1024; it += kThr) cp16(sbase + OFF_AQK + it * 16, src + it * 16);
+  // The chunk tiles Bk, Qg, Khat, Aqk, A and 2^G_last saved by the forward
+  // recompute: one bulk copy of the 64 KB record (the Bk .. A region of the
+  // shared-memory map, same swizzled layout) and one of the 512-byte vector.
+  auto load_tiles = [&](int cidx) {
+    const unsigned char *src = W.tc_tiles + ((size_t)cidx * HV + j) * kTileRecord;
+    mbar_expect_tx(bar_t, 65536u + 512u);
+    bulk_load(sbase + OFF_BK, src, 65536u, bar_t);
+    bulk_load(smem_u32(vec + V_GAML * kD), src + 65536, 512u, bar_t);
   };
   if (si.w > 0) {
     const int2 chl = chunk_span(si, si.w - 1);
-    if (tid == 0) tma_kqg(maps, sbase, chl.x, h, j, true, bar_kqg);
-    load_beta(P, betab, chl.x, chl.y, j);
+    if (tid == 0) load_tiles(si.z + si.w - 1);
     load_rows(sbase + OFF_VRAW, dO, chl.x, chl.y, HV, j);
-    load_aqk_a(si.z + si.w - 1);
     cp_commit();
   }
 
   for (int ci = si.w - 1; ci >= 0; --ci) {
     const int cidx = si.z + ci;
-    const int len = chunk_span(si, ci).y;
-    const int buf = (si.w - 1 - ci) & 1;
-    const float *beta = betab + buf * kC;
     const size_t slot = (size_t)cidx * HV + j;
-    cp_wait_all();  // beta, dO, Aqk / A
-    bar_wait(bar_kqg, kq_par, err);
-    kq_par ^= 1;
-    if (len < kC) {  // rows past the sequence end hold other tokens: clear them
-      zero_tail(sm + OFF_KRAW, len);
-      zero_tail(sm + OFF_QRAW, len);
-      fence_async_smem();
-    }
+    cp_wait_all();  // dO
+    bar_wait(bar_t, t_par, err);
+    t_par ^= 1;
     __syncthreads();
-
-    phase_a<true, false>(sm, len, beta);
-    if (ci > 0) {
-      const int2 pv = chunk_span(si, ci - 1);
-      if (tid == 0) tma_kqg(maps, sbase, pv.x, h, j, true, bar_kqg);
-      load_beta(P, betab + (buf ^ 1) * kC, pv.x, pv.y, j);
-      cp_commit();
-    }
 
     // ---------------- (c) ----------------
     {
@@ -215,10 +199,13 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
     fence_before();
     __syncthreads();
     fence_after();
-    if (ci > 0) {  // dO, Aqk and A of this chunk consumed
+    if (ci > 0) {  // dO, the tiles and 2^G_last of this chunk consumed
       const int2 pv = chunk_span(si, ci - 1);
+      if (tid == 0) {
+        fence_async_smem();
+        load_tiles(cidx - 1);
+      }
       load_rows(sbase + OFF_VRAW, dO, pv.x, pv.y, HV, j);
-      load_aqk_a(cidx - 1);
       cp_commit();
     }
   }
@@ -245,11 +232,9 @@ cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *d
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  TmaMaps maps;
-  if ((e = make_tma_maps(P, nullptr, &maps)) != cudaSuccess) return e;
   KDA_LAUNCH("kda_bwd_scan_tc", s,
              kda_bwd_scan_tc_kernel<<<dim3(P.N, P.HV), kThr, SMEM_BYTES, s>>>(
-                 P, W, (const __nv_bfloat16 *)dO, dhT, dh0, err, maps));
+                 P, W, (const __nv_bfloat16 *)dO, dhT, dh0, err));
   return cudaGetLastError();
 }
 

@@ -100,6 +100,9 @@ constexpr uint32_t OFF_BETA = 225280;  // beta, two buffers of 64 fp32
 constexpr uint32_t OFF_MISC = 225792;  // mbarriers (MMA +0, k/q/g loads +16, v loads +24), tmem slot +8
 constexpr uint32_t SMEM_BYTES = 225792 + 64 + 1024;  // + alignment slack
 constexpr int V_GL = 0, V_GAML = 1, V_GREF = 2, V_EREF = 6, V_D = 10, V_LAM = 16;
+static_assert(OFF_QG == OFF_BK + 16384 && OFF_KH == OFF_QG + 16384 && OFF_AQK == OFF_KH + 16384 &&
+                  OFF_AM == OFF_AQK + 8192 && OFF_AM - OFF_BK == kTileRecA && OFF_AM + 8192 - OFF_BK == 65536,
+              "the saved tile record is the contiguous Bk .. A region");
 
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
@@ -174,6 +177,12 @@ __device__ __forceinline__ int2 chunk_span(const int4 &si, int ci) {
 // ---- TMA (bulk tensor) loads of the per-token tiles ----
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// Contiguous global -> shared bulk copy (16-byte aligned, size a multiple of 16); completion on bar.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 // Box (c0, c1, c2) of a 3-D tensor map into shared memory; completion counted on bar.
 __device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {

@@ -19,7 +19,7 @@
 //
 // In "states" mode (no output) the kernel saves, per chunk, what the backward
 // needs from the forward recompute: the chunk-start state h_c (bf16 row-major
-// [K][V]) and the swizzled tiles Aqk, A, X^T and D^T, copied verbatim.
+// [K][V]) and the swizzled tiles Bk, Qg, Khat, Aqk, A, X^T and D^T, copied verbatim.
 #include "tc_common.cuh"
 
 namespace kda {
@@ -121,10 +121,11 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     }
     KDA_PT(3);
     phase_b<true>(sm, beta);
-    if (!kOut) {  // Aqk and A tiles (adjacent, 16 KB) for the backward, verbatim
-      const uint4 *src = (const uint4 *)(sm + OFF_AQK);
-      uint4 *dst = (uint4 *)(W.tc_aqk_a + slot * 16384);
-      for (int e = tid; e < 1024; e += kThr) dst[e] = src[e];
+    if (!kOut) {  // Bk, Qg, Khat, Aqk, A tiles (adjacent, 64 KB) and 2^G_last for the backward, verbatim
+      const uint4 *src = (const uint4 *)(sm + OFF_BK);
+      uint4 *dst = (uint4 *)(W.tc_tiles + slot * kTileRecord);
+      for (int e = tid; e < 4096; e += kThr) dst[e] = src[e];
+      if (tid < 32) dst[4096 + tid] = reinterpret_cast<const uint4 *>(vec + V_GAML * kD)[tid];
     }
 
     // ---------------- (c) state chain on tcgen05 ----------------
