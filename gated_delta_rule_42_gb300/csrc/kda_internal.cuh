@@ -50,7 +50,7 @@ struct Workspace {
   float *dkp;    // [Ttot][HV][K]
   float *dw;     // [slot][64][K]
   // tensor-core backward (bf16, K = V = 128), per (chunk, value head) slot
-  __nv_bfloat16 *tc_hs;     // [slot][K][V]  chunk-start state (forward recompute)
+  __nv_bfloat16 *tc_hs;     // [slot] 32 KB: chunk-start state h [K][V], swizzled operand tile (forward recompute)
   unsigned char *tc_tiles;  // [slot] kTileRecord bytes: swizzled Bk | Qg | Khat | Aqk | A tiles, then 2^G_last (fp32 [K])
   unsigned char *tc_xt;     // [slot] 16 KB: swizzled X^T tile [V][64]
   unsigned char *tc_dt;     // [slot] 16 KB: swizzled D^T tile [V][64]

@@ -184,6 +184,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// Contiguous shared -> global bulk copy (16-byte aligned, size a multiple of 16), in the
+// calling thread's bulk group; the source must stay unchanged until bulk_wait_read().
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// The calling thread's bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// The calling thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 // Box (c0, c1, c2) of a 3-D tensor map into shared memory; completion counted on bar.
 __device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
   asm volatile(
@@ -348,48 +359,57 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
   const float *vec = (const float *)(sm + OFF_VEC);
   unsigned char *U = sm + OFF_U;
   float *Lf = (float *)(U + U_LF);
-  // Gram blocks: the 10 block pairs R >= I, each split into its two 8-column
-  // halves: 20 equal units over the 8 warps.
-  for (int u = warp; u < 20; u += 8) {
-    const int p = u >> 1, nt = u & 1;
+  // Gram blocks: the 10 block pairs R >= I over the 8 warps (the A fragments of
+  // a pair serve both 8-column halves: shared-memory wavefronts bound this phase).
+  for (int p = warp; p < 10; p += 8) {
     const int R = p >= 6 ? 3 : p >= 3 ? 2 : p >= 1 ? 1 : 0, I = p - R * (R + 1) / 2;
     const float *Dv = (I < R) ? vec + (V_D + R * (R - 1) / 2 + I) * kD : nullptr;
-    float accL[4] = {}, accQ[4] = {};
+    float accL[2][4] = {}, accQ[2][4] = {};
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
-      uint32_t ak[4], aq[4] = {0, 0, 0, 0}, b0, b1;
+      uint32_t ak[4], aq[4] = {0, 0, 0, 0}, b[4];
       {
         const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
         ldsm_x4(sbase + OFF_U + U_KR + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
         if (kQ) ldsm_x4(sbase + OFF_U + U_QR + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
       }
       {
-        const int row = 16 * I + 8 * nt + (lane & 7), jj = 2 * s + ((lane >> 3) & 1);
-        ldsm_x2(sbase + OFF_U + U_KC + sw_chunk(row, jj, kC), b0, b1);
+        const int mi = lane >> 3;
+        const int row = 16 * I + (lane & 7) + (mi >> 1) * 8, jj = 2 * s + (mi & 1);
+        ldsm_x4(sbase + OFF_U + U_KC + sw_chunk(row, jj, kC), b[0], b[1], b[2], b[3]);
       }
       if (Dv != nullptr) {
         const int c0 = 16 * s + (lane & 3) * 2;
         const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
         const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
-        const float2 f0 = unpack_bf16(b0), f1 = unpack_bf16(b1);
-        b0 = pack_bf16(f0.x * d01.x, f0.y * d01.y);
-        b1 = pack_bf16(f1.x * d89.x, f1.y * d89.y);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = unpack_bf16(b[t]);
+          b[t] = (t & 1) ? pack_bf16(f.x * d89.x, f.y * d89.y) : pack_bf16(f.x * d01.x, f.y * d01.y);
+        }
       }
-      mma16816(accL, ak, b0, b1);
-      if (kQ) mma16816(accQ, aq, b0, b1);
+      mma16816(accL[0], ak, b[0], b[1]);
+      mma16816(accL[1], ak, b[2], b[3]);
+      if (kQ) {
+        mma16816(accQ[0], aq, b[0], b[1]);
+        mma16816(accQ[1], aq, b[2], b[3]);
+      }
     }
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int r = 16 * R + (lane >> 2) + hh * 8;
-      const int i = 16 * I + nt * 8 + (lane & 3) * 2;
-      const float br = beta[r];
-      const float l0 = (i < r) ? br * accL[2 * hh] : 0.f;
-      const float l1 = (i + 1 < r) ? br * accL[2 * hh + 1] : 0.f;
-      *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
-      if (kQ) {
-        const float a0 = (i <= r) ? accQ[2 * hh] : 0.f;
-        const float a1 = (i + 1 <= r) ? accQ[2 * hh + 1] : 0.f;
-        st_bf2(sm + OFF_AQK, r, i, kC, a0, a1);
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * R + (lane >> 2) + hh * 8;
+        const int i = 16 * I + nt * 8 + (lane & 3) * 2;
+        const float br = beta[r];
+        const float l0 = (i < r) ? br * accL[nt][2 * hh] : 0.f;
+        const float l1 = (i + 1 < r) ? br * accL[nt][2 * hh + 1] : 0.f;
+        *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
+        if (kQ) {
+          const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
+          const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
+          st_bf2(sm + OFF_AQK, r, i, kC, a0, a1);
+        }
       }
     }
   }
@@ -409,11 +429,24 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
 #pragma unroll
     for (int m = 0; m < 16; ++m) a[m] = (m == i) ? 1.f : 0.f;
     // column-oriented substitution: once a[m] is final, subtract its multiples
-    // from every later row (independent updates: a short dependency chain)
+    // from every later row (independent updates: a short dependency chain);
+    // L is read four columns at a time (one float4 per row and column group)
 #pragma unroll
-    for (int m = 0; m < 15; ++m)
+    for (int mg = 0; mg < 4; ++mg) {
+      float4 lr[16];
 #pragma unroll
-      for (int r = m + 1; r < 16; ++r) a[r] = fmaf(-Lf[fsw(16 * R + r, 16 * R + m)], a[m], a[r]);
+      for (int r = 4 * mg + 1; r < 16; ++r)
+        lr[r] = *reinterpret_cast<const float4 *>(Lf + fsw(16 * R + r, 16 * R + 4 * mg));
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm) {
+        const int m = 4 * mg + mm;
+#pragma unroll
+        for (int r = m + 1; r < 16; ++r) {
+          const float l = mm == 0 ? lr[r].x : mm == 1 ? lr[r].y : mm == 2 ? lr[r].z : lr[r].w;
+          a[r] = fmaf(-l, a[m], a[r]);
+        }
+      }
+    }
 #pragma unroll
     for (int m = 0; m < 16; ++m) Af[fsw(16 * R + m, 16 * R + i)] = a[m];
   }
@@ -484,6 +517,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     for (int t = 0; t < 8; ++t) x[t] = Af[fsw(r, jj * 8 + t)];
     *reinterpret_cast<uint4 *>(sm + OFF_AM + sw_chunk(r, jj, kC)) = pack8(x);
   }
+  fence_async_smem();  // the tiles may be read next by the async proxy (bulk stores)
   __syncthreads();
   KDA_PT(6);
 }

@@ -18,8 +18,9 @@
 // torchtitan (training)" (pytorch/torchtitan PR #4164).
 //
 // In "states" mode (no output) the kernel saves, per chunk, what the backward
-// needs from the forward recompute: the chunk-start state h_c (bf16 row-major
-// [K][V]) and the swizzled tiles Bk, Qg, Khat, Aqk, A, X^T and D^T, copied verbatim.
+// needs from the forward recompute, as bulk copies of its shared-memory tiles
+// (swizzled, verbatim): the chunk-start state h_c (bf16 [K][V]), the record
+// Bk | Qg | Khat | Aqk | A with 2^G_last, and X^T, D^T.
 #include "tc_common.cuh"
 
 namespace kda {
@@ -101,6 +102,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     const size_t slot = (size_t)cidx * HV + j;
     const float *beta = betab + (ci & 1) * kC;
     cp_wait_all();  // beta
+    if (!kOut && tid == 0) bulk_wait_read();  // the previous chunk's saved tiles have left shared memory
     bar_wait(bar_kqg, kq_par, args.err);
     kq_par ^= 1;
     if (len < kC) {  // rows past the sequence end hold other tokens: clear them
@@ -121,11 +123,11 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     }
     KDA_PT(3);
     phase_b<true>(sm, beta);
-    if (!kOut) {  // Bk, Qg, Khat, Aqk, A tiles (adjacent, 64 KB) and 2^G_last for the backward, verbatim
-      const uint4 *src = (const uint4 *)(sm + OFF_BK);
-      uint4 *dst = (uint4 *)(W.tc_tiles + slot * kTileRecord);
-      for (int e = tid; e < 4096; e += kThr) dst[e] = src[e];
-      if (tid < 32) dst[4096 + tid] = reinterpret_cast<const uint4 *>(vec + V_GAML * kD)[tid];
+    if (!kOut && tid == 0) {  // Bk, Qg, Khat, Aqk, A tiles (adjacent, 64 KB) and 2^G_last
+      unsigned char *dst = W.tc_tiles + slot * kTileRecord;
+      bulk_store(dst, sbase + OFF_BK, 65536u);
+      bulk_store(dst + 65536, smem_u32(vec + V_GAML * kD), 512u);
+      bulk_commit();
     }
 
     // ---------------- (c) state chain on tcgen05 ----------------
@@ -141,7 +143,6 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
         for (int e = 0; e < 8; ++e) t[e] = hreg[8 * x8 + e];
         const uint4 u = pack8(t);
         *reinterpret_cast<uint4 *>(H + sw_chunk(cown, 8 * vhalf + x8, kD)) = u;
-        if (!kOut) *reinterpret_cast<uint4 *>(W.tc_hs + (slot * kD + cown) * kD + 64 * vhalf + 8 * x8) = u;
       }
     }
     fence_async_smem();
@@ -150,6 +151,13 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     fence_after();
     KDA_PT(8);
     const uint32_t aH = sbase + OFF_U + U_H, aXT = sbase + OFF_U + U_XT;
+    // D^T reuses the X^T tile, except in states mode, where X^T is still being saved
+    const uint32_t aD = kOut ? aXT : sbase + OFF_U + U_O;
+    unsigned char *Dt = kOut ? U + U_XT : U + U_O;
+    if (!kOut && tid == 0) {  // h_c for the backward
+      bulk_store(W.tc_hs + slot * kD * kD, aH, 32768u);
+      bulk_commit();
+    }
     if (tid == 0) {  // X'^T[v][r] = sum_c h[c][v] Bk[r][c]   (M=128 v, N=64 r, K=128 c)
       const uint32_t id = idesc(128, 64, 1, 0);
 #pragma unroll
@@ -181,10 +189,9 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     __syncthreads();
     fence_after();
     KDA_PT(10);
-    if (!kOut) {  // X^T tile for the backward, verbatim
-      const uint4 *src = (const uint4 *)(U + U_XT);
-      uint4 *dst = (uint4 *)(W.tc_xt + slot * 16384);
-      for (int e = tid; e < 1024; e += kThr) dst[e] = src[e];
+    if (!kOut && tid == 0) {  // X^T tile for the backward
+      bulk_store(W.tc_xt + slot * 16384, aXT, 16384u);
+      bulk_commit();
     }
     if (ci + 1 < si.w && tid == 0) {  // v of this chunk consumed
       const int2 nx = chunk_span(si, ci + 1);
@@ -201,7 +208,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     phase ^= 1;
     fence_after();
     KDA_PT(11);
-    {  // D^T -> bf16 tile [v][r] (reuses the X^T tile)
+    {  // D^T -> bf16 tile [v][r]
       const int v = cown, r0 = 32 * vhalf;
       float d[32];
       tmem_ld32(tq + 64u + (uint32_t)r0, d);
@@ -210,7 +217,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = d[q8 * 8 + e];
-        *reinterpret_cast<uint4 *>(U + U_XT + sw_chunk(v, (r0 >> 3) + q8, kD)) = pack8(x);
+        *reinterpret_cast<uint4 *>(Dt + sw_chunk(v, (r0 >> 3) + q8, kD)) = pack8(x);
       }
     }
     fence_async_smem();
@@ -218,10 +225,9 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     __syncthreads();
     fence_after();
     KDA_PT(12);
-    if (!kOut) {  // D^T tile for the backward, verbatim
-      const uint4 *src = (const uint4 *)(U + U_XT);
-      uint4 *dst = (uint4 *)(W.tc_dt + slot * 16384);
-      for (int e = tid; e < 1024; e += kThr) dst[e] = src[e];
+    if (!kOut && tid == 0) {  // D^T tile for the backward
+      bulk_store(W.tc_dt + slot * 16384, aD, 16384u);
+      bulk_commit();
     }
     if (tid == 0) {
       if (kOut) {  // O^T[v][r] = sum_c h[c][v] Qg[r][c] + sum_i D^T[v][i] Aqk[r][i]
@@ -229,13 +235,13 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
 #pragma unroll
         for (int s = 0; s < 8; ++s) mma(tmem, desc_mn(aH, s, 16384), desc_k16(sbase + OFF_QG, s, kC), id, s > 0);
 #pragma unroll
-        for (int s = 0; s < 4; ++s) mma(tmem, desc_k16(aXT, s, kD), desc_k16(sbase + OFF_AQK, s, kC), id2, 1);
+        for (int s = 0; s < 4; ++s) mma(tmem, desc_k16(aD, s, kD), desc_k16(sbase + OFF_AQK, s, kC), id2, 1);
       }
       // U[c][v] = sum_r Khat[r][c] D[r][v]   (M=128 c, N=128 v, K=64 r)
       const uint32_t id3 = idesc(128, 128, 1, 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma(tmem + 128, desc_mn(sbase + OFF_KH, s, 8192), desc_k16(aXT, s, kD), id3, s > 0);
+        mma(tmem + 128, desc_mn(sbase + OFF_KH, s, 8192), desc_k16(aD, s, kD), id3, s > 0);
       commit(bar);
     }
     bar_wait(bar, phase, args.err);
@@ -280,6 +286,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     for (int x = 0; x < 64; x += 4)
       *reinterpret_cast<float4 *>(dst + x) = make_float4(hreg[x], hreg[x + 1], hreg[x + 2], hreg[x + 3]);
   }
+  if (!kOut && tid == 0) bulk_wait_all();  // the saved tiles are in global memory before the CTA exits
   fence_before();
   __syncthreads();
   if (warp == 0) {
