@@ -54,7 +54,7 @@ struct Workspace {
   unsigned char *tc_tiles;  // [slot] kTileRecord bytes: swizzled Bk | Qg | Khat | Aqk | A tiles, then 2^G_last (fp32 [K])
   unsigned char *tc_xt;     // [slot] 16 KB: swizzled X^T tile [V][64]
   unsigned char *tc_dt;     // [slot] 16 KB: swizzled D^T tile [V][64]
-  __nv_bfloat16 *tc_dh;     // [slot][K][V]  gradient of the chunk-end state
+  __nv_bfloat16 *tc_dh;     // [slot] 32 KB: gradient of the chunk-end state [K][V], swizzled operand tile
   __nv_bfloat16 *tc_dd;     // [slot][64][V] gradient of the deltas
   __nv_bfloat16 *tc_dx;     // [slot][64][V] dX = A^T dD
   float *tc_dqg;           // [slot][64][K] dO h^T

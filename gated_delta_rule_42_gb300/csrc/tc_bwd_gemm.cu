@@ -79,10 +79,9 @@ __global__ void __launch_bounds__(kThr, 1) kda_bwd_gemm_tc_kernel(Problem P, Wor
       cp16(sbase + G_XT + it * 16, xt + it * 16);
       cp16(sbase + G_DT + it * 16, dt + it * 16);
     }
-    for (int it = tid; it < 128 * 16; it += kThr) {  // h (saved swizzled: verbatim) and dh' [128][128]
-      const int r = it >> 4, jj = it & 15;
+    for (int it = tid; it < 128 * 16; it += kThr) {  // h and dh' [128][128], saved swizzled: verbatim
       cp16(sbase + G_H + it * 16, reinterpret_cast<const unsigned char *>(W.tc_hs + slot * kD * kD) + it * 16);
-      cp16(sbase + G_DH + sw_chunk(r, jj, kD), W.tc_dh + (slot * kD + r) * kD + jj * 8);
+      cp16(sbase + G_DH + it * 16, reinterpret_cast<const unsigned char *>(W.tc_dh + slot * kD * kD) + it * 16);
     }
     for (int it = tid; it < 192 * 16; it += kThr) {  // [dX; dO; dD]
       const int r = it >> 4, jj = it & 15;

@@ -13,9 +13,10 @@
 // gate scale when A_log is omitted", fla-org/flash-linear-attention PR #1294,
 // commit log: "the kernel's reverse state-gradient recurrence").  Every
 // operand is read straight from the row-major tiles through K- or MN-major
-// descriptors.  For the per-chunk gradient kernel the scan stores, per chunk:
-// dh' (bf16 [K][V]) and dD, dX (bf16 [64][V]); at the start of the sequence it
-// writes dh0 (fp32).
+// descriptors.  For the per-chunk gradient kernel the scan saves, per chunk,
+// with bulk stores from shared memory: dh' (bf16 [K][V], swizzled operand
+// layout) and dD, dX (bf16 [64][V], row-major); at the start of the sequence
+// it writes dh0 (fp32).
 #include "tc_common.cuh"
 
 namespace kda {
@@ -90,21 +91,20 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
     const int cidx = si.z + ci;
     const size_t slot = (size_t)cidx * HV + j;
     cp_wait_all();  // dO
+    if (tid == 0) bulk_wait_read();  // the previous chunk's saved tiles have left shared memory
     bar_wait(bar_t, t_par, err);
     t_par ^= 1;
     __syncthreads();
 
     // ---------------- (c) ----------------
     {
-      unsigned char *DH = U + U_DH;  // dh' row-major [c][v]
+      unsigned char *DH = U + U_DH;  // dh' [c][v], swizzled
 #pragma unroll
       for (int x8 = 0; x8 < 8; ++x8) {
         float t[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) t[e] = dreg[8 * x8 + e];
-        const uint4 u = pack8(t);
-        *reinterpret_cast<uint4 *>(DH + sw_chunk(cown, 8 * vhalf + x8, kD)) = u;
-        *reinterpret_cast<uint4 *>(W.tc_dh + (slot * kD + cown) * kD + 64 * vhalf + 8 * x8) = u;
+        *reinterpret_cast<uint4 *>(DH + sw_chunk(cown, 8 * vhalf + x8, kD)) = pack8(t);
       }
     }
     fence_async_smem();
@@ -112,6 +112,10 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
     __syncthreads();
     fence_after();
     const uint32_t aDH = sbase + OFF_U + U_DH, aDDT = sbase + OFF_U + U_DDT, aNDX = sbase + OFF_U + U_NDX;
+    if (tid == 0) {  // dh' for the per-chunk kernel (its swizzled operand layout)
+      bulk_store(W.tc_dh + slot * kD * kD, aDH, 32768u);
+      bulk_commit();
+    }
     if (tid == 0) {
       // dD^T[v][r] = sum_i dO[i][v] Aqk[i][r] + sum_c dh'[c][v] Khat[r][c]   (M=128 v, N=64 r)
       const uint32_t id1 = idesc(128, 64, 1, 1), id2 = idesc(128, 64, 1, 0);
@@ -136,14 +140,18 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
         for (int e = 0; e < 8; ++e) x[e] = d[q8 * 8 + e];
         *reinterpret_cast<uint4 *>(U + U_DDT + sw_chunk(v, (r0 >> 3) + q8, kD)) = pack8(x);
       }
-      __nv_bfloat16 *dst = W.tc_dd + slot * kC * kD + v;
+      __nv_bfloat16 *st = (__nv_bfloat16 *)(sm + OFF_KRAW) + v;  // row-major [r][v] staging
 #pragma unroll
-      for (int e = 0; e < 32; ++e) dst[(r0 + e) * kD] = __float2bfloat16_rn(d[e]);
+      for (int e = 0; e < 32; ++e) st[(r0 + e) * kD] = __float2bfloat16_rn(d[e]);
     }
     fence_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
+    if (tid == 0) {  // dD, row-major [r][v], for the per-chunk kernel
+      bulk_store(W.tc_dd + slot * kC * kD, sbase + OFF_KRAW, 16384u);
+      bulk_commit();
+    }
     if (tid == 0) {  // dX^T[v][i] = sum_r dD^T[v][r] A[r][i]   (M=128 v, N=64 i, K=64 r)
       const uint32_t id = idesc(128, 64, 0, 1);
 #pragma unroll
@@ -164,14 +172,18 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
         for (int e = 0; e < 8; ++e) x[e] = -d[q8 * 8 + e];
         *reinterpret_cast<uint4 *>(U + U_NDX + sw_chunk(v, (r0 >> 3) + q8, kD)) = pack8(x);
       }
-      __nv_bfloat16 *dst = W.tc_dx + slot * kC * kD + v;
+      __nv_bfloat16 *st = (__nv_bfloat16 *)(sm + OFF_QRAW) + v;  // row-major [i][v] staging
 #pragma unroll
-      for (int e = 0; e < 32; ++e) dst[(r0 + e) * kD] = __float2bfloat16_rn(d[e]);
+      for (int e = 0; e < 32; ++e) st[(r0 + e) * kD] = __float2bfloat16_rn(d[e]);
     }
     fence_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
+    if (tid == 0) {  // dX, row-major [i][v], for the per-chunk kernel
+      bulk_store(W.tc_dx + slot * kC * kD, sbase + OFF_QRAW, 16384u);
+      bulk_commit();
+    }
     if (tid == 0) {
       // U[c][v] = sum_r Qg[r][c] dO[r][v] - sum_r Bk[r][c] dX[r][v]   (M=128 c, N=128 v, K=64 r)
       const uint32_t id1 = idesc(128, 128, 1, 1), id2 = idesc(128, 128, 1, 0);
@@ -216,6 +228,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
     for (int x = 0; x < 64; x += 4)
       *reinterpret_cast<float4 *>(dst + x) = make_float4(dreg[x], dreg[x + 1], dreg[x + 2], dreg[x + 3]);
   }
+  if (tid == 0) bulk_wait_all();  // the saved tiles are in global memory before the CTA exits
   fence_before();
   __syncthreads();
   if (warp == 0) {

@@ -474,6 +474,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     *reinterpret_cast<float4 *>(Tf + (b * 16 + rr) * 16 + i4) = acc;
   }
   __syncthreads();
+  KDA_PT(16);
   for (int e = tid; e < 2 * 64; e += kThr) {  // A_{R,R-1} = -D_R T_b
     const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -487,6 +488,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     *reinterpret_cast<float4 *>(Af + fsw(16 * R + rr, 16 * (R - 1) + i4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
+  KDA_PT(17);
   {
     const int r = tid >> 3, c4 = (tid & 7) * 4;  // one 1 x 4 segment of a 32 x 32 block per thread
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -499,6 +501,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     }
     *reinterpret_cast<float4 *>(Tf + r * 32 + c4) = acc;
     __syncthreads();
+    KDA_PT(18);
     acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
     for (int m = 0; m < 32; ++m) {  // A21 = -A2 T2
@@ -510,6 +513,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     *reinterpret_cast<float4 *>(Af + fsw(32 + r, c4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
+  KDA_PT(19);
   for (int e = tid; e < kC * kC / 8; e += kThr) {  // A -> bf16 tile, 16-byte chunks
     const int r = e >> 3, jj = e & 7;
     float x[8];
