@@ -81,8 +81,7 @@ def kernel_bytes_per_token(name, cfg):
         "kda_fwd_tc": 2 * qk + 2 * vv + g + b,
         "kda_fwd_tc_states": 2 * qk + vv + g + b + hs + rec + 2 * t16,
         "kda_bwd_scan_tc": rec + vv + hs + 2 * vv,
-        "kda_bwd_gemm_tc": 2 * t16 + 2 * hs + 3 * vv + vv + b + vv + 3 * f32K + 2 * cc + b + dgl,
-        "kda_bwd_chain_tc": g + b + t16 / 2 + 3 * f32K + 2 * cc + 2 * qk + b + dgl + 2 * qk + g + b,
+        "kda_bwd_intra_tc": 2 * t16 + 2 * hs + 3 * vv + vv + b + g + t16 / 2 + 2 * qk + vv + 2 * qk + g + b,
         # fp32 path
         "simple_intra_kernel": 2 * qk + vv + g + b + 2 * f32K + 2 * cc + f32K + f32V,
         "simple_scan_kernel": qk + 2 * f32K + f32V + hh + f32V,

@@ -98,7 +98,7 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   w.chunk = (int4 *)take(sizeof(int4) * (size_t)(P.NC > 0 ? P.NC : 1));
   w.flags = (int *)take(sizeof(int) * 4);
   if (use_tc(P)) {
-    if (backward) {  // tensor-core backward: per-slot bf16 / fp32 intermediates
+    if (backward) {  // tensor-core backward: per-slot tiles passed between its kernels
       w.tc_hs = (__nv_bfloat16 *)take(2 * slots * K * V);
       w.tc_tiles = (unsigned char *)take(kTileRecord * slots);
       w.tc_xt = (unsigned char *)take(16384 * slots);
@@ -106,13 +106,6 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
       w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);
       w.tc_dd = (__nv_bfloat16 *)take(2 * slots * C * V);
       w.tc_dx = (__nv_bfloat16 *)take(2 * slots * C * V);
-      w.tc_dqg = (float *)take(4 * slots * C * K);
-      w.tc_dbk = (float *)take(4 * slots * C * K);
-      w.tc_dkh = (float *)take(4 * slots * K * C);
-      w.tc_dat = (float *)take(4 * slots * C * C);
-      w.tc_dqkt = (float *)take(4 * slots * C * C);
-      w.tc_dbx = (float *)take(4 * slots * C);
-      w.tc_dgl = (float *)take(4 * slots * K);
       if (P.HV != P.H) {
         w.dqp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
         w.dkp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
@@ -227,8 +220,7 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
     int *err = W.flags + 2;
     e = tc_forward(P, W, nullptr, nullptr, true, err, s);
     if (e == cudaSuccess) e = tc_backward_scan(P, W, dO, dhT, dh0, err, s);
-    if (e == cudaSuccess) e = tc_backward_gemm(P, W, dO, dv, err, s);
-    if (e == cudaSuccess) e = tc_backward_chain(P, W, dq, dk, dg, dbeta, s);
+    if (e == cudaSuccess) e = tc_backward_intra(P, W, dO, dv, dq, dk, dg, dbeta, err, s);
     if (e == cudaSuccess && P.HV != P.H) e = launch_group_reduce(P, W.dqp, W.dkp, dq, dk, s);
   } else {
     e = simple_backward(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, (cudaStream_t)stream);

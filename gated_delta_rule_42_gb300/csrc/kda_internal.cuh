@@ -57,13 +57,6 @@ struct Workspace {
   __nv_bfloat16 *tc_dh;     // [slot] 32 KB: gradient of the chunk-end state [K][V], swizzled operand tile
   __nv_bfloat16 *tc_dd;     // [slot][64][V] gradient of the deltas
   __nv_bfloat16 *tc_dx;     // [slot][64][V] dX = A^T dD
-  float *tc_dqg;           // [slot][64][K] dO h^T
-  float *tc_dbk;           // [slot][64][K] -dX h^T
-  float *tc_dkh;           // [slot][64][K] dKhat
-  float *tc_dat;           // [slot][64][64] dA^T
-  float *tc_dqkt;          // [slot][64][64] dAqk^T (unmasked)
-  float *tc_dbx;           // [slot][64] sum_v dX v
-  float *tc_dgl;           // [slot][K]  rowsum(dh' .* h)
 };
 
 // --- element access -------------------------------------------------------
@@ -122,10 +115,9 @@ cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT,
                        int *err, cudaStream_t s);
 cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,
                              float *dh0, int *err, cudaStream_t s);
-cudaError_t tc_backward_gemm(const Problem &P, const Workspace &W, const void *dO, void *dv, int *err,
-                             cudaStream_t s);
-cudaError_t tc_backward_chain(const Problem &P, const Workspace &W, void *dq, void *dk, float *dg,
-                              float *dbeta, cudaStream_t s);
+// Per-chunk gradients: tcgen05 products and the gradient chain in one kernel.
+cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *dO, void *dv, void *dq, void *dk,
+                              float *dg, float *dbeta, int *err, cudaStream_t s);
 // dq = (group sum of dqp) / sqrt(K), dk = group sum of dkp, over the HV/H value heads
 cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                 cudaStream_t s);

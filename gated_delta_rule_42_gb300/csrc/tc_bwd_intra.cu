@@ -1,7 +1,16 @@
-// Gradient assembly of the bf16 chunked KDA backward (K = V = 128).
+// Per-chunk gradients of the bf16 chunked KDA backward (K = V = 128): the
+// tensor-core products and the gradient chain in one kernel.
 //
-// One CTA per (chunk, value head).  From the tensor-core products of the
-// per-chunk kernel (dQg, dBk, dKhat, dA, dAqk) it finishes
+// One CTA (16 warps) per (chunk, value head), all chunks at once.  Inputs: the
+// chunk-start state h and the tiles X^T (X = beta v - Bk h), D^T (D = A X) and
+// A from the forward recompute, the gradient of the chunk-end state dh', and
+// dD, dX from the reverse scan.  First, on tcgen05 (fp32 in TMEM):
+//   [dX; dO] h^T    -> rows 0..63: -dBk, rows 64..127: dQg   (one M=128 product)
+//   dKhat^T = dh' D^T                                          (Khat = k 2^(G_last - G))
+//   [X; D] [dO; dD]^T -> block (X, dD) = dA^T, block (D, dO) = dAqk^T
+// and on the SIMT cores dv = beta dX, sum_v dX v and d(2^G_last) = rowsum(dh' .* h).
+// The products never leave the chip: the chain reads them from TMEM.  It
+// finishes
 //   dL   = -tril_{-1}(A^T dA A^T)                 gradient through A = (I + L)^-1
 //   the chain through L = beta*KK and Aqk to the keys, queries and gate,
 // and assembles dq, dk, dg and dbeta.  With 2^(G_r - G_i) split at 16-token
@@ -16,6 +25,9 @@
 //   dG_last += ln2 (sum_r dKhat k khat + 2^G_last d(2^G_last))
 //   dbeta   = sum_v dX v + sum_c (dBk k Gamma + k e1 xr)
 //   dg = reverse cumsum of dG inside the chunk (G is in log2 units).
+// These are the intra-chunk backward steps of FLA's chunk_bwd_dqkwg /
+// chunk_bwd_dv_local / prepare_wy_repr_bwd ("[Fix] Use unit KDA gate scale when
+// A_log is omitted", fla-org/flash-linear-attention PR #1294, commit log).
 // All reductions run in a fixed order: the result is bitwise reproducible.
 #include "tc_common.cuh"
 
@@ -25,55 +37,61 @@ namespace {
 using namespace umma;
 using namespace tc;
 
-// shared memory map (bytes from a 1024-aligned base).  "hi/lo" tiles hold a
-// value as the sum of two bf16 numbers, so warp MMAs over hi*hi + hi*lo + lo*hi
-// keep ~16 mantissa bits: the pairwise terms below sum to zero over a chunk and
-// dg accumulates them, so their rounding must stay far below the bf16 level.
-constexpr uint32_t C_G = 0;          // G fp32 [64][132]
-constexpr uint32_t C_VEC = 33792;    // vectors (20 x 128 fp32)
-constexpr uint32_t C_BETA = 44032;   // beta [64]
-constexpr uint32_t C_RB = 44288;     // dbeta partials [4][64]
-constexpr uint32_t C_RC = 45312;     // prefetched d(2^G_last) [128] and sum_v dX v [64]
-constexpr uint32_t C_KR = 47104;     // Kr  hi [64][128] | lo (+16 KB)
-constexpr uint32_t C_QR = 79872;     // Qr  hi | lo
-constexpr uint32_t C_KC = 112640;    // Kc  hi | lo
-constexpr uint32_t C_A = 145408;     // A   [64 r][64 i] bf16
-constexpr uint32_t C_DAB = 153600;   // dA^T [64 i][64 m] hi | lo (+8 KB) -> later dL [64 r][64 i] hi | lo
-constexpr uint32_t C_DQK = 169984;   // dAqk^T [64 i][64 r] hi | lo
-constexpr uint32_t C_XB = 186368;    // X = beta dL [64 r][64 i] hi | lo
-constexpr uint32_t C_T = 202752;     // T = A^T dA [64 r][64 m] hi | lo
+// Shared memory map (bytes from a 1024-aligned base).  [0, 160 KB) first holds
+// the operands of the tensor-core products, then the chain tiles.  "hi/lo"
+// tiles hold a value as the sum of two bf16 numbers, so warp MMAs over
+// hi*hi + hi*lo + lo*hi keep ~16 mantissa bits: the pairwise terms below sum to
+// zero over a chunk and dg accumulates them, so their rounding must stay far
+// below the bf16 level.
+constexpr uint32_t I_XT = 0;          // X^T [128 v][64 r]  (saved by the forward recompute)
+constexpr uint32_t I_DT = 16384;      // D^T [128 v][64 r]  (adjacent: [X; D]^T is one MN-major operand)
+constexpr uint32_t I_STK = 32768;     // [dX; dO; dD] [192][128]
+constexpr uint32_t I_H = 81920;       // h  [128 c][128 v]
+constexpr uint32_t I_DH = 114688;     // dh' [128 c][128 v]
+constexpr uint32_t I_V = 147456;      // v  [64 r][128 v]
+constexpr uint32_t C_KR = 0;          // Kr  hi [64][128] | lo (+16 KB)
+constexpr uint32_t C_QR = 32768;      // Qr  hi | lo
+constexpr uint32_t C_KC = 65536;      // Kc  hi | lo
+constexpr uint32_t C_DAB = 98304;     // dA^T [64 i][64 m] hi | lo (+8 KB) -> later dL [64 r][64 i] hi | lo
+constexpr uint32_t C_DQK = 114688;    // dAqk^T [64 i][64 r] hi | lo
+constexpr uint32_t C_XB = 131072;     // X = beta dL [64 r][64 i] hi | lo   (before: raw k rows)
+constexpr uint32_t C_T = 147456;      // T = A^T dA [64 r][64 m] hi | lo    (before: raw q rows)
+constexpr uint32_t C_KRAW = C_XB, C_QRAW = C_T;
+constexpr uint32_t C_G = 163840;      // G fp32 [64][132]
+constexpr uint32_t C_A = 197632;      // A   [64 r][64 i] bf16
+constexpr uint32_t C_VEC = 205824;    // vectors (20 x 128 fp32)
+constexpr uint32_t C_BETA = 216064;   // beta [64]
+constexpr uint32_t C_RB = 216320;     // dbeta partials [4][64]
+constexpr uint32_t C_RED = 217344;    // sum_v dX v [64], d(2^G_last) [128]
+constexpr uint32_t C_MISC = 218112;   // mbarrier, tmem slot
+constexpr uint32_t C_SMEM = 218176 + 1024;
 constexpr uint32_t LO128 = 16384, LO64 = 8192;
-// Product staging for the assembly, in four passes of 32 columns (16 per
-// column half), double-buffered: each pass holds dQg, dBk, dKhat as
-// [64][32] fp32 tiles with 16-byte chunks XOR-swizzled by row % 8 (8 KB each).
-// Buffer 0 lives in the A and T tiles (dead after dL, so pass 0 loads during
-// the pairwise chains); buffer 1 in the dL / dAqk tiles (dead after the
-// chains).  The dG tiles of a pass and the segment totals of its column scans
-// use the rest of the dead chain tiles; d(2^G_last) and sum_v dX v are
-// prefetched into the C_RC scratch right after dL.
-constexpr uint32_t ST_BYTES = 64 * 32 * 4;        // one staged [64][32] product
-constexpr uint32_t C_ST0_QB = C_T;                // pass buffer 0: dQg | dBk (16 KB)
-constexpr uint32_t C_ST0_K = C_A;                 //                dKhat (8 KB)
-constexpr uint32_t C_ST1 = C_DAB;                 // pass buffer 1: dQg | dBk | dKhat (24 KB)
-constexpr uint32_t SQ_LD = 36;                    // row stride (floats) of the dG pass tiles
-constexpr uint32_t C_SQ = C_ST1 + 3 * ST_BYTES;   // Q part of dG, one pass [64][SQ_LD]
-constexpr uint32_t C_SP = C_SQ + 64 * SQ_LD * 4;  // P part
-constexpr uint32_t C_TOT = C_SP + 64 * SQ_LD * 4; // segment totals of Q, P [16][32]; Khat column term [2][4][32]
-constexpr uint32_t C_DGL = C_RC;                  // d(2^G_last) [128]
-constexpr uint32_t C_DBX = C_RC + 512;            // sum_v dX v [64]
-static_assert(C_TOT + (16 + 16 + 8) * 32 * 4 <= C_T, "pass scratch overlaps staging buffer 0");
-static_assert(C_RC + 768 <= C_KR, "prefetch scratch overlaps the Kr tile");
+constexpr uint32_t TMEM_COLS = 512;   // [128,256) S, [256,320) dKhat^T, [384,512) Z
+// Assembly scratch in the dead dL .. T tiles: the products of one pass (32
+// columns: 8 per column quarter) read out of TMEM as [64][32] fp32 tiles with
+// 16-byte chunks XOR-swizzled by row % 8, the dG tiles of the pass and the
+// segment totals of its column scans.
+constexpr uint32_t ST_BYTES = 64 * 32 * 4;          // one staged [64][32] product
+constexpr uint32_t C_ST = C_DAB;                    // dQg | dBk | dKhat (24 KB)
+constexpr uint32_t SQ_LD = 36;                      // row stride (floats) of the dG pass tiles
+constexpr uint32_t C_SQ = C_ST + 3 * ST_BYTES;      // Q part of dG, one pass [64][SQ_LD]
+constexpr uint32_t C_SP = C_SQ + 64 * SQ_LD * 4;    // P part
+constexpr uint32_t C_TOT = C_SP + 64 * SQ_LD * 4;   // segment totals of Q, P [16][32]; Khat column term [2][4][32]
+static_assert(C_TOT + (16 + 16 + 8) * 32 * 4 <= C_G, "assembly scratch overflows the chain tiles");
+static_assert(I_V + 16384 == C_G && C_A % 1024 == 0, "map");
 // byte offset of element (r, c) of a staged [64][32] product
 __device__ __forceinline__ uint32_t st_off(int r, int c) {
   return (uint32_t)r * 128u + ((uint32_t)((c >> 2) ^ (r & 7)) << 4) + (uint32_t)(c & 3) * 4u;
 }
-constexpr uint32_t C_SMEM = 219136 + 1024;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-struct ChainArgs {
-  void *dq, *dk;  // bf16 [B*T][H][K] when HV == H, else fp32 partials [B*T][HV][K]
+struct IntraArgs {
+  const __nv_bfloat16 *dO;
+  __nv_bfloat16 *dv;  // [B*T][HV][V]
+  void *dq, *dk;      // bf16 [B*T][H][K] when HV == H, else fp32 partials [B*T][HV][K]
   float *dg, *dbeta;
   bool partial;
+  int *err;
 };
 
 // A fragment (16x16, row-major operand) of rows m0.., cols k0.. of a swizzled tile.
@@ -129,9 +147,9 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
   mma16816(acc, al, bh0, bh1);
 }
 
-constexpr int kCT = 512;  // 16 warps: the assembly is latency-bound, so more warps hide more of it
+constexpr int kCT = 512;  // 16 warps: the chain is latency-bound, so more warps hide more of it
 
-__global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Workspace W, ChainArgs args) {
+__global__ void __launch_bounds__(kCT, 1) kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
@@ -141,62 +159,141 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Wor
   const int t0 = ch.y, len = ch.z;
   const int HV = P.HV, H = P.H, h = j / (HV / H);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3;
   const size_t slot = (size_t)c_idx * HV + j;
   float *G = (float *)(sm + C_G);
   float *vec = (float *)(sm + C_VEC);
   float *beta = (float *)(sm + C_BETA);
   float *rb = (float *)(sm + C_RB);
+  float *red = (float *)(sm + C_RED);  // [0, 64): sum_v dX v; [64, 192): d(2^G_last)
+  uint64_t *bar = (uint64_t *)(sm + C_MISC);
+  uint32_t *tslot = (uint32_t *)(sm + C_MISC + 8);
   const __nv_bfloat16 *kin = (const __nv_bfloat16 *)P.k, *qin = (const __nv_bfloat16 *)P.q;
+  const __nv_bfloat16 *vin = (const __nv_bfloat16 *)P.v;
   constexpr float qscale = 0.08838834764831845f;
   KDA_PT_DECL;
 
-  // ---- loads ----
-  load_gate<kCT>(sbase + C_G, P.g, t0, len, HV, j);
-  {  // A, saved by the forward recompute in this kernel's swizzled layout
-    const unsigned char *src = W.tc_tiles + slot * kTileRecord + kTileRecA;
-    for (int it = tid; it < 512; it += kCT) cp16(sbase + C_A + it * 16, src + it * 16);
-  }
-  if (tid < kC) {
-    if (tid < len) cp4(smem_u32(beta + tid), P.beta + (size_t)(t0 + tid) * HV + j);
-    else beta[tid] = 0.f;
-  }
-  // Staged asynchronously in tiles that are written only later, so that no
-  // thread waits on a plain global load: dA^T, dAqk^T (fp32) in the Kr tile;
-  // raw k, q rows in the lo halves of Kc and Qr -- the decay-tile pass reads
-  // each 16-byte chunk there before the same thread overwrites it.
-  for (int it = tid; it < kC * 16; it += kCT) {
-    cp16(sbase + C_KR + it * 16, W.tc_dat + slot * kC * kC + it * 4);
-    cp16(sbase + C_KR + LO128 + it * 16, W.tc_dqkt + slot * kC * kC + it * 4);
-  }
-  load_rows<kCT>(sbase + C_KC + LO128, kin, t0, len, H, h);
-  load_rows<kCT>(sbase + C_QR + LO128, qin, t0, len, H, h);
-  cp_commit();
-  cp_wait_all();
-  __syncthreads();
-  for (int it = tid; it < kC * 8; it += kCT) {  // dA^T, dAqk^T fp32 -> hi/lo bf16 tiles
-    const int r = it >> 3, jj = it & 7;
-    const float *a = (const float *)(sm + C_KR) + r * kC + jj * 8;
-    const float *b = (const float *)(sm + C_KR + LO128) + r * kC + jj * 8;
-    float x[8], y[8];
-#pragma unroll
-    for (int e = 0; e < 8; e += 4) {
-      *reinterpret_cast<float4 *>(x + e) = *reinterpret_cast<const float4 *>(a + e);
-      *reinterpret_cast<float4 *>(y + e) = *reinterpret_cast<const float4 *>(b + e);
+  // ---- loads: the product operands, then G, A and beta of the chain ----
+  {
+    const unsigned char *xt = W.tc_xt + slot * 16384, *dt = W.tc_dt + slot * 16384;
+    const unsigned char *hs = reinterpret_cast<const unsigned char *>(W.tc_hs + slot * kD * kD);
+    const unsigned char *dh = reinterpret_cast<const unsigned char *>(W.tc_dh + slot * kD * kD);
+    for (int it = tid; it < 1024; it += kCT) {  // X^T, D^T: verbatim (same swizzled layout)
+      cp16(sbase + I_XT + it * 16, xt + it * 16);
+      cp16(sbase + I_DT + it * 16, dt + it * 16);
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e)  // dAqk^T[i][r] is a gradient of Aqk only where i <= r
-      if (r > jj * 8 + e) y[e] = 0.f;
-    const uint32_t off = sw_chunk(r, jj, kC);
-    uint4 hi, lo;
-    split8(x, hi, lo);
-    *reinterpret_cast<uint4 *>(sm + C_DAB + off) = hi;
-    *reinterpret_cast<uint4 *>(sm + C_DAB + LO64 + off) = lo;
-    split8(y, hi, lo);
-    *reinterpret_cast<uint4 *>(sm + C_DQK + off) = hi;
-    *reinterpret_cast<uint4 *>(sm + C_DQK + LO64 + off) = lo;
+    for (int it = tid; it < 2048; it += kCT) {  // h, dh': verbatim
+      cp16(sbase + I_H + it * 16, hs + it * 16);
+      cp16(sbase + I_DH + it * 16, dh + it * 16);
+    }
+    for (int it = tid; it < 192 * 16; it += kCT) {  // [dX; dO; dD]
+      const int r = it >> 4, jj = it & 15;
+      const uint32_t dst = sbase + I_STK + sw_chunk(r, jj, 192);
+      const int rr = r & 63;
+      if (r < 64) cp16(dst, W.tc_dx + (slot * kC + rr) * kD + jj * 8);
+      else if (r >= 128) cp16(dst, W.tc_dd + (slot * kC + rr) * kD + jj * 8);
+      else if (rr < len) cp16(dst, args.dO + ((size_t)(t0 + rr) * HV + j) * kD + jj * 8);
+      else st_zero16(dst);
+    }
+    load_rows<kCT>(sbase + I_V, vin, t0, len, HV, j);
+    load_gate<kCT>(sbase + C_G, P.g, t0, len, HV, j);
+    const unsigned char *a = W.tc_tiles + slot * kTileRecord + kTileRecA;  // A, swizzled as here
+    for (int it = tid; it < 512; it += kCT) cp16(sbase + C_A + it * 16, a + it * 16);
+    if (tid < kC) {
+      if (tid < len) cp4(smem_u32(beta + tid), P.beta + (size_t)(t0 + tid) * HV + j);
+      else beta[tid] = 0.f;
+    }
+    cp_commit();
   }
-  KDA_PT(0);  // (the barrier after the cumsum also orders the Kr staging reads before the Kr writes)
+  if (tid == 0) {
+    bar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  cp_wait_all();
+  fence_async_smem();
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
 
+  // ---- tensor-core products ----
+  if (tid == 0) {
+    // S[i'][c] = sum_v [dX; dO][i'][v] h[c][v]   (M=128, N=128 c, K=128 v)
+    const uint32_t id3 = idesc(128, 128, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mma(tmem + 128, desc_k16(sbase + I_STK, k, 192), desc_k16(sbase + I_H, k, kD), id3, k > 0);
+    // dKhat^T[c][r] = sum_v dh'[c][v] D[r][v]   (M=128 c, N=64 r, K=128 v)
+    const uint32_t id4 = idesc(128, 64, 0, 1), id5 = idesc(128, 128, 1, 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mma(tmem + 256, desc_k16(sbase + I_DH, k, kD), desc_mn(sbase + I_DT, k, 8192), id4, k > 0);
+    // Z[i'][n'] = sum_v [X; D][i'][v] [dO; dD][n'][v]   (M=128, N=128, K=128 v)
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      mma(tmem + 384, desc_mn(sbase + I_XT, k, 16384), desc_k16(sbase + I_STK + 64 * 128, k, 192), id5, k > 0);
+    commit(bar);
+  }
+  // meanwhile on the SIMT cores: d(2^G_last)[c] = sum_v dh'[c][v] h[c][v]; dv = beta dX; sum_v dX v
+  if (tid < kD) {
+    const int c = tid;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int jj = 0; jj < 16; ++jj) {
+      float a[8], b[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + I_H + sw_chunk(c, jj, kD)), a);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + I_DH + sw_chunk(c, jj, kD)), b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(a[e], b[e], acc);
+    }
+    red[64 + c] = acc;
+  }
+  for (int r = warp; r < kC; r += kCT / 32) {  // one warp per row, 4 columns per lane
+    float part = 0.f;
+    if (r < len) {
+      const float br = beta[r];
+      const int v0 = lane * 4;
+      const uint2 xd = *reinterpret_cast<const uint2 *>(sm + I_STK + sw_off(r, v0, 192));
+      const uint2 xv = *reinterpret_cast<const uint2 *>(sm + I_V + sw_off(r, v0, kC));
+      const float2 d01 = unpack_bf16(xd.x), d23 = unpack_bf16(xd.y);
+      const float2 v01 = unpack_bf16(xv.x), v23 = unpack_bf16(xv.y);
+      *reinterpret_cast<uint2 *>(args.dv + ((size_t)(t0 + r) * HV + j) * kD + v0) =
+          make_uint2(pack_bf16(br * d01.x, br * d01.y), pack_bf16(br * d23.x, br * d23.y));
+      part = d01.x * v01.x + d01.y * v01.y + d23.x * v23.x + d23.y * v23.y;
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    }
+    if (lane == 0) red[r] = part;
+  }
+  bar_wait(bar, 0, args.err);
+  fence_after();
+  __syncthreads();  // products in TMEM; the operand tiles are dead
+  KDA_PT(0);
+
+  // ---- raw k, q rows for the decay tiles; dA^T, dAqk^T out of TMEM as hi/lo tiles; gate cumsum ----
+  load_rows<kCT>(sbase + C_KRAW, kin, t0, len, H, h);
+  load_rows<kCT>(sbase + C_QRAW, qin, t0, len, H, h);
+  cp_commit();
+  {
+    // Z: lanes 0..63 (i), cols 64..127 (m) = dA^T[i][m]; lanes 64..127, cols 0..63 = dAqk^T[i][r]
+    const int cg = warp >> 2, i = 32 * (quarter & 1) + lane;
+    const bool qk = quarter >= 2;
+    float x[16];
+    tmem_ld16(tq + 384u + (qk ? 0u : 64u) + (uint32_t)(16 * cg), x);
+#pragma unroll
+    for (int hx = 0; hx < 2; ++hx) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int col = 16 * cg + 8 * hx + e;
+        y[e] = (qk && i > col) ? 0.f : x[8 * hx + e];  // dAqk^T[i][r] is a gradient of Aqk only where i <= r
+      }
+      uint4 hi, lo;
+      split8(y, hi, lo);
+      const uint32_t off = sw_chunk(i, 2 * cg + hx, kC);
+      *reinterpret_cast<uint4 *>(sm + (qk ? C_DQK : C_DAB) + off) = hi;
+      *reinterpret_cast<uint4 *>(sm + (qk ? C_DQK : C_DAB) + LO64 + off) = lo;
+    }
+  }
   // ---- G, block references, decay tiles Kr, Qr, Kc (hi/lo) ----
   if (tid < kD) {
     const int c = tid;
@@ -228,6 +325,7 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Wor
 #pragma unroll
       for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
   }
+  cp_wait_all();  // raw k, q
   __syncthreads();
   KDA_PT(1);
   {
@@ -241,8 +339,8 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Wor
       const int r = rg * 2 + rr;
       const uint32_t off = sw_chunk(r, jj, kC);
       float kv[8], qv[8], o[8], e1[8], e2[8];
-      unpack8(*reinterpret_cast<const uint4 *>(sm + C_KC + LO128 + off), kv);  // raw k, q (zero past len)
-      unpack8(*reinterpret_cast<const uint4 *>(sm + C_QR + LO128 + off), qv);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + C_KRAW + off), kv);  // raw k, q (zero past len)
+      unpack8(*reinterpret_cast<const uint4 *>(sm + C_QRAW + off), qv);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float g = G[r * kGLD + c0 + e];
@@ -321,22 +419,6 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Wor
       }
   }
   __syncthreads();
-  // Asynchronous loads of product pass g (columns 32 q + 8 g .. +7 of each quarter q) into buffer g & 1.
-  auto stage = [&](int g) {
-    for (int it = tid; it < 3 * 512; it += kCT) {
-      const int prod = it >> 9, w = it & 511, r = w >> 3, q = w & 7;  // q: 16-byte chunk of the 32 columns
-      const int gc = 32 * (q >> 1) + 8 * g + 4 * (q & 1);             // first global column of the chunk
-      const float *src = (prod == 0 ? W.tc_dqg : prod == 1 ? W.tc_dbk : W.tc_dkh) + (slot * kC + r) * kD + gc;
-      const uint32_t base = (g & 1) ? C_ST1 + (uint32_t)prod * ST_BYTES
-                                    : (prod < 2 ? C_ST0_QB + (uint32_t)prod * ST_BYTES : C_ST0_K);
-      cp16(sbase + base + st_off(r, 4 * q), src);
-    }
-    cp_commit();
-  };
-  if (tid < 32) cp16(sbase + C_DGL + tid * 16, W.tc_dgl + slot * kD + tid * 4);
-  else if (tid < 48) cp16(sbase + C_DBX + (tid - 32) * 16, W.tc_dbx + slot * kC + (tid - 32) * 4);
-  stage(0);  // A and T are dead: pass 0 loads during the pairwise chains
-
   KDA_PT(4);
   // ---- pairwise chains: warp owns rows 16B..16B+15 (as r and as i), columns ch0 .. ch0+31 ----
   // Block-pair products are formed in a temporary, scaled by the per-channel
@@ -395,28 +477,51 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Wor
       }
     }
   }
-  __syncthreads();  // every warp is done with the chain tiles: A .. X become the product staging
+  __syncthreads();  // every warp is done with the chain tiles: dL .. T become the assembly scratch
   KDA_PT(5);
 
   // ---- assembly (fragment element (r, c)), in four passes of 8 columns per warp ----
-  // Raw k and q are not re-read: every term that needs them is a product with
-  // a decay factor that the hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2 hold.
-  // dg = reverse cumsum of dG over the chunk runs per pass as column scans
-  // over 4-row segments with segment totals exchanged in shared memory.
+  // Each pass reads its 32 columns (8 per column quarter) of dQg, dBk and
+  // dKhat out of TMEM into a swizzled shared-memory tile.  Raw k and q are not
+  // re-read: every term that needs them is a product with a decay factor that
+  // the hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2 hold.  dg = reverse cumsum
+  // of dG over the chunk runs per pass as column scans over 4-row segments with
+  // segment totals exchanged in shared memory.
+  auto stage = [&](int g) {
+    const int cg = warp >> 2;  // column quarter of this warp (8 columns of the pass)
+    {  // S: lane quarters 0, 1 = -dBk rows, 2, 3 = dQg rows
+      float x[8];
+      tmem_ld8(tq + 128u + (uint32_t)(32 * cg + 8 * g), x);
+      const int r = 32 * (quarter & 1) + lane;
+      const bool isq = quarter >= 2;
+      const float sg = isq ? 1.f : -1.f;
+      unsigned char *dst = sm + C_ST + (isq ? 0u : ST_BYTES);
+      *reinterpret_cast<float4 *>(dst + st_off(r, 8 * cg)) = make_float4(sg * x[0], sg * x[1], sg * x[2], sg * x[3]);
+      *reinterpret_cast<float4 *>(dst + st_off(r, 8 * cg + 4)) = make_float4(sg * x[4], sg * x[5], sg * x[6], sg * x[7]);
+    }
+    {  // dKhat^T: lane c (this quarter), columns r = 16 cg .. 16 cg + 15; lanes 8 g .. 8 g + 7 hold the pass
+      float x[16];
+      tmem_ld16(tq + 256u + (uint32_t)(16 * cg), x);
+      if ((lane >> 3) == g) {
+        const int lc = 8 * quarter + (lane & 7);
+        unsigned char *dst = sm + C_ST + 2 * ST_BYTES;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) *reinterpret_cast<float *>(dst + st_off(16 * cg + e, lc)) = x[e];
+      }
+    }
+  };
   float *sQ = (float *)(sm + C_SQ), *sP = (float *)(sm + C_SP);
   float *totQ = (float *)(sm + C_TOT), *totP = totQ + 16 * 32;
-  const float *dglv = (const float *)(sm + C_DGL), *dbxv = (const float *)(sm + C_DBX);
+  const float *dglv = red + 64;
   const int i8 = lane >> 2, l4 = lane & 3, mid = len >> 1;
   float bpart[2] = {0.f, 0.f};
-  stage(1);
+  stage(0);
+  __syncthreads();
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    if (g < 3) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
-    else cp_wait_all();
-    __syncthreads();
     KDA_PT(9);
     float *totC = totP + 16 * 32 + (g & 1) * 4 * 32;  // double-buffered: read after the next pass starts
-    const uint32_t bq = (g & 1) ? C_ST1 : C_ST0_QB, bb = bq + ST_BYTES, bk = (g & 1) ? C_ST1 + 2 * ST_BYTES : C_ST0_K;
+    const uint32_t bq = C_ST, bb = C_ST + ST_BYTES, bk = C_ST + 2 * ST_BYTES;
     {
       float qv[1][2][2], pv[1][2][2], cq[1][2];  // [nt of the pass][hh][u], column sums [nt][u]
 #pragma unroll
@@ -501,8 +606,8 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Wor
           if (i8 == 0) totC[Bk * 32 + lc + u] = cs;
         }
       }
-      __syncthreads();  // buffer g & 1 consumed; dG tiles complete
-      if (g + 2 < 4) stage(g + 2);
+      __syncthreads();  // the staged products of pass g consumed; dG tiles complete
+      if (g + 1 < 4) stage(g + 1);
       KDA_PT(11);
       {  // thread: one column of the pass, one 4-row segment (warp = segment)
         const int col = tid & 31, seg = warp;
@@ -560,24 +665,32 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_chain_tc_kernel(Problem P, Wor
   __syncthreads();
   KDA_PT(7);
   if (tid < kC && tid < len)
-    args.dbeta[(size_t)(t0 + tid) * HV + j] = dbxv[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
+    args.dbeta[(size_t)(t0 + tid) * HV + j] = red[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
   KDA_PT(8);
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    tmem_free(tmem, TMEM_COLS);
+  }
   KDA_PT_FLUSH;
 }
 
 }  // namespace
 
-KDA_PT_EXPORT(kda_debug_chain_phase_cycles)
+KDA_PT_EXPORT(kda_debug_intra_phase_cycles)
 
-cudaError_t tc_backward_chain(const Problem &P, const Workspace &W, void *dq, void *dk, float *dg,
-                              float *dbeta, cudaStream_t s) {
+cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *dO, void *dv, void *dq, void *dk,
+                              float *dg, float *dbeta, int *err, cudaStream_t s) {
   if (P.NC == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kda_bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C_SMEM);
   if (e != cudaSuccess) return e;
   const bool partial = P.HV != P.H;
-  ChainArgs a{partial ? (void *)W.dqp : dq, partial ? (void *)W.dkp : dk, dg, dbeta, partial};
-  KDA_LAUNCH("kda_bwd_chain_tc", s, kda_bwd_chain_tc_kernel<<<dim3(P.NC, P.HV), kCT, C_SMEM, s>>>(P, W, a));
+  IntraArgs a{(const __nv_bfloat16 *)dO, (__nv_bfloat16 *)dv, partial ? (void *)W.dqp : dq,
+              partial ? (void *)W.dkp : dk, dg, dbeta, partial, err};
+  KDA_LAUNCH("kda_bwd_intra_tc", s,
+             kda_bwd_intra_tc_kernel<<<dim3(P.NC, P.HV), kCT, C_SMEM, s>>>(P, W, a));
   return cudaGetLastError();
 }
 
