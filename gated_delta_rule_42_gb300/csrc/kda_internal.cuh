@@ -55,8 +55,8 @@ struct Workspace {
   unsigned char *tc_xt;     // [slot] 16 KB: swizzled X^T tile [V][64]
   unsigned char *tc_dt;     // [slot] 16 KB: swizzled D^T tile [V][64]
   __nv_bfloat16 *tc_dh;     // [slot] 32 KB: gradient of the chunk-end state [K][V], swizzled operand tile
-  __nv_bfloat16 *tc_dd;     // [slot][64][V] gradient of the deltas
-  __nv_bfloat16 *tc_dx;     // [slot][64][V] dX = A^T dD
+  __nv_bfloat16 *tc_dd;     // [slot] 16 KB: gradient of the deltas [64][V], swizzled operand tile
+  __nv_bfloat16 *tc_dx;     // [slot] 16 KB: dX = A^T dD [64][V], swizzled operand tile
 };
 
 // --- element access -------------------------------------------------------
@@ -69,16 +69,17 @@ __device__ __forceinline__ void stf(__nv_bfloat16 *p, int64_t i, float x) {
   p[i] = __float2bfloat16_rn(x);
 }
 
-// TMA tensor maps of one call's per-token tensors, passed to the sequential
-// kernels as a __grid_constant__ parameter (tma.cu).  k, q: [Ttot][H][128]
-// bf16 and v (or dO): [Ttot][HV][128] bf16 as 64 x 64 boxes with the 128-byte
-// swizzle of the operand tiles; g: [Ttot][HV][128] fp32 as 64-row x 128 boxes.
+// TMA tensor maps of one call's per-token tensors, passed to the kernels as a
+// __grid_constant__ parameter (tma.cu).  k, q: [Ttot][H][128] bf16 and v, d (a
+// second per-value-head tensor: dO in the backward): [Ttot][HV][128] bf16 as
+// 64 x 64 boxes with the 128-byte swizzle of the operand tiles; g:
+// [Ttot][HV][128] fp32 as 64-row x 128 boxes.
 struct TmaMaps {
-  CUtensorMap k, q, v, g;
+  CUtensorMap k, q, v, g, d;
 };
-// Encodes the maps (v may be NULL: no map).  Fails without launching anything
-// if the driver rejects a map (e.g. a base pointer not 16-byte aligned).
-cudaError_t make_tma_maps(const Problem &P, const void *v, TmaMaps *out);
+// Encodes the maps (v, d may be NULL: no map).  Fails without launching
+// anything if the driver rejects a map (e.g. a base pointer not 16-byte aligned).
+cudaError_t make_tma_maps(const Problem &P, const void *v, const void *d, TmaMaps *out);
 
 // Number of SMs of the current device, cached per device (api.cu).
 cudaError_t sm_count(int *out);

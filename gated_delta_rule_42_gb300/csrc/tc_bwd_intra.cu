@@ -149,7 +149,8 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
 
 constexpr int kCT = 512;  // 16 warps: the chain is latency-bound, so more warps hide more of it
 
-__global__ void __launch_bounds__(kCT, 1) kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args) {
+__global__ void __launch_bounds__(kCT, 1)
+kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
@@ -168,48 +169,50 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_intra_tc_kernel(Problem P, Wor
   float *red = (float *)(sm + C_RED);  // [0, 64): sum_v dX v; [64, 192): d(2^G_last)
   uint64_t *bar = (uint64_t *)(sm + C_MISC);
   uint32_t *tslot = (uint32_t *)(sm + C_MISC + 8);
-  const __nv_bfloat16 *kin = (const __nv_bfloat16 *)P.k, *qin = (const __nv_bfloat16 *)P.q;
-  const __nv_bfloat16 *vin = (const __nv_bfloat16 *)P.v;
+  uint64_t *bar_ld = (uint64_t *)(sm + C_MISC + 16);
   constexpr float qscale = 0.08838834764831845f;
   KDA_PT_DECL;
 
-  // ---- loads: the product operands, then G, A and beta of the chain ----
-  {
-    const unsigned char *xt = W.tc_xt + slot * 16384, *dt = W.tc_dt + slot * 16384;
-    const unsigned char *hs = reinterpret_cast<const unsigned char *>(W.tc_hs + slot * kD * kD);
-    const unsigned char *dh = reinterpret_cast<const unsigned char *>(W.tc_dh + slot * kD * kD);
-    for (int it = tid; it < 1024; it += kCT) {  // X^T, D^T: verbatim (same swizzled layout)
-      cp16(sbase + I_XT + it * 16, xt + it * 16);
-      cp16(sbase + I_DT + it * 16, dt + it * 16);
-    }
-    for (int it = tid; it < 2048; it += kCT) {  // h, dh': verbatim
-      cp16(sbase + I_H + it * 16, hs + it * 16);
-      cp16(sbase + I_DH + it * 16, dh + it * 16);
-    }
-    for (int it = tid; it < 192 * 16; it += kCT) {  // [dX; dO; dD]
-      const int r = it >> 4, jj = it & 15;
-      const uint32_t dst = sbase + I_STK + sw_chunk(r, jj, 192);
-      const int rr = r & 63;
-      if (r < 64) cp16(dst, W.tc_dx + (slot * kC + rr) * kD + jj * 8);
-      else if (r >= 128) cp16(dst, W.tc_dd + (slot * kC + rr) * kD + jj * 8);
-      else if (rr < len) cp16(dst, args.dO + ((size_t)(t0 + rr) * HV + j) * kD + jj * 8);
-      else st_zero16(dst);
-    }
-    load_rows<kCT>(sbase + I_V, vin, t0, len, HV, j);
-    load_gate<kCT>(sbase + C_G, P.g, t0, len, HV, j);
-    const unsigned char *a = W.tc_tiles + slot * kTileRecord + kTileRecA;  // A, swizzled as here
-    for (int it = tid; it < 512; it += kCT) cp16(sbase + C_A + it * 16, a + it * 16);
-    if (tid < kC) {
-      if (tid < len) cp4(smem_u32(beta + tid), P.beta + (size_t)(t0 + tid) * HV + j);
-      else beta[tid] = 0.f;
-    }
-    cp_commit();
-  }
+  // ---- loads.  Bulk copies (one thread, counted on bar_ld): the saved tiles
+  // X^T, D^T, h, dh', dX, dD, A verbatim (dX, dD: one 8 KB piece per 64-column
+  // sub-tile of the stacked [dX; dO; dD] operand) and, by TMA, the dO and v rows.
+  // cp.async: G and beta. ----
   if (tid == 0) {
     bar_init(bar, 1);
+    bar_init(bar_ld, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_expect_tx(bar_ld, 2 * 16384u + 2 * 32768u + 2 * 16384u + 8192u + 2 * 16384u);
+    bulk_load(sbase + I_XT, W.tc_xt + slot * 16384, 16384u, bar_ld);
+    bulk_load(sbase + I_DT, W.tc_dt + slot * 16384, 16384u, bar_ld);
+    bulk_load(sbase + I_H, W.tc_hs + slot * kD * kD, 32768u, bar_ld);
+    bulk_load(sbase + I_DH, W.tc_dh + slot * kD * kD, 32768u, bar_ld);
+    const unsigned char *dx = reinterpret_cast<const unsigned char *>(W.tc_dx + slot * kC * kD);
+    const unsigned char *dd = reinterpret_cast<const unsigned char *>(W.tc_dd + slot * kC * kD);
+    bulk_load(sbase + I_STK, dx, 8192u, bar_ld);                        // rows 0..63, sub-tile 0
+    bulk_load(sbase + I_STK + 192 * 128, dx + 8192, 8192u, bar_ld);     //               sub-tile 1
+    bulk_load(sbase + I_STK + 128 * 128, dd, 8192u, bar_ld);            // rows 128..191
+    bulk_load(sbase + I_STK + 320 * 128, dd + 8192, 8192u, bar_ld);
+    bulk_load(sbase + C_A, W.tc_tiles + slot * kTileRecord + kTileRecA, 8192u, bar_ld);
+    tma_load3(sbase + I_STK + 64 * 128, &maps.d, 0, j, t0, bar_ld);    // dO rows 64..127
+    tma_load3(sbase + I_STK + 256 * 128, &maps.d, 64, j, t0, bar_ld);
+    tma_tile(sbase + I_V, &maps.v, j, t0, bar_ld);
+  }
+  load_gate<kCT>(sbase + C_G, P.g, t0, len, HV, j);
+  if (tid < kC) {
+    if (tid < len) cp4(smem_u32(beta + tid), P.beta + (size_t)(t0 + tid) * HV + j);
+    else beta[tid] = 0.f;
+  }
+  cp_commit();
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  bar_wait(bar_ld, 0, args.err);
+  if (len < kC)  // dO rows past the sequence end hold other tokens: clear them
+    for (int it = tid; it < (kC - len) * 16; it += kCT) {
+      const int r = 64 + len + (it >> 4), q = it & 15;
+      *reinterpret_cast<uint4 *>(sm + I_STK + sw_chunk(r, q, 192)) = make_uint4(0, 0, 0, 0);
+    }
   cp_wait_all();
   fence_async_smem();
   fence_before();
@@ -270,9 +273,12 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_intra_tc_kernel(Problem P, Wor
   KDA_PT(0);
 
   // ---- raw k, q rows for the decay tiles; dA^T, dAqk^T out of TMEM as hi/lo tiles; gate cumsum ----
-  load_rows<kCT>(sbase + C_KRAW, kin, t0, len, H, h);
-  load_rows<kCT>(sbase + C_QRAW, qin, t0, len, H, h);
-  cp_commit();
+  if (tid == 0) {  // raw k, q rows (TMA) into the dead operand tiles
+    fence_async_smem();
+    mbar_expect_tx(bar_ld, 32768u);
+    tma_tile(sbase + C_KRAW, &maps.k, h, t0, bar_ld);
+    tma_tile(sbase + C_QRAW, &maps.q, h, t0, bar_ld);
+  }
   {
     // Z: lanes 0..63 (i), cols 64..127 (m) = dA^T[i][m]; lanes 64..127, cols 0..63 = dAqk^T[i][r]
     const int cg = warp >> 2, i = 32 * (quarter & 1) + lane;
@@ -325,7 +331,11 @@ __global__ void __launch_bounds__(kCT, 1) kda_bwd_intra_tc_kernel(Problem P, Wor
 #pragma unroll
       for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
   }
-  cp_wait_all();  // raw k, q
+  bar_wait(bar_ld, 1, args.err);  // raw k, q
+  if (len < kC) {  // rows past the sequence end hold other tokens: clear them
+    zero_tail<kCT>(sm + C_KRAW, len);
+    zero_tail<kCT>(sm + C_QRAW, len);
+  }
   __syncthreads();
   KDA_PT(1);
   {
@@ -689,8 +699,10 @@ cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *
   const bool partial = P.HV != P.H;
   IntraArgs a{(const __nv_bfloat16 *)dO, (__nv_bfloat16 *)dv, partial ? (void *)W.dqp : dq,
               partial ? (void *)W.dkp : dk, dg, dbeta, partial, err};
+  TmaMaps maps;
+  if ((e = make_tma_maps(P, P.v, dO, &maps)) != cudaSuccess) return e;
   KDA_LAUNCH("kda_bwd_intra_tc", s,
-             kda_bwd_intra_tc_kernel<<<dim3(P.NC, P.HV), kCT, C_SMEM, s>>>(P, W, a));
+             kda_bwd_intra_tc_kernel<<<dim3(P.NC, P.HV), kCT, C_SMEM, s>>>(P, W, a, maps));
   return cudaGetLastError();
 }
 

@@ -14,8 +14,8 @@
 // commit log: "the kernel's reverse state-gradient recurrence").  Every
 // operand is read straight from the row-major tiles through K- or MN-major
 // descriptors.  For the per-chunk gradient kernel the scan saves, per chunk,
-// with bulk stores from shared memory: dh' (bf16 [K][V], swizzled operand
-// layout) and dD, dX (bf16 [64][V], row-major); at the start of the sequence
+// with bulk stores from shared memory: dh' (bf16 [K][V]) and dD, dX (bf16
+// [64][V]), all in the swizzled operand layout; at the start of the sequence
 // it writes dh0 (fp32).
 #include "tc_common.cuh"
 
@@ -140,15 +140,15 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
         for (int e = 0; e < 8; ++e) x[e] = d[q8 * 8 + e];
         *reinterpret_cast<uint4 *>(U + U_DDT + sw_chunk(v, (r0 >> 3) + q8, kD)) = pack8(x);
       }
-      __nv_bfloat16 *st = (__nv_bfloat16 *)(sm + OFF_KRAW) + v;  // row-major [r][v] staging
 #pragma unroll
-      for (int e = 0; e < 32; ++e) st[(r0 + e) * kD] = __float2bfloat16_rn(d[e]);
+      for (int e = 0; e < 32; ++e)  // [r][v] in the swizzled K-major operand layout
+        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_KRAW + sw_off(r0 + e, v, kC)) = __float2bfloat16_rn(d[e]);
     }
     fence_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
-    if (tid == 0) {  // dD, row-major [r][v], for the per-chunk kernel
+    if (tid == 0) {  // dD [r][v] (swizzled operand layout) for the per-chunk kernel
       bulk_store(W.tc_dd + slot * kC * kD, sbase + OFF_KRAW, 16384u);
       bulk_commit();
     }
@@ -172,15 +172,15 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const __nv_bfloat16 *__restrict__
         for (int e = 0; e < 8; ++e) x[e] = -d[q8 * 8 + e];
         *reinterpret_cast<uint4 *>(U + U_NDX + sw_chunk(v, (r0 >> 3) + q8, kD)) = pack8(x);
       }
-      __nv_bfloat16 *st = (__nv_bfloat16 *)(sm + OFF_QRAW) + v;  // row-major [i][v] staging
 #pragma unroll
-      for (int e = 0; e < 32; ++e) st[(r0 + e) * kD] = __float2bfloat16_rn(d[e]);
+      for (int e = 0; e < 32; ++e)  // [i][v] in the swizzled K-major operand layout
+        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_QRAW + sw_off(r0 + e, v, kC)) = __float2bfloat16_rn(d[e]);
     }
     fence_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
-    if (tid == 0) {  // dX, row-major [i][v], for the per-chunk kernel
+    if (tid == 0) {  // dX [i][v] (swizzled operand layout) for the per-chunk kernel
       bulk_store(W.tc_dx + slot * kC * kD, sbase + OFF_QRAW, 16384u);
       bulk_commit();
     }

@@ -219,8 +219,9 @@ __device__ __forceinline__ void tma_kqg(const TmaMaps &M, uint32_t base, int t0,
   tma_load3(base + OFF_GRAW, &M.g, 0, j, t0, bar);
 }
 // Rows len..63 of a swizzled [64][128] bf16 tile -> 0 (after its load completed).
+template <int NT = kThr>
 __device__ __forceinline__ void zero_tail(unsigned char *tile, int len) {
-  for (int it = threadIdx.x; it < (kC - len) * 16; it += kThr) {
+  for (int it = threadIdx.x; it < (kC - len) * 16; it += NT) {
     const int r = len + (it >> 4), q = it & 15;
     *reinterpret_cast<uint4 *>(tile + (q >> 3) * 8192 + r * 128 + (q & 7) * 16) = make_uint4(0, 0, 0, 0);
   }

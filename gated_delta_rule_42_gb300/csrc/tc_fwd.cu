@@ -306,7 +306,7 @@ cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT,
   if (e != cudaSuccess || P.N == 0) return e;
   FwdArgs a{(__nv_bfloat16 *)o, hT, err};
   TmaMaps maps;
-  if ((e = make_tma_maps(P, P.v, &maps)) != cudaSuccess) return e;
+  if ((e = make_tma_maps(P, P.v, nullptr, &maps)) != cudaSuccess) return e;
   const dim3 grid(P.N, P.HV);
   if (states) {
     e = cudaFuncSetAttribute(kda_fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -48,11 +48,12 @@ cudaError_t encode(CUtensorMap *m, const void *base, int bytes, int heads, int64
 
 }  // namespace
 
-cudaError_t make_tma_maps(const Problem &P, const void *v, TmaMaps *out) {
+cudaError_t make_tma_maps(const Problem &P, const void *v, const void *d, TmaMaps *out) {
   cudaError_t e;
   if ((e = encode(&out->k, P.k, 2, P.H, P.Ttot, 64, true)) != cudaSuccess) return e;
   if ((e = encode(&out->q, P.q, 2, P.H, P.Ttot, 64, true)) != cudaSuccess) return e;
   if (v != nullptr && (e = encode(&out->v, v, 2, P.HV, P.Ttot, 64, true)) != cudaSuccess) return e;
+  if (d != nullptr && (e = encode(&out->d, d, 2, P.HV, P.Ttot, 64, true)) != cudaSuccess) return e;
   return encode(&out->g, P.g, 4, P.HV, P.Ttot, 128, false);
 }
 
