@@ -97,7 +97,7 @@ constexpr uint32_t U_KR = 0, U_QR = 16384, U_KC = 32768, U_LF = 49152;  // (a)/(
 constexpr uint32_t U_AF = 0, U_T = 16384;                              // (b) inverse scratch
 constexpr uint32_t OFF_VEC = 215040;   // fp32 vectors (20 rows of 128)
 constexpr uint32_t OFF_BETA = 225280;  // beta, two buffers of 64 fp32
-constexpr uint32_t OFF_MISC = 225792;  // mbarriers (MMA +0, k/q/g loads +16, v loads +24), tmem slot +8
+constexpr uint32_t OFF_MISC = 225792;  // mbarriers (MMA +0, k/q/g loads +16, v loads +24, output MMA +32), tmem slot +8
 constexpr uint32_t SMEM_BYTES = 225792 + 64 + 1024;  // + alignment slack
 constexpr int V_GL = 0, V_GAML = 1, V_GREF = 2, V_EREF = 6, V_D = 10, V_LAM = 16;
 static_assert(OFF_QG == OFF_BK + 16384 && OFF_KH == OFF_QG + 16384 && OFF_AQK == OFF_KH + 16384 &&
@@ -490,28 +490,40 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
   }
   __syncthreads();
   KDA_PT(17);
-  {
-    const int r = tid >> 3, c4 = (tid & 7) * 4;  // one 1 x 4 segment of a 32 x 32 block per thread
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid < 128) {  // 32 x 32 products as 2 x 4 register tiles (rows rg, rg + 16) on four warps
+    const int rg = tid >> 3, c4 = (tid & 7) * 4;
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
 #pragma unroll 8
     for (int m = 0; m < 32; ++m) {  // T2 = L21 A1  (A1 lower triangular: zeros above)
-      const float l = Lf[fsw(32 + r, m)];
       const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(m, c4));
-      acc.x = fmaf(l, a.x, acc.x); acc.y = fmaf(l, a.y, acc.y);
-      acc.z = fmaf(l, a.z, acc.z); acc.w = fmaf(l, a.w, acc.w);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float l = Lf[fsw(32 + rg + 16 * k, m)];
+        acc[k].x = fmaf(l, a.x, acc[k].x); acc[k].y = fmaf(l, a.y, acc[k].y);
+        acc[k].z = fmaf(l, a.z, acc[k].z); acc[k].w = fmaf(l, a.w, acc[k].w);
+      }
     }
-    *reinterpret_cast<float4 *>(Tf + r * 32 + c4) = acc;
-    __syncthreads();
-    KDA_PT(18);
-    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) *reinterpret_cast<float4 *>(Tf + (rg + 16 * k) * 32 + c4) = acc[k];
+  }
+  __syncthreads();
+  KDA_PT(18);
+  if (tid < 128) {
+    const int rg = tid >> 3, c4 = (tid & 7) * 4;
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
 #pragma unroll 8
     for (int m = 0; m < 32; ++m) {  // A21 = -A2 T2
-      const float l = Af[fsw(32 + r, 32 + m)];
       const float4 t = *reinterpret_cast<const float4 *>(Tf + m * 32 + c4);
-      acc.x = fmaf(l, t.x, acc.x); acc.y = fmaf(l, t.y, acc.y);
-      acc.z = fmaf(l, t.z, acc.z); acc.w = fmaf(l, t.w, acc.w);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float l = Af[fsw(32 + rg + 16 * k, 32 + m)];
+        acc[k].x = fmaf(l, t.x, acc[k].x); acc[k].y = fmaf(l, t.y, acc[k].y);
+        acc[k].z = fmaf(l, t.z, acc[k].z); acc[k].w = fmaf(l, t.w, acc[k].w);
+      }
     }
-    *reinterpret_cast<float4 *>(Af + fsw(32 + r, c4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      *reinterpret_cast<float4 *>(Af + fsw(32 + rg + 16 * k, c4)) = make_float4(-acc[k].x, -acc[k].y, -acc[k].z, -acc[k].w);
   }
   __syncthreads();
   KDA_PT(19);

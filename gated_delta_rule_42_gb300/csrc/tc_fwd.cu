@@ -49,6 +49,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
   uint64_t *bar = (uint64_t *)(sm + OFF_MISC);
   uint32_t *tslot = (uint32_t *)(sm + OFF_MISC + 8);
   uint64_t *bar_kqg = (uint64_t *)(sm + OFF_MISC + 16), *bar_v = (uint64_t *)(sm + OFF_MISC + 24);
+  uint64_t *bar_o = (uint64_t *)(sm + OFF_MISC + 32);
   unsigned char *U = sm + OFF_U;
 
   const int n = blockIdx.x, j = blockIdx.y;
@@ -62,6 +63,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     bar_init(bar, 1);
     bar_init(bar_kqg, 1);
     bar_init(bar_v, 1);
+    bar_init(bar_o, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
@@ -70,7 +72,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
   fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
-  uint32_t phase = 0, kq_par = 0, v_par = 0;
+  uint32_t phase = 0, phase_o = 0, kq_par = 0, v_par = 0;
   KDA_PT_DECL;
 
   float hreg[64];  // h[cown][64 * vhalf + x]
@@ -230,32 +232,25 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
       bulk_commit();
     }
     if (tid == 0) {
-      if (kOut) {  // O^T[v][r] = sum_c h[c][v] Qg[r][c] + sum_i D^T[v][i] Aqk[r][i]
-        const uint32_t id = idesc(128, 64, 1, 0), id2 = idesc(128, 64, 0, 0);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) mma(tmem, desc_mn(aH, s, 16384), desc_k16(sbase + OFF_QG, s, kC), id, s > 0);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) mma(tmem, desc_k16(aD, s, kD), desc_k16(sbase + OFF_AQK, s, kC), id2, 1);
-      }
-      // U[c][v] = sum_r Khat[r][c] D[r][v]   (M=128 c, N=128 v, K=64 r)
+      // U[c][v] = sum_r Khat[r][c] D[r][v]   (M=128 c, N=128 v, K=64 r): the carried state first
       const uint32_t id3 = idesc(128, 128, 1, 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
         mma(tmem + 128, desc_mn(sbase + OFF_KH, s, 8192), desc_k16(aD, s, kD), id3, s > 0);
       commit(bar);
+      if (kOut) {  // O^T[v][r] = sum_c h[c][v] Qg[r][c] + sum_i D^T[v][i] Aqk[r][i], while the state updates
+        const uint32_t id = idesc(128, 64, 1, 0), id2 = idesc(128, 64, 0, 0);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mma(tmem, desc_mn(aH, s, 16384), desc_k16(sbase + OFF_QG, s, kC), id, s > 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) mma(tmem, desc_k16(aD, s, kD), desc_k16(sbase + OFF_AQK, s, kC), id2, 1);
+        commit(bar_o);
+      }
     }
     bar_wait(bar, phase, args.err);
     phase ^= 1;
     fence_after();
     KDA_PT(13);
-    if (kOut) {  // O^T -> staging tile [r][v], then coalesced 16-byte stores
-      const int v = cown, r0 = 32 * vhalf;
-      float d[32];
-      tmem_ld32(tq + (uint32_t)r0, d);
-      __nv_bfloat16 *Ot = (__nv_bfloat16 *)(U + U_O);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) Ot[(r0 + e) * kD + v] = __float2bfloat16_rn(d[e]);
-    }
     {
       const float gl = vec[V_GAML * kD + cown];
       float d[32];
@@ -265,6 +260,17 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
 #pragma unroll
         for (int e = 0; e < 32; ++e) hreg[32 * hx + e] = fmaf(gl, hreg[32 * hx + e], d[e]);
       }
+    }
+    if (kOut) {  // O^T -> staging tile [r][v], then coalesced 16-byte stores
+      bar_wait(bar_o, phase_o, args.err);
+      phase_o ^= 1;
+      fence_after();
+      const int v = cown, r0 = 32 * vhalf;
+      float d[32];
+      tmem_ld32(tq + (uint32_t)r0, d);
+      __nv_bfloat16 *Ot = (__nv_bfloat16 *)(U + U_O);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) Ot[(r0 + e) * kD + v] = __float2bfloat16_rn(d[e]);
     }
     fence_before();
     __syncthreads();
