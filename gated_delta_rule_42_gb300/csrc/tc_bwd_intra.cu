@@ -69,16 +69,15 @@ constexpr uint32_t LO128 = 16384, LO64 = 8192;
 constexpr uint32_t TMEM_COLS = 512;   // [128,256) S, [256,320) dKhat^T, [384,512) Z
 // Assembly scratch in the dead dL .. T tiles: the products of one pass (32
 // columns: 8 per column quarter) read out of TMEM as [64][32] fp32 tiles with
-// 16-byte chunks XOR-swizzled by row % 8, the dG tiles of the pass and the
-// segment totals of its column scans.
+// 16-byte chunks XOR-swizzled by row % 8, double-buffered, and the segment and
+// block totals of the final dg column scan.  dG itself is parked in the Kr / Qr
+// tiles: once a thread has read its Kr, Qr (hi and lo) at (r, c..c+1), the
+// 8 bytes of each pair slot hold dG's Q and P parts of (r, c) and (r, c+1).
 constexpr uint32_t ST_BYTES = 64 * 32 * 4;          // one staged [64][32] product
-constexpr uint32_t C_ST = C_DAB;                    // dQg | dBk | dKhat (24 KB)
-constexpr uint32_t SQ_LD = 36;                      // row stride (floats) of the dG pass tiles
-constexpr uint32_t C_SQ = C_ST + 3 * ST_BYTES;      // Q part of dG, one pass [64][SQ_LD]
-constexpr uint32_t C_SP = C_SQ + 64 * SQ_LD * 4;    // P part
-constexpr uint32_t C_TOT = C_SP + 64 * SQ_LD * 4;   // segment totals of Q, P [16][32]; Khat column term [2][4][32]
-static_assert(C_TOT + (16 + 16 + 8) * 32 * 4 <= C_G, "assembly scratch overflows the chain tiles");
-static_assert(I_V + 16384 == C_G && C_A % 1024 == 0, "map");
+constexpr uint32_t C_ST0 = C_DAB;                   // pass buffer 0: dQg | dBk | dKhat (24 KB)
+constexpr uint32_t C_ST1 = C_ST0 + 3 * ST_BYTES;    // pass buffer 1
+constexpr uint32_t C_TOT = C_ST1 + 3 * ST_BYTES;    // totals of Q, P [4 segments][128]; Khat column term [4 blocks][128]
+static_assert(C_TOT + 3 * 4 * 128 * 4 <= C_G, "assembly scratch overflows the chain tiles");
 // byte offset of element (r, c) of a staged [64][32] product
 __device__ __forceinline__ uint32_t st_off(int r, int c) {
   return (uint32_t)r * 128u + ((uint32_t)((c >> 2) ^ (r & 7)) << 4) + (uint32_t)(c & 3) * 4u;
@@ -492,20 +491,22 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 
   // ---- assembly (fragment element (r, c)), in four passes of 8 columns per warp ----
   // Each pass reads its 32 columns (8 per column quarter) of dQg, dBk and
-  // dKhat out of TMEM into a swizzled shared-memory tile.  Raw k and q are not
-  // re-read: every term that needs them is a product with a decay factor that
-  // the hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2 hold.  dg = reverse cumsum
-  // of dG over the chunk runs per pass as column scans over 4-row segments with
-  // segment totals exchanged in shared memory.
+  // dKhat out of TMEM into a swizzled shared-memory tile (two buffers: pass
+  // g + 2 is staged once pass g is done).  Raw k and q are not re-read: every
+  // term that needs them is a product with a decay factor that the hi/lo
+  // tiles Kr = k e1, Qr = q~ e1, Kc = k e2 hold.  dg = reverse cumsum of dG
+  // over the chunk runs once, after the last pass, as column scans over
+  // 16-row segments with segment totals exchanged in shared memory.
   auto stage = [&](int g) {
     const int cg = warp >> 2;  // column quarter of this warp (8 columns of the pass)
+    const uint32_t buf = (g & 1) ? C_ST1 : C_ST0;
     {  // S: lane quarters 0, 1 = -dBk rows, 2, 3 = dQg rows
       float x[8];
       tmem_ld8(tq + 128u + (uint32_t)(32 * cg + 8 * g), x);
       const int r = 32 * (quarter & 1) + lane;
       const bool isq = quarter >= 2;
       const float sg = isq ? 1.f : -1.f;
-      unsigned char *dst = sm + C_ST + (isq ? 0u : ST_BYTES);
+      unsigned char *dst = sm + buf + (isq ? 0u : ST_BYTES);
       *reinterpret_cast<float4 *>(dst + st_off(r, 8 * cg)) = make_float4(sg * x[0], sg * x[1], sg * x[2], sg * x[3]);
       *reinterpret_cast<float4 *>(dst + st_off(r, 8 * cg + 4)) = make_float4(sg * x[4], sg * x[5], sg * x[6], sg * x[7]);
     }
@@ -514,155 +515,145 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       tmem_ld16(tq + 256u + (uint32_t)(16 * cg), x);
       if ((lane >> 3) == g) {
         const int lc = 8 * quarter + (lane & 7);
-        unsigned char *dst = sm + C_ST + 2 * ST_BYTES;
+        unsigned char *dst = sm + buf + 2 * ST_BYTES;
 #pragma unroll
         for (int e = 0; e < 16; ++e) *reinterpret_cast<float *>(dst + st_off(16 * cg + e, lc)) = x[e];
       }
     }
   };
-  float *sQ = (float *)(sm + C_SQ), *sP = (float *)(sm + C_SP);
-  float *totQ = (float *)(sm + C_TOT), *totP = totQ + 16 * 32;
+  float *totQ = (float *)(sm + C_TOT), *totP = totQ + 4 * kD, *totC = totP + 4 * kD;
   const float *dglv = red + 64;
-  const int i8 = lane >> 2, l4 = lane & 3, mid = len >> 1;
+  const int i8 = lane >> 2, l4 = lane & 3;
   float bpart[2] = {0.f, 0.f};
   stage(0);
+  stage(1);
   __syncthreads();
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     KDA_PT(9);
-    float *totC = totP + 16 * 32 + (g & 1) * 4 * 32;  // double-buffered: read after the next pass starts
-    const uint32_t bq = C_ST, bb = C_ST + ST_BYTES, bk = C_ST + 2 * ST_BYTES;
+    const uint32_t bq = (g & 1) ? C_ST1 : C_ST0, bb = bq + ST_BYTES, bk = bq + 2 * ST_BYTES;
     {
-      float qv[1][2][2], pv[1][2][2], cq[1][2];  // [nt of the pass][hh][u], column sums [nt][u]
+      const int nt = g;
+      const int c = ch0 + 8 * nt + 2 * l4;
+      const int lc = 8 * (warp & 3) + 2 * l4;  // column in the staging
+      const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
+      const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
+      const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
+      float cq[2] = {0.f, 0.f};
 #pragma unroll
-      for (int ntl = 0; ntl < 1; ++ntl) {
-        const int nt = g;
-        const int c = ch0 + 8 * nt + 2 * l4;
-        const int lc = 8 * (warp & 3) + 2 * l4;  // column in the staging
-        const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
-        const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
-        const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
-        cq[ntl][0] = cq[ntl][1] = 0.f;
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * Bk + i8 + 8 * hh;
+        const float br = beta[r];
+        const uint32_t so = st_off(r, lc);
+        const float2 vq = *reinterpret_cast<const float2 *>(sm + bq + so);
+        const float2 vb = *reinterpret_cast<const float2 *>(sm + bb + so);
+        const float2 vk = *reinterpret_cast<const float2 *>(sm + bk + so);
+        const uint32_t to = sw_off(r, c, kC);
+        uint32_t *krh_p = reinterpret_cast<uint32_t *>(sm + C_KR + to), *krl_p = reinterpret_cast<uint32_t *>(sm + C_KR + LO128 + to);
+        uint32_t *qrh_p = reinterpret_cast<uint32_t *>(sm + C_QR + to), *qrl_p = reinterpret_cast<uint32_t *>(sm + C_QR + LO128 + to);
+        const float2 krh = unpack_bf16(*krh_p), krl = unpack_bf16(*krl_p);
+        const float2 qrh = unpack_bf16(*qrh_p), qrl = unpack_bf16(*qrl_p);
+        const float2 kch = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + to));
+        const float2 kcl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + LO128 + to));
+        const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
+        float dq2[2], dk2[2], qv[2], pv[2];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * Bk + i8 + 8 * hh;
-          const float br = beta[r];
-          const uint32_t so = st_off(r, lc);
-          const float2 vq = *reinterpret_cast<const float2 *>(sm + bq + so);
-          const float2 vb = *reinterpret_cast<const float2 *>(sm + bb + so);
-          const float2 vk = *reinterpret_cast<const float2 *>(sm + bk + so);
-          const uint32_t to = sw_off(r, c, kC);
-          const float2 krh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + to));
-          const float2 krl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + LO128 + to));
-          const float2 qrh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + to));
-          const float2 qrl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + LO128 + to));
-          const float2 kch = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + to));
-          const float2 kcl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + LO128 + to));
-          const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
-          float dq2[2], dk2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float Kr = u ? krh.y + krl.y : krh.x + krl.x;  // k e1
-            const float Qr = u ? qrh.y + qrl.y : qrh.x + qrl.x;  // q~ e1
-            const float Kc = u ? kch.y + kcl.y : kch.x + kcl.x;  // k e2
-            const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = u ? vk.y : vk.x;
-            const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
-            const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
-            const float e1 = exp2f(gg_ - gref), e2 = exp2f(gref - gg_);
-            const float gam = e1 * eref, kh = e2 * lam;
-            const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
-            const float xyI = xyi[nt][2 * hh + u];
-            dq2[u] = dQg * gam + e1 * yR;
-            dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * xyI;
-            // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
-            const bool in = r < len;
-            qv[ntl][hh][u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
-            pv[ntl][hh][u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * xyI - dKh * Kc * lam) : 0.f;
-            bpart[hh] += dBk * Kr * eref + Kr * xR;
-            cq[ntl][u] += dKh * Kc * lam;
+        for (int u = 0; u < 2; ++u) {
+          const float Kr = u ? krh.y + krl.y : krh.x + krl.x;  // k e1
+          const float Qr = u ? qrh.y + qrl.y : qrh.x + qrl.x;  // q~ e1
+          const float Kc = u ? kch.y + kcl.y : kch.x + kcl.x;  // k e2
+          const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = u ? vk.y : vk.x;
+          const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
+          const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
+          const float e1 = exp2f(gg_ - gref), e2 = exp2f(gref - gg_);
+          const float gam = e1 * eref, kh = e2 * lam;
+          const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
+          const float xyI = xyi[nt][2 * hh + u];
+          dq2[u] = dQg * gam + e1 * yR;
+          dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * xyI;
+          // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
+          const bool in = r < len;
+          qv[u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
+          pv[u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * xyI - dKh * Kc * lam) : 0.f;
+          bpart[hh] += dBk * Kr * eref + Kr * xR;
+          cq[u] += dKh * Kc * lam;
+        }
+        // dG of (r, c) and (r, c + 1) into the Kr (Q part) and Qr (P part) pair slots just read
+        *krh_p = __float_as_uint(qv[0]);
+        *krl_p = __float_as_uint(qv[1]);
+        *qrh_p = __float_as_uint(pv[0]);
+        *qrl_p = __float_as_uint(pv[1]);
+        if (r < len) {
+          const size_t tok = (size_t)(t0 + r);
+          if (args.partial) {
+            float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
+            *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
+            *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
+          } else {
+            __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
+            __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
+            *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
+            *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
           }
-          if (r < len) {
-            const size_t tok = (size_t)(t0 + r);
-            if (args.partial) {
-              float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
-              *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
-              *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
-            } else {
-              __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
-              __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
-              *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
-              *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
-            }
-          }
         }
       }
-      KDA_PT(10);
-      // dG of this pass's 32 columns -> shared memory, then the column scans
 #pragma unroll
-      for (int ntl = 0; ntl < 1; ++ntl) {
-        const int lc = 8 * (warp & 3) + 2 * l4;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * Bk + i8 + 8 * hh;
-          *reinterpret_cast<float2 *>(sQ + r * SQ_LD + lc) = make_float2(qv[ntl][hh][0], qv[ntl][hh][1]);
-          *reinterpret_cast<float2 *>(sP + r * SQ_LD + lc) = make_float2(pv[ntl][hh][0], pv[ntl][hh][1]);
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {  // column sums of dKhat k khat over the warp's 16 rows
-          float cs = cq[ntl][u];
-          cs += __shfl_xor_sync(0xffffffffu, cs, 4);
-          cs += __shfl_xor_sync(0xffffffffu, cs, 8);
-          cs += __shfl_xor_sync(0xffffffffu, cs, 16);
-          if (i8 == 0) totC[Bk * 32 + lc + u] = cs;
-        }
+      for (int u = 0; u < 2; ++u) {  // column sums of dKhat k khat over the warp's 16 rows
+        float cs = cq[u];
+        cs += __shfl_xor_sync(0xffffffffu, cs, 4);
+        cs += __shfl_xor_sync(0xffffffffu, cs, 8);
+        cs += __shfl_xor_sync(0xffffffffu, cs, 16);
+        if (i8 == 0) totC[Bk * kD + c + u] = cs;
       }
-      __syncthreads();  // the staged products of pass g consumed; dG tiles complete
-      if (g + 1 < 4) stage(g + 1);
-      KDA_PT(11);
-      {  // thread: one column of the pass, one 4-row segment (warp = segment)
-        const int col = tid & 31, seg = warp;
-        const int cc = 32 * (col >> 3) + 8 * g + (col & 7);
-        float q8[4], p8[4], tq = 0.f, tp = 0.f;
+    }
+    KDA_PT(10);
+    __syncthreads();  // the staged products of pass g consumed
+    if (g + 2 < 4) stage(g + 2);
+    KDA_PT(11);
+  }
+  {  // dg = reverse cumsum of dG: thread = one column, one 16-row segment (4 segments)
+    const int c = tid & (kD - 1), seg = tid >> 7, mid = len >> 1;
+    // element (r, c) of the parked dG: even c in the hi slot of its pair, odd c in the lo slot
+    const uint32_t po = (c & 1) ? LO128 : 0u;
+    float q16[16], p16[16], tq = 0.f, tp = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          q8[k] = sQ[(4 * seg + k) * SQ_LD + col];
-          p8[k] = sP[(4 * seg + k) * SQ_LD + col];
-          tq += q8[k];
-          tp += p8[k];
-        }
-        totQ[seg * 32 + col] = tq;
-        totP[seg * 32 + col] = tp;
-        __syncthreads();
-        float aq = 0.f, aps = 0.f, app = 0.f;
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t to = sw_off(16 * seg + k, c & ~1, kC) + po;
+      q16[k] = *reinterpret_cast<const float *>(sm + C_KR + to);
+      p16[k] = *reinterpret_cast<const float *>(sm + C_QR + to);
+      tq += q16[k];
+      tp += p16[k];
+    }
+    totQ[seg * kD + c] = tq;
+    totP[seg * kD + c] = tp;
+    __syncthreads();
+    float aq = 0.f, aps = 0.f, app = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2) {
-          const float a = totQ[s2 * 32 + col], b = totP[s2 * 32 + col];
-          if (s2 > seg) { aq += a; aps += b; }
-          if (s2 < seg) app += b;
-        }
-        const float ks = totC[col] + totC[32 + col] + totC[64 + col] + totC[96 + col];
-        // dg_t = sum_{s>=t} dG_s: the Q part and the carried-state decay term
-        // from the chunk end; the zero-sum P part from whichever end is nearer
-        // (sum_{s>=t} P_s = -sum_{s<t} P_s, the Khat column sum counted at the
-        // last row), halving the cancelling terms it sums.
-        const float carried = kLn2 * vec[V_GAML * kD + cc] * dglv[cc];
-        float pre[4];
-        pre[0] = app;
+    for (int s2 = 0; s2 < 4; ++s2) {
+      const float a = totQ[s2 * kD + c], b = totP[s2 * kD + c];
+      if (s2 > seg) { aq += a; aps += b; }
+      if (s2 < seg) app += b;
+    }
+    const float ks = totC[c] + totC[kD + c] + totC[2 * kD + c] + totC[3 * kD + c];
+    // dg_t = sum_{s>=t} dG_s: the Q part and the carried-state decay term
+    // from the chunk end; the zero-sum P part from whichever end is nearer
+    // (sum_{s>=t} P_s = -sum_{s<t} P_s, the Khat column sum counted at the
+    // last row), halving the cancelling terms it sums.
+    const float carried = kLn2 * vec[V_GAML * kD + c] * dglv[c];
+    float pre[16];
+    pre[0] = app;
 #pragma unroll
-        for (int k = 1; k < 4; ++k) pre[k] = pre[k - 1] + p8[k - 1];
-        float qs = aq, ps = aps + kLn2 * ks;
+    for (int k = 1; k < 16; ++k) pre[k] = pre[k - 1] + p16[k - 1];
+    float qs = aq, ps = aps + kLn2 * ks;
 #pragma unroll
-        for (int k = 3; k >= 0; --k) {
-          const int r = 4 * seg + k;
-          qs += q8[k];
-          ps += p8[k];
-          if (r < len)
-            args.dg[((size_t)(t0 + r) * HV + j) * kD + cc] = qs + carried + (r >= mid ? ps : -pre[k]);
-        }
-      }
-      KDA_PT(12);
+    for (int k = 15; k >= 0; --k) {
+      const int r = 16 * seg + k;
+      qs += q16[k];
+      ps += p16[k];
+      if (r < len) args.dg[((size_t)(t0 + r) * HV + j) * kD + c] = qs + carried + (r >= mid ? ps : -pre[k]);
     }
   }
+  KDA_PT(12);
   KDA_PT(6);
   // dbeta partials: reduce over the 4 lanes sharing a row, then per column half
 #pragma unroll
