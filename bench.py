@@ -94,6 +94,39 @@ def kernel_bytes_per_token(name, cfg):
     return table.get(name)
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
+# kernel from one ncu --set full capture, per token of the captured launch, with
+# the SHA-256 of the sources the kernel was built from at capture time.  The
+# value is reported only while those sources are unchanged.
+NCU_TRAFFIC = {
+    "kda_bwd_intra_tc": dict(
+        bytes_per_token=1293894400 / 8192,  # 981.0 MB read + 312.9 MB written, B=8 T=1024 H=HV=32
+        sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_intra.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh",
+                 "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
+        sha256="045197515c46e68797bc0585b436ded83feaa3a0815eea318684e495adee4542",
+        profile="profiles/ncu_full_kernels_B8_T1024_H32_K128.md"),
+}
+
+
+def sources_sha256(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(name, tokens):
+    """Per-launch DRAM bytes of kernel ``name`` scaled to ``tokens`` (its traffic
+    grows in proportion to the (chunk, head) slots), or None when no capture of
+    the current sources exists."""
+    t = NCU_TRAFFIC.get(name)
+    if t is None or sources_sha256(t["sources"]) != t["sha256"]:
+        return None
+    return int(round(t["bytes_per_token"] * tokens))
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -400,7 +433,7 @@ def main():
     roof = dict(kernel=dom, bound="hbm", achieved=None if achieved is None else round(achieved, 1),
                 peak=peaks["hbm"], unit="GB/s",
                 frac=None if achieved is None else round(achieved / peaks["hbm"], 4),
-                traffic=None, launch_ms=round(dom_ms / dom_n, 4),
+                traffic=measured_traffic(dom, toks), launch_ms=round(dom_ms / dom_n, 4),
                 peak_source=f"{peaks['src']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["src"] == "measured"
                 else "fallback 6.8 TB/s")
     out = {
