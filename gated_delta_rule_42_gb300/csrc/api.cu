@@ -98,9 +98,9 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   w.chunk = (int4 *)take(sizeof(int4) * (size_t)(P.NC > 0 ? P.NC : 1));
   w.flags = (int *)take(sizeof(int) * 4);
   if (use_tc(P)) {
+    w.tc_tiles = (unsigned char *)take(kTileRecord * slots);  // per-chunk records of the preparation kernel
     if (backward) {  // tensor-core backward: per-slot tiles passed between its kernels
       w.tc_hs = (__nv_bfloat16 *)take(2 * slots * K * V);
-      w.tc_tiles = (unsigned char *)take(kTileRecord * slots);
       w.tc_xt = (unsigned char *)take(16384 * slots);
       w.tc_dt = (unsigned char *)take(16384 * slots);
       w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);
@@ -112,7 +112,7 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
       }
     }
     if (W) *W = w;
-    return off;  // the fused forward keeps everything on chip
+    return off;
   }
   w.G = (float *)take(sizeof(float) * slots * C * K);
   w.Aqk = (float *)take(sizeof(float) * slots * C * C);

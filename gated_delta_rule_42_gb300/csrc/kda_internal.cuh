@@ -112,6 +112,8 @@ cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t 
 // "states" mode for the backward: no output; per (chunk, value head) slot it
 // saves the chunk-start state and the Aqk, A, X^T and D^T tiles to
 // W.tc_hs / tc_tiles / tc_xt / tc_dt.
+// Per-chunk records (tc_prep.cu): one CTA per (chunk, value head) slot.
+cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps, int *err, cudaStream_t s);
 cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, bool states,
                        int *err, cudaStream_t s);
 cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,

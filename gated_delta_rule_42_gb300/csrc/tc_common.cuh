@@ -1,17 +1,7 @@
-// Shared pieces of the fused bf16 tensor-core KDA kernels (K = V = 128,
-// chunk 64): the shared-memory map, the asynchronous chunk loads, and the two
-// V-independent phases every chunk step needs:
-//  (a) chunk-local cumsum G of the log2 gate and the decay-scaled operand tiles;
-//  (b) the decayed Gram blocks L (strictly lower, beta-scaled) and Aqk (lower)
-//      on 16x16 warp MMAs, and A = (I + L)^-1 in fp32.
-//
-// Decay scaling.  2^(G_r - G_i) is split at the first row of each 16-token
-// block (ref): rows carry 2^(G_r - G_ref) <= 1 (tile Kr / Qr), columns carry
-// 2^(G_ref - G_i) <= 2^(15 |g|max) (tile Kc), and between blocks the per-channel
-// factor D_RI = 2^(G_ref(R) - G_ref(I)) <= 1 is applied to the column fragments
-// in registers.  Nothing overflows for gates >= -8 per token (log2 units).  The
-// chunk-level tiles Bk = beta k 2^G, Qg = q~ 2^G and Khat = k 2^(G_last - G)
-// only underflow where the true value is negligible.
+// Shared pieces of the bf16 tensor-core KDA kernels (K = V = 128, chunk 64):
+// the shared-memory map of the reverse scan, the asynchronous loads and bulk
+// copies, the vectors of per-channel decay factors, and the operand-descriptor
+// helpers.
 //
 // Every operand tile is 128-byte swizzled (see umma.cuh), so the same bytes
 // serve as a K-major or an MN-major tcgen05 operand and as an ldmatrix source.
@@ -79,10 +69,10 @@ static __shared__ long long kda_pt_acc[33];  // [32] = time of the last stamp
 constexpr int kC = 64;     // chunk
 constexpr int kD = 128;    // K = V
 constexpr int kThr = 256;  // 8 warps
-constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile of the chain kernel
-constexpr int kGT = 128;   // row stride of the TMA-loaded gate tile of the sequential kernels
+constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile of the per-chunk gradient kernel
+constexpr int kGT = 128;   // row stride of the TMA-loaded gate tile (dense rows)
 
-// shared memory map (bytes from a 1024-aligned base)
+// shared memory map of the reverse scan (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_KRAW = 0;       // k  [64][128] bf16
 constexpr uint32_t OFF_QRAW = 16384;   // q  [64][128]
 constexpr uint32_t OFF_VRAW = 32768;   // v (forward) or dO (backward) [64][128]
@@ -92,9 +82,7 @@ constexpr uint32_t OFF_QG = 100352;    // q~ 2^G             [64 r][128 c]
 constexpr uint32_t OFF_KH = 116736;    // k 2^(G_last - G)   [64 r][128 c]
 constexpr uint32_t OFF_AQK = 133120;   // Aqk                [64 r][64 i]
 constexpr uint32_t OFF_AM = 141312;    // A = (I + L)^-1     [64 r][64 i]
-constexpr uint32_t OFF_U = 149504;     // union (64 KB): phases (a)/(b) | phase (c)
-constexpr uint32_t U_KR = 0, U_QR = 16384, U_KC = 32768, U_LF = 49152;  // (a)/(b)
-constexpr uint32_t U_AF = 0, U_T = 16384;                              // (b) inverse scratch
+constexpr uint32_t OFF_U = 149504;     // 64 KB of per-kernel scratch
 constexpr uint32_t OFF_VEC = 215040;   // fp32 vectors (20 rows of 128)
 constexpr uint32_t OFF_BETA = 225280;  // beta, two buffers of 64 fp32
 constexpr uint32_t OFF_MISC = 225792;  // mbarriers (MMA +0, k/q/g loads +16, v loads +24, output MMA +32), tmem slot +8
@@ -208,16 +196,6 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, i
   tma_load3(dst, map, 0, head, t0, bar);
   tma_load3(dst + 8192, map, 64, head, t0, bar);
 }
-// k, q (when with_q) and the gate rows of one chunk, issued by one thread:
-// rows past the tensor end arrive as zeros, rows past the sequence end hold
-// the next tokens (zero_tail clears them where it matters).
-__device__ __forceinline__ void tma_kqg(const TmaMaps &M, uint32_t base, int t0, int h, int j, bool with_q,
-                                        uint64_t *bar) {
-  mbar_expect_tx(bar, (with_q ? 32768u : 16384u) + 32768u);
-  tma_tile(base + OFF_KRAW, &M.k, h, t0, bar);
-  if (with_q) tma_tile(base + OFF_QRAW, &M.q, h, t0, bar);
-  tma_load3(base + OFF_GRAW, &M.g, 0, j, t0, bar);
-}
 // Rows len..63 of a swizzled [64][128] bf16 tile -> 0 (after its load completed).
 template <int NT = kThr>
 __device__ __forceinline__ void zero_tail(unsigned char *tile, int len) {
@@ -232,311 +210,6 @@ __device__ __forceinline__ void load_beta(const Problem &P, float *dst, int t0, 
     if (threadIdx.x < len) cp4(smem_u32(dst + threadIdx.x), P.beta + (size_t)(t0 + threadIdx.x) * P.HV + j);
     else dst[threadIdx.x] = 0.f;
   }
-}
-
-// Phase (a).  Needs the k (and q) staging tiles, the gate tile and beta of the
-// chunk; ends with a __syncthreads.  Writes G (in place), the vectors, and the
-// tiles Bk, Khat (and Qg when kQ); with kGram also the decay tiles Kr, Kc (and
-// Qr) that the Gram blocks of phase (b) need.
-template <bool kQ, bool kGram = true>
-__device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float *beta) {
-  const int tid = threadIdx.x;
-  float *G = (float *)(sm + OFF_GRAW);
-  float *vec = (float *)(sm + OFF_VEC);
-  unsigned char *U = sm + OFF_U;
-  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
-  {  // two threads per channel (adjacent lanes), 32 rows each
-    const int c = tid >> 1, hf = tid & 1, r0 = 32 * hf, lane = tid & 31;
-    float col[32];
-    float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) col[k] = G[(r0 + k) * kGT + c];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      if (r0 + k < len) s += col[k];
-      col[k] = s;
-    }
-    const float lo_total = __shfl_sync(0xffffffffu, s, lane & ~1);
-    const float add = hf ? lo_total : 0.f;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      col[k] += add;
-      G[(r0 + k) * kGT + c] = col[k];
-    }
-    const float gl = __shfl_sync(0xffffffffu, s + add, lane | 1);
-    // block references: rows 0, 16 (lower partner) and 32, 48 (upper partner)
-    const float ga = (r0 < len) ? col[0] : gl, gb = (r0 + 16 < len) ? col[16] : gl;
-    float gref[4];
-    gref[0] = __shfl_sync(0xffffffffu, ga, lane & ~1);
-    gref[1] = __shfl_sync(0xffffffffu, gb, lane & ~1);
-    gref[2] = __shfl_sync(0xffffffffu, ga, lane | 1);
-    gref[3] = __shfl_sync(0xffffffffu, gb, lane | 1);
-    if (hf == 0) {
-      vec[V_GL * kD + c] = gl;
-      vec[V_GAML * kD + c] = exp2f(gl);
-    }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {  // this partner's own two references (ga, gb)
-      const int R = 2 * hf + q;
-      const float gr = q ? gb : ga;
-      vec[(V_GREF + R) * kD + c] = gr;
-      vec[(V_EREF + R) * kD + c] = exp2f(gr);
-      vec[(V_LAM + R) * kD + c] = exp2f(gl - gr);
-    }
-    // D_RI = 2^(gref_R - gref_I) for the pairs (1,0) (2,0) (2,1) | (3,0) (3,1) (3,2)
-    if (hf == 0) {
-      vec[(V_D + 0) * kD + c] = exp2f(gref[1] - gref[0]);
-      vec[(V_D + 1) * kD + c] = exp2f(gref[2] - gref[0]);
-      vec[(V_D + 2) * kD + c] = exp2f(gref[2] - gref[1]);
-    } else {
-      vec[(V_D + 3) * kD + c] = exp2f(gref[3] - gref[0]);
-      vec[(V_D + 4) * kD + c] = exp2f(gref[3] - gref[1]);
-      vec[(V_D + 5) * kD + c] = exp2f(gref[3] - gref[2]);
-    }
-  }
-  __syncthreads();
-  KDA_PT(1);
-  // thread: 8 consecutive channels (one 16-byte chunk) of 4 consecutive rows
-  {
-    const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
-    float gref[8], eref[8], lam[8];
-#pragma unroll
-    for (int e = 0; e < 8; e += 4) {
-      *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (V_GREF + R) * kD + c0 + e);
-      *reinterpret_cast<float4 *>(eref + e) = *reinterpret_cast<const float4 *>(vec + (V_EREF + R) * kD + c0 + e);
-      *reinterpret_cast<float4 *>(lam + e) = *reinterpret_cast<const float4 *>(vec + (V_LAM + R) * kD + c0 + e);
-    }
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int r = rg * 4 + rr;
-      const uint32_t off = sw_chunk(r, jj, kC);
-      float kv[8], qv[8], g[8], e1[8], e2[8], o[8];
-      unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + off), kv);
-      if (kQ) unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + off), qv);
-      *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGT + c0);
-      *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + 4);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        e1[e] = exp2f(g[e] - gref[e]);  // <= 1
-        e2[e] = exp2f(gref[e] - g[e]);  // >= 1
-      }
-      const float br = beta[r];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
-      if (kGram) *reinterpret_cast<uint4 *>(U + U_KR + off) = pack8(o);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
-      if (kGram) *reinterpret_cast<uint4 *>(U + U_KC + off) = pack8(o);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * e1[e] * eref[e];
-      *reinterpret_cast<uint4 *>(sm + OFF_BK + off) = pack8(o);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e] * lam[e];
-      *reinterpret_cast<uint4 *>(sm + OFF_KH + off) = pack8(o);
-      if (kQ) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
-        if (kGram) *reinterpret_cast<uint4 *>(U + U_QR + off) = pack8(o);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] *= eref[e];
-        *reinterpret_cast<uint4 *>(sm + OFF_QG + off) = pack8(o);
-      }
-    }
-  }
-  __syncthreads();
-}
-
-// fp32 [64][64] scratch of phase (b) (L, then A): columns XOR-swizzled by
-// 4 * (row % 8), so reads of one column across 8 rows and float4 reads of four
-// consecutive columns are both free of bank conflicts.
-__device__ __forceinline__ int fsw(int r, int c) { return r * kC + (c ^ ((r & 7) << 2)); }
-
-// Phase (b).  Needs the tiles of phase (a); ends with a __syncthreads.  Writes
-// the A tile (and the Aqk tile when kQ).  Clobbers the union region.
-template <bool kQ>
-__device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t sbase = smem_u32(sm);
-  const float *vec = (const float *)(sm + OFF_VEC);
-  unsigned char *U = sm + OFF_U;
-  float *Lf = (float *)(U + U_LF);
-  // Gram blocks: the 10 block pairs R >= I over the 8 warps (the A fragments of
-  // a pair serve both 8-column halves: shared-memory wavefronts bound this phase).
-  for (int p = warp; p < 10; p += 8) {
-    const int R = p >= 6 ? 3 : p >= 3 ? 2 : p >= 1 ? 1 : 0, I = p - R * (R + 1) / 2;
-    const float *Dv = (I < R) ? vec + (V_D + R * (R - 1) / 2 + I) * kD : nullptr;
-    float accL[2][4] = {}, accQ[2][4] = {};
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint32_t ak[4], aq[4] = {0, 0, 0, 0}, b[4];
-      {
-        const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
-        ldsm_x4(sbase + OFF_U + U_KR + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
-        if (kQ) ldsm_x4(sbase + OFF_U + U_QR + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
-      }
-      {
-        const int mi = lane >> 3;
-        const int row = 16 * I + (lane & 7) + (mi >> 1) * 8, jj = 2 * s + (mi & 1);
-        ldsm_x4(sbase + OFF_U + U_KC + sw_chunk(row, jj, kC), b[0], b[1], b[2], b[3]);
-      }
-      if (Dv != nullptr) {
-        const int c0 = 16 * s + (lane & 3) * 2;
-        const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
-        const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float2 f = unpack_bf16(b[t]);
-          b[t] = (t & 1) ? pack_bf16(f.x * d89.x, f.y * d89.y) : pack_bf16(f.x * d01.x, f.y * d01.y);
-        }
-      }
-      mma16816(accL[0], ak, b[0], b[1]);
-      mma16816(accL[1], ak, b[2], b[3]);
-      if (kQ) {
-        mma16816(accQ[0], aq, b[0], b[1]);
-        mma16816(accQ[1], aq, b[2], b[3]);
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * R + (lane >> 2) + hh * 8;
-        const int i = 16 * I + nt * 8 + (lane & 3) * 2;
-        const float br = beta[r];
-        const float l0 = (i < r) ? br * accL[nt][2 * hh] : 0.f;
-        const float l1 = (i + 1 < r) ? br * accL[nt][2 * hh + 1] : 0.f;
-        *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
-        if (kQ) {
-          const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
-          const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
-          st_bf2(sm + OFF_AQK, r, i, kC, a0, a1);
-        }
-      }
-    }
-  }
-  if (kQ && tid < 6 * 32) {  // Aqk blocks above the diagonal (R < I) are zero
-    const int b = tid >> 5, w = tid & 31;
-    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
-    *reinterpret_cast<uint4 *>(sm + OFF_AQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();
-  KDA_PT(4);
-  float *Af = (float *)(U + U_AF);  // overwrites Kr (dead)
-  float *Tf = (float *)(U + U_T);   // overwrites Qr (dead)
-  if (warp < 4 && lane < 16) {
-    // diagonal block R = warp: lane i computes column i of (I + L_RR)^-1
-    const int R = warp, i = lane;
-    float a[16];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) a[m] = (m == i) ? 1.f : 0.f;
-    // column-oriented substitution: once a[m] is final, subtract its multiples
-    // from every later row (independent updates: a short dependency chain);
-    // L is read four columns at a time (one float4 per row and column group)
-#pragma unroll
-    for (int mg = 0; mg < 4; ++mg) {
-      float4 lr[16];
-#pragma unroll
-      for (int r = 4 * mg + 1; r < 16; ++r)
-        lr[r] = *reinterpret_cast<const float4 *>(Lf + fsw(16 * R + r, 16 * R + 4 * mg));
-#pragma unroll
-      for (int mm = 0; mm < 4; ++mm) {
-        const int m = 4 * mg + mm;
-#pragma unroll
-        for (int r = m + 1; r < 16; ++r) {
-          const float l = mm == 0 ? lr[r].x : mm == 1 ? lr[r].y : mm == 2 ? lr[r].z : lr[r].w;
-          a[r] = fmaf(-l, a[m], a[r]);
-        }
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < 16; ++m) Af[fsw(16 * R + m, 16 * R + i)] = a[m];
-  }
-  for (int e = tid; e < 6 * 256; e += kThr) {  // strictly-upper blocks of A
-    const int b = e >> 8, w = e & 255;
-    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2);
-    const int I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
-    Af[fsw(16 * R + (w >> 4), 16 * I + (w & 15))] = 0.f;
-  }
-  __syncthreads();
-  KDA_PT(5);
-  // Off-diagonal blocks, 32-blocked: A = [[A1, 0], [A21, A2]] with A21 = -A2 L21 A1,
-  // where A1 = [[D0, 0], [-D1 L10 D0, D1]] and A2 likewise from D2, D3 (D_R the
-  // diagonal-block inverses above).  Each thread forms 1 x 4 row segments.
-  for (int e = tid; e < 2 * 64; e += kThr) {  // T_b = L_{R,R-1} D_{R-1} for R = 1, 3
-    const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float l = Lf[fsw(16 * R + rr, 16 * (R - 1) + m)];
-      const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(16 * (R - 1) + m, 16 * (R - 1) + i4));
-      acc.x = fmaf(l, a.x, acc.x); acc.y = fmaf(l, a.y, acc.y);
-      acc.z = fmaf(l, a.z, acc.z); acc.w = fmaf(l, a.w, acc.w);
-    }
-    *reinterpret_cast<float4 *>(Tf + (b * 16 + rr) * 16 + i4) = acc;
-  }
-  __syncthreads();
-  KDA_PT(16);
-  for (int e = tid; e < 2 * 64; e += kThr) {  // A_{R,R-1} = -D_R T_b
-    const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float l = Af[fsw(16 * R + rr, 16 * R + m)];
-      const float4 t = *reinterpret_cast<const float4 *>(Tf + (b * 16 + m) * 16 + i4);
-      acc.x = fmaf(l, t.x, acc.x); acc.y = fmaf(l, t.y, acc.y);
-      acc.z = fmaf(l, t.z, acc.z); acc.w = fmaf(l, t.w, acc.w);
-    }
-    *reinterpret_cast<float4 *>(Af + fsw(16 * R + rr, 16 * (R - 1) + i4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-  }
-  __syncthreads();
-  KDA_PT(17);
-  if (tid < 128) {  // 32 x 32 products as 2 x 4 register tiles (rows rg, rg + 16) on four warps
-    const int rg = tid >> 3, c4 = (tid & 7) * 4;
-    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {  // T2 = L21 A1  (A1 lower triangular: zeros above)
-      const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(m, c4));
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float l = Lf[fsw(32 + rg + 16 * k, m)];
-        acc[k].x = fmaf(l, a.x, acc[k].x); acc[k].y = fmaf(l, a.y, acc[k].y);
-        acc[k].z = fmaf(l, a.z, acc[k].z); acc[k].w = fmaf(l, a.w, acc[k].w);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) *reinterpret_cast<float4 *>(Tf + (rg + 16 * k) * 32 + c4) = acc[k];
-  }
-  __syncthreads();
-  KDA_PT(18);
-  if (tid < 128) {
-    const int rg = tid >> 3, c4 = (tid & 7) * 4;
-    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {  // A21 = -A2 T2
-      const float4 t = *reinterpret_cast<const float4 *>(Tf + m * 32 + c4);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float l = Af[fsw(32 + rg + 16 * k, 32 + m)];
-        acc[k].x = fmaf(l, t.x, acc[k].x); acc[k].y = fmaf(l, t.y, acc[k].y);
-        acc[k].z = fmaf(l, t.z, acc[k].z); acc[k].w = fmaf(l, t.w, acc[k].w);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-      *reinterpret_cast<float4 *>(Af + fsw(32 + rg + 16 * k, c4)) = make_float4(-acc[k].x, -acc[k].y, -acc[k].z, -acc[k].w);
-  }
-  __syncthreads();
-  KDA_PT(19);
-  for (int e = tid; e < kC * kC / 8; e += kThr) {  // A -> bf16 tile, 16-byte chunks
-    const int r = e >> 3, jj = e & 7;
-    float x[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) x[t] = Af[fsw(r, jj * 8 + t)];
-    *reinterpret_cast<uint4 *>(sm + OFF_AM + sw_chunk(r, jj, kC)) = pack8(x);
-  }
-  fence_async_smem();  // the tiles may be read next by the async proxy (bulk stores)
-  __syncthreads();
-  KDA_PT(6);
 }
 
 }  // namespace tc

@@ -1,0 +1,414 @@
+// Per-chunk preparation of the bf16 chunked KDA forward (K = V = 128, chunk 64):
+// everything a chunk step needs that does not depend on v or on the carried
+// state, for every (chunk, value head) slot in parallel.
+//
+// One CTA per slot (two per SM: 92 KB of shared memory, no tensor memory):
+//  (a) chunk-local cumsum G of the log2 gate and the decay-scaled tiles;
+//  (b) the decayed Gram blocks L (strictly lower, beta-scaled) and Aqk (lower)
+//      on 16x16 warp MMAs, and A = (I + L)^-1 in fp32;
+// and writes the slot's tile record: Bk = beta k 2^G, Qg = q~ 2^G,
+// Khat = k 2^(G_last - G), Aqk and A (bf16, swizzled operand tiles) and
+// 2^G_last (fp32 [K]).  The sequential state kernel and the reverse scan load
+// the record with one bulk copy per chunk.
+//
+// These are the kkt, solve_tril and recompute_w_u steps of the FLA chunk
+// pipeline, as listed in the fla-org/flash-linear-attention commit log (PR #1294,
+// "[Fix] Use unit KDA gate scale when A_log is omitted"; PR #985, "[Test] Add
+// per-kernel torch baselines + tests for GDN kernels"): L = beta-scaled strictly
+// lower decayed K K^T, A = (I + L)^-1, w = A Bk and u = A beta v.  Here w and u
+// stay factored as A and Bk: the state kernel forms w h and u with tensor-core
+// products.
+//
+// Decay scaling.  2^(G_r - G_i) is split at the first row of each 16-token
+// block (ref): rows carry 2^(G_r - G_ref) <= 1 (tile Kr / Qr), columns carry
+// 2^(G_ref - G_i) <= 2^(15 |g|max) (tile Kc), and between blocks the per-channel
+// factor D_RI = 2^(G_ref(R) - G_ref(I)) <= 1 is applied to the column fragments
+// in registers.  Nothing overflows for gates >= -8 per token (log2 units).  The
+// chunk-level tiles Bk, Qg and Khat only underflow where the true value is
+// negligible.
+#include "tc_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace umma;
+using namespace tc;
+
+// Shared-memory map (offsets from the 1024-aligned base).  Kr and Qr are formed
+// in place of the raw k and q rows; once the Gram blocks are done, G's space
+// holds L (fp32) and the Aqk | A tiles, and Kr / Qr's hold the inverse scratch.
+constexpr uint32_t P_K = 0;          // k [64][128] bf16 -> Kr -> A (fp32 scratch)
+constexpr uint32_t P_Q = 16384;      // q [64][128] bf16 -> Qr -> T (fp32 scratch)
+constexpr uint32_t P_KC = 32768;     // Kc [64][128] bf16
+constexpr uint32_t P_G = 49152;      // g -> G fp32 [64][128] (dense rows: a TMA box) -> L fp32 [64][64]
+constexpr uint32_t P_AQK = 65536;    // Aqk [64 r][64 i] bf16 (inside G's space, after L)
+constexpr uint32_t P_AM = 73728;     // A = (I + L)^-1 [64 r][64 i] bf16
+constexpr uint32_t P_VEC = 81920;    // fp32 vectors (20 rows of 128)
+constexpr uint32_t P_BETA = 92160;   // beta [64]
+constexpr uint32_t P_MISC = 92416;   // mbarrier
+constexpr uint32_t P_SMEM = P_MISC + 16 + 1024;  // + alignment slack
+static_assert(P_AM == P_AQK + 8192 && P_AM + 8192 <= P_VEC, "Aqk | A adjacent (one bulk store)");
+static_assert(P_AQK - P_G >= 64 * 64 * 4, "L fits before Aqk");
+static_assert(65536 - (uint32_t)kTileRecA == 8192 && (uint32_t)kTileRecA - 8192 == 49152,
+              "record: Bk 0, Qg 16384, Khat 32768, Aqk 49152, A 57344, 2^G_last 65536");
+
+// fp32 [64][64] scratch (L, then A): columns XOR-swizzled by 4 * (row % 8), so
+// reads of one column across 8 rows and float4 reads of four consecutive
+// columns are both free of bank conflicts.
+__device__ __forceinline__ int fsw(int r, int c) { return r * kC + (c ^ ((r & 7) << 2)); }
+
+// Phase (a).  Needs k, q, the gate rows and beta of the chunk in shared memory;
+// writes G (in place), the vectors, the decay tiles Kr, Qr (in place of k, q)
+// and Kc, and the record's Bk, Qg, Khat tiles straight to global memory (rec).
+// Ends with a __syncthreads.
+__device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec) {
+  const int tid = threadIdx.x;
+  float *G = (float *)(sm + P_G);
+  float *vec = (float *)(sm + P_VEC);
+  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
+  {  // two threads per channel (adjacent lanes), 32 rows each
+    const int c = tid >> 1, hf = tid & 1, r0 = 32 * hf, lane = tid & 31;
+    float col[32];
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) col[k] = G[(r0 + k) * kGT + c];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      if (r0 + k < len) s += col[k];
+      col[k] = s;
+    }
+    const float lo_total = __shfl_sync(0xffffffffu, s, lane & ~1);
+    const float add = hf ? lo_total : 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      col[k] += add;
+      G[(r0 + k) * kGT + c] = col[k];
+    }
+    const float gl = __shfl_sync(0xffffffffu, s + add, lane | 1);
+    // block references: rows 0, 16 (lower partner) and 32, 48 (upper partner)
+    const float ga = (r0 < len) ? col[0] : gl, gb = (r0 + 16 < len) ? col[16] : gl;
+    float gref[4];
+    gref[0] = __shfl_sync(0xffffffffu, ga, lane & ~1);
+    gref[1] = __shfl_sync(0xffffffffu, gb, lane & ~1);
+    gref[2] = __shfl_sync(0xffffffffu, ga, lane | 1);
+    gref[3] = __shfl_sync(0xffffffffu, gb, lane | 1);
+    if (hf == 0) {
+      vec[V_GL * kD + c] = gl;
+      vec[V_GAML * kD + c] = exp2f(gl);
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {  // this partner's own two references (ga, gb)
+      const int R = 2 * hf + q;
+      const float gr = q ? gb : ga;
+      vec[(V_GREF + R) * kD + c] = gr;
+      vec[(V_EREF + R) * kD + c] = exp2f(gr);
+      vec[(V_LAM + R) * kD + c] = exp2f(gl - gr);
+    }
+    // D_RI = 2^(gref_R - gref_I) for the pairs (1,0) (2,0) (2,1) | (3,0) (3,1) (3,2)
+    if (hf == 0) {
+      vec[(V_D + 0) * kD + c] = exp2f(gref[1] - gref[0]);
+      vec[(V_D + 1) * kD + c] = exp2f(gref[2] - gref[0]);
+      vec[(V_D + 2) * kD + c] = exp2f(gref[2] - gref[1]);
+    } else {
+      vec[(V_D + 3) * kD + c] = exp2f(gref[3] - gref[0]);
+      vec[(V_D + 4) * kD + c] = exp2f(gref[3] - gref[1]);
+      vec[(V_D + 5) * kD + c] = exp2f(gref[3] - gref[2]);
+    }
+  }
+  __syncthreads();
+  KDA_PT(1);
+  // thread: 8 consecutive channels (one 16-byte chunk) of 4 consecutive rows;
+  // a half-warp covers one row, so the record stores are whole 128-byte lines
+  {
+    const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
+    float gref[8], eref[8], lam[8];
+#pragma unroll
+    for (int e = 0; e < 8; e += 4) {
+      *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (V_GREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(eref + e) = *reinterpret_cast<const float4 *>(vec + (V_EREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(lam + e) = *reinterpret_cast<const float4 *>(vec + (V_LAM + R) * kD + c0 + e);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = rg * 4 + rr;
+      const uint32_t off = sw_chunk(r, jj, kC);
+      float kv[8], qv[8], g[8], e1[8], e2[8], o[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + P_K + off), kv);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + P_Q + off), qv);
+      *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGT + c0);
+      *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + 4);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        e1[e] = exp2f(g[e] - gref[e]);  // <= 1
+        e2[e] = exp2f(gref[e] - g[e]);  // >= 1
+      }
+      const float br = beta[r];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
+      *reinterpret_cast<uint4 *>(sm + P_K + off) = pack8(o);  // Kr, in place of k
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
+      *reinterpret_cast<uint4 *>(sm + P_KC + off) = pack8(o);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * e1[e] * eref[e];
+      *reinterpret_cast<uint4 *>(rec + off) = pack8(o);  // Bk
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e] * lam[e];
+      *reinterpret_cast<uint4 *>(rec + 32768 + off) = pack8(o);  // Khat
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
+      *reinterpret_cast<uint4 *>(sm + P_Q + off) = pack8(o);  // Qr, in place of q
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] *= eref[e];
+      *reinterpret_cast<uint4 *>(rec + 16384 + off) = pack8(o);  // Qg
+    }
+  }
+  __syncthreads();
+}
+
+// Phase (b).  Needs the decay tiles of phase (a); writes the Aqk and A tiles.
+// Ends with a __syncthreads after a proxy fence (the tiles leave by bulk store).
+__device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_u32(sm);
+  const float *vec = (const float *)(sm + P_VEC);
+  float *Lf = (float *)(sm + P_G);  // G is dead
+  // Gram blocks: the 10 block pairs R >= I over the 8 warps (the A fragments of
+  // a pair serve both 8-column halves: shared-memory wavefronts bound this phase).
+  for (int p = warp; p < 10; p += 8) {
+    const int R = p >= 6 ? 3 : p >= 3 ? 2 : p >= 1 ? 1 : 0, I = p - R * (R + 1) / 2;
+    const float *Dv = (I < R) ? vec + (V_D + R * (R - 1) / 2 + I) * kD : nullptr;
+    float accL[2][4] = {}, accQ[2][4] = {};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t ak[4], aq[4], b[4];
+      {
+        const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
+        ldsm_x4(sbase + P_K + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
+        ldsm_x4(sbase + P_Q + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
+      }
+      {
+        const int mi = lane >> 3;
+        const int row = 16 * I + (lane & 7) + (mi >> 1) * 8, jj = 2 * s + (mi & 1);
+        ldsm_x4(sbase + P_KC + sw_chunk(row, jj, kC), b[0], b[1], b[2], b[3]);
+      }
+      if (Dv != nullptr) {
+        const int c0 = 16 * s + (lane & 3) * 2;
+        const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
+        const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = unpack_bf16(b[t]);
+          b[t] = (t & 1) ? pack_bf16(f.x * d89.x, f.y * d89.y) : pack_bf16(f.x * d01.x, f.y * d01.y);
+        }
+      }
+      mma16816(accL[0], ak, b[0], b[1]);
+      mma16816(accL[1], ak, b[2], b[3]);
+      mma16816(accQ[0], aq, b[0], b[1]);
+      mma16816(accQ[1], aq, b[2], b[3]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * R + (lane >> 2) + hh * 8;
+        const int i = 16 * I + nt * 8 + (lane & 3) * 2;
+        const float br = beta[r];
+        const float l0 = (i < r) ? br * accL[nt][2 * hh] : 0.f;
+        const float l1 = (i + 1 < r) ? br * accL[nt][2 * hh + 1] : 0.f;
+        *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
+        const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
+        const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
+        st_bf2(sm + P_AQK, r, i, kC, a0, a1);
+      }
+    }
+  }
+  if (tid < 6 * 32) {  // Aqk blocks above the diagonal (R < I) are zero
+    const int b = tid >> 5, w = tid & 31;
+    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
+    *reinterpret_cast<uint4 *>(sm + P_AQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  KDA_PT(4);
+  float *Af = (float *)(sm + P_K);  // overwrites Kr (dead)
+  float *Tf = (float *)(sm + P_Q);  // overwrites Qr (dead)
+  if (warp < 4 && lane < 16) {
+    // diagonal block R = warp: lane i computes column i of (I + L_RR)^-1
+    const int R = warp, i = lane;
+    float a[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) a[m] = (m == i) ? 1.f : 0.f;
+    // column-oriented substitution: once a[m] is final, subtract its multiples
+    // from every later row (independent updates: a short dependency chain);
+    // L is read four columns at a time (one float4 per row and column group)
+#pragma unroll
+    for (int mg = 0; mg < 4; ++mg) {
+      float4 lr[16];
+#pragma unroll
+      for (int r = 4 * mg + 1; r < 16; ++r)
+        lr[r] = *reinterpret_cast<const float4 *>(Lf + fsw(16 * R + r, 16 * R + 4 * mg));
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm) {
+        const int m = 4 * mg + mm;
+#pragma unroll
+        for (int r = m + 1; r < 16; ++r) {
+          const float l = mm == 0 ? lr[r].x : mm == 1 ? lr[r].y : mm == 2 ? lr[r].z : lr[r].w;
+          a[r] = fmaf(-l, a[m], a[r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) Af[fsw(16 * R + m, 16 * R + i)] = a[m];
+  }
+  for (int e = tid; e < 6 * 256; e += kThr) {  // strictly-upper blocks of A
+    const int b = e >> 8, w = e & 255;
+    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2);
+    const int I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
+    Af[fsw(16 * R + (w >> 4), 16 * I + (w & 15))] = 0.f;
+  }
+  __syncthreads();
+  KDA_PT(5);
+  // Off-diagonal blocks, 32-blocked: A = [[A1, 0], [A21, A2]] with A21 = -A2 L21 A1,
+  // where A1 = [[D0, 0], [-D1 L10 D0, D1]] and A2 likewise from D2, D3 (D_R the
+  // diagonal-block inverses above).  Each thread forms 1 x 4 row segments.
+  for (int e = tid; e < 2 * 64; e += kThr) {  // T_b = L_{R,R-1} D_{R-1} for R = 1, 3
+    const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float l = Lf[fsw(16 * R + rr, 16 * (R - 1) + m)];
+      const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(16 * (R - 1) + m, 16 * (R - 1) + i4));
+      acc.x = fmaf(l, a.x, acc.x); acc.y = fmaf(l, a.y, acc.y);
+      acc.z = fmaf(l, a.z, acc.z); acc.w = fmaf(l, a.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(Tf + (b * 16 + rr) * 16 + i4) = acc;
+  }
+  __syncthreads();
+  KDA_PT(6);
+  for (int e = tid; e < 2 * 64; e += kThr) {  // A_{R,R-1} = -D_R T_b
+    const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float l = Af[fsw(16 * R + rr, 16 * R + m)];
+      const float4 t = *reinterpret_cast<const float4 *>(Tf + (b * 16 + m) * 16 + i4);
+      acc.x = fmaf(l, t.x, acc.x); acc.y = fmaf(l, t.y, acc.y);
+      acc.z = fmaf(l, t.z, acc.z); acc.w = fmaf(l, t.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(Af + fsw(16 * R + rr, 16 * (R - 1) + i4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+  KDA_PT(7);
+  if (tid < 128) {  // 32 x 32 products as 2 x 4 register tiles (rows rg, rg + 16) on four warps
+    const int rg = tid >> 3, c4 = (tid & 7) * 4;
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {  // T2 = L21 A1  (A1 lower triangular: zeros above)
+      const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(m, c4));
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float l = Lf[fsw(32 + rg + 16 * k, m)];
+        acc[k].x = fmaf(l, a.x, acc[k].x); acc[k].y = fmaf(l, a.y, acc[k].y);
+        acc[k].z = fmaf(l, a.z, acc[k].z); acc[k].w = fmaf(l, a.w, acc[k].w);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) *reinterpret_cast<float4 *>(Tf + (rg + 16 * k) * 32 + c4) = acc[k];
+  }
+  __syncthreads();
+  KDA_PT(8);
+  if (tid < 128) {
+    const int rg = tid >> 3, c4 = (tid & 7) * 4;
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {  // A21 = -A2 T2
+      const float4 t = *reinterpret_cast<const float4 *>(Tf + m * 32 + c4);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float l = Af[fsw(32 + rg + 16 * k, 32 + m)];
+        acc[k].x = fmaf(l, t.x, acc[k].x); acc[k].y = fmaf(l, t.y, acc[k].y);
+        acc[k].z = fmaf(l, t.z, acc[k].z); acc[k].w = fmaf(l, t.w, acc[k].w);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      *reinterpret_cast<float4 *>(Af + fsw(32 + rg + 16 * k, c4)) = make_float4(-acc[k].x, -acc[k].y, -acc[k].z, -acc[k].w);
+  }
+  __syncthreads();
+  KDA_PT(9);
+  for (int e = tid; e < kC * kC / 8; e += kThr) {  // A -> bf16 tile, 16-byte chunks
+    const int r = e >> 3, jj = e & 7;
+    float x[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) x[t] = Af[fsw(r, jj * 8 + t)];
+    *reinterpret_cast<uint4 *>(sm + P_AM + sw_chunk(r, jj, kC)) = pack8(x);
+  }
+  fence_async_smem();  // Aqk, A and 2^G_last leave by bulk store
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThr, 2)
+kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps) {
+  extern __shared__ unsigned char smraw[];
+  unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(sm);
+  const int c_idx = blockIdx.x, j = blockIdx.y;
+  const int4 ch = W.chunk[c_idx];
+  if (ch.x < 0) return;  // unused chunk slot
+  const int t0 = ch.y, len = ch.z;
+  const int HV = P.HV, h = j / (HV / P.H);
+  const int tid = threadIdx.x;
+  const size_t slot = (size_t)c_idx * HV + j;
+  float *beta = (float *)(sm + P_BETA);
+  uint64_t *bar = (uint64_t *)(sm + P_MISC);
+  KDA_PT_DECL;
+
+  if (tid == 0) {
+    bar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (tid == 0) {  // k, q rows and the gate rows (TMA); rows past the tensor end arrive as zeros
+    mbar_expect_tx(bar, 32768u + 32768u);
+    tma_tile(sbase + P_K, &maps.k, h, t0, bar);
+    tma_tile(sbase + P_Q, &maps.q, h, t0, bar);
+    tma_load3(sbase + P_G, &maps.g, 0, j, t0, bar);
+  }
+  load_beta(P, beta, t0, len, j);
+  cp_commit();
+  cp_wait_all();
+  bar_wait(bar, 0, err);
+  if (len < kC) {  // rows past the sequence end hold the next tokens: clear them
+    zero_tail(sm + P_K, len);
+    zero_tail(sm + P_Q, len);
+  }
+  __syncthreads();
+  KDA_PT(0);
+
+  unsigned char *rec = W.tc_tiles + slot * kTileRecord;
+  phase_a(sm, len, beta, rec);
+  KDA_PT(2);
+  phase_b(sm, beta);
+  if (tid == 0) {  // Aqk | A (adjacent) and 2^G_last
+    bulk_store(rec + kTileRecA - 8192, sbase + P_AQK, 16384u);
+    bulk_store(rec + 65536, sbase + P_VEC + (uint32_t)(V_GAML * kD * 4), 512u);
+    bulk_commit();
+    bulk_wait_all();  // complete before the CTA exits
+  }
+  KDA_PT(10);
+  KDA_PT_FLUSH;
+}
+
+}  // namespace
+
+KDA_PT_EXPORT(kda_debug_prep_phase_cycles)
+
+cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps, int *err, cudaStream_t s) {
+  if (P.NC == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kda_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+  if (e != cudaSuccess) return e;
+  KDA_LAUNCH("kda_prep_tc", s, kda_prep_tc_kernel<<<dim3(P.NC, P.HV), kThr, P_SMEM, s>>>(P, W, err, maps));
+  return cudaGetLastError();
+}
+
+}  // namespace kda
