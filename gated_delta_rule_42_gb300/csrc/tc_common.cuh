@@ -181,6 +181,10 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // The calling thread's bulk stores have read their shared-memory sources.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// All but the most recent of the calling thread's bulk store groups have read their sources.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
+}
 // The calling thread's bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 // Box (c0, c1, c2) of a 3-D tensor map into shared memory; completion counted on bar.

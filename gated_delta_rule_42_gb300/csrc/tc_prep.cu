@@ -393,7 +393,7 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
     bulk_store(rec + kTileRecA - 8192, sbase + P_AQK, 16384u);
     bulk_store(rec + 65536, sbase + P_VEC + (uint32_t)(V_GAML * kD * 4), 512u);
     bulk_commit();
-    bulk_wait_all();  // complete before the CTA exits
+    bulk_wait_read();  // the sources stay valid until read; the writes complete with the grid
   }
   KDA_PT(10);
   KDA_PT_FLUSH;
