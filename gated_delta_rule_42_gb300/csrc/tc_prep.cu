@@ -36,21 +36,19 @@ using namespace tc;
 
 // Shared-memory map (offsets from the 1024-aligned base).  Kr and Qr are formed
 // in place of the raw k and q rows; once the Gram blocks are done, G's space
-// holds L (fp32) and the Aqk | A tiles, and Kr / Qr's hold the inverse scratch.
+// holds L (fp32) and Kr / Qr's hold the inverse scratch.  Every record tile is
+// written straight to global memory, so nothing is left to copy out at the end.
 constexpr uint32_t P_K = 0;          // k [64][128] bf16 -> Kr -> A (fp32 scratch)
 constexpr uint32_t P_Q = 16384;      // q [64][128] bf16 -> Qr -> T (fp32 scratch)
 constexpr uint32_t P_KC = 32768;     // Kc [64][128] bf16
 constexpr uint32_t P_G = 49152;      // g -> G fp32 [64][128] (dense rows: a TMA box) -> L fp32 [64][64]
-constexpr uint32_t P_AQK = 65536;    // Aqk [64 r][64 i] bf16 (inside G's space, after L)
-constexpr uint32_t P_AM = 73728;     // A = (I + L)^-1 [64 r][64 i] bf16
 constexpr uint32_t P_VEC = 81920;    // fp32 vectors (20 rows of 128)
 constexpr uint32_t P_BETA = 92160;   // beta [64]
 constexpr uint32_t P_MISC = 92416;   // mbarrier
 constexpr uint32_t P_SMEM = P_MISC + 16 + 1024;  // + alignment slack
-static_assert(P_AM == P_AQK + 8192 && P_AM + 8192 <= P_VEC, "Aqk | A adjacent (one bulk store)");
-static_assert(P_AQK - P_G >= 64 * 64 * 4, "L fits before Aqk");
-static_assert(65536 - (uint32_t)kTileRecA == 8192 && (uint32_t)kTileRecA - 8192 == 49152,
-              "record: Bk 0, Qg 16384, Khat 32768, Aqk 49152, A 57344, 2^G_last 65536");
+// record layout: Bk 0, Qg 16384, Khat 32768, Aqk 49152, A 57344, 2^G_last 65536
+constexpr uint32_t REC_QG = 16384, REC_KH = 32768, REC_AQK = 49152, REC_AM = 57344, REC_GAML = 65536;
+static_assert(REC_AM == (uint32_t)kTileRecA && REC_GAML + 512 == (uint32_t)kTileRecord, "record layout");
 
 // fp32 [64][64] scratch (L, then A): columns XOR-swizzled by 4 * (row % 8), so
 // reads of one column across 8 rows and float4 reads of four consecutive
@@ -59,61 +57,42 @@ __device__ __forceinline__ int fsw(int r, int c) { return r * kC + (c ^ ((r & 7)
 
 // Phase (a).  Needs k, q, the gate rows and beta of the chunk in shared memory;
 // writes G (in place), the vectors, the decay tiles Kr, Qr (in place of k, q)
-// and Kc, and the record's Bk, Qg, Khat tiles straight to global memory (rec).
-// Ends with a __syncthreads.
+// and Kc, and the record's Bk, Qg, Khat tiles and 2^G_last straight to global
+// memory (rec).  Ends with a __syncthreads.
 __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec) {
   const int tid = threadIdx.x;
   float *G = (float *)(sm + P_G);
   float *vec = (float *)(sm + P_VEC);
   constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
-  {  // two threads per channel (adjacent lanes), 32 rows each
-    const int c = tid >> 1, hf = tid & 1, r0 = 32 * hf, lane = tid & 31;
-    float col[32];
+  if (tid < kD) {  // one thread per channel (a warp reads 32 consecutive channels: no bank conflicts)
+    const int c = tid;
+    float col[kC];
     float s = 0.f;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) col[k] = G[(r0 + k) * kGT + c];
+    for (int r = 0; r < kC; ++r) col[r] = G[r * kGT + c];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      if (r0 + k < len) s += col[k];
-      col[k] = s;
+    for (int r = 0; r < kC; ++r) {
+      if (r < len) s += col[r];
+      col[r] = s;
     }
-    const float lo_total = __shfl_sync(0xffffffffu, s, lane & ~1);
-    const float add = hf ? lo_total : 0.f;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      col[k] += add;
-      G[(r0 + k) * kGT + c] = col[k];
-    }
-    const float gl = __shfl_sync(0xffffffffu, s + add, lane | 1);
-    // block references: rows 0, 16 (lower partner) and 32, 48 (upper partner)
-    const float ga = (r0 < len) ? col[0] : gl, gb = (r0 + 16 < len) ? col[16] : gl;
+    for (int r = 0; r < kC; ++r) G[r * kGT + c] = col[r];
+    const float gl = s;
+    reinterpret_cast<float *>(rec + REC_GAML)[c] = exp2f(gl);
     float gref[4];
-    gref[0] = __shfl_sync(0xffffffffu, ga, lane & ~1);
-    gref[1] = __shfl_sync(0xffffffffu, gb, lane & ~1);
-    gref[2] = __shfl_sync(0xffffffffu, ga, lane | 1);
-    gref[3] = __shfl_sync(0xffffffffu, gb, lane | 1);
-    if (hf == 0) {
-      vec[V_GL * kD + c] = gl;
-      vec[V_GAML * kD + c] = exp2f(gl);
-    }
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {  // this partner's own two references (ga, gb)
-      const int R = 2 * hf + q;
-      const float gr = q ? gb : ga;
-      vec[(V_GREF + R) * kD + c] = gr;
-      vec[(V_EREF + R) * kD + c] = exp2f(gr);
-      vec[(V_LAM + R) * kD + c] = exp2f(gl - gr);
+    for (int R = 0; R < 4; ++R) {  // block references: rows 0, 16, 32, 48 (the chunk end past len)
+      gref[R] = (16 * R < len) ? col[16 * R] : gl;
+      vec[(V_GREF + R) * kD + c] = gref[R];
+      vec[(V_EREF + R) * kD + c] = exp2f(gref[R]);
+      vec[(V_LAM + R) * kD + c] = exp2f(gl - gref[R]);
     }
-    // D_RI = 2^(gref_R - gref_I) for the pairs (1,0) (2,0) (2,1) | (3,0) (3,1) (3,2)
-    if (hf == 0) {
-      vec[(V_D + 0) * kD + c] = exp2f(gref[1] - gref[0]);
-      vec[(V_D + 1) * kD + c] = exp2f(gref[2] - gref[0]);
-      vec[(V_D + 2) * kD + c] = exp2f(gref[2] - gref[1]);
-    } else {
-      vec[(V_D + 3) * kD + c] = exp2f(gref[3] - gref[0]);
-      vec[(V_D + 4) * kD + c] = exp2f(gref[3] - gref[1]);
-      vec[(V_D + 5) * kD + c] = exp2f(gref[3] - gref[2]);
-    }
+    // D_RI = 2^(gref_R - gref_I) for the pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+    int p = 0;
+#pragma unroll
+    for (int R = 1; R < 4; ++R)
+#pragma unroll
+      for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
   }
   __syncthreads();
   KDA_PT(1);
@@ -154,21 +133,21 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       *reinterpret_cast<uint4 *>(rec + off) = pack8(o);  // Bk
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e] * lam[e];
-      *reinterpret_cast<uint4 *>(rec + 32768 + off) = pack8(o);  // Khat
+      *reinterpret_cast<uint4 *>(rec + REC_KH + off) = pack8(o);  // Khat
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
       *reinterpret_cast<uint4 *>(sm + P_Q + off) = pack8(o);  // Qr, in place of q
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] *= eref[e];
-      *reinterpret_cast<uint4 *>(rec + 16384 + off) = pack8(o);  // Qg
+      *reinterpret_cast<uint4 *>(rec + REC_QG + off) = pack8(o);  // Qg
     }
   }
   __syncthreads();
 }
 
-// Phase (b).  Needs the decay tiles of phase (a); writes the Aqk and A tiles.
-// Ends with a __syncthreads after a proxy fence (the tiles leave by bulk store).
-__device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
+// Phase (b).  Needs the decay tiles of phase (a); writes the record's Aqk and A
+// tiles straight to global memory (rec).
+__device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, unsigned char *rec) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(sm);
   const float *vec = (const float *)(sm + P_VEC);
@@ -219,14 +198,14 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
         *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
         const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
         const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
-        st_bf2(sm + P_AQK, r, i, kC, a0, a1);
+        *reinterpret_cast<uint32_t *>(rec + REC_AQK + sw_off(r, i, kC)) = pack_bf16(a0, a1);
       }
     }
   }
   if (tid < 6 * 32) {  // Aqk blocks above the diagonal (R < I) are zero
     const int b = tid >> 5, w = tid & 31;
     const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
-    *reinterpret_cast<uint4 *>(sm + P_AQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4 *>(rec + REC_AQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   KDA_PT(4);
@@ -341,10 +320,8 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta) {
     float x[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) x[t] = Af[fsw(r, jj * 8 + t)];
-    *reinterpret_cast<uint4 *>(sm + P_AM + sw_chunk(r, jj, kC)) = pack8(x);
+    *reinterpret_cast<uint4 *>(rec + REC_AM + sw_chunk(r, jj, kC)) = pack8(x);
   }
-  fence_async_smem();  // Aqk, A and 2^G_last leave by bulk store
-  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThr, 2)
@@ -388,13 +365,7 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
   unsigned char *rec = W.tc_tiles + slot * kTileRecord;
   phase_a(sm, len, beta, rec);
   KDA_PT(2);
-  phase_b(sm, beta);
-  if (tid == 0) {  // Aqk | A (adjacent) and 2^G_last
-    bulk_store(rec + kTileRecA - 8192, sbase + P_AQK, 16384u);
-    bulk_store(rec + 65536, sbase + P_VEC + (uint32_t)(V_GAML * kD * 4), 512u);
-    bulk_commit();
-    bulk_wait_read();  // the sources stay valid until read; the writes complete with the grid
-  }
+  phase_b(sm, beta, rec);
   KDA_PT(10);
   KDA_PT_FLUSH;
 }
