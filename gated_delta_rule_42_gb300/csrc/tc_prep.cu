@@ -2,7 +2,7 @@
 // everything a chunk step needs that does not depend on v or on the carried
 // state, for every (chunk, value head) slot in parallel.
 //
-// One CTA per slot (two per SM: 92 KB of shared memory, no tensor memory):
+// One CTA per slot (three per SM: 75 KB of shared memory, no tensor memory):
 //  (a) chunk-local cumsum G of the log2 gate and the decay-scaled tiles;
 //  (b) the decayed Gram blocks L (strictly lower, beta-scaled) and Aqk (lower)
 //      on 16x16 warp MMAs, and A = (I + L)^-1 in fp32;
@@ -35,17 +35,22 @@ using namespace umma;
 using namespace tc;
 
 // Shared-memory map (offsets from the 1024-aligned base).  Kr and Qr are formed
-// in place of the raw k and q rows; once the Gram blocks are done, G's space
-// holds L (fp32) and Kr / Qr's hold the inverse scratch.  Every record tile is
-// written straight to global memory, so nothing is left to copy out at the end.
+// in place of the raw k and q rows; once every thread has read its G values,
+// G's space holds Kc and then L (fp32); once the Gram blocks are done, Kr / Qr's
+// hold the inverse scratch.  Every record tile is written straight to global
+// memory, so nothing is left to copy out at the end.
 constexpr uint32_t P_K = 0;          // k [64][128] bf16 -> Kr -> A (fp32 scratch)
 constexpr uint32_t P_Q = 16384;      // q [64][128] bf16 -> Qr -> T (fp32 scratch)
-constexpr uint32_t P_KC = 32768;     // Kc [64][128] bf16
-constexpr uint32_t P_G = 49152;      // g -> G fp32 [64][128] (dense rows: a TMA box) -> L fp32 [64][64]
-constexpr uint32_t P_VEC = 81920;    // fp32 vectors (20 rows of 128)
-constexpr uint32_t P_BETA = 92160;   // beta [64]
-constexpr uint32_t P_MISC = 92416;   // mbarrier
+constexpr uint32_t P_G = 32768;      // g -> G fp32 [64][128] (dense rows: a TMA box) -> L fp32 [64][64] | Kc
+constexpr uint32_t P_KC = 49152;     // Kc [64][128] bf16 (the upper half of G's space)
+constexpr uint32_t P_VEC = 65536;    // fp32 vectors: 18 rows of 128
+constexpr uint32_t P_BETA = 74752;   // beta [64]
+constexpr uint32_t P_MISC = 75008;   // mbarrier
 constexpr uint32_t P_SMEM = P_MISC + 16 + 1024;  // + alignment slack
+static_assert(P_SMEM + 1024 <= 233472 / 3, "three CTAs per SM (228 KB, 1 KB reserved per CTA)");
+// vector rows: block references G_ref(R), 2^G_ref(R), 2^(G_last - G_ref(R)), and
+// the block-pair factors D_RI = 2^(G_ref(R) - G_ref(I)) for R > I
+constexpr int W_GREF = 0, W_EREF = 4, W_LAM = 8, W_D = 12;
 // record layout: Bk 0, Qg 16384, Khat 32768, Aqk 49152, A 57344, 2^G_last 65536
 constexpr uint32_t REC_QG = 16384, REC_KH = 32768, REC_AQK = 49152, REC_AM = 57344, REC_GAML = 65536;
 static_assert(REC_AM == (uint32_t)kTileRecA && REC_GAML + 512 == (uint32_t)kTileRecord, "record layout");
@@ -83,16 +88,16 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
 #pragma unroll
     for (int R = 0; R < 4; ++R) {  // block references: rows 0, 16, 32, 48 (the chunk end past len)
       gref[R] = (16 * R < len) ? col[16 * R] : gl;
-      vec[(V_GREF + R) * kD + c] = gref[R];
-      vec[(V_EREF + R) * kD + c] = exp2f(gref[R]);
-      vec[(V_LAM + R) * kD + c] = exp2f(gl - gref[R]);
+      vec[(W_GREF + R) * kD + c] = gref[R];
+      vec[(W_EREF + R) * kD + c] = exp2f(gref[R]);
+      vec[(W_LAM + R) * kD + c] = exp2f(gl - gref[R]);
     }
     // D_RI = 2^(gref_R - gref_I) for the pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
     int p = 0;
 #pragma unroll
     for (int R = 1; R < 4; ++R)
 #pragma unroll
-      for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
+      for (int I = 0; I < R; ++I) vec[(W_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
   }
   __syncthreads();
   KDA_PT(1);
@@ -101,11 +106,12 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
   {
     const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
     float gref[8], eref[8], lam[8];
+    uint4 kc[4];  // Kc rows, written once every thread has read its G values
 #pragma unroll
     for (int e = 0; e < 8; e += 4) {
-      *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (V_GREF + R) * kD + c0 + e);
-      *reinterpret_cast<float4 *>(eref + e) = *reinterpret_cast<const float4 *>(vec + (V_EREF + R) * kD + c0 + e);
-      *reinterpret_cast<float4 *>(lam + e) = *reinterpret_cast<const float4 *>(vec + (V_LAM + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (W_GREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(eref + e) = *reinterpret_cast<const float4 *>(vec + (W_EREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(lam + e) = *reinterpret_cast<const float4 *>(vec + (W_LAM + R) * kD + c0 + e);
     }
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
@@ -127,7 +133,7 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       *reinterpret_cast<uint4 *>(sm + P_K + off) = pack8(o);  // Kr, in place of k
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
-      *reinterpret_cast<uint4 *>(sm + P_KC + off) = pack8(o);
+      kc[rr] = pack8(o);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * e1[e] * eref[e];
       *reinterpret_cast<uint4 *>(rec + off) = pack8(o);  // Bk
@@ -141,6 +147,9 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       for (int e = 0; e < 8; ++e) o[e] *= eref[e];
       *reinterpret_cast<uint4 *>(rec + REC_QG + off) = pack8(o);  // Qg
     }
+    __syncthreads();  // G is dead: its upper half takes Kc
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) *reinterpret_cast<uint4 *>(sm + P_KC + sw_chunk(rg * 4 + rr, jj, kC)) = kc[rr];
   }
   __syncthreads();
 }
@@ -156,7 +165,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, un
   // a pair serve both 8-column halves: shared-memory wavefronts bound this phase).
   for (int p = warp; p < 10; p += 8) {
     const int R = p >= 6 ? 3 : p >= 3 ? 2 : p >= 1 ? 1 : 0, I = p - R * (R + 1) / 2;
-    const float *Dv = (I < R) ? vec + (V_D + R * (R - 1) / 2 + I) * kD : nullptr;
+    const float *Dv = (I < R) ? vec + (W_D + R * (R - 1) / 2 + I) * kD : nullptr;
     float accL[2][4] = {}, accQ[2][4] = {};
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -219,21 +228,18 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, un
     for (int m = 0; m < 16; ++m) a[m] = (m == i) ? 1.f : 0.f;
     // column-oriented substitution: once a[m] is final, subtract its multiples
     // from every later row (independent updates: a short dependency chain);
-    // L is read four columns at a time (one float4 per row and column group)
+    // L is read two columns at a time (one float2 per row and column pair)
 #pragma unroll
-    for (int mg = 0; mg < 4; ++mg) {
-      float4 lr[16];
+    for (int mg = 0; mg < 8; ++mg) {
+      float2 lr[16];
 #pragma unroll
-      for (int r = 4 * mg + 1; r < 16; ++r)
-        lr[r] = *reinterpret_cast<const float4 *>(Lf + fsw(16 * R + r, 16 * R + 4 * mg));
+      for (int r = 2 * mg + 1; r < 16; ++r)
+        lr[r] = *reinterpret_cast<const float2 *>(Lf + fsw(16 * R + r, 16 * R + 2 * mg));
 #pragma unroll
-      for (int mm = 0; mm < 4; ++mm) {
-        const int m = 4 * mg + mm;
+      for (int mm = 0; mm < 2; ++mm) {
+        const int m = 2 * mg + mm;
 #pragma unroll
-        for (int r = m + 1; r < 16; ++r) {
-          const float l = mm == 0 ? lr[r].x : mm == 1 ? lr[r].y : mm == 2 ? lr[r].z : lr[r].w;
-          a[r] = fmaf(-l, a[m], a[r]);
-        }
+        for (int r = m + 1; r < 16; ++r) a[r] = fmaf(-(mm == 0 ? lr[r].x : lr[r].y), a[m], a[r]);
       }
     }
 #pragma unroll
@@ -324,7 +330,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, un
   }
 }
 
-__global__ void __launch_bounds__(kThr, 2)
+__global__ void __launch_bounds__(kThr, 3)
 kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
