@@ -85,8 +85,37 @@ def _offsets(B, T, cu_seqlens):
     return np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
 
 
-def kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, output_final_state=True, nthreads=0):
-    """Token-by-token KDA forward.  Returns (o [B,T,HV,V], hT [N,HV,K,V] or None)."""
+# The q/k L2-norm prologue.  The KDA layer of "kda in torchtitan (training)"
+# (pytorch/torchtitan PR #4164) imports an attention-gym `l2norm` next to
+# `recurrent_kda`; the pages print neither its formula nor its epsilon.  Reading:
+# each (token, head) row of q and of k is divided by sqrt(sum of its squares +
+# eps) over the head dimension, with eps = 1e-6, before the 1/sqrt(K) query
+# scale; gradients are taken w.r.t. the raw rows.
+L2NORM_EPS = 1e-6
+
+
+def l2norm_rows(x, eps=L2NORM_EPS):
+    """y = x / sqrt(sum_c x_c^2 + eps) over the last axis."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def l2norm_rows_bwd(x, dy, eps=L2NORM_EPS):
+    """Gradient of :func:`l2norm_rows` w.r.t. x given dy: with r = (sum x^2 +
+    eps)^(-1/2) and y = x r, dx = r (dy - y (y . dy))."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+    y = x * r
+    return r * (dy - y * np.sum(y * dy, axis=-1, keepdims=True))
+
+
+def kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, output_final_state=True, nthreads=0,
+            qk_l2norm=False):
+    """Token-by-token KDA forward.  Returns (o [B,T,HV,V], hT [N,HV,K,V] or None).
+    With qk_l2norm, q and k rows are normalised first (:func:`l2norm_rows`)."""
+    if qk_l2norm:
+        q, k = l2norm_rows(q), l2norm_rows(k)
     lib = _load()
     q, k, v, g, beta, h0 = map(_c64, (q, k, v, g, beta, h0))
     B, T, H, K = q.shape
@@ -102,8 +131,15 @@ def kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, output_final_state=True,
     return o, hT
 
 
-def kda_bwd(q, k, v, g, beta, h0, do, dhT, cu_seqlens=None, nthreads=0):
-    """Token-by-token KDA backward.  Returns dict dq, dk, dv, dg, dbeta, dh0."""
+def kda_bwd(q, k, v, g, beta, h0, do, dhT, cu_seqlens=None, nthreads=0, qk_l2norm=False):
+    """Token-by-token KDA backward.  Returns dict dq, dk, dv, dg, dbeta, dh0.
+    With qk_l2norm, the gradients of the normalised rows are carried back
+    through :func:`l2norm_rows` to the raw q and k."""
+    if qk_l2norm:
+        out = kda_bwd(l2norm_rows(q), l2norm_rows(k), v, g, beta, h0, do, dhT, cu_seqlens, nthreads)
+        out["dq"] = l2norm_rows_bwd(q, out["dq"])
+        out["dk"] = l2norm_rows_bwd(k, out["dk"])
+        return out
     lib = _load()
     q, k, v, g, beta, h0, do, dhT = map(_c64, (q, k, v, g, beta, h0, do, dhT))
     B, T, H, K = q.shape

@@ -1,11 +1,13 @@
 """The oracle's pins must catch plausible mistakes.  Each case plants one
-mistake in a copy of the C oracle (on the CPU), loads it in place of the real
-one and runs the pins; at least one pin must fail."""
+mistake in a copy of the C oracle (on the CPU) and loads it in place of the
+real one, or, for the numpy q/k L2-norm prologue, replaces one of the oracle's
+functions; then it runs the pins, and at least one pin must fail."""
 import ctypes
 import os
 import subprocess
 import tempfile
 
+import numpy as np
 import pytest
 
 import oracle
@@ -74,3 +76,46 @@ def test_pins_catch_planted_mistake(name, find, repl, monkeypatch):
             except AssertionError:
                 caught.append(pin.__name__)
         assert caught, f"no pin caught mutant {name}"
+
+
+# The q/k L2-norm prologue lives in numpy: its planted mistakes replace the
+# oracle's functions in place, and the prologue pins must catch each one.
+def _bwd_no_projection(x, dy, eps=oracle.L2NORM_EPS):
+    x, dy = np.asarray(x, np.float64), np.asarray(dy, np.float64)
+    return dy / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def _bwd_projection_sign(x, dy, eps=oracle.L2NORM_EPS):
+    x, dy = np.asarray(x, np.float64), np.asarray(dy, np.float64)
+    r = 1.0 / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+    y = x * r
+    return r * (dy + y * np.sum(y * dy, axis=-1, keepdims=True))
+
+
+def _fwd_wrong_axis(x, eps=oracle.L2NORM_EPS):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=0, keepdims=True) + eps)
+
+
+def _fwd_no_sqrt(x, eps=oracle.L2NORM_EPS):
+    x = np.asarray(x, np.float64)
+    return x / (np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+L2_MUTANTS = [("l2norm_rows_bwd", _bwd_no_projection), ("l2norm_rows_bwd", _bwd_projection_sign),
+              ("l2norm_rows", _fwd_wrong_axis), ("l2norm_rows", _fwd_no_sqrt)]
+L2_PINS = [pins.test_l2norm_rows_unit_norm_scale_invariance_and_eps,
+           pins.test_l2norm_backward_finite_differences_and_orthogonality,
+           pins.test_qk_l2norm_kda_scale_invariance_and_finite_differences]
+
+
+@pytest.mark.parametrize("attr,fn", L2_MUTANTS, ids=[m[1].__name__ for m in L2_MUTANTS])
+def test_l2norm_pins_catch_planted_mistake(attr, fn, monkeypatch):
+    monkeypatch.setattr(oracle, attr, fn)
+    caught = []
+    for pin in L2_PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught {fn.__name__}"

@@ -273,3 +273,85 @@ def test_rel_rms_definition():
     assert abs(oracle.rel_rms([3.0, 5.0], [3.0, 4.0]) - 0.2) < 1e-15
     assert oracle.rel_rms([0.0], [0.0]) == 0.0
     assert oracle.rel_rms([1e-30], [0.0]) == float("inf")
+
+
+# ---- the q/k L2-norm prologue ----
+
+def test_l2norm_rows_unit_norm_scale_invariance_and_eps():
+    """Rows come out with norm sqrt(s / (s + eps)) (s = the row's sum of
+    squares): exactly 1 at eps = 0, where positive row scales drop out."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((2, 5, 3, 7))
+    y0 = oracle.l2norm_rows(x, eps=0.0)
+    np.testing.assert_allclose(np.sqrt(np.sum(y0 * y0, axis=-1)), 1.0, rtol=0, atol=1e-15)
+    c = np.exp(rng.standard_normal((2, 5, 3, 1)))
+    np.testing.assert_allclose(oracle.l2norm_rows(c * x, eps=0.0), y0, rtol=1e-14, atol=1e-15)
+    s = np.sum(x * x, axis=-1)
+    y = oracle.l2norm_rows(x)
+    np.testing.assert_allclose(np.sum(y * y, axis=-1), s / (s + oracle.L2NORM_EPS), rtol=1e-14)
+    assert np.all(oracle.l2norm_rows(np.zeros((1, 4))) == 0.0)  # zero rows stay zero
+
+
+def test_l2norm_backward_finite_differences_and_orthogonality():
+    """Central differences of <W, l2norm_rows(x)>; and x . dx = r (x . dy) eps / (s + eps):
+    at eps = 0 the gradient is orthogonal to its row."""
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((3, 6))
+    W = rng.standard_normal((3, 6))
+    gr = oracle.l2norm_rows_bwd(x, W)
+    fd = np.zeros_like(x)
+    h = 1e-6
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = (np.sum(W * oracle.l2norm_rows(xp)) - np.sum(W * oracle.l2norm_rows(xm))) / (2 * h)
+    assert np.max(np.abs(fd - gr)) < 1e-8
+    g0 = oracle.l2norm_rows_bwd(x, W, eps=0.0)
+    np.testing.assert_allclose(np.sum(x * g0, axis=-1), 0.0, atol=1e-14)
+    s = np.sum(x * x, axis=-1)
+    r = 1.0 / np.sqrt(s + oracle.L2NORM_EPS)
+    np.testing.assert_allclose(np.sum(x * gr, axis=-1),
+                               r * np.sum(x * W, axis=-1) * oracle.L2NORM_EPS / (s + oracle.L2NORM_EPS),
+                               rtol=0, atol=1e-14)
+
+
+def test_qk_l2norm_kda_scale_invariance_and_finite_differences():
+    """With the prologue, positive per-row scales of q and k leave o and hT
+    unchanged (up to the eps effect); dq, dk match central differences of the
+    whole layer, GVA with an empty slot."""
+    rng = np.random.default_rng(23)
+    T, H, HV, K, V = 6, 1, 2, 3, 2
+    q, k, v, g, beta = rand_problem(rng, 1, T, H, HV, K, V)
+    k = k * np.exp(rng.standard_normal((1, T, H, 1)))  # rows of any norm
+    cu = [0, 2, 2, 6]
+    N = 3
+    h0 = rng.standard_normal((N, HV, K, V))
+    o1, h1 = oracle.kda_fwd(q, k, v, g, beta, h0, cu, nthreads=1, qk_l2norm=True)
+    cq = np.exp(rng.standard_normal((1, T, H, 1)))
+    ck = np.exp(rng.standard_normal((1, T, H, 1)))
+    o2, h2 = oracle.kda_fwd(cq * q, ck * k, v, g, beta, h0, cu, nthreads=1, qk_l2norm=True)
+    assert oracle.rel_rms(o2, o1) < 1e-5 and oracle.rel_rms(h2, h1) < 1e-5
+    W = rng.standard_normal((1, T, HV, V))
+    Wh = rng.standard_normal((N, HV, K, V))
+
+    def loss(q, k):
+        o, hT = oracle.kda_fwd(q, k, v, g, beta, h0, cu, nthreads=1, qk_l2norm=True)
+        return float(np.sum(o * W) + np.sum(hT * Wh))
+
+    gr = oracle.kda_bwd(q, k, v, g, beta, h0, W, Wh, cu, nthreads=1, qk_l2norm=True)
+    args = dict(q=q, k=k)
+    h = 1e-6
+    for name in ("q", "k"):
+        arr = args[name]
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = loss(**args)
+            arr[idx] = old - h
+            lm = loss(**args)
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.max(np.abs(fd - gr["d" + name])) / max(1.0, np.max(np.abs(fd)))
+        assert err < 1e-7, (name, err)
