@@ -78,8 +78,9 @@ def kernel_bytes_per_token(name, cfg):
     dgl = 4 * HV * K / 64               # fp32 K-vector per chunk, per token
     table = {
         # tensor-core path (bf16, K = V = 128)
-        "kda_fwd_tc": 2 * qk + 2 * vv + g + b,
-        "kda_fwd_tc_states": 2 * qk + vv + g + b + hs + rec + 2 * t16,
+        "kda_prep_tc": 2 * qk + g + b + rec,
+        "kda_fwd_tc": rec + 2 * vv,
+        "kda_fwd_tc_states": rec + vv + hs + 2 * t16,
         "kda_bwd_scan_tc": rec + vv + hs + 2 * vv,
         "kda_bwd_intra_tc": 2 * t16 + 2 * hs + 3 * vv + vv + b + g + t16 / 2 + 2 * qk + vv + 2 * qk + g + b,
         # fp32 path
@@ -90,6 +91,8 @@ def kernel_bytes_per_token(name, cfg):
         "simple_bwd_intra_kernel": 3 * qk - qk + vv + vv + b + f32K + 2 * cc + 2 * hh + 2 * f32V
         + vv + b + g + 2 * f32K + 2 * f32K,
         "group_reduce_kernel": 2 * f32K + 2 * qk,
+        "group_reduce_l2norm_kernel": 2 * f32K + 4 * qk,
+        "l2norm_rows_kernel": 4 * qk,
     }
     return table.get(name)
 
@@ -196,13 +199,13 @@ class ClockSampler:
 class Runner:
     """Preallocated device buffers and the two C-ABI calls of one step."""
 
-    def __init__(self, cfg, device):
+    def __init__(self, cfg, device, qk_l2norm=False):
         self.lib = _lib.load()
         self.cfg = cfg
         self.dev = device
         d = cfg.to(device)
         self.d = d
-        self.s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+        self.s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, qk_l2norm)
         s = self.s
         self.o = torch.empty_like(d.v)
         self.hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=device)
@@ -351,6 +354,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=["step", "fwd", "bwd"], default="step",
                     help="time only the forward or only the backward call (profiling aid)")
+    ap.add_argument("--qk-l2norm", action="store_true",
+                    help="the same layer with the q/k L2-norm prologue inside the op")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="profiling aid: the dense workload with T replaced (e.g. 1024 for small ncu captures); "
                          "the JSON line names the changed workload")
@@ -381,7 +386,7 @@ def main():
         cfg = inputs.make_inputs(seed=1000 + args.config + 7919 * rank, name=f"{name}_T{args.seq_len}", **kw)
     else:
         cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
-    runner = Runner(cfg, dev)
+    runner = Runner(cfg, dev, qk_l2norm=args.qk_l2norm)
     if args.only != "step":  # profiling aid: time one half of the step only
         runner.step = runner.fwd if args.only == "fwd" else runner.bwd
         args.no_e2e = args.no_cpu_baseline = True
@@ -444,7 +449,8 @@ def main():
         "config": {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "H": cfg.H, "HV": cfg.HV, "K": cfg.K,
                    "V": cfg.V, "global_batch": cfg.B * world, "seq_len": cfg.T,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": f"inputs {ab['fwd'] / 1e9:.2f} GB read per step > L2 (no flush)"},
+                   "l2": f"inputs {ab['fwd'] / 1e9:.2f} GB read per step > L2 (no flush)",
+                   "qk_l2norm": bool(args.qk_l2norm)},
         "roofline": roof,
         "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
                           "algorithmic_bytes": ab["total"], "algorithmic_flops": af,

@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(_HERE, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
 KDA_F32, KDA_BF16 = 0, 1
+KDA_QK_L2NORM = 1  # kda_inputs.flags bit: q/k rows L2-normalised inside the op
 
 EXPORTS = (
     "kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_chunk_bwd_workspace_size",
@@ -28,7 +29,7 @@ class KdaInputs(ctypes.Structure):
         ("K", ctypes.c_int), ("V", ctypes.c_int), ("N", ctypes.c_int), ("dtype", ctypes.c_int),
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
         ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
-        ("cu_seqlens", ctypes.c_void_p),
+        ("cu_seqlens", ctypes.c_void_p), ("flags", ctypes.c_int),
     ]
 
 

@@ -40,6 +40,8 @@ kda_status validate(const kda_inputs *in, Problem &P) {
   if (in->HV > 65535) return fail(KDA_ERR_UNSUPPORTED, "HV=%d above 65535", in->HV);
   if (in->dtype != KDA_F32 && in->dtype != KDA_BF16)
     return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)in->dtype);
+  if ((in->flags & ~(int)KDA_QK_L2NORM) != 0)
+    return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", (unsigned)in->flags);
   const int64_t Ttot = (int64_t)in->B * in->T;
   if (Ttot * (in->HV > in->H ? in->HV : in->H) * kMaxDim >= ((int64_t)1 << 46))
     return fail(KDA_ERR_UNSUPPORTED, "problem too large");
@@ -66,8 +68,11 @@ kda_status validate(const kda_inputs *in, Problem &P) {
   if (nc >= (1 << 30)) return fail(KDA_ERR_UNSUPPORTED, "too many chunks");
   P.NC = (int)nc;
   P.bf16 = in->dtype == KDA_BF16;
+  P.l2norm = (in->flags & KDA_QK_L2NORM) != 0;
   P.q = in->q;
   P.k = in->k;
+  P.qr = in->q;
+  P.kr = in->k;
   P.v = in->v;
   P.g = in->g;
   P.beta = in->beta;
@@ -106,13 +111,18 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
       w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);
       w.tc_dd = (__nv_bfloat16 *)take(2 * slots * C * V);
       w.tc_dx = (__nv_bfloat16 *)take(2 * slots * C * V);
-      if (P.HV != P.H) {
+      if (P.HV != P.H || P.l2norm) {  // fp32 dq, dk partials, reduced per q/k head afterwards
         w.dqp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
         w.dkp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
       }
     }
     if (W) *W = w;
     return off;
+  }
+  if (P.l2norm) {  // normalised copies of q, k for the fp32 path
+    const size_t e = P.bf16 ? 2 : 4;
+    w.qn = take(e * (size_t)P.Ttot * P.H * K);
+    w.kn = take(e * (size_t)P.Ttot * P.H * K);
   }
   w.G = (float *)take(sizeof(float) * slots * C * K);
   w.Aqk = (float *)take(sizeof(float) * slots * C * C);
@@ -130,6 +140,16 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   }
   if (W) *W = w;
   return off;
+}
+
+// The fp32 path with the q/k L2-norm prologue runs on normalised copies of q
+// and k in the workspace; the raw rows stay in qr, kr for the backward.
+cudaError_t normalised_copies(const Problem &P, const Workspace &W, Problem *Pn, cudaStream_t s) {
+  if (!P.l2norm) return cudaSuccess;
+  cudaError_t e = launch_l2norm_rows(P, W.qn, W.kn, s);
+  Pn->q = W.qn;
+  Pn->k = W.kn;
+  return e;
 }
 
 kda_status check_ws(size_t need, void *ws, size_t bytes) {
@@ -193,8 +213,14 @@ kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspa
   if (P.N == 0) return KDA_OK;
   Workspace W;
   layout(P, false, (char *)workspace, &W);
-  cudaError_t e = use_tc(P) ? tc_forward(P, W, o, hT, false, W.flags + 2, (cudaStream_t)stream)
-                            : simple_forward(P, W, o, hT, (cudaStream_t)stream);
+  cudaError_t e;
+  if (use_tc(P)) {
+    e = tc_forward(P, W, o, hT, false, W.flags + 2, (cudaStream_t)stream);
+  } else {
+    Problem Pn = P;
+    e = normalised_copies(P, W, &Pn, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = simple_forward(Pn, W, o, hT, (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd");
   return KDA_OK;
 }
@@ -221,9 +247,11 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
     e = tc_forward(P, W, nullptr, nullptr, true, err, s);
     if (e == cudaSuccess) e = tc_backward_scan(P, W, dO, dhT, dh0, err, s);
     if (e == cudaSuccess) e = tc_backward_intra(P, W, dO, dv, dq, dk, dg, dbeta, err, s);
-    if (e == cudaSuccess && P.HV != P.H) e = launch_group_reduce(P, W.dqp, W.dkp, dq, dk, s);
+    if (e == cudaSuccess && (P.HV != P.H || P.l2norm)) e = launch_group_reduce(P, W.dqp, W.dkp, dq, dk, s);
   } else {
-    e = simple_backward(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, (cudaStream_t)stream);
+    Problem Pn = P;
+    e = normalised_copies(P, W, &Pn, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = simple_backward(Pn, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, (cudaStream_t)stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_bwd");
   return KDA_OK;
@@ -253,6 +281,6 @@ const char *kda_status_string(kda_status s) {
 
 const char *kda_last_error(void) { return g_err; }
 
-int kda_version(void) { return 100; }
+int kda_version(void) { return 101; }
 
 }  // extern "C"

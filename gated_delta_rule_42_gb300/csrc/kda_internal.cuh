@@ -25,10 +25,13 @@ struct Problem {
   int64_t Ttot;  // rows of the packed token axis (B*T)
   int NC;        // chunk-table capacity, an upper bound on the number of chunks
   bool bf16;
+  bool l2norm;   // KDA_QK_L2NORM: q, k rows L2-normalised inside the op
   const void *q, *k, *v;
   const float *g, *beta, *h0;
   const int32_t *cu;
+  const void *qr, *kr;  // the caller's raw q, k (== q, k unless the fp32 path runs on normalised copies)
 };
+constexpr float kL2NormEps = 1e-6f;  // epsilon of the q/k L2-norm prologue
 
 // Device workspace, carved from the caller's buffer.  Per-(chunk, value head)
 // slots are indexed slot = chunk * HV + j.
@@ -57,6 +60,8 @@ struct Workspace {
   __nv_bfloat16 *tc_dh;     // [slot] 32 KB: gradient of the chunk-end state [K][V], swizzled operand tile
   __nv_bfloat16 *tc_dd;     // [slot] 16 KB: gradient of the deltas [64][V], swizzled operand tile
   __nv_bfloat16 *tc_dx;     // [slot] 16 KB: dX = A^T dD [64][V], swizzled operand tile
+  // fp32 path with the q/k L2-norm prologue: normalised copies of q, k (dtype, [Ttot][H][K])
+  void *qn, *kn;
 };
 
 // --- element access -------------------------------------------------------
@@ -122,6 +127,11 @@ cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *d
 cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *dO, void *dv, void *dq, void *dk,
                               float *dg, float *dbeta, int *err, cudaStream_t s);
 // dq = (group sum of dqp) / sqrt(K), dk = group sum of dkp, over the HV/H value heads
+// q/k L2-norm prologue (l2norm.cu): normalised copies of the raw rows, and the
+// partial reduction fused with the backward through the normalisation.
+cudaError_t launch_l2norm_rows(const Problem &P, void *qn, void *kn, cudaStream_t s);
+cudaError_t launch_group_reduce_l2norm(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
+                                       cudaStream_t s);
 cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                 cudaStream_t s);
 // true when the tensor-core kernels handle this problem

@@ -9,7 +9,9 @@
 // registers, one program per (sequence, head, value block)).
 //
 // Per token: S <- diag(2^g) S ; e = S^T k ; S <- S + k (beta (v - e))^T ;
-// o = S^T q / sqrt(K).  An empty slot leaves the state untouched.
+// o = S^T q / sqrt(K).  An empty slot leaves the state untouched.  With the
+// q/k L2-norm prologue, k and q are divided by their row norms (sqrt of the sum
+// of squares + eps), applied as the factors rk and rq.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -52,7 +54,7 @@ recurrent_kernel(Problem P, Tin *__restrict__ o, float *__restrict__ hT) {
       if (c < K) {
         const int64_t e = (t * H + h) * K + c;
         kv = ldf(k, e);
-        qv = ldf(q, e) * scale;
+        qv = ldf(q, e);
         av = exp2f(P.g[(t * HV + j) * K + c]);
       }
       sk[c] = kv;
@@ -61,6 +63,16 @@ recurrent_kernel(Problem P, Tin *__restrict__ o, float *__restrict__ hT) {
     }
     const float b = P.beta[t * HV + j];
     __syncthreads();
+    float rk = 1.f, rq = scale;  // key and query row factors
+    if (P.l2norm) {  // q/k L2-norm prologue: every thread sums the two rows itself
+      float a2 = 0.f, b2 = 0.f;
+      for (int c = 0; c < K; ++c) {
+        a2 = fmaf(sk[c], sk[c], a2);
+        b2 = fmaf(sq[c], sq[c], b2);
+      }
+      rk = 1.0f / sqrtf(a2 + kL2NormEps);
+      rq = scale / sqrtf(b2 + kL2NormEps);
+    }
     float e = 0.f;
 #pragma unroll
     for (int c = 0; c < KHALF; ++c) {
@@ -68,7 +80,7 @@ recurrent_kernel(Problem P, Tin *__restrict__ o, float *__restrict__ hT) {
       e = fmaf(S[c], sk[c0 + c], e);
     }
     e += __shfl_xor_sync(0xffffffffu, e, 1);
-    const float d = active ? b * (ldf(v, (t * HV + j) * V + x) - e) : 0.f;
+    const float d = active ? b * (ldf(v, (t * HV + j) * V + x) - e * rk) * rk : 0.f;
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < KHALF; ++c) {
@@ -76,7 +88,7 @@ recurrent_kernel(Problem P, Tin *__restrict__ o, float *__restrict__ hT) {
       acc = fmaf(S[c], sq[c0 + c], acc);
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (active && half == 0) stf(o, (t * HV + j) * V + x, acc);
+    if (active && half == 0) stf(o, (t * HV + j) * V + x, acc * rq);
   }
   if (hT != nullptr && active) {
 #pragma unroll

@@ -379,20 +379,14 @@ cudaError_t run_backward(const Problem &P, const Workspace &W, const void *dO, c
                                                                        (Tin *)dv, dg, dbeta));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (P.Ttot > 0) {
-    const int64_t total = P.Ttot * P.H * P.K;
-    int blocks = (int)((total + 255) / 256);
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    KDA_LAUNCH("group_reduce_kernel", s, group_reduce_kernel<Tin><<<blocks, 256, 0, s>>>(P, W.dqp, W.dkp, (Tin *)dq, (Tin *)dk));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return launch_group_reduce(P, W.dqp, W.dkp, dq, dk, s);
 }
 
 }  // namespace
 
 cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                 cudaStream_t s) {
+  if (P.l2norm) return launch_group_reduce_l2norm(P, dqp, dkp, dq, dk, s);
   if (P.Ttot == 0) return cudaSuccess;
   const int64_t total = P.Ttot * P.H * P.K;
   int blocks = (int)((total + 255) / 256);

@@ -350,6 +350,25 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       float kv[8], qv[8], o[8], e1[8], e2[8];
       unpack8(*reinterpret_cast<const uint4 *>(sm + C_KRAW + off), kv);  // raw k, q (zero past len)
       unpack8(*reinterpret_cast<const uint4 *>(sm + C_QRAW + off), qv);
+      if (P.l2norm) {  // q/k L2-norm prologue: the row's 16 chunks sit on this half-warp
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sk = fmaf(kv[e], kv[e], sk);
+          sq = fmaf(qv[e], qv[e], sq);
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+          sk += __shfl_xor_sync(0xffffffffu, sk, o);
+          sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        }
+        const float rk = 1.0f / sqrtf(sk + kL2NormEps), rq = 1.0f / sqrtf(sq + kL2NormEps);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kv[e] *= rk;
+          qv[e] *= rq;
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float g = G[r * kGLD + c0 + e];
@@ -687,7 +706,7 @@ cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  const bool partial = P.HV != P.H;
+  const bool partial = P.HV != P.H || P.l2norm;  // fp32 partials, reduced (and normalised) per q/k head
   IntraArgs a{(const __nv_bfloat16 *)dO, (__nv_bfloat16 *)dv, partial ? (void *)W.dqp : dq,
               partial ? (void *)W.dkp : dk, dg, dbeta, partial, err};
   TmaMaps maps;

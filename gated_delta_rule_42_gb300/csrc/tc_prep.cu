@@ -60,11 +60,34 @@ static_assert(REC_AM == (uint32_t)kTileRecA && REC_GAML + 512 == (uint32_t)kTile
 // columns are both free of bank conflicts.
 __device__ __forceinline__ int fsw(int r, int c) { return r * kC + (c ^ ((r & 7) << 2)); }
 
+// q/k L2-norm prologue on one row held by the 16 lanes of a half-warp, 8
+// channels each: x <- x / sqrt(sum of the row's squares + eps).
+__device__ __forceinline__ void l2norm_row16(float (&kv)[8], float (&qv)[8]) {
+  float sk = 0.f, sq = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sk = fmaf(kv[e], kv[e], sk);
+    sq = fmaf(qv[e], qv[e], sq);
+  }
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) {
+    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  }
+  const float rk = 1.0f / sqrtf(sk + kL2NormEps), rq = 1.0f / sqrtf(sq + kL2NormEps);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    kv[e] *= rk;
+    qv[e] *= rq;
+  }
+}
+
 // Phase (a).  Needs k, q, the gate rows and beta of the chunk in shared memory;
 // writes G (in place), the vectors, the decay tiles Kr, Qr (in place of k, q)
 // and Kc, and the record's Bk, Qg, Khat tiles and 2^G_last straight to global
-// memory (rec).  Ends with a __syncthreads.
-__device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec) {
+// memory (rec).  With l2n, the k and q rows are L2-normalised first.  Ends
+// with a __syncthreads.
+__device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec, bool l2n) {
   const int tid = threadIdx.x;
   float *G = (float *)(sm + P_G);
   float *vec = (float *)(sm + P_VEC);
@@ -120,6 +143,7 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       float kv[8], qv[8], g[8], e1[8], e2[8], o[8];
       unpack8(*reinterpret_cast<const uint4 *>(sm + P_K + off), kv);
       unpack8(*reinterpret_cast<const uint4 *>(sm + P_Q + off), qv);
+      if (l2n) l2norm_row16(kv, qv);
       *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGT + c0);
       *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + 4);
 #pragma unroll
@@ -369,7 +393,7 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
   KDA_PT(0);
 
   unsigned char *rec = W.tc_tiles + slot * kTileRecord;
-  phase_a(sm, len, beta, rec);
+  phase_a(sm, len, beta, rec, P.l2norm);
   KDA_PT(2);
   phase_b(sm, beta, rec);
   KDA_PT(10);

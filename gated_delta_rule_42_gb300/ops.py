@@ -40,8 +40,9 @@ def _check_tensor(name, t, dtype, device, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None):
-    """Validate the tensors and build the C ``kda_inputs`` struct."""
+def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None, use_qk_l2norm=False):
+    """Validate the tensors and build the C ``kda_inputs`` struct.  With
+    use_qk_l2norm the library L2-normalises every q and k row itself."""
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
     B, T, H, K = q.shape
@@ -70,6 +71,7 @@ def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None):
     s.g, s.beta = g.data_ptr(), beta.data_ptr()
     s.h0 = None if initial_state is None else initial_state.data_ptr()
     s.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
+    s.flags = _lib.KDA_QK_L2NORM if use_qk_l2norm else 0
     return s
 
 
@@ -88,9 +90,10 @@ def _aligned(ws: torch.Tensor):
 
 
 def chunk_kda_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_final_state=False,
-                  workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                  workspace: Optional[torch.Tensor] = None,
+                  use_qk_l2norm: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     lib = _lib.load()
-    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens)
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
     o = torch.empty_like(v)
     hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
           if output_final_state else None)
@@ -103,9 +106,10 @@ def chunk_kda_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_
 
 
 def chunk_kda_bwd(q, k, v, g, beta, initial_state, cu_seqlens, do, dht,
-                  workspace: Optional[torch.Tensor] = None, need_dh0: bool = True):
+                  workspace: Optional[torch.Tensor] = None, need_dh0: bool = True,
+                  use_qk_l2norm: bool = False):
     lib = _lib.load()
-    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens)
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
     _check_tensor("do", do, q.dtype, q.device, tuple(v.shape))
     if dht is not None:
         _check_tensor("dht", dht, torch.float32, q.device, (s.N, s.HV, s.K, s.V))
@@ -128,10 +132,12 @@ def chunk_kda_bwd(q, k, v, g, beta, initial_state, cu_seqlens, do, dht,
 
 class ChunkKDAFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, output_final_state):
-        o, hT = chunk_kda_fwd(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state)
+    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, use_qk_l2norm):
+        o, hT = chunk_kda_fwd(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
+                              use_qk_l2norm=use_qk_l2norm)
         ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
         ctx.has_h0 = initial_state is not None
+        ctx.l2 = use_qk_l2norm
         return o, hT
 
     @staticmethod
@@ -140,23 +146,27 @@ class ChunkKDAFunction(torch.autograd.Function):
         do = do.contiguous()
         dht = None if dht is None else dht.contiguous()
         dq, dk, dv, dg, db, dh0 = chunk_kda_bwd(q, k, v, g, beta, h0, cu, do, dht,
-                                                need_dh0=ctx.has_h0)
-        return dq, dk, dv, dg, db, dh0, None, None
+                                                need_dh0=ctx.has_h0, use_qk_l2norm=ctx.l2)
+        return dq, dk, dv, dg, db, dh0, None, None, None
 
 
-def chunk_kda(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, output_final_state=False):
-    """Chunked KDA forward (with autograd).  Returns (o, final_state or None)."""
-    return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state)
+def chunk_kda(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, output_final_state=False,
+              use_qk_l2norm=False):
+    """Chunked KDA forward (with autograd).  Returns (o, final_state or None).
+    use_qk_l2norm: L2-normalise every q and k row inside the op (its backward
+    included)."""
+    return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
+                                  use_qk_l2norm)
 
 
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
-                  output_final_state=False):
+                  output_final_state=False, use_qk_l2norm=False):
     """Token-by-token KDA forward for inference (fp32 arithmetic).  Rejects
     inputs that require grad: train through :func:`chunk_kda`."""
     if any(t is not None and t.requires_grad for t in (q, k, v, gate, beta, initial_state)):
         raise RuntimeError("recurrent_kda is inference-only; use chunk_kda for training")
     lib = _lib.load()
-    s = make_inputs_struct(q, k, v, gate, beta, initial_state, cu_seqlens)
+    s = make_inputs_struct(q, k, v, gate, beta, initial_state, cu_seqlens, use_qk_l2norm)
     o = torch.empty_like(v)
     hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
           if output_final_state else None)

@@ -73,7 +73,20 @@ typedef enum kda_dtype {
   KDA_BF16 = 1  /* q, k, v (and o, dO, dq, dk, dv) in bf16: fp32 accumulation          */
 } kda_dtype;
 
-/* Problem description shared by every entry point. */
+/* Bits of kda_inputs.flags. */
+enum {
+  /* q/k L2-norm prologue: each (token, q/k head) row of q and of k is divided
+   * by sqrt(sum over the K channels of its squares + 1e-6) before the op (and
+   * before the 1/sqrt(K) query scale); dq and dk are then gradients w.r.t. the
+   * raw rows.  The KDA layer of "kda in torchtitan (training)"
+   * (pytorch/torchtitan PR #4164) imports such an `l2norm` beside
+   * `recurrent_kda`; its epsilon is not printed there (1e-6 is this library's
+   * choice). */
+  KDA_QK_L2NORM = 1
+};
+
+/* Problem description shared by every entry point.  Zero-initialise it: a
+ * zero flags field keeps the plain behaviour. */
 typedef struct kda_inputs {
   int B, T;         /* batch and (padded) tokens per batch row; B must be 1 with cu_seqlens */
   int H, HV;        /* query/key heads and value heads; HV must be a multiple of H          */
@@ -85,6 +98,7 @@ typedef struct kda_inputs {
   const float *beta;        /* per (token, value head) write strength                        */
   const float *h0;          /* initial states [N][HV][K][V], or NULL for zeros               */
   const int32_t *cu_seqlens;/* device [N+1] packed offsets, or NULL for a dense batch         */
+  int flags;                /* KDA_QK_L2NORM or 0; any other bit is KDA_ERR_INVALID_ARG       */
 } kda_inputs;
 
 /* Bytes of device workspace kda_chunk_fwd needs for this problem (256-byte
@@ -122,7 +136,7 @@ const char *kda_status_string(kda_status s);
 /* Message describing the last failure on the calling thread ("" if none). */
 const char *kda_last_error(void);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 101 (kda_inputs gained `flags`). */
 int kda_version(void);
 
 /* Chunked forward without a caller workspace (no counterpart on the pages).

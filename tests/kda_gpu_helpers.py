@@ -28,11 +28,12 @@ def _poisoned_ws(nbytes, dev):
     return ws, ctypes.c_void_p(a), nbytes + 512 - (a - p)
 
 
-def gpu_fwd(inp, dev="cuda", lib=None):
-    """kda_chunk_fwd on the inputs (moved to dev); returns CPU o, hT."""
+def gpu_fwd(inp, dev="cuda", lib=None, l2=False):
+    """kda_chunk_fwd on the inputs (moved to dev); returns CPU o, hT.  l2: the
+    q/k L2-norm prologue flag."""
     lib = lib or _lib.load()
     d = inp.to(dev)
-    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
     o = _nan_like(d.v.shape, d.dtype, dev)
     hT = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if inp.output_final_state else None
     need = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s))
@@ -45,10 +46,10 @@ def gpu_fwd(inp, dev="cuda", lib=None):
     return o.cpu(), (None if hT is None else hT.cpu())
 
 
-def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True):
+def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True, l2=False):
     lib = lib or _lib.load()
     d = inp.to(dev)
-    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
     out = dict(dq=_nan_like(d.q.shape, d.dtype, dev), dk=_nan_like(d.k.shape, d.dtype, dev),
                dv=_nan_like(d.v.shape, d.dtype, dev), dg=_nan_like(d.g.shape, torch.float32, dev),
                dbeta=_nan_like(d.beta.shape, torch.float32, dev))
@@ -67,10 +68,10 @@ def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True):
     return {k: (None if v is None else v.cpu()) for k, v in out.items()}
 
 
-def gpu_recurrent(inp, dev="cuda", lib=None):
+def gpu_recurrent(inp, dev="cuda", lib=None, l2=False):
     lib = lib or _lib.load()
     d = inp.to(dev)
-    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
     o = _nan_like(d.v.shape, d.dtype, dev)
     hT = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if inp.output_final_state else None
     st = lib.kda_recurrent_fwd(ctypes.byref(s), ctypes.c_void_p(o.data_ptr()),
@@ -81,16 +82,17 @@ def gpu_recurrent(inp, dev="cuda", lib=None):
     return o.cpu(), (None if hT is None else hT.cpu())
 
 
-def oracle_fwd(inp):
+def oracle_fwd(inp, l2=False):
     f = inp.f64()
     cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
-    return oracle.kda_fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], cu, True)
+    return oracle.kda_fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], cu, True, qk_l2norm=l2)
 
 
-def oracle_bwd(inp):
+def oracle_bwd(inp, l2=False):
     f = inp.f64()
     cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
-    return oracle.kda_bwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], f["do"], f["dhT"], cu)
+    return oracle.kda_bwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], f["do"], f["dhT"], cu,
+                          qk_l2norm=l2)
 
 
 def valid_mask(inp):

@@ -50,6 +50,8 @@ def _inputs(**kw):
     (dict(B=2, N=2, cu_seqlens=0x2000), _lib.KDA_ERR_INVALID_ARG),  # packed needs B == 1
     (dict(q=None), _lib.KDA_ERR_INVALID_ARG),
     (dict(dtype=7), _lib.KDA_ERR_INVALID_ARG),
+    (dict(flags=2), _lib.KDA_ERR_INVALID_ARG),          # unknown flag bit
+    (dict(flags=-1), _lib.KDA_ERR_INVALID_ARG),
 ])
 def test_host_validation(lib, kw, status):
     s = _inputs(**kw)
@@ -79,3 +81,31 @@ def test_workspace_checks(lib):
 def test_status_strings(lib):
     for st in range(5):
         assert lib.kda_status_string(st).decode()
+
+
+def test_struct_fields_follow_the_header(lib):
+    """The ctypes mirror of kda_inputs lists the header's members in order."""
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    body = re.search(r"typedef struct kda_inputs \{(.*?)\} kda_inputs;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if decl:
+            names += [re.sub(r"[*\s]", "", n).split()[-1] if n.strip() else n
+                      for n in re.sub(r"^(const\s+)?[a-z0-9_]+\s+", "", decl).split(",")]
+    assert [n.strip("* ") for n in names] == [f[0] for f in _lib.KdaInputs._fields_]
+
+
+def test_l2norm_flag_workspace(lib):
+    """The fp32 path with the q/k L2-norm prologue works on normalised copies
+    of q and k (two more [T][H][K] buffers); the bf16 path normalises in its
+    kernels and only reduces dq, dk partials per q/k head."""
+    s0 = _inputs(K=64, V=64)
+    s1 = _inputs(K=64, V=64, flags=_lib.KDA_QK_L2NORM)
+    extra = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s1)) - lib.kda_chunk_fwd_workspace_size(ctypes.byref(s0))
+    assert extra >= 2 * 128 * 2 * 64 * 2
+    t0 = _inputs(K=128, V=128, HV=2)
+    t1 = _inputs(K=128, V=128, HV=2, flags=_lib.KDA_QK_L2NORM)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(t1)) == lib.kda_chunk_fwd_workspace_size(ctypes.byref(t0))
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(t1)) > lib.kda_chunk_bwd_workspace_size(ctypes.byref(t0))

@@ -161,3 +161,47 @@ def test_backward_is_bitwise_deterministic():
     b = H.gpu_bwd(inp)
     for key in a:
         assert torch.equal(a[key], b[key]), key
+
+
+# ---- the q/k L2-norm prologue (KDA_QK_L2NORM) ----
+
+def _unnormalised(inp, seed):
+    """q and k rows rescaled by seeded positive factors (the generator's rows
+    are unit-norm, which would hide the prologue)."""
+    rng = np.random.default_rng(seed)
+    for name in ("q", "k"):
+        x = getattr(inp, name)
+        f = torch.from_numpy(np.exp(rng.normal(0.0, 0.7, size=x.shape[:-1] + (1,))))
+        setattr(inp, name, (x.to(torch.float64) * f).to(inp.dtype))
+    return inp
+
+
+L2 = [
+    ("tc_dense", dict(B=2, T=130, H=2, HV=2, K=128, V=128), torch.bfloat16),
+    ("tc_varlen_gva", dict(B=1, T=300, H=2, HV=4, K=128, V=128, cu_seqlens=[0, 0, 100, 100, 300]),
+     torch.bfloat16),
+    ("fp32_gva_odd", dict(B=1, T=129, H=1, HV=3, K=32, V=48), torch.float32),
+    ("bf16_small_dims", dict(B=2, T=70, H=2, HV=2, K=64, V=64), torch.bfloat16),
+    ("fp32_k128", dict(B=1, T=90, H=1, HV=2, K=128, V=64), torch.float32),
+]
+
+
+@pytest.mark.parametrize("name,kw,dtype", L2, ids=[e[0] for e in L2])
+def test_qk_l2norm_prologue(name, kw, dtype):
+    inp = _unnormalised(inputs.make_inputs(dtype=dtype, seed=zlib.crc32(name.encode()) % 1000, name=name, **kw),
+                        seed=zlib.crc32(name.encode()) % 997)
+    tol = H.TOL[dtype]
+    o, hT = H.gpu_fwd(inp, l2=True)
+    ro, rhT = H.oracle_fwd(inp, l2=True)
+    H.check_fwd(inp, o, hT, ro, rhT if inp.output_final_state else None, tol["fwd"])
+    gr = H.gpu_bwd(inp, want_dh0=inp.h0 is not None, l2=True)
+    H.check_bwd(inp, gr, H.oracle_bwd(inp, l2=True), tol["bwd"])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_qk_l2norm_recurrent(dtype):
+    inp = _unnormalised(inputs.make_inputs(B=1, T=200, H=2, HV=4, K=128, V=128, dtype=dtype, seed=13,
+                                           cu_seqlens=[0, 0, 80, 80, 200]), seed=14)
+    o, hT = H.gpu_recurrent(inp, l2=True)
+    ro, rhT = H.oracle_fwd(inp, l2=True)
+    H.check_fwd(inp, o, hT, ro, rhT, H.TOL[dtype]["fwd"])
