@@ -110,12 +110,33 @@ def l2norm_rows_bwd(x, dy, eps=L2NORM_EPS):
     return r * (dy - y * np.sum(y * dy, axis=-1, keepdims=True))
 
 
+# The scalar-gate (GDN) variant: one log2 decay per (token, value head), shared
+# by every key channel -- the gated delta rule that the GDN pipeline of
+# "[Fix] Use unit KDA gate scale when A_log is omitted" (fla-org/flash-linear-
+# attention PR #1294) and the triton-ascend GDN port of its commit log (PR #1011)
+# run, of which KDA is the per-channel generalisation.  g is [B,T,HV]; the
+# recurrence is KDA's with that gate repeated over K, and dg sums the
+# per-channel gradients over K.
+def gate_per_channel(g, K):
+    """[B,T,HV] scalar gates -> [B,T,HV,K] (the same decay on every channel)."""
+    g = np.asarray(g, dtype=np.float64)
+    return np.ascontiguousarray(np.repeat(g[..., None], K, axis=-1))
+
+
+def gate_grad_reduce(dg):
+    """[B,T,HV,K] per-channel gate gradients -> [B,T,HV] (sum over K)."""
+    return np.sum(np.asarray(dg, dtype=np.float64), axis=-1)
+
+
 def kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, output_final_state=True, nthreads=0,
-            qk_l2norm=False):
+            qk_l2norm=False, scalar_gate=False):
     """Token-by-token KDA forward.  Returns (o [B,T,HV,V], hT [N,HV,K,V] or None).
-    With qk_l2norm, q and k rows are normalised first (:func:`l2norm_rows`)."""
+    With qk_l2norm, q and k rows are normalised first (:func:`l2norm_rows`);
+    with scalar_gate, g is [B,T,HV] (:func:`gate_per_channel`)."""
     if qk_l2norm:
         q, k = l2norm_rows(q), l2norm_rows(k)
+    if scalar_gate:
+        g = gate_per_channel(g, np.shape(q)[-1])
     lib = _load()
     q, k, v, g, beta, h0 = map(_c64, (q, k, v, g, beta, h0))
     B, T, H, K = q.shape
@@ -131,10 +152,17 @@ def kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, output_final_state=True,
     return o, hT
 
 
-def kda_bwd(q, k, v, g, beta, h0, do, dhT, cu_seqlens=None, nthreads=0, qk_l2norm=False):
+def kda_bwd(q, k, v, g, beta, h0, do, dhT, cu_seqlens=None, nthreads=0, qk_l2norm=False,
+            scalar_gate=False):
     """Token-by-token KDA backward.  Returns dict dq, dk, dv, dg, dbeta, dh0.
     With qk_l2norm, the gradients of the normalised rows are carried back
-    through :func:`l2norm_rows` to the raw q and k."""
+    through :func:`l2norm_rows` to the raw q and k; with scalar_gate, g and dg
+    are [B,T,HV] (:func:`gate_grad_reduce`)."""
+    if scalar_gate:
+        out = kda_bwd(q, k, v, gate_per_channel(g, np.shape(q)[-1]), beta, h0, do, dhT, cu_seqlens, nthreads,
+                      qk_l2norm)
+        out["dg"] = gate_grad_reduce(out["dg"])
+        return out
     if qk_l2norm:
         out = kda_bwd(l2norm_rows(q), l2norm_rows(k), v, g, beta, h0, do, dhT, cu_seqlens, nthreads)
         out["dq"] = l2norm_rows_bwd(q, out["dq"])

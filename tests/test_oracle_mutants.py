@@ -119,3 +119,33 @@ def test_l2norm_pins_catch_planted_mistake(attr, fn, monkeypatch):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin caught {fn.__name__}"
+
+
+def _reduce_mean(dg):
+    return np.mean(np.asarray(dg, np.float64), axis=-1)
+
+
+def _broadcast_scaled(g, K):
+    g = np.asarray(g, np.float64)
+    return np.ascontiguousarray(np.repeat(g[..., None] / K, K, axis=-1))
+
+
+def _reduce_first_channel(dg):
+    return np.asarray(dg, np.float64)[..., 0]
+
+
+GATE_MUTANTS = [("gate_grad_reduce", _reduce_mean), ("gate_per_channel", _broadcast_scaled),
+                ("gate_grad_reduce", _reduce_first_channel)]
+GATE_PINS = [pins.test_scalar_gate_pure_decay_closed_form, pins.test_scalar_gate_finite_differences]
+
+
+@pytest.mark.parametrize("attr,fn", GATE_MUTANTS, ids=[m[1].__name__ for m in GATE_MUTANTS])
+def test_scalar_gate_pins_catch_planted_mistake(attr, fn, monkeypatch):
+    monkeypatch.setattr(oracle, attr, fn)
+    caught = []
+    for pin in GATE_PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught {fn.__name__}"

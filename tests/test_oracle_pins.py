@@ -355,3 +355,65 @@ def test_qk_l2norm_kda_scale_invariance_and_finite_differences():
             fd[idx] = (lp - lm) / (2 * h)
         err = np.max(np.abs(fd - gr["d" + name])) / max(1.0, np.max(np.abs(fd)))
         assert err < 1e-7, (name, err)
+
+
+# ---- the scalar-gate (GDN) variant ----
+
+def test_scalar_gate_pure_decay_closed_form():
+    """beta = 0: the state only decays, by one scalar factor per token, so
+    o_t = 2^(G_t) h0^T q~_t and hT = 2^(G_T) h0 with G_t = sum_{s<=t} g_s, and
+    dL/dg_s = ln 2 (sum_{t>=s} <o_t, W_t> + <hT, Wh>)."""
+    rng = np.random.default_rng(31)
+    T, H, HV, K, V = 5, 1, 2, 3, 2
+    q, k, v, _, beta = rand_problem(rng, 1, T, H, HV, K, V)
+    beta = np.zeros_like(beta)
+    g = -np.log1p(np.exp(rng.standard_normal((1, T, HV))))
+    h0 = rng.standard_normal((1, HV, K, V))
+    W = rng.standard_normal((1, T, HV, V))
+    Wh = rng.standard_normal((1, HV, K, V))
+    o, hT = oracle.kda_fwd(q, k, v, g, beta, h0, scalar_gate=True)
+    gr = oracle.kda_bwd(q, k, v, g, beta, h0, W, Wh, scalar_gate=True)
+    assert gr["dg"].shape == g.shape
+    for j in range(HV):
+        G = np.cumsum(g[0, :, j])
+        ref_o = np.stack([2.0 ** G[t] * (h0[0, j].T @ q[0, t, 0]) / math.sqrt(K) for t in range(T)])
+        np.testing.assert_allclose(o[0, :, j], ref_o, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(hT[0, j], 2.0 ** G[-1] * h0[0, j], rtol=1e-13)
+        contrib = np.array([np.dot(ref_o[t], W[0, t, j]) for t in range(T)])
+        final = np.sum(2.0 ** G[-1] * h0[0, j] * Wh[0, j])
+        ref_dg = math.log(2.0) * (np.cumsum(contrib[::-1])[::-1] + final)
+        np.testing.assert_allclose(gr["dg"][0, :, j], ref_dg, rtol=1e-12, atol=1e-13)
+
+
+def test_scalar_gate_finite_differences():
+    """Central differences of every input with a scalar gate, GVA + an empty slot."""
+    rng = np.random.default_rng(32)
+    T, H, HV, K, V = 6, 1, 2, 3, 2
+    q, k, v, _, beta = rand_problem(rng, 1, T, H, HV, K, V)
+    g = -np.log1p(np.exp(rng.standard_normal((1, T, HV))))
+    cu = [0, 2, 2, 6]
+    N = 3
+    h0 = rng.standard_normal((N, HV, K, V))
+    W = rng.standard_normal((1, T, HV, V))
+    Wh = rng.standard_normal((N, HV, K, V))
+
+    def loss(q, k, v, g, beta, h0):
+        o, hT = oracle.kda_fwd(q, k, v, g, beta, h0, cu, nthreads=1, scalar_gate=True)
+        return float(np.sum(o * W) + np.sum(hT * Wh))
+
+    gr = oracle.kda_bwd(q, k, v, g, beta, h0, W, Wh, cu, nthreads=1, scalar_gate=True)
+    args = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0)
+    h = 1e-6
+    for name, arr in args.items():
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = loss(**args)
+            arr[idx] = old - h
+            lm = loss(**args)
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        key = "dbeta" if name == "beta" else "dh0" if name == "h0" else "d" + name
+        err = np.max(np.abs(fd - gr[key])) / max(1.0, np.max(np.abs(fd)))
+        assert err < 1e-7, (name, err)
