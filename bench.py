@@ -46,9 +46,10 @@ L2_BYTES = 126 * 2 ** 20
 def algorithmic_bytes(cfg):
     e = 2 if cfg.dtype == torch.bfloat16 else 4
     H, HV, K, V = cfg.H, cfg.HV, cfg.K, cfg.V
-    inp = 2 * H * K * e + HV * V * e + 4 * HV * K + 4 * HV
+    gb = 4 * HV if cfg.g.dim() == 3 else 4 * HV * K  # the gate (and dg): scalar or per channel
+    inp = 2 * H * K * e + HV * V * e + gb + 4 * HV
     fwd = inp + HV * V * e
-    bwd = inp + HV * V * e + 2 * H * K * e + HV * V * e + 4 * HV * K + 4 * HV
+    bwd = inp + HV * V * e + 2 * H * K * e + HV * V * e + gb + 4 * HV
     toks = cfg.valid_tokens
     state = 4 * cfg.N * HV * K * V
     st_f = (state if cfg.h0 is not None else 0) + (state if cfg.output_final_state else 0)
@@ -93,6 +94,8 @@ def kernel_bytes_per_token(name, cfg):
         "group_reduce_kernel": 2 * f32K + 2 * qk,
         "group_reduce_l2norm_kernel": 2 * f32K + 4 * qk,
         "l2norm_rows_kernel": 4 * qk,
+        "gate_expand_kernel": 4 * HV + f32K,
+        "gate_grad_reduce_kernel": f32K + 4 * HV,
     }
     return table.get(name)
 
@@ -356,6 +359,8 @@ def main():
                     help="time only the forward or only the backward call (profiling aid)")
     ap.add_argument("--qk-l2norm", action="store_true",
                     help="the same layer with the q/k L2-norm prologue inside the op")
+    ap.add_argument("--scalar-gate", action="store_true",
+                    help="the same layer with a scalar gate g [B, T, HV] (the GDN variant)")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="profiling aid: the dense workload with T replaced (e.g. 1024 for small ncu captures); "
                          "the JSON line names the changed workload")
@@ -379,11 +384,16 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    if args.seq_len is not None:  # profiling aid: same dense shape with another T
+    if args.seq_len is not None or args.scalar_gate:  # the same shape with another T, or a scalar gate
         name, kw = inputs.CONFIGS[args.config]
-        assert kw.get("cu_seqlens") is None and "T" in kw, "--seq-len needs a dense configuration"
-        kw = dict(kw, T=args.seq_len)
-        cfg = inputs.make_inputs(seed=1000 + args.config + 7919 * rank, name=f"{name}_T{args.seq_len}", **kw)
+        if args.seq_len is not None:
+            assert kw.get("cu_seqlens") is None and "T" in kw, "--seq-len needs a dense configuration"
+            kw = dict(kw, T=args.seq_len)
+            name = f"{name}_T{args.seq_len}"
+        if args.scalar_gate:
+            kw = dict(kw, scalar_gate=True)
+            name = f"{name}_scalar_gate"
+        cfg = inputs.make_inputs(seed=1000 + args.config + 7919 * rank, name=name, **kw)
     else:
         cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
     runner = Runner(cfg, dev, qk_l2norm=args.qk_l2norm)
@@ -450,7 +460,7 @@ def main():
                    "V": cfg.V, "global_batch": cfg.B * world, "seq_len": cfg.T,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": f"inputs {ab['fwd'] / 1e9:.2f} GB read per step > L2 (no flush)",
-                   "qk_l2norm": bool(args.qk_l2norm)},
+                   "qk_l2norm": bool(args.qk_l2norm), "scalar_gate": bool(args.scalar_gate)},
         "roofline": roof,
         "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
                           "algorithmic_bytes": ab["total"], "algorithmic_flops": af,

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_HERE, "libkda.so")
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
 KDA_F32, KDA_BF16 = 0, 1
 KDA_QK_L2NORM = 1  # kda_inputs.flags bit: q/k rows L2-normalised inside the op
+KDA_SCALAR_GATE = 2  # kda_inputs.flags bit: g, dg are [B, T, HV] (one decay per token and value head)
 
 EXPORTS = (
     "kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_chunk_bwd_workspace_size",

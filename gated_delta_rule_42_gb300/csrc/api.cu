@@ -40,7 +40,7 @@ kda_status validate(const kda_inputs *in, Problem &P) {
   if (in->HV > 65535) return fail(KDA_ERR_UNSUPPORTED, "HV=%d above 65535", in->HV);
   if (in->dtype != KDA_F32 && in->dtype != KDA_BF16)
     return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)in->dtype);
-  if ((in->flags & ~(int)KDA_QK_L2NORM) != 0)
+  if ((in->flags & ~(int)(KDA_QK_L2NORM | KDA_SCALAR_GATE)) != 0)
     return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", (unsigned)in->flags);
   const int64_t Ttot = (int64_t)in->B * in->T;
   if (Ttot * (in->HV > in->H ? in->HV : in->H) * kMaxDim >= ((int64_t)1 << 46))
@@ -69,6 +69,7 @@ kda_status validate(const kda_inputs *in, Problem &P) {
   P.NC = (int)nc;
   P.bf16 = in->dtype == KDA_BF16;
   P.l2norm = (in->flags & KDA_QK_L2NORM) != 0;
+  P.scalar_gate = (in->flags & KDA_SCALAR_GATE) != 0;
   P.q = in->q;
   P.k = in->k;
   P.qr = in->q;
@@ -102,6 +103,10 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   w.seq = (int4 *)take(sizeof(int4) * (size_t)(P.N > 0 ? P.N : 1));
   w.chunk = (int4 *)take(sizeof(int4) * (size_t)(P.NC > 0 ? P.NC : 1));
   w.flags = (int *)take(sizeof(int) * 4);
+  if (P.scalar_gate) {  // the gate repeated over K (and its per-channel gradient)
+    w.gx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
+    if (backward) w.dgx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
+  }
   if (use_tc(P)) {
     w.tc_tiles = (unsigned char *)take(kTileRecord * slots);  // per-chunk records of the preparation kernel
     if (backward) {  // tensor-core backward: per-slot tiles passed between its kernels
@@ -140,6 +145,15 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
   }
   if (W) *W = w;
   return off;
+}
+
+// With a scalar gate every kernel reads the gate repeated over K from the
+// workspace (the recurrent kernel alone reads the scalars directly).
+cudaError_t gate_per_channel(const Problem &P, const Workspace &W, Problem *Pg, cudaStream_t s) {
+  if (!P.scalar_gate) return cudaSuccess;
+  cudaError_t e = launch_gate_expand(P, W.gx, s);
+  Pg->g = W.gx;
+  return e;
 }
 
 // The fp32 path with the q/k L2-norm prologue runs on normalised copies of q
@@ -213,13 +227,16 @@ kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspa
   if (P.N == 0) return KDA_OK;
   Workspace W;
   layout(P, false, (char *)workspace, &W);
-  cudaError_t e;
-  if (use_tc(P)) {
-    e = tc_forward(P, W, o, hT, false, W.flags + 2, (cudaStream_t)stream);
-  } else {
-    Problem Pn = P;
-    e = normalised_copies(P, W, &Pn, (cudaStream_t)stream);
-    if (e == cudaSuccess) e = simple_forward(Pn, W, o, hT, (cudaStream_t)stream);
+  Problem Pg = P;
+  cudaError_t e = gate_per_channel(P, W, &Pg, (cudaStream_t)stream);
+  if (e == cudaSuccess) {
+    if (use_tc(P)) {
+      e = tc_forward(Pg, W, o, hT, false, W.flags + 2, (cudaStream_t)stream);
+    } else {
+      Problem Pn = Pg;
+      e = normalised_copies(Pg, W, &Pn, (cudaStream_t)stream);
+      if (e == cudaSuccess) e = simple_forward(Pn, W, o, hT, (cudaStream_t)stream);
+    }
   }
   if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd");
   return KDA_OK;
@@ -240,19 +257,24 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
   if (P.N == 0) return KDA_OK;
   Workspace W;
   layout(P, true, (char *)workspace, &W);
-  cudaError_t e;
-  if (use_tc(P)) {
-    cudaStream_t s = (cudaStream_t)stream;
-    int *err = W.flags + 2;
-    e = tc_forward(P, W, nullptr, nullptr, true, err, s);
-    if (e == cudaSuccess) e = tc_backward_scan(P, W, dO, dhT, dh0, err, s);
-    if (e == cudaSuccess) e = tc_backward_intra(P, W, dO, dv, dq, dk, dg, dbeta, err, s);
-    if (e == cudaSuccess && (P.HV != P.H || P.l2norm)) e = launch_group_reduce(P, W.dqp, W.dkp, dq, dk, s);
-  } else {
-    Problem Pn = P;
-    e = normalised_copies(P, W, &Pn, (cudaStream_t)stream);
-    if (e == cudaSuccess) e = simple_backward(Pn, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, (cudaStream_t)stream);
+  cudaStream_t s = (cudaStream_t)stream;
+  Problem Pg = P;
+  cudaError_t e = gate_per_channel(P, W, &Pg, s);
+  float *dgk = P.scalar_gate ? W.dgx : dg;  // per-channel gate gradient
+  if (e == cudaSuccess) {
+    if (use_tc(P)) {
+      int *err = W.flags + 2;
+      e = tc_forward(Pg, W, nullptr, nullptr, true, err, s);
+      if (e == cudaSuccess) e = tc_backward_scan(Pg, W, dO, dhT, dh0, err, s);
+      if (e == cudaSuccess) e = tc_backward_intra(Pg, W, dO, dv, dq, dk, dgk, dbeta, err, s);
+      if (e == cudaSuccess && (P.HV != P.H || P.l2norm)) e = launch_group_reduce(Pg, W.dqp, W.dkp, dq, dk, s);
+    } else {
+      Problem Pn = Pg;
+      e = normalised_copies(Pg, W, &Pn, s);
+      if (e == cudaSuccess) e = simple_backward(Pn, W, dO, dhT, dq, dk, dv, dgk, dbeta, dh0, s);
+    }
   }
+  if (e == cudaSuccess && P.scalar_gate) e = launch_gate_grad_reduce(P, W.dgx, dg, s);
   if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_bwd");
   return KDA_OK;
 }

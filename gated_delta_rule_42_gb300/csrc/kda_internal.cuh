@@ -26,6 +26,7 @@ struct Problem {
   int NC;        // chunk-table capacity, an upper bound on the number of chunks
   bool bf16;
   bool l2norm;   // KDA_QK_L2NORM: q, k rows L2-normalised inside the op
+  bool scalar_gate;  // KDA_SCALAR_GATE: g, dg are [Ttot][HV] (the kernels see g repeated over K)
   const void *q, *k, *v;
   const float *g, *beta, *h0;
   const int32_t *cu;
@@ -62,6 +63,8 @@ struct Workspace {
   __nv_bfloat16 *tc_dx;     // [slot] 16 KB: dX = A^T dD [64][V], swizzled operand tile
   // fp32 path with the q/k L2-norm prologue: normalised copies of q, k (dtype, [Ttot][H][K])
   void *qn, *kn;
+  // scalar gate: the gate repeated over K, and the per-channel gate gradient (fp32, [Ttot][HV][K])
+  float *gx, *dgx;
 };
 
 // --- element access -------------------------------------------------------
@@ -132,6 +135,10 @@ cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *
 cudaError_t launch_l2norm_rows(const Problem &P, void *qn, void *kn, cudaStream_t s);
 cudaError_t launch_group_reduce_l2norm(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                        cudaStream_t s);
+// Scalar gate (gate.cu): [Ttot][HV] -> [Ttot][HV][K] for the kernels, and the
+// per-channel gradient summed over K.
+cudaError_t launch_gate_expand(const Problem &P, float *gx, cudaStream_t s);
+cudaError_t launch_gate_grad_reduce(const Problem &P, const float *dgx, float *dg, cudaStream_t s);
 cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                 cudaStream_t s);
 // true when the tensor-core kernels handle this problem

@@ -11,7 +11,8 @@
 // Per token: S <- diag(2^g) S ; e = S^T k ; S <- S + k (beta (v - e))^T ;
 // o = S^T q / sqrt(K).  An empty slot leaves the state untouched.  With the
 // q/k L2-norm prologue, k and q are divided by their row norms (sqrt of the sum
-// of squares + eps), applied as the factors rk and rq.
+// of squares + eps), applied as the factors rk and rq.  A scalar gate (one
+// decay per token and value head) is read as such.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -55,7 +56,7 @@ recurrent_kernel(Problem P, Tin *__restrict__ o, float *__restrict__ hT) {
         const int64_t e = (t * H + h) * K + c;
         kv = ldf(k, e);
         qv = ldf(q, e);
-        av = exp2f(P.g[(t * HV + j) * K + c]);
+        av = exp2f(P.scalar_gate ? P.g[t * HV + j] : P.g[(t * HV + j) * K + c]);
       }
       sk[c] = kv;
       sq[c] = qv;

@@ -173,9 +173,10 @@ def packed_lengths(rng: np.random.Generator, n_seq: int, total: int, lo: int, hi
 def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.bfloat16,
                 cu_seqlens=None, lengths_fn=None, h0: bool = True, final_state: bool = True,
                 dhT: Optional[bool] = None, g_mean: float = 0.0, seed: int = 0,
-                name: str = "custom") -> KdaInputs:
+                name: str = "custom", scalar_gate: bool = False) -> KdaInputs:
     """Draw one problem.  ``cu_seqlens`` may be a list of offsets (B must be 1);
-    ``lengths_fn(rng)`` may instead return the offsets from the generator."""
+    ``lengths_fn(rng)`` may instead return the offsets from the generator.
+    ``scalar_gate`` draws g as [B, T, HV] (one decay per token and value head)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     cu = None
     if lengths_fn is not None:
@@ -191,7 +192,7 @@ def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.
     k = _l2_rows(_normal(rng, (B, T, H, K)))
     v = _normal(rng, (B, T, HV, V))
     beta = _sigmoid(_normal(rng, (B, T, HV)))
-    g = _neg_softplus_clipped(_normal(rng, (B, T, HV, K), mean=g_mean))
+    g = _neg_softplus_clipped(_normal(rng, (B, T, HV) if scalar_gate else (B, T, HV, K), mean=g_mean))
     h0_t = _normal(rng, (N, HV, K, V), std=0.1) if h0 else None
     do = _normal(rng, (B, T, HV, V))
     if dhT is None:

@@ -42,7 +42,8 @@ def _check_tensor(name, t, dtype, device, shape=None):
 
 def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None, use_qk_l2norm=False):
     """Validate the tensors and build the C ``kda_inputs`` struct.  With
-    use_qk_l2norm the library L2-normalises every q and k row itself."""
+    use_qk_l2norm the library L2-normalises every q and k row itself; a gate of
+    shape [B, T, HV] (instead of [B, T, HV, K]) is the scalar-gate variant."""
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
     B, T, H, K = q.shape
@@ -55,7 +56,8 @@ def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None, us
     _check_tensor("q", q, q.dtype, dev)
     _check_tensor("k", k, q.dtype, dev, (B, T, H, K))
     _check_tensor("v", v, q.dtype, dev, (B, T, HV, V))
-    _check_tensor("g", g, torch.float32, dev, (B, T, HV, K))
+    scalar_gate = g.dim() == 3  # [B, T, HV]: one decay per (token, value head), the GDN variant
+    _check_tensor("g", g, torch.float32, dev, (B, T, HV) if scalar_gate else (B, T, HV, K))
     _check_tensor("beta", beta, torch.float32, dev, (B, T, HV))
     if cu_seqlens is not None:
         _check_tensor("cu_seqlens", cu_seqlens, torch.int32, dev)
@@ -71,7 +73,7 @@ def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None, us
     s.g, s.beta = g.data_ptr(), beta.data_ptr()
     s.h0 = None if initial_state is None else initial_state.data_ptr()
     s.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
-    s.flags = _lib.KDA_QK_L2NORM if use_qk_l2norm else 0
+    s.flags = (_lib.KDA_QK_L2NORM if use_qk_l2norm else 0) | (_lib.KDA_SCALAR_GATE if scalar_gate else 0)
     return s
 
 

@@ -31,7 +31,7 @@
  * Layouts (row-major, all DEVICE pointers):
  *   q, k, dq, dk   [B][T][H][K]      dtype
  *   v, o, dO, dv   [B][T][HV][V]     dtype
- *   g, dg          [B][T][HV][K]     fp32
+ *   g, dg          [B][T][HV][K]     fp32  ([B][T][HV] with KDA_SCALAR_GATE)
  *   beta, dbeta    [B][T][HV]        fp32
  *   h0,hT,dhT,dh0  [N][HV][K][V]     fp32
  * Value head j reads query/key head j / (HV/H) (contiguous groups).
@@ -82,7 +82,14 @@ enum {
    * (pytorch/torchtitan PR #4164) imports such an `l2norm` beside
    * `recurrent_kda`; its epsilon is not printed there (1e-6 is this library's
    * choice). */
-  KDA_QK_L2NORM = 1
+  KDA_QK_L2NORM = 1,
+  /* scalar gate (the GDN variant): g and dg are [B][T][HV] fp32, one log2 decay
+   * per (token, value head) shared by every key channel -- the gated delta rule
+   * of the GDN pipeline named in "[Fix] Use unit KDA gate scale when A_log is
+   * omitted" (fla-org/flash-linear-attention PR #1294, commit log), of which
+   * KDA's per-channel gate is the generalisation.  dg is the sum over K of the
+   * per-channel gradients. */
+  KDA_SCALAR_GATE = 2
 };
 
 /* Problem description shared by every entry point.  Zero-initialise it: a
@@ -98,7 +105,7 @@ typedef struct kda_inputs {
   const float *beta;        /* per (token, value head) write strength                        */
   const float *h0;          /* initial states [N][HV][K][V], or NULL for zeros               */
   const int32_t *cu_seqlens;/* device [N+1] packed offsets, or NULL for a dense batch         */
-  int flags;                /* KDA_QK_L2NORM or 0; any other bit is KDA_ERR_INVALID_ARG       */
+  int flags;                /* KDA_QK_L2NORM | KDA_SCALAR_GATE or 0; other bits: INVALID_ARG */
 } kda_inputs;
 
 /* Bytes of device workspace kda_chunk_fwd needs for this problem (256-byte

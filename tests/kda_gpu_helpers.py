@@ -85,14 +85,15 @@ def gpu_recurrent(inp, dev="cuda", lib=None, l2=False):
 def oracle_fwd(inp, l2=False):
     f = inp.f64()
     cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
-    return oracle.kda_fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], cu, True, qk_l2norm=l2)
+    return oracle.kda_fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], cu, True, qk_l2norm=l2,
+                          scalar_gate=f["g"].ndim == 3)
 
 
 def oracle_bwd(inp, l2=False):
     f = inp.f64()
     cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
     return oracle.kda_bwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], f["do"], f["dhT"], cu,
-                          qk_l2norm=l2)
+                          qk_l2norm=l2, scalar_gate=f["g"].ndim == 3)
 
 
 def valid_mask(inp):

@@ -50,7 +50,7 @@ def _inputs(**kw):
     (dict(B=2, N=2, cu_seqlens=0x2000), _lib.KDA_ERR_INVALID_ARG),  # packed needs B == 1
     (dict(q=None), _lib.KDA_ERR_INVALID_ARG),
     (dict(dtype=7), _lib.KDA_ERR_INVALID_ARG),
-    (dict(flags=2), _lib.KDA_ERR_INVALID_ARG),          # unknown flag bit
+    (dict(flags=4), _lib.KDA_ERR_INVALID_ARG),          # unknown flag bit
     (dict(flags=-1), _lib.KDA_ERR_INVALID_ARG),
 ])
 def test_host_validation(lib, kw, status):

@@ -205,3 +205,37 @@ def test_qk_l2norm_recurrent(dtype):
     o, hT = H.gpu_recurrent(inp, l2=True)
     ro, rhT = H.oracle_fwd(inp, l2=True)
     H.check_fwd(inp, o, hT, ro, rhT, H.TOL[dtype]["fwd"])
+
+
+# ---- the scalar-gate (GDN) variant (KDA_SCALAR_GATE: g, dg [B, T, HV]) ----
+
+SG = [
+    ("tc_dense", dict(B=2, T=130, H=2, HV=2, K=128, V=128), torch.bfloat16, False),
+    ("tc_varlen_gva_l2norm", dict(B=1, T=300, H=2, HV=4, K=128, V=128, cu_seqlens=[0, 0, 100, 100, 250]),
+     torch.bfloat16, True),
+    ("fp32_gva_odd", dict(B=1, T=129, H=1, HV=3, K=32, V=48), torch.float32, False),
+]
+
+
+@pytest.mark.parametrize("name,kw,dtype,l2", SG, ids=[e[0] for e in SG])
+def test_scalar_gate(name, kw, dtype, l2):
+    inp = inputs.make_inputs(dtype=dtype, seed=zlib.crc32(name.encode()) % 1000, name="sg_" + name,
+                             scalar_gate=True, **kw)
+    if l2:
+        inp = _unnormalised(inp, seed=5)
+    assert inp.g.dim() == 3
+    tol = H.TOL[dtype]
+    o, hT = H.gpu_fwd(inp, l2=l2)
+    ro, rhT = H.oracle_fwd(inp, l2=l2)
+    H.check_fwd(inp, o, hT, ro, rhT if inp.output_final_state else None, tol["fwd"])
+    gr = H.gpu_bwd(inp, want_dh0=inp.h0 is not None, l2=l2)
+    H.check_bwd(inp, gr, H.oracle_bwd(inp, l2=l2), tol["bwd"])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_scalar_gate_recurrent(dtype):
+    inp = inputs.make_inputs(B=1, T=200, H=2, HV=4, K=128, V=128, dtype=dtype, seed=15,
+                             cu_seqlens=[0, 0, 80, 80, 200], scalar_gate=True)
+    o, hT = H.gpu_recurrent(inp)
+    ro, rhT = H.oracle_fwd(inp)
+    H.check_fwd(inp, o, hT, ro, rhT, H.TOL[dtype]["fwd"])
