@@ -106,10 +106,10 @@ def kernel_bytes_per_token(name, cfg):
 # value is reported only while those sources are unchanged.
 NCU_TRAFFIC = {
     "kda_bwd_intra_tc": dict(
-        bytes_per_token=1293894400 / 8192,  # 981.0 MB read + 312.9 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=1292881664 / 8192,  # 980.8 MB read + 312.0 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_intra.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh",
                  "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="045197515c46e68797bc0585b436ded83feaa3a0815eea318684e495adee4542",
+        sha256="8534f9a19489cd7af083b99416613443ec2b7d8dfb337e891c220842a307f414",
         profile="profiles/ncu_full_kernels_B8_T1024_H32_K128.md"),
 }
 
@@ -255,32 +255,75 @@ def timed(fn, steps, stream):
     return a.elapsed_time(b)
 
 
-def e2e_measure(cfg, runner, steps):
-    """Same step through the public API with HOST buffers: pinned host inputs
-    copied in and every output copied out inside the timed region."""
-    d = runner.d
+def e2e_measure(cfg, runner, steps, qk_l2norm=False):
+    """Same step through the public API with HOST buffers: every step copies its
+    inputs in from pinned host memory and every output back out, inside the
+    timed region.  The steps are pipelined the way a training loop would run
+    them: copies in on one stream, the two C-ABI calls on another, copies out
+    on a third, with two device sets so that step i+1's inputs arrive and step
+    i-1's outputs leave while step i computes.  Timed with CUDA events from the
+    first copy in to the last copy out."""
+    dev = runner.dev
     host_in = {k: getattr(cfg, k).pin_memory() for k in ("q", "k", "v", "g", "beta", "do")
                if getattr(cfg, k) is not None}
     for k in ("h0", "dhT"):
         if getattr(cfg, k) is not None:
             host_in[k] = getattr(cfg, k).pin_memory()
-    outs = [runner.o, runner.dq, runner.dk, runner.dv, runner.dg, runner.db] + \
-        [t for t in (runner.hT, runner.dh0) if t is not None]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    with torch.cuda.stream(s_cmp):
+        runners = [runner, Runner(cfg, dev, qk_l2norm=qk_l2norm)]
+    for r in runners:
+        r.sp = ctypes.c_void_p(s_cmp.cuda_stream)
+
+    def outs_of(r):
+        return [r.o, r.dq, r.dk, r.dv, r.dg, r.db] + [t for t in (r.hT, r.dh0) if t is not None]
+
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_of(runner)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
 
-    def one():
-        for k, t in host_in.items():
-            getattr(d, k).copy_(t, non_blocking=True)
-        runner.step()
-        for dst, src in zip(host_out, outs):
-            dst.copy_(src, non_blocking=True)
+    def run(n, start=None, end=None):
+        torch.cuda.synchronize()
+        done_cmp = [None, None]   # compute of the last step on each set (its inputs are free after it)
+        done_out = [None, None]   # copy-out of the last step on each set (its outputs are free after it)
+        if start is not None:
+            start.record(s_in)
+        last = None
+        for i in range(n):
+            b = i & 1
+            r = runners[b]
+            with torch.cuda.stream(s_in):
+                if done_cmp[b] is not None:
+                    s_in.wait_event(done_cmp[b])
+                for k, t in host_in.items():
+                    getattr(r.d, k).copy_(t, non_blocking=True)
+                arrived = ev()
+                arrived.record(s_in)
+            s_cmp.wait_event(arrived)
+            if done_out[b] is not None:
+                s_cmp.wait_event(done_out[b])
+            r.step()
+            done_cmp[b] = ev()
+            done_cmp[b].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_cmp[b])
+                for dst, src in zip(host_out, outs_of(r)):
+                    dst.copy_(src, non_blocking=True)
+                done_out[b] = ev()
+                done_out[b].record(s_out)
+            last = done_out[b]
+        if end is not None:
+            s_in.wait_event(last)
+            end.record(s_in)
+        torch.cuda.synchronize()
 
-    one()
-    torch.cuda.synchronize()
-    ms = timed(one, steps, runner.stream)
-    return ms / steps, h2d, d2h
+    run(2)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(steps, a, b)
+    for r in runners:
+        r.sp = ctypes.c_void_p(runner.stream.cuda_stream)
+    return a.elapsed_time(b) / steps, h2d, d2h
 
 
 def kernel_split(runner, steps):
@@ -421,7 +464,7 @@ def main():
     split = kernel_split(runner, max(3, min(args.steps, 10)))
     e2e = None
     if not args.no_e2e:
-        e_ms, h2d, d2h = e2e_measure(cfg, runner, max(3, min(args.steps, 10)))
+        e_ms, h2d, d2h = e2e_measure(cfg, runner, max(3, min(args.steps, 10)), args.qk_l2norm)
         e_value, e_ms = job_throughput(e_ms, cfg.valid_tokens, 1, dist, device=dev)  # ms per step, max over ranks
         e2e = (e_value, e_ms, h2d, d2h)
 
