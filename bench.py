@@ -338,41 +338,53 @@ def kernel_split(runner, steps):
     return _lib.timing_collect(lib)
 
 
-def oracle_sample(cfg, units):
-    """fp64 slices of batch row 0 holding ``units`` value heads (rounded up to
-    whole q/k head groups), for the oracle."""
+def oracle_sample(cfg, units, seqs=1):
+    """fp64 slices of the first ``seqs`` sequences holding ``units`` value heads
+    (rounded up to whole q/k head groups), for the oracle, packed as one batch
+    row with offsets."""
     r = cfg.HV // cfg.H
     hs = list(range((min(units, cfg.HV) + r - 1) // r))
     js = list(range(hs[0] * r, (hs[-1] + 1) * r))
     off = cfg.offsets()
-    a, b = int(off[0]), int(off[1])
+    seqs = max(1, min(seqs, len(off) - 1))
+    a, b = int(off[0]), int(off[seqs])
     sl = {}
     for k in ("q", "k", "v", "g", "beta", "do"):
         x = getattr(cfg, k)
         y = x.reshape(cfg.B * cfg.T, *x.shape[2:])[a:b]
         y = y[:, hs] if k in ("q", "k") else y[:, js]
         sl[k] = np.ascontiguousarray(y.to(torch.float64).numpy()[None])
+    sl["cu"] = np.ascontiguousarray((off[:seqs + 1] - a).astype(np.int32))
     return sl, len(js), b - a
 
 
 def run_oracle(sl, cores):
     import oracle
-    oracle.kda_fwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], None, None, False, nthreads=cores)
-    oracle.kda_bwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], None, sl["do"], None, nthreads=cores)
+    oracle.kda_fwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], None, sl["cu"], False, nthreads=cores)
+    oracle.kda_bwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], None, sl["do"], None, sl["cu"], nthreads=cores)
 
 
 def cpu_baseline(cfg):
     """The fp64 oracle as it stands, on the host cores, on a bounded sample:
     whole (sequence, value head) units of the same workload, fwd + bwd."""
     cores = os.cpu_count() or 1
-    sl, nj, L = oracle_sample(cfg, 2 * cores)
+    # one sequence first, to size a sample of about ten seconds of CPU work
+    sl, nj, L = oracle_sample(cfg, cfg.HV, 1)
     t0 = time.perf_counter()
     run_oracle(sl, cores)
-    dt = time.perf_counter() - t0
+    dt1 = time.perf_counter() - t0
+    seqs = int(max(1, min(cfg.N, 10.0 // max(dt1, 1e-3))))
+    if seqs > 1:
+        sl, nj, L = oracle_sample(cfg, cfg.HV, seqs)
+        t0 = time.perf_counter()
+        run_oracle(sl, cores)
+        dt = time.perf_counter() - t0
+    else:
+        dt = dt1
     value = L * nj / cfg.HV / dt  # a layer token needs all HV value heads
     return dict(value=round(value, 2), unit="tokens/s", cores=cores, kind="oracle",
-                sample=f"batch row 0, {nj} of {cfg.HV} value heads x {L} tokens, fwd+bwd in fp64 "
-                       f"({dt:.1f} s); tokens/s = tokens x heads / HV / seconds")
+                sample=f"the first {seqs} of {cfg.N} sequences, {nj} of {cfg.HV} value heads, {L} tokens, "
+                       f"fwd+bwd in fp64 ({dt:.1f} s); tokens/s = tokens x heads / HV / seconds")
 
 
 # --------------------------------------------------------------------------
