@@ -21,6 +21,7 @@ EXPORTS = (
     "kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_chunk_bwd_workspace_size",
     "kda_chunk_bwd", "kda_recurrent_fwd", "kda_status_string", "kda_last_error", "kda_version",
     "kda_launch_count", "kda_timing_enable", "kda_timing_collect", "kda_chunk_fwd_noalloc",
+    "kda_state_compose",
 )
 
 
@@ -68,6 +69,8 @@ def load(path: str = LIB_PATH):
         lib.kda_recurrent_fwd.restype = i
         lib.kda_chunk_fwd_noalloc.argtypes = [P, vp, vp, vp]
         lib.kda_chunk_fwd_noalloc.restype = i
+        lib.kda_state_compose.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        lib.kda_state_compose.restype = i
         lib.kda_status_string.argtypes = [i]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_last_error.argtypes = []

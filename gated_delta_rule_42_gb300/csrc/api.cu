@@ -290,6 +290,27 @@ kda_status kda_recurrent_fwd(const kda_inputs *in, void *o, float *hT, void *str
   return KDA_OK;
 }
 
+kda_status kda_state_compose(const float *M, const float *h, const float *c, float *out, int count, int K,
+                             int V, int transpose, void *stream) {
+  g_err[0] = 0;
+  if (count < 0) return fail(KDA_ERR_INVALID_ARG, "count=%d must be >= 0", count);
+  if (K < 1 || V < 1) return fail(KDA_ERR_INVALID_ARG, "K=%d V=%d must be positive", K, V);
+  if (K > kMaxDim || V > kMaxDim)
+    return fail(KDA_ERR_UNSUPPORTED, "K=%d V=%d: dims above %d are not implemented", K, V, kMaxDim);
+  if (count == 0) return KDA_OK;
+  if (M == nullptr || h == nullptr || out == nullptr) return fail(KDA_ERR_INVALID_ARG, "M, h and out are required");
+  const char *o0 = (const char *)out, *o1 = o0 + sizeof(float) * (size_t)count * K * V;
+  auto overlaps = [&](const void *p, size_t bytes) {
+    const char *a = (const char *)p;
+    return a < o1 && o0 < a + bytes;
+  };
+  if (overlaps(M, sizeof(float) * (size_t)count * K * K) || overlaps(h, sizeof(float) * (size_t)count * K * V))
+    return fail(KDA_ERR_INVALID_ARG, "out overlaps M or h");
+  cudaError_t e = launch_state_compose(M, h, c, out, count, K, V, transpose != 0, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_state_compose");
+  return KDA_OK;
+}
+
 const char *kda_status_string(kda_status s) {
   switch (s) {
     case KDA_OK: return "ok";

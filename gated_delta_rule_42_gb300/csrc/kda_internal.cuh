@@ -135,6 +135,9 @@ cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *
 cudaError_t launch_l2norm_rows(const Problem &P, void *qn, void *kn, cudaStream_t s);
 cudaError_t launch_group_reduce_l2norm(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                        cudaStream_t s);
+// State composition for the context-parallel relay (relay.cu).
+cudaError_t launch_state_compose(const float *M, const float *h, const float *c, float *out, int64_t count, int K,
+                                 int V, bool transpose, cudaStream_t s);
 // Scalar gate (gate.cu): [Ttot][HV] -> [Ttot][HV][K] for the kernels, and the
 // per-channel gradient summed over K.
 cudaError_t launch_gate_expand(const Problem &P, float *gx, cudaStream_t s);

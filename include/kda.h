@@ -137,6 +137,23 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
  * recurrent_kda entry point of "kda in torchtitan (training)". */
 kda_status kda_recurrent_fwd(const kda_inputs *in, void *o, float *hT, void *stream);
 
+/* State composition for the context-parallel state relay.  When a sequence is
+ * split across ranks, each rank's segment maps the state it starts from
+ * affinely, S_end = M S_start + c: c is the segment's final state from a zero
+ * start and M (K x K) the segment's transition, which kda_chunk_fwd returns
+ * as hT when run on the segment with v = 0, V = K and h0 = the identity.  An
+ * exclusive scan of out = M h + c across ranks gives every rank its true start
+ * state, and the backward scan uses out = M^T dh + c on state gradients: the
+ * synchronous context parallelism of "[KDA] Add Paddle training compatibility"
+ * (PFCCLab/flash-linear-attention PR #2, summary and test plan).
+ *   M    [count][K][K] fp32     h, out [count][K][V] fp32     c [count][K][V] fp32 or NULL (zero)
+ *   out[i] = op(M[i]) h[i] + c[i], op = transpose when `transpose` != 0.
+ * DEVICE pointers; out may equal c but must not overlap M or h.  count >= 0,
+ * 1 <= K, V <= 128; violations are KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED
+ * before anything is launched. */
+kda_status kda_state_compose(const float *M, const float *h, const float *c, float *out, int count, int K,
+                             int V, int transpose, void *stream);
+
 /* Static description of a status code. */
 const char *kda_status_string(kda_status s);
 

@@ -109,3 +109,17 @@ def test_l2norm_flag_workspace(lib):
     t1 = _inputs(K=128, V=128, HV=2, flags=_lib.KDA_QK_L2NORM)
     assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(t1)) == lib.kda_chunk_fwd_workspace_size(ctypes.byref(t0))
     assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(t1)) > lib.kda_chunk_bwd_workspace_size(ctypes.byref(t0))
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(count=-1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(K=129), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(V=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(M=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(out=0x100000 + 4 * 64), _lib.KDA_ERR_INVALID_ARG),  # out overlaps h
+])
+def test_state_compose_validation(lib, args, status):
+    a = dict(M=0x400000, h=0x100000, c=None, out=0x800000, count=2, K=64, V=64, transpose=0)
+    a.update(args)
+    st = lib.kda_state_compose(a["M"], a["h"], a["c"], a["out"], a["count"], a["K"], a["V"], a["transpose"], None)
+    assert st == status, lib.kda_last_error()
