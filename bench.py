@@ -244,6 +244,41 @@ class Runner:
         self.bwd()
 
 
+def cp_step_fn(runner, R):
+    """One fwd+bwd step of the context-parallel layer: every sequence split into
+    R equal segments, each processed as its rank would (local pass, transition,
+    relay scan, final pass; the mirror image backward), the ranks one after the
+    other on this GPU."""
+    from gated_delta_rule_42_gb300 import cp
+    from gated_delta_rule_42_gb300.ops import chunk_kda_bwd, chunk_kda_fwd
+    d = runner.d
+    T = d.q.shape[1]
+    bounds = [T * r // R for r in range(R + 1)]
+    segs = [[x[:, bounds[r]:bounds[r + 1]].contiguous() for x in (d.q, d.k, d.v, d.g, d.beta, d.do)]
+            for r in range(R)]
+
+    def step():
+        cs, Ms = [], []
+        for q, k, v, g, beta, _ in segs:
+            cs.append(chunk_kda_fwd(q, k, v, g, beta, None, None, True)[1])
+            Ms.append(cp.segment_transition(q, k, g, beta))
+        hs = [d.h0 if d.h0 is not None else torch.zeros_like(cs[0])]
+        for r in range(1, R):
+            hs.append(cp.compose(Ms[r - 1], hs[-1], cs[r - 1]))
+        for r, (q, k, v, g, beta, _) in enumerate(segs):
+            chunk_kda_fwd(q, k, v, g, beta, hs[r], None, r == R - 1)
+        ds = [chunk_kda_bwd(q, k, v, g, beta, hs[r], None, do, None)[5]
+              for r, (q, k, v, g, beta, do) in enumerate(segs)]
+        ends = [None] * R
+        ends[R - 1] = d.dhT
+        for r in range(R - 1, 0, -1):
+            ends[r - 1] = cp.compose(Ms[r], ends[r] if ends[r] is not None else torch.zeros_like(ds[r]), ds[r], True)
+        for r, (q, k, v, g, beta, do) in enumerate(segs):
+            chunk_kda_bwd(q, k, v, g, beta, hs[r], None, do, ends[r], need_dh0=(r == 0 and d.h0 is not None))
+
+    return step
+
+
 def timed(fn, steps, stream):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -416,6 +451,9 @@ def main():
                     help="the same layer with the q/k L2-norm prologue inside the op")
     ap.add_argument("--scalar-gate", action="store_true",
                     help="the same layer with a scalar gate g [B, T, HV] (the GDN variant)")
+    ap.add_argument("--cp-ranks", type=int, default=0,
+                    help="context parallelism: split every sequence into this many segments and run the state "
+                         "relay, the ranks serialized on this GPU (measures the relay's per-rank work)")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="profiling aid: the dense workload with T replaced (e.g. 1024 for small ncu captures); "
                          "the JSON line names the changed workload")
@@ -452,6 +490,9 @@ def main():
     else:
         cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
     runner = Runner(cfg, dev, qk_l2norm=args.qk_l2norm)
+    if args.cp_ranks > 1:  # context parallelism, the ranks serialized on this GPU
+        runner.step = cp_step_fn(runner, args.cp_ranks)
+        args.no_e2e = True
     if args.only != "step":  # profiling aid: time one half of the step only
         runner.step = runner.fwd if args.only == "fwd" else runner.bwd
         args.no_e2e = args.no_cpu_baseline = True
@@ -499,11 +540,12 @@ def main():
     dom = max(split, key=lambda k: split[k][0])
     dom_ms, dom_n = split[dom]
     bpt = kernel_bytes_per_token(dom, cfg)
-    achieved = (bpt * toks / (dom_ms / dom_n / 1e3) / 1e9) if bpt else None
+    toks_launch = toks / max(1, args.cp_ranks)  # with context parallelism a launch covers one segment
+    achieved = (bpt * toks_launch / (dom_ms / dom_n / 1e3) / 1e9) if bpt else None
     roof = dict(kernel=dom, bound="hbm", achieved=None if achieved is None else round(achieved, 1),
                 peak=peaks["hbm"], unit="GB/s",
                 frac=None if achieved is None else round(achieved / peaks["hbm"], 4),
-                traffic=measured_traffic(dom, toks), launch_ms=round(dom_ms / dom_n, 4),
+                traffic=measured_traffic(dom, toks_launch), launch_ms=round(dom_ms / dom_n, 4),
                 peak_source=f"{peaks['src']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["src"] == "measured"
                 else "fallback 6.8 TB/s")
     out = {
@@ -515,7 +557,9 @@ def main():
                    "V": cfg.V, "global_batch": cfg.B * world, "seq_len": cfg.T,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": f"inputs {ab['fwd'] / 1e9:.2f} GB read per step > L2 (no flush)",
-                   "qk_l2norm": bool(args.qk_l2norm), "scalar_gate": bool(args.scalar_gate)},
+                   "qk_l2norm": bool(args.qk_l2norm), "scalar_gate": bool(args.scalar_gate),
+                   **({"cp_ranks": args.cp_ranks, "cp": "sequences split into cp_ranks segments, state relay, "
+                       "ranks serialized on one GPU"} if args.cp_ranks > 1 else {})},
         "roofline": roof,
         "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
                           "algorithmic_bytes": ab["total"], "algorithmic_flops": af,

@@ -14,8 +14,17 @@ constexpr int kChunk = 64;    // tokens per chunk
 constexpr int kMaxDim = 128;  // largest K and V the kernels are built for
 // Per-slot record of the chunk tiles the states pass saves for the reverse scan
 // and the gradient chain: Bk, Qg, Khat (16 KB each), Aqk, A (8 KB each), 2^G_last.
+// The per-chunk record of the bf16 path (one per (chunk, value head) slot),
+// written by the record kernel: swizzled bf16 operand tiles, then 2^G_last.
+// Bk, Khat and A come first: the states pass reads only those 40 KB.
+constexpr uint32_t kRecBK = 0;        // beta k 2^G            [64 r][128 c]
+constexpr uint32_t kRecKH = 16384;    // k 2^(G_last - G)      [64 r][128 c]
+constexpr uint32_t kRecAM = 32768;    // A = (I + L)^-1        [64 r][64 i]
+constexpr uint32_t kRecAQK = 40960;   // Aqk                   [64 r][64 i]
+constexpr uint32_t kRecQG = 49152;    // q~ 2^G                [64 r][128 c]
+constexpr uint32_t kRecGAML = 65536;  // 2^G_last              fp32 [128]
+constexpr uint32_t kRecStates = 40960;  // Bk | Khat | A: what the states pass loads
 constexpr size_t kTileRecord = 65536 + 512;
-constexpr size_t kTileRecA = 57344;  // offset of the A tile in the record
 
 // A chunk-table entry: the chunk's logical sequence n (-1 = unused slot), its
 // first packed token, its length (1..64) and its index inside the sequence.
@@ -55,7 +64,7 @@ struct Workspace {
   float *dw;     // [slot][64][K]
   // tensor-core backward (bf16, K = V = 128), per (chunk, value head) slot
   __nv_bfloat16 *tc_hs;     // [slot] 32 KB: chunk-start state h [K][V], swizzled operand tile (forward recompute)
-  unsigned char *tc_tiles;  // [slot] kTileRecord bytes: swizzled Bk | Qg | Khat | Aqk | A tiles, then 2^G_last (fp32 [K])
+  unsigned char *tc_tiles;  // [slot] kTileRecord bytes: the per-chunk record (kRec* offsets)
   unsigned char *tc_xt;     // [slot] 16 KB: swizzled X^T tile [V][64]
   unsigned char *tc_dt;     // [slot] 16 KB: swizzled D^T tile [V][64]
   __nv_bfloat16 *tc_dh;     // [slot] 32 KB: gradient of the chunk-end state [K][V], swizzled operand tile

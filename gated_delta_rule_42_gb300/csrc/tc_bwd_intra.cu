@@ -194,7 +194,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     bulk_load(sbase + I_STK + 192 * 128, dx + 8192, 8192u, bar_ld);     //               sub-tile 1
     bulk_load(sbase + I_STK + 128 * 128, dd, 8192u, bar_ld);            // rows 128..191
     bulk_load(sbase + I_STK + 320 * 128, dd + 8192, 8192u, bar_ld);
-    bulk_load(sbase + C_A, W.tc_tiles + slot * kTileRecord + kTileRecA, 8192u, bar_ld);
+    bulk_load(sbase + C_A, W.tc_tiles + slot * kTileRecord + kRecAM, 8192u, bar_ld);
     tma_load3(sbase + I_STK + 64 * 128, &maps.d, 0, j, t0, bar_ld);    // dO rows 64..127
     tma_load3(sbase + I_STK + 256 * 128, &maps.d, 64, j, t0, bar_ld);
     tma_tile(sbase + I_V, &maps.v, j, t0, bar_ld);

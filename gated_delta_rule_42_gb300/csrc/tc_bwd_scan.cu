@@ -30,8 +30,7 @@ using namespace umma;
 using namespace tc;
 
 // Shared-memory map (offsets from the 1024-aligned base).
-constexpr uint32_t S_REC = 0;      // record: Bk | Qg | Khat | Aqk | A (64 KB); Khat -> dD [64 r][128 v]
-constexpr uint32_t REC_QG = 16384, REC_KH = 32768, REC_AQK = 49152, REC_AM = (uint32_t)kTileRecA;
+constexpr uint32_t S_REC = 0;      // record: Bk | Khat | A | Aqk | Qg (64 KB); Khat -> dD [64 r][128 v]
 constexpr uint32_t S_DO = 65536;   // dO [64][128] bf16
 constexpr uint32_t S_DH = 81920;   // dh' [K][V] bf16 (swizzled, 32 KB) -> dX [64 i][128 v]
 constexpr uint32_t S_TILES = 114688;
@@ -100,7 +99,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const float *__restrict__ dhT, fl
     const int len = chunk_span(si, ci).y;
     const size_t slot = (size_t)(si.z + ci) * HV + j;
     // 2^G_last of this thread's key channel, read from the record in global memory
-    const float gaml = reinterpret_cast<const float *>(W.tc_tiles + slot * kTileRecord + 65536)[cown];
+    const float gaml = reinterpret_cast<const float *>(W.tc_tiles + slot * kTileRecord + kRecGAML)[cown];
     {  // dh' -> bf16 operand tile, row-major [c][v]
       unsigned char *DH = sm + S_DH;
 #pragma unroll
@@ -125,10 +124,10 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const float *__restrict__ dhT, fl
       const uint32_t id1 = idesc(128, 64, 1, 1), id2 = idesc(128, 64, 1, 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma(tmem, desc_mn(sbase + S_DO, s, 8192), desc_mn(sbase + S_REC + REC_AQK, s, 8192), id1, s > 0);
+        mma(tmem, desc_mn(sbase + S_DO, s, 8192), desc_mn(sbase + S_REC + kRecAQK, s, 8192), id1, s > 0);
 #pragma unroll
       for (int s = 0; s < 8; ++s)
-        mma(tmem, desc_mn(sbase + S_DH, s, 16384), desc_k16(sbase + S_REC + REC_KH, s, kC), id2, 1);
+        mma(tmem, desc_mn(sbase + S_DH, s, 16384), desc_k16(sbase + S_REC + kRecKH, s, kC), id2, 1);
       commit(bar);
     }
     bar_wait(bar, phase, err);
@@ -140,14 +139,14 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const float *__restrict__ dhT, fl
       tmem_ld32(tq + (uint32_t)r0, d);
 #pragma unroll
       for (int e = 0; e < 32; ++e)
-        *reinterpret_cast<__nv_bfloat16 *>(sm + S_REC + REC_KH + sw_off(r0 + e, v, kC)) = __float2bfloat16_rn(d[e]);
+        *reinterpret_cast<__nv_bfloat16 *>(sm + S_REC + kRecKH + sw_off(r0 + e, v, kC)) = __float2bfloat16_rn(d[e]);
     }
     fence_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
     if (tid == 0) {
-      bulk_store(W.tc_dd + slot * kC * kD, sbase + S_REC + REC_KH, 16384u);  // dD for the per-chunk kernel
+      bulk_store(W.tc_dd + slot * kC * kD, sbase + S_REC + kRecKH, 16384u);  // dD for the per-chunk kernel
       bulk_commit();
       // dh' has left its tile before the product whose completion lets every
       // thread write dX there is issued; dD may still be in flight
@@ -156,7 +155,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const float *__restrict__ dhT, fl
       const uint32_t id = idesc(128, 64, 1, 1);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma(tmem + 64, desc_mn(sbase + S_REC + REC_KH, s, 8192), desc_mn(sbase + S_REC + REC_AM, s, 8192), id, s > 0);
+        mma(tmem + 64, desc_mn(sbase + S_REC + kRecKH, s, 8192), desc_mn(sbase + S_REC + kRecAM, s, 8192), id, s > 0);
       commit(bar);
     }
     bar_wait(bar, phase, err);
@@ -181,7 +180,7 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const float *__restrict__ dhT, fl
       const uint32_t id = idesc(128, 128, 1, 1);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma(tmem + 128, desc_mn(sbase + S_REC + REC_QG, s, 8192), desc_mn(sbase + S_DO, s, 8192), id, s > 0);
+        mma(tmem + 128, desc_mn(sbase + S_REC + kRecQG, s, 8192), desc_mn(sbase + S_DO, s, 8192), id, s > 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
         mma(tmem + 128, desc_mn(sbase + S_REC, s, 8192), desc_mn(sbase + S_DH, s, 8192), id | kNegB, 1);

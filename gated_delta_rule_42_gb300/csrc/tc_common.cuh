@@ -1,7 +1,6 @@
 // Shared pieces of the bf16 tensor-core KDA kernels (K = V = 128, chunk 64):
-// the shared-memory map of the reverse scan, the asynchronous loads and bulk
-// copies, the vectors of per-channel decay factors, and the operand-descriptor
-// helpers.
+// the asynchronous loads and bulk copies, the phase-timing hooks and the
+// operand-descriptor helpers.
 //
 // Every operand tile is 128-byte swizzled (see umma.cuh), so the same bytes
 // serve as a K-major or an MN-major tcgen05 operand and as an ldmatrix source.
@@ -72,25 +71,8 @@ constexpr int kThr = 256;  // 8 warps
 constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile of the per-chunk gradient kernel
 constexpr int kGT = 128;   // row stride of the TMA-loaded gate tile (dense rows)
 
-// shared memory map of the reverse scan (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_KRAW = 0;       // k  [64][128] bf16
-constexpr uint32_t OFF_QRAW = 16384;   // q  [64][128]
-constexpr uint32_t OFF_VRAW = 32768;   // v (forward) or dO (backward) [64][128]
-constexpr uint32_t OFF_GRAW = 49152;   // g -> G  fp32 [64][128] (dense rows: a TMA box)
-constexpr uint32_t OFF_BK = 83968;     // beta k 2^G         [64 r][128 c]
-constexpr uint32_t OFF_QG = 100352;    // q~ 2^G             [64 r][128 c]
-constexpr uint32_t OFF_KH = 116736;    // k 2^(G_last - G)   [64 r][128 c]
-constexpr uint32_t OFF_AQK = 133120;   // Aqk                [64 r][64 i]
-constexpr uint32_t OFF_AM = 141312;    // A = (I + L)^-1     [64 r][64 i]
-constexpr uint32_t OFF_U = 149504;     // 64 KB of per-kernel scratch
-constexpr uint32_t OFF_VEC = 215040;   // fp32 vectors (20 rows of 128)
-constexpr uint32_t OFF_BETA = 225280;  // beta, two buffers of 64 fp32
-constexpr uint32_t OFF_MISC = 225792;  // mbarriers (MMA +0, k/q/g loads +16, v loads +24, output MMA +32), tmem slot +8
-constexpr uint32_t SMEM_BYTES = 225792 + 64 + 1024;  // + alignment slack
+// rows of the per-channel vector table of the per-chunk gradient kernel
 constexpr int V_GL = 0, V_GAML = 1, V_GREF = 2, V_EREF = 6, V_D = 10, V_LAM = 16;
-static_assert(OFF_QG == OFF_BK + 16384 && OFF_KH == OFF_QG + 16384 && OFF_AQK == OFF_KH + 16384 &&
-                  OFF_AM == OFF_AQK + 8192 && OFF_AM - OFF_BK == kTileRecA && OFF_AM + 8192 - OFF_BK == 65536,
-              "the saved tile record is the contiguous Bk .. A region");
 
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");

@@ -36,7 +36,7 @@ using namespace umma;
 using namespace tc;
 
 // Shared-memory map (offsets from the 1024-aligned base).
-constexpr uint32_t S_REC = 0;         // record: Bk | Qg | Khat | Aqk | A (64 KB); Bk -> D^T [128 v][64 r]
+constexpr uint32_t S_REC = 0;         // record: Bk | Khat | A | Aqk | Qg (64 KB; states mode: the first 40 KB); Bk -> D^T [128 v][64 r]
 constexpr uint32_t S_V = 65536;       // v [64][128] bf16 -> X^T [128 v][64 r]
 constexpr uint32_t S_H = 81920;       // h [K][V] bf16 (swizzled) -> output staging [64][128] bf16
 constexpr uint32_t S_TILES = 114688;
@@ -46,7 +46,7 @@ constexpr uint32_t S_SMALL = 320;
 constexpr uint32_t S_SMEM = S_TILES + 1024;
 static_assert(S_SMEM + 1024 <= 233472 / 2, "two CTAs per SM (228 KB, 1 KB reserved per CTA)");
 constexpr uint32_t TMEM_COLS = 256;  // [0,64) X'^T / O^T, [64,128) D^T, [128,256) Khat^T D
-constexpr uint32_t REC_QG = 16384, REC_KH = 32768, REC_AQK = 49152, REC_AM = (uint32_t)kTileRecA;
+
 
 struct FwdArgs {
   __nv_bfloat16 *o;   // [B*T][HV][V] or null
@@ -75,6 +75,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
   const int cown = quarter * 32 + lane;  // key channel (state) or value column (X, D, O): the TMEM lane
   const int r0 = 32 * vhalf;             // the token columns this thread's epilogues cover
   const int4 si = W.seq[n];
+  constexpr uint32_t kRecBytes = kOut ? 65536u : kRecStates;  // the states pass needs Bk, Khat and A only
 
   if (tid == 0) {
     bar_init(bar, 1);
@@ -105,8 +106,8 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
   if (si.w > 0) {  // chunk 0: record and v (one thread, on bar_ld), beta (cp.async)
     const int2 ch0 = chunk_span(si, 0);
     if (tid == 0) {
-      mbar_expect_tx(bar_ld, 65536u + 16384u);
-      bulk_load(sbase + S_REC, W.tc_tiles + ((size_t)si.z * HV + j) * kTileRecord, 65536u, bar_ld);
+      mbar_expect_tx(bar_ld, kRecBytes + 16384u);
+      bulk_load(sbase + S_REC, W.tc_tiles + ((size_t)si.z * HV + j) * kTileRecord, kRecBytes, bar_ld);
       tma_tile(sbase + S_V, &maps.v, j, ch0.x, bar_ld);
     }
     load_beta(P, beta, ch0.x, ch0.y, j);
@@ -119,7 +120,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     const size_t slot = (size_t)(si.z + ci) * HV + j;
     // 2^G_last of this thread's key channel, read from the record in global memory
     // (needed only at the state update, so the load latency hides behind the chain)
-    const float gaml = reinterpret_cast<const float *>(W.tc_tiles + slot * kTileRecord + 65536)[cown];
+    const float gaml = reinterpret_cast<const float *>(W.tc_tiles + slot * kTileRecord + kRecGAML)[cown];
     {  // h -> bf16 operand tile, row-major [c][v]
       unsigned char *H = sm + S_H;
 #pragma unroll
@@ -185,7 +186,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
       const uint32_t id = idesc(128, 64, 0, 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma(tmem + 64, desc_k16(sbase + S_V, s, kD), desc_k16(sbase + S_REC + REC_AM, s, kC), id, s > 0);
+        mma(tmem + 64, desc_k16(sbase + S_V, s, kD), desc_k16(sbase + S_REC + kRecAM, s, kC), id, s > 0);
       commit(bar);
     }
     bar_wait(bar, phase, args.err);
@@ -218,16 +219,16 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
       const uint32_t id3 = idesc(128, 128, 1, 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma(tmem + 128, desc_mn(sbase + S_REC + REC_KH, s, 8192), desc_k16(sbase + S_REC, s, kD), id3, s > 0);
+        mma(tmem + 128, desc_mn(sbase + S_REC + kRecKH, s, 8192), desc_k16(sbase + S_REC, s, kD), id3, s > 0);
       commit(bar);
       if (kOut) {  // O^T[v][r] = sum_c h[c][v] Qg[r][c] + sum_i D^T[v][i] Aqk[r][i], while the state updates
         const uint32_t id = idesc(128, 64, 1, 0), id2 = idesc(128, 64, 0, 0);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma(tmem, desc_mn(sbase + S_H, s, 16384), desc_k16(sbase + S_REC + REC_QG, s, kC), id, s > 0);
+          mma(tmem, desc_mn(sbase + S_H, s, 16384), desc_k16(sbase + S_REC + kRecQG, s, kC), id, s > 0);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma(tmem, desc_k16(sbase + S_REC, s, kD), desc_k16(sbase + S_REC + REC_AQK, s, kC), id2, 1);
+          mma(tmem, desc_k16(sbase + S_REC, s, kD), desc_k16(sbase + S_REC + kRecAQK, s, kC), id2, 1);
         commit(bar_o);
       }
     }
@@ -244,8 +245,8 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
       const int2 nx = chunk_span(si, ci + 1);
       if (tid == 0) {
         if (!kOut) bulk_wait_read();  // h_c, X^T, D^T have left shared memory
-        mbar_expect_tx(bar_ld, 65536u + 16384u);
-        bulk_load(sbase + S_REC, W.tc_tiles + (slot + HV) * kTileRecord, 65536u, bar_ld);
+        mbar_expect_tx(bar_ld, kRecBytes + 16384u);
+        bulk_load(sbase + S_REC, W.tc_tiles + (slot + HV) * kTileRecord, kRecBytes, bar_ld);
         tma_tile(sbase + S_V, &maps.v, j, nx.x, bar_ld);
       }
       load_beta(P, beta, nx.x, nx.y, j);

@@ -51,9 +51,6 @@ static_assert(P_SMEM + 1024 <= 233472 / 3, "three CTAs per SM (228 KB, 1 KB rese
 // vector rows: block references G_ref(R), 2^G_ref(R), 2^(G_last - G_ref(R)), and
 // the block-pair factors D_RI = 2^(G_ref(R) - G_ref(I)) for R > I
 constexpr int W_GREF = 0, W_EREF = 4, W_LAM = 8, W_D = 12;
-// record layout: Bk 0, Qg 16384, Khat 32768, Aqk 49152, A 57344, 2^G_last 65536
-constexpr uint32_t REC_QG = 16384, REC_KH = 32768, REC_AQK = 49152, REC_AM = 57344, REC_GAML = 65536;
-static_assert(REC_AM == (uint32_t)kTileRecA && REC_GAML + 512 == (uint32_t)kTileRecord, "record layout");
 
 // fp32 [64][64] scratch (L, then A): columns XOR-swizzled by 4 * (row % 8), so
 // reads of one column across 8 rows and float4 reads of four consecutive
@@ -106,7 +103,7 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
 #pragma unroll
     for (int r = 0; r < kC; ++r) G[r * kGT + c] = col[r];
     const float gl = s;
-    reinterpret_cast<float *>(rec + REC_GAML)[c] = exp2f(gl);
+    reinterpret_cast<float *>(rec + kRecGAML)[c] = exp2f(gl);
     float gref[4];
 #pragma unroll
     for (int R = 0; R < 4; ++R) {  // block references: rows 0, 16, 32, 48 (the chunk end past len)
@@ -160,16 +157,16 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       kc[rr] = pack8(o);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * e1[e] * eref[e];
-      *reinterpret_cast<uint4 *>(rec + off) = pack8(o);  // Bk
+      *reinterpret_cast<uint4 *>(rec + kRecBK + off) = pack8(o);  // Bk
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e] * lam[e];
-      *reinterpret_cast<uint4 *>(rec + REC_KH + off) = pack8(o);  // Khat
+      *reinterpret_cast<uint4 *>(rec + kRecKH + off) = pack8(o);  // Khat
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
       *reinterpret_cast<uint4 *>(sm + P_Q + off) = pack8(o);  // Qr, in place of q
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] *= eref[e];
-      *reinterpret_cast<uint4 *>(rec + REC_QG + off) = pack8(o);  // Qg
+      *reinterpret_cast<uint4 *>(rec + kRecQG + off) = pack8(o);  // Qg
     }
     __syncthreads();  // G is dead: its upper half takes Kc
 #pragma unroll
@@ -231,14 +228,14 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, un
         *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
         const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
         const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
-        *reinterpret_cast<uint32_t *>(rec + REC_AQK + sw_off(r, i, kC)) = pack_bf16(a0, a1);
+        *reinterpret_cast<uint32_t *>(rec + kRecAQK + sw_off(r, i, kC)) = pack_bf16(a0, a1);
       }
     }
   }
   if (tid < 6 * 32) {  // Aqk blocks above the diagonal (R < I) are zero
     const int b = tid >> 5, w = tid & 31;
     const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
-    *reinterpret_cast<uint4 *>(rec + REC_AQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4 *>(rec + kRecAQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   KDA_PT(4);
@@ -350,7 +347,7 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, un
     float x[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) x[t] = Af[fsw(r, jj * 8 + t)];
-    *reinterpret_cast<uint4 *>(rec + REC_AM + sw_chunk(r, jj, kC)) = pack8(x);
+    *reinterpret_cast<uint4 *>(rec + kRecAM + sw_chunk(r, jj, kC)) = pack8(x);
   }
 }
 
