@@ -206,6 +206,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
   }
   cp_commit();
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  KDA_PT(13);
   bar_wait(bar_ld, 0, args.err);
   if (len < kC)  // dO rows past the sequence end hold other tokens: clear them
     for (int it = tid; it < (kC - len) * 16; it += kCT) {
@@ -217,6 +218,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
   fence_before();
   __syncthreads();
   fence_after();
+  KDA_PT(14);
   const uint32_t tmem = *tslot;
   const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
 
@@ -236,9 +238,10 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       mma(tmem + 384, desc_mn(sbase + I_XT, k, 16384), desc_k16(sbase + I_STK + 64 * 128, k, 192), id5, k > 0);
     commit(bar);
   }
-  // meanwhile on the SIMT cores: d(2^G_last)[c] = sum_v dh'[c][v] h[c][v]; dv = beta dX; sum_v dX v
-  if (tid < kD) {
-    const int c = tid;
+  // meanwhile on the other warps (warp 0 only issues the products): warps 4..7
+  // d(2^G_last)[c] = sum_v dh'[c][v] h[c][v]; warps 1..3, 8..15 dv = beta dX and sum_v dX v
+  if (warp >= 4 && warp < 8) {
+    const int c = tid - kD;
     float acc = 0.f;
 #pragma unroll 4
     for (int jj = 0; jj < 16; ++jj) {
@@ -250,7 +253,8 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     }
     red[64 + c] = acc;
   }
-  for (int r = warp; r < kC; r += kCT / 32) {  // one warp per row, 4 columns per lane
+  const int rw = warp < 4 ? warp - 1 : warp - 5;  // 0..10 on warps 1..3 and 8..15
+  for (int r = rw; warp != 0 && (warp < 4 || warp >= 8) && r < kC; r += 11) {  // one warp per row, 4 columns per lane
     float part = 0.f;
     if (r < len) {
       const float br = beta[r];
@@ -266,6 +270,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     }
     if (lane == 0) red[r] = part;
   }
+  KDA_PT(15);
   bar_wait(bar, 0, args.err);
   fence_after();
   __syncthreads();  // products in TMEM; the operand tiles are dead
