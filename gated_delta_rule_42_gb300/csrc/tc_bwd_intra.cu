@@ -66,22 +66,17 @@ constexpr uint32_t C_RED = 217344;    // sum_v dX v [64], d(2^G_last) [128]
 constexpr uint32_t C_MISC = 218112;   // mbarrier, tmem slot
 constexpr uint32_t C_SMEM = 218176 + 1024;
 constexpr uint32_t LO128 = 16384, LO64 = 8192;
-constexpr uint32_t TMEM_COLS = 512;   // [128,256) S, [256,320) dKhat^T, [384,512) Z
-// Assembly scratch in the dead dL .. T tiles: the products of one pass (32
-// columns: 8 per column quarter) read out of TMEM as [64][32] fp32 tiles with
-// 16-byte chunks XOR-swizzled by row % 8, double-buffered, and the segment and
-// block totals of the final dg column scan.  dG itself is parked in the Kr / Qr
-// tiles: once a thread has read its Kr, Qr (hi and lo) at (r, c..c+1), the
-// 8 bytes of each pair slot hold dG's Q and P parts of (r, c) and (r, c+1).
-constexpr uint32_t ST_BYTES = 64 * 32 * 4;          // one staged [64][32] product
-constexpr uint32_t C_ST0 = C_DAB;                   // pass buffer 0: dQg | dBk | dKhat (24 KB)
-constexpr uint32_t C_ST1 = C_ST0 + 3 * ST_BYTES;    // pass buffer 1
-constexpr uint32_t C_TOT = C_ST1 + 3 * ST_BYTES;    // totals of Q, P [4 segments][128]; Khat column term [4 blocks][128]
+// Tensor memory: the per-chunk products that the assembly reads element-wise are
+// M = 64 accumulators, whose 16-row block R sits in lanes 0..15 of lane quarter R:
+// a warp of quarter R reads its 16 x 8 blocks straight in mma C-fragment order
+// (tcgen05.ld .16x256b).  Z (M = 128) feeds the dA split only.
+constexpr uint32_t TMEM_COLS = 512;   // [0,128) dX h^T, [128,256) dO h^T, [256,384) dKhat, [384,512) Z
+// Assembly scratch in the dead dL .. T tiles: the segment and block totals of the
+// final dg column scan.  dG itself is parked in the Kr / Qr tiles: once a thread
+// has read its Kr, Qr (hi and lo) at (r, c..c+1), the 8 bytes of each pair slot
+// hold dG's Q and P parts of (r, c) and (r, c+1).
+constexpr uint32_t C_TOT = C_DAB;     // totals of Q, P [4 segments][128]; Khat column term [4 blocks][128]
 static_assert(C_TOT + 3 * 4 * 128 * 4 <= C_G, "assembly scratch overflows the chain tiles");
-// byte offset of element (r, c) of a staged [64][32] product
-__device__ __forceinline__ uint32_t st_off(int r, int c) {
-  return (uint32_t)r * 128u + ((uint32_t)((c >> 2) ^ (r & 7)) << 4) + (uint32_t)(c & 3) * 4u;
-}
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct IntraArgs {
@@ -224,14 +219,17 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 
   // ---- tensor-core products ----
   if (tid == 0) {
-    // S[i'][c] = sum_v [dX; dO][i'][v] h[c][v]   (M=128, N=128 c, K=128 v)
-    const uint32_t id3 = idesc(128, 128, 0, 0);
+    // (dX h^T)[r][c] = sum_v dX[r][v] h[c][v] and (dO h^T)[r][c]   (M=64 r, N=128 c, K=128 v)
+    const uint32_t id3 = idesc(64, 128, 0, 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mma(tmem + 128, desc_k16(sbase + I_STK, k, 192), desc_k16(sbase + I_H, k, kD), id3, k > 0);
-    // dKhat^T[c][r] = sum_v dh'[c][v] D[r][v]   (M=128 c, N=64 r, K=128 v)
-    const uint32_t id4 = idesc(128, 64, 0, 1), id5 = idesc(128, 128, 1, 0);
+    for (int k = 0; k < 8; ++k) mma(tmem, desc_k16(sbase + I_STK, k, 192), desc_k16(sbase + I_H, k, kD), id3, k > 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mma(tmem + 256, desc_k16(sbase + I_DH, k, kD), desc_mn(sbase + I_DT, k, 8192), id4, k > 0);
+    for (int k = 0; k < 8; ++k)
+      mma(tmem + 128, desc_k16(sbase + I_STK + 64 * 128, k, 192), desc_k16(sbase + I_H, k, kD), id3, k > 0);
+    // dKhat[r][c] = sum_v D[r][v] dh'[c][v]   (M=64 r, N=128 c, K=128 v)
+    const uint32_t id4 = idesc(64, 128, 1, 0), id5 = idesc(128, 128, 1, 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mma(tmem + 256, desc_mn(sbase + I_DT, k, 8192), desc_k16(sbase + I_DH, k, kD), id4, k > 0);
     // Z[i'][n'] = sum_v [X; D][i'][v] [dO; dD][n'][v]   (M=128, N=128, K=128 v)
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -456,7 +454,8 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
   // ---- pairwise chains: warp owns rows 16B..16B+15 (as r and as i), columns ch0 .. ch0+31 ----
   // Block-pair products are formed in a temporary, scaled by the per-channel
   // factor D_RI in fp32, and added to the accumulators.
-  const int Bk = warp >> 2, ch0 = 32 * (warp & 3);
+  // (row block = the warp's TMEM lane quarter, so that the assembly reads its products from TMEM)
+  const int Bk = warp & 3, ch0 = 32 * (warp >> 2);
   float xr[4][4] = {}, yr[4][4] = {}, xyi[4][4] = {};  // xyi = xi + yi (only their sum is used)
   for (int I = 0; I <= Bk; ++I) {  // row side: R = Bk, I = 0..Bk
     const float *Dv = (I < Bk) ? vec + (V_D + Bk * (Bk - 1) / 2 + I) * kD : nullptr;
@@ -514,52 +513,28 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
   KDA_PT(5);
 
   // ---- assembly (fragment element (r, c)), in four passes of 8 columns per warp ----
-  // Each pass reads its 32 columns (8 per column quarter) of dQg, dBk and
-  // dKhat out of TMEM into a swizzled shared-memory tile (two buffers: pass
-  // g + 2 is staged once pass g is done).  Raw k and q are not re-read: every
-  // term that needs them is a product with a decay factor that the hi/lo
-  // tiles Kr = k e1, Qr = q~ e1, Kc = k e2 hold.  dg = reverse cumsum of dG
-  // over the chunk runs once, after the last pass, as column scans over
-  // 16-row segments with segment totals exchanged in shared memory.
-  auto stage = [&](int g) {
-    const int cg = warp >> 2;  // column quarter of this warp (8 columns of the pass)
-    const uint32_t buf = (g & 1) ? C_ST1 : C_ST0;
-    {  // S: lane quarters 0, 1 = -dBk rows, 2, 3 = dQg rows
-      float x[8];
-      tmem_ld8(tq + 128u + (uint32_t)(32 * cg + 8 * g), x);
-      const int r = 32 * (quarter & 1) + lane;
-      const bool isq = quarter >= 2;
-      const float sg = isq ? 1.f : -1.f;
-      unsigned char *dst = sm + buf + (isq ? 0u : ST_BYTES);
-      *reinterpret_cast<float4 *>(dst + st_off(r, 8 * cg)) = make_float4(sg * x[0], sg * x[1], sg * x[2], sg * x[3]);
-      *reinterpret_cast<float4 *>(dst + st_off(r, 8 * cg + 4)) = make_float4(sg * x[4], sg * x[5], sg * x[6], sg * x[7]);
-    }
-    {  // dKhat^T: lane c (this quarter), columns r = 16 cg .. 16 cg + 15; lanes 8 g .. 8 g + 7 hold the pass
-      float x[16];
-      tmem_ld16(tq + 256u + (uint32_t)(16 * cg), x);
-      if ((lane >> 3) == g) {
-        const int lc = 8 * quarter + (lane & 7);
-        unsigned char *dst = sm + buf + 2 * ST_BYTES;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) *reinterpret_cast<float *>(dst + st_off(16 * cg + e, lc)) = x[e];
-      }
-    }
-  };
+  // Each pass reads this warp's 16 x 8 blocks of dX h^T (= -dBk), dO h^T (= dQg)
+  // and dKhat straight out of tensor memory, in the C-fragment order of the
+  // chain accumulators.  Raw k and q are not re-read: every term that needs them
+  // is a product with a decay factor that the hi/lo tiles Kr = k e1, Qr = q~ e1,
+  // Kc = k e2 hold.  dg = reverse cumsum of dG over the chunk runs once, after
+  // the last pass, as column scans over 16-row segments with segment totals
+  // exchanged in shared memory.
   float *totQ = (float *)(sm + C_TOT), *totP = totQ + 4 * kD, *totC = totP + 4 * kD;
   const float *dglv = red + 64;
   const int i8 = lane >> 2, l4 = lane & 3;
   float bpart[2] = {0.f, 0.f};
-  stage(0);
-  stage(1);
-  __syncthreads();
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     KDA_PT(9);
-    const uint32_t bq = (g & 1) ? C_ST1 : C_ST0, bb = bq + ST_BYTES, bk = bq + 2 * ST_BYTES;
     {
       const int nt = g;
       const int c = ch0 + 8 * nt + 2 * l4;
-      const int lc = 8 * (warp & 3) + 2 * l4;  // column in the staging
+      float px[4], po[4], pk[4];  // element (i8 + 8 hh, c + u) at index 2 hh + u
+      {
+        const uint32_t tb = tmem + ((uint32_t)(32 * Bk) << 16) + (uint32_t)(ch0 + 8 * nt);
+        tmem_ld_frag3(tb, tb + 128u, tb + 256u, px, po, pk);
+      }
       const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
       const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
       const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
@@ -568,10 +543,9 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       for (int hh = 0; hh < 2; ++hh) {
         const int r = 16 * Bk + i8 + 8 * hh;
         const float br = beta[r];
-        const uint32_t so = st_off(r, lc);
-        const float2 vq = *reinterpret_cast<const float2 *>(sm + bq + so);
-        const float2 vb = *reinterpret_cast<const float2 *>(sm + bb + so);
-        const float2 vk = *reinterpret_cast<const float2 *>(sm + bk + so);
+        const float2 vq = make_float2(po[2 * hh], po[2 * hh + 1]);
+        const float2 vb = make_float2(-px[2 * hh], -px[2 * hh + 1]);
+        const float2 vk = make_float2(pk[2 * hh], pk[2 * hh + 1]);
         const uint32_t to = sw_off(r, c, kC);
         uint32_t *krh_p = reinterpret_cast<uint32_t *>(sm + C_KR + to), *krl_p = reinterpret_cast<uint32_t *>(sm + C_KR + LO128 + to);
         uint32_t *qrh_p = reinterpret_cast<uint32_t *>(sm + C_QR + to), *qrl_p = reinterpret_cast<uint32_t *>(sm + C_QR + LO128 + to);
@@ -631,10 +605,9 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       }
     }
     KDA_PT(10);
-    __syncthreads();  // the staged products of pass g consumed
-    if (g + 2 < 4) stage(g + 2);
-    KDA_PT(11);
   }
+  __syncthreads();  // every thread has parked its dG and its Khat column terms
+  KDA_PT(11);
   {  // dg = reverse cumsum of dG: thread = one column, one 16-row segment (4 segments)
     const int c = tid & (kD - 1), seg = tid >> 7, mid = len >> 1;
     // element (r, c) of the parked dG: even c in the hi slot of its pair, odd c in the lo slot
@@ -685,7 +658,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     float v = bpart[hh];
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
-    if (l4 == 0) rb[(warp & 3) * kC + 16 * Bk + i8 + 8 * hh] = v;
+    if (l4 == 0) rb[(warp >> 2) * kC + 16 * Bk + i8 + 8 * hh] = v;
   }
   __syncthreads();
   KDA_PT(7);

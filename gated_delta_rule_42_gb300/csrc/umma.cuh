@@ -141,6 +141,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Three 16-lane x 8-column blocks of fp32 accumulators (lane base: the warp's
+// quarter, + column offsets a0, a1, a2) in mma.sync C-fragment order: thread t
+// gets (lane t/4, columns 2(t%4), 2(t%4)+1) then (lane t/4 + 8, the same columns).
+__device__ __forceinline__ void tmem_ld_frag3(uint32_t a0, uint32_t a1, uint32_t a2, float (&x)[4], float (&y)[4],
+                                              float (&z)[4]) {
+  uint32_t r[12];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%12];\n"
+      "tcgen05.ld.sync.aligned.16x256b.x1.b32 {%4,%5,%6,%7}, [%13];\n"
+      "tcgen05.ld.sync.aligned.16x256b.x1.b32 {%8,%9,%10,%11}, [%14];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11])
+      : "r"(a0), "r"(a1), "r"(a2)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[i] = __uint_as_float(r[i]);
+    y[i] = __uint_as_float(r[4 + i]);
+    z[i] = __uint_as_float(r[8 + i]);
+  }
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
