@@ -76,12 +76,13 @@ def kernel_bytes_per_token(name, cfg):
     hs = 2 * HV * K * V / 64            # bf16 K x V state per chunk, per token
     t16 = 16384 * HV / 64               # one 16 KB per-chunk tile (X^T or D^T), per token
     rec = (65536 + 512) * HV / 64       # the per-chunk tile record (Bk, Qg, Khat, Aqk, A, 2^G_last), per token
+    recs = (40960 + 512) * HV / 64      # what the states pass reads of it (Bk, Khat, A, 2^G_last)
     dgl = 4 * HV * K / 64               # fp32 K-vector per chunk, per token
     table = {
         # tensor-core path (bf16, K = V = 128)
         "kda_prep_tc": 2 * qk + g + b + rec,
         "kda_fwd_tc": rec + 2 * vv,
-        "kda_fwd_tc_states": rec + vv + hs + 2 * t16,
+        "kda_fwd_tc_states": recs + vv + hs + 2 * t16,
         "kda_bwd_scan_tc": rec + vv + hs + 2 * vv,
         "kda_bwd_intra_tc": 2 * t16 + 2 * hs + 3 * vv + vv + b + g + t16 / 2 + 2 * qk + vv + 2 * qk + g + b,
         # fp32 path
@@ -106,10 +107,10 @@ def kernel_bytes_per_token(name, cfg):
 # value is reported only while those sources are unchanged.
 NCU_TRAFFIC = {
     "kda_bwd_intra_tc": dict(
-        bytes_per_token=1292881664 / 8192,  # 980.8 MB read + 312.0 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=1292057344 / 8192,  # 980.4 MB read + 311.7 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_intra.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh",
                  "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="8534f9a19489cd7af083b99416613443ec2b7d8dfb337e891c220842a307f414",
+        sha256="c8663d53ee092f2f8b3e581d610e1df14df3ce485d2312a4c88bcac4cfaf3b94",
         profile="profiles/ncu_full_kernels_B8_T1024_H32_K128.md"),
 }
 
