@@ -252,6 +252,8 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
   if (P.Ttot > 0 && (dO == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
                      dg == nullptr || dbeta == nullptr))
     return fail(KDA_ERR_INVALID_ARG, "dO, dq, dk, dv, dg and dbeta are required");
+  if (use_tc(P) && ((uintptr_t)dO & 15) != 0)
+    return fail(KDA_ERR_INVALID_ARG, "dO must be 16-byte aligned (bf16, K = V = 128 path)");
   const size_t need = layout(P, true, nullptr, nullptr);
   if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
   if (P.N == 0) return KDA_OK;

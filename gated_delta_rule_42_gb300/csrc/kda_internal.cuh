@@ -154,6 +154,11 @@ cudaError_t launch_gate_grad_reduce(const Problem &P, const float *dgx, float *d
 cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                 cudaStream_t s);
 // true when the tensor-core kernels handle this problem
-inline bool tc_eligible(const Problem &P) { return P.bf16 && P.K == 128 && P.V == 128; }
+// The tensor-core kernels: bf16, K = V = 128, and q, k, v (and a per-channel g)
+// 16-byte aligned, since they arrive by TMA; other problems run the fp32 kernels.
+inline bool tc_eligible(const Problem &P) {
+  const uintptr_t a = (uintptr_t)P.q | (uintptr_t)P.k | (uintptr_t)P.v | (P.scalar_gate ? 0 : (uintptr_t)P.g);
+  return P.bf16 && P.K == 128 && P.V == 128 && (a & 15) == 0;
+}
 
 }  // namespace kda

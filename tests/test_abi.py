@@ -123,3 +123,14 @@ def test_state_compose_validation(lib, args, status):
     a.update(args)
     st = lib.kda_state_compose(a["M"], a["h"], a["c"], a["out"], a["count"], a["K"], a["V"], a["transpose"], None)
     assert st == status, lib.kda_last_error()
+
+
+def test_misaligned_dO_on_the_tensor_core_path_is_rejected(lib):
+    """bf16, K = V = 128 with aligned q, k, v, g selects the tensor-core kernels,
+    whose TMA loads need a 16-byte aligned dO: rejected before any launch."""
+    s = _inputs(K=128, V=128)
+    fake = [ctypes.c_void_p(0x200000 + 0x1000 * i) for i in range(6)]
+    st = lib.kda_chunk_bwd(ctypes.byref(s), ctypes.c_void_p(0x100002), None, *fake[:5], None,
+                           ctypes.c_void_p(0x10000), 1 << 30, None)
+    assert st == _lib.KDA_ERR_INVALID_ARG, lib.kda_last_error()
+    assert b"aligned" in lib.kda_last_error()

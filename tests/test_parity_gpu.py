@@ -239,3 +239,35 @@ def test_scalar_gate_recurrent(dtype):
     o, hT = H.gpu_recurrent(inp)
     ro, rhT = H.oracle_fwd(inp)
     H.check_fwd(inp, o, hT, ro, rhT, H.TOL[dtype]["fwd"])
+
+
+def _misaligned(t):
+    """A device copy of t whose data starts one element past a 256-byte boundary."""
+    buf = torch.empty(t.numel() + 16, dtype=t.dtype, device="cuda")
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def test_misaligned_bf16_inputs_run_the_general_kernels():
+    """bf16 K = V = 128 inputs that are not 16-byte aligned cannot use the TMA
+    kernels: the general kernels run instead, with the same results."""
+    import ctypes
+    from gated_delta_rule_42_gb300 import _lib
+    from gated_delta_rule_42_gb300.ops import make_inputs_struct
+    inp = inputs.make_inputs(B=1, T=150, H=1, HV=2, K=128, V=128, dtype=torch.bfloat16, seed=23, name="misaligned")
+    lib = _lib.load()
+    q, k, v, g = (_misaligned(x) for x in (inp.q, inp.k, inp.v, inp.g))
+    beta, h0 = inp.beta.cuda(), inp.h0.cuda()
+    assert (q.data_ptr() & 15) != 0
+    s = make_inputs_struct(q, k, v, g, beta, h0, None)
+    o = torch.full(v.shape, float("nan"), dtype=v.dtype, device="cuda")
+    hT = torch.empty((s.N, s.HV, 128, 128), dtype=torch.float32, device="cuda")
+    need = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s))
+    ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    wp = ctypes.c_void_p((ws.data_ptr() + 255) & ~255)
+    _lib.check(lib, lib.kda_chunk_fwd(ctypes.byref(s), ctypes.c_void_p(o.data_ptr()), ctypes.c_void_p(hT.data_ptr()),
+                                      wp, need, None))
+    torch.cuda.synchronize()
+    ro, rhT = H.oracle_fwd(inp)
+    H.check_fwd(inp, o.cpu(), hT.cpu(), ro, rhT, H.TOL[torch.bfloat16]["fwd"])
