@@ -85,9 +85,6 @@ __device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_grou
 __device__ __forceinline__ void st_zero16(uint32_t dst) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};\n" ::"r"(dst), "r"(0u) : "memory");
 }
-__device__ __forceinline__ void st_bf2(unsigned char *tile, int r, int c, int R, float a, float b) {
-  *reinterpret_cast<uint32_t *>(tile + sw_off(r, c, R)) = pack_bf16(a, b);
-}
 __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
   return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                     pack_bf16(x[6], x[7]));
@@ -113,19 +110,8 @@ __device__ __forceinline__ uint32_t idesc(int M, int N, int a_mn, int b_mn) {
   return idesc_bf16(M, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
 }
 
-// Asynchronous loads of one chunk's rows of a [tokens][heads][128] bf16
-// tensor into a swizzled [64][128] tile; rows at or past len are zeroed.
-template <int NT = kThr>
-__device__ __forceinline__ void load_rows(uint32_t tile, const __nv_bfloat16 *src, int t0, int len,
-                                          int heads, int head) {
-  for (int it = threadIdx.x; it < kC * 16; it += NT) {
-    const int r = it >> 4, jj = it & 15;
-    const uint32_t dst = tile + sw_chunk(r, jj, kC);
-    if (r < len) cp16(dst, src + ((size_t)(t0 + r) * heads + head) * kD + jj * 8);
-    else st_zero16(dst);
-  }
-}
-
+// Asynchronous loads of one chunk's gate rows ([tokens][HV][128] fp32) into a
+// [64][kGLD] tile; rows at or past len are zeroed.
 template <int NT = kThr>
 __device__ __forceinline__ void load_gate(uint32_t tile, const float *g, int t0, int len, int HV, int j) {
   for (int it = threadIdx.x; it < kC * 32; it += NT) {
