@@ -1,7 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark: chunked KDA forward + backward on one GB300 (or N replicas).
 
-One step = kda_chunk_fwd + kda_chunk_bwd through the C ABI on the dense
+One step = kda_chunk_fwd_ctx + kda_chunk_bwd_ctx (the backward reads the
+intermediates the forward kept; --recompute: kda_chunk_fwd + kda_chunk_bwd,
+the backward recomputes them) through the C ABI on the dense
 training layer (B=8, T=4096, H=HV=32, K=V=128, bf16 q/k/v, fp32 g/beta, no
 initial or final state), inputs resident in HBM.  Prints one JSON line.
 
@@ -83,6 +85,7 @@ def kernel_bytes_per_token(name, cfg):
         "kda_prep_tc": 2 * qk + g + b + rec,
         "kda_fwd_tc": rec + 2 * vv,
         "kda_fwd_tc_states": recs + vv + hs + 2 * t16,
+        "kda_fwd_tc_save": rec + 2 * vv + hs + 2 * t16,
         "kda_bwd_scan_tc": rec + vv + hs + 2 * vv,
         "kda_bwd_intra_tc": 2 * t16 + 2 * hs + 3 * vv + vv + b + g + t16 / 2 + 2 * qk + vv + 2 * qk + g + b,
         # fp32 path
@@ -201,9 +204,12 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------
 class Runner:
-    """Preallocated device buffers and the two C-ABI calls of one step."""
+    """Preallocated device buffers and the two C-ABI calls of one step: the
+    forward-context pair (kda_chunk_fwd_ctx, kda_chunk_bwd_ctx: the backward
+    reads what the forward kept) or, with keep_context=False, the recompute
+    pair (kda_chunk_fwd, kda_chunk_bwd)."""
 
-    def __init__(self, cfg, device, qk_l2norm=False):
+    def __init__(self, cfg, device, qk_l2norm=False, keep_context=True):
         self.lib = _lib.load()
         self.cfg = cfg
         self.dev = device
@@ -217,12 +223,23 @@ class Runner:
         self.dq, self.dk, self.dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
         self.dg, self.db = torch.empty_like(d.g), torch.empty_like(d.beta)
         self.dh0 = torch.empty_like(d.h0) if d.h0 is not None else None
-        need = max(self.lib.kda_chunk_fwd_workspace_size(ctypes.byref(s)),
-                   self.lib.kda_chunk_bwd_workspace_size(ctypes.byref(s)))
+        lib = self.lib
+        self.keep_context = keep_context
+        if keep_context:
+            need = max(lib.kda_chunk_fwd_ctx_workspace_size(ctypes.byref(s)),
+                       lib.kda_chunk_bwd_ctx_workspace_size(ctypes.byref(s)))
+            self.ctx_bytes = lib.kda_chunk_ctx_size(ctypes.byref(s))
+        else:
+            need = max(lib.kda_chunk_fwd_workspace_size(ctypes.byref(s)),
+                       lib.kda_chunk_bwd_workspace_size(ctypes.byref(s)))
+            self.ctx_bytes = 0
         self.ws = torch.empty(need + 256, dtype=torch.uint8, device=device)
         p = self.ws.data_ptr()
         self.wp = ctypes.c_void_p((p + 255) & ~255)
         self.wb = need
+        self.ctx = torch.empty(self.ctx_bytes + 256, dtype=torch.uint8, device=device)
+        p = self.ctx.data_ptr()
+        self.cp = ctypes.c_void_p((p + 255) & ~255) if self.ctx_bytes else None
         self.stream = torch.cuda.current_stream(device)
         self.sp = ctypes.c_void_p(self.stream.cuda_stream)
 
@@ -232,13 +249,20 @@ class Runner:
 
     def fwd(self):
         p, lib, s = self._p, self.lib, self.s
-        _lib.check(lib, lib.kda_chunk_fwd(ctypes.byref(s), p(self.o), p(self.hT), self.wp, self.wb, self.sp))
+        if self.keep_context:
+            _lib.check(lib, lib.kda_chunk_fwd_ctx(ctypes.byref(s), p(self.o), p(self.hT), self.cp, self.ctx_bytes,
+                                                  self.wp, self.wb, self.sp))
+        else:
+            _lib.check(lib, lib.kda_chunk_fwd(ctypes.byref(s), p(self.o), p(self.hT), self.wp, self.wb, self.sp))
 
     def bwd(self):
         p, lib, s = self._p, self.lib, self.s
-        _lib.check(lib, lib.kda_chunk_bwd(ctypes.byref(s), p(self.d.do), p(self.d.dhT), p(self.dq), p(self.dk),
-                                          p(self.dv), p(self.dg), p(self.db), p(self.dh0), self.wp, self.wb,
-                                          self.sp))
+        grads = (p(self.d.do), p(self.d.dhT), p(self.dq), p(self.dk), p(self.dv), p(self.dg), p(self.db),
+                 p(self.dh0), self.wp, self.wb, self.sp)
+        if self.keep_context:
+            _lib.check(lib, lib.kda_chunk_bwd_ctx(ctypes.byref(s), self.cp, self.ctx_bytes, *grads))
+        else:
+            _lib.check(lib, lib.kda_chunk_bwd(ctypes.byref(s), *grads))
 
     def step(self):
         self.fwd()
@@ -307,7 +331,7 @@ def e2e_measure(cfg, runner, steps, qk_l2norm=False):
             host_in[k] = getattr(cfg, k).pin_memory()
     s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     with torch.cuda.stream(s_cmp):
-        runners = [runner, Runner(cfg, dev, qk_l2norm=qk_l2norm)]
+        runners = [runner, Runner(cfg, dev, qk_l2norm=qk_l2norm, keep_context=runner.keep_context)]
     for r in runners:
         r.sp = ctypes.c_void_p(s_cmp.cuda_stream)
 
@@ -455,6 +479,11 @@ def main():
     ap.add_argument("--cp-ranks", type=int, default=0,
                     help="context parallelism: split every sequence into this many segments and run the state "
                          "relay, the ranks serialized on this GPU (measures the relay's per-rank work)")
+    ap.add_argument("--recompute", action="store_true",
+                    help="time the recompute pair (kda_chunk_fwd + kda_chunk_bwd) instead of the forward-context "
+                         "pair: the backward re-runs the record kernel and the states pass")
+    ap.add_argument("--no-compare", action="store_true",
+                    help="skip timing the other backward mode (profiling aid: only this mode's kernels launch)")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="profiling aid: the dense workload with T replaced (e.g. 1024 for small ncu captures); "
                          "the JSON line names the changed workload")
@@ -490,7 +519,7 @@ def main():
         cfg = inputs.make_inputs(seed=1000 + args.config + 7919 * rank, name=name, **kw)
     else:
         cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
-    runner = Runner(cfg, dev, qk_l2norm=args.qk_l2norm)
+    runner = Runner(cfg, dev, qk_l2norm=args.qk_l2norm, keep_context=not args.recompute)
     if args.cp_ranks > 1:  # context parallelism, the ranks serialized on this GPU
         runner.step = cp_step_fn(runner, args.cp_ranks)
         args.no_e2e = True
@@ -516,6 +545,16 @@ def main():
     value, ms = job_throughput(ms, cfg.valid_tokens, args.steps, dist, device=dev)
 
     split = kernel_split(runner, max(3, min(args.steps, 10)))
+    other = None  # the other backward mode, timed the same way, for comparison
+    if args.only == "step" and args.cp_ranks <= 1 and not args.no_compare:
+        alt = Runner(cfg, dev, qk_l2norm=args.qk_l2norm, keep_context=args.recompute)
+        for _ in range(warmup):
+            alt.step()
+        a_ms = timed(alt.step, args.steps, alt.stream)
+        a_value, a_ms = job_throughput(a_ms, cfg.valid_tokens, args.steps, dist, device=dev)
+        other = dict(backward="forward context kept" if args.recompute else "recompute",
+                     value=round(a_value, 1), ms_per_step=round(a_ms / args.steps, 4))
+        del alt
     e2e = None
     if not args.no_e2e:
         e_ms, h2d, d2h = e2e_measure(cfg, runner, max(3, min(args.steps, 10)), args.qk_l2norm)
@@ -559,6 +598,7 @@ def main():
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": f"inputs {ab['fwd'] / 1e9:.2f} GB read per step > L2 (no flush)",
                    "qk_l2norm": bool(args.qk_l2norm), "scalar_gate": bool(args.scalar_gate),
+                   "backward": "recompute" if args.recompute else "forward context kept",
                    **({"cp_ranks": args.cp_ranks, "cp": "sequences split into cp_ranks segments, state relay, "
                        "ranks serialized on one GPU"} if args.cp_ranks > 1 else {})},
         "roofline": roof,
@@ -571,6 +611,7 @@ def main():
                                     "source": peaks["src"]}},
         "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(per_step.items(), key=lambda x: -x[1])},
         "gpu_launches": int(launches),
+        **({"other_backward_mode": other} if other is not None else {}),
         "clocks": ck,
     }
     if e2e is not None:

@@ -21,7 +21,8 @@ EXPORTS = (
     "kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_chunk_bwd_workspace_size",
     "kda_chunk_bwd", "kda_recurrent_fwd", "kda_status_string", "kda_last_error", "kda_version",
     "kda_launch_count", "kda_timing_enable", "kda_timing_collect", "kda_chunk_fwd_noalloc",
-    "kda_state_compose",
+    "kda_state_compose", "kda_chunk_ctx_size", "kda_chunk_fwd_ctx_workspace_size",
+    "kda_chunk_bwd_ctx_workspace_size", "kda_chunk_fwd_ctx", "kda_chunk_bwd_ctx",
 )
 
 
@@ -65,6 +66,13 @@ def load(path: str = LIB_PATH):
         lib.kda_chunk_fwd.restype = i
         lib.kda_chunk_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_chunk_bwd.restype = i
+        for nm in ("kda_chunk_ctx_size", "kda_chunk_fwd_ctx_workspace_size", "kda_chunk_bwd_ctx_workspace_size"):
+            getattr(lib, nm).argtypes = [P]
+            getattr(lib, nm).restype = sz
+        lib.kda_chunk_fwd_ctx.argtypes = [P, vp, vp, vp, sz, vp, sz, vp]
+        lib.kda_chunk_fwd_ctx.restype = i
+        lib.kda_chunk_bwd_ctx.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.kda_chunk_bwd_ctx.restype = i
         lib.kda_recurrent_fwd.argtypes = [P, vp, vp, vp]
         lib.kda_recurrent_fwd.restype = i
         lib.kda_chunk_fwd_noalloc.argtypes = [P, vp, vp, vp]

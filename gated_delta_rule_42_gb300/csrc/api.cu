@@ -82,14 +82,35 @@ kda_status validate(const kda_inputs *in, Problem &P) {
   return KDA_OK;
 }
 
-// Workspace regions, in order.  Returns the total size; with base != NULL
-// also fills W.
 bool use_tc(const Problem &P) {
   const char *f = getenv("KDA_FORCE_SIMPLE");
   return tc_eligible(P) && !(f != nullptr && f[0] == '1');
 }
 
-size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
+// The forward context of the tensor-core path: what a forward keeps for its
+// backward -- the per-chunk records and, per (chunk, value head) slot, the
+// chunk-start state and the X^T, D^T tiles -- so that the backward runs
+// neither the record kernel nor the states pass.  Returns its size (0 on the
+// general path, which keeps nothing); with base != NULL also points W's
+// tc_tiles, tc_hs, tc_xt and tc_dt into it.
+size_t ctx_layout(const Problem &P, char *base, Workspace *W) {
+  if (!use_tc(P)) return 0;
+  const size_t slots = (size_t)P.NC * P.HV;
+  const size_t rec = align256(kTileRecord * slots), hs = align256(2 * slots * P.K * P.V);
+  const size_t t16 = align256(16384 * slots);
+  if (base != nullptr && W != nullptr) {
+    W->tc_tiles = (unsigned char *)base;
+    W->tc_hs = (__nv_bfloat16 *)(base + rec);
+    W->tc_xt = (unsigned char *)(base + rec + hs);
+    W->tc_dt = (unsigned char *)(base + rec + hs + t16);
+  }
+  return rec + hs + 2 * t16;
+}
+
+// Workspace regions, in order.  Returns the total size; with base != NULL
+// also fills W.  With with_ctx the regions the forward context holds are
+// left out (ctx_layout points W at them).
+size_t layout(const Problem &P, bool backward, bool with_ctx, char *base, Workspace *W) {
   const size_t slots = (size_t)P.NC * P.HV;
   const size_t K = P.K, V = P.V, C = kChunk;
   size_t off = 0;
@@ -108,11 +129,13 @@ size_t layout(const Problem &P, bool backward, char *base, Workspace *W) {
     if (backward) w.dgx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
   }
   if (use_tc(P)) {
-    w.tc_tiles = (unsigned char *)take(kTileRecord * slots);  // per-chunk records of the preparation kernel
+    if (!with_ctx) w.tc_tiles = (unsigned char *)take(kTileRecord * slots);  // per-chunk records of the preparation kernel
     if (backward) {  // tensor-core backward: per-slot tiles passed between its kernels
-      w.tc_hs = (__nv_bfloat16 *)take(2 * slots * K * V);
-      w.tc_xt = (unsigned char *)take(16384 * slots);
-      w.tc_dt = (unsigned char *)take(16384 * slots);
+      if (!with_ctx) {
+        w.tc_hs = (__nv_bfloat16 *)take(2 * slots * K * V);
+        w.tc_xt = (unsigned char *)take(16384 * slots);
+        w.tc_dt = (unsigned char *)take(16384 * slots);
+      }
       w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);
       w.tc_dd = (__nv_bfloat16 *)take(2 * slots * C * V);
       w.tc_dx = (__nv_bfloat16 *)take(2 * slots * C * V);
@@ -166,12 +189,89 @@ cudaError_t normalised_copies(const Problem &P, const Workspace &W, Problem *Pn,
   return e;
 }
 
-kda_status check_ws(size_t need, void *ws, size_t bytes) {
+kda_status check_ws(size_t need, const void *ws, size_t bytes, const char *what = "workspace") {
   if (need == 0) return KDA_OK;
-  if (ws == nullptr) return fail(KDA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+  if (ws == nullptr) return fail(KDA_ERR_WORKSPACE, "%s is NULL (%zu bytes needed)", what, need);
   if (bytes < need)
-    return fail(KDA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", bytes, need);
-  if (((uintptr_t)ws & 255) != 0) return fail(KDA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    return fail(KDA_ERR_WORKSPACE, "%s has %zu bytes, %zu needed", what, bytes, need);
+  if (((uintptr_t)ws & 255) != 0) return fail(KDA_ERR_WORKSPACE, "%s not 256-byte aligned", what);
+  return KDA_OK;
+}
+
+// kda_chunk_fwd, and with with_ctx kda_chunk_fwd_ctx.
+kda_status chunk_fwd(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes, bool with_ctx,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+  g_err[0] = 0;
+  Problem P{};
+  kda_status st = validate(in, P);
+  if (st != KDA_OK) return st;
+  if (P.Ttot > 0 && o == nullptr) return fail(KDA_ERR_INVALID_ARG, "o is NULL");
+  const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
+  with_ctx = need_ctx > 0;
+  if ((st = check_ws(need_ctx, ctx, ctx_bytes, "forward context")) != KDA_OK) return st;
+  const size_t need = layout(P, false, with_ctx, nullptr, nullptr);
+  if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
+  if (P.N == 0) return KDA_OK;
+  Workspace W;
+  layout(P, false, with_ctx, (char *)workspace, &W);
+  if (with_ctx) ctx_layout(P, (char *)ctx, &W);
+  Problem Pg = P;
+  cudaError_t e = gate_per_channel(P, W, &Pg, (cudaStream_t)stream);
+  if (e == cudaSuccess) {
+    if (use_tc(P)) {
+      e = tc_forward(Pg, W, o, hT, with_ctx ? kFwdOutput | kFwdSave : kFwdOutput, W.flags + 2,
+                     (cudaStream_t)stream);
+    } else {
+      Problem Pn = Pg;
+      e = normalised_copies(Pg, W, &Pn, (cudaStream_t)stream);
+      if (e == cudaSuccess) e = simple_forward(Pn, W, o, hT, (cudaStream_t)stream);
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(e, with_ctx ? "kda_chunk_fwd_ctx" : "kda_chunk_fwd");
+  return KDA_OK;
+}
+
+// kda_chunk_bwd, and with with_ctx kda_chunk_bwd_ctx.
+kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bool with_ctx, const void *dO,
+                     const float *dhT, void *dq, void *dk, void *dv, float *dg, float *dbeta, float *dh0,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+  g_err[0] = 0;
+  Problem P{};
+  kda_status st = validate(in, P);
+  if (st != KDA_OK) return st;
+  if (P.Ttot > 0 && (dO == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+                     dg == nullptr || dbeta == nullptr))
+    return fail(KDA_ERR_INVALID_ARG, "dO, dq, dk, dv, dg and dbeta are required");
+  if (use_tc(P) && ((uintptr_t)dO & 15) != 0)
+    return fail(KDA_ERR_INVALID_ARG, "dO must be 16-byte aligned (bf16, K = V = 128 path)");
+  const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
+  with_ctx = need_ctx > 0;
+  if ((st = check_ws(need_ctx, ctx, ctx_bytes, "forward context")) != KDA_OK) return st;
+  const size_t need = layout(P, true, with_ctx, nullptr, nullptr);
+  if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
+  if (P.N == 0) return KDA_OK;
+  Workspace W;
+  layout(P, true, with_ctx, (char *)workspace, &W);
+  if (with_ctx) ctx_layout(P, (char *)ctx, &W);  // read only: the context serves any number of backwards
+  cudaStream_t s = (cudaStream_t)stream;
+  Problem Pg = P;
+  cudaError_t e = gate_per_channel(P, W, &Pg, s);
+  float *dgk = P.scalar_gate ? W.dgx : dg;  // per-channel gate gradient
+  if (e == cudaSuccess) {
+    if (use_tc(P)) {
+      int *err = W.flags + 2;
+      e = with_ctx ? launch_chunk_map(Pg, W, s) : tc_forward(Pg, W, nullptr, nullptr, kFwdSave, err, s);
+      if (e == cudaSuccess) e = tc_backward_scan(Pg, W, dO, dhT, dh0, err, s);
+      if (e == cudaSuccess) e = tc_backward_intra(Pg, W, dO, dv, dq, dk, dgk, dbeta, err, s);
+      if (e == cudaSuccess && (P.HV != P.H || P.l2norm)) e = launch_group_reduce(Pg, W.dqp, W.dkp, dq, dk, s);
+    } else {
+      Problem Pn = Pg;
+      e = normalised_copies(Pg, W, &Pn, s);
+      if (e == cudaSuccess) e = simple_backward(Pn, W, dO, dhT, dq, dk, dv, dgk, dbeta, dh0, s);
+    }
+  }
+  if (e == cudaSuccess && P.scalar_gate) e = launch_gate_grad_reduce(P, W.dgx, dg, s);
+  if (e != cudaSuccess) return cuda_fail(e, with_ctx ? "kda_chunk_bwd_ctx" : "kda_chunk_bwd");
   return KDA_OK;
 }
 
@@ -206,79 +306,55 @@ extern "C" {
 size_t kda_chunk_fwd_workspace_size(const kda_inputs *in) {
   Problem P{};
   if (validate(in, P) != KDA_OK) return 0;
-  return layout(P, false, nullptr, nullptr);
+  return layout(P, false, false, nullptr, nullptr);
 }
 
 size_t kda_chunk_bwd_workspace_size(const kda_inputs *in) {
   Problem P{};
   if (validate(in, P) != KDA_OK) return 0;
-  return layout(P, true, nullptr, nullptr);
+  return layout(P, true, false, nullptr, nullptr);
 }
 
 kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspace,
                          size_t workspace_bytes, void *stream) {
-  g_err[0] = 0;
-  Problem P{};
-  kda_status st = validate(in, P);
-  if (st != KDA_OK) return st;
-  if (P.Ttot > 0 && o == nullptr) return fail(KDA_ERR_INVALID_ARG, "o is NULL");
-  const size_t need = layout(P, false, nullptr, nullptr);
-  if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
-  if (P.N == 0) return KDA_OK;
-  Workspace W;
-  layout(P, false, (char *)workspace, &W);
-  Problem Pg = P;
-  cudaError_t e = gate_per_channel(P, W, &Pg, (cudaStream_t)stream);
-  if (e == cudaSuccess) {
-    if (use_tc(P)) {
-      e = tc_forward(Pg, W, o, hT, false, W.flags + 2, (cudaStream_t)stream);
-    } else {
-      Problem Pn = Pg;
-      e = normalised_copies(Pg, W, &Pn, (cudaStream_t)stream);
-      if (e == cudaSuccess) e = simple_forward(Pn, W, o, hT, (cudaStream_t)stream);
-    }
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd");
-  return KDA_OK;
+  return chunk_fwd(in, o, hT, nullptr, 0, false, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT, void *dq,
                          void *dk, void *dv, float *dg, float *dbeta, float *dh0,
                          void *workspace, size_t workspace_bytes, void *stream) {
-  g_err[0] = 0;
+  return chunk_bwd(in, nullptr, 0, false, dO, dhT, dq, dk, dv, dg, dbeta, dh0, workspace, workspace_bytes,
+                   stream);
+}
+
+size_t kda_chunk_ctx_size(const kda_inputs *in) {
   Problem P{};
-  kda_status st = validate(in, P);
-  if (st != KDA_OK) return st;
-  if (P.Ttot > 0 && (dO == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
-                     dg == nullptr || dbeta == nullptr))
-    return fail(KDA_ERR_INVALID_ARG, "dO, dq, dk, dv, dg and dbeta are required");
-  if (use_tc(P) && ((uintptr_t)dO & 15) != 0)
-    return fail(KDA_ERR_INVALID_ARG, "dO must be 16-byte aligned (bf16, K = V = 128 path)");
-  const size_t need = layout(P, true, nullptr, nullptr);
-  if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
-  if (P.N == 0) return KDA_OK;
-  Workspace W;
-  layout(P, true, (char *)workspace, &W);
-  cudaStream_t s = (cudaStream_t)stream;
-  Problem Pg = P;
-  cudaError_t e = gate_per_channel(P, W, &Pg, s);
-  float *dgk = P.scalar_gate ? W.dgx : dg;  // per-channel gate gradient
-  if (e == cudaSuccess) {
-    if (use_tc(P)) {
-      int *err = W.flags + 2;
-      e = tc_forward(Pg, W, nullptr, nullptr, true, err, s);
-      if (e == cudaSuccess) e = tc_backward_scan(Pg, W, dO, dhT, dh0, err, s);
-      if (e == cudaSuccess) e = tc_backward_intra(Pg, W, dO, dv, dq, dk, dgk, dbeta, err, s);
-      if (e == cudaSuccess && (P.HV != P.H || P.l2norm)) e = launch_group_reduce(Pg, W.dqp, W.dkp, dq, dk, s);
-    } else {
-      Problem Pn = Pg;
-      e = normalised_copies(Pg, W, &Pn, s);
-      if (e == cudaSuccess) e = simple_backward(Pn, W, dO, dhT, dq, dk, dv, dgk, dbeta, dh0, s);
-    }
-  }
-  if (e == cudaSuccess && P.scalar_gate) e = launch_gate_grad_reduce(P, W.dgx, dg, s);
-  if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_bwd");
-  return KDA_OK;
+  if (validate(in, P) != KDA_OK) return 0;
+  return ctx_layout(P, nullptr, nullptr);
+}
+
+size_t kda_chunk_fwd_ctx_workspace_size(const kda_inputs *in) {
+  Problem P{};
+  if (validate(in, P) != KDA_OK) return 0;
+  return layout(P, false, ctx_layout(P, nullptr, nullptr) > 0, nullptr, nullptr);
+}
+
+size_t kda_chunk_bwd_ctx_workspace_size(const kda_inputs *in) {
+  Problem P{};
+  if (validate(in, P) != KDA_OK) return 0;
+  return layout(P, true, ctx_layout(P, nullptr, nullptr) > 0, nullptr, nullptr);
+}
+
+kda_status kda_chunk_fwd_ctx(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  return chunk_fwd(in, o, hT, ctx, ctx_bytes, true, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_chunk_bwd_ctx(const kda_inputs *in, const void *ctx, size_t ctx_bytes, const void *dO,
+                             const float *dhT, void *dq, void *dk, void *dv, float *dg, float *dbeta,
+                             float *dh0, void *workspace, size_t workspace_bytes, void *stream) {
+  return chunk_bwd(in, ctx, ctx_bytes, true, dO, dhT, dq, dk, dv, dg, dbeta, dh0, workspace, workspace_bytes,
+                   stream);
 }
 
 kda_status kda_recurrent_fwd(const kda_inputs *in, void *o, float *hT, void *stream) {
@@ -326,6 +402,6 @@ const char *kda_status_string(kda_status s) {
 
 const char *kda_last_error(void) { return g_err; }
 
-int kda_version(void) { return 101; }
+int kda_version(void) { return 102; }
 
 }  // extern "C"

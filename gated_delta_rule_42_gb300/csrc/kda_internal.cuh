@@ -125,14 +125,15 @@ cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO
                             const float *dhT, void *dq, void *dk, void *dv, float *dg,
                             float *dbeta, float *dh0, cudaStream_t s);
 cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t s);
-// bf16, K = V = 128 tensor-core forward.  With states = true it runs in
-// "states" mode for the backward: no output; per (chunk, value head) slot it
-// saves the chunk-start state and the Aqk, A, X^T and D^T tiles to
-// W.tc_hs / tc_tiles / tc_xt / tc_dt.
 // Per-chunk records (tc_prep.cu): one CTA per (chunk, value head) slot.
 cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps, int *err, cudaStream_t s);
-cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, bool states,
-                       int *err, cudaStream_t s);
+// bf16, K = V = 128 tensor-core forward: the records into W.tc_tiles, then the
+// state chain.  mode is kFwdOutput (o, hT), kFwdSave (no output: per (chunk,
+// value head) slot the chunk-start state and the X^T, D^T tiles go to
+// W.tc_hs / tc_xt / tc_dt for the backward) or both bits.
+constexpr int kFwdOutput = 1, kFwdSave = 2;
+cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, int *err,
+                       cudaStream_t s);
 cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,
                              float *dh0, int *err, cudaStream_t s);
 // Per-chunk gradients: tcgen05 products and the gradient chain in one kernel.

@@ -24,9 +24,11 @@
 // h tile becomes the output staging, and the next chunk's loads are issued as
 // soon as the last products of this chunk complete.
 //
-// In "states" mode (no output) the kernel saves, per chunk, what the backward
-// needs from the forward recompute beside the record: the chunk-start state
-// h_c (bf16 [K][V]) and X^T, D^T, as bulk copies of the swizzled tiles.
+// Three modes.  Output: o (and hT).  States (no output): the kernel saves, per
+// chunk, what the backward needs beside the record -- the chunk-start state
+// h_c (bf16 [K][V]) and X^T, D^T, as bulk copies of the swizzled tiles -- when
+// the backward recomputes the forward.  Output + save: both at once, for a
+// forward whose context the backward keeps.
 #include "tc_common.cuh"
 
 namespace kda {
@@ -54,7 +56,7 @@ struct FwdArgs {
   int *err;           // device error flag (a bounded wait gave up)
 };
 
-template <bool kOut>
+template <int kMode>
 __global__ void __launch_bounds__(kThr, 2)
 kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smraw[];
@@ -75,6 +77,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
   const int cown = quarter * 32 + lane;  // key channel (state) or value column (X, D, O): the TMEM lane
   const int r0 = 32 * vhalf;             // the token columns this thread's epilogues cover
   const int4 si = W.seq[n];
+  constexpr bool kOut = (kMode & kFwdOutput) != 0, kSave = (kMode & kFwdSave) != 0;
   constexpr uint32_t kRecBytes = kOut ? 65536u : kRecStates;  // the states pass needs Bk, Khat and A only
 
   if (tid == 0) {
@@ -140,7 +143,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     __syncthreads();
     fence_after();
     KDA_PT(0);
-    if (!kOut && tid == 0) {  // h_c for the backward
+    if (kSave && tid == 0) {  // h_c for the backward
       bulk_store(W.tc_hs + slot * kD * kD, sbase + S_H, 32768u);
       bulk_commit();
     }
@@ -178,7 +181,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     __syncthreads();
     fence_after();
     KDA_PT(2);
-    if (!kOut && tid == 0) {  // X^T tile for the backward
+    if (kSave && tid == 0) {  // X^T tile for the backward
       bulk_store(W.tc_xt + slot * 16384, sbase + S_V, 16384u);
       bulk_commit();
     }
@@ -210,7 +213,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     __syncthreads();
     fence_after();
     KDA_PT(4);
-    if (!kOut && tid == 0) {  // D^T tile for the backward
+    if (kSave && tid == 0) {  // D^T tile for the backward
       bulk_store(W.tc_dt + slot * 16384, sbase + S_REC, 16384u);
       bulk_commit();
     }
@@ -241,10 +244,10 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     fence_after();
     KDA_PT(5);
     // Every tile but h is dead: the next chunk's loads go now.
+    if (kSave && tid == 0) bulk_wait_read();  // h_c, X^T, D^T have left shared memory
     if (ci + 1 < si.w) {
       const int2 nx = chunk_span(si, ci + 1);
       if (tid == 0) {
-        if (!kOut) bulk_wait_read();  // h_c, X^T, D^T have left shared memory
         mbar_expect_tx(bar_ld, kRecBytes + 16384u);
         bulk_load(sbase + S_REC, W.tc_tiles + (slot + HV) * kTileRecord, kRecBytes, bar_ld);
         tma_tile(sbase + S_V, &maps.v, j, nx.x, bar_ld);
@@ -262,6 +265,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
       }
     }
     if (kOut) {  // O^T -> staging tile [r][v] over the h tile, then coalesced 16-byte stores
+      if (kSave) __syncthreads();  // the h_c copy out of the h tile is complete
       const int v = cown;
       __nv_bfloat16 *Ot = (__nv_bfloat16 *)(sm + S_H);
 #pragma unroll
@@ -292,7 +296,7 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     for (int x = 0; x < 64; x += 4)
       *reinterpret_cast<float4 *>(dst + x) = make_float4(hreg[x], hreg[x + 1], hreg[x + 2], hreg[x + 3]);
   }
-  if (!kOut && tid == 0) bulk_wait_all();  // the saved tiles are in global memory before the CTA exits
+  if (kSave && tid == 0) bulk_wait_all();  // the saved tiles are in global memory before the CTA exits
   fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -306,25 +310,30 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
 
 KDA_PT_EXPORT(kda_debug_fwd_phase_cycles)
 
-cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, bool states,
-                       int *err, cudaStream_t s) {
+template <int kMode>
+cudaError_t launch_fwd(const char *name, const Problem &P, const Workspace &W, const FwdArgs &a,
+                       const TmaMaps &maps, cudaStream_t s) {
+  cudaError_t e =
+      cudaFuncSetAttribute(kda_fwd_tc_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
+  if (e != cudaSuccess) return e;
+  KDA_LAUNCH(name, s, kda_fwd_tc_kernel<kMode><<<dim3(P.N, P.HV), kThr, S_SMEM, s>>>(P, W, a, maps));
+  return cudaGetLastError();
+}
+
+cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, int *err,
+                       cudaStream_t s) {
   cudaError_t e = launch_chunk_map(P, W, s);
   if (e != cudaSuccess || P.N == 0) return e;
   FwdArgs a{(__nv_bfloat16 *)o, hT, err};
   TmaMaps maps;
   if ((e = make_tma_maps(P, P.v, nullptr, &maps)) != cudaSuccess) return e;
   if ((e = tc_prepare(P, W, maps, err, s)) != cudaSuccess) return e;
-  const dim3 grid(P.N, P.HV);
-  if (states) {
-    e = cudaFuncSetAttribute(kda_fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
-    if (e != cudaSuccess) return e;
-    KDA_LAUNCH("kda_fwd_tc_states", s, kda_fwd_tc_kernel<false><<<grid, kThr, S_SMEM, s>>>(P, W, a, maps));
-  } else {
-    e = cudaFuncSetAttribute(kda_fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
-    if (e != cudaSuccess) return e;
-    KDA_LAUNCH("kda_fwd_tc", s, kda_fwd_tc_kernel<true><<<grid, kThr, S_SMEM, s>>>(P, W, a, maps));
+  switch (mode) {
+    case kFwdOutput: return launch_fwd<kFwdOutput>("kda_fwd_tc", P, W, a, maps, s);
+    case kFwdSave: return launch_fwd<kFwdSave>("kda_fwd_tc_states", P, W, a, maps, s);
+    case kFwdOutput | kFwdSave: return launch_fwd<kFwdOutput | kFwdSave>("kda_fwd_tc_save", P, W, a, maps, s);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kda

@@ -20,7 +20,8 @@ import torch
 
 from . import _lib
 
-__all__ = ["chunk_kda", "recurrent_kda", "chunk_kda_fwd", "chunk_kda_bwd", "make_inputs_struct"]
+__all__ = ["chunk_kda", "recurrent_kda", "chunk_kda_fwd", "chunk_kda_bwd", "chunk_kda_fwd_ctx",
+           "chunk_kda_bwd_ctx", "make_inputs_struct"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -132,11 +133,64 @@ def chunk_kda_bwd(q, k, v, g, beta, initial_state, cu_seqlens, do, dht,
     return dq, dk, dv, dg, db, dh0
 
 
+def chunk_kda_fwd_ctx(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_final_state=False,
+                      use_qk_l2norm: bool = False):
+    """Forward that also returns the forward context (a uint8 device tensor,
+    empty on the general path) for :func:`chunk_kda_bwd_ctx`: the per-chunk
+    records, chunk-start states and X^T, D^T tiles the backward would otherwise
+    recompute.  Returns (o, final_state or None, context)."""
+    lib = _lib.load()
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    o = torch.empty_like(v)
+    hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
+          if output_final_state else None)
+    nctx = lib.kda_chunk_ctx_size(ctypes.byref(s))
+    kctx = _workspace(nctx, q.device) if nctx else torch.empty(0, dtype=torch.uint8, device=q.device)
+    cp, cb = _aligned(kctx) if nctx else (None, 0)
+    workspace = _workspace(lib.kda_chunk_fwd_ctx_workspace_size(ctypes.byref(s)), q.device)
+    wp, wb = _aligned(workspace)
+    _lib.check(lib, lib.kda_chunk_fwd_ctx(ctypes.byref(s), _ptr(o), _ptr(hT), cp, cb, wp, wb,
+                                          _stream(q.device)))
+    return o, hT, kctx
+
+
+def chunk_kda_bwd_ctx(q, k, v, g, beta, initial_state, cu_seqlens, kctx, do, dht, need_dh0: bool = True,
+                      use_qk_l2norm: bool = False):
+    """Backward on the context :func:`chunk_kda_fwd_ctx` returned for the same
+    inputs (it is only read).  Same results as :func:`chunk_kda_bwd`."""
+    lib = _lib.load()
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    _check_tensor("do", do, q.dtype, q.device, tuple(v.shape))
+    if dht is not None:
+        _check_tensor("dht", dht, torch.float32, q.device, (s.N, s.HV, s.K, s.V))
+    _check_tensor("context", kctx, torch.uint8, q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dg = torch.empty_like(g)
+    db = torch.empty_like(beta)
+    dh0 = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
+           if need_dh0 else None)
+    cp, cb = _aligned(kctx) if kctx.numel() else (None, 0)
+    workspace = _workspace(lib.kda_chunk_bwd_ctx_workspace_size(ctypes.byref(s)), q.device)
+    wp, wb = _aligned(workspace)
+    _lib.check(lib, lib.kda_chunk_bwd_ctx(ctypes.byref(s), cp, cb, _ptr(do), _ptr(dht), _ptr(dq), _ptr(dk),
+                                          _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), wp, wb,
+                                          _stream(q.device)))
+    return dq, dk, dv, dg, db, dh0
+
+
 class ChunkKDAFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, use_qk_l2norm):
-        o, hT = chunk_kda_fwd(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
-                              use_qk_l2norm=use_qk_l2norm)
+    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, use_qk_l2norm,
+                keep_context):
+        if keep_context:
+            o, hT, ctx.kctx = chunk_kda_fwd_ctx(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
+                                                use_qk_l2norm=use_qk_l2norm)
+        else:
+            o, hT = chunk_kda_fwd(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
+                                  use_qk_l2norm=use_qk_l2norm)
+            ctx.kctx = None
         ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
         ctx.has_h0 = initial_state is not None
         ctx.l2 = use_qk_l2norm
@@ -147,18 +201,26 @@ class ChunkKDAFunction(torch.autograd.Function):
         q, k, v, g, beta, h0, cu = ctx.saved_tensors
         do = do.contiguous()
         dht = None if dht is None else dht.contiguous()
-        dq, dk, dv, dg, db, dh0 = chunk_kda_bwd(q, k, v, g, beta, h0, cu, do, dht,
-                                                need_dh0=ctx.has_h0, use_qk_l2norm=ctx.l2)
-        return dq, dk, dv, dg, db, dh0, None, None, None
+        if ctx.kctx is not None:
+            dq, dk, dv, dg, db, dh0 = chunk_kda_bwd_ctx(q, k, v, g, beta, h0, cu, ctx.kctx, do, dht,
+                                                        need_dh0=ctx.has_h0, use_qk_l2norm=ctx.l2)
+            ctx.kctx = None  # the context's memory goes back as soon as the backward is enqueued
+        else:
+            dq, dk, dv, dg, db, dh0 = chunk_kda_bwd(q, k, v, g, beta, h0, cu, do, dht,
+                                                    need_dh0=ctx.has_h0, use_qk_l2norm=ctx.l2)
+        return dq, dk, dv, dg, db, dh0, None, None, None, None
 
 
 def chunk_kda(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, output_final_state=False,
-              use_qk_l2norm=False):
+              use_qk_l2norm=False, keep_context=True):
     """Chunked KDA forward (with autograd).  Returns (o, final_state or None).
     use_qk_l2norm: L2-normalise every q and k row inside the op (its backward
-    included)."""
+    included).  keep_context: the forward keeps its per-chunk intermediates
+    (about 2 KB per token and value head on the bf16 K = V = 128 path) so that
+    the backward does not recompute them; False trades that memory for the
+    recompute.  The gradients are the same either way."""
     return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
-                                  use_qk_l2norm)
+                                  use_qk_l2norm, keep_context)
 
 
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,

@@ -44,8 +44,9 @@
  * Ownership: the caller allocates every input, output and workspace buffer;
  * the library never allocates or frees device memory, never synchronises and
  * never reads device data on the host.  Work is enqueued on `stream`
- * (a cudaStream_t; NULL = the legacy default stream).  The backward recomputes
- * everything it needs from the inputs: no forward context is saved.
+ * (a cudaStream_t; NULL = the legacy default stream).  kda_chunk_bwd
+ * recomputes everything it needs from the inputs; the _ctx pair instead keeps
+ * the forward's intermediates in a caller-owned context buffer.
  *
  * Errors: arguments the host can check are validated before anything is
  * enqueued and reported synchronously (KDA_ERR_INVALID_ARG,
@@ -135,6 +136,42 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
                          void *dk, void *dv, float *dg, float *dbeta, float *dh0,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- forward context: the backward without its recompute (no counterpart on
+ * the pages, which leave open what a forward keeps for its backward) ----
+ * On the tensor-core path (bf16, K = V = 128, aligned q/k/v/g) the backward
+ * first re-runs two forward kernels: the per-chunk record kernel and the
+ * state chain that saves every chunk's start state.  kda_chunk_fwd_ctx writes
+ * those results into a caller-owned context buffer while it computes o, and
+ * kda_chunk_bwd_ctx reads them from it instead: same results, bit for bit, as
+ * kda_chunk_fwd + kda_chunk_bwd, for kda_chunk_ctx_size() bytes of device
+ * memory per layer -- per (64-token chunk, value head): the 66,048-byte record
+ * (decayed key and query tiles, the inverse A, Aqk, 2^G_last), the bf16
+ * chunk-start state (32 KB) and two 16 KB bf16 tiles (X^T, D^T).
+ * The context must come from kda_chunk_fwd_ctx on the same inputs (q, k, v,
+ * g, beta, h0, cu_seqlens, flags), unchanged since; that is a precondition,
+ * not checked.  The backward only reads it, so it serves any number of
+ * backward calls.  Both calls require a 256-byte aligned context of at least
+ * kda_chunk_ctx_size() bytes (KDA_ERR_WORKSPACE otherwise).  On the general
+ * path kda_chunk_ctx_size() is 0, nothing is kept, ctx may be NULL and the
+ * _ctx calls behave as kda_chunk_fwd / kda_chunk_bwd. */
+
+/* Bytes of forward context for this problem (0: general path, or invalid). */
+size_t kda_chunk_ctx_size(const kda_inputs *in);
+
+/* Workspace of kda_chunk_fwd_ctx / kda_chunk_bwd_ctx: the plain sizes minus
+ * the regions the context holds. */
+size_t kda_chunk_fwd_ctx_workspace_size(const kda_inputs *in);
+size_t kda_chunk_bwd_ctx_workspace_size(const kda_inputs *in);
+
+/* kda_chunk_fwd that also fills ctx. */
+kda_status kda_chunk_fwd_ctx(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* kda_chunk_bwd on the context kda_chunk_fwd_ctx filled (read only). */
+kda_status kda_chunk_bwd_ctx(const kda_inputs *in, const void *ctx, size_t ctx_bytes, const void *dO,
+                             const float *dhT, void *dq, void *dk, void *dv, float *dg, float *dbeta,
+                             float *dh0, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Token-by-token recurrent forward (inference): one sequential pass per
  * (sequence, value head), fp32 state and fp32 arithmetic whatever the dtype,
  * no workspace.  Same arguments and results as kda_chunk_fwd, as in the
@@ -164,7 +201,8 @@ const char *kda_status_string(kda_status s);
 /* Message describing the last failure on the calling thread ("" if none). */
 const char *kda_last_error(void);
 
-/* Library ABI version (major * 100 + minor): 101 (kda_inputs gained `flags`). */
+/* Library ABI version (major * 100 + minor): 102 (101: kda_inputs gained
+ * `flags`; 102: the forward-context entry points). */
 int kda_version(void);
 
 /* Chunked forward without a caller workspace (no counterpart on the pages).

@@ -182,3 +182,37 @@ def sample_units(inp, units):
         gr = oracle.kda_bwd(q, k, v, g, beta, h0, do, dhT)
         out.append((n, hq, js, t0, t1, (o, hT), gr))
     return out
+
+
+def gpu_fwd_bwd_ctx(inp, dev="cuda", lib=None, want_dh0=True, l2=False, backwards=1):
+    """kda_chunk_fwd_ctx, then kda_chunk_bwd_ctx ``backwards`` times on the
+    context it kept (NaN-poisoned outputs, 0xFF-poisoned context and
+    workspaces).  Returns the DEVICE results: o, hT and a list of gradient
+    dicts, one per backward call."""
+    lib = lib or _lib.load()
+    d = inp.to(dev)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
+    sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def p(t):
+        return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+    o = _nan_like(d.v.shape, d.dtype, dev)
+    hT = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if inp.output_final_state else None
+    nctx = lib.kda_chunk_ctx_size(ctypes.byref(s))
+    cbuf, cp, cb = _poisoned_ws(nctx, dev) if nctx else (None, None, 0)
+    ws, wp, wb = _poisoned_ws(lib.kda_chunk_fwd_ctx_workspace_size(ctypes.byref(s)), dev)
+    _lib.check(lib, lib.kda_chunk_fwd_ctx(ctypes.byref(s), p(o), p(hT), cp, cb, wp, wb, sp))
+    grads = []
+    for _ in range(backwards):
+        out = dict(dq=_nan_like(d.q.shape, d.dtype, dev), dk=_nan_like(d.k.shape, d.dtype, dev),
+                   dv=_nan_like(d.v.shape, d.dtype, dev), dg=_nan_like(d.g.shape, torch.float32, dev),
+                   dbeta=_nan_like(d.beta.shape, torch.float32, dev))
+        out["dh0"] = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if want_dh0 else None
+        ws, wp, wb = _poisoned_ws(lib.kda_chunk_bwd_ctx_workspace_size(ctypes.byref(s)), dev)
+        _lib.check(lib, lib.kda_chunk_bwd_ctx(ctypes.byref(s), cp, cb, p(d.do), p(d.dhT), p(out["dq"]),
+                                              p(out["dk"]), p(out["dv"]), p(out["dg"]), p(out["dbeta"]),
+                                              p(out["dh0"]), wp, wb, sp))
+        grads.append(out)
+    torch.cuda.synchronize()
+    return o, hT, grads, nctx

@@ -134,3 +134,48 @@ def test_misaligned_dO_on_the_tensor_core_path_is_rejected(lib):
                            ctypes.c_void_p(0x10000), 1 << 30, None)
     assert st == _lib.KDA_ERR_INVALID_ARG, lib.kda_last_error()
     assert b"aligned" in lib.kda_last_error()
+
+
+def _a256(x):
+    return (x + 255) & ~255
+
+
+def test_forward_context_sizes(lib):
+    """The forward context holds, per (64-token chunk, value head), the record
+    (66,048 B), the bf16 chunk-start state and the X^T, D^T tiles; the _ctx
+    workspaces are the plain ones minus those regions.  The general path keeps
+    nothing."""
+    s = _inputs(K=128, V=128, T=200)          # 4 chunks x 4 value heads, tensor-core path
+    slots = 4 * 4
+    ctx = lib.kda_chunk_ctx_size(ctypes.byref(s))
+    assert ctx == _a256(66048 * slots) + _a256(2 * 128 * 128 * slots) + 2 * _a256(16384 * slots)
+    f, b = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s)), lib.kda_chunk_bwd_workspace_size(ctypes.byref(s))
+    fc = lib.kda_chunk_fwd_ctx_workspace_size(ctypes.byref(s))
+    bc = lib.kda_chunk_bwd_ctx_workspace_size(ctypes.byref(s))
+    assert f - fc == _a256(66048 * slots)
+    assert b - bc == ctx
+    for kw in (dict(K=64, V=64), dict(K=128, V=128, dtype=_lib.KDA_F32), dict(K=128, V=128, v=0x1008)):
+        g = _inputs(T=200, **kw)                # general path: fp32, K != 128, or a misaligned v
+        assert lib.kda_chunk_ctx_size(ctypes.byref(g)) == 0
+        assert lib.kda_chunk_fwd_ctx_workspace_size(ctypes.byref(g)) == lib.kda_chunk_fwd_workspace_size(ctypes.byref(g))
+        assert lib.kda_chunk_bwd_ctx_workspace_size(ctypes.byref(g)) == lib.kda_chunk_bwd_workspace_size(ctypes.byref(g))
+    assert lib.kda_chunk_ctx_size(ctypes.byref(_inputs(HV=3))) == 0  # invalid problem
+
+
+def test_forward_context_checks(lib):
+    """A missing, short or misaligned context is KDA_ERR_WORKSPACE before any launch."""
+    s = _inputs(K=128, V=128)
+    need = lib.kda_chunk_ctx_size(ctypes.byref(s))
+    ws = ctypes.c_void_p(0x10000)
+    o = ctypes.c_void_p(0x3000)
+    for ctx, nbytes in ((None, need), (ctypes.c_void_p(0x100000), need - 1), (ctypes.c_void_p(0x100010), need)):
+        st = lib.kda_chunk_fwd_ctx(ctypes.byref(s), o, None, ctx, nbytes, ws, 1 << 30, None)
+        assert st == _lib.KDA_ERR_WORKSPACE, lib.kda_last_error()
+        assert b"forward context" in lib.kda_last_error()
+        fake = [ctypes.c_void_p(0x200000 + 0x1000 * i) for i in range(6)]
+        st = lib.kda_chunk_bwd_ctx(ctypes.byref(s), ctx, nbytes, fake[0], None, *fake[1:6], None, ws, 1 << 30, None)
+        assert st == _lib.KDA_ERR_WORKSPACE, lib.kda_last_error()
+    # a general-path problem keeps nothing: a NULL context is fine up to the workspace check
+    g = _inputs(K=64, V=64)
+    st = lib.kda_chunk_fwd_ctx(ctypes.byref(g), o, None, None, 0, None, 0, None)
+    assert st == _lib.KDA_ERR_WORKSPACE and b"workspace is NULL" in lib.kda_last_error()
