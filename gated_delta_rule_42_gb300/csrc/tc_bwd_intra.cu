@@ -1,7 +1,10 @@
 // Per-chunk gradients of the bf16 chunked KDA backward (K = V = 128): the
 // tensor-core products and the gradient chain in one kernel.
 //
-// One CTA (16 warps) per (chunk, value head), all chunks at once.  Inputs: the
+// Persistent: one CTA (16 warps) per SM walks the (chunk, value head) slots,
+// and loads the next slot's inputs into tiles as soon as the current slot's
+// work leaves them dead (three groups, below), so most of each slot's loads
+// overlap the previous slot's chain and assembly.  Inputs: the
 // chunk-start state h and the tiles X^T (X = beta v - Bk h), D^T (D = A X) and
 // A from the forward recompute, the gradient of the chunk-end state dh', and
 // dD, dX from the reverse scan.  First, on tcgen05 (fp32 in TMEM):
@@ -63,7 +66,7 @@ constexpr uint32_t C_VEC = 205824;    // vectors (20 x 128 fp32)
 constexpr uint32_t C_BETA = 216064;   // beta [64]
 constexpr uint32_t C_RB = 216320;     // dbeta partials [4][64]
 constexpr uint32_t C_RED = 217344;    // sum_v dX v [64], d(2^G_last) [128]
-constexpr uint32_t C_MISC = 218112;   // mbarrier, tmem slot
+constexpr uint32_t C_MISC = 218112;   // mbarriers (loads S, P1, P2, raw k/q, products), tmem slot
 constexpr uint32_t C_SMEM = 218176 + 1024;
 constexpr uint32_t LO128 = 16384, LO64 = 8192;
 // Tensor memory: the per-chunk products that the assembly reads element-wise are
@@ -143,528 +146,619 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
 
 constexpr int kCT = 512;  // 16 warps: the chain is latency-bound, so more warps hide more of it
 
+// Slot s of the chunk-major (chunk, value head) list; false past the valid
+// chunks (the chunk table lists them first).
+struct Slot {
+  int t0, len, j, h;
+  size_t slot;
+};
+__device__ __forceinline__ bool get_slot(const Problem &P, const Workspace &W, int64_t s, Slot &o) {
+  if (s >= (int64_t)P.NC * P.HV) return false;
+  const int c = (int)(s / P.HV);
+  const int4 ch = W.chunk[c];
+  if (ch.x < 0) return false;
+  o.j = (int)(s - (int64_t)c * P.HV);
+  o.h = o.j / (P.HV / P.H);
+  o.t0 = ch.y;
+  o.len = ch.z;
+  o.slot = (size_t)s;
+  return true;
+}
+
+// A slot's inputs arrive in three groups of bulk / TMA copies (issued by one
+// thread), each into tiles that die at a different point of the previous
+// slot's work:
+//   P1 (after the pairwise chains): dh', v, A            -> the dAqk^T, X, T and A tiles
+//   P2 (after the assembly):        dO, dD columns 64..127, h columns 0..63 -> the Kc tile
+//   S  (after the dg scan):         X^T, D^T, dX, dO and dD columns 0..63, dX columns
+//                                   64..127, h columns 64..127 -> the Kr, Qr and dL tiles
+// (G and beta follow P2 by cp.async from every thread.)  The stacked
+// [dX; dO; dD] operand is two 64-column sub-tiles of 192 rows; h and dh' are
+// the saved swizzled tiles, two 64-column halves each.
+constexpr uint32_t kBytesS = 2 * 16384u + 4 * 8192u + 16384u, kBytesP1 = 32768u + 16384u + 8192u,
+                   kBytesP2 = 2 * 8192u + 16384u;
+// X^T, D^T, h, dh', [dX; dO; dD], v, A: every operand once
+static_assert(kBytesS + kBytesP1 + kBytesP2 == 2 * 16384u + 2 * 32768u + 49152u + 16384u + 8192u, "group sizes");
+__device__ __forceinline__ void issue_s(uint32_t sbase, const Workspace &W, const TmaMaps &maps, const Slot &q,
+                                        uint64_t *bar) {
+  mbar_expect_tx(bar, kBytesS);
+  bulk_load(sbase + I_XT, W.tc_xt + q.slot * 16384, 16384u, bar);
+  bulk_load(sbase + I_DT, W.tc_dt + q.slot * 16384, 16384u, bar);
+  const unsigned char *dx = reinterpret_cast<const unsigned char *>(W.tc_dx + q.slot * kC * kD);
+  const unsigned char *dd = reinterpret_cast<const unsigned char *>(W.tc_dd + q.slot * kC * kD);
+  bulk_load(sbase + I_STK, dx, 8192u, bar);                       // dX: rows 0..63, sub-tile 0
+  bulk_load(sbase + I_STK + 192 * 128, dx + 8192, 8192u, bar);    //                 sub-tile 1
+  tma_load3(sbase + I_STK + 64 * 128, &maps.d, 0, q.j, q.t0, bar);  // dO: rows 64..127, sub-tile 0
+  bulk_load(sbase + I_STK + 128 * 128, dd, 8192u, bar);           // dD: rows 128..191, sub-tile 0
+  bulk_load(sbase + I_H + 16384, reinterpret_cast<const unsigned char *>(W.tc_hs + q.slot * kD * kD) + 16384,
+            16384u, bar);
+}
+__device__ __forceinline__ void issue_p1(uint32_t sbase, const Workspace &W, const TmaMaps &maps, const Slot &q,
+                                         uint64_t *bar) {
+  mbar_expect_tx(bar, kBytesP1);
+  bulk_load(sbase + I_DH, W.tc_dh + q.slot * kD * kD, 32768u, bar);
+  tma_tile(sbase + I_V, &maps.v, q.j, q.t0, bar);
+  bulk_load(sbase + C_A, W.tc_tiles + q.slot * kTileRecord + kRecAM, 8192u, bar);
+}
+__device__ __forceinline__ void issue_p2(uint32_t sbase, const Workspace &W, const TmaMaps &maps, const Slot &q,
+                                         uint64_t *bar) {
+  mbar_expect_tx(bar, kBytesP2);
+  tma_load3(sbase + I_STK + 256 * 128, &maps.d, 64, q.j, q.t0, bar);  // dO: rows 64..127, sub-tile 1
+  bulk_load(sbase + I_STK + 320 * 128,
+            reinterpret_cast<const unsigned char *>(W.tc_dd + q.slot * kC * kD) + 8192, 8192u, bar);  // dD, sub-tile 1
+  bulk_load(sbase + I_H, W.tc_hs + q.slot * kD * kD, 16384u, bar);
+}
+// G rows (zero past len) and beta of a slot, cp.async from every thread
+__device__ __forceinline__ void issue_gate_beta(uint32_t sbase, const Problem &P, float *beta, const Slot &q) {
+  load_gate<kCT>(sbase + C_G, P.g, q.t0, q.len, P.HV, q.j);
+  const int tid = threadIdx.x;
+  if (tid < kC) {
+    if (tid < q.len) cp4(smem_u32(beta + tid), P.beta + (size_t)(q.t0 + tid) * P.HV + q.j);
+    else beta[tid] = 0.f;
+  }
+  cp_commit();
+}
+
 __global__ void __launch_bounds__(kCT, 1)
 kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
-  const int c_idx = blockIdx.x, j = blockIdx.y;
-  const int4 ch = W.chunk[c_idx];
-  if (ch.x < 0) return;
-  const int t0 = ch.y, len = ch.z;
-  const int HV = P.HV, H = P.H, h = j / (HV / H);
+  const int HV = P.HV, H = P.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3;
-  const size_t slot = (size_t)c_idx * HV + j;
   float *G = (float *)(sm + C_G);
   float *vec = (float *)(sm + C_VEC);
   float *beta = (float *)(sm + C_BETA);
   float *rb = (float *)(sm + C_RB);
   float *red = (float *)(sm + C_RED);  // [0, 64): sum_v dX v; [64, 192): d(2^G_last)
-  uint64_t *bar = (uint64_t *)(sm + C_MISC);
-  uint32_t *tslot = (uint32_t *)(sm + C_MISC + 8);
-  uint64_t *bar_ld = (uint64_t *)(sm + C_MISC + 16);
+  uint64_t *bar_s = (uint64_t *)(sm + C_MISC), *bar_p1 = bar_s + 1, *bar_p2 = bar_s + 2;
+  uint64_t *bar_kq = bar_s + 3, *bar = bar_s + 4;
+  uint32_t *tslot = (uint32_t *)(sm + C_MISC + 40);
   constexpr float qscale = 0.08838834764831845f;
   KDA_PT_DECL;
 
-  // ---- loads.  Bulk copies (one thread, counted on bar_ld): the saved tiles
-  // X^T, D^T, h, dh', dX, dD, A verbatim (dX, dD: one 8 KB piece per 64-column
-  // sub-tile of the stacked [dX; dO; dD] operand) and, by TMA, the dO and v rows.
-  // cp.async: G and beta. ----
   if (tid == 0) {
-    bar_init(bar, 1);
-    bar_init(bar_ld, 1);
+    for (int b = 0; b < 5; ++b) bar_init(bar_s + b, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  __syncthreads();
-  if (tid == 0) {
-    mbar_expect_tx(bar_ld, 2 * 16384u + 2 * 32768u + 2 * 16384u + 8192u + 2 * 16384u);
-    bulk_load(sbase + I_XT, W.tc_xt + slot * 16384, 16384u, bar_ld);
-    bulk_load(sbase + I_DT, W.tc_dt + slot * 16384, 16384u, bar_ld);
-    bulk_load(sbase + I_H, W.tc_hs + slot * kD * kD, 32768u, bar_ld);
-    bulk_load(sbase + I_DH, W.tc_dh + slot * kD * kD, 32768u, bar_ld);
-    const unsigned char *dx = reinterpret_cast<const unsigned char *>(W.tc_dx + slot * kC * kD);
-    const unsigned char *dd = reinterpret_cast<const unsigned char *>(W.tc_dd + slot * kC * kD);
-    bulk_load(sbase + I_STK, dx, 8192u, bar_ld);                        // rows 0..63, sub-tile 0
-    bulk_load(sbase + I_STK + 192 * 128, dx + 8192, 8192u, bar_ld);     //               sub-tile 1
-    bulk_load(sbase + I_STK + 128 * 128, dd, 8192u, bar_ld);            // rows 128..191
-    bulk_load(sbase + I_STK + 320 * 128, dd + 8192, 8192u, bar_ld);
-    bulk_load(sbase + C_A, W.tc_tiles + slot * kTileRecord + kRecAM, 8192u, bar_ld);
-    tma_load3(sbase + I_STK + 64 * 128, &maps.d, 0, j, t0, bar_ld);    // dO rows 64..127
-    tma_load3(sbase + I_STK + 256 * 128, &maps.d, 64, j, t0, bar_ld);
-    tma_tile(sbase + I_V, &maps.v, j, t0, bar_ld);
-  }
-  load_gate<kCT>(sbase + C_G, P.g, t0, len, HV, j);
-  if (tid < kC) {
-    if (tid < len) cp4(smem_u32(beta + tid), P.beta + (size_t)(t0 + tid) * HV + j);
-    else beta[tid] = 0.f;
-  }
-  cp_commit();
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
-  KDA_PT(13);
-  bar_wait(bar_ld, 0, args.err);
-  if (len < kC)  // dO rows past the sequence end hold other tokens: clear them
-    for (int it = tid; it < (kC - len) * 16; it += kCT) {
-      const int r = 64 + len + (it >> 4), q = it & 15;
-      *reinterpret_cast<uint4 *>(sm + I_STK + sw_chunk(r, q, 192)) = make_uint4(0, 0, 0, 0);
-    }
-  cp_wait_all();
-  fence_async_smem();
   fence_before();
   __syncthreads();
   fence_after();
-  KDA_PT(14);
   const uint32_t tmem = *tslot;
   const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
 
-  // ---- tensor-core products ----
-  if (tid == 0) {
-    // (dX h^T)[r][c] = sum_v dX[r][v] h[c][v] and (dO h^T)[r][c]   (M=64 r, N=128 c, K=128 v)
-    const uint32_t id3 = idesc(64, 128, 0, 0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mma(tmem, desc_k16(sbase + I_STK, k, 192), desc_k16(sbase + I_H, k, kD), id3, k > 0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      mma(tmem + 128, desc_k16(sbase + I_STK + 64 * 128, k, 192), desc_k16(sbase + I_H, k, kD), id3, k > 0);
-    // dKhat[r][c] = sum_v D[r][v] dh'[c][v]   (M=64 r, N=128 c, K=128 v)
-    const uint32_t id4 = idesc(64, 128, 1, 0), id5 = idesc(128, 128, 1, 0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mma(tmem + 256, desc_mn(sbase + I_DT, k, 8192), desc_k16(sbase + I_DH, k, kD), id4, k > 0);
-    // Z[i'][n'] = sum_v [X; D][i'][v] [dO; dD][n'][v]   (M=128, N=128, K=128 v)
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      mma(tmem + 384, desc_mn(sbase + I_XT, k, 16384), desc_k16(sbase + I_STK + 64 * 128, k, 192), id5, k > 0);
-    commit(bar);
-  }
-  // meanwhile on the other warps (warp 0 only issues the products): warps 4..7
-  // d(2^G_last)[c] = sum_v dh'[c][v] h[c][v]; warps 1..3, 8..15 dv = beta dX and sum_v dX v
-  if (warp >= 4 && warp < 8) {
-    const int c = tid - kD;
-    float acc = 0.f;
-#pragma unroll 4
-    for (int jj = 0; jj < 16; ++jj) {
-      float a[8], b[8];
-      unpack8(*reinterpret_cast<const uint4 *>(sm + I_H + sw_chunk(c, jj, kD)), a);
-      unpack8(*reinterpret_cast<const uint4 *>(sm + I_DH + sw_chunk(c, jj, kD)), b);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc = fmaf(a[e], b[e], acc);
+  int64_t s_idx = blockIdx.x;
+  Slot cur;
+  bool have = get_slot(P, W, s_idx, cur);
+  if (have) {  // the first slot: every group at once
+    if (tid == 0) {
+      issue_s(sbase, W, maps, cur, bar_s);
+      issue_p1(sbase, W, maps, cur, bar_p1);
+      issue_p2(sbase, W, maps, cur, bar_p2);
     }
-    red[64 + c] = acc;
+    issue_gate_beta(sbase, P, beta, cur);
   }
-  const int rw = warp < 4 ? warp - 1 : warp - 5;  // 0..10 on warps 1..3 and 8..15
-  for (int r = rw; warp != 0 && (warp < 4 || warp >= 8) && r < kC; r += 11) {  // one warp per row, 4 columns per lane
-    float part = 0.f;
-    if (r < len) {
-      const float br = beta[r];
-      const int v0 = lane * 4;
-      const uint2 xd = *reinterpret_cast<const uint2 *>(sm + I_STK + sw_off(r, v0, 192));
-      const uint2 xv = *reinterpret_cast<const uint2 *>(sm + I_V + sw_off(r, v0, kC));
-      const float2 d01 = unpack_bf16(xd.x), d23 = unpack_bf16(xd.y);
-      const float2 v01 = unpack_bf16(xv.x), v23 = unpack_bf16(xv.y);
-      *reinterpret_cast<uint2 *>(args.dv + ((size_t)(t0 + r) * HV + j) * kD + v0) =
-          make_uint2(pack_bf16(br * d01.x, br * d01.y), pack_bf16(br * d23.x, br * d23.y));
-      part = d01.x * v01.x + d01.y * v01.y + d23.x * v23.x + d23.y * v23.y;
-      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    }
-    if (lane == 0) red[r] = part;
-  }
-  KDA_PT(15);
-  bar_wait(bar, 0, args.err);
-  fence_after();
-  __syncthreads();  // products in TMEM; the operand tiles are dead
-  KDA_PT(0);
-
-  // ---- raw k, q rows for the decay tiles; dA^T, dAqk^T out of TMEM as hi/lo tiles; gate cumsum ----
-  if (tid == 0) {  // raw k, q rows (TMA) into the dead operand tiles
+  for (uint32_t it = 0; have; ++it) {
+    const uint32_t par = it & 1u;
+    const int t0 = cur.t0, len = cur.len, j = cur.j, h = cur.h;
+    Slot nxt;
+    const bool more = get_slot(P, W, s_idx + gridDim.x, nxt);
+    bool ok = true;  // every bounded wait of this thread succeeded
+    KDA_PT(13);
+    ok &= bar_wait(bar_s, par, args.err);
+    ok &= bar_wait(bar_p1, par, args.err);
+    ok &= bar_wait(bar_p2, par, args.err);
+    if (len < kC)  // dO rows past the sequence end hold other tokens: clear them
+      for (int it2 = tid; it2 < (kC - len) * 16; it2 += kCT) {
+        const int r = 64 + len + (it2 >> 4), q = it2 & 15;
+        *reinterpret_cast<uint4 *>(sm + I_STK + sw_chunk(r, q, 192)) = make_uint4(0, 0, 0, 0);
+      }
+    cp_wait_all();  // G, beta
     fence_async_smem();
-    mbar_expect_tx(bar_ld, 32768u);
-    tma_tile(sbase + C_KRAW, &maps.k, h, t0, bar_ld);
-    tma_tile(sbase + C_QRAW, &maps.q, h, t0, bar_ld);
-  }
-  {
-    // Z: lanes 0..63 (i), cols 64..127 (m) = dA^T[i][m]; lanes 64..127, cols 0..63 = dAqk^T[i][r]
-    const int cg = warp >> 2, i = 32 * (quarter & 1) + lane;
-    const bool qk = quarter >= 2;
-    float x[16];
-    tmem_ld16(tq + 384u + (qk ? 0u : 64u) + (uint32_t)(16 * cg), x);
-#pragma unroll
-    for (int hx = 0; hx < 2; ++hx) {
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int col = 16 * cg + 8 * hx + e;
-        y[e] = (qk && i > col) ? 0.f : x[8 * hx + e];  // dAqk^T[i][r] is a gradient of Aqk only where i <= r
-      }
-      uint4 hi, lo;
-      split8(y, hi, lo);
-      const uint32_t off = sw_chunk(i, 2 * cg + hx, kC);
-      *reinterpret_cast<uint4 *>(sm + (qk ? C_DQK : C_DAB) + off) = hi;
-      *reinterpret_cast<uint4 *>(sm + (qk ? C_DQK : C_DAB) + LO64 + off) = lo;
-    }
-  }
-  // ---- G, block references, decay tiles Kr, Qr, Kc (hi/lo) ----
-  if (tid < kD) {
-    const int c = tid;
-    float s = 0.f;
-    float col[kC];
-#pragma unroll
-    for (int r = 0; r < kC; ++r) col[r] = G[r * kGLD + c];
-#pragma unroll
-    for (int r = 0; r < kC; ++r) {
-      if (r < len) s += col[r];
-      col[r] = s;
-    }
-#pragma unroll
-    for (int r = 0; r < kC; ++r) G[r * kGLD + c] = col[r];
-    const float gl = s;
-    vec[V_GL * kD + c] = gl;
-    vec[V_GAML * kD + c] = exp2f(gl);
-    float gref[4];
-#pragma unroll
-    for (int R = 0; R < 4; ++R) {
-      gref[R] = (16 * R < len) ? col[16 * R] : gl;
-      vec[(V_GREF + R) * kD + c] = gref[R];
-      vec[(V_EREF + R) * kD + c] = exp2f(gref[R]);
-      vec[(V_LAM + R) * kD + c] = exp2f(gl - gref[R]);
-    }
-    int p = 0;
-#pragma unroll
-    for (int R = 1; R < 4; ++R)
-#pragma unroll
-      for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
-  }
-  bar_wait(bar_ld, 1, args.err);  // raw k, q
-  if (len < kC) {  // rows past the sequence end hold other tokens: clear them
-    zero_tail<kCT>(sm + C_KRAW, len);
-    zero_tail<kCT>(sm + C_QRAW, len);
-  }
-  __syncthreads();
-  KDA_PT(1);
-  {
-    const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 3;  // two rows per thread
-    float gref[8];
-#pragma unroll
-    for (int e = 0; e < 8; e += 4)
-      *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (V_GREF + R) * kD + c0 + e);
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int r = rg * 2 + rr;
-      const uint32_t off = sw_chunk(r, jj, kC);
-      float kv[8], qv[8], o[8], e1[8], e2[8];
-      unpack8(*reinterpret_cast<const uint4 *>(sm + C_KRAW + off), kv);  // raw k, q (zero past len)
-      unpack8(*reinterpret_cast<const uint4 *>(sm + C_QRAW + off), qv);
-      if (P.l2norm) {  // q/k L2-norm prologue: the row's 16 chunks sit on this half-warp
-        float sk = 0.f, sq = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          sk = fmaf(kv[e], kv[e], sk);
-          sq = fmaf(qv[e], qv[e], sq);
-        }
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) {
-          sk += __shfl_xor_sync(0xffffffffu, sk, o);
-          sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        }
-        const float rk = 1.0f / sqrtf(sk + kL2NormEps), rq = 1.0f / sqrtf(sq + kL2NormEps);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          kv[e] *= rk;
-          qv[e] *= rq;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float g = G[r * kGLD + c0 + e];
-        e1[e] = exp2f(g - gref[e]);
-        e2[e] = exp2f(gref[e] - g);
-      }
-      uint4 hi, lo;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
-      split8(o, hi, lo);
-      *reinterpret_cast<uint4 *>(sm + C_KR + off) = hi;
-      *reinterpret_cast<uint4 *>(sm + C_KR + LO128 + off) = lo;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
-      split8(o, hi, lo);
-      *reinterpret_cast<uint4 *>(sm + C_QR + off) = hi;
-      *reinterpret_cast<uint4 *>(sm + C_QR + LO128 + off) = lo;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
-      split8(o, hi, lo);
-      *reinterpret_cast<uint4 *>(sm + C_KC + off) = hi;
-      *reinterpret_cast<uint4 *>(sm + C_KC + LO128 + off) = lo;
-    }
-  }
-  __syncthreads();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    KDA_PT(14);
 
-  KDA_PT(2);
-  // ---- T = A^T dA  (T[r][m] = sum_i' A[i'][r] dA[i'][m]; dA[i'][m] = dA^T[m][i']) ----
-  const int mt = warp >> 2, nq = warp & 3;  // 16-row block, 16-column quarter
-  {
-    float acc[2][4] = {};
+    // ---- tensor-core products ----
+    if (tid == 0) {
+      // (dX h^T)[r][c] = sum_v dX[r][v] h[c][v] and (dO h^T)[r][c]   (M=64 r, N=128 c, K=128 v)
+      const uint32_t id3 = idesc(64, 128, 0, 0);
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      uint32_t a[4], bh[4], bl[4];
-      lda_t(sbase + C_A, kC, 16 * mt, 16 * s, a);  // element (r, i') = A[i'][r]
-      ldb(sbase + C_DAB, kC, 16 * nq, 16 * s, bh);  // element (i', m) = dA^T[m][i']
-      ldb(sbase + C_DAB + LO64, kC, 16 * nq, 16 * s, bl);
-      mma16816(acc[0], a, bh[0], bh[1]);
-      mma16816(acc[0], a, bl[0], bl[1]);
-      mma16816(acc[1], a, bh[2], bh[3]);
-      mma16816(acc[1], a, bl[2], bl[3]);
+      for (int k = 0; k < 8; ++k) mma(tmem, desc_k16(sbase + I_STK, k, 192), desc_k16(sbase + I_H, k, kD), id3, k > 0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma(tmem + 128, desc_k16(sbase + I_STK + 64 * 128, k, 192), desc_k16(sbase + I_H, k, kD), id3, k > 0);
+      // dKhat[r][c] = sum_v D[r][v] dh'[c][v]   (M=64 r, N=128 c, K=128 v)
+      const uint32_t id4 = idesc(64, 128, 1, 0), id5 = idesc(128, 128, 1, 0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mma(tmem + 256, desc_mn(sbase + I_DT, k, 8192), desc_k16(sbase + I_DH, k, kD), id4, k > 0);
+      // Z[i'][n'] = sum_v [X; D][i'][v] [dO; dD][n'][v]   (M=128, N=128, K=128 v)
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma(tmem + 384, desc_mn(sbase + I_XT, k, 16384), desc_k16(sbase + I_STK + 64 * 128, k, 192), id5, k > 0);
+      commit(bar);
     }
+    // meanwhile on the other warps (warp 0 only issues the products): warps 4..7
+    // d(2^G_last)[c] = sum_v dh'[c][v] h[c][v]; warps 1..3, 8..15 dv = beta dX and sum_v dX v
+    if (warp >= 4 && warp < 8) {
+      const int c = tid - kD;
+      float acc = 0.f;
+#pragma unroll 4
+      for (int jj = 0; jj < 16; ++jj) {
+        float a[8], b[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sm + I_H + sw_chunk(c, jj, kD)), a);
+        unpack8(*reinterpret_cast<const uint4 *>(sm + I_DH + sw_chunk(c, jj, kD)), b);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * mt + (lane >> 2) + 8 * hh, m = 16 * nq + 8 * nt + (lane & 3) * 2;
-        st_split2(sm + C_T, LO64, r, m, kC, acc[nt][2 * hh], acc[nt][2 * hh + 1]);
+        for (int e = 0; e < 8; ++e) acc = fmaf(a[e], b[e], acc);
       }
-  }
-  __syncthreads();
-  KDA_PT(3);
-  // ---- dL = -tril_{-1}(T A^T); X = beta dL ----
-  {
-    float acc[2][4] = {};
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      uint32_t ah[4], al[4], b[4];
-      lda(sbase + C_T, kC, 16 * mt, 16 * s, ah);  // element (r, m) = T[r][m]
-      lda(sbase + C_T + LO64, kC, 16 * mt, 16 * s, al);
-      ldb(sbase + C_A, kC, 16 * nq, 16 * s, b);  // element (m, i) = A[i][m]
-      mma16816(acc[0], ah, b[0], b[1]);
-      mma16816(acc[0], al, b[0], b[1]);
-      mma16816(acc[1], ah, b[2], b[3]);
-      mma16816(acc[1], al, b[2], b[3]);
+      red[64 + c] = acc;
     }
-    __syncthreads();  // every warp has read dA^T: its tiles become dL
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * mt + (lane >> 2) + 8 * hh, i = 16 * nq + 8 * nt + (lane & 3) * 2;
-        const float d0 = (i < r) ? -acc[nt][2 * hh] : 0.f, d1 = (i + 1 < r) ? -acc[nt][2 * hh + 1] : 0.f;
-        st_split2(sm + C_DAB, LO64, r, i, kC, d0, d1);
-        st_split2(sm + C_XB, LO64, r, i, kC, beta[r] * d0, beta[r] * d1);
-      }
-  }
-  __syncthreads();
-  KDA_PT(4);
-  // ---- pairwise chains: warp owns rows 16B..16B+15 (as r and as i), columns ch0 .. ch0+31 ----
-  // Block-pair products are formed in a temporary, scaled by the per-channel
-  // factor D_RI in fp32, and added to the accumulators.
-  // (row block = the warp's TMEM lane quarter, so that the assembly reads its products from TMEM)
-  const int Bk = warp & 3, ch0 = 32 * (warp >> 2);
-  float xr[4][4] = {}, yr[4][4] = {}, xyi[4][4] = {};  // xyi = xi + yi (only their sum is used)
-  for (int I = 0; I <= Bk; ++I) {  // row side: R = Bk, I = 0..Bk
-    const float *Dv = (I < Bk) ? vec + (V_D + Bk * (Bk - 1) / 2 + I) * kD : nullptr;
-    uint32_t aLh[4], aLl[4], aQh[4], aQl[4];
-    lda(sbase + C_DAB, kC, 16 * Bk, 16 * I, aLh);  // dL[r][i]
-    lda(sbase + C_DAB + LO64, kC, 16 * Bk, 16 * I, aLl);
-    lda_t(sbase + C_DQK, kC, 16 * Bk, 16 * I, aQh);  // dAqk[r][i] = dAqk^T[i][r]
-    lda_t(sbase + C_DQK + LO64, kC, 16 * Bk, 16 * I, aQl);
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      uint32_t bh[4], bl[4];
-      ldb_t(sbase + C_KC, kC, ch0 + 16 * nb, 16 * I, bh);  // element (i, c) = Kc[i][c]
-      ldb_t(sbase + C_KC + LO128, kC, ch0 + 16 * nb, 16 * I, bl);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        float tx[4] = {}, ty[4] = {};
-        mma3(tx, aLh, aLl, bh[2 * t], bh[2 * t + 1], bl[2 * t], bl[2 * t + 1]);
-        mma3(ty, aQh, aQl, bh[2 * t], bh[2 * t + 1], bl[2 * t], bl[2 * t + 1]);
-        const int c = ch0 + 16 * nb + 8 * t + (lane & 3) * 2;
-        const float d0 = Dv ? Dv[c] : 1.f, d1 = Dv ? Dv[c + 1] : 1.f;
-        float(&X)[4] = xr[2 * nb + t];
-        float(&Y)[4] = yr[2 * nb + t];
-        X[0] = fmaf(d0, tx[0], X[0]); X[1] = fmaf(d1, tx[1], X[1]); X[2] = fmaf(d0, tx[2], X[2]); X[3] = fmaf(d1, tx[3], X[3]);
-        Y[0] = fmaf(d0, ty[0], Y[0]); Y[1] = fmaf(d1, ty[1], Y[1]); Y[2] = fmaf(d0, ty[2], Y[2]); Y[3] = fmaf(d1, ty[3], Y[3]);
-      }
-    }
-  }
-  for (int R = Bk; R < 4; ++R) {  // column side: I = Bk, R = Bk..3
-    const float *Dv = (R > Bk) ? vec + (V_D + R * (R - 1) / 2 + Bk) * kD : nullptr;
-    uint32_t aXh[4], aXl[4], aQh[4], aQl[4];
-    lda_t(sbase + C_XB, kC, 16 * Bk, 16 * R, aXh);  // element (i, r) = X[r][i]
-    lda_t(sbase + C_XB + LO64, kC, 16 * Bk, 16 * R, aXl);
-    lda(sbase + C_DQK, kC, 16 * Bk, 16 * R, aQh);  // element (i, r) = dAqk^T[i][r]
-    lda(sbase + C_DQK + LO64, kC, 16 * Bk, 16 * R, aQl);
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      uint32_t kh[4], kl[4], qh[4], ql[4];
-      ldb_t(sbase + C_KR, kC, ch0 + 16 * nb, 16 * R, kh);  // element (r, c) = Kr[r][c]
-      ldb_t(sbase + C_KR + LO128, kC, ch0 + 16 * nb, 16 * R, kl);
-      ldb_t(sbase + C_QR, kC, ch0 + 16 * nb, 16 * R, qh);
-      ldb_t(sbase + C_QR + LO128, kC, ch0 + 16 * nb, 16 * R, ql);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        float tx[4] = {};  // X Kr + dAqk Qr of this block pair, before the channel decay
-        mma3(tx, aXh, aXl, kh[2 * t], kh[2 * t + 1], kl[2 * t], kl[2 * t + 1]);
-        mma3(tx, aQh, aQl, qh[2 * t], qh[2 * t + 1], ql[2 * t], ql[2 * t + 1]);
-        const int c = ch0 + 16 * nb + 8 * t + (lane & 3) * 2;
-        const float d0 = Dv ? Dv[c] : 1.f, d1 = Dv ? Dv[c + 1] : 1.f;
-        float(&X)[4] = xyi[2 * nb + t];
-        X[0] = fmaf(d0, tx[0], X[0]); X[1] = fmaf(d1, tx[1], X[1]); X[2] = fmaf(d0, tx[2], X[2]); X[3] = fmaf(d1, tx[3], X[3]);
-      }
-    }
-  }
-  __syncthreads();  // every warp is done with the chain tiles: dL .. T become the assembly scratch
-  KDA_PT(5);
-
-  // ---- assembly (fragment element (r, c)), in four passes of 8 columns per warp ----
-  // Each pass reads this warp's 16 x 8 blocks of dX h^T (= -dBk), dO h^T (= dQg)
-  // and dKhat straight out of tensor memory, in the C-fragment order of the
-  // chain accumulators.  Raw k and q are not re-read: every term that needs them
-  // is a product with a decay factor that the hi/lo tiles Kr = k e1, Qr = q~ e1,
-  // Kc = k e2 hold.  dg = reverse cumsum of dG over the chunk runs once, after
-  // the last pass, as column scans over 16-row segments with segment totals
-  // exchanged in shared memory.
-  float *totQ = (float *)(sm + C_TOT), *totP = totQ + 4 * kD, *totC = totP + 4 * kD;
-  const float *dglv = red + 64;
-  const int i8 = lane >> 2, l4 = lane & 3;
-  float bpart[2] = {0.f, 0.f};
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    KDA_PT(9);
-    {
-      const int nt = g;
-      const int c = ch0 + 8 * nt + 2 * l4;
-      float px[4], po[4], pk[4];  // element (i8 + 8 hh, c + u) at index 2 hh + u
-      {
-        const uint32_t tb = tmem + ((uint32_t)(32 * Bk) << 16) + (uint32_t)(ch0 + 8 * nt);
-        tmem_ld_frag3(tb, tb + 128u, tb + 256u, px, po, pk);
-      }
-      const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
-      const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
-      const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
-      float cq[2] = {0.f, 0.f};
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * Bk + i8 + 8 * hh;
+    const int rw = warp < 4 ? warp - 1 : warp - 5;  // 0..10 on warps 1..3 and 8..15
+    for (int r = rw; warp != 0 && (warp < 4 || warp >= 8) && r < kC; r += 11) {  // one warp per row, 4 columns per lane
+      float part = 0.f;
+      if (r < len) {
         const float br = beta[r];
-        const float2 vq = make_float2(po[2 * hh], po[2 * hh + 1]);
-        const float2 vb = make_float2(-px[2 * hh], -px[2 * hh + 1]);
-        const float2 vk = make_float2(pk[2 * hh], pk[2 * hh + 1]);
-        const uint32_t to = sw_off(r, c, kC);
-        uint32_t *krh_p = reinterpret_cast<uint32_t *>(sm + C_KR + to), *krl_p = reinterpret_cast<uint32_t *>(sm + C_KR + LO128 + to);
-        uint32_t *qrh_p = reinterpret_cast<uint32_t *>(sm + C_QR + to), *qrl_p = reinterpret_cast<uint32_t *>(sm + C_QR + LO128 + to);
-        const float2 krh = unpack_bf16(*krh_p), krl = unpack_bf16(*krl_p);
-        const float2 qrh = unpack_bf16(*qrh_p), qrl = unpack_bf16(*qrl_p);
-        const float2 kch = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + to));
-        const float2 kcl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + LO128 + to));
-        const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
-        float dq2[2], dk2[2], qv[2], pv[2];
+        const int v0 = lane * 4;
+        const uint2 xd = *reinterpret_cast<const uint2 *>(sm + I_STK + sw_off(r, v0, 192));
+        const uint2 xv = *reinterpret_cast<const uint2 *>(sm + I_V + sw_off(r, v0, kC));
+        const float2 d01 = unpack_bf16(xd.x), d23 = unpack_bf16(xd.y);
+        const float2 v01 = unpack_bf16(xv.x), v23 = unpack_bf16(xv.y);
+        *reinterpret_cast<uint2 *>(args.dv + ((size_t)(t0 + r) * HV + j) * kD + v0) =
+            make_uint2(pack_bf16(br * d01.x, br * d01.y), pack_bf16(br * d23.x, br * d23.y));
+        part = d01.x * v01.x + d01.y * v01.y + d23.x * v23.x + d23.y * v23.y;
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      }
+      if (lane == 0) red[r] = part;
+    }
+    KDA_PT(15);
+    ok &= bar_wait(bar, par, args.err);
+    fence_after();
+    __syncthreads();  // products in TMEM; the operand tiles are dead
+    KDA_PT(0);
+
+    // ---- raw k, q rows for the decay tiles; dA^T, dAqk^T out of TMEM as hi/lo tiles; gate cumsum ----
+    if (tid == 0) {  // raw k, q rows (TMA) into the dead operand tiles
+      fence_async_smem();
+      mbar_expect_tx(bar_kq, 32768u);
+      tma_tile(sbase + C_KRAW, &maps.k, h, t0, bar_kq);
+      tma_tile(sbase + C_QRAW, &maps.q, h, t0, bar_kq);
+    }
+    {
+      // Z: lanes 0..63 (i), cols 64..127 (m) = dA^T[i][m]; lanes 64..127, cols 0..63 = dAqk^T[i][r]
+      const int cg = warp >> 2, i = 32 * (quarter & 1) + lane;
+      const bool qk = quarter >= 2;
+      float x[16];
+      tmem_ld16(tq + 384u + (qk ? 0u : 64u) + (uint32_t)(16 * cg), x);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float Kr = u ? krh.y + krl.y : krh.x + krl.x;  // k e1
-          const float Qr = u ? qrh.y + qrl.y : qrh.x + qrl.x;  // q~ e1
-          const float Kc = u ? kch.y + kcl.y : kch.x + kcl.x;  // k e2
-          const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = u ? vk.y : vk.x;
-          const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
-          const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
-          const float e1 = exp2f(gg_ - gref), e2 = exp2f(gref - gg_);
-          const float gam = e1 * eref, kh = e2 * lam;
-          const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
-          const float xyI = xyi[nt][2 * hh + u];
-          dq2[u] = dQg * gam + e1 * yR;
-          dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * xyI;
-          // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
-          const bool in = r < len;
-          qv[u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
-          pv[u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * xyI - dKh * Kc * lam) : 0.f;
-          bpart[hh] += dBk * Kr * eref + Kr * xR;
-          cq[u] += dKh * Kc * lam;
+      for (int hx = 0; hx < 2; ++hx) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int col = 16 * cg + 8 * hx + e;
+          y[e] = (qk && i > col) ? 0.f : x[8 * hx + e];  // dAqk^T[i][r] is a gradient of Aqk only where i <= r
         }
-        // dG of (r, c) and (r, c + 1) into the Kr (Q part) and Qr (P part) pair slots just read
-        *krh_p = __float_as_uint(qv[0]);
-        *krl_p = __float_as_uint(qv[1]);
-        *qrh_p = __float_as_uint(pv[0]);
-        *qrl_p = __float_as_uint(pv[1]);
-        if (r < len) {
-          const size_t tok = (size_t)(t0 + r);
-          if (args.partial) {
-            float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
-            *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
-            *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
-          } else {
-            __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
-            __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
-            *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
-            *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
+        uint4 hi, lo;
+        split8(y, hi, lo);
+        const uint32_t off = sw_chunk(i, 2 * cg + hx, kC);
+        *reinterpret_cast<uint4 *>(sm + (qk ? C_DQK : C_DAB) + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + (qk ? C_DQK : C_DAB) + LO64 + off) = lo;
+      }
+    }
+    // ---- G, block references, decay tiles Kr, Qr, Kc (hi/lo) ----
+    if (tid < kD) {
+      const int c = tid;
+      float s = 0.f;
+      float col[kC];
+#pragma unroll
+      for (int r = 0; r < kC; ++r) col[r] = G[r * kGLD + c];
+#pragma unroll
+      for (int r = 0; r < kC; ++r) {
+        if (r < len) s += col[r];
+        col[r] = s;
+      }
+#pragma unroll
+      for (int r = 0; r < kC; ++r) G[r * kGLD + c] = col[r];
+      const float gl = s;
+      vec[V_GL * kD + c] = gl;
+      vec[V_GAML * kD + c] = exp2f(gl);
+      float gref[4];
+#pragma unroll
+      for (int R = 0; R < 4; ++R) {
+        gref[R] = (16 * R < len) ? col[16 * R] : gl;
+        vec[(V_GREF + R) * kD + c] = gref[R];
+        vec[(V_EREF + R) * kD + c] = exp2f(gref[R]);
+        vec[(V_LAM + R) * kD + c] = exp2f(gl - gref[R]);
+      }
+      int p = 0;
+#pragma unroll
+      for (int R = 1; R < 4; ++R)
+#pragma unroll
+        for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
+    }
+    ok &= bar_wait(bar_kq, par, args.err);  // raw k, q
+    if (len < kC) {  // rows past the sequence end hold other tokens: clear them
+      zero_tail<kCT>(sm + C_KRAW, len);
+      zero_tail<kCT>(sm + C_QRAW, len);
+    }
+    __syncthreads();
+    KDA_PT(1);
+    {
+      const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 3;  // two rows per thread
+      float gref[8];
+#pragma unroll
+      for (int e = 0; e < 8; e += 4)
+        *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (V_GREF + R) * kD + c0 + e);
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int r = rg * 2 + rr;
+        const uint32_t off = sw_chunk(r, jj, kC);
+        float kv[8], qv[8], o[8], e1[8], e2[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sm + C_KRAW + off), kv);  // raw k, q (zero past len)
+        unpack8(*reinterpret_cast<const uint4 *>(sm + C_QRAW + off), qv);
+        if (P.l2norm) {  // q/k L2-norm prologue: the row's 16 chunks sit on this half-warp
+          float sk = 0.f, sq = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            sk = fmaf(kv[e], kv[e], sk);
+            sq = fmaf(qv[e], qv[e], sq);
+          }
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) {
+            sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            sq += __shfl_xor_sync(0xffffffffu, sq, o);
+          }
+          const float rk = 1.0f / sqrtf(sk + kL2NormEps), rq = 1.0f / sqrtf(sq + kL2NormEps);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            kv[e] *= rk;
+            qv[e] *= rq;
           }
         }
-      }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {  // column sums of dKhat k khat over the warp's 16 rows
-        float cs = cq[u];
-        cs += __shfl_xor_sync(0xffffffffu, cs, 4);
-        cs += __shfl_xor_sync(0xffffffffu, cs, 8);
-        cs += __shfl_xor_sync(0xffffffffu, cs, 16);
-        if (i8 == 0) totC[Bk * kD + c + u] = cs;
+        for (int e = 0; e < 8; ++e) {
+          const float g = G[r * kGLD + c0 + e];
+          e1[e] = exp2f(g - gref[e]);
+          e2[e] = exp2f(gref[e] - g);
+        }
+        uint4 hi, lo;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
+        split8(o, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + C_KR + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + C_KR + LO128 + off) = lo;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
+        split8(o, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + C_QR + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + C_QR + LO128 + off) = lo;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
+        split8(o, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + C_KC + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + C_KC + LO128 + off) = lo;
       }
     }
-    KDA_PT(10);
-  }
-  __syncthreads();  // every thread has parked its dG and its Khat column terms
-  KDA_PT(11);
-  {  // dg = reverse cumsum of dG: thread = one column, one 16-row segment (4 segments)
-    const int c = tid & (kD - 1), seg = tid >> 7, mid = len >> 1;
-    // element (r, c) of the parked dG: even c in the hi slot of its pair, odd c in the lo slot
-    const uint32_t po = (c & 1) ? LO128 : 0u;
-    float q16[16], p16[16], tq = 0.f, tp = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const uint32_t to = sw_off(16 * seg + k, c & ~1, kC) + po;
-      q16[k] = *reinterpret_cast<const float *>(sm + C_KR + to);
-      p16[k] = *reinterpret_cast<const float *>(sm + C_QR + to);
-      tq += q16[k];
-      tp += p16[k];
-    }
-    totQ[seg * kD + c] = tq;
-    totP[seg * kD + c] = tp;
     __syncthreads();
-    float aq = 0.f, aps = 0.f, app = 0.f;
+
+    KDA_PT(2);
+    // ---- T = A^T dA  (T[r][m] = sum_i' A[i'][r] dA[i'][m]; dA[i'][m] = dA^T[m][i']) ----
+    const int mt = warp >> 2, nq = warp & 3;  // 16-row block, 16-column quarter
+    {
+      float acc[2][4] = {};
 #pragma unroll
-    for (int s2 = 0; s2 < 4; ++s2) {
-      const float a = totQ[s2 * kD + c], b = totP[s2 * kD + c];
-      if (s2 > seg) { aq += a; aps += b; }
-      if (s2 < seg) app += b;
+      for (int s = 0; s < 4; ++s) {
+        uint32_t a[4], bh[4], bl[4];
+        lda_t(sbase + C_A, kC, 16 * mt, 16 * s, a);  // element (r, i') = A[i'][r]
+        ldb(sbase + C_DAB, kC, 16 * nq, 16 * s, bh);  // element (i', m) = dA^T[m][i']
+        ldb(sbase + C_DAB + LO64, kC, 16 * nq, 16 * s, bl);
+        mma16816(acc[0], a, bh[0], bh[1]);
+        mma16816(acc[0], a, bl[0], bl[1]);
+        mma16816(acc[1], a, bh[2], bh[3]);
+        mma16816(acc[1], a, bl[2], bl[3]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * mt + (lane >> 2) + 8 * hh, m = 16 * nq + 8 * nt + (lane & 3) * 2;
+          st_split2(sm + C_T, LO64, r, m, kC, acc[nt][2 * hh], acc[nt][2 * hh + 1]);
+        }
     }
-    const float ks = totC[c] + totC[kD + c] + totC[2 * kD + c] + totC[3 * kD + c];
-    // dg_t = sum_{s>=t} dG_s: the Q part and the carried-state decay term
-    // from the chunk end; the zero-sum P part from whichever end is nearer
-    // (sum_{s>=t} P_s = -sum_{s<t} P_s, the Khat column sum counted at the
-    // last row), halving the cancelling terms it sums.
-    const float carried = kLn2 * vec[V_GAML * kD + c] * dglv[c];
-    float pre[16];
-    pre[0] = app;
+    __syncthreads();
+    KDA_PT(3);
+    // ---- dL = -tril_{-1}(T A^T); X = beta dL ----
+    {
+      float acc[2][4] = {};
 #pragma unroll
-    for (int k = 1; k < 16; ++k) pre[k] = pre[k - 1] + p16[k - 1];
-    float qs = aq, ps = aps + kLn2 * ks;
+      for (int s = 0; s < 4; ++s) {
+        uint32_t ah[4], al[4], b[4];
+        lda(sbase + C_T, kC, 16 * mt, 16 * s, ah);  // element (r, m) = T[r][m]
+        lda(sbase + C_T + LO64, kC, 16 * mt, 16 * s, al);
+        ldb(sbase + C_A, kC, 16 * nq, 16 * s, b);  // element (m, i) = A[i][m]
+        mma16816(acc[0], ah, b[0], b[1]);
+        mma16816(acc[0], al, b[0], b[1]);
+        mma16816(acc[1], ah, b[2], b[3]);
+        mma16816(acc[1], al, b[2], b[3]);
+      }
+      __syncthreads();  // every warp has read dA^T: its tiles become dL
 #pragma unroll
-    for (int k = 15; k >= 0; --k) {
-      const int r = 16 * seg + k;
-      qs += q16[k];
-      ps += p16[k];
-      if (r < len) args.dg[((size_t)(t0 + r) * HV + j) * kD + c] = qs + carried + (r >= mid ? ps : -pre[k]);
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * mt + (lane >> 2) + 8 * hh, i = 16 * nq + 8 * nt + (lane & 3) * 2;
+          const float d0 = (i < r) ? -acc[nt][2 * hh] : 0.f, d1 = (i + 1 < r) ? -acc[nt][2 * hh + 1] : 0.f;
+          st_split2(sm + C_DAB, LO64, r, i, kC, d0, d1);
+          st_split2(sm + C_XB, LO64, r, i, kC, beta[r] * d0, beta[r] * d1);
+        }
     }
-  }
-  KDA_PT(12);
-  KDA_PT(6);
-  // dbeta partials: reduce over the 4 lanes sharing a row, then per column half
+    __syncthreads();
+    KDA_PT(4);
+    // ---- pairwise chains: warp owns rows 16B..16B+15 (as r and as i), columns ch0 .. ch0+31 ----
+    // Block-pair products are formed in a temporary, scaled by the per-channel
+    // factor D_RI in fp32, and added to the accumulators.
+    // (row block = the warp's TMEM lane quarter, so that the assembly reads its products from TMEM)
+    const int Bk = warp & 3, ch0 = 32 * (warp >> 2);
+    float xr[4][4] = {}, yr[4][4] = {}, xyi[4][4] = {};  // xyi = xi + yi (only their sum is used)
+    for (int I = 0; I <= Bk; ++I) {  // row side: R = Bk, I = 0..Bk
+      const float *Dv = (I < Bk) ? vec + (V_D + Bk * (Bk - 1) / 2 + I) * kD : nullptr;
+      uint32_t aLh[4], aLl[4], aQh[4], aQl[4];
+      lda(sbase + C_DAB, kC, 16 * Bk, 16 * I, aLh);  // dL[r][i]
+      lda(sbase + C_DAB + LO64, kC, 16 * Bk, 16 * I, aLl);
+      lda_t(sbase + C_DQK, kC, 16 * Bk, 16 * I, aQh);  // dAqk[r][i] = dAqk^T[i][r]
+      lda_t(sbase + C_DQK + LO64, kC, 16 * Bk, 16 * I, aQl);
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    float v = bpart[hh];
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    v += __shfl_xor_sync(0xffffffffu, v, 2);
-    if (l4 == 0) rb[(warp >> 2) * kC + 16 * Bk + i8 + 8 * hh] = v;
-  }
-  __syncthreads();
-  KDA_PT(7);
-  if (tid < kC && tid < len)
-    args.dbeta[(size_t)(t0 + tid) * HV + j] = red[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
-  KDA_PT(8);
+      for (int nb = 0; nb < 2; ++nb) {
+        uint32_t bh[4], bl[4];
+        ldb_t(sbase + C_KC, kC, ch0 + 16 * nb, 16 * I, bh);  // element (i, c) = Kc[i][c]
+        ldb_t(sbase + C_KC + LO128, kC, ch0 + 16 * nb, 16 * I, bl);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          float tx[4] = {}, ty[4] = {};
+          mma3(tx, aLh, aLl, bh[2 * t], bh[2 * t + 1], bl[2 * t], bl[2 * t + 1]);
+          mma3(ty, aQh, aQl, bh[2 * t], bh[2 * t + 1], bl[2 * t], bl[2 * t + 1]);
+          const int c = ch0 + 16 * nb + 8 * t + (lane & 3) * 2;
+          const float d0 = Dv ? Dv[c] : 1.f, d1 = Dv ? Dv[c + 1] : 1.f;
+          float(&X)[4] = xr[2 * nb + t];
+          float(&Y)[4] = yr[2 * nb + t];
+          X[0] = fmaf(d0, tx[0], X[0]); X[1] = fmaf(d1, tx[1], X[1]); X[2] = fmaf(d0, tx[2], X[2]); X[3] = fmaf(d1, tx[3], X[3]);
+          Y[0] = fmaf(d0, ty[0], Y[0]); Y[1] = fmaf(d1, ty[1], Y[1]); Y[2] = fmaf(d0, ty[2], Y[2]); Y[3] = fmaf(d1, ty[3], Y[3]);
+        }
+      }
+    }
+    for (int R = Bk; R < 4; ++R) {  // column side: I = Bk, R = Bk..3
+      const float *Dv = (R > Bk) ? vec + (V_D + R * (R - 1) / 2 + Bk) * kD : nullptr;
+      uint32_t aXh[4], aXl[4], aQh[4], aQl[4];
+      lda_t(sbase + C_XB, kC, 16 * Bk, 16 * R, aXh);  // element (i, r) = X[r][i]
+      lda_t(sbase + C_XB + LO64, kC, 16 * Bk, 16 * R, aXl);
+      lda(sbase + C_DQK, kC, 16 * Bk, 16 * R, aQh);  // element (i, r) = dAqk^T[i][r]
+      lda(sbase + C_DQK + LO64, kC, 16 * Bk, 16 * R, aQl);
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        uint32_t kh[4], kl[4], qh[4], ql[4];
+        ldb_t(sbase + C_KR, kC, ch0 + 16 * nb, 16 * R, kh);  // element (r, c) = Kr[r][c]
+        ldb_t(sbase + C_KR + LO128, kC, ch0 + 16 * nb, 16 * R, kl);
+        ldb_t(sbase + C_QR, kC, ch0 + 16 * nb, 16 * R, qh);
+        ldb_t(sbase + C_QR + LO128, kC, ch0 + 16 * nb, 16 * R, ql);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          float tx[4] = {};  // X Kr + dAqk Qr of this block pair, before the channel decay
+          mma3(tx, aXh, aXl, kh[2 * t], kh[2 * t + 1], kl[2 * t], kl[2 * t + 1]);
+          mma3(tx, aQh, aQl, qh[2 * t], qh[2 * t + 1], ql[2 * t], ql[2 * t + 1]);
+          const int c = ch0 + 16 * nb + 8 * t + (lane & 3) * 2;
+          const float d0 = Dv ? Dv[c] : 1.f, d1 = Dv ? Dv[c + 1] : 1.f;
+          float(&X)[4] = xyi[2 * nb + t];
+          X[0] = fmaf(d0, tx[0], X[0]); X[1] = fmaf(d1, tx[1], X[1]); X[2] = fmaf(d0, tx[2], X[2]); X[3] = fmaf(d1, tx[3], X[3]);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with the chain tiles: dL .. T become the assembly scratch
+    KDA_PT(5);
+    if (more && tid == 0) {  // the next slot's dh', v, A into the dead dAqk^T, X, T and A tiles
+      fence_async_smem();
+      issue_p1(sbase, W, maps, nxt, bar_p1);
+    }
+
+    // ---- assembly (fragment element (r, c)), in four passes of 8 columns per warp ----
+    // Each pass reads this warp's 16 x 8 blocks of dX h^T (= -dBk), dO h^T (= dQg)
+    // and dKhat straight out of tensor memory, in the C-fragment order of the
+    // chain accumulators.  Raw k and q are not re-read: every term that needs them
+    // is a product with a decay factor that the hi/lo tiles Kr = k e1, Qr = q~ e1,
+    // Kc = k e2 hold.  dg = reverse cumsum of dG over the chunk runs once, after
+    // the last pass, as column scans over 16-row segments with segment totals
+    // exchanged in shared memory.
+    float *totQ = (float *)(sm + C_TOT), *totP = totQ + 4 * kD, *totC = totP + 4 * kD;
+    const float *dglv = red + 64;
+    const int i8 = lane >> 2, l4 = lane & 3;
+    float bpart[2] = {0.f, 0.f};
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      KDA_PT(9);
+      {
+        const int nt = g;
+        const int c = ch0 + 8 * nt + 2 * l4;
+        float px[4], po[4], pk[4];  // element (i8 + 8 hh, c + u) at index 2 hh + u
+        {
+          const uint32_t tb = tmem + ((uint32_t)(32 * Bk) << 16) + (uint32_t)(ch0 + 8 * nt);
+          tmem_ld_frag3(tb, tb + 128u, tb + 256u, px, po, pk);
+        }
+        const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
+        const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
+        const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
+        float cq[2] = {0.f, 0.f};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * Bk + i8 + 8 * hh;
+          const float br = beta[r];
+          const float2 vq = make_float2(po[2 * hh], po[2 * hh + 1]);
+          const float2 vb = make_float2(-px[2 * hh], -px[2 * hh + 1]);
+          const float2 vk = make_float2(pk[2 * hh], pk[2 * hh + 1]);
+          const uint32_t to = sw_off(r, c, kC);
+          uint32_t *krh_p = reinterpret_cast<uint32_t *>(sm + C_KR + to), *krl_p = reinterpret_cast<uint32_t *>(sm + C_KR + LO128 + to);
+          uint32_t *qrh_p = reinterpret_cast<uint32_t *>(sm + C_QR + to), *qrl_p = reinterpret_cast<uint32_t *>(sm + C_QR + LO128 + to);
+          const float2 krh = unpack_bf16(*krh_p), krl = unpack_bf16(*krl_p);
+          const float2 qrh = unpack_bf16(*qrh_p), qrl = unpack_bf16(*qrl_p);
+          const float2 kch = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + to));
+          const float2 kcl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + LO128 + to));
+          const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
+          float dq2[2], dk2[2], qv[2], pv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float Kr = u ? krh.y + krl.y : krh.x + krl.x;  // k e1
+            const float Qr = u ? qrh.y + qrl.y : qrh.x + qrl.x;  // q~ e1
+            const float Kc = u ? kch.y + kcl.y : kch.x + kcl.x;  // k e2
+            const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = u ? vk.y : vk.x;
+            const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
+            const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
+            const float e1 = exp2f(gg_ - gref), e2 = exp2f(gref - gg_);
+            const float gam = e1 * eref, kh = e2 * lam;
+            const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
+            const float xyI = xyi[nt][2 * hh + u];
+            dq2[u] = dQg * gam + e1 * yR;
+            dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * xyI;
+            // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
+            const bool in = r < len;
+            qv[u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
+            pv[u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * xyI - dKh * Kc * lam) : 0.f;
+            bpart[hh] += dBk * Kr * eref + Kr * xR;
+            cq[u] += dKh * Kc * lam;
+          }
+          // dG of (r, c) and (r, c + 1) into the Kr (Q part) and Qr (P part) pair slots just read
+          *krh_p = __float_as_uint(qv[0]);
+          *krl_p = __float_as_uint(qv[1]);
+          *qrh_p = __float_as_uint(pv[0]);
+          *qrl_p = __float_as_uint(pv[1]);
+          if (r < len) {
+            const size_t tok = (size_t)(t0 + r);
+            if (args.partial) {
+              float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
+              *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
+              *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
+            } else {
+              __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
+              __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
+              *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
+              *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {  // column sums of dKhat k khat over the warp's 16 rows
+          float cs = cq[u];
+          cs += __shfl_xor_sync(0xffffffffu, cs, 4);
+          cs += __shfl_xor_sync(0xffffffffu, cs, 8);
+          cs += __shfl_xor_sync(0xffffffffu, cs, 16);
+          if (i8 == 0) totC[Bk * kD + c + u] = cs;
+        }
+      }
+      KDA_PT(10);
+    }
+    __syncthreads();  // every thread has parked its dG and its Khat column terms
+    KDA_PT(11);
+    if (more) {  // the Kc tile, G and beta are dead: the next slot's group P2, G and beta
+      if (tid == 0) {
+        fence_async_smem();
+        issue_p2(sbase, W, maps, nxt, bar_p2);
+      }
+      issue_gate_beta(sbase, P, beta, nxt);
+    }
+    {  // dg = reverse cumsum of dG: thread = one column, one 16-row segment (4 segments)
+      const int c = tid & (kD - 1), seg = tid >> 7, mid = len >> 1;
+      // element (r, c) of the parked dG: even c in the hi slot of its pair, odd c in the lo slot
+      const uint32_t po = (c & 1) ? LO128 : 0u;
+      float q16[16], p16[16], tq = 0.f, tp = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t to = sw_off(16 * seg + k, c & ~1, kC) + po;
+        q16[k] = *reinterpret_cast<const float *>(sm + C_KR + to);
+        p16[k] = *reinterpret_cast<const float *>(sm + C_QR + to);
+        tq += q16[k];
+        tp += p16[k];
+      }
+      totQ[seg * kD + c] = tq;
+      totP[seg * kD + c] = tp;
+      __syncthreads();
+      float aq = 0.f, aps = 0.f, app = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) {
+        const float a = totQ[s2 * kD + c], b = totP[s2 * kD + c];
+        if (s2 > seg) { aq += a; aps += b; }
+        if (s2 < seg) app += b;
+      }
+      const float ks = totC[c] + totC[kD + c] + totC[2 * kD + c] + totC[3 * kD + c];
+      // dg_t = sum_{s>=t} dG_s: the Q part and the carried-state decay term
+      // from the chunk end; the zero-sum P part from whichever end is nearer
+      // (sum_{s>=t} P_s = -sum_{s<t} P_s, the Khat column sum counted at the
+      // last row), halving the cancelling terms it sums.
+      const float carried = kLn2 * vec[V_GAML * kD + c] * dglv[c];
+      float pre[16];
+      pre[0] = app;
+#pragma unroll
+      for (int k = 1; k < 16; ++k) pre[k] = pre[k - 1] + p16[k - 1];
+      float qs = aq, ps = aps + kLn2 * ks;
+#pragma unroll
+      for (int k = 15; k >= 0; --k) {
+        const int r = 16 * seg + k;
+        qs += q16[k];
+        ps += p16[k];
+        if (r < len) args.dg[((size_t)(t0 + r) * HV + j) * kD + c] = qs + carried + (r >= mid ? ps : -pre[k]);
+      }
+    }
+    KDA_PT(12);
+    KDA_PT(6);
+    // dbeta partials: reduce over the 4 lanes sharing a row, then per column half
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float v = bpart[hh];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (l4 == 0) rb[(warp >> 2) * kC + 16 * Bk + i8 + 8 * hh] = v;
+    }
+    const bool all_ok = __syncthreads_and(ok) != 0;  // the dg scan is done: Kr, Qr and dL are dead
+    KDA_PT(7);
+    if (more && all_ok && tid == 0) {
+      fence_async_smem();
+      issue_s(sbase, W, maps, nxt, bar_s);
+    }
+    if (tid < kC && tid < len)
+      args.dbeta[(size_t)(t0 + tid) * HV + j] = red[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
+    KDA_PT(8);
+    if (!all_ok) {  // a wait gave up (error flag set): let the copies already issued land, then stop
+      if (more) {
+        if (tid == 0) {
+          bar_wait(bar_p1, par ^ 1u, args.err);
+          bar_wait(bar_p2, par ^ 1u, args.err);
+        }
+        cp_wait_all();
+      }
+      break;
+    }
+    cur = nxt;
+    have = more;
+    s_idx += gridDim.x;
+  }  // slot loop
   fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -689,8 +783,11 @@ cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *
               partial ? (void *)W.dkp : dk, dg, dbeta, partial, err};
   TmaMaps maps;
   if ((e = make_tma_maps(P, P.v, dO, &maps)) != cudaSuccess) return e;
-  KDA_LAUNCH("kda_bwd_intra_tc", s,
-             kda_bwd_intra_tc_kernel<<<dim3(P.NC, P.HV), kCT, C_SMEM, s>>>(P, W, a, maps));
+  int nsm = 0;
+  if ((e = sm_count(&nsm)) != cudaSuccess) return e;
+  const int64_t slots = (int64_t)P.NC * P.HV;
+  const unsigned grid = (unsigned)(slots < nsm ? slots : nsm);  // one CTA per SM, persistent over the slots
+  KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
   return cudaGetLastError();
 }
 
