@@ -206,6 +206,8 @@ kda_status chunk_fwd(const kda_inputs *in, void *o, float *hT, void *ctx, size_t
   kda_status st = validate(in, P);
   if (st != KDA_OK) return st;
   if (P.Ttot > 0 && o == nullptr) return fail(KDA_ERR_INVALID_ARG, "o is NULL");
+  if (use_tc(P) && ((uintptr_t)o & 15) != 0)
+    return fail(KDA_ERR_INVALID_ARG, "o must be 16-byte aligned (bf16, K = V = 128 path)");
   const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
   with_ctx = need_ctx > 0;
   if ((st = check_ws(need_ctx, ctx, ctx_bytes, "forward context")) != KDA_OK) return st;
@@ -242,8 +244,11 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
   if (P.Ttot > 0 && (dO == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
                      dg == nullptr || dbeta == nullptr))
     return fail(KDA_ERR_INVALID_ARG, "dO, dq, dk, dv, dg and dbeta are required");
-  if (use_tc(P) && ((uintptr_t)dO & 15) != 0)
-    return fail(KDA_ERR_INVALID_ARG, "dO must be 16-byte aligned (bf16, K = V = 128 path)");
+  if (use_tc(P)) {  // the tensor-core kernels load dO by TMA and store the gradients in 4-16 byte vectors
+    const char *bad = ((uintptr_t)dO & 15) ? "dO" : ((uintptr_t)dq & 15) ? "dq" : ((uintptr_t)dk & 15) ? "dk"
+                      : ((uintptr_t)dv & 15) ? "dv" : (!P.scalar_gate && ((uintptr_t)dg & 15)) ? "dg" : nullptr;
+    if (bad != nullptr) return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned (bf16, K = V = 128 path)", bad);
+  }
   const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
   with_ctx = need_ctx > 0;
   if ((st = check_ws(need_ctx, ctx, ctx_bytes, "forward context")) != KDA_OK) return st;

@@ -78,8 +78,9 @@ constexpr uint32_t TMEM_COLS = 512;   // [0,128) dX h^T, [128,256) dO h^T, [256,
 // final dg column scan.  dG itself is parked in the Kr / Qr tiles: once a thread
 // has read its Kr, Qr (hi and lo) at (r, c..c+1), the 8 bytes of each pair slot
 // hold dG's Q and P parts of (r, c) and (r, c+1).
-constexpr uint32_t C_TOT = C_DAB;     // totals of Q, P [4 segments][128]; Khat column term [4 blocks][128]
-static_assert(C_TOT + 3 * 4 * 128 * 4 <= C_G, "assembly scratch overflows the chain tiles");
+constexpr uint32_t C_TOT = C_DAB;     // totals of Q, P [8 segments][128]; Khat column term [4 blocks][128]
+// (it ends inside the dL tiles: the next slot's dh' arrives in the dAqk^T tile during the assembly)
+static_assert(C_TOT + (8 + 8 + 4) * 128 * 4 <= C_DQK, "assembly scratch overflows the dL tiles");
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct IntraArgs {
@@ -589,7 +590,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     // Kc = k e2 hold.  dg = reverse cumsum of dG over the chunk runs once, after
     // the last pass, as column scans over 16-row segments with segment totals
     // exchanged in shared memory.
-    float *totQ = (float *)(sm + C_TOT), *totP = totQ + 4 * kD, *totC = totP + 4 * kD;
+    float *totQ = (float *)(sm + C_TOT), *totP = totQ + 8 * kD, *totC = totP + 8 * kD;
     const float *dglv = red + 64;
     const int i8 = lane >> 2, l4 = lane & 3;
     float bpart[2] = {0.f, 0.f};
@@ -684,46 +685,61 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       }
       issue_gate_beta(sbase, P, beta, nxt);
     }
-    {  // dg = reverse cumsum of dG: thread = one column, one 16-row segment (4 segments)
-      const int c = tid & (kD - 1), seg = tid >> 7, mid = len >> 1;
-      // element (r, c) of the parked dG: even c in the hi slot of its pair, odd c in the lo slot
-      const uint32_t po = (c & 1) ? LO128 : 0u;
-      float q16[16], p16[16], tq = 0.f, tp = 0.f;
+    {  // dg = reverse cumsum of dG: thread = one column pair, one 8-row segment (8 segments)
+      const int c = 2 * (tid & 63), seg = tid >> 6, mid = len >> 1;
+      // dG of (r, c) and (r, c + 1): Q parts in the Kr hi / lo slots of the pair, P parts in the
+      // Qr hi / lo slots (a warp reads one 128-byte row of each: conflict-free)
+      float2 q8[8], p8[8];
+      float2 tq = make_float2(0.f, 0.f), tp = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t to = sw_off(16 * seg + k, c & ~1, kC) + po;
-        q16[k] = *reinterpret_cast<const float *>(sm + C_KR + to);
-        p16[k] = *reinterpret_cast<const float *>(sm + C_QR + to);
-        tq += q16[k];
-        tp += p16[k];
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t to = sw_off(8 * seg + k, c, kC);
+        q8[k] = make_float2(*reinterpret_cast<const float *>(sm + C_KR + to),
+                            *reinterpret_cast<const float *>(sm + C_KR + LO128 + to));
+        p8[k] = make_float2(*reinterpret_cast<const float *>(sm + C_QR + to),
+                            *reinterpret_cast<const float *>(sm + C_QR + LO128 + to));
+        tq.x += q8[k].x; tq.y += q8[k].y;
+        tp.x += p8[k].x; tp.y += p8[k].y;
       }
-      totQ[seg * kD + c] = tq;
-      totP[seg * kD + c] = tp;
+      *reinterpret_cast<float2 *>(totQ + seg * kD + c) = tq;
+      *reinterpret_cast<float2 *>(totP + seg * kD + c) = tp;
       __syncthreads();
-      float aq = 0.f, aps = 0.f, app = 0.f;
+      float2 aq = make_float2(0.f, 0.f), aps = aq, app = aq;
 #pragma unroll
-      for (int s2 = 0; s2 < 4; ++s2) {
-        const float a = totQ[s2 * kD + c], b = totP[s2 * kD + c];
-        if (s2 > seg) { aq += a; aps += b; }
-        if (s2 < seg) app += b;
+      for (int s2 = 0; s2 < 8; ++s2) {
+        const float2 a = *reinterpret_cast<const float2 *>(totQ + s2 * kD + c);
+        const float2 b = *reinterpret_cast<const float2 *>(totP + s2 * kD + c);
+        if (s2 > seg) { aq.x += a.x; aq.y += a.y; aps.x += b.x; aps.y += b.y; }
+        if (s2 < seg) { app.x += b.x; app.y += b.y; }
       }
-      const float ks = totC[c] + totC[kD + c] + totC[2 * kD + c] + totC[3 * kD + c];
+      float2 ks = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float2 t = *reinterpret_cast<const float2 *>(totC + b * kD + c);
+        ks.x += t.x; ks.y += t.y;
+      }
       // dg_t = sum_{s>=t} dG_s: the Q part and the carried-state decay term
       // from the chunk end; the zero-sum P part from whichever end is nearer
       // (sum_{s>=t} P_s = -sum_{s<t} P_s, the Khat column sum counted at the
       // last row), halving the cancelling terms it sums.
-      const float carried = kLn2 * vec[V_GAML * kD + c] * dglv[c];
-      float pre[16];
+      const float2 gam = *reinterpret_cast<const float2 *>(vec + V_GAML * kD + c);
+      const float2 dgl = *reinterpret_cast<const float2 *>(dglv + c);
+      const float2 carried = make_float2(kLn2 * gam.x * dgl.x, kLn2 * gam.y * dgl.y);
+      float2 pre[8];
       pre[0] = app;
 #pragma unroll
-      for (int k = 1; k < 16; ++k) pre[k] = pre[k - 1] + p16[k - 1];
-      float qs = aq, ps = aps + kLn2 * ks;
+      for (int k = 1; k < 8; ++k) pre[k] = make_float2(pre[k - 1].x + p8[k - 1].x, pre[k - 1].y + p8[k - 1].y);
+      float2 qs = aq, ps = make_float2(aps.x + kLn2 * ks.x, aps.y + kLn2 * ks.y);
 #pragma unroll
-      for (int k = 15; k >= 0; --k) {
-        const int r = 16 * seg + k;
-        qs += q16[k];
-        ps += p16[k];
-        if (r < len) args.dg[((size_t)(t0 + r) * HV + j) * kD + c] = qs + carried + (r >= mid ? ps : -pre[k]);
+      for (int k = 7; k >= 0; --k) {
+        const int r = 8 * seg + k;
+        qs.x += q8[k].x; qs.y += q8[k].y;
+        ps.x += p8[k].x; ps.y += p8[k].y;
+        if (r < len) {
+          const bool hi = r >= mid;
+          *reinterpret_cast<float2 *>(args.dg + ((size_t)(t0 + r) * HV + j) * kD + c) =
+              make_float2(qs.x + carried.x + (hi ? ps.x : -pre[k].x), qs.y + carried.y + (hi ? ps.y : -pre[k].y));
+        }
       }
     }
     KDA_PT(12);

@@ -36,8 +36,8 @@
  *   h0,hT,dhT,dh0  [N][HV][K][V]     fp32
  * The bf16 K = V = 128 problems run the tensor-core kernels when q, k, v and g
  * are 16-byte aligned (they arrive by TMA); otherwise the general kernels run,
- * with the same results.  On the tensor-core path dO must be 16-byte aligned
- * too (KDA_ERR_INVALID_ARG otherwise).
+ * with the same results.  On the tensor-core path o, dO, dq, dk, dv and (per-
+ * channel gate) dg must be 16-byte aligned too (KDA_ERR_INVALID_ARG otherwise).
  * Value head j reads query/key head j / (HV/H) (contiguous groups).
  * dq and dk are summed over the HV/H value heads that share a q/k head.
  *

@@ -179,3 +179,30 @@ def test_forward_context_checks(lib):
     g = _inputs(K=64, V=64)
     st = lib.kda_chunk_fwd_ctx(ctypes.byref(g), o, None, None, 0, None, 0, None)
     assert st == _lib.KDA_ERR_WORKSPACE and b"workspace is NULL" in lib.kda_last_error()
+
+
+@pytest.mark.parametrize("bad", ["o", "dq", "dk", "dv", "dg"])
+def test_misaligned_outputs_on_the_tensor_core_path_are_rejected(lib, bad):
+    """The tensor-core kernels store o and the gradients in 4- to 16-byte vectors: a
+    caller pointer off a 16-byte boundary is rejected before any launch."""
+    s = _inputs(K=128, V=128)
+    ptr = {n: 0x200000 + 0x1000 * i for i, n in enumerate(("o", "dO", "dq", "dk", "dv", "dg", "db"))}
+    ptr[bad] += 4
+    ws = ctypes.c_void_p(0x10000)
+    if bad == "o":
+        st = lib.kda_chunk_fwd(ctypes.byref(s), ctypes.c_void_p(ptr["o"]), None, ws, 1 << 30, None)
+    else:
+        p = [ctypes.c_void_p(ptr[n]) for n in ("dO", "dq", "dk", "dv", "dg", "db")]
+        st = lib.kda_chunk_bwd(ctypes.byref(s), p[0], None, *p[1:], None, ws, 1 << 30, None)
+    assert st == _lib.KDA_ERR_INVALID_ARG, lib.kda_last_error()
+    assert bad.encode() + b" must be 16-byte aligned" in lib.kda_last_error()
+
+
+def test_scalar_gate_dg_needs_no_vector_alignment(lib):
+    """With a scalar gate the caller's dg [B, T, HV] is written one float at a time: a
+    4-byte aligned dg passes the host checks (here up to the workspace check)."""
+    s = _inputs(K=128, V=128, flags=_lib.KDA_SCALAR_GATE)
+    p = [ctypes.c_void_p(0x200000 + 0x1000 * i) for i in range(6)]
+    p[4] = ctypes.c_void_p(0x204004)
+    st = lib.kda_chunk_bwd(ctypes.byref(s), p[0], None, *p[1:], None, None, 0, None)
+    assert st == _lib.KDA_ERR_WORKSPACE, lib.kda_last_error()
