@@ -272,10 +272,12 @@ class Runner:
 def cp_step_fn(runner, R):
     """One fwd+bwd step of the context-parallel layer: every sequence split into
     R equal segments, each processed as its rank would (local pass, transition,
-    relay scan, final pass; the mirror image backward), the ranks one after the
-    other on this GPU."""
+    relay scan, final pass keeping its forward context; the mirror image
+    backward: the start-state gradient by the reverse scan alone, relay scan,
+    full backward, both reading that context), the ranks one after the other on
+    this GPU."""
     from gated_delta_rule_42_gb300 import cp
-    from gated_delta_rule_42_gb300.ops import chunk_kda_bwd, chunk_kda_fwd
+    from gated_delta_rule_42_gb300.ops import chunk_kda_bwd_ctx, chunk_kda_bwd_state, chunk_kda_fwd, chunk_kda_fwd_ctx
     d = runner.d
     T = d.q.shape[1]
     bounds = [T * r // R for r in range(R + 1)]
@@ -290,16 +292,17 @@ def cp_step_fn(runner, R):
         hs = [d.h0 if d.h0 is not None else torch.zeros_like(cs[0])]
         for r in range(1, R):
             hs.append(cp.compose(Ms[r - 1], hs[-1], cs[r - 1]))
-        for r, (q, k, v, g, beta, _) in enumerate(segs):
-            chunk_kda_fwd(q, k, v, g, beta, hs[r], None, r == R - 1)
-        ds = [chunk_kda_bwd(q, k, v, g, beta, hs[r], None, do, None)[5]
+        ctxs = [chunk_kda_fwd_ctx(q, k, v, g, beta, hs[r], None, r == R - 1)[2]
+                for r, (q, k, v, g, beta, _) in enumerate(segs)]
+        ds = [chunk_kda_bwd_state(q, k, v, g, beta, hs[r], None, do, None, ctxs[r])
               for r, (q, k, v, g, beta, do) in enumerate(segs)]
         ends = [None] * R
         ends[R - 1] = d.dhT
         for r in range(R - 1, 0, -1):
             ends[r - 1] = cp.compose(Ms[r], ends[r] if ends[r] is not None else torch.zeros_like(ds[r]), ds[r], True)
         for r, (q, k, v, g, beta, do) in enumerate(segs):
-            chunk_kda_bwd(q, k, v, g, beta, hs[r], None, do, ends[r], need_dh0=(r == 0 and d.h0 is not None))
+            chunk_kda_bwd_ctx(q, k, v, g, beta, hs[r], None, ctxs[r], do, ends[r],
+                              need_dh0=(r == 0 and d.h0 is not None))
 
     return step
 

@@ -24,12 +24,12 @@ be checked with CPU ranks.
 from __future__ import annotations
 
 import ctypes
-from typing import Callable, List, Optional
+from typing import Callable, List, NamedTuple, Optional, Union
 
 import torch
 
 from . import _lib
-from .ops import chunk_kda_bwd, chunk_kda_fwd
+from .ops import chunk_kda_bwd, chunk_kda_bwd_ctx, chunk_kda_bwd_state, chunk_kda_fwd, chunk_kda_fwd_ctx
 
 
 def compose(M: torch.Tensor, h: torch.Tensor, c: Optional[torch.Tensor], transpose: bool = False) -> torch.Tensor:
@@ -95,24 +95,47 @@ def segment_transition(q, k, g, beta, **kw) -> torch.Tensor:
     return M
 
 
-def cp_forward(q, k, v, g, beta, h0, rank: int, gather, compose_fn: Callable = compose, **kw):
+class SegmentContext(NamedTuple):
+    """What a rank's forward keeps for its backward: the segment's true start
+    state, its transition M, and the forward context of the final pass (the
+    per-chunk records and chunk-start states; None when not kept)."""
+    h_start: torch.Tensor
+    M: torch.Tensor
+    kctx: Optional[torch.Tensor]
+
+
+def cp_forward(q, k, v, g, beta, h0, rank: int, gather, compose_fn: Callable = compose,
+               keep_context: bool = True, **kw):
     """Forward of this rank's segment.  h0: the sequences' initial state (read
-    from rank 0; may be None).  Returns (o, hT, start state): hT of the last rank
-    is the sequences' final state."""
+    from rank 0; may be None).  Returns (o, hT, SegmentContext): hT of the last
+    rank is the sequences' final state.  keep_context: the final pass keeps its
+    forward context, so the two backward passes do not recompute it."""
     _, c = chunk_kda_fwd(q, k, v, g, beta, None, None, True, **kw)
     M = segment_transition(q, k, g, beta, **kw)
     hs = relay_start_state(c, M, h0, rank, gather, compose_fn)
-    o, hT = chunk_kda_fwd(q, k, v, g, beta, hs, None, True, **kw)
-    return o, hT, hs
+    if keep_context:
+        o, hT, kctx = chunk_kda_fwd_ctx(q, k, v, g, beta, hs, None, True, **kw)
+    else:
+        (o, hT), kctx = chunk_kda_fwd(q, k, v, g, beta, hs, None, True, **kw), None
+    return o, hT, SegmentContext(hs, M, kctx)
 
 
-def cp_backward(q, k, v, g, beta, h_start, do, dhT, rank: int, world: int, gather,
-                compose_fn: Callable = compose, **kw):
-    """Backward of this rank's segment given its start state (from
-    :func:`cp_forward`) and dhT (the final-state gradient, read from the last
-    rank; may be None).  Returns dq, dk, dv, dg, dbeta and the start-state gradient (rank 0:
+def cp_backward(q, k, v, g, beta, seg: Union[SegmentContext, torch.Tensor], do, dhT, rank: int, world: int,
+                gather, compose_fn: Callable = compose, **kw):
+    """Backward of this rank's segment given what :func:`cp_forward` kept (or
+    just the start state, in which case M and the forward context are
+    recomputed) and dhT (the final-state gradient, read from the last rank; may
+    be None).  Returns dq, dk, dv, dg, dbeta and the start-state gradient (rank 0:
     the gradient of the sequences' initial state)."""
-    d = chunk_kda_bwd(q, k, v, g, beta, h_start, None, do, None, **kw)[5]
-    M = segment_transition(q, k, g, beta, **kw)
-    dh_end = relay_end_grad(d, M, dhT, rank, world, gather, compose_fn)
-    return chunk_kda_bwd(q, k, v, g, beta, h_start, None, do, dh_end, **kw)
+    if not isinstance(seg, SegmentContext):
+        seg = SegmentContext(seg, segment_transition(q, k, g, beta, **kw), None)
+
+    def bwd(dh_end):
+        if seg.kctx is not None:
+            return chunk_kda_bwd_ctx(q, k, v, g, beta, seg.h_start, None, seg.kctx, do, dh_end, **kw)
+        return chunk_kda_bwd(q, k, v, g, beta, seg.h_start, None, do, dh_end, **kw)
+
+    # d: the start-state gradient from a zero end gradient (the reverse scan alone)
+    d = chunk_kda_bwd_state(q, k, v, g, beta, seg.h_start, None, do, None, seg.kctx, **kw)
+    dh_end = relay_end_grad(d, seg.M, dhT, rank, world, gather, compose_fn)
+    return bwd(dh_end)

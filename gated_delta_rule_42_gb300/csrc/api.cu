@@ -241,9 +241,13 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
   Problem P{};
   kda_status st = validate(in, P);
   if (st != KDA_OK) return st;
-  if (P.Ttot > 0 && (dO == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
-                     dg == nullptr || dbeta == nullptr))
-    return fail(KDA_ERR_INVALID_ARG, "dO, dq, dk, dv, dg and dbeta are required");
+  // dq .. dbeta all NULL with a dh0: the start-state gradient alone (the reverse scan)
+  const bool state_only =
+      dq == nullptr && dk == nullptr && dv == nullptr && dg == nullptr && dbeta == nullptr && dh0 != nullptr;
+  if (P.Ttot > 0 && (dO == nullptr || (!state_only && (dq == nullptr || dk == nullptr || dv == nullptr ||
+                                                       dg == nullptr || dbeta == nullptr))))
+    return fail(KDA_ERR_INVALID_ARG,
+                "dO, dq, dk, dv, dg and dbeta are required (or dq .. dbeta all NULL with dh0: dh0 alone)");
   if (use_tc(P)) {  // the tensor-core kernels load dO by TMA and store the gradients in 4-16 byte vectors
     const char *bad = ((uintptr_t)dO & 15) ? "dO" : ((uintptr_t)dq & 15) ? "dq" : ((uintptr_t)dk & 15) ? "dk"
                       : ((uintptr_t)dv & 15) ? "dv" : (!P.scalar_gate && ((uintptr_t)dg & 15)) ? "dg" : nullptr;
@@ -265,17 +269,22 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
   if (e == cudaSuccess) {
     if (use_tc(P)) {
       int *err = W.flags + 2;
-      e = with_ctx ? launch_chunk_map(Pg, W, s) : tc_forward(Pg, W, nullptr, nullptr, kFwdSave, err, s);
+      // the saved tiles come from the context, or from the states pass (the scan alone needs only the records)
+      e = with_ctx     ? launch_chunk_map(Pg, W, s)
+          : state_only ? tc_records(Pg, W, err, s)
+                       : tc_forward(Pg, W, nullptr, nullptr, kFwdSave, err, s);
       if (e == cudaSuccess) e = tc_backward_scan(Pg, W, dO, dhT, dh0, err, s);
-      if (e == cudaSuccess) e = tc_backward_intra(Pg, W, dO, dv, dq, dk, dgk, dbeta, err, s);
-      if (e == cudaSuccess && (P.HV != P.H || P.l2norm)) e = launch_group_reduce(Pg, W.dqp, W.dkp, dq, dk, s);
+      if (!state_only) {
+        if (e == cudaSuccess) e = tc_backward_intra(Pg, W, dO, dv, dq, dk, dgk, dbeta, err, s);
+        if (e == cudaSuccess && (P.HV != P.H || P.l2norm)) e = launch_group_reduce(Pg, W.dqp, W.dkp, dq, dk, s);
+      }
     } else {
       Problem Pn = Pg;
       e = normalised_copies(Pg, W, &Pn, s);
-      if (e == cudaSuccess) e = simple_backward(Pn, W, dO, dhT, dq, dk, dv, dgk, dbeta, dh0, s);
+      if (e == cudaSuccess) e = simple_backward(Pn, W, dO, dhT, dq, dk, dv, dgk, dbeta, dh0, state_only, s);
     }
   }
-  if (e == cudaSuccess && P.scalar_gate) e = launch_gate_grad_reduce(P, W.dgx, dg, s);
+  if (e == cudaSuccess && P.scalar_gate && !state_only) e = launch_gate_grad_reduce(P, W.dgx, dg, s);
   if (e != cudaSuccess) return cuda_fail(e, with_ctx ? "kda_chunk_bwd_ctx" : "kda_chunk_bwd");
   return KDA_OK;
 }

@@ -121,9 +121,10 @@ cudaError_t launch_chunk_map(const Problem &P, const Workspace &W, cudaStream_t 
 cudaError_t simple_prepare(const Problem &P, const Workspace &W, float *hT, cudaStream_t s);
 cudaError_t simple_forward(const Problem &P, const Workspace &W, void *o, float *hT,
                            cudaStream_t s);
+// state_only: stop after the dh scan (dh0 alone; dq .. dbeta untouched)
 cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO,
                             const float *dhT, void *dq, void *dk, void *dv, float *dg,
-                            float *dbeta, float *dh0, cudaStream_t s);
+                            float *dbeta, float *dh0, bool state_only, cudaStream_t s);
 cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t s);
 // Per-chunk records (tc_prep.cu): one CTA per (chunk, value head) slot.
 cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps, int *err, cudaStream_t s);
@@ -132,6 +133,8 @@ cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps
 // value head) slot the chunk-start state and the X^T, D^T tiles go to
 // W.tc_hs / tc_xt / tc_dt for the backward) or both bits.
 constexpr int kFwdOutput = 1, kFwdSave = 2;
+// The chunk map and the records alone (what the reverse scan needs).
+cudaError_t tc_records(const Problem &P, const Workspace &W, int *err, cudaStream_t s);
 cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, int *err,
                        cudaStream_t s);
 cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,

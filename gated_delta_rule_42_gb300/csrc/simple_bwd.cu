@@ -361,7 +361,7 @@ __global__ void group_reduce_kernel(Problem P, const float *__restrict__ dqp,
 template <typename Tin>
 cudaError_t run_backward(const Problem &P, const Workspace &W, const void *dO, const float *dhT,
                          void *dq, void *dk, void *dv, float *dg, float *dbeta, float *dh0,
-                         cudaStream_t s) {
+                         bool state_only, cudaStream_t s) {
   cudaError_t e = simple_prepare(P, W, nullptr, s);
   if (e != cudaSuccess) return e;
   const size_t sd = dh_smem(P.K), sb = bwd_intra_smem(P.K);
@@ -374,6 +374,7 @@ cudaError_t run_backward(const Problem &P, const Workspace &W, const void *dO, c
         P, W, (const Tin *)dO, dhT, dh0));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (state_only) return cudaSuccess;
   if (P.NC > 0) {
     KDA_LAUNCH("simple_bwd_intra_kernel", s, simple_bwd_intra_kernel<Tin><<<dim3(P.NC, P.HV), kThreads, sb, s>>>(P, W, (const Tin *)dO,
                                                                        (Tin *)dv, dg, dbeta));
@@ -402,9 +403,9 @@ cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float 
 
 cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO,
                             const float *dhT, void *dq, void *dk, void *dv, float *dg,
-                            float *dbeta, float *dh0, cudaStream_t s) {
-  return P.bf16 ? run_backward<__nv_bfloat16>(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, s)
-                : run_backward<float>(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, s);
+                            float *dbeta, float *dh0, bool state_only, cudaStream_t s) {
+  return P.bf16 ? run_backward<__nv_bfloat16>(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, state_only, s)
+                : run_backward<float>(P, W, dO, dhT, dq, dk, dv, dg, dbeta, dh0, state_only, s);
 }
 
 }  // namespace kda

@@ -320,14 +320,21 @@ cudaError_t launch_fwd(const char *name, const Problem &P, const Workspace &W, c
   return cudaGetLastError();
 }
 
+cudaError_t tc_records(const Problem &P, const Workspace &W, int *err, cudaStream_t s) {
+  cudaError_t e = launch_chunk_map(P, W, s);
+  if (e != cudaSuccess || P.N == 0) return e;
+  TmaMaps maps;
+  if ((e = make_tma_maps(P, P.v, nullptr, &maps)) != cudaSuccess) return e;
+  return tc_prepare(P, W, maps, err, s);
+}
+
 cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, int *err,
                        cudaStream_t s) {
-  cudaError_t e = launch_chunk_map(P, W, s);
+  cudaError_t e = tc_records(P, W, err, s);
   if (e != cudaSuccess || P.N == 0) return e;
   FwdArgs a{(__nv_bfloat16 *)o, hT, err};
   TmaMaps maps;
   if ((e = make_tma_maps(P, P.v, nullptr, &maps)) != cudaSuccess) return e;
-  if ((e = tc_prepare(P, W, maps, err, s)) != cudaSuccess) return e;
   switch (mode) {
     case kFwdOutput: return launch_fwd<kFwdOutput>("kda_fwd_tc", P, W, a, maps, s);
     case kFwdSave: return launch_fwd<kFwdSave>("kda_fwd_tc_states", P, W, a, maps, s);

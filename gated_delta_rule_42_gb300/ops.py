@@ -21,7 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["chunk_kda", "recurrent_kda", "chunk_kda_fwd", "chunk_kda_bwd", "chunk_kda_fwd_ctx",
-           "chunk_kda_bwd_ctx", "make_inputs_struct"]
+           "chunk_kda_bwd_ctx", "chunk_kda_bwd_state", "make_inputs_struct"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -178,6 +178,34 @@ def chunk_kda_bwd_ctx(q, k, v, g, beta, initial_state, cu_seqlens, kctx, do, dht
                                           _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), wp, wb,
                                           _stream(q.device)))
     return dq, dk, dv, dg, db, dh0
+
+
+def chunk_kda_bwd_state(q, k, v, g, beta, initial_state, cu_seqlens, do, dht, kctx=None,
+                        use_qk_l2norm: bool = False) -> torch.Tensor:
+    """Gradient of the initial state alone, dh0 [N, HV, K, V] fp32: the reverse
+    state scan without the per-token gradient work (the C ABI's backward with
+    dq .. dbeta NULL).  kctx: a forward context of the same inputs
+    (:func:`chunk_kda_fwd_ctx`), or None to recompute from the inputs."""
+    lib = _lib.load()
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    _check_tensor("do", do, q.dtype, q.device, tuple(v.shape))
+    if dht is not None:
+        _check_tensor("dht", dht, torch.float32, q.device, (s.N, s.HV, s.K, s.V))
+    dh0 = torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
+    sp = _stream(q.device)
+    if kctx is not None:
+        _check_tensor("context", kctx, torch.uint8, q.device)
+        cp, cb = _aligned(kctx) if kctx.numel() else (None, 0)
+        workspace = _workspace(lib.kda_chunk_bwd_ctx_workspace_size(ctypes.byref(s)), q.device)
+        wp, wb = _aligned(workspace)
+        _lib.check(lib, lib.kda_chunk_bwd_ctx(ctypes.byref(s), cp, cb, _ptr(do), _ptr(dht), None, None, None, None,
+                                              None, _ptr(dh0), wp, wb, sp))
+    else:
+        workspace = _workspace(lib.kda_chunk_bwd_workspace_size(ctypes.byref(s)), q.device)
+        wp, wb = _aligned(workspace)
+        _lib.check(lib, lib.kda_chunk_bwd(ctypes.byref(s), _ptr(do), _ptr(dht), None, None, None, None, None,
+                                          _ptr(dh0), wp, wb, sp))
+    return dh0
 
 
 class ChunkKDAFunction(torch.autograd.Function):

@@ -131,7 +131,10 @@ size_t kda_chunk_bwd_workspace_size(const kda_inputs *in);
  * final-state gradient dhT [N][HV][K][V] (fp32, NULL = zero), writes
  * dq, dk [B][T][H][K] (dtype), dv [B][T][HV][V] (dtype), dg [B][T][HV][K] (fp32,
  * gradient w.r.t. the log2 gate), dbeta [B][T][HV] (fp32) for every valid token
- * and, if dh0 is not NULL, dh0 [N][HV][K][V] (fp32). */
+ * and, if dh0 is not NULL, dh0 [N][HV][K][V] (fp32).  With dq, dk, dv, dg and
+ * dbeta all NULL and dh0 not NULL, only dh0 is computed (the initial-state
+ * gradient alone: the reverse state scan, none of the per-token gradient
+ * work) -- what a context-parallel rank needs before its relay. */
 kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT, void *dq,
                          void *dk, void *dv, float *dg, float *dbeta, float *dh0,
                          void *workspace, size_t workspace_bytes, void *stream);

@@ -206,3 +206,19 @@ def test_scalar_gate_dg_needs_no_vector_alignment(lib):
     p[4] = ctypes.c_void_p(0x204004)
     st = lib.kda_chunk_bwd(ctypes.byref(s), p[0], None, *p[1:], None, None, 0, None)
     assert st == _lib.KDA_ERR_WORKSPACE, lib.kda_last_error()
+
+
+def test_start_state_gradient_only_mode_validation(lib):
+    """dq .. dbeta all NULL with a dh0 asks for dh0 alone; a partial set of NULL
+    gradients, or no dh0 either, is an invalid argument."""
+    s = _inputs(K=128, V=128)
+    p = [ctypes.c_void_p(0x200000 + 0x1000 * i) for i in range(7)]
+    dO, dh0 = p[0], p[6]
+    st = lib.kda_chunk_bwd(ctypes.byref(s), dO, None, None, None, None, None, None, dh0, None, 0, None)
+    assert st == _lib.KDA_ERR_WORKSPACE, lib.kda_last_error()  # valid request: stops at the workspace check
+    st = lib.kda_chunk_bwd(ctypes.byref(s), dO, None, None, None, None, None, None, None, None, 0, None)
+    assert st == _lib.KDA_ERR_INVALID_ARG  # nothing to compute
+    st = lib.kda_chunk_bwd(ctypes.byref(s), dO, None, p[1], None, None, None, None, dh0, None, 0, None)
+    assert st == _lib.KDA_ERR_INVALID_ARG  # dq given, the rest NULL
+    st = lib.kda_chunk_bwd_ctx(ctypes.byref(s), None, 0, dO, None, None, None, None, None, None, dh0, None, 0, None)
+    assert st == _lib.KDA_ERR_WORKSPACE and b"forward context" in lib.kda_last_error()

@@ -38,7 +38,8 @@ class ThreadGather:
     ("bf16_tc", dict(B=2, T=300, H=2, HV=4, K=128, V=128), torch.bfloat16, 130),
     ("fp32_small", dict(B=1, T=150, H=1, HV=2, K=64, V=48), torch.float32, 64),
 ], ids=["bf16_tc", "fp32_small"])
-def test_state_relay_two_emulated_ranks(name, kw, dtype, split):
+@pytest.mark.parametrize("keep", [True, False], ids=["kept_context", "recompute"])
+def test_state_relay_two_emulated_ranks(name, kw, dtype, split, keep):
     inp = inputs.make_inputs(dtype=dtype, seed=77, name=name, **kw)
     d = inp.to("cuda")
     world = 2
@@ -52,9 +53,11 @@ def test_state_relay_two_emulated_ranks(name, kw, dtype, split):
             s = segs[rank]
             q, k, v, g, beta, do = (x[:, s].contiguous() for x in (d.q, d.k, d.v, d.g, d.beta, d.do))
             gather = tg.for_rank(rank)
-            o, hT, hs = cp.cp_forward(q, k, v, g, beta, d.h0 if rank == 0 else None, rank, gather)
-            grads = cp.cp_backward(q, k, v, g, beta, hs, do, d.dhT if rank == world - 1 else None, rank, world,
-                                   gather)
+            o, hT, seg = cp.cp_forward(q, k, v, g, beta, d.h0 if rank == 0 else None, rank, gather,
+                                       keep_context=keep)
+            # kept: the backward reuses M and the forward context; else it gets the start state alone
+            grads = cp.cp_backward(q, k, v, g, beta, seg if keep else seg.h_start, do,
+                                   d.dhT if rank == world - 1 else None, rank, world, gather)
             torch.cuda.synchronize()
             res[rank] = (o.cpu(), hT.cpu(), [t.cpu() for t in grads])
         except Exception as e:  # surfaced after the join

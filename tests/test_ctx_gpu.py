@@ -118,3 +118,28 @@ def test_autograd_tensor_core_path_matches_c_abi(keep_context):
     gr = H.gpu_bwd(inp)
     for t, key in zip(leaves, GRADS):
         assert torch.equal(t.grad.cpu(), gr[key]), key
+
+
+STATE_CASES = [
+    ("tc_varlen_empty", dict(B=1, T=300, H=2, HV=4, K=128, V=128, cu_seqlens=[0, 0, 100, 100, 300])),
+    ("tc_scalar_gate", dict(B=2, T=130, H=1, HV=2, K=128, V=128, scalar_gate=True)),
+    ("general_fp32", dict(B=1, T=150, H=1, HV=2, K=64, V=48, dtype=torch.float32)),
+]
+
+
+@pytest.mark.parametrize("name,kw", STATE_CASES, ids=[c[0] for c in STATE_CASES])
+def test_start_state_gradient_alone_matches_the_full_backward(name, kw):
+    """The backward with dq .. dbeta NULL (the reverse scan alone) returns the
+    full backward's dh0, bit for bit, with and without a forward context."""
+    from gated_delta_rule_42_gb300.ops import chunk_kda_bwd_state, chunk_kda_fwd_ctx
+    kw = dict(kw)
+    dtype = kw.pop("dtype", torch.bfloat16)
+    inp = inputs.make_inputs(dtype=dtype, seed=zlib.crc32(name.encode()) % 1000, name=name, **kw)
+    d = inp.to("cuda")
+    full = H.gpu_bwd(inp)["dh0"]
+    alone = chunk_kda_bwd_state(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, d.do, d.dhT)
+    _, _, kctx = chunk_kda_fwd_ctx(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, True)
+    alone_ctx = chunk_kda_bwd_state(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, d.do, d.dhT, kctx)
+    torch.cuda.synchronize()
+    assert torch.equal(alone.cpu(), full)
+    assert torch.equal(alone_ctx.cpu(), full)
