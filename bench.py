@@ -271,13 +271,15 @@ class Runner:
 
 def cp_step_fn(runner, R):
     """One fwd+bwd step of the context-parallel layer: every sequence split into
-    R equal segments, each processed as its rank would (local pass, transition,
-    relay scan, final pass keeping its forward context; the mirror image
+    R equal segments, each processed as its rank would (local pass keeping a
+    forward context, transition and final pass reusing its records, relay scan;
+    the mirror image
     backward: the start-state gradient by the reverse scan alone, relay scan,
     full backward, both reading that context), the ranks one after the other on
     this GPU."""
     from gated_delta_rule_42_gb300 import cp
-    from gated_delta_rule_42_gb300.ops import chunk_kda_bwd_ctx, chunk_kda_bwd_state, chunk_kda_fwd, chunk_kda_fwd_ctx
+    from gated_delta_rule_42_gb300.ops import (chunk_kda_bwd_ctx, chunk_kda_bwd_state, chunk_kda_fwd_ctx,
+                                               chunk_kda_fwd_reuse)
     d = runner.d
     T = d.q.shape[1]
     bounds = [T * r // R for r in range(R + 1)]
@@ -285,15 +287,17 @@ def cp_step_fn(runner, R):
             for r in range(R)]
 
     def step():
-        cs, Ms = [], []
-        for q, k, v, g, beta, _ in segs:
-            cs.append(chunk_kda_fwd(q, k, v, g, beta, None, None, True)[1])
-            Ms.append(cp.segment_transition(q, k, g, beta))
+        cs, Ms, ctxs = [], [], []
+        for q, k, v, g, beta, _ in segs:  # local pass (final state only), the context's one record pass
+            _, c, kctx = chunk_kda_fwd_ctx(q, k, v, g, beta, None, None, True, need_output=False)
+            cs.append(c)
+            ctxs.append(kctx)
+            Ms.append(cp.segment_transition(q, k, g, beta, kctx))
         hs = [d.h0 if d.h0 is not None else torch.zeros_like(cs[0])]
         for r in range(1, R):
             hs.append(cp.compose(Ms[r - 1], hs[-1], cs[r - 1]))
-        ctxs = [chunk_kda_fwd_ctx(q, k, v, g, beta, hs[r], None, r == R - 1)[2]
-                for r, (q, k, v, g, beta, _) in enumerate(segs)]
+        for r, (q, k, v, g, beta, _) in enumerate(segs):
+            chunk_kda_fwd_reuse(q, k, v, g, beta, hs[r], None, ctxs[r], r == R - 1)
         ds = [chunk_kda_bwd_state(q, k, v, g, beta, hs[r], None, do, None, ctxs[r])
               for r, (q, k, v, g, beta, do) in enumerate(segs)]
         ends = [None] * R

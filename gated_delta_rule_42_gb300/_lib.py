@@ -22,7 +22,7 @@ EXPORTS = (
     "kda_chunk_bwd", "kda_recurrent_fwd", "kda_status_string", "kda_last_error", "kda_version",
     "kda_launch_count", "kda_timing_enable", "kda_timing_collect", "kda_chunk_fwd_noalloc",
     "kda_state_compose", "kda_chunk_ctx_size", "kda_chunk_fwd_ctx_workspace_size",
-    "kda_chunk_bwd_ctx_workspace_size", "kda_chunk_fwd_ctx", "kda_chunk_bwd_ctx",
+    "kda_chunk_bwd_ctx_workspace_size", "kda_chunk_fwd_ctx", "kda_chunk_bwd_ctx", "kda_chunk_fwd_reuse",
 )
 
 
@@ -69,8 +69,9 @@ def load(path: str = LIB_PATH):
         for nm in ("kda_chunk_ctx_size", "kda_chunk_fwd_ctx_workspace_size", "kda_chunk_bwd_ctx_workspace_size"):
             getattr(lib, nm).argtypes = [P]
             getattr(lib, nm).restype = sz
-        lib.kda_chunk_fwd_ctx.argtypes = [P, vp, vp, vp, sz, vp, sz, vp]
-        lib.kda_chunk_fwd_ctx.restype = i
+        for nm in ("kda_chunk_fwd_ctx", "kda_chunk_fwd_reuse"):
+            getattr(lib, nm).argtypes = [P, vp, vp, vp, sz, vp, sz, vp]
+            getattr(lib, nm).restype = i
         lib.kda_chunk_bwd_ctx.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_chunk_bwd_ctx.restype = i
         lib.kda_recurrent_fwd.argtypes = [P, vp, vp, vp]

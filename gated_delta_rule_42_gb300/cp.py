@@ -29,7 +29,8 @@ from typing import Callable, List, NamedTuple, Optional, Union
 import torch
 
 from . import _lib
-from .ops import chunk_kda_bwd, chunk_kda_bwd_ctx, chunk_kda_bwd_state, chunk_kda_fwd, chunk_kda_fwd_ctx
+from .ops import (chunk_kda_bwd, chunk_kda_bwd_ctx, chunk_kda_bwd_state, chunk_kda_fwd, chunk_kda_fwd_ctx,
+                  chunk_kda_fwd_reuse)
 
 
 def compose(M: torch.Tensor, h: torch.Tensor, c: Optional[torch.Tensor], transpose: bool = False) -> torch.Tensor:
@@ -84,15 +85,19 @@ def all_gather_fn(group=None) -> Callable[[torch.Tensor], List[torch.Tensor]]:
     return gather
 
 
-def segment_transition(q, k, g, beta, **kw) -> torch.Tensor:
+def segment_transition(q, k, g, beta, kctx=None, **kw) -> torch.Tensor:
     """M [B, HV, K, K] of this segment: the forward with v = 0, V = K and
-    h0 = the identity, whose final state is M (the state evolves linearly)."""
+    h0 = the identity, whose final state is M (the state evolves linearly);
+    the final state alone, no output.  kctx: a forward context of this segment
+    (same q, k, g, beta) whose records it reuses (the context then holds this
+    pass's chunk-start states)."""
     B, T, H, K = q.shape
     HV = beta.shape[2]
     v0 = torch.zeros((B, T, HV, K), dtype=q.dtype, device=q.device)
     eye = torch.eye(K, dtype=torch.float32, device=q.device).expand(B, HV, K, K).contiguous()
-    _, M = chunk_kda_fwd(q, k, v0, g, beta, eye, None, True, **kw)
-    return M
+    if kctx is not None:
+        return chunk_kda_fwd_reuse(q, k, v0, g, beta, eye, None, kctx, True, need_output=False, **kw)[1]
+    return chunk_kda_fwd(q, k, v0, g, beta, eye, None, True, need_output=False, **kw)[1]
 
 
 class SegmentContext(NamedTuple):
@@ -110,12 +115,15 @@ def cp_forward(q, k, v, g, beta, h0, rank: int, gather, compose_fn: Callable = c
     from rank 0; may be None).  Returns (o, hT, SegmentContext): hT of the last
     rank is the sequences' final state.  keep_context: the final pass keeps its
     forward context, so the two backward passes do not recompute it."""
-    _, c = chunk_kda_fwd(q, k, v, g, beta, None, None, True, **kw)
-    M = segment_transition(q, k, g, beta, **kw)
-    hs = relay_start_state(c, M, h0, rank, gather, compose_fn)
-    if keep_context:
-        o, hT, kctx = chunk_kda_fwd_ctx(q, k, v, g, beta, hs, None, True, **kw)
+    if keep_context:  # one record pass: the transition and the final pass reuse the context's records
+        _, c, kctx = chunk_kda_fwd_ctx(q, k, v, g, beta, None, None, True, need_output=False, **kw)
+        M = segment_transition(q, k, g, beta, kctx, **kw)
+        hs = relay_start_state(c, M, h0, rank, gather, compose_fn)
+        o, hT = chunk_kda_fwd_reuse(q, k, v, g, beta, hs, None, kctx, True, **kw)
     else:
+        _, c = chunk_kda_fwd(q, k, v, g, beta, None, None, True, need_output=False, **kw)
+        M = segment_transition(q, k, g, beta, **kw)
+        hs = relay_start_state(c, M, h0, rank, gather, compose_fn)
         (o, hT), kctx = chunk_kda_fwd(q, k, v, g, beta, hs, None, True, **kw), None
     return o, hT, SegmentContext(hs, M, kctx)
 

@@ -198,14 +198,16 @@ kda_status check_ws(size_t need, const void *ws, size_t bytes, const char *what 
   return KDA_OK;
 }
 
-// kda_chunk_fwd, and with with_ctx kda_chunk_fwd_ctx.
+// kda_chunk_fwd, with with_ctx kda_chunk_fwd_ctx, and with reuse as well
+// kda_chunk_fwd_reuse (the records are already in the context).
 kda_status chunk_fwd(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes, bool with_ctx,
-                     void *workspace, size_t workspace_bytes, void *stream) {
+                     bool reuse, void *workspace, size_t workspace_bytes, void *stream) {
   g_err[0] = 0;
   Problem P{};
   kda_status st = validate(in, P);
   if (st != KDA_OK) return st;
-  if (P.Ttot > 0 && o == nullptr) return fail(KDA_ERR_INVALID_ARG, "o is NULL");
+  if (P.Ttot > 0 && o == nullptr && hT == nullptr)
+    return fail(KDA_ERR_INVALID_ARG, "o and hT are NULL (o NULL: the final state alone, which needs hT)");
   if (use_tc(P) && ((uintptr_t)o & 15) != 0)
     return fail(KDA_ERR_INVALID_ARG, "o must be 16-byte aligned (bf16, K = V = 128 path)");
   const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
@@ -221,15 +223,15 @@ kda_status chunk_fwd(const kda_inputs *in, void *o, float *hT, void *ctx, size_t
   cudaError_t e = gate_per_channel(P, W, &Pg, (cudaStream_t)stream);
   if (e == cudaSuccess) {
     if (use_tc(P)) {
-      e = tc_forward(Pg, W, o, hT, with_ctx ? kFwdOutput | kFwdSave : kFwdOutput, W.flags + 2,
-                     (cudaStream_t)stream);
+      const int mode = (o != nullptr ? kFwdOutput : 0) | (with_ctx ? kFwdSave : 0);
+      e = tc_forward(Pg, W, o, hT, mode, with_ctx && reuse, W.flags + 2, (cudaStream_t)stream);
     } else {
       Problem Pn = Pg;
       e = normalised_copies(Pg, W, &Pn, (cudaStream_t)stream);
       if (e == cudaSuccess) e = simple_forward(Pn, W, o, hT, (cudaStream_t)stream);
     }
   }
-  if (e != cudaSuccess) return cuda_fail(e, with_ctx ? "kda_chunk_fwd_ctx" : "kda_chunk_fwd");
+  if (e != cudaSuccess) return cuda_fail(e, reuse ? "kda_chunk_fwd_reuse" : with_ctx ? "kda_chunk_fwd_ctx" : "kda_chunk_fwd");
   return KDA_OK;
 }
 
@@ -272,7 +274,7 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
       // the saved tiles come from the context, or from the states pass (the scan alone needs only the records)
       e = with_ctx     ? launch_chunk_map(Pg, W, s)
           : state_only ? tc_records(Pg, W, err, s)
-                       : tc_forward(Pg, W, nullptr, nullptr, kFwdSave, err, s);
+                       : tc_forward(Pg, W, nullptr, nullptr, kFwdSave, false, err, s);
       if (e == cudaSuccess) e = tc_backward_scan(Pg, W, dO, dhT, dh0, err, s);
       if (!state_only) {
         if (e == cudaSuccess) e = tc_backward_intra(Pg, W, dO, dv, dq, dk, dgk, dbeta, err, s);
@@ -331,7 +333,7 @@ size_t kda_chunk_bwd_workspace_size(const kda_inputs *in) {
 
 kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspace,
                          size_t workspace_bytes, void *stream) {
-  return chunk_fwd(in, o, hT, nullptr, 0, false, workspace, workspace_bytes, stream);
+  return chunk_fwd(in, o, hT, nullptr, 0, false, false, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT, void *dq,
@@ -361,7 +363,12 @@ size_t kda_chunk_bwd_ctx_workspace_size(const kda_inputs *in) {
 
 kda_status kda_chunk_fwd_ctx(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes,
                              void *workspace, size_t workspace_bytes, void *stream) {
-  return chunk_fwd(in, o, hT, ctx, ctx_bytes, true, workspace, workspace_bytes, stream);
+  return chunk_fwd(in, o, hT, ctx, ctx_bytes, true, false, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_chunk_fwd_reuse(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+  return chunk_fwd(in, o, hT, ctx, ctx_bytes, true, true, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_chunk_bwd_ctx(const kda_inputs *in, const void *ctx, size_t ctx_bytes, const void *dO,
@@ -416,6 +423,6 @@ const char *kda_status_string(kda_status s) {
 
 const char *kda_last_error(void) { return g_err; }
 
-int kda_version(void) { return 102; }
+int kda_version(void) { return 103; }
 
 }  // extern "C"

@@ -128,15 +128,16 @@ cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO
 cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t s);
 // Per-chunk records (tc_prep.cu): one CTA per (chunk, value head) slot.
 cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps, int *err, cudaStream_t s);
-// bf16, K = V = 128 tensor-core forward: the records into W.tc_tiles, then the
-// state chain.  mode is kFwdOutput (o, hT), kFwdSave (no output: per (chunk,
-// value head) slot the chunk-start state and the X^T, D^T tiles go to
-// W.tc_hs / tc_xt / tc_dt for the backward) or both bits.
+// bf16, K = V = 128 tensor-core forward: the records into W.tc_tiles (unless
+// records_ready: W.tc_tiles already holds them for these q, k, g, beta), then
+// the state chain.  mode is kFwdOutput (o, hT), kFwdSave (no output: per
+// (chunk, value head) slot the chunk-start state and the X^T, D^T tiles go to
+// W.tc_hs / tc_xt / tc_dt for the backward), both bits, or 0 (hT alone).
 constexpr int kFwdOutput = 1, kFwdSave = 2;
 // The chunk map and the records alone (what the reverse scan needs).
 cudaError_t tc_records(const Problem &P, const Workspace &W, int *err, cudaStream_t s);
-cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, int *err,
-                       cudaStream_t s);
+cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, bool records_ready,
+                       int *err, cudaStream_t s);
 cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,
                              float *dh0, int *err, cudaStream_t s);
 // Per-chunk gradients: tcgen05 products and the gradient chain in one kernel.

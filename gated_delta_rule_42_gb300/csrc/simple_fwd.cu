@@ -291,7 +291,7 @@ cudaError_t simple_prepare(const Problem &P, const Workspace &W, float *hT, cuda
 cudaError_t simple_forward(const Problem &P, const Workspace &W, void *o, float *hT,
                            cudaStream_t s) {
   cudaError_t e = simple_prepare(P, W, hT, s);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || o == nullptr) return e;  // o NULL: the final state alone
   return P.bf16 ? run_output<__nv_bfloat16>(P, W, o, s) : run_output<float>(P, W, o, s);
 }
 

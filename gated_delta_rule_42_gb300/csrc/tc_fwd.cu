@@ -24,11 +24,11 @@
 // h tile becomes the output staging, and the next chunk's loads are issued as
 // soon as the last products of this chunk complete.
 //
-// Three modes.  Output: o (and hT).  States (no output): the kernel saves, per
+// Four modes.  Output: o (and hT).  States (no output): the kernel saves, per
 // chunk, what the backward needs beside the record -- the chunk-start state
 // h_c (bf16 [K][V]) and X^T, D^T, as bulk copies of the swizzled tiles -- when
 // the backward recomputes the forward.  Output + save: both at once, for a
-// forward whose context the backward keeps.
+// forward whose context the backward keeps.  Neither: the final state alone.
 #include "tc_common.cuh"
 
 namespace kda {
@@ -328,14 +328,15 @@ cudaError_t tc_records(const Problem &P, const Workspace &W, int *err, cudaStrea
   return tc_prepare(P, W, maps, err, s);
 }
 
-cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, int *err,
-                       cudaStream_t s) {
-  cudaError_t e = tc_records(P, W, err, s);
+cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, bool records_ready,
+                       int *err, cudaStream_t s) {
+  cudaError_t e = records_ready ? launch_chunk_map(P, W, s) : tc_records(P, W, err, s);
   if (e != cudaSuccess || P.N == 0) return e;
   FwdArgs a{(__nv_bfloat16 *)o, hT, err};
   TmaMaps maps;
   if ((e = make_tma_maps(P, P.v, nullptr, &maps)) != cudaSuccess) return e;
   switch (mode) {
+    case 0: return launch_fwd<0>("kda_fwd_tc_final_state", P, W, a, maps, s);
     case kFwdOutput: return launch_fwd<kFwdOutput>("kda_fwd_tc", P, W, a, maps, s);
     case kFwdSave: return launch_fwd<kFwdSave>("kda_fwd_tc_states", P, W, a, maps, s);
     case kFwdOutput | kFwdSave: return launch_fwd<kFwdOutput | kFwdSave>("kda_fwd_tc_save", P, W, a, maps, s);

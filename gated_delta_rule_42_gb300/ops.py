@@ -21,7 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["chunk_kda", "recurrent_kda", "chunk_kda_fwd", "chunk_kda_bwd", "chunk_kda_fwd_ctx",
-           "chunk_kda_bwd_ctx", "chunk_kda_bwd_state", "make_inputs_struct"]
+           "chunk_kda_bwd_ctx", "chunk_kda_bwd_state", "chunk_kda_fwd_reuse", "make_inputs_struct"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -92,12 +92,20 @@ def _aligned(ws: torch.Tensor):
     return ctypes.c_void_p((p + 255) & ~255), ws.numel() - (((p + 255) & ~255) - p)
 
 
+def _output(v, need_output, output_final_state):
+    if not need_output and not output_final_state:
+        raise ValueError("need_output=False computes the final state alone: it needs output_final_state=True")
+    return torch.empty_like(v) if need_output else None
+
+
 def chunk_kda_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_final_state=False,
-                  workspace: Optional[torch.Tensor] = None,
-                  use_qk_l2norm: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                  workspace: Optional[torch.Tensor] = None, use_qk_l2norm: bool = False,
+                  need_output: bool = True) -> Tuple[Optional[torch.Tensor], Optional[torch.Tensor]]:
+    """Chunked forward (no autograd).  need_output=False: the final state alone
+    (o is None), without the output work."""
     lib = _lib.load()
     s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
-    o = torch.empty_like(v)
+    o = _output(v, need_output, output_final_state)
     hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
           if output_final_state else None)
     need = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s))
@@ -134,14 +142,14 @@ def chunk_kda_bwd(q, k, v, g, beta, initial_state, cu_seqlens, do, dht,
 
 
 def chunk_kda_fwd_ctx(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_final_state=False,
-                      use_qk_l2norm: bool = False):
+                      use_qk_l2norm: bool = False, need_output: bool = True):
     """Forward that also returns the forward context (a uint8 device tensor,
     empty on the general path) for :func:`chunk_kda_bwd_ctx`: the per-chunk
     records, chunk-start states and X^T, D^T tiles the backward would otherwise
-    recompute.  Returns (o, final_state or None, context)."""
+    recompute.  Returns (o or None, final_state or None, context)."""
     lib = _lib.load()
     s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
-    o = torch.empty_like(v)
+    o = _output(v, need_output, output_final_state)
     hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
           if output_final_state else None)
     nctx = lib.kda_chunk_ctx_size(ctypes.byref(s))
@@ -152,6 +160,26 @@ def chunk_kda_fwd_ctx(q, k, v, g, beta, initial_state=None, cu_seqlens=None, out
     _lib.check(lib, lib.kda_chunk_fwd_ctx(ctypes.byref(s), _ptr(o), _ptr(hT), cp, cb, wp, wb,
                                           _stream(q.device)))
     return o, hT, kctx
+
+
+def chunk_kda_fwd_reuse(q, k, v, g, beta, initial_state, cu_seqlens, kctx, output_final_state=False,
+                        use_qk_l2norm: bool = False, need_output: bool = True):
+    """:func:`chunk_kda_fwd_ctx` for inputs that share q, k, g, beta and
+    cu_seqlens with the ones ``kctx`` was last filled from (v and the initial
+    state may differ): the per-chunk records are read from the context, not
+    recomputed, and the context is rewritten to serve these inputs' backward.
+    Returns (o or None, final_state or None)."""
+    lib = _lib.load()
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    o = _output(v, need_output, output_final_state)
+    hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
+          if output_final_state else None)
+    _check_tensor("context", kctx, torch.uint8, q.device)
+    cp, cb = _aligned(kctx) if kctx.numel() else (None, 0)
+    workspace = _workspace(lib.kda_chunk_fwd_ctx_workspace_size(ctypes.byref(s)), q.device)
+    wp, wb = _aligned(workspace)
+    _lib.check(lib, lib.kda_chunk_fwd_reuse(ctypes.byref(s), _ptr(o), _ptr(hT), cp, cb, wp, wb, _stream(q.device)))
+    return o, hT
 
 
 def chunk_kda_bwd_ctx(q, k, v, g, beta, initial_state, cu_seqlens, kctx, do, dht, need_dh0: bool = True,

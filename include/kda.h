@@ -118,7 +118,8 @@ typedef struct kda_inputs {
 size_t kda_chunk_fwd_workspace_size(const kda_inputs *in);
 
 /* Chunked forward.  Writes o [B][T][HV][V] (dtype) for every valid token and,
- * if hT is not NULL, the final states hT [N][HV][K][V] (fp32).
+ * if hT is not NULL, the final states hT [N][HV][K][V] (fp32).  o may be NULL
+ * when hT is not: then only the final states are computed (no output work).
  * workspace: device scratch of at least kda_chunk_fwd_workspace_size() bytes;
  * its contents on entry do not matter and are clobbered. */
 kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspace,
@@ -170,6 +171,15 @@ size_t kda_chunk_bwd_ctx_workspace_size(const kda_inputs *in);
 kda_status kda_chunk_fwd_ctx(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes,
                              void *workspace, size_t workspace_bytes, void *stream);
 
+/* kda_chunk_fwd_ctx for inputs that share q, k, g, beta, cu_seqlens, flags and
+ * sizes with the ones ctx was last filled from (v and h0 may differ): the
+ * per-chunk records, which depend on those alone, are read from ctx instead of
+ * recomputed -- the several passes of a context-parallel rank over one segment.
+ * The chunk-start states and tiles in ctx are rewritten for these inputs, so
+ * the context then serves their backward.  On the general path: kda_chunk_fwd. */
+kda_status kda_chunk_fwd_reuse(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
 /* kda_chunk_bwd on the context kda_chunk_fwd_ctx filled (read only). */
 kda_status kda_chunk_bwd_ctx(const kda_inputs *in, const void *ctx, size_t ctx_bytes, const void *dO,
                              const float *dhT, void *dq, void *dk, void *dv, float *dg, float *dbeta,
@@ -204,8 +214,9 @@ const char *kda_status_string(kda_status s);
 /* Message describing the last failure on the calling thread ("" if none). */
 const char *kda_last_error(void);
 
-/* Library ABI version (major * 100 + minor): 102 (101: kda_inputs gained
- * `flags`; 102: the forward-context entry points). */
+/* Library ABI version (major * 100 + minor): 103 (101: kda_inputs gained
+ * `flags`; 102: the forward-context entry points; 103: the final-state-only
+ * forward, the start-state-gradient-only backward, kda_chunk_fwd_reuse). */
 int kda_version(void);
 
 /* Chunked forward without a caller workspace (no counterpart on the pages).

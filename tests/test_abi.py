@@ -222,3 +222,17 @@ def test_start_state_gradient_only_mode_validation(lib):
     assert st == _lib.KDA_ERR_INVALID_ARG  # dq given, the rest NULL
     st = lib.kda_chunk_bwd_ctx(ctypes.byref(s), None, 0, dO, None, None, None, None, None, None, dh0, None, 0, None)
     assert st == _lib.KDA_ERR_WORKSPACE and b"forward context" in lib.kda_last_error()
+
+
+def test_final_state_only_forward_validation(lib):
+    """o may be NULL when hT is not (the final state alone); both NULL is an
+    invalid argument.  kda_chunk_fwd_reuse checks its context like the _ctx pair."""
+    s = _inputs(K=128, V=128)
+    hT = ctypes.c_void_p(0x300000)
+    st = lib.kda_chunk_fwd(ctypes.byref(s), None, hT, None, 0, None)
+    assert st == _lib.KDA_ERR_WORKSPACE, lib.kda_last_error()  # valid request: stops at the workspace check
+    st = lib.kda_chunk_fwd(ctypes.byref(s), None, None, None, 0, None)
+    assert st == _lib.KDA_ERR_INVALID_ARG
+    st = lib.kda_chunk_fwd_reuse(ctypes.byref(s), ctypes.c_void_p(0x3000), None, None, 0, ctypes.c_void_p(0x10000),
+                                 1 << 30, None)
+    assert st == _lib.KDA_ERR_WORKSPACE and b"forward context" in lib.kda_last_error()

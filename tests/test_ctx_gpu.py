@@ -143,3 +143,38 @@ def test_start_state_gradient_alone_matches_the_full_backward(name, kw):
     torch.cuda.synchronize()
     assert torch.equal(alone.cpu(), full)
     assert torch.equal(alone_ctx.cpu(), full)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tc_varlen_gva", dict(B=1, T=300, H=2, HV=4, K=128, V=128, cu_seqlens=[0, 0, 100, 100, 300])),
+    ("general_fp32", dict(B=1, T=150, H=1, HV=2, K=64, V=48, dtype=torch.float32)),
+], ids=["tc_varlen_gva", "general_fp32"])
+def test_final_state_only_and_record_reuse(name, kw):
+    """(1) The forward without o returns the full forward's final state, bit for
+    bit.  (2) A context filled on one (v, h0), then reused for another (v', h0')
+    with the same q, k, g, beta, gives what the plain pair gives on (v', h0'):
+    o, hT and every gradient, bit for bit."""
+    from gated_delta_rule_42_gb300.ops import (chunk_kda_bwd, chunk_kda_bwd_ctx, chunk_kda_fwd, chunk_kda_fwd_ctx,
+                                               chunk_kda_fwd_reuse)
+    kw = dict(kw)
+    dtype = kw.pop("dtype", torch.bfloat16)
+    inp = inputs.make_inputs(dtype=dtype, seed=zlib.crc32(name.encode()) % 1000, name=name, **kw)
+    d = inp.to("cuda")
+    args = (d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+    o_full, hT_full = chunk_kda_fwd(*args, True)
+    none, hT_only = chunk_kda_fwd(*args, True, need_output=False)
+    assert none is None and torch.equal(hT_only, hT_full)
+    # another v and h0 on the same q, k, g, beta
+    v2 = torch.flip(d.v, dims=[1]).contiguous()
+    h2 = (0.5 * d.h0).contiguous()
+    _, _, kctx = chunk_kda_fwd_ctx(*args, True, need_output=False)
+    o_r, hT_r = chunk_kda_fwd_reuse(d.q, d.k, v2, d.g, d.beta, h2, d.cu_seqlens, kctx, True)
+    o_p, hT_p = chunk_kda_fwd(d.q, d.k, v2, d.g, d.beta, h2, d.cu_seqlens, True)
+    torch.cuda.synchronize()
+    _same("o", o_r, o_p)
+    _same("hT", hT_r, hT_p)
+    g_r = chunk_kda_bwd_ctx(d.q, d.k, v2, d.g, d.beta, h2, d.cu_seqlens, kctx, d.do, d.dhT)
+    g_p = chunk_kda_bwd(d.q, d.k, v2, d.g, d.beta, h2, d.cu_seqlens, d.do, d.dhT)
+    torch.cuda.synchronize()
+    for key, a, b in zip(GRADS, g_r, g_p):
+        _same(key, a, b)
