@@ -213,7 +213,7 @@ def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.
         output_final_state=final_state, seed=seed)
 
 
-def _cfg4_offsets(rng: np.random.Generator) -> np.ndarray:
+def _packed_varlen_offsets(rng: np.random.Generator) -> np.ndarray:
     lens = list(packed_lengths(rng, 64, 131072, 1, 8192))
     for pos in (0, 21, 42, 67):  # empty slots: leading, interior, trailing
         lens.insert(pos, 0)
@@ -235,7 +235,7 @@ CONFIGS = [
           final_state=True, g_mean=-3.0)),
     ("packed_varlen_bf16_T131072_H16_HV32_K128",
      dict(B=1, T=131072, H=16, HV=32, K=128, V=128, dtype=torch.bfloat16,
-          lengths_fn=_cfg4_offsets, h0=True, final_state=True)),
+          lengths_fn=_packed_varlen_offsets, h0=True, final_state=True)),
 ]
 
 

@@ -27,7 +27,7 @@ def test_varlen_gva_config_offsets():
 
 def test_packed_lengths_recipe():
     rng = np.random.Generator(np.random.PCG64(1004))
-    cu = inputs._cfg4_offsets(rng)
+    cu = inputs._packed_varlen_offsets(rng)
     lens = np.diff(cu)
     assert len(cu) == 69 and cu[0] == 0 and cu[-1] == 131072
     assert [i for i, l in enumerate(lens) if l == 0] == [0, 21, 42, 67]
