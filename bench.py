@@ -606,6 +606,7 @@ def main():
                    "l2": f"inputs {ab['fwd'] / 1e9:.2f} GB read per step > L2 (no flush)",
                    "qk_l2norm": bool(args.qk_l2norm), "scalar_gate": bool(args.scalar_gate),
                    "backward": "recompute" if args.recompute else "forward context kept",
+                   "forward_context_bytes": int(runner.ctx_bytes),
                    **({"cp_ranks": args.cp_ranks, "cp": "sequences split into cp_ranks segments, state relay, "
                        "ranks serialized on one GPU"} if args.cp_ranks > 1 else {})},
         "roofline": roof,
