@@ -343,6 +343,15 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
                    stream);
 }
 
+size_t kda_status_offset(const kda_inputs *in) {
+  Problem P{};
+  if (validate(in, P) != KDA_OK) return ~(size_t)0;
+  char *const base = reinterpret_cast<char *>((uintptr_t)1 << 20);  // any aligned address: only offsets are taken
+  Workspace W;
+  layout(P, false, false, base, &W);
+  return (size_t)(reinterpret_cast<char *>(W.flags) - base);  // the same in every workspace layout (it comes first)
+}
+
 size_t kda_chunk_ctx_size(const kda_inputs *in) {
   Problem P{};
   if (validate(in, P) != KDA_OK) return 0;
@@ -423,6 +432,6 @@ const char *kda_status_string(kda_status s) {
 
 const char *kda_last_error(void) { return g_err; }
 
-int kda_version(void) { return 103; }
+int kda_version(void) { return 104; }
 
 }  // extern "C"

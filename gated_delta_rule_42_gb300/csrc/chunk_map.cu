@@ -25,6 +25,7 @@ chunk_map_kernel(const int32_t *__restrict__ cu, int B, int T, int N, int64_t Tt
   if (tid == 0) {
     s_carry = 0;
     s_bad = 0;
+    flags[2] = 0;  // the call's bounded-wait error word: every call starts clean
   }
   __syncthreads();
   for (int base = 0; base < N; base += kMapThreads) {

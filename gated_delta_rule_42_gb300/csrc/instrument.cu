@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "kda_internal.cuh"
+#include "umma.cuh"
 
 namespace kda {
 namespace {
@@ -58,7 +59,37 @@ void inst_end(cudaStream_t s) {
 
 }  // namespace kda
 
+namespace kda {
+namespace {
+
+// One thread waits, with a bounded wait, on an mbarrier that nothing arrives
+// on: the wait gives up after `polls` polls and raises *err.
+__global__ void bounded_wait_probe_kernel(int *err, long polls) {
+  __shared__ uint64_t bar;
+  umma::bar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  umma::bar_wait(&bar, 0, err, polls);
+}
+
+}  // namespace
+}  // namespace kda
+
 extern "C" {
+
+kda_status kda_debug_bounded_wait(int *err, long long polls, void *stream) {
+  if (err == nullptr || polls < 1 || polls > (1LL << 24)) {
+    kda::set_last_error("kda_debug_bounded_wait: err must be a device int and 1 <= polls <= 2^24");
+    return KDA_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  KDA_LAUNCH("bounded_wait_probe_kernel", s, kda::bounded_wait_probe_kernel<<<1, 1, 0, s>>>(err, (long)polls));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    kda::set_last_error(cudaGetErrorString(e));
+    return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
 
 unsigned long long kda_launch_count(void) {
   std::lock_guard<std::mutex> lk(kda::g_mu);

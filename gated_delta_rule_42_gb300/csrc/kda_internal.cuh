@@ -48,7 +48,7 @@ constexpr float kL2NormEps = 1e-6f;  // epsilon of the q/k L2-norm prologue
 struct Workspace {
   int4 *seq;     // [N]
   int4 *chunk;   // [NC]
-  int *flags;    // [0] = number of chunks, [1] = malformed-offsets flag
+  int *flags;    // [0] = number of chunks, [1] = malformed-offsets flag, [2] = a bounded wait gave up
   float *G;      // [slot][64][K]   chunk-local inclusive gate cumsum
   float *Aqk;    // [slot][64][64]  lower (incl. diagonal) decayed q~ k^T
   float *A;      // [slot][64][64]  (I + L)^-1

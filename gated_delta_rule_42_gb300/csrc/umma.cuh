@@ -80,9 +80,9 @@ __device__ __forceinline__ void bar_init(uint64_t *bar, uint32_t count) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and sets *err) when the limit is hit.
-__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, int *err) {
-  for (long it = 0; it < kSpinLimit; ++it) {
+// false (and sets *err) after `limit` unsuccessful polls.
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, int *err, long limit = kSpinLimit) {
+  for (long it = 0; it < limit; ++it) {
     uint32_t ok;
     asm volatile(
         "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"

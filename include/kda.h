@@ -208,15 +208,29 @@ kda_status kda_recurrent_fwd(const kda_inputs *in, void *o, float *hT, void *str
 kda_status kda_state_compose(const float *M, const float *h, const float *c, float *out, int count, int K,
                              int V, int transpose, void *stream);
 
+/* Device status words of a call.  Every chunked call (forward, backward, any
+ * variant) writes three int32 words into its workspace, at byte offset
+ * kda_status_offset() (the same for every workspace of the problem):
+ *   [0] the number of 64-token chunks mapped;
+ *   [1] nonzero if cu_seqlens was malformed (decreasing, negative or past the
+ *       token axis): those sequences were treated as empty;
+ *   [2] nonzero if a bounded device wait gave up (a copy or product never
+ *       completed): the call's results are invalid.  Word 2 is cleared at the
+ *       start of every call.
+ * The library never reads them on the host: copy them out after the call (in
+ * stream order) to check.  Returns SIZE_MAX for an invalid problem. */
+size_t kda_status_offset(const kda_inputs *in);
+
 /* Static description of a status code. */
 const char *kda_status_string(kda_status s);
 
 /* Message describing the last failure on the calling thread ("" if none). */
 const char *kda_last_error(void);
 
-/* Library ABI version (major * 100 + minor): 103 (101: kda_inputs gained
+/* Library ABI version (major * 100 + minor): 104 (101: kda_inputs gained
  * `flags`; 102: the forward-context entry points; 103: the final-state-only
- * forward, the start-state-gradient-only backward, kda_chunk_fwd_reuse). */
+ * forward, the start-state-gradient-only backward, kda_chunk_fwd_reuse; 104:
+ * kda_status_offset, kda_debug_bounded_wait). */
 int kda_version(void);
 
 /* Chunked forward without a caller workspace (no counterpart on the pages).
@@ -237,6 +251,12 @@ kda_status kda_chunk_fwd_noalloc(const kda_inputs *in, void *o, float *hT, void 
 /* ---- instrumentation (benchmarks and profiling; no counterpart on the pages) ----
  * Every kernel the library launches is counted.  While timing is enabled, a
  * CUDA event pair is recorded on the launching stream around each launch. */
+
+/* Runs one device thread that waits, bounded by `polls` polls (1 .. 2^24), on
+ * an mbarrier that nothing completes: the wait gives up and sets *err (a device
+ * int) to 1, the way a kernel of this library reports a copy that never
+ * arrived.  For tests of that path; it neither faults nor hangs the GPU. */
+kda_status kda_debug_bounded_wait(int *err, long long polls, void *stream);
 
 /* Kernels launched by this library in this process so far. */
 unsigned long long kda_launch_count(void);

@@ -236,3 +236,19 @@ def test_final_state_only_forward_validation(lib):
     st = lib.kda_chunk_fwd_reuse(ctypes.byref(s), ctypes.c_void_p(0x3000), None, None, 0, ctypes.c_void_p(0x10000),
                                  1 << 30, None)
     assert st == _lib.KDA_ERR_WORKSPACE and b"forward context" in lib.kda_last_error()
+
+
+def test_status_offset_follows_the_workspace_layout(lib):
+    """The status words sit after the sequence and chunk tables: byte offset
+    align256(16 N) + align256(16 NC), the same for every workspace of a problem."""
+    s = _inputs(K=128, V=128, T=200)               # N = 1, 4 chunks
+    assert lib.kda_status_offset(ctypes.byref(s)) == _a256(16) + _a256(16 * 4)
+    v = _inputs(K=64, V=64, T=1000, N=3, cu_seqlens=0x2000)  # packed: NC = ceil(1000/64) + N = 19
+    assert lib.kda_status_offset(ctypes.byref(v)) == _a256(16 * 3) + _a256(16 * 19)
+    assert lib.kda_status_offset(ctypes.byref(_inputs(HV=3))) == ctypes.c_size_t(-1).value
+
+
+def test_bounded_wait_probe_validation(lib):
+    assert lib.kda_debug_bounded_wait(None, 100, None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_debug_bounded_wait(ctypes.c_void_p(0x1000), 0, None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_debug_bounded_wait(ctypes.c_void_p(0x1000), (1 << 24) + 1, None) == _lib.KDA_ERR_INVALID_ARG
