@@ -78,9 +78,11 @@ constexpr uint32_t TMEM_COLS = 512;   // [0,128) dX h^T, [128,256) dO h^T, [256,
 // final dg column scan.  dG itself is parked in the Kr / Qr tiles: once a thread
 // has read its Kr, Qr (hi and lo) at (r, c..c+1), the 8 bytes of each pair slot
 // hold dG's Q and P parts of (r, c) and (r, c+1).
-constexpr uint32_t C_TOT = C_DAB;     // totals of Q, P [8 segments][128]; Khat column term [4 blocks][128]
-// (it ends inside the dL tiles: the next slot's dh' arrives in the dAqk^T tile during the assembly)
-static_assert(C_TOT + (8 + 8 + 4) * 128 * 4 <= C_DQK, "assembly scratch overflows the dL tiles");
+// The assembly's Khat column terms [4 blocks][128] go to the vector rows of the
+// block factors D_RI (dead after the pairwise chains), and the dg scan's segment
+// totals (of Q for segments 1..7 -- segment 0's is never read -- and of P for
+// segments 0..7) to 15 vector rows the scan does not read, so every chain tile
+// is free for the next slot's inputs as soon as its own work ends.
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct IntraArgs {
@@ -166,48 +168,58 @@ __device__ __forceinline__ bool get_slot(const Problem &P, const Workspace &W, i
   return true;
 }
 
-// A slot's inputs arrive in three groups of bulk / TMA copies (issued by one
-// thread), each into tiles that die at a different point of the previous
-// slot's work:
-//   P1 (after the pairwise chains): dh', v, A            -> the dAqk^T, X, T and A tiles
+// A slot's inputs arrive in three groups of bulk / TMA copies, each into tiles
+// that die at a different point of the previous slot's work:
+//   P1 (after the pairwise chains): dh', v, A, h columns 64..127 -> the dAqk^T, X, T, A and dL tiles
 //   P2 (after the assembly):        dO, dD columns 64..127, h columns 0..63 -> the Kc tile
-//   S  (after the dg scan):         X^T, D^T, dX, dO and dD columns 0..63, dX columns
-//                                   64..127, h columns 64..127 -> the Kr, Qr and dL tiles
+//   S  (once the dg scan holds its parked dG in registers): X^T, D^T, dX, dO and dD
+//                                   columns 0..63, dX columns 64..127 -> the Kr, Qr tiles
 // (G and beta follow P2 by cp.async from every thread.)  The stacked
 // [dX; dO; dD] operand is two 64-column sub-tiles of 192 rows; h and dh' are
-// the saved swizzled tiles, two 64-column halves each.
-constexpr uint32_t kBytesS = 2 * 16384u + 4 * 8192u + 16384u, kBytesP1 = 32768u + 16384u + 8192u,
+// the saved swizzled tiles, two 64-column halves each.  Inside the slot loop
+// thread 0 posts a group's byte count and lane 0 of warps 1.. issue one copy
+// each, so no warp stalls for a whole group's issue (an mbarrier's
+// transaction count may run below zero until the count is posted).
+constexpr uint32_t kBytesS = 2 * 16384u + 4 * 8192u, kBytesP1 = 32768u + 16384u + 8192u + 16384u,
                    kBytesP2 = 2 * 8192u + 16384u;
+constexpr int kCopiesS = 6, kCopiesP1 = 4, kCopiesP2 = 3;
 // X^T, D^T, h, dh', [dX; dO; dD], v, A: every operand once
 static_assert(kBytesS + kBytesP1 + kBytesP2 == 2 * 16384u + 2 * 32768u + 49152u + 16384u + 8192u, "group sizes");
-__device__ __forceinline__ void issue_s(uint32_t sbase, const Workspace &W, const TmaMaps &maps, const Slot &q,
-                                        uint64_t *bar) {
-  mbar_expect_tx(bar, kBytesS);
-  bulk_load(sbase + I_XT, W.tc_xt + q.slot * 16384, 16384u, bar);
-  bulk_load(sbase + I_DT, W.tc_dt + q.slot * 16384, 16384u, bar);
+__device__ __forceinline__ void copy_s(int i, uint32_t sbase, const Workspace &W, const TmaMaps &maps, const Slot &q,
+                                       uint64_t *bar) {
   const unsigned char *dx = reinterpret_cast<const unsigned char *>(W.tc_dx + q.slot * kC * kD);
   const unsigned char *dd = reinterpret_cast<const unsigned char *>(W.tc_dd + q.slot * kC * kD);
-  bulk_load(sbase + I_STK, dx, 8192u, bar);                       // dX: rows 0..63, sub-tile 0
-  bulk_load(sbase + I_STK + 192 * 128, dx + 8192, 8192u, bar);    //                 sub-tile 1
-  tma_load3(sbase + I_STK + 64 * 128, &maps.d, 0, q.j, q.t0, bar);  // dO: rows 64..127, sub-tile 0
-  bulk_load(sbase + I_STK + 128 * 128, dd, 8192u, bar);           // dD: rows 128..191, sub-tile 0
-  bulk_load(sbase + I_H + 16384, reinterpret_cast<const unsigned char *>(W.tc_hs + q.slot * kD * kD) + 16384,
-            16384u, bar);
+  switch (i) {
+    case 0: bulk_load(sbase + I_XT, W.tc_xt + q.slot * 16384, 16384u, bar); break;
+    case 1: bulk_load(sbase + I_DT, W.tc_dt + q.slot * 16384, 16384u, bar); break;
+    case 2: bulk_load(sbase + I_STK, dx, 8192u, bar); break;                        // dX: rows 0..63, sub-tile 0
+    case 3: bulk_load(sbase + I_STK + 192 * 128, dx + 8192, 8192u, bar); break;     //                 sub-tile 1
+    case 4: tma_load3(sbase + I_STK + 64 * 128, &maps.d, 0, q.j, q.t0, bar); break;  // dO: rows 64..127, sub-tile 0
+    default: bulk_load(sbase + I_STK + 128 * 128, dd, 8192u, bar); break;           // dD: rows 128..191, sub-tile 0
+  }
 }
-__device__ __forceinline__ void issue_p1(uint32_t sbase, const Workspace &W, const TmaMaps &maps, const Slot &q,
-                                         uint64_t *bar) {
-  mbar_expect_tx(bar, kBytesP1);
-  bulk_load(sbase + I_DH, W.tc_dh + q.slot * kD * kD, 32768u, bar);
-  tma_tile(sbase + I_V, &maps.v, q.j, q.t0, bar);
-  bulk_load(sbase + C_A, W.tc_tiles + q.slot * kTileRecord + kRecAM, 8192u, bar);
+__device__ __forceinline__ void copy_p1(int i, uint32_t sbase, const Workspace &W, const TmaMaps &maps,
+                                        const Slot &q, uint64_t *bar) {
+  switch (i) {
+    case 0: bulk_load(sbase + I_DH, W.tc_dh + q.slot * kD * kD, 32768u, bar); break;
+    case 1: tma_tile(sbase + I_V, &maps.v, q.j, q.t0, bar); break;
+    case 2: bulk_load(sbase + C_A, W.tc_tiles + q.slot * kTileRecord + kRecAM, 8192u, bar); break;
+    default:
+      bulk_load(sbase + I_H + 16384, reinterpret_cast<const unsigned char *>(W.tc_hs + q.slot * kD * kD) + 16384,
+                16384u, bar);
+      break;
+  }
 }
-__device__ __forceinline__ void issue_p2(uint32_t sbase, const Workspace &W, const TmaMaps &maps, const Slot &q,
-                                         uint64_t *bar) {
-  mbar_expect_tx(bar, kBytesP2);
-  tma_load3(sbase + I_STK + 256 * 128, &maps.d, 64, q.j, q.t0, bar);  // dO: rows 64..127, sub-tile 1
-  bulk_load(sbase + I_STK + 320 * 128,
-            reinterpret_cast<const unsigned char *>(W.tc_dd + q.slot * kC * kD) + 8192, 8192u, bar);  // dD, sub-tile 1
-  bulk_load(sbase + I_H, W.tc_hs + q.slot * kD * kD, 16384u, bar);
+__device__ __forceinline__ void copy_p2(int i, uint32_t sbase, const Workspace &W, const TmaMaps &maps,
+                                        const Slot &q, uint64_t *bar) {
+  switch (i) {
+    case 0: tma_load3(sbase + I_STK + 256 * 128, &maps.d, 64, q.j, q.t0, bar); break;  // dO: rows 64..127, sub-tile 1
+    case 1:
+      bulk_load(sbase + I_STK + 320 * 128, reinterpret_cast<const unsigned char *>(W.tc_dd + q.slot * kC * kD) + 8192,
+                8192u, bar);  // dD, sub-tile 1
+      break;
+    default: bulk_load(sbase + I_H, W.tc_hs + q.slot * kD * kD, 16384u, bar); break;
+  }
 }
 // G rows (zero past len) and beta of a slot, cp.async from every thread
 __device__ __forceinline__ void issue_gate_beta(uint32_t sbase, const Problem &P, float *beta, const Slot &q) {
@@ -255,9 +267,12 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
   bool have = get_slot(P, W, s_idx, cur);
   if (have) {  // the first slot: every group at once
     if (tid == 0) {
-      issue_s(sbase, W, maps, cur, bar_s);
-      issue_p1(sbase, W, maps, cur, bar_p1);
-      issue_p2(sbase, W, maps, cur, bar_p2);
+      mbar_expect_tx(bar_s, kBytesS);
+      mbar_expect_tx(bar_p1, kBytesP1);
+      mbar_expect_tx(bar_p2, kBytesP2);
+      for (int i = 0; i < kCopiesS; ++i) copy_s(i, sbase, W, maps, cur, bar_s);
+      for (int i = 0; i < kCopiesP1; ++i) copy_p1(i, sbase, W, maps, cur, bar_p1);
+      for (int i = 0; i < kCopiesP2; ++i) copy_p2(i, sbase, W, maps, cur, bar_p2);
     }
     issue_gate_beta(sbase, P, beta, cur);
   }
@@ -577,9 +592,12 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     }
     __syncthreads();  // every warp is done with the chain tiles: dL .. T become the assembly scratch
     KDA_PT(5);
-    if (more && tid == 0) {  // the next slot's dh', v, A into the dead dAqk^T, X, T and A tiles
-      fence_async_smem();
-      issue_p1(sbase, W, maps, nxt, bar_p1);
+    if (more) {  // the next slot's dh', v, A and h columns 64..127 into the dead dAqk^T, X, T, A and dL tiles
+      if (tid == 0) mbar_expect_tx(bar_p1, kBytesP1);
+      if (lane == 0 && warp >= 1 && warp <= kCopiesP1) {
+        fence_async_smem();
+        copy_p1(warp - 1, sbase, W, maps, nxt, bar_p1);
+      }
     }
 
     // ---- assembly (fragment element (r, c)), in four passes of 8 columns per warp ----
@@ -590,7 +608,12 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     // Kc = k e2 hold.  dg = reverse cumsum of dG over the chunk runs once, after
     // the last pass, as column scans over 16-row segments with segment totals
     // exchanged in shared memory.
-    float *totQ = (float *)(sm + C_TOT), *totP = totQ + 8 * kD, *totC = totP + 8 * kD;
+    float *totC = vec + V_D * kD;  // [4 blocks][128] in the rows of the block factors
+    // segment totals of the dg scan, rows of 128 fp32 (k = 0..14): every vector row
+    // but 2^G_last and the four holding totC
+    auto tot_row = [&](int k) -> float * {
+      return vec + (k == 0 ? V_GL : k < 9 ? V_GREF + (k - 1) : k < 11 ? V_D + 4 + (k - 9) : V_LAM + (k - 11)) * kD;
+    };
     const float *dglv = red + 64;
     const int i8 = lane >> 2, l4 = lane & 3;
     float bpart[2] = {0.f, 0.f};
@@ -679,9 +702,10 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     __syncthreads();  // every thread has parked its dG and its Khat column terms
     KDA_PT(11);
     if (more) {  // the Kc tile, G and beta are dead: the next slot's group P2, G and beta
-      if (tid == 0) {
+      if (tid == 0) mbar_expect_tx(bar_p2, kBytesP2);
+      if (lane == 0 && warp >= 1 && warp <= kCopiesP2) {
         fence_async_smem();
-        issue_p2(sbase, W, maps, nxt, bar_p2);
+        copy_p2(warp - 1, sbase, W, maps, nxt, bar_p2);
       }
       issue_gate_beta(sbase, P, beta, nxt);
     }
@@ -701,15 +725,24 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
         tq.x += q8[k].x; tq.y += q8[k].y;
         tp.x += p8[k].x; tp.y += p8[k].y;
       }
-      *reinterpret_cast<float2 *>(totQ + seg * kD + c) = tq;
-      *reinterpret_cast<float2 *>(totP + seg * kD + c) = tp;
-      __syncthreads();
+      if (seg > 0) *reinterpret_cast<float2 *>(tot_row(seg - 1) + c) = tq;  // Q totals: rows 0..6
+      *reinterpret_cast<float2 *>(tot_row(7 + seg) + c) = tp;                // P totals: rows 7..14
+      __syncthreads();  // every thread holds its parked dG in registers: the Kr, Qr tiles are dead
+      if (more) {  // the next slot's X^T, D^T, dX and the first column halves of dO, dD into them
+        if (tid == 0) mbar_expect_tx(bar_s, kBytesS);
+        if (lane == 0 && warp >= 1 && warp <= kCopiesS) {
+          fence_async_smem();
+          copy_s(warp - 1, sbase, W, maps, nxt, bar_s);
+        }
+      }
       float2 aq = make_float2(0.f, 0.f), aps = aq, app = aq;
 #pragma unroll
       for (int s2 = 0; s2 < 8; ++s2) {
-        const float2 a = *reinterpret_cast<const float2 *>(totQ + s2 * kD + c);
-        const float2 b = *reinterpret_cast<const float2 *>(totP + s2 * kD + c);
-        if (s2 > seg) { aq.x += a.x; aq.y += a.y; aps.x += b.x; aps.y += b.y; }
+        const float2 b = *reinterpret_cast<const float2 *>(tot_row(7 + s2) + c);
+        if (s2 > seg) {
+          const float2 a = *reinterpret_cast<const float2 *>(tot_row(s2 - 1) + c);
+          aq.x += a.x; aq.y += a.y; aps.x += b.x; aps.y += b.y;
+        }
         if (s2 < seg) { app.x += b.x; app.y += b.y; }
       }
       float2 ks = make_float2(0.f, 0.f);
@@ -752,18 +785,15 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       if (l4 == 0) rb[(warp >> 2) * kC + 16 * Bk + i8 + 8 * hh] = v;
     }
-    const bool all_ok = __syncthreads_and(ok) != 0;  // the dg scan is done: Kr, Qr and dL are dead
+    const bool all_ok = __syncthreads_and(ok) != 0;
     KDA_PT(7);
-    if (more && all_ok && tid == 0) {
-      fence_async_smem();
-      issue_s(sbase, W, maps, nxt, bar_s);
-    }
     if (tid < kC && tid < len)
       args.dbeta[(size_t)(t0 + tid) * HV + j] = red[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
     KDA_PT(8);
     if (!all_ok) {  // a wait gave up (error flag set): let the copies already issued land, then stop
       if (more) {
         if (tid == 0) {
+          bar_wait(bar_s, par ^ 1u, args.err);
           bar_wait(bar_p1, par ^ 1u, args.err);
           bar_wait(bar_p2, par ^ 1u, args.err);
         }
