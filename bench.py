@@ -73,7 +73,8 @@ def algorithmic_flops(cfg, C=64):
 def kernel_bytes_per_token(name, cfg):
     e = 2 if cfg.dtype == torch.bfloat16 else 4
     H, HV, K, V = cfg.H, cfg.HV, cfg.K, cfg.V
-    qk, vv, g, b = H * K * e, HV * V * e, 4 * HV * K, 4 * HV
+    qk, vv, b = H * K * e, HV * V * e, 4 * HV
+    g = 4 * HV if cfg.g.dim() == 3 else 4 * HV * K  # a scalar gate: one fp32 per (token, value head)
     f32K, f32V, cc, hh = 4 * HV * K, 4 * HV * V, 4 * HV * 64, 4 * HV * K * V / 64
     hs = 2 * HV * K * V / 64            # bf16 K x V state per chunk, per token
     t16 = 16384 * HV / 64               # one 16 KB per-chunk tile (X^T or D^T), per token

@@ -124,7 +124,7 @@ size_t layout(const Problem &P, bool backward, bool with_ctx, char *base, Worksp
   w.seq = (int4 *)take(sizeof(int4) * (size_t)(P.N > 0 ? P.N : 1));
   w.chunk = (int4 *)take(sizeof(int4) * (size_t)(P.NC > 0 ? P.NC : 1));
   w.flags = (int *)take(sizeof(int) * 4);
-  if (P.scalar_gate) {  // the gate repeated over K (and its per-channel gradient)
+  if (P.scalar_gate && !use_tc(P)) {  // fp32 path: the gate repeated over K (and its per-channel gradient)
     w.gx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
     if (backward) w.dgx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
   }
@@ -170,10 +170,11 @@ size_t layout(const Problem &P, bool backward, bool with_ctx, char *base, Worksp
   return off;
 }
 
-// With a scalar gate every kernel reads the gate repeated over K from the
-// workspace (the recurrent kernel alone reads the scalars directly).
+// With a scalar gate the fp32 chunked kernels read the gate repeated over K
+// from the workspace; the tensor-core kernels and the recurrent kernel read
+// the scalars directly.
 cudaError_t gate_per_channel(const Problem &P, const Workspace &W, Problem *Pg, cudaStream_t s) {
-  if (!P.scalar_gate) return cudaSuccess;
+  if (!P.scalar_gate || use_tc(P)) return cudaSuccess;  // the tensor-core kernels broadcast the scalars themselves
   cudaError_t e = launch_gate_expand(P, W.gx, s);
   Pg->g = W.gx;
   return e;
@@ -267,7 +268,8 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
   cudaStream_t s = (cudaStream_t)stream;
   Problem Pg = P;
   cudaError_t e = gate_per_channel(P, W, &Pg, s);
-  float *dgk = P.scalar_gate ? W.dgx : dg;  // per-channel gate gradient
+  // per-channel gate gradient (a scalar gate's dg is summed over K inside the tensor-core kernel)
+  float *dgk = P.scalar_gate && !use_tc(P) ? W.dgx : dg;
   if (e == cudaSuccess) {
     if (use_tc(P)) {
       int *err = W.flags + 2;
@@ -286,7 +288,7 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
       if (e == cudaSuccess) e = simple_backward(Pn, W, dO, dhT, dq, dk, dv, dgk, dbeta, dh0, state_only, s);
     }
   }
-  if (e == cudaSuccess && P.scalar_gate && !state_only) e = launch_gate_grad_reduce(P, W.dgx, dg, s);
+  if (e == cudaSuccess && P.scalar_gate && !use_tc(P) && !state_only) e = launch_gate_grad_reduce(P, W.dgx, dg, s);
   if (e != cudaSuccess) return cuda_fail(e, with_ctx ? "kda_chunk_bwd_ctx" : "kda_chunk_bwd");
   return KDA_OK;
 }

@@ -1,9 +1,11 @@
 // Scalar gate (KDA_SCALAR_GATE, the GDN variant): one log2 decay per (token,
-// value head), shared by every key channel.  The chunked kernels are written
-// for KDA's per-channel gate, so the scalar gate reaches them repeated over
-// K (gate_expand_kernel), and the per-channel gate gradient they produce is
-// summed back over K (gate_grad_reduce_kernel): dg_t = sum_c dG_t[c], the
-// chain rule of g_t[c] = g_t for every c.
+// value head), shared by every key channel.  The fp32 chunked kernels are
+// written for KDA's per-channel gate, so the scalar gate reaches them repeated
+// over K (gate_expand_kernel), and the per-channel gate gradient they produce
+// is summed back over K (gate_grad_reduce_kernel): dg_t = sum_c dG_t[c], the
+// chain rule of g_t[c] = g_t for every c.  (The tensor-core kernels do both
+// inside: they repeat the scalars into their shared-memory gate tile and sum
+// dg over the channels in their dg scan.)
 //
 // Both kernels are HBM-bound streams: 16-byte stores of the expanded rows;
 // one warp per (token, value head) row for the sum, in a fixed order.

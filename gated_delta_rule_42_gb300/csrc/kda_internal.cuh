@@ -35,7 +35,7 @@ struct Problem {
   int NC;        // chunk-table capacity, an upper bound on the number of chunks
   bool bf16;
   bool l2norm;   // KDA_QK_L2NORM: q, k rows L2-normalised inside the op
-  bool scalar_gate;  // KDA_SCALAR_GATE: g, dg are [Ttot][HV] (the kernels see g repeated over K)
+  bool scalar_gate;  // KDA_SCALAR_GATE: g, dg are [Ttot][HV] (the fp32 kernels see g repeated over K)
   const void *q, *k, *v;
   const float *g, *beta, *h0;
   const int32_t *cu;

@@ -221,10 +221,29 @@ __device__ __forceinline__ void copy_p2(int i, uint32_t sbase, const Workspace &
     default: bulk_load(sbase + I_H, W.tc_hs + q.slot * kD * kD, 16384u, bar); break;
   }
 }
-// G rows (zero past len) and beta of a slot, cp.async from every thread
-__device__ __forceinline__ void issue_gate_beta(uint32_t sbase, const Problem &P, float *beta, const Slot &q) {
-  load_gate<kCT>(sbase + C_G, P.g, q.t0, q.len, P.HV, q.j);
+// G rows (zero past len) and beta of a slot, cp.async from every thread; a
+// scalar gate (one decay per token) is repeated over the 128 channels instead
+template <bool kScalarGate>
+__device__ __forceinline__ void issue_gate_beta(uint32_t sbase, unsigned char *sm, const Problem &P, float *beta,
+                                                const Slot &q) {
   const int tid = threadIdx.x;
+  if (kScalarGate) {
+    float *G = (float *)(sm + C_G);
+    constexpr int kIt = kC * 32 / kCT;  // float4 stores per thread; all loads go out first
+    float x[kIt];
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      const int r = (tid + u * kCT) >> 5;
+      x[u] = r < q.len ? P.g[(size_t)(q.t0 + r) * P.HV + q.j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      const int it = tid + u * kCT, r = it >> 5, c4 = (it & 31) * 4;
+      *reinterpret_cast<float4 *>(G + r * kGLD + c4) = make_float4(x[u], x[u], x[u], x[u]);
+    }
+  } else {
+    load_gate<kCT>(sbase + C_G, P.g, q.t0, q.len, P.HV, q.j);
+  }
   if (tid < kC) {
     if (tid < q.len) cp4(smem_u32(beta + tid), P.beta + (size_t)(q.t0 + tid) * P.HV + q.j);
     else beta[tid] = 0.f;
@@ -232,6 +251,8 @@ __device__ __forceinline__ void issue_gate_beta(uint32_t sbase, const Problem &P
   cp_commit();
 }
 
+// kScalarGate: g and dg are [tokens][HV] (one decay per token, repeated over the channels here)
+template <bool kScalarGate>
 __global__ void __launch_bounds__(kCT, 1)
 kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smraw[];
@@ -274,7 +295,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       for (int i = 0; i < kCopiesP1; ++i) copy_p1(i, sbase, W, maps, cur, bar_p1);
       for (int i = 0; i < kCopiesP2; ++i) copy_p2(i, sbase, W, maps, cur, bar_p2);
     }
-    issue_gate_beta(sbase, P, beta, cur);
+    issue_gate_beta<kScalarGate>(sbase, sm, P, beta, cur);
   }
   for (uint32_t it = 0; have; ++it) {
     const uint32_t par = it & 1u;
@@ -609,6 +630,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     // the last pass, as column scans over 16-row segments with segment totals
     // exchanged in shared memory.
     float *totC = vec + V_D * kD;  // [4 blocks][128] in the rows of the block factors
+    float sg_part = 0.f;            // scalar gate: this warp's share of dg for row 8 * seg + lane (lanes 0..7)
     // segment totals of the dg scan, rows of 128 fp32 (k = 0..14): every vector row
     // but 2^G_last and the four holding totC
     auto tot_row = [&](int k) -> float * {
@@ -707,7 +729,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
         fence_async_smem();
         copy_p2(warp - 1, sbase, W, maps, nxt, bar_p2);
       }
-      issue_gate_beta(sbase, P, beta, nxt);
+      issue_gate_beta<kScalarGate>(sbase, sm, P, beta, nxt);
     }
     {  // dg = reverse cumsum of dG: thread = one column pair, one 8-row segment (8 segments)
       const int c = 2 * (tid & 63), seg = tid >> 6, mid = len >> 1;
@@ -768,10 +790,15 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
         const int r = 8 * seg + k;
         qs.x += q8[k].x; qs.y += q8[k].y;
         ps.x += p8[k].x; ps.y += p8[k].y;
-        if (r < len) {
-          const bool hi = r >= mid;
-          *reinterpret_cast<float2 *>(args.dg + ((size_t)(t0 + r) * HV + j) * kD + c) =
-              make_float2(qs.x + carried.x + (hi ? ps.x : -pre[k].x), qs.y + carried.y + (hi ? ps.y : -pre[k].y));
+        const bool hi = r >= mid;
+        const float2 v = make_float2(qs.x + carried.x + (hi ? ps.x : -pre[k].x), qs.y + carried.y + (hi ? ps.y : -pre[k].y));
+        if (kScalarGate) {  // dg_t = sum over the channels: this warp's 64 columns, row k's sum kept by lane k
+          float t = r < len ? v.x + v.y : 0.f;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+          if (lane == k) sg_part = t;
+        } else if (r < len) {
+          *reinterpret_cast<float2 *>(args.dg + ((size_t)(t0 + r) * HV + j) * kD + c) = v;
         }
       }
     }
@@ -789,6 +816,15 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     KDA_PT(7);
     if (tid < kC && tid < len)
       args.dbeta[(size_t)(t0 + tid) * HV + j] = red[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
+    if (kScalarGate) {  // the two warps of each 8-row segment add their halves of the 128 channels
+      float *part = vec + V_GL * kD;  // [16 warps][8 rows]: the dg scan has read its totals
+      if (lane < 8) part[warp * 8 + lane] = sg_part;
+      __syncthreads();
+      if (tid < kC && tid < len) {
+        const int sg = tid >> 3, k = tid & 7;
+        args.dg[(size_t)(t0 + tid) * HV + j] = part[(2 * sg) * 8 + k] + part[(2 * sg + 1) * 8 + k];
+      }
+    }
     KDA_PT(8);
     if (!all_ok) {  // a wait gave up (error flag set): let the copies already issued land, then stop
       if (more) {
@@ -821,8 +857,8 @@ KDA_PT_EXPORT(kda_debug_intra_phase_cycles)
 cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *dO, void *dv, void *dq, void *dk,
                               float *dg, float *dbeta, int *err, cudaStream_t s) {
   if (P.NC == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)C_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(P.scalar_gate ? kda_bwd_intra_tc_kernel<true> : kda_bwd_intra_tc_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
   const bool partial = P.HV != P.H || P.l2norm;  // fp32 partials, reduced (and normalised) per q/k head
   IntraArgs a{(const __nv_bfloat16 *)dO, (__nv_bfloat16 *)dv, partial ? (void *)W.dqp : dq,
@@ -833,7 +869,10 @@ cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *
   if ((e = sm_count(&nsm)) != cudaSuccess) return e;
   const int64_t slots = (int64_t)P.NC * P.HV;
   const unsigned grid = (unsigned)(slots < nsm ? slots : nsm);  // one CTA per SM, persistent over the slots
-  KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
+  if (P.scalar_gate)
+    KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<true><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
+  else
+    KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<false><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
   return cudaGetLastError();
 }
 

@@ -373,10 +373,25 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
   }
   __syncthreads();
   if (tid == 0) {  // k, q rows and the gate rows (TMA); rows past the tensor end arrive as zeros
-    mbar_expect_tx(bar, 32768u + 32768u);
+    mbar_expect_tx(bar, 32768u + (P.scalar_gate ? 0u : 32768u));
     tma_tile(sbase + P_K, &maps.k, h, t0, bar);
     tma_tile(sbase + P_Q, &maps.q, h, t0, bar);
-    tma_load3(sbase + P_G, &maps.g, 0, j, t0, bar);
+    if (!P.scalar_gate) tma_load3(sbase + P_G, &maps.g, 0, j, t0, bar);
+  }
+  if (P.scalar_gate) {  // one decay per token: repeated over the 128 channels of the gate tile
+    float *Gt = (float *)(sm + P_G);
+    constexpr int kIt = kC * 32 / kThr;  // float4 stores per thread; all loads go out first
+    float x[kIt];
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      const int r = (tid + u * kThr) >> 5;
+      x[u] = r < len ? P.g[(size_t)(t0 + r) * HV + j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      const int it = tid + u * kThr, r = it >> 5, c4 = (it & 31) * 4;
+      *reinterpret_cast<float4 *>(Gt + r * kGT + c4) = make_float4(x[u], x[u], x[u], x[u]);
+    }
   }
   load_beta(P, beta, t0, len, j);
   cp_commit();

@@ -54,6 +54,7 @@ cudaError_t make_tma_maps(const Problem &P, const void *v, const void *d, TmaMap
   if ((e = encode(&out->q, P.q, 2, P.H, P.Ttot, 64, true)) != cudaSuccess) return e;
   if (v != nullptr && (e = encode(&out->v, v, 2, P.HV, P.Ttot, 64, true)) != cudaSuccess) return e;
   if (d != nullptr && (e = encode(&out->d, d, 2, P.HV, P.Ttot, 64, true)) != cudaSuccess) return e;
+  if (P.scalar_gate) return cudaSuccess;  // [tokens][HV] scalars: no tiled view (the kernels broadcast them)
   return encode(&out->g, P.g, 4, P.HV, P.Ttot, 128, false);
 }
 
