@@ -477,8 +477,8 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float g = G[r * kGLD + c0 + e];
-          e1[e] = exp2f(g - gref[e]);
-          e2[e] = exp2f(gref[e] - g);
+          e1[e] = ex2(g - gref[e]);
+          e2[e] = ex2(gref[e] - g);
         }
         uint4 hi, lo;
 #pragma unroll
@@ -678,7 +678,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
             const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = u ? vk.y : vk.x;
             const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
             const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
-            const float e1 = exp2f(gg_ - gref), e2 = exp2f(gref - gg_);
+            const float e1 = ex2(gg_ - gref), e2 = ex2(gref - gg_);
             const float gam = e1 * eref, kh = e2 * lam;
             const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
             const float xyI = xyi[nt][2 * hh + u];

@@ -110,6 +110,15 @@ __device__ __forceinline__ uint32_t idesc(int M, int N, int a_mn, int b_mn) {
   return idesc_bf16(M, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
 }
 
+// 2^x for the per-element decay factors: one hardware base-2 exponential (PTX
+// ex2.approx.ftz.f32, within about 2 ulp; results below 2^-126 flush to zero).
+// The factors it serves lie within 2^-120 .. 2^120 for gates >= -8 per token.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Asynchronous loads of one chunk's gate rows ([tokens][HV][128] fp32) into a
 // [64][kGLD] tile; rows at or past len are zeroed.
 template <int NT = kThr>

@@ -145,8 +145,8 @@ __device__ __forceinline__ void phase_a(unsigned char *sm, int len, const float 
       *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + 4);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        e1[e] = exp2f(g[e] - gref[e]);  // <= 1
-        e2[e] = exp2f(gref[e] - g[e]);  // >= 1
+        e1[e] = ex2(g[e] - gref[e]);  // <= 1
+        e2[e] = ex2(gref[e] - g[e]);  // >= 1
       }
       const float br = beta[r];
 #pragma unroll
