@@ -139,7 +139,7 @@ size_t layout(const Problem &P, bool backward, bool with_ctx, char *base, Worksp
       w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);
       w.tc_dd = (__nv_bfloat16 *)take(2 * slots * C * V);
       w.tc_dx = (__nv_bfloat16 *)take(2 * slots * C * V);
-      if (P.HV != P.H || P.l2norm) {  // fp32 dq, dk partials, reduced per q/k head afterwards
+      if (P.HV != P.H) {  // fp32 dq, dk partials, reduced (and normalised) per q/k head afterwards
         w.dqp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
         w.dkp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
       }
@@ -280,7 +280,7 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
       if (e == cudaSuccess) e = tc_backward_scan(Pg, W, dO, dhT, dh0, err, s);
       if (!state_only) {
         if (e == cudaSuccess) e = tc_backward_intra(Pg, W, dO, dv, dq, dk, dgk, dbeta, err, s);
-        if (e == cudaSuccess && (P.HV != P.H || P.l2norm)) e = launch_group_reduce(Pg, W.dqp, W.dkp, dq, dk, s);
+        if (e == cudaSuccess && P.HV != P.H) e = launch_group_reduce(Pg, W.dqp, W.dkp, dq, dk, s);
       }
     } else {
       Problem Pn = Pg;

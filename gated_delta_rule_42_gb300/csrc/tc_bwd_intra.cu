@@ -251,8 +251,11 @@ __device__ __forceinline__ void issue_gate_beta(uint32_t sbase, unsigned char *s
   cp_commit();
 }
 
-// kScalarGate: g and dg are [tokens][HV] (one decay per token, repeated over the channels here)
-template <bool kScalarGate>
+// kScalarGate: g and dg are [tokens][HV] (one decay per token, repeated over the channels here).
+// kL2: the q/k L2-norm prologue with HV = H, its backward fused: dx = r (dy - y (y . dy)) per
+// (token, head) row, from the inverse norms r of the decay-tile pass and row dots y . dy that a
+// first pass over the assembly's formulas forms, so dq and dk leave as bf16 in one pass.
+template <bool kScalarGate, bool kL2>
 __global__ void __launch_bounds__(kCT, 1)
 kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smraw[];
@@ -468,6 +471,10 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
             sq += __shfl_xor_sync(0xffffffffu, sq, o);
           }
           const float rk = 1.0f / sqrtf(sk + kL2NormEps), rq = 1.0f / sqrtf(sq + kL2NormEps);
+          if (kL2 && jj == 0) {  // the row's inverse norms, for the fused backward (rb is free until the dbeta partials)
+            rb[r] = rk;
+            rb[kC + r] = rq;
+          }
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             kv[e] *= rk;
@@ -639,6 +646,68 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     const float *dglv = red + 64;
     const int i8 = lane >> 2, l4 = lane & 3;
     float bpart[2] = {0.f, 0.f};
+    float dotq[2] = {0.f, 0.f}, dotk[2] = {0.f, 0.f};  // kL2: y . dy of rows i8, i8 + 8 of block Bk
+    if (kL2) {
+      // per-quarter partial dots [4 column quarters][64 rows]: q in the rows of the last two
+      // block factors, k in the unused row and the upper half of the dbeta partials
+      float *pdq = vec + (V_D + 4) * kD;
+      float *pdk = (warp >> 2) < 2 ? vec + V_GL * kD + (warp >> 2) * kC : rb + 2 * kC + ((warp >> 2) - 2) * kC;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int c = ch0 + 8 * nt + 2 * l4;
+        float px[4], po[4], pk[4];
+        {
+          const uint32_t tb = tmem + ((uint32_t)(32 * Bk) << 16) + (uint32_t)(ch0 + 8 * nt);
+          tmem_ld_frag3(tb, tb + 128u, tb + 256u, px, po, pk);
+        }
+        const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
+        const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
+        const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * Bk + i8 + 8 * hh;
+          const float br = beta[r];
+          const uint32_t to = sw_off(r, c, kC);
+          const float2 krh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + to));
+          const float2 krl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + LO128 + to));
+          const float2 qrh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + to));
+          const float2 qrl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + LO128 + to));
+          const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float Kr = u ? krh.y + krl.y : krh.x + krl.x, Qr = u ? qrh.y + qrl.y : qrh.x + qrl.x;
+            const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
+            const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
+            const float e1 = ex2(gg_ - gref), e2 = ex2(gref - gg_);
+            const float dq2 = po[2 * hh + u] * (e1 * eref) + e1 * yr[nt][2 * hh + u];
+            const float dk2 = pk[2 * hh + u] * (e2 * lam) - br * (e1 * eref) * px[2 * hh + u] +
+                              br * e1 * xr[nt][2 * hh + u] + e2 * xyi[nt][2 * hh + u];
+            dotq[hh] = fmaf(Qr * e2, dq2, dotq[hh]);  // y_q = Qr e2 / qscale and dy_q = qscale dq2
+            dotk[hh] = fmaf(Kr * e2, dk2, dotk[hh]);  // y_k = Kr e2 and dy_k = dk2
+          }
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+          dotq[hh] += __shfl_xor_sync(0xffffffffu, dotq[hh], o);
+          dotk[hh] += __shfl_xor_sync(0xffffffffu, dotk[hh], o);
+        }
+        if (l4 == 0) {
+          const int r = 16 * Bk + i8 + 8 * hh;
+          pdq[(warp >> 2) * kC + r] = dotq[hh];
+          pdk[r] = dotk[hh];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * Bk + i8 + 8 * hh;
+        dotq[hh] = pdq[r] + pdq[kC + r] + pdq[2 * kC + r] + pdq[3 * kC + r];
+        dotk[hh] = vec[V_GL * kD + r] + vec[V_GL * kD + kC + r] + rb[2 * kC + r] + rb[3 * kC + r];
+      }
+    }
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       KDA_PT(9);
@@ -669,7 +738,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
           const float2 kch = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + to));
           const float2 kcl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + LO128 + to));
           const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
-          float dq2[2], dk2[2], qv[2], pv[2];
+          float dq2[2], dk2[2], qv[2], pv[2], yq[2], yk[2];  // yq, yk: kL2's normalised rows (yq times qscale)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const float Kr = u ? krh.y + krl.y : krh.x + krl.x;  // k e1
@@ -684,6 +753,8 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
             const float xyI = xyi[nt][2 * hh + u];
             dq2[u] = dQg * gam + e1 * yR;
             dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * xyI;
+            yq[u] = Qr * e2;
+            yk[u] = Kr * e2;
             // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
             const bool in = r < len;
             qv[u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
@@ -698,7 +769,14 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
           *qrl_p = __float_as_uint(pv[1]);
           if (r < len) {
             const size_t tok = (size_t)(t0 + r);
-            if (args.partial) {
+            if (kL2) {  // dx = r (dy - y (y . dy)), y_q = Qr e2 / qscale, y_k = Kr e2
+              const float rk = rb[r], rq = rb[kC + r], dq_dot = dotq[hh] / qscale;
+              __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
+              __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
+              *reinterpret_cast<uint32_t *>(pq) = pack_bf16(rq * (dq2[0] * qscale - yq[0] * dq_dot),
+                                                          rq * (dq2[1] * qscale - yq[1] * dq_dot));
+              *reinterpret_cast<uint32_t *>(pk) = pack_bf16(rk * (dk2[0] - yk[0] * dotk[hh]), rk * (dk2[1] - yk[1] * dotk[hh]));
+            } else if (args.partial) {
               float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
               *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
               *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
@@ -854,26 +932,34 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 
 KDA_PT_EXPORT(kda_debug_intra_phase_cycles)
 
+template <bool kSG, bool kL2>
+cudaError_t launch_intra(const Problem &P, const Workspace &W, const IntraArgs &a, const TmaMaps &maps, unsigned grid,
+                         cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C_SMEM);
+  if (e != cudaSuccess) return e;
+  KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<kSG, kL2><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
+  return cudaGetLastError();
+}
+
 cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *dO, void *dv, void *dq, void *dk,
                               float *dg, float *dbeta, int *err, cudaStream_t s) {
   if (P.NC == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(P.scalar_gate ? kda_bwd_intra_tc_kernel<true> : kda_bwd_intra_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
-  if (e != cudaSuccess) return e;
-  const bool partial = P.HV != P.H || P.l2norm;  // fp32 partials, reduced (and normalised) per q/k head
+  // fp32 partials when several value heads share a q/k head (reduced, and with the L2-norm
+  // prologue normalised, per q/k head afterwards); with HV = H the L2-norm backward is fused
+  const bool partial = P.HV != P.H, fuse_l2 = P.l2norm && !partial;
   IntraArgs a{(const __nv_bfloat16 *)dO, (__nv_bfloat16 *)dv, partial ? (void *)W.dqp : dq,
               partial ? (void *)W.dkp : dk, dg, dbeta, partial, err};
   TmaMaps maps;
-  if ((e = make_tma_maps(P, P.v, dO, &maps)) != cudaSuccess) return e;
+  cudaError_t e = make_tma_maps(P, P.v, dO, &maps);
+  if (e != cudaSuccess) return e;
   int nsm = 0;
   if ((e = sm_count(&nsm)) != cudaSuccess) return e;
   const int64_t slots = (int64_t)P.NC * P.HV;
   const unsigned grid = (unsigned)(slots < nsm ? slots : nsm);  // one CTA per SM, persistent over the slots
-  if (P.scalar_gate)
-    KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<true><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
-  else
-    KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<false><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
-  return cudaGetLastError();
+  if (P.scalar_gate) return fuse_l2 ? launch_intra<true, true>(P, W, a, maps, grid, s)
+                                    : launch_intra<true, false>(P, W, a, maps, grid, s);
+  return fuse_l2 ? launch_intra<false, true>(P, W, a, maps, grid, s) : launch_intra<false, false>(P, W, a, maps, grid, s);
 }
 
 }  // namespace kda
