@@ -114,7 +114,7 @@ NCU_TRAFFIC = {
         bytes_per_token=1281294592 / 8192,  # 974.5 MB read + 306.8 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_intra.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh",
                  "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="c61f4101d5537827462bd65ba826ca4cc7697094e196ea357cf1966f4b4da6cd",
+        sha256="e0b0a192344717a07c01b1fbb5ea461f58c667d9e4fdedaf1608e9063bbb319a",
         profile="profiles/ncu_full_kernels_B8_T1024_H32_K128.md"),
 }
 

@@ -6,10 +6,11 @@
 // work leaves them dead (three groups, below), so most of each slot's loads
 // overlap the previous slot's chain and assembly.  Inputs: the
 // chunk-start state h and the tiles X^T (X = beta v - Bk h), D^T (D = A X) and
-// A from the forward recompute, the gradient of the chunk-end state dh', and
-// dD, dX from the reverse scan.  First, on tcgen05 (fp32 in TMEM):
-//   [dX; dO] h^T    -> rows 0..63: -dBk, rows 64..127: dQg   (one M=128 product)
-//   dKhat^T = dh' D^T                                          (Khat = k 2^(G_last - G))
+// A that the forward kept (or its recompute saved), the gradient of the
+// chunk-end state dh', and dD, dX from the reverse scan.  First, on tcgen05
+// (fp32 in TMEM):
+//   dX h^T -> -dBk,  dO h^T -> dQg                             (two M=64 products)
+//   dKhat = D dh'^T                                            (Khat = k 2^(G_last - G))
 //   [X; D] [dO; dD]^T -> block (X, dD) = dA^T, block (D, dO) = dAqk^T
 // and on the SIMT cores dv = beta dX, sum_v dX v and d(2^G_last) = rowsum(dh' .* h).
 // The products never leave the chip: the chain reads them from TMEM.  It
@@ -634,7 +635,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     // chain accumulators.  Raw k and q are not re-read: every term that needs them
     // is a product with a decay factor that the hi/lo tiles Kr = k e1, Qr = q~ e1,
     // Kc = k e2 hold.  dg = reverse cumsum of dG over the chunk runs once, after
-    // the last pass, as column scans over 16-row segments with segment totals
+    // the last pass, as column-pair scans over 8-row segments with segment totals
     // exchanged in shared memory.
     float *totC = vec + V_D * kD;  // [4 blocks][128] in the rows of the block factors
     float sg_part = 0.f;            // scalar gate: this warp's share of dg for row 8 * seg + lane (lanes 0..7)
