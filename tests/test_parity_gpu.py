@@ -213,6 +213,7 @@ SG = [
     ("tc_dense", dict(B=2, T=130, H=2, HV=2, K=128, V=128), torch.bfloat16, False),
     ("tc_varlen_gva_l2norm", dict(B=1, T=300, H=2, HV=4, K=128, V=128, cu_seqlens=[0, 0, 100, 100, 250]),
      torch.bfloat16, True),
+    ("tc_dense_l2norm", dict(B=1, T=200, H=2, HV=2, K=128, V=128), torch.bfloat16, True),  # fused norm backward
     ("fp32_gva_odd", dict(B=1, T=129, H=1, HV=3, K=32, V=48), torch.float32, False),
 ]
 
