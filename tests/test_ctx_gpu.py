@@ -38,6 +38,7 @@ CASES = [
     ("tc_varlen_gva_empty", dict(B=1, T=300, H=2, HV=4, K=128, V=128, cu_seqlens=[0, 0, 100, 100, 300]),
      False, True),
     ("tc_l2norm", dict(B=1, T=200, H=1, HV=2, K=128, V=128), True, False),
+    ("tc_l2norm_fused", dict(B=1, T=200, H=2, HV=2, K=128, V=128), True, True),
     ("tc_scalar_gate", dict(B=1, T=190, H=2, HV=4, K=128, V=128, scalar_gate=True), False, True),
     ("general_bf16_k64", dict(B=1, T=150, H=1, HV=2, K=64, V=64), False, True),
     ("general_fp32", dict(B=1, T=100, H=1, HV=2, K=128, V=128, dtype=torch.float32), False, True),

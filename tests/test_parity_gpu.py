@@ -180,6 +180,8 @@ L2 = [
     ("tc_dense", dict(B=2, T=130, H=2, HV=2, K=128, V=128), torch.bfloat16),
     ("tc_varlen_gva", dict(B=1, T=300, H=2, HV=4, K=128, V=128, cu_seqlens=[0, 0, 100, 100, 300]),
      torch.bfloat16),
+    ("tc_varlen_fused", dict(B=1, T=300, H=2, HV=2, K=128, V=128, cu_seqlens=[0, 0, 100, 100, 300]),
+     torch.bfloat16),  # HV = H: the norm's backward inside the gradient kernel
     ("fp32_gva_odd", dict(B=1, T=129, H=1, HV=3, K=32, V=48), torch.float32),
     ("bf16_small_dims", dict(B=2, T=70, H=2, HV=2, K=64, V=64), torch.bfloat16),
     ("fp32_k128", dict(B=1, T=90, H=1, HV=2, K=128, V=64), torch.float32),
