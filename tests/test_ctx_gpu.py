@@ -231,3 +231,21 @@ def test_context_pair_cuda_graph_replay_with_mutated_offsets():
         _same(f"hT {cu}", hT, rhT)
         for key, x in zip(GRADS, grads):
             _same(f"{key} {cu}", x, rg[key])
+
+
+def test_context_from_a_forward_without_output_serves_the_backward():
+    """kda_chunk_fwd_ctx with o NULL (the chain saves its tiles but writes no
+    output) leaves a complete context: the backward on it equals the recompute
+    pair's, bit for bit."""
+    from gated_delta_rule_42_gb300.ops import chunk_kda_bwd, chunk_kda_bwd_ctx, chunk_kda_fwd_ctx
+    inp = inputs.make_inputs(B=1, T=260, H=2, HV=4, K=128, V=128, dtype=torch.bfloat16, seed=61,
+                             cu_seqlens=[0, 70, 70, 260], name="ctx_no_output")
+    d = inp.to("cuda")
+    args = (d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
+    none, hT, kctx = chunk_kda_fwd_ctx(*args, True, need_output=False)
+    assert none is None and kctx.numel() > 0
+    g_ctx = chunk_kda_bwd_ctx(*args, kctx, d.do, d.dhT)
+    g_ref = chunk_kda_bwd(*args, d.do, d.dhT)
+    torch.cuda.synchronize()
+    for key, a, b in zip(GRADS, g_ctx, g_ref):
+        _same(key, a, b)
