@@ -312,6 +312,22 @@ def cp_step_fn(runner, R):
     return step
 
 
+def segmented_step_fn(runner, S, qk_l2norm=False):
+    """One fwd+bwd step with every sequence split into S segments that run at
+    once on this GPU (gated_delta_rule_42_gb300.segments)."""
+    from gated_delta_rule_42_gb300.segments import chunk_kda_bwd_segmented, chunk_kda_fwd_segmented
+    d = runner.d
+    assert d.cu_seqlens is None, "segments: dense workloads only"
+
+    def step():
+        _, _, ctx = chunk_kda_fwd_segmented(d.q, d.k, d.v, d.g, d.beta, d.h0, S, runner.hT is not None,
+                                            use_qk_l2norm=qk_l2norm)
+        chunk_kda_bwd_segmented(d.q, d.k, d.v, d.g, d.beta, ctx, d.do, d.dhT, need_dh0=d.h0 is not None,
+                                use_qk_l2norm=qk_l2norm)
+
+    return step
+
+
 def timed(fn, steps, stream):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -490,6 +506,9 @@ def main():
     ap.add_argument("--recompute", action="store_true",
                     help="time the recompute pair (kda_chunk_fwd + kda_chunk_bwd) instead of the forward-context "
                          "pair: the backward re-runs the record kernel and the states pass")
+    ap.add_argument("--segments", type=int, default=0,
+                    help="split every sequence into this many segments that run at once on this GPU, with the "
+                         "state relay (for few long sequences); the dense workloads only")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip timing the other backward mode (profiling aid: only this mode's kernels launch)")
     ap.add_argument("--seq-len", type=int, default=None,
@@ -531,6 +550,9 @@ def main():
     if args.cp_ranks > 1:  # context parallelism, the ranks serialized on this GPU
         runner.step = cp_step_fn(runner, args.cp_ranks)
         args.no_e2e = True
+    if args.segments > 1:  # every sequence in segments that run at once, with the state relay
+        runner.step = segmented_step_fn(runner, args.segments, args.qk_l2norm)
+        args.no_e2e = True
     if args.only != "step":  # profiling aid: time one half of the step only
         runner.step = runner.fwd if args.only == "fwd" else runner.bwd
         args.no_e2e = args.no_cpu_baseline = True
@@ -554,7 +576,7 @@ def main():
 
     split = kernel_split(runner, max(3, min(args.steps, 10)))
     other = None  # the other backward mode, timed the same way, for comparison
-    if args.only == "step" and args.cp_ranks <= 1 and not args.no_compare:
+    if args.only == "step" and args.cp_ranks <= 1 and args.segments <= 1 and not args.no_compare:
         alt = Runner(cfg, dev, qk_l2norm=args.qk_l2norm, keep_context=args.recompute)
         for _ in range(warmup):
             alt.step()
@@ -609,7 +631,9 @@ def main():
                    "backward": "recompute" if args.recompute else "forward context kept",
                    "forward_context_bytes": int(runner.ctx_bytes),
                    **({"cp_ranks": args.cp_ranks, "cp": "sequences split into cp_ranks segments, state relay, "
-                       "ranks serialized on one GPU"} if args.cp_ranks > 1 else {})},
+                       "ranks serialized on one GPU"} if args.cp_ranks > 1 else {}),
+                   **({"segments": args.segments, "segmented": "every sequence split into segments that run at "
+                       "once, state relay"} if args.segments > 1 else {})},
         "roofline": roof,
         "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
                           "algorithmic_bytes": ab["total"], "algorithmic_flops": af,

@@ -267,14 +267,44 @@ class ChunkKDAFunction(torch.autograd.Function):
         return dq, dk, dv, dg, db, dh0, None, None, None, None
 
 
+class SegmentedChunkKDAFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm, segments):
+        from .segments import chunk_kda_fwd_segmented
+        o, hT, ctx.seg = chunk_kda_fwd_segmented(q, k, v, g, beta, initial_state, segments, output_final_state,
+                                                 use_qk_l2norm=use_qk_l2norm)
+        ctx.save_for_backward(q, k, v, g, beta)
+        ctx.has_h0 = initial_state is not None
+        ctx.l2 = use_qk_l2norm
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        from .segments import chunk_kda_bwd_segmented
+        q, k, v, g, beta = ctx.saved_tensors
+        dht = None if dht is None else dht.contiguous()
+        dq, dk, dv, dg, db, dh0 = chunk_kda_bwd_segmented(q, k, v, g, beta, ctx.seg, do.contiguous(), dht,
+                                                          need_dh0=ctx.has_h0, use_qk_l2norm=ctx.l2)
+        ctx.seg = None
+        return dq, dk, dv, dg, db, dh0, None, None, None
+
+
 def chunk_kda(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, output_final_state=False,
-              use_qk_l2norm=False, keep_context=True):
+              use_qk_l2norm=False, keep_context=True, segments=1):
     """Chunked KDA forward (with autograd).  Returns (o, final_state or None).
     use_qk_l2norm: L2-normalise every q and k row inside the op (its backward
     included).  keep_context: the forward keeps its per-chunk intermediates
     (about 2 KB per token and value head on the bf16 K = V = 128 path) so that
     the backward does not recompute them; False trades that memory for the
-    recompute.  The gradients are the same either way."""
+    recompute.  The gradients are the same either way.  segments > 1 (dense
+    batches only): every sequence runs as that many segments at once, joined by
+    the state relay -- for a few long sequences, whose chunk chains alone would
+    leave most SMs idle (see :mod:`.segments`)."""
+    if segments > 1:
+        if cu_seqlens is not None:
+            raise ValueError("segments > 1 splits dense batches only")
+        return SegmentedChunkKDAFunction.apply(q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
+                                               segments)
     return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
                                   use_qk_l2norm, keep_context)
 

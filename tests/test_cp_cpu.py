@@ -8,6 +8,7 @@ import os
 import socket
 
 import numpy as np
+import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -88,3 +89,12 @@ def test_state_relay_two_gloo_ranks_match_the_unsplit_oracle():
         np.testing.assert_allclose(np.concatenate([res[0][key], res[1][key]], axis=1), gr[key],
                                    rtol=1e-10, atol=1e-10, err_msg=key)
     np.testing.assert_allclose(res[0]["dh0"], gr["dh0"], rtol=1e-10, atol=1e-10)
+
+
+def test_segment_offsets():
+    from gated_delta_rule_42_gb300.segments import segment_offsets
+    cu = segment_offsets(2, 1024, 4, "cpu")
+    assert cu.tolist() == [0, 256, 512, 768, 1024, 1280, 1536, 1792, 2048]
+    for T, S in ((1000, 4), (1024, 3), (1024, 32)):  # not whole 64-token chunks per segment
+        with pytest.raises(ValueError):
+            segment_offsets(1, T, S, "cpu")
