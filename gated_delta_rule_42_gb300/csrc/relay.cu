@@ -11,15 +11,16 @@
 // M_r^T on the state gradients.
 //
 // out[i] = op(M[i]) h[i] + c[i] for every (sequence, value head) i, fp32,
-// op = identity or transpose; one CTA per (i, 32-row block of out), each
-// thread one output column, K streamed through shared memory.  Each output is
+// op = identity or transpose; one CTA per (i, 8-row block of out) -- enough
+// CTAs to spread the few states of a relay step over the SMs -- each thread one
+// output column, K streamed through shared memory.  Each output is
 // a fixed-order sum, so the result does not depend on the launch.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kRows = 32;  // output rows per CTA
+constexpr int kRows = 8;  // output rows per CTA
 
 __global__ void __launch_bounds__(128)
 state_compose_kernel(const float *__restrict__ M, const float *__restrict__ h, const float *__restrict__ c,
@@ -38,6 +39,7 @@ state_compose_kernel(const float *__restrict__ M, const float *__restrict__ h, c
     float acc[kRows];
 #pragma unroll
     for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
+#pragma unroll 8
     for (int b = 0; b < K; ++b) {
       const float hb = hi[(int64_t)b * V + x];
 #pragma unroll
