@@ -224,7 +224,8 @@ kda_status chunk_fwd(const kda_inputs *in, void *o, float *hT, void *ctx, size_t
   cudaError_t e = gate_per_channel(P, W, &Pg, (cudaStream_t)stream);
   if (e == cudaSuccess) {
     if (use_tc(P)) {
-      const int mode = (o != nullptr ? kFwdOutput : 0) | (with_ctx ? kFwdSave : 0);
+      // with o NULL a context call computes the final state alone: the context keeps the records only
+      const int mode = o != nullptr ? (kFwdOutput | (with_ctx ? kFwdSave : 0)) : 0;
       e = tc_forward(Pg, W, o, hT, mode, with_ctx && reuse, W.flags + 2, (cudaStream_t)stream);
     } else {
       Problem Pn = Pg;

@@ -146,7 +146,9 @@ def chunk_kda_fwd_ctx(q, k, v, g, beta, initial_state=None, cu_seqlens=None, out
     """Forward that also returns the forward context (a uint8 device tensor,
     empty on the general path) for :func:`chunk_kda_bwd_ctx`: the per-chunk
     records, chunk-start states and X^T, D^T tiles the backward would otherwise
-    recompute.  Returns (o or None, final_state or None, context)."""
+    recompute.  need_output=False computes the final state alone and keeps the
+    records only (a backward then needs :func:`chunk_kda_fwd_reuse` with output
+    first).  Returns (o or None, final_state or None, context)."""
     lib = _lib.load()
     s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
     o = _output(v, need_output, output_final_state)
@@ -167,8 +169,9 @@ def chunk_kda_fwd_reuse(q, k, v, g, beta, initial_state, cu_seqlens, kctx, outpu
     """:func:`chunk_kda_fwd_ctx` for inputs that share q, k, g, beta and
     cu_seqlens with the ones ``kctx`` was last filled from (v and the initial
     state may differ): the per-chunk records are read from the context, not
-    recomputed, and the context is rewritten to serve these inputs' backward.
-    Returns (o or None, final_state or None)."""
+    recomputed.  With output, the context is rewritten to serve these inputs'
+    backward; need_output=False computes the final state alone and leaves the
+    context as it was.  Returns (o or None, final_state or None)."""
     lib = _lib.load()
     s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
     o = _output(v, need_output, output_final_state)

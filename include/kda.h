@@ -150,7 +150,10 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
  * kda_chunk_fwd + kda_chunk_bwd, for kda_chunk_ctx_size() bytes of device
  * memory per layer -- per (64-token chunk, value head): the 66,048-byte record
  * (decayed key and query tiles, the inverse A, Aqk, 2^G_last), the bf16
- * chunk-start state (32 KB) and two 16 KB bf16 tiles (X^T, D^T).
+ * chunk-start state (32 KB) and two 16 KB bf16 tiles (X^T, D^T).  A _ctx or
+ * _reuse forward with o NULL computes the final states alone: it leaves the
+ * context holding the records only, and a backward needs a later forward on
+ * the context with o.
  * The context must come from kda_chunk_fwd_ctx on the same inputs (q, k, v,
  * g, beta, h0, cu_seqlens, flags), unchanged since; that is a precondition,
  * not checked.  The backward only reads it, so it serves any number of
@@ -175,8 +178,9 @@ kda_status kda_chunk_fwd_ctx(const kda_inputs *in, void *o, float *hT, void *ctx
  * sizes with the ones ctx was last filled from (v and h0 may differ): the
  * per-chunk records, which depend on those alone, are read from ctx instead of
  * recomputed -- the several passes of a context-parallel rank over one segment.
- * The chunk-start states and tiles in ctx are rewritten for these inputs, so
- * the context then serves their backward.  On the general path: kda_chunk_fwd. */
+ * With o not NULL the chunk-start states and tiles in ctx are rewritten for
+ * these inputs, so the context then serves their backward.  On the general
+ * path: kda_chunk_fwd. */
 kda_status kda_chunk_fwd_reuse(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes,
                                void *workspace, size_t workspace_bytes, void *stream);
 

@@ -233,17 +233,24 @@ def test_context_pair_cuda_graph_replay_with_mutated_offsets():
             _same(f"{key} {cu}", x, rg[key])
 
 
-def test_context_from_a_forward_without_output_serves_the_backward():
-    """kda_chunk_fwd_ctx with o NULL (the chain saves its tiles but writes no
-    output) leaves a complete context: the backward on it equals the recompute
-    pair's, bit for bit."""
-    from gated_delta_rule_42_gb300.ops import chunk_kda_bwd, chunk_kda_bwd_ctx, chunk_kda_fwd_ctx
+def test_context_filled_without_output_then_reused_with_output_serves_the_backward():
+    """kda_chunk_fwd_ctx with o NULL computes the final state alone and keeps
+    the records; a reuse forward with o on the same inputs completes the
+    context, and the backward on it equals the recompute pair's, bit for bit."""
+    from gated_delta_rule_42_gb300.ops import (chunk_kda_bwd, chunk_kda_bwd_ctx, chunk_kda_fwd, chunk_kda_fwd_ctx,
+                                               chunk_kda_fwd_reuse)
     inp = inputs.make_inputs(B=1, T=260, H=2, HV=4, K=128, V=128, dtype=torch.bfloat16, seed=61,
                              cu_seqlens=[0, 70, 70, 260], name="ctx_no_output")
     d = inp.to("cuda")
     args = (d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
     none, hT, kctx = chunk_kda_fwd_ctx(*args, True, need_output=False)
     assert none is None and kctx.numel() > 0
+    o_ref, hT_ref = chunk_kda_fwd(*args, True)
+    o, hT2 = chunk_kda_fwd_reuse(*args, kctx, True)
+    torch.cuda.synchronize()
+    _same("hT (final state alone)", hT, hT_ref)
+    _same("o", o, o_ref)
+    _same("hT", hT2, hT_ref)
     g_ctx = chunk_kda_bwd_ctx(*args, kctx, d.do, d.dhT)
     g_ref = chunk_kda_bwd(*args, d.do, d.dhT)
     torch.cuda.synchronize()
