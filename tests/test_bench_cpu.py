@@ -1,0 +1,53 @@
+"""The benchmark's roofline arithmetic, pinned on the host: the algorithmic
+bytes and flops of the dense training layer (per token and value head), the
+interface bytes per token that each tensor-core kernel's roofline divides by,
+and the rule that the measured DRAM traffic is reported only while the
+dominant kernel's sources match its capture."""
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from gated_delta_rule_42_gb300 import inputs  # noqa: E402
+
+
+def _layer(**kw):
+    # the dense training layer's head shape; per-token figures do not depend on T
+    return inputs.make_inputs(B=1, T=64, H=32, HV=32, K=128, V=128, dtype=torch.bfloat16, h0=False,
+                              final_state=False, seed=1, **kw)
+
+
+def test_algorithmic_cost_per_token_head():
+    cfg = _layer()
+    # fwd: q, k, v, g, beta in, o out; bwd: the same plus dO in, dq, dk, dv, dg, dbeta out
+    e, K, V = 2, 128, 128
+    fwd = 2 * K * e + V * e + 4 * K + 4 + V * e
+    bwd = fwd + 2 * K * e + V * e + 4 * K + 4
+    assert bench.algorithmic_bytes(cfg)["per_token_head"] == fwd + bwd == 4364
+    # 18 d^2 + 15 C d + 2 C^2 at d = 128, C = 64
+    assert bench.algorithmic_flops(cfg) / (cfg.valid_tokens * cfg.HV) == 18 * 128 ** 2 + 15 * 64 * 128 + 2 * 64 ** 2
+    # a scalar gate moves one fp32 per (token, value head) instead of K of them, three times
+    assert bench.algorithmic_bytes(_layer(scalar_gate=True))["per_token_head"] == 4364 - 3 * (4 * K - 4)
+
+
+def test_interface_bytes_per_token_of_the_tensor_core_kernels():
+    cfg = _layer()
+    want = {"kda_prep_tc": 65920, "kda_fwd_tc": 49408, "kda_fwd_tc_states": 61696, "kda_fwd_tc_save": 82176,
+            "kda_bwd_scan_tc": 73984, "kda_bwd_intra_tc": 160000}
+    for name, b in want.items():
+        assert bench.kernel_bytes_per_token(name, cfg) == b, name
+    assert bench.kernel_bytes_per_token("no_such_kernel", cfg) is None
+
+
+def test_traffic_is_reported_only_for_the_captured_sources():
+    t = bench.NCU_TRAFFIC["kda_bwd_intra_tc"]
+    current = bench.sources_sha256(t["sources"]) == t["sha256"]
+    got = bench.measured_traffic("kda_bwd_intra_tc", 8192)
+    assert (got is not None) == current
+    if current:  # the capture's own size gives back its bytes
+        assert abs(got - t["bytes_per_token"] * 8192) <= 1
+    assert bench.measured_traffic("kda_prep_tc", 8192) is None  # no capture recorded for it

@@ -72,7 +72,7 @@ def _rank(rank, world, port, out):
 
 def test_state_relay_two_gloo_ranks_match_the_unsplit_oracle():
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:  # no fork of a multi-threaded parent
         out = mgr.dict()
         mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
         res = {r: dict(out[r]) for r in (0, 1)}

@@ -38,7 +38,7 @@ def test_job_throughput_single_rank():
 
 def test_job_throughput_two_gloo_ranks_take_the_slowest_rank():
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:  # no fork of a multi-threaded parent
         out = mgr.dict()
         mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
