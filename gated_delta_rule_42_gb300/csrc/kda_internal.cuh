@@ -48,7 +48,8 @@ constexpr float kL2NormEps = 1e-6f;  // epsilon of the q/k L2-norm prologue
 struct Workspace {
   int4 *seq;     // [N]
   int4 *chunk;   // [NC]
-  int *flags;    // [0] = number of chunks, [1] = malformed-offsets flag, [2] = a bounded wait gave up
+  int *flags;    // [0] = number of chunks, [1] = malformed-offsets flag, [2] = a bounded wait gave up,
+                 // [3] = (chunk, value head) slots that took the exact path for a wide decay span
   float *G;      // [slot][64][K]   chunk-local inclusive gate cumsum
   float *Aqk;    // [slot][64][64]  lower (incl. diagonal) decayed q~ k^T
   float *A;      // [slot][64][64]  (I + L)^-1

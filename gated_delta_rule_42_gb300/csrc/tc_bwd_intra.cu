@@ -17,12 +17,18 @@
 // finishes
 //   dL   = -tril_{-1}(A^T dA A^T)                 gradient through A = (I + L)^-1
 //   the chain through L = beta*KK and Aqk to the keys, queries and gate,
-// and assembles dq, dk, dg and dbeta.  With 2^(G_r - G_i) split at 16-token
-// block starts exactly as in the forward (rows: e1 = 2^(G_r - G_ref) <= 1,
-// columns: e2 = 2^(G_ref - G_i), between blocks D_RI <= 1 on the operand):
+// and assembles dq, dk, dg and dbeta.  With 2^(G_r - G_i) split per channel
+// at 16-token block references exactly as in the record kernel (rows:
+// e1 = 2^(G_r - Gr(R)), columns: e2 = 2^(Gc(I) - G_i), between blocks the
+// factor D_RI = 2^(Gr(R) - Gc(I)) <= 1 on the block product; Gr = Gc = the
+// middle of the block's range, or for a channel whose span exceeds kSpanMax
+// the block's first and last row):
 //   row side    xr = sum_i dL_ri  Kc_i D_RI,  yr = sum_i dAqk_ri Kc_i D_RI
 //   column side xi = sum_r X_ri   Kr_r D_RI,  yi = sum_r dAqk_ri Qr_r D_RI   (X = beta dL)
-// on 16x16 warp MMAs, then per element (Gamma = 2^G, khat = 2^(G_last - G)):
+// on 16x16 warp MMAs.  A slot with such a wide channel forms its diagonal
+// blocks from the raw rows with pairwise exponents instead and carries true
+// values (e1 = e2 = 1) into the assembly: exact for any gate.  Then per element
+// (Gamma = 2^G, khat = 2^(G_last - G)):
 //   dq~ = dQg Gamma + e1 yr
 //   dk  = dKhat khat + beta Gamma dBk + beta e1 xr + e2 (xi + yi)
 //   dG  = ln2 [dQg q~ Gamma - dKhat k khat + beta dBk k Gamma + beta k e1 xr + q~ e1 yr - k e2 (xi + yi)]
@@ -63,12 +69,17 @@ constexpr uint32_t C_T = 147456;      // T = A^T dA [64 r][64 m] hi | lo    (bef
 constexpr uint32_t C_KRAW = C_XB, C_QRAW = C_T;
 constexpr uint32_t C_G = 163840;      // G fp32 [64][132]
 constexpr uint32_t C_A = 197632;      // A   [64 r][64 i] bf16
-constexpr uint32_t C_VEC = 205824;    // vectors (20 x 128 fp32)
-constexpr uint32_t C_BETA = 216064;   // beta [64]
-constexpr uint32_t C_RB = 216320;     // dbeta partials [4][64]
-constexpr uint32_t C_RED = 217344;    // sum_v dX v [64], d(2^G_last) [128]
-constexpr uint32_t C_MISC = 218112;   // mbarriers (loads S, P1, P2, raw k/q, products), tmem slot
-constexpr uint32_t C_SMEM = 218176 + 1024;
+constexpr uint32_t C_VEC = 205824;    // vectors (24 x 128 fp32)
+constexpr uint32_t C_BETA = 218112;   // beta [64]
+constexpr uint32_t C_RB = 218368;     // dbeta partials [4][64] (before them: inverse row norms of the L2-norm prologue)
+constexpr uint32_t C_RED = 219392;    // sum_v dX v [64], d(2^G_last) [128]
+constexpr uint32_t C_MISC = 220160;   // mbarriers (loads S, P1, P2, raw k/q, products), tmem slot
+constexpr uint32_t C_SMEM = 220224 + 1024;
+static_assert(C_SMEM <= 232448, "one CTA per SM (227 KB)");
+// Widest per-channel decay span (log2) of a 16-token block that the middle
+// references carry (e1, e2 within 2^(+-kSpanMax / 2)); a slot with a wider
+// channel takes the exact path for its diagonal blocks.
+constexpr float kSpanMax = 192.f;
 constexpr uint32_t LO128 = 16384, LO64 = 8192;
 // Tensor memory: the per-chunk products that the assembly reads element-wise are
 // M = 64 accumulators, whose 16-row block R sits in lanes 0..15 of lane quarter R:
@@ -252,6 +263,58 @@ __device__ __forceinline__ void issue_gate_beta(uint32_t sbase, unsigned char *s
   cp_commit();
 }
 
+// Element (a, b) of a hi/lo tile pair (64 columns, the lo twin LO64 bytes on).
+__device__ __forceinline__ float hilo(const unsigned char *tile, int a, int b) {
+  const uint32_t off = sw_off(a, b, kC);
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off)) +
+         __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + LO64 + off));
+}
+// Channels (c, c + 1) of row t of the chunk: k, or q~ = q / sqrt(K) (is_q), as the
+// chain sees them (L2-normalised with the prologue, by the inverse norms in rb);
+// zero past the chunk's length is the caller's guard.  For the exact path only.
+__device__ __forceinline__ float2 raw_row(const Problem &P, const IntraArgs &a, int t0, int h, int t, int c,
+                                          const float *rb, bool is_q) {
+  (void)a;
+  const __nv_bfloat16 *base = (const __nv_bfloat16 *)(is_q ? P.q : P.k);
+  const float2 x = unpack_bf16(__ldg(reinterpret_cast<const unsigned int *>(base + ((size_t)(t0 + t) * P.H + h) * kD + c)));
+  float s = is_q ? 0.08838834764831845f : 1.f;
+  if (P.l2norm) s *= rb[(is_q ? kC : 0) + t];
+  return make_float2(x.x * s, x.y * s);
+}
+
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
+// Per-element operands of the gradient assembly.  Block-factor path: the decay
+// tiles Kr = k e1, Qr = q~ e1, Kc = k e2, the vectors eref = 2^Gr, lam =
+// 2^(G_last - Gc), and e1 = 2^(G - Gr), e2 = 2^(Gc - G), einv = 1 / e1 (kInv),
+// with gm = Gr, ge = Gc.  Exact path: k, q~ themselves with e1 = e2 = einv = 1,
+// eref = 2^G and lam = 2^(G_last - G), so that every product below means the
+// same in both.
+struct Opnd {
+  float Kr, Qr, Kc, e1, e2, einv, eref, lam;
+};
+template <bool kWide, bool kInv>
+__device__ __forceinline__ Opnd opnd(float Kr, float Qr, float Kc, float g, float gm, float ge, float eref, float lam,
+                                     float kraw, float qraw) {
+  Opnd o;
+  if (kWide) {
+    o.Kr = kraw; o.Qr = qraw; o.Kc = kraw;
+    o.e1 = 1.f; o.e2 = 1.f; o.einv = 1.f;
+    o.eref = ex2(g);
+    o.lam = lam * ex2(ge - g);
+  } else {
+    o.Kr = Kr; o.Qr = Qr; o.Kc = Kc;
+    o.e1 = ex2(g - gm);
+    o.e2 = ex2(ge - g);
+    o.einv = kInv ? ex2(gm - g) : 0.f;
+    o.eref = eref;
+    o.lam = lam;
+  }
+  return o;
+}
+
 // kScalarGate: g and dg are [tokens][HV] (one decay per token, repeated over the channels here).
 // kL2: the q/k L2-norm prologue with HV = H, its backward fused: dx = r (dy - y (y . dy)) per
 // (token, head) row, from the inverse norms r of the decay-tile pass and row dots y . dy that a
@@ -409,6 +472,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       }
     }
     // ---- G, block references, decay tiles Kr, Qr, Kc (hi/lo) ----
+    int wide_c = 0;
     if (tid < kD) {
       const int c = tid;
       float s = 0.f;
@@ -425,33 +489,41 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       const float gl = s;
       vec[V_GL * kD + c] = gl;
       vec[V_GAML * kD + c] = exp2f(gl);
-      float gref[4];
+      float rref[4], cref[4];
 #pragma unroll
-      for (int R = 0; R < 4; ++R) {
-        gref[R] = (16 * R < len) ? col[16 * R] : gl;
-        vec[(V_GREF + R) * kD + c] = gref[R];
-        vec[(V_EREF + R) * kD + c] = exp2f(gref[R]);
-        vec[(V_LAM + R) * kD + c] = exp2f(gl - gref[R]);
+      for (int R = 0; R < 4; ++R) {  // rows past len hold G_last, so the references need no clamping
+        const float gref = col[16 * R], gend = col[16 * R + 15];
+        const bool wide = !(gref - gend <= kSpanMax);  // (NaN-safe)
+        wide_c |= wide;
+        const float gmid = 0.5f * (gref + gend);
+        rref[R] = wide ? gref : gmid;
+        cref[R] = wide ? gend : gmid;
+        vec[(V_RREF + R) * kD + c] = rref[R];
+        vec[(V_EREF + R) * kD + c] = exp2f(rref[R]);
+        vec[(V_LAM + R) * kD + c] = exp2f(gl - cref[R]);
+        vec[(V_CREF + R) * kD + c] = cref[R];
       }
       int p = 0;
 #pragma unroll
       for (int R = 1; R < 4; ++R)
 #pragma unroll
-        for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
+        for (int I = 0; I < R; ++I) vec[(V_D + p++) * kD + c] = exp2f(rref[R] - cref[I]);
     }
     ok &= bar_wait(bar_kq, par, args.err);  // raw k, q
     if (len < kC) {  // rows past the sequence end hold other tokens: clear them
       zero_tail<kCT>(sm + C_KRAW, len);
       zero_tail<kCT>(sm + C_QRAW, len);
     }
-    __syncthreads();
+    // some block's decay span is wider than the block factors carry: the exact path
+    const bool wide = __syncthreads_or(wide_c) != 0;
+    if (wide && tid == 0) atomicAdd(W.flags + 3, 1);  // status word 3
     KDA_PT(1);
     {
       const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 3;  // two rows per thread
-      float gref[8];
+      float rref[8];
 #pragma unroll
       for (int e = 0; e < 8; e += 4)
-        *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (V_GREF + R) * kD + c0 + e);
+        *reinterpret_cast<float4 *>(rref + e) = *reinterpret_cast<const float4 *>(vec + (V_RREF + R) * kD + c0 + e);
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const int r = rg * 2 + rr;
@@ -472,7 +544,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
             sq += __shfl_xor_sync(0xffffffffu, sq, o);
           }
           const float rk = 1.0f / sqrtf(sk + kL2NormEps), rq = 1.0f / sqrtf(sq + kL2NormEps);
-          if (kL2 && jj == 0) {  // the row's inverse norms, for the fused backward (rb is free until the dbeta partials)
+          if (jj == 0) {  // the row's inverse norms, for the fused backward and the exact path (rb is free until the dbeta partials)
             rb[r] = rk;
             rb[kC + r] = rq;
           }
@@ -482,11 +554,13 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
             qv[e] *= rq;
           }
         }
+        *reinterpret_cast<float4 *>(e2) = *reinterpret_cast<const float4 *>(vec + (V_CREF + R) * kD + c0);  // Gc(R)
+        *reinterpret_cast<float4 *>(e2 + 4) = *reinterpret_cast<const float4 *>(vec + (V_CREF + R) * kD + c0 + 4);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float g = G[r * kGLD + c0 + e];
-          e1[e] = ex2(g - gref[e]);
-          e2[e] = ex2(gref[e] - g);
+          e1[e] = ex2(g - rref[e]);  // within 2^(+-kSpanMax/2), or <= 1 on a wide channel
+          e2[e] = ex2(e2[e] - g);    // likewise
         }
         uint4 hi, lo;
 #pragma unroll
@@ -566,9 +640,10 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     // factor D_RI in fp32, and added to the accumulators.
     // (row block = the warp's TMEM lane quarter, so that the assembly reads its products from TMEM)
     const int Bk = warp & 3, ch0 = 32 * (warp >> 2);
+    const int i8 = lane >> 2, l4 = lane & 3;  // fragment row (and row + 8) and column pair of this lane
     float xr[4][4] = {}, yr[4][4] = {}, xyi[4][4] = {};  // xyi = xi + yi (only their sum is used)
-    for (int I = 0; I <= Bk; ++I) {  // row side: R = Bk, I = 0..Bk
-      const float *Dv = (I < Bk) ? vec + (V_D + Bk * (Bk - 1) / 2 + I) * kD : nullptr;
+    for (int I = 0; I <= (wide ? Bk - 1 : Bk); ++I) {  // row side: R = Bk, I = 0..Bk (the exact path: I < Bk)
+      const float *Dv = (I < Bk) ? vec + (V_D + Bk * (Bk - 1) / 2 + I) * kD : nullptr;  // no factor inside a block
       uint32_t aLh[4], aLl[4], aQh[4], aQl[4];
       lda(sbase + C_DAB, kC, 16 * Bk, 16 * I, aLh);  // dL[r][i]
       lda(sbase + C_DAB + LO64, kC, 16 * Bk, 16 * I, aLl);
@@ -593,7 +668,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
         }
       }
     }
-    for (int R = Bk; R < 4; ++R) {  // column side: I = Bk, R = Bk..3
+    for (int R = wide ? Bk + 1 : Bk; R < 4; ++R) {  // column side: I = Bk, R = Bk..3 (the exact path: R > Bk)
       const float *Dv = (R > Bk) ? vec + (V_D + R * (R - 1) / 2 + Bk) * kD : nullptr;
       uint32_t aXh[4], aXl[4], aQh[4], aQl[4];
       lda_t(sbase + C_XB, kC, 16 * Bk, 16 * R, aXh);  // element (i, r) = X[r][i]
@@ -616,6 +691,55 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
           const float d0 = Dv ? Dv[c] : 1.f, d1 = Dv ? Dv[c + 1] : 1.f;
           float(&X)[4] = xyi[2 * nb + t];
           X[0] = fmaf(d0, tx[0], X[0]); X[1] = fmaf(d1, tx[1], X[1]); X[2] = fmaf(d0, tx[2], X[2]); X[3] = fmaf(d1, tx[3], X[3]);
+        }
+      }
+    }
+    if (wide) {  // the exact path: the sums to true values, plus the diagonal block from pairwise exponents
+      const int r0 = 16 * Bk;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int c = ch0 + 8 * nt + 2 * l4;
+        const float2 gm = *reinterpret_cast<const float2 *>(vec + (V_RREF + Bk) * kD + c);
+        const float2 ge = *reinterpret_cast<const float2 *>(vec + (V_CREF + Bk) * kD + c);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = r0 + i8 + 8 * hh;
+          const float2 gr = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
+          // the row sums carry e1, the column sums e2: multiply them in
+          float x0 = xr[nt][2 * hh] * ex2(gr.x - gm.x), x1 = xr[nt][2 * hh + 1] * ex2(gr.y - gm.y);
+          float y0 = yr[nt][2 * hh] * ex2(gr.x - gm.x), y1 = yr[nt][2 * hh + 1] * ex2(gr.y - gm.y);
+          float z0 = xyi[nt][2 * hh] * ex2(ge.x - gr.x), z1 = xyi[nt][2 * hh + 1] * ex2(ge.y - gr.y);
+#pragma unroll 1
+          for (int ts = r0; ts < r0 + 16 && ts < len; ++ts) {  // the diagonal block: every exponent <= 0
+            const float2 gs = *reinterpret_cast<const float2 *>(G + ts * kGLD + c);
+            const float2 kk = raw_row(P, args, t0, h, ts, c, rb, false);
+            if (ts <= r) {  // row side, i = ts
+              const float f0 = ex2(gr.x - gs.x), f1 = ex2(gr.y - gs.y);
+              const float aq = hilo(sm + C_DQK, ts, r);  // dAqk[r][ts]
+              y0 = fmaf(aq * kk.x, f0, y0);
+              y1 = fmaf(aq * kk.y, f1, y1);
+              if (ts < r) {
+                const float al = hilo(sm + C_DAB, r, ts);  // dL[r][ts]
+                x0 = fmaf(al * kk.x, f0, x0);
+                x1 = fmaf(al * kk.y, f1, x1);
+              }
+            }
+            if (ts >= r) {  // column side, r' = ts
+              const float f0 = ex2(gs.x - gr.x), f1 = ex2(gs.y - gr.y);
+              const float2 qq = raw_row(P, args, t0, h, ts, c, rb, true);
+              const float aq = hilo(sm + C_DQK, r, ts);  // dAqk[ts][r]
+              z0 = fmaf(aq * qq.x, f0, z0);
+              z1 = fmaf(aq * qq.y, f1, z1);
+              if (ts > r) {
+                const float ax = hilo(sm + C_XB, ts, r);  // X[ts][r]
+                z0 = fmaf(ax * kk.x, f0, z0);
+                z1 = fmaf(ax * kk.y, f1, z1);
+              }
+            }
+          }
+          xr[nt][2 * hh] = x0; xr[nt][2 * hh + 1] = x1;
+          yr[nt][2 * hh] = y0; yr[nt][2 * hh + 1] = y1;
+          xyi[nt][2 * hh] = z0; xyi[nt][2 * hh + 1] = z1;
         }
       }
     }
@@ -642,164 +766,175 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     // segment totals of the dg scan, rows of 128 fp32 (k = 0..14): every vector row
     // but 2^G_last and the four holding totC
     auto tot_row = [&](int k) -> float * {
-      return vec + (k == 0 ? V_GL : k < 9 ? V_GREF + (k - 1) : k < 11 ? V_D + 4 + (k - 9) : V_LAM + (k - 11)) * kD;
+      return vec + (k == 0 ? V_GL : k < 9 ? V_RREF + (k - 1) : k < 11 ? V_D + 4 + (k - 9) : V_LAM + (k - 11)) * kD;
     };
     const float *dglv = red + 64;
-    const int i8 = lane >> 2, l4 = lane & 3;
     float bpart[2] = {0.f, 0.f};
     float dotq[2] = {0.f, 0.f}, dotk[2] = {0.f, 0.f};  // kL2: y . dy of rows i8, i8 + 8 of block Bk
-    if (kL2) {
-      // per-quarter partial dots [4 column quarters][64 rows]: q in the rows of the last two
-      // block factors, k in the unused row and the upper half of the dbeta partials
-      float *pdq = vec + (V_D + 4) * kD;
-      float *pdk = (warp >> 2) < 2 ? vec + V_GL * kD + (warp >> 2) * kC : rb + 2 * kC + ((warp >> 2) - 2) * kC;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int c = ch0 + 8 * nt + 2 * l4;
-        float px[4], po[4], pk[4];
-        {
-          const uint32_t tb = tmem + ((uint32_t)(32 * Bk) << 16) + (uint32_t)(ch0 + 8 * nt);
-          tmem_ld_frag3(tb, tb + 128u, tb + 256u, px, po, pk);
-        }
-        const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
-        const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
-        const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * Bk + i8 + 8 * hh;
-          const float br = beta[r];
-          const uint32_t to = sw_off(r, c, kC);
-          const float2 krh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + to));
-          const float2 krl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + LO128 + to));
-          const float2 qrh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + to));
-          const float2 qrl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + LO128 + to));
-          const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float Kr = u ? krh.y + krl.y : krh.x + krl.x, Qr = u ? qrh.y + qrl.y : qrh.x + qrl.x;
-            const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
-            const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
-            const float e1 = ex2(gg_ - gref), e2 = ex2(gref - gg_);
-            const float dq2 = po[2 * hh + u] * (e1 * eref) + e1 * yr[nt][2 * hh + u];
-            const float dk2 = pk[2 * hh + u] * (e2 * lam) - br * (e1 * eref) * px[2 * hh + u] +
-                              br * e1 * xr[nt][2 * hh + u] + e2 * xyi[nt][2 * hh + u];
-            dotq[hh] = fmaf(Qr * e2, dq2, dotq[hh]);  // y_q = Qr e2 / qscale and dy_q = qscale dq2
-            dotk[hh] = fmaf(Kr * e2, dk2, dotk[hh]);  // y_k = Kr e2 and dy_k = dk2
+    // The assembly, once per kind of slot (block factors, or the exact path's true values).
+    auto assemble = [&](auto wide_tag) {
+      constexpr bool kWide = decltype(wide_tag)::value;
+      if (kL2) {
+        // per-quarter partial dots [4 column quarters][64 rows]: q in the rows of the last two
+        // block factors, k in the unused row and the upper half of the dbeta partials
+        float *pdq = vec + (V_D + 4) * kD;
+        float *pdk = (warp >> 2) < 2 ? vec + V_GL * kD + (warp >> 2) * kC : rb + 2 * kC + ((warp >> 2) - 2) * kC;
+  #pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const int c = ch0 + 8 * nt + 2 * l4;
+          float px[4], po[4], pk[4];
+          {
+            const uint32_t tb = tmem + ((uint32_t)(32 * Bk) << 16) + (uint32_t)(ch0 + 8 * nt);
+            tmem_ld_frag3(tb, tb + 128u, tb + 256u, px, po, pk);
           }
-        }
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-        for (int o = 1; o < 4; o <<= 1) {
-          dotq[hh] += __shfl_xor_sync(0xffffffffu, dotq[hh], o);
-          dotk[hh] += __shfl_xor_sync(0xffffffffu, dotk[hh], o);
-        }
-        if (l4 == 0) {
-          const int r = 16 * Bk + i8 + 8 * hh;
-          pdq[(warp >> 2) * kC + r] = dotq[hh];
-          pdk[r] = dotk[hh];
-        }
-      }
-      __syncthreads();
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * Bk + i8 + 8 * hh;
-        dotq[hh] = pdq[r] + pdq[kC + r] + pdq[2 * kC + r] + pdq[3 * kC + r];
-        dotk[hh] = vec[V_GL * kD + r] + vec[V_GL * kD + kC + r] + rb[2 * kC + r] + rb[3 * kC + r];
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      KDA_PT(9);
-      {
-        const int nt = g;
-        const int c = ch0 + 8 * nt + 2 * l4;
-        float px[4], po[4], pk[4];  // element (i8 + 8 hh, c + u) at index 2 hh + u
-        {
-          const uint32_t tb = tmem + ((uint32_t)(32 * Bk) << 16) + (uint32_t)(ch0 + 8 * nt);
-          tmem_ld_frag3(tb, tb + 128u, tb + 256u, px, po, pk);
-        }
-        const float2 gref2 = *reinterpret_cast<const float2 *>(vec + (V_GREF + Bk) * kD + c);
-        const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
-        const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
-        float cq[2] = {0.f, 0.f};
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * Bk + i8 + 8 * hh;
-          const float br = beta[r];
-          const float2 vq = make_float2(po[2 * hh], po[2 * hh + 1]);
-          const float2 vb = make_float2(-px[2 * hh], -px[2 * hh + 1]);
-          const float2 vk = make_float2(pk[2 * hh], pk[2 * hh + 1]);
-          const uint32_t to = sw_off(r, c, kC);
-          uint32_t *krh_p = reinterpret_cast<uint32_t *>(sm + C_KR + to), *krl_p = reinterpret_cast<uint32_t *>(sm + C_KR + LO128 + to);
-          uint32_t *qrh_p = reinterpret_cast<uint32_t *>(sm + C_QR + to), *qrl_p = reinterpret_cast<uint32_t *>(sm + C_QR + LO128 + to);
-          const float2 krh = unpack_bf16(*krh_p), krl = unpack_bf16(*krl_p);
-          const float2 qrh = unpack_bf16(*qrh_p), qrl = unpack_bf16(*qrl_p);
-          const float2 kch = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + to));
-          const float2 kcl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + LO128 + to));
-          const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
-          float dq2[2], dk2[2], qv[2], pv[2], yq[2], yk[2];  // yq, yk: kL2's normalised rows (yq times qscale)
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float Kr = u ? krh.y + krl.y : krh.x + krl.x;  // k e1
-            const float Qr = u ? qrh.y + qrl.y : qrh.x + qrl.x;  // q~ e1
-            const float Kc = u ? kch.y + kcl.y : kch.x + kcl.x;  // k e2
-            const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = u ? vk.y : vk.x;
-            const float gg_ = u ? g2.y : g2.x, gref = u ? gref2.y : gref2.x;
-            const float eref = u ? eref2.y : eref2.x, lam = u ? lam2.y : lam2.x;
-            const float e1 = ex2(gg_ - gref), e2 = ex2(gref - gg_);
-            const float gam = e1 * eref, kh = e2 * lam;
-            const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
-            const float xyI = xyi[nt][2 * hh + u];
-            dq2[u] = dQg * gam + e1 * yR;
-            dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * xyI;
-            yq[u] = Qr * e2;
-            yk[u] = Kr * e2;
-            // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
-            const bool in = r < len;
-            qv[u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
-            pv[u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * xyI - dKh * Kc * lam) : 0.f;
-            bpart[hh] += dBk * Kr * eref + Kr * xR;
-            cq[u] += dKh * Kc * lam;
-          }
-          // dG of (r, c) and (r, c + 1) into the Kr (Q part) and Qr (P part) pair slots just read
-          *krh_p = __float_as_uint(qv[0]);
-          *krl_p = __float_as_uint(qv[1]);
-          *qrh_p = __float_as_uint(pv[0]);
-          *qrl_p = __float_as_uint(pv[1]);
-          if (r < len) {
-            const size_t tok = (size_t)(t0 + r);
-            if (kL2) {  // dx = r (dy - y (y . dy)), y_q = Qr e2 / qscale, y_k = Kr e2
-              const float rk = rb[r], rq = rb[kC + r], dq_dot = dotq[hh] / qscale;
-              __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
-              __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
-              *reinterpret_cast<uint32_t *>(pq) = pack_bf16(rq * (dq2[0] * qscale - yq[0] * dq_dot),
-                                                          rq * (dq2[1] * qscale - yq[1] * dq_dot));
-              *reinterpret_cast<uint32_t *>(pk) = pack_bf16(rk * (dk2[0] - yk[0] * dotk[hh]), rk * (dk2[1] - yk[1] * dotk[hh]));
-            } else if (args.partial) {
-              float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
-              *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
-              *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
-            } else {
-              __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
-              __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
-              *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
-              *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
+          const float2 gm2 = *reinterpret_cast<const float2 *>(vec + (V_RREF + Bk) * kD + c);
+          const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
+          const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
+          const float2 ge2 = *reinterpret_cast<const float2 *>(vec + (V_CREF + Bk) * kD + c);
+  #pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r = 16 * Bk + i8 + 8 * hh;
+            const float br = beta[r];
+            const uint32_t to = sw_off(r, c, kC);
+            const float2 krh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + to));
+            const float2 krl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KR + LO128 + to));
+            const float2 qrh = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + to));
+            const float2 qrl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_QR + LO128 + to));
+            const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
+            const float2 kw = kWide && r < len ? raw_row(P, args, t0, h, r, c, rb, false) : make_float2(0.f, 0.f);
+            const float2 qw = kWide && r < len ? raw_row(P, args, t0, h, r, c, rb, true) : make_float2(0.f, 0.f);
+  #pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const Opnd o = opnd<kWide, true>(u ? krh.y + krl.y : krh.x + krl.x, u ? qrh.y + qrl.y : qrh.x + qrl.x, 0.f,
+                                               u ? g2.y : g2.x, u ? gm2.y : gm2.x, u ? ge2.y : ge2.x,
+                                               u ? eref2.y : eref2.x, u ? lam2.y : lam2.x, u ? kw.y : kw.x,
+                                               u ? qw.y : qw.x);
+              const float dq2 = po[2 * hh + u] * (o.e1 * o.eref) + o.e1 * yr[nt][2 * hh + u];
+              const float dk2 = pk[2 * hh + u] * (o.e2 * o.lam) - br * (o.e1 * o.eref) * px[2 * hh + u] +
+                                br * o.e1 * xr[nt][2 * hh + u] + o.e2 * xyi[nt][2 * hh + u];
+              dotq[hh] = fmaf(o.Qr * o.einv, dq2, dotq[hh]);  // y_q = Qr / e1 / qscale and dy_q = qscale dq2
+              dotk[hh] = fmaf(o.Kr * o.einv, dk2, dotk[hh]);  // y_k = Kr / e1 and dy_k = dk2
             }
           }
         }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {  // column sums of dKhat k khat over the warp's 16 rows
-          float cs = cq[u];
-          cs += __shfl_xor_sync(0xffffffffu, cs, 4);
-          cs += __shfl_xor_sync(0xffffffffu, cs, 8);
-          cs += __shfl_xor_sync(0xffffffffu, cs, 16);
-          if (i8 == 0) totC[Bk * kD + c + u] = cs;
+  #pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+  #pragma unroll
+          for (int o = 1; o < 4; o <<= 1) {
+            dotq[hh] += __shfl_xor_sync(0xffffffffu, dotq[hh], o);
+            dotk[hh] += __shfl_xor_sync(0xffffffffu, dotk[hh], o);
+          }
+          if (l4 == 0) {
+            const int r = 16 * Bk + i8 + 8 * hh;
+            pdq[(warp >> 2) * kC + r] = dotq[hh];
+            pdk[r] = dotk[hh];
+          }
+        }
+        __syncthreads();
+  #pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * Bk + i8 + 8 * hh;
+          dotq[hh] = pdq[r] + pdq[kC + r] + pdq[2 * kC + r] + pdq[3 * kC + r];
+          dotk[hh] = vec[V_GL * kD + r] + vec[V_GL * kD + kC + r] + rb[2 * kC + r] + rb[3 * kC + r];
         }
       }
-      KDA_PT(10);
-    }
+  #pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        KDA_PT(9);
+        {
+          const int nt = g;
+          const int c = ch0 + 8 * nt + 2 * l4;
+          float px[4], po[4], pk[4];  // element (i8 + 8 hh, c + u) at index 2 hh + u
+          {
+            const uint32_t tb = tmem + ((uint32_t)(32 * Bk) << 16) + (uint32_t)(ch0 + 8 * nt);
+            tmem_ld_frag3(tb, tb + 128u, tb + 256u, px, po, pk);
+          }
+          const float2 gm2 = *reinterpret_cast<const float2 *>(vec + (V_RREF + Bk) * kD + c);
+          const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
+          const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
+          const float2 ge2 = *reinterpret_cast<const float2 *>(vec + (V_CREF + Bk) * kD + c);
+          float cq[2] = {0.f, 0.f};
+  #pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r = 16 * Bk + i8 + 8 * hh;
+            const float br = beta[r];
+            const float2 vq = make_float2(po[2 * hh], po[2 * hh + 1]);
+            const float2 vb = make_float2(-px[2 * hh], -px[2 * hh + 1]);
+            const float2 vk = make_float2(pk[2 * hh], pk[2 * hh + 1]);
+            const uint32_t to = sw_off(r, c, kC);
+            uint32_t *krh_p = reinterpret_cast<uint32_t *>(sm + C_KR + to), *krl_p = reinterpret_cast<uint32_t *>(sm + C_KR + LO128 + to);
+            uint32_t *qrh_p = reinterpret_cast<uint32_t *>(sm + C_QR + to), *qrl_p = reinterpret_cast<uint32_t *>(sm + C_QR + LO128 + to);
+            const float2 krh = unpack_bf16(*krh_p), krl = unpack_bf16(*krl_p);
+            const float2 qrh = unpack_bf16(*qrh_p), qrl = unpack_bf16(*qrl_p);
+            const float2 kch = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + to));
+            const float2 kcl = unpack_bf16(*reinterpret_cast<const uint32_t *>(sm + C_KC + LO128 + to));
+            const float2 g2 = *reinterpret_cast<const float2 *>(G + r * kGLD + c);
+            const float2 kw = kWide && r < len ? raw_row(P, args, t0, h, r, c, rb, false) : make_float2(0.f, 0.f);
+            const float2 qw = kWide && r < len ? raw_row(P, args, t0, h, r, c, rb, true) : make_float2(0.f, 0.f);
+            float dq2[2], dk2[2], qv[2], pv[2], yq[2], yk[2];  // yq, yk: kL2's normalised rows (yq times qscale)
+  #pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              // k e1, q~ e1, k e2 and the factors (the exact path: k, q~ and true factors)
+              const Opnd o = opnd<kWide, kL2>(u ? krh.y + krl.y : krh.x + krl.x, u ? qrh.y + qrl.y : qrh.x + qrl.x,
+                                              u ? kch.y + kcl.y : kch.x + kcl.x, u ? g2.y : g2.x, u ? gm2.y : gm2.x,
+                                              u ? ge2.y : ge2.x, u ? eref2.y : eref2.x, u ? lam2.y : lam2.x,
+                                              u ? kw.y : kw.x, u ? qw.y : qw.x);
+              const float Kr = o.Kr, Qr = o.Qr, Kc = o.Kc, e1 = o.e1, e2 = o.e2, eref = o.eref, lam = o.lam;
+              const float dQg = u ? vq.y : vq.x, dBk = u ? vb.y : vb.x, dKh = u ? vk.y : vk.x;
+              const float gam = e1 * eref, kh = e2 * lam;
+              const float xR = xr[nt][2 * hh + u], yR = yr[nt][2 * hh + u];
+              const float xyI = xyi[nt][2 * hh + u];
+              dq2[u] = dQg * gam + e1 * yR;
+              dk2[u] = dKh * kh + br * gam * dBk + br * e1 * xR + e2 * xyI;
+              yq[u] = Qr * o.einv;
+              yk[u] = Kr * o.einv;
+              // dG = Q + P: P (pairwise decay terms and the Khat term) sums to zero over the chunk
+              const bool in = r < len;
+              qv[u] = in ? kLn2 * (dQg * Qr * eref + br * dBk * Kr * eref) : 0.f;
+              pv[u] = in ? kLn2 * (br * Kr * xR + Qr * yR - Kc * xyI - dKh * Kc * lam) : 0.f;
+              bpart[hh] += dBk * Kr * eref + Kr * xR;
+              cq[u] += dKh * Kc * lam;
+            }
+            // dG of (r, c) and (r, c + 1) into the Kr (Q part) and Qr (P part) pair slots just read
+            *krh_p = __float_as_uint(qv[0]);
+            *krl_p = __float_as_uint(qv[1]);
+            *qrh_p = __float_as_uint(pv[0]);
+            *qrl_p = __float_as_uint(pv[1]);
+            if (r < len) {
+              const size_t tok = (size_t)(t0 + r);
+              if (kL2) {  // dx = r (dy - y (y . dy)), y_q = Qr / e1 / qscale, y_k = Kr / e1
+                const float rk = rb[r], rq = rb[kC + r], dq_dot = dotq[hh] / qscale;
+                __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
+                __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
+                *reinterpret_cast<uint32_t *>(pq) = pack_bf16(rq * (dq2[0] * qscale - yq[0] * dq_dot),
+                                                            rq * (dq2[1] * qscale - yq[1] * dq_dot));
+                *reinterpret_cast<uint32_t *>(pk) = pack_bf16(rk * (dk2[0] - yk[0] * dotk[hh]), rk * (dk2[1] - yk[1] * dotk[hh]));
+              } else if (args.partial) {
+                float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
+                *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
+                *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
+              } else {
+                __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
+                __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
+                *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
+                *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
+              }
+            }
+          }
+  #pragma unroll
+          for (int u = 0; u < 2; ++u) {  // column sums of dKhat k khat over the warp's 16 rows
+            float cs = cq[u];
+            cs += __shfl_xor_sync(0xffffffffu, cs, 4);
+            cs += __shfl_xor_sync(0xffffffffu, cs, 8);
+            cs += __shfl_xor_sync(0xffffffffu, cs, 16);
+            if (i8 == 0) totC[Bk * kD + c + u] = cs;
+          }
+        }
+        KDA_PT(10);
+      }
+    };
+    if (wide) assemble(BoolC<true>{});
+    else assemble(BoolC<false>{});
     __syncthreads();  // every thread has parked its dG and its Khat column terms
     KDA_PT(11);
     if (more) {  // the Kc tile, G and beta are dead: the next slot's group P2, G and beta

@@ -71,8 +71,10 @@ constexpr int kThr = 256;  // 8 warps
 constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile of the per-chunk gradient kernel
 constexpr int kGT = 128;   // row stride of the TMA-loaded gate tile (dense rows)
 
-// rows of the per-channel vector table of the per-chunk gradient kernel
-constexpr int V_GL = 0, V_GAML = 1, V_GREF = 2, V_EREF = 6, V_D = 10, V_LAM = 16;
+// rows of the per-channel vector table of the per-chunk gradient kernel: G_last,
+// 2^G_last, the row references Gr(R) and 2^Gr(R), the block-pair factors D_RI,
+// 2^(G_last - Gc(R)) and the column references Gc(R)
+constexpr int V_GL = 0, V_GAML = 1, V_RREF = 2, V_EREF = 6, V_D = 10, V_LAM = 16, V_CREF = 20;
 
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
@@ -112,7 +114,7 @@ __device__ __forceinline__ uint32_t idesc(int M, int N, int a_mn, int b_mn) {
 
 // 2^x for the per-element decay factors: one hardware base-2 exponential (PTX
 // ex2.approx.ftz.f32, within about 2 ulp; results below 2^-126 flush to zero).
-// The factors it serves lie within 2^-120 .. 2^120 for gates >= -8 per token.
+// The block factors it serves lie within 2^-96 .. 2^96, or are <= 1.
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -14,7 +14,8 @@ sequence lengths (packed batches only), q, k, v, beta, g, h0, dO, dhT):
 * v ~ N(0, 1);
 * beta = sigmoid(N(0, 1)), one per (token, value head);
 * g = clip(-softplus(N(mu, 1)), -5, 0): a per-token, per-channel log2 decay
-  (mu = 0, or -3 for the near-1 decays of the long-context case);
+  (mu = 0, or -3 for the near-1 decays of the long-context case; strong-decay
+  test cases widen the spread and the clip);
 * h0 ~ 0.1 * N(0, 1); dO ~ N(0, 1); dhT ~ 0.1 * N(0, 1).
 
 The packed-varlen contract (device int32 offsets, repeated offsets = empty
@@ -124,10 +125,10 @@ def _sigmoid(x: np.ndarray) -> np.ndarray:
     return (1.0 / (1.0 + np.exp(-x.astype(np.float64)))).astype(np.float32)
 
 
-def _neg_softplus_clipped(x: np.ndarray) -> np.ndarray:
+def _neg_softplus_clipped(x: np.ndarray, lo: float = -5.0) -> np.ndarray:
     x64 = x.astype(np.float64)
     sp = np.where(x64 > 20, x64, np.log1p(np.exp(np.minimum(x64, 20))))
-    return np.clip(-sp, -5.0, 0.0).astype(np.float32)
+    return np.clip(-sp, lo, 0.0).astype(np.float32)
 
 
 def packed_lengths(rng: np.random.Generator, n_seq: int, total: int, lo: int, hi: int) -> np.ndarray:
@@ -173,10 +174,13 @@ def packed_lengths(rng: np.random.Generator, n_seq: int, total: int, lo: int, hi
 def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.bfloat16,
                 cu_seqlens=None, lengths_fn=None, h0: bool = True, final_state: bool = True,
                 dhT: Optional[bool] = None, g_mean: float = 0.0, seed: int = 0,
-                name: str = "custom", scalar_gate: bool = False) -> KdaInputs:
+                name: str = "custom", scalar_gate: bool = False, g_std: float = 1.0,
+                g_lo: float = -5.0) -> KdaInputs:
     """Draw one problem.  ``cu_seqlens`` may be a list of offsets (B must be 1);
     ``lengths_fn(rng)`` may instead return the offsets from the generator.
-    ``scalar_gate`` draws g as [B, T, HV] (one decay per token and value head)."""
+    ``scalar_gate`` draws g as [B, T, HV] (one decay per token and value head).
+    The gate is clip(-softplus(N(g_mean, g_std)), g_lo, 0); the workloads keep
+    the defaults (std 1, clip at -5), the strong-decay cases widen both."""
     rng = np.random.Generator(np.random.PCG64(seed))
     cu = None
     if lengths_fn is not None:
@@ -192,7 +196,8 @@ def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.
     k = _l2_rows(_normal(rng, (B, T, H, K)))
     v = _normal(rng, (B, T, HV, V))
     beta = _sigmoid(_normal(rng, (B, T, HV)))
-    g = _neg_softplus_clipped(_normal(rng, (B, T, HV) if scalar_gate else (B, T, HV, K), mean=g_mean))
+    g = _neg_softplus_clipped(_normal(rng, (B, T, HV) if scalar_gate else (B, T, HV, K), mean=g_mean, std=g_std),
+                              lo=g_lo)
     h0_t = _normal(rng, (N, HV, K, V), std=0.1) if h0 else None
     do = _normal(rng, (B, T, HV, V))
     if dhT is None:

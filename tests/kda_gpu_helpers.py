@@ -28,9 +28,16 @@ def _poisoned_ws(nbytes, dev):
     return ws, ctypes.c_void_p(a), nbytes + 512 - (a - p)
 
 
-def gpu_fwd(inp, dev="cuda", lib=None, l2=False):
+def status_words(lib, s, ws, wp):
+    """The four int32 status words a call left in its workspace (after a sync)."""
+    off = lib.kda_status_offset(ctypes.byref(s))
+    base = wp.value - ws.data_ptr() + off
+    return ws[base:base + 16].cpu().numpy().view(np.int32).tolist()
+
+
+def gpu_fwd(inp, dev="cuda", lib=None, l2=False, status=None):
     """kda_chunk_fwd on the inputs (moved to dev); returns CPU o, hT.  l2: the
-    q/k L2-norm prologue flag."""
+    q/k L2-norm prologue flag.  A ``status`` list receives the call's status words."""
     lib = lib or _lib.load()
     d = inp.to(dev)
     s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
@@ -43,10 +50,12 @@ def gpu_fwd(inp, dev="cuda", lib=None, l2=False):
                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     _lib.check(lib, st)
     torch.cuda.synchronize()
+    if status is not None:
+        status[:] = status_words(lib, s, ws, wp)
     return o.cpu(), (None if hT is None else hT.cpu())
 
 
-def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True, l2=False):
+def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True, l2=False, status=None):
     lib = lib or _lib.load()
     d = inp.to(dev)
     s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
@@ -65,6 +74,8 @@ def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True, l2=False):
                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     _lib.check(lib, st)
     torch.cuda.synchronize()
+    if status is not None:
+        status[:] = status_words(lib, s, ws, wp)
     return {k: (None if v is None else v.cpu()) for k, v in out.items()}
 
 
