@@ -123,7 +123,11 @@ size_t layout(const Problem &P, bool backward, bool with_ctx, char *base, Worksp
   memset(&w, 0, sizeof(w));
   w.seq = (int4 *)take(sizeof(int4) * (size_t)(P.N > 0 ? P.N : 1));
   w.chunk = (int4 *)take(sizeof(int4) * (size_t)(P.NC > 0 ? P.NC : 1));
-  w.flags = (int *)take(sizeof(int) * 4);
+  w.flags = (int *)take(sizeof(int) * 8);
+  if (use_tc(P)) {  // slots the record / gradient kernel leaves to its exact-path fix-up launch
+    w.wide_rec = (int *)take(sizeof(int) * (slots > 0 ? slots : 1));
+    if (backward) w.wide_grad = (int *)take(sizeof(int) * (slots > 0 ? slots : 1));
+  }
   if (P.scalar_gate && !use_tc(P)) {  // fp32 path: the gate repeated over K (and its per-channel gradient)
     w.gx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
     if (backward) w.dgx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
@@ -435,6 +439,6 @@ const char *kda_status_string(kda_status s) {
 
 const char *kda_last_error(void) { return g_err; }
 
-int kda_version(void) { return 104; }
+int kda_version(void) { return 105; }
 
 }  // extern "C"

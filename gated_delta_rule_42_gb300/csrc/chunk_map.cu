@@ -26,7 +26,8 @@ chunk_map_kernel(const int32_t *__restrict__ cu, int B, int T, int N, int64_t Tt
     s_carry = 0;
     s_bad = 0;
     flags[2] = 0;  // the call's bounded-wait error word: every call starts clean
-    flags[3] = 0;  // and its count of slots on the exact (wide-decay) path
+    flags[3] = 0;  // and its counts of slots on the exact (wide-decay) path
+    flags[4] = 0;
   }
   __syncthreads();
   for (int base = 0; base < N; base += kMapThreads) {

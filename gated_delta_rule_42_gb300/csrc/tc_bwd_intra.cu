@@ -25,10 +25,13 @@
 // the block's first and last row):
 //   row side    xr = sum_i dL_ri  Kc_i D_RI,  yr = sum_i dAqk_ri Kc_i D_RI
 //   column side xi = sum_r X_ri   Kr_r D_RI,  yi = sum_r dAqk_ri Qr_r D_RI   (X = beta dL)
-// on 16x16 warp MMAs.  A slot with such a wide channel forms its diagonal
-// blocks from the raw rows with pairwise exponents instead and carries true
-// values (e1 = e2 = 1) into the assembly: exact for any gate.  Then per element
-// (Gamma = 2^G, khat = 2^(G_last - G)):
+// on 16x16 warp MMAs.  References in the middle of each block's range (Gr =
+// Gc) keep every factor within 2^(+-kSpanMax/2); a slot with a block whose
+// span is wider is listed for the fix-up launch of this kernel, which takes
+// each block's first row as Gr and its last as Gc (factors <= 1), forms the
+// diagonal blocks from the raw rows with pairwise exponents and carries true
+// values (e1 = e2 = 1) into the assembly: exact for any gate.  Then per
+// element (Gamma = 2^G, khat = 2^(G_last - G)):
 //   dq~ = dQg Gamma + e1 yr
 //   dk  = dKhat khat + beta Gamma dBk + beta e1 xr + e2 (xi + yi)
 //   dG  = ln2 [dQg q~ Gamma - dKhat k khat + beta dBk k Gamma + beta k e1 xr + q~ e1 yr - k e2 (xi + yi)]
@@ -78,7 +81,7 @@ constexpr uint32_t C_SMEM = 220224 + 1024;
 static_assert(C_SMEM <= 232448, "one CTA per SM (227 KB)");
 // Widest per-channel decay span (log2) of a 16-token block that the middle
 // references carry (e1, e2 within 2^(+-kSpanMax / 2)); a slot with a wider
-// channel takes the exact path for its diagonal blocks.
+// block goes to the fix-up launch.
 constexpr float kSpanMax = 192.f;
 constexpr uint32_t LO128 = 16384, LO64 = 8192;
 // Tensor memory: the per-chunk products that the assembly reads element-wise are
@@ -167,7 +170,13 @@ struct Slot {
   int t0, len, j, h;
   size_t slot;
 };
-__device__ __forceinline__ bool get_slot(const Problem &P, const Workspace &W, int64_t s, Slot &o) {
+// kFix: s indexes the list of slots the first launch left to the fix-up (nfix of them).
+template <bool kFix>
+__device__ __forceinline__ bool get_slot(const Problem &P, const Workspace &W, int64_t s, int nfix, Slot &o) {
+  if (kFix) {
+    if (s >= nfix) return false;
+    s = W.wide_grad[s];
+  }
   if (s >= (int64_t)P.NC * P.HV) return false;
   const int c = (int)(s / P.HV);
   const int4 ch = W.chunk[c];
@@ -319,9 +328,12 @@ __device__ __forceinline__ Opnd opnd(float Kr, float Qr, float Kc, float g, floa
 // kL2: the q/k L2-norm prologue with HV = H, its backward fused: dx = r (dy - y (y . dy)) per
 // (token, head) row, from the inverse norms r of the decay-tile pass and row dots y . dy that a
 // first pass over the assembly's formulas forms, so dq and dk leave as bf16 in one pass.
-template <bool kScalarGate, bool kL2>
+// kFix: the fix-up launch, over the slots the first launch listed (status word 4 counts them).
+template <bool kScalarGate, bool kL2, bool kFix>
 __global__ void __launch_bounds__(kCT, 1)
 kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps) {
+  const int nfix = kFix ? *(volatile const int *)(W.flags + 4) : 0;
+  if (kFix && (int)blockIdx.x >= nfix) return;
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
@@ -352,7 +364,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 
   int64_t s_idx = blockIdx.x;
   Slot cur;
-  bool have = get_slot(P, W, s_idx, cur);
+  bool have = get_slot<kFix>(P, W, s_idx, nfix, cur);
   if (have) {  // the first slot: every group at once
     if (tid == 0) {
       mbar_expect_tx(bar_s, kBytesS);
@@ -368,7 +380,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     const uint32_t par = it & 1u;
     const int t0 = cur.t0, len = cur.len, j = cur.j, h = cur.h;
     Slot nxt;
-    const bool more = get_slot(P, W, s_idx + gridDim.x, nxt);
+    const bool more = get_slot<kFix>(P, W, s_idx + gridDim.x, nfix, nxt);
     bool ok = true;  // every bounded wait of this thread succeeded
     KDA_PT(13);
     ok &= bar_wait(bar_s, par, args.err);
@@ -493,15 +505,13 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 #pragma unroll
       for (int R = 0; R < 4; ++R) {  // rows past len hold G_last, so the references need no clamping
         const float gref = col[16 * R], gend = col[16 * R + 15];
-        const bool wide = !(gref - gend <= kSpanMax);  // (NaN-safe)
-        wide_c |= wide;
-        const float gmid = 0.5f * (gref + gend);
-        rref[R] = wide ? gref : gmid;
-        cref[R] = wide ? gend : gmid;
+        wide_c |= !(gref - gend <= kSpanMax);  // (NaN-safe)
+        rref[R] = kFix ? gref : 0.5f * (gref + gend);
+        cref[R] = kFix ? gend : rref[R];
         vec[(V_RREF + R) * kD + c] = rref[R];
         vec[(V_EREF + R) * kD + c] = exp2f(rref[R]);
         vec[(V_LAM + R) * kD + c] = exp2f(gl - cref[R]);
-        vec[(V_CREF + R) * kD + c] = cref[R];
+        if (kFix) vec[(V_CREF + R) * kD + c] = cref[R];
       }
       int p = 0;
 #pragma unroll
@@ -514,9 +524,11 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       zero_tail<kCT>(sm + C_KRAW, len);
       zero_tail<kCT>(sm + C_QRAW, len);
     }
-    // some block's decay span is wider than the block factors carry: the exact path
-    const bool wide = __syncthreads_or(wide_c) != 0;
-    if (wide && tid == 0) atomicAdd(W.flags + 3, 1);  // status word 3
+    // a block's decay span is wider than the middle references carry: list the
+    // slot for the fix-up launch (whose exact results replace this launch's)
+    constexpr bool wide = kFix;
+    if (!kFix && __syncthreads_or(wide_c) != 0 && tid == 0) W.wide_grad[atomicAdd(W.flags + 4, 1)] = (int)cur.slot;
+    if (kFix) __syncthreads();
     KDA_PT(1);
     {
       const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 3;  // two rows per thread
@@ -554,12 +566,13 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
             qv[e] *= rq;
           }
         }
-        *reinterpret_cast<float4 *>(e2) = *reinterpret_cast<const float4 *>(vec + (V_CREF + R) * kD + c0);  // Gc(R)
-        *reinterpret_cast<float4 *>(e2 + 4) = *reinterpret_cast<const float4 *>(vec + (V_CREF + R) * kD + c0 + 4);
+        const float *cref = vec + ((kFix ? V_CREF : V_RREF) + R) * kD + c0;  // Gc(R) = Gr(R) outside the fix-up
+        *reinterpret_cast<float4 *>(e2) = *reinterpret_cast<const float4 *>(cref);
+        *reinterpret_cast<float4 *>(e2 + 4) = *reinterpret_cast<const float4 *>(cref + 4);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float g = G[r * kGLD + c0 + e];
-          e1[e] = ex2(g - rref[e]);  // within 2^(+-kSpanMax/2), or <= 1 on a wide channel
+          e1[e] = ex2(g - rref[e]);  // within 2^(+-kSpanMax/2); <= 1 in the fix-up
           e2[e] = ex2(e2[e] - g);    // likewise
         }
         uint4 hi, lo;
@@ -771,7 +784,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     const float *dglv = red + 64;
     float bpart[2] = {0.f, 0.f};
     float dotq[2] = {0.f, 0.f}, dotk[2] = {0.f, 0.f};  // kL2: y . dy of rows i8, i8 + 8 of block Bk
-    // The assembly, once per kind of slot (block factors, or the exact path's true values).
+    // The assembly: block factors, or the fix-up's true values.
     auto assemble = [&](auto wide_tag) {
       constexpr bool kWide = decltype(wide_tag)::value;
       if (kL2) {
@@ -790,7 +803,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
           const float2 gm2 = *reinterpret_cast<const float2 *>(vec + (V_RREF + Bk) * kD + c);
           const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
           const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
-          const float2 ge2 = *reinterpret_cast<const float2 *>(vec + (V_CREF + Bk) * kD + c);
+          const float2 ge2 = kWide ? *reinterpret_cast<const float2 *>(vec + (V_CREF + Bk) * kD + c) : gm2;  // Gc(Bk)
   #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int r = 16 * Bk + i8 + 8 * hh;
@@ -852,7 +865,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
           const float2 gm2 = *reinterpret_cast<const float2 *>(vec + (V_RREF + Bk) * kD + c);
           const float2 eref2 = *reinterpret_cast<const float2 *>(vec + (V_EREF + Bk) * kD + c);
           const float2 lam2 = *reinterpret_cast<const float2 *>(vec + (V_LAM + Bk) * kD + c);
-          const float2 ge2 = *reinterpret_cast<const float2 *>(vec + (V_CREF + Bk) * kD + c);
+          const float2 ge2 = kWide ? *reinterpret_cast<const float2 *>(vec + (V_CREF + Bk) * kD + c) : gm2;  // Gc(Bk)
           float cq[2] = {0.f, 0.f};
   #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
@@ -933,8 +946,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
         KDA_PT(10);
       }
     };
-    if (wide) assemble(BoolC<true>{});
-    else assemble(BoolC<false>{});
+    assemble(BoolC<kFix>{});
     __syncthreads();  // every thread has parked its dG and its Khat column terms
     KDA_PT(11);
     if (more) {  // the Kc tile, G and beta are dead: the next slot's group P2, G and beta
@@ -1068,13 +1080,21 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 
 KDA_PT_EXPORT(kda_debug_intra_phase_cycles)
 
+// The per-chunk gradients, then the fix-up launch over the slots with a wide
+// decay span (none, usually: every CTA reads the count and leaves).
 template <bool kSG, bool kL2>
 cudaError_t launch_intra(const Problem &P, const Workspace &W, const IntraArgs &a, const TmaMaps &maps, unsigned grid,
                          cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)C_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<kSG, kL2><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
+  KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<kSG, kL2, false><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  KDA_LAUNCH("kda_bwd_intra_tc_fix", s,
+             kda_bwd_intra_tc_kernel<kSG, kL2, true><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
   return cudaGetLastError();
 }
 

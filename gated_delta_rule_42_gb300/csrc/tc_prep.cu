@@ -23,16 +23,16 @@
 // the 16-token blocks: row r of block R carries e1 = 2^(G_r - Gr(R)) (tiles Kr,
 // Qr), column i of block I carries e2 = 2^(Gc(I) - G_i) (tile Kc), and between
 // blocks (R > I) the factor D_RI = 2^(Gr(R) - Gc(I)) <= 1 goes onto the column
-// fragments in registers.  For a channel whose decay span over the block (G at
-// its first row minus G at its last, Ge) is at most kSpanMax, both references
-// sit in the middle of the block's range, so e1 and e2 stay within
-// 2^(+-kSpanMax/2) and a diagonal block needs no factor at all.  A wider
-// channel takes the block's first row as Gr and its last as Gc: e1, e2 <= 1,
-// so its off-diagonal products stay exact (they only underflow where the true
-// product does), and the slot's four diagonal blocks take the exact path: L
-// and Aqk there are formed from the raw rows, the decay between tokens i and r
-// as the running product of the per-token decays (diag_direct).  Wide blocks
-// need per-token gates averaging below about -12.8 (log2).  Chunk-level tiles:
+// fragments in registers.  kda_prep_tc puts both references in the middle of
+// each block's range, so e1 and e2 stay within 2^(+-kSpanMax/2) as long as the
+// block's decay span (G at its first row minus G at its last) is at most
+// kSpanMax, and a diagonal block needs no factor at all.  A slot with a wider
+// block (per-token gates averaging below about -12.8, log2) is listed instead
+// and left to kda_prep_tc_fix, which takes each block's first row as Gr and
+// its last as Gc on every channel: e1, e2 <= 1, so the off-diagonal products
+// only underflow where the true product does, and it forms the diagonal blocks
+// exactly from the raw rows, the decay between tokens i and r as the running
+// product of the per-token decays (diag_direct).  Chunk-level tiles:
 // Bk = beta k e1 2^Gr, Qg = q~ e1 2^Gr and Khat = k e2 2^(G_last - Gc); terms
 // below 2^-30 of the largest may flush to zero.
 #include "tc_common.cuh"
@@ -52,14 +52,15 @@ constexpr uint32_t P_K = 0;          // k [64][128] bf16 -> Kr -> A (fp32 scratc
 constexpr uint32_t P_Q = 16384;      // q [64][128] bf16 -> Qr -> T (fp32 scratch)
 constexpr uint32_t P_G = 32768;      // g -> G fp32 [64][128] (dense rows: a TMA box) -> L fp32 [64][64] | Kc
 constexpr uint32_t P_KC = 49152;     // Kc [64][128] bf16 (the upper half of G's space)
-constexpr uint32_t P_VEC = 65536;    // fp32 vectors: 14 rows of 128 (room for 18)
+constexpr uint32_t P_VEC = 65536;    // fp32 vectors: 18 rows of 128
 constexpr uint32_t P_BETA = 74752;   // beta [64]
 constexpr uint32_t P_MISC = 75008;   // mbarrier
 constexpr uint32_t P_SMEM = P_MISC + 16 + 1024;  // + alignment slack
 static_assert(P_SMEM + 1024 <= 233472 / 3, "three CTAs per SM (228 KB, 1 KB reserved per CTA)");
-// vector rows: the row references Gr(R), the column references Gc(R) and the
-// block-pair factors D_RI = 2^(Gr(R) - Gc(I)) for R > I
-constexpr int W_RREF = 0, W_CREF = 4, W_D = 8;
+// vector rows: the row references Gr(R) (= Gc(R) in kda_prep_tc), 2^Gr(R) (in
+// kda_prep_tc_fix the column references Gc(R) instead), 2^(G_last - Gc(R)), and
+// the block-pair factors D_RI = 2^(Gr(R) - Gc(I)) for R > I
+constexpr int W_GREF = 0, W_EREF = 4, W_CREF = 4, W_LAM = 8, W_D = 12;
 // Widest per-channel decay span (log2) of a 16-token block that the middle
 // references carry: e1 and e2 stay within 2^(+-kSpanMax / 2).
 constexpr float kSpanMax = 192.f;
@@ -95,8 +96,8 @@ __device__ __forceinline__ void l2norm_row16(float (&kv)[8], float (&qv)[8]) {
 // writes G (in place), the vectors, the decay tiles Kr, Qr (in place of k, q)
 // and Kc, and the record's Bk, Qg, Khat tiles and 2^G_last straight to global
 // memory (rec).  With l2n, the k and q rows are L2-normalised first.  Ends
-// with a __syncthreads.  Returns nonzero (on every thread) when some block's
-// decay span exceeds kSpanMax: the diagonal blocks then take diag_direct.
+// with a __syncthreads.  Returns nonzero (every thread, right after the
+// cumsum) when a block's span exceeds kSpanMax: the slot is left to the fix-up.
 __device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec, bool l2n) {
   const int tid = threadIdx.x;
   int wide_c = 0;
@@ -118,53 +119,51 @@ __device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *
     for (int r = 0; r < kC; ++r) G[r * kGT + c] = col[r];
     const float gl = s;
     reinterpret_cast<float *>(rec + kRecGAML)[c] = exp2f(gl);
-    float rref[4], cref[4];
+    float gref[4];
 #pragma unroll
-    for (int R = 0; R < 4; ++R) {  // rows past len hold G_last, so the references need no clamping
-      const float gref = col[16 * R], gend = col[16 * R + 15];
-      const bool wide = !(gref - gend <= kSpanMax);  // (NaN-safe)
-      wide_c |= wide;
-      const float gmid = 0.5f * (gref + gend);
-      rref[R] = wide ? gref : gmid;
-      cref[R] = wide ? gend : gmid;
-      vec[(W_RREF + R) * kD + c] = rref[R];
-      vec[(W_CREF + R) * kD + c] = cref[R];
+    for (int R = 0; R < 4; ++R) {
+      // rows past len hold G_last; the middle of the block's range (NaN-safe span test)
+      wide_c |= !(col[16 * R] - col[16 * R + 15] <= kSpanMax);
+      gref[R] = 0.5f * (col[16 * R] + col[16 * R + 15]);
+      vec[(W_GREF + R) * kD + c] = gref[R];
+      vec[(W_EREF + R) * kD + c] = exp2f(gref[R]);
+      vec[(W_LAM + R) * kD + c] = exp2f(gl - gref[R]);
     }
-    // D_RI = 2^(Gr(R) - Gc(I)) for the pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+    // D_RI = 2^(gref_R - gref_I) for the pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
     int p = 0;
 #pragma unroll
     for (int R = 1; R < 4; ++R)
 #pragma unroll
-      for (int I = 0; I < R; ++I) vec[(W_D + p++) * kD + c] = exp2f(rref[R] - cref[I]);
+      for (int I = 0; I < R; ++I) vec[(W_D + p++) * kD + c] = exp2f(gref[R] - gref[I]);
   }
-  const int wide = __syncthreads_or(wide_c);
+  if (__syncthreads_or(wide_c)) return 1;
   KDA_PT(1);
   // thread: 8 consecutive channels (one 16-byte chunk) of 4 consecutive rows;
   // a half-warp covers one row, so the record stores are whole 128-byte lines
   {
     const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
-    float eref[8], lam[8];  // 2^Gr(R) and 2^(G_last - Gc(R))
-    uint4 kc[4];            // Kc rows, written once every thread has read its G values
+    float gref[8], eref[8], lam[8];
+    uint4 kc[4];  // Kc rows, written once every thread has read its G values
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      eref[e] = ex2(vec[(W_RREF + R) * kD + c0 + e]);
-      lam[e] = ex2(G[(kC - 1) * kGT + c0 + e] - vec[(W_CREF + R) * kD + c0 + e]);  // G's last row is G_last
+    for (int e = 0; e < 8; e += 4) {
+      *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (W_GREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(eref + e) = *reinterpret_cast<const float4 *>(vec + (W_EREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(lam + e) = *reinterpret_cast<const float4 *>(vec + (W_LAM + R) * kD + c0 + e);
     }
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
       const int r = rg * 4 + rr;
       const uint32_t off = sw_chunk(r, jj, kC);
-      float kv[8], qv[8], e1[8], e2[8], o[8];
+      float kv[8], qv[8], g[8], e1[8], e2[8], o[8];
       unpack8(*reinterpret_cast<const uint4 *>(sm + P_K + off), kv);
       unpack8(*reinterpret_cast<const uint4 *>(sm + P_Q + off), qv);
       if (l2n) l2norm_row16(kv, qv);
+      *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGT + c0);
+      *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + 4);
 #pragma unroll
-      for (int e = 0; e < 8; e += 4) {
-        const float4 g = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + e);
-        const float4 rf = *reinterpret_cast<const float4 *>(vec + (W_RREF + R) * kD + c0 + e);
-        const float4 cf = *reinterpret_cast<const float4 *>(vec + (W_CREF + R) * kD + c0 + e);
-        e1[e] = ex2(g.x - rf.x); e1[e + 1] = ex2(g.y - rf.y); e1[e + 2] = ex2(g.z - rf.z); e1[e + 3] = ex2(g.w - rf.w);
-        e2[e] = ex2(cf.x - g.x); e2[e + 1] = ex2(cf.y - g.y); e2[e + 2] = ex2(cf.z - g.z); e2[e + 3] = ex2(cf.w - g.w);
+      for (int e = 0; e < 8; ++e) {
+        e1[e] = ex2(g[e] - gref[e]);  // within 2^(+-kSpanMax/2)
+        e2[e] = ex2(gref[e] - g[e]);
       }
       const float br = beta[r];
 #pragma unroll
@@ -174,10 +173,10 @@ __device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *
       for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
       kc[rr] = pack8(o);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * (e1[e] * eref[e]);
+      for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * e1[e] * eref[e];
       *reinterpret_cast<uint4 *>(rec + kRecBK + off) = pack8(o);  // Bk
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = kv[e] * (e2[e] * lam[e]);
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e] * lam[e];
       *reinterpret_cast<uint4 *>(rec + kRecKH + off) = pack8(o);  // Khat
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
@@ -191,172 +190,14 @@ __device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *
     for (int rr = 0; rr < 4; ++rr) *reinterpret_cast<uint4 *>(sm + P_KC + sw_chunk(rg * 4 + rr, jj, kC)) = kc[rr];
   }
   __syncthreads();
-  return wide;
+  return 0;
 }
 
-// One diagonal block (R, R) of a slot whose decay span defeats the block
-// factors: L_ri = beta_r sum_c k_rc k_ic 2^(G_rc - G_ic) (i < r) and
-// Aqk_ri = sum_c q~_rc k_ic 2^(G_rc - G_ic) (i <= r) from the raw rows (L2-
-// normalised with l2n), the decay between tokens i and r formed as the running
-// product of the per-token decays 2^g_s, s = i+1 .. r: exact for any gate, it
-// only underflows where the true factor does.  One warp; lane l holds channels
-// 4l .. 4l+3.  Writes the block's L (fp32, Lf) and Aqk (bf16, rec), zeros above
-// the diagonal and past len.
-__device__ __noinline__ void diag_direct(const Problem &P, int t0, int len, int h, int j, int R, const float *beta,
-                                         float *Lf, unsigned char *rec) {
-  const int lane = threadIdx.x & 31, c0 = lane * 4;
-  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
-  const __nv_bfloat16 *kp = (const __nv_bfloat16 *)P.k, *qp = (const __nv_bfloat16 *)P.q;
-  auto ld4 = [&](const __nv_bfloat16 *base, int r, float (&x)[4]) {  // row r of the chunk, this lane's channels
-    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(base + ((size_t)(t0 + r) * P.H + h) * kD + c0));
-    const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y);
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-  };
-  // inverse row norms of the q/k L2-norm prologue: row 16R + r's are kept by lane r
-  float nk = 1.f, nq = 1.f;
-  if (P.l2norm) {
-    for (int r = 0; r < 16; ++r) {
-      float sk = 0.f, sq = 0.f;
-      if (16 * R + r < len) {
-        float a[4], b[4];
-        ld4(kp, 16 * R + r, a);
-        ld4(qp, 16 * R + r, b);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sk = fmaf(a[e], a[e], sk);
-          sq = fmaf(b[e], b[e], sq);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      }
-      if (lane == r) {
-        nk = 1.0f / sqrtf(sk + kL2NormEps);
-        nq = 1.0f / sqrtf(sq + kL2NormEps);
-      }
-    }
-  }
-  for (int i = 0; i < 16 && 16 * R + i < len; ++i) {
-    const int ti = 16 * R + i;
-    float ki[4], F[4] = {1.f, 1.f, 1.f, 1.f};
-    ld4(kp, ti, ki);
-    const float nki = __shfl_sync(0xffffffffu, nk, i);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) ki[e] *= nki;
-    for (int r = i; r < 16 && 16 * R + r < len; ++r) {
-      const int tr = 16 * R + r;
-      if (r > i) {  // F *= 2^g of token tr
-        const size_t row = (size_t)(t0 + tr) * P.HV + j;
-        if (P.scalar_gate) {
-          const float a = exp2f(__ldg(P.g + row));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) F[e] *= a;
-        } else {
-          const float4 g4 = __ldg(reinterpret_cast<const float4 *>(P.g + row * kD + c0));
-          F[0] *= exp2f(g4.x); F[1] *= exp2f(g4.y); F[2] *= exp2f(g4.z); F[3] *= exp2f(g4.w);
-        }
-      }
-      float kr[4], qr[4];
-      ld4(kp, tr, kr);
-      ld4(qp, tr, qr);
-      const float nkr = __shfl_sync(0xffffffffu, nk, r), nqr = __shfl_sync(0xffffffffu, nq, r) * qscale;
-      float sL = 0.f, sQ = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float f = ki[e] * F[e];
-        sL = fmaf(kr[e] * nkr, f, sL);
-        sQ = fmaf(qr[e] * nqr, f, sQ);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sL += __shfl_xor_sync(0xffffffffu, sL, o);
-        sQ += __shfl_xor_sync(0xffffffffu, sQ, o);
-      }
-      if (lane == 0) {
-        Lf[fsw(tr, ti)] = r > i ? beta[tr] * sL : 0.f;
-        *reinterpret_cast<__nv_bfloat16 *>(rec + kRecAQK + sw_off(tr, ti, kC)) = __float2bfloat16_rn(sQ);
-      }
-    }
-  }
-  for (int e = lane; e < 256; e += 32) {  // the rest of the block: above the diagonal, or past len
-    const int r = e >> 4, i = e & 15, tr = 16 * R + r, ti = 16 * R + i;
-    if (i > r || tr >= len || ti >= len) {
-      Lf[fsw(tr, ti)] = 0.f;
-      *reinterpret_cast<__nv_bfloat16 *>(rec + kRecAQK + sw_off(tr, ti, kC)) = __float2bfloat16_rn(0.f);
-    }
-  }
-}
-
-// Phase (b).  Needs the decay tiles of phase (a); writes the record's Aqk and A
-// tiles straight to global memory (rec).  With wide set, the diagonal block
-// pairs take diag_direct instead of the block factors.
-__device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, unsigned char *rec, int wide,
-                                        const Problem &P, int t0, int len, int h, int j) {
+// The inverse A = (I + L)^-1 of L (fp32 in shared memory, strictly lower) and
+// its bf16 record tile.  Begins after a __syncthreads that published L.
+__device__ __forceinline__ void invert_store(unsigned char *sm, unsigned char *rec) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t sbase = smem_u32(sm);
-  const float *vec = (const float *)(sm + P_VEC);
-  float *Lf = (float *)(sm + P_G);  // G is dead
-  // Gram blocks: the 10 block pairs R >= I over the 8 warps (the A fragments of
-  // a pair serve both 8-column halves: shared-memory wavefronts bound this phase).
-  for (int p = warp; p < 10; p += 8) {
-    const int R = p >= 6 ? 3 : p >= 3 ? 2 : p >= 1 ? 1 : 0, I = p - R * (R + 1) / 2;
-    if (wide && I == R) continue;  // diag_direct, below
-    const float *Dv = (I < R) ? vec + (W_D + R * (R - 1) / 2 + I) * kD : nullptr;  // no factor inside a block
-    float accL[2][4] = {}, accQ[2][4] = {};
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint32_t ak[4], aq[4], b[4];
-      {
-        const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
-        ldsm_x4(sbase + P_K + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
-        ldsm_x4(sbase + P_Q + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
-      }
-      {
-        const int mi = lane >> 3;
-        const int row = 16 * I + (lane & 7) + (mi >> 1) * 8, jj = 2 * s + (mi & 1);
-        ldsm_x4(sbase + P_KC + sw_chunk(row, jj, kC), b[0], b[1], b[2], b[3]);
-      }
-      if (Dv != nullptr) {
-        const int c0 = 16 * s + (lane & 3) * 2;
-        const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
-        const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float2 f = unpack_bf16(b[t]);
-          b[t] = (t & 1) ? pack_bf16(f.x * d89.x, f.y * d89.y) : pack_bf16(f.x * d01.x, f.y * d01.y);
-        }
-      }
-      mma16816(accL[0], ak, b[0], b[1]);
-      mma16816(accL[1], ak, b[2], b[3]);
-      mma16816(accQ[0], aq, b[0], b[1]);
-      mma16816(accQ[1], aq, b[2], b[3]);
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * R + (lane >> 2) + hh * 8;
-        const int i = 16 * I + nt * 8 + (lane & 3) * 2;
-        const float br = beta[r];
-        const float l0 = (i < r) ? br * accL[nt][2 * hh] : 0.f;
-        const float l1 = (i + 1 < r) ? br * accL[nt][2 * hh + 1] : 0.f;
-        *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
-        const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
-        const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
-        *reinterpret_cast<uint32_t *>(rec + kRecAQK + sw_off(r, i, kC)) = pack_bf16(a0, a1);
-      }
-    }
-  }
-  if (wide && warp >= 4) diag_direct(P, t0, len, h, j, warp - 4, beta, Lf, rec);
-  if (tid < 6 * 32) {  // Aqk blocks above the diagonal (R < I) are zero
-    const int b = tid >> 5, w = tid & 31;
-    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
-    *reinterpret_cast<uint4 *>(rec + kRecAQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();
-  KDA_PT(4);
+  float *Lf = (float *)(sm + P_G);
   float *Af = (float *)(sm + P_K);  // overwrites Kr (dead)
   float *Tf = (float *)(sm + P_Q);  // overwrites Qr (dead)
   if (warp < 4 && lane < 16) {
@@ -469,28 +310,81 @@ __device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, un
   }
 }
 
-__global__ void __launch_bounds__(kThr, 3)
-kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps) {
-  extern __shared__ unsigned char smraw[];
-  unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+// Phase (b).  Needs the decay tiles of phase (a); writes the record's Aqk and A
+// tiles straight to global memory (rec).
+__device__ __forceinline__ void phase_b(unsigned char *sm, const float *beta, unsigned char *rec) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(sm);
-  const int c_idx = blockIdx.x, j = blockIdx.y;
-  const int4 ch = W.chunk[c_idx];
-  if (ch.x < 0) return;  // unused chunk slot
-  const int t0 = ch.y, len = ch.z;
-  const int HV = P.HV, h = j / (HV / P.H);
-  const int tid = threadIdx.x;
-  const size_t slot = (size_t)c_idx * HV + j;
-  float *beta = (float *)(sm + P_BETA);
-  uint64_t *bar = (uint64_t *)(sm + P_MISC);
-  KDA_PT_DECL;
-
-  if (tid == 0) {
-    bar_init(bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  const float *vec = (const float *)(sm + P_VEC);
+  float *Lf = (float *)(sm + P_G);  // G is dead
+  // Gram blocks: the 10 block pairs R >= I over the 8 warps (the A fragments of
+  // a pair serve both 8-column halves: shared-memory wavefronts bound this phase).
+  for (int p = warp; p < 10; p += 8) {
+    const int R = p >= 6 ? 3 : p >= 3 ? 2 : p >= 1 ? 1 : 0, I = p - R * (R + 1) / 2;
+    const float *Dv = (I < R) ? vec + (W_D + R * (R - 1) / 2 + I) * kD : nullptr;
+    float accL[2][4] = {}, accQ[2][4] = {};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t ak[4], aq[4], b[4];
+      {
+        const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
+        ldsm_x4(sbase + P_K + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
+        ldsm_x4(sbase + P_Q + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
+      }
+      {
+        const int mi = lane >> 3;
+        const int row = 16 * I + (lane & 7) + (mi >> 1) * 8, jj = 2 * s + (mi & 1);
+        ldsm_x4(sbase + P_KC + sw_chunk(row, jj, kC), b[0], b[1], b[2], b[3]);
+      }
+      if (Dv != nullptr) {
+        const int c0 = 16 * s + (lane & 3) * 2;
+        const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
+        const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = unpack_bf16(b[t]);
+          b[t] = (t & 1) ? pack_bf16(f.x * d89.x, f.y * d89.y) : pack_bf16(f.x * d01.x, f.y * d01.y);
+        }
+      }
+      mma16816(accL[0], ak, b[0], b[1]);
+      mma16816(accL[1], ak, b[2], b[3]);
+      mma16816(accQ[0], aq, b[0], b[1]);
+      mma16816(accQ[1], aq, b[2], b[3]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * R + (lane >> 2) + hh * 8;
+        const int i = 16 * I + nt * 8 + (lane & 3) * 2;
+        const float br = beta[r];
+        const float l0 = (i < r) ? br * accL[nt][2 * hh] : 0.f;
+        const float l1 = (i + 1 < r) ? br * accL[nt][2 * hh + 1] : 0.f;
+        *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(l0, l1);
+        const float a0 = (i <= r) ? accQ[nt][2 * hh] : 0.f;
+        const float a1 = (i + 1 <= r) ? accQ[nt][2 * hh + 1] : 0.f;
+        *reinterpret_cast<uint32_t *>(rec + kRecAQK + sw_off(r, i, kC)) = pack_bf16(a0, a1);
+      }
+    }
+  }
+  if (tid < 6 * 32) {  // Aqk blocks above the diagonal (R < I) are zero
+    const int b = tid >> 5, w = tid & 31;
+    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
+    *reinterpret_cast<uint4 *>(rec + kRecAQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
-  if (tid == 0) {  // k, q rows and the gate rows (TMA); rows past the tensor end arrive as zeros
+  KDA_PT(4);
+  invert_store(sm, rec);
+}
+
+// A slot's k, q and gate rows (TMA; rows past the tensor end arrive as zeros) and
+// beta; rows past len cleared.  Ends with a __syncthreads.
+__device__ __forceinline__ void load_slot(const Problem &P, const TmaMaps &maps, unsigned char *sm, uint64_t *bar,
+                                          uint32_t parity, int *err, int t0, int len, int h, int j) {
+  const uint32_t sbase = smem_u32(sm);
+  const int tid = threadIdx.x, HV = P.HV;
+  float *beta = (float *)(sm + P_BETA);
+  if (tid == 0) {
     mbar_expect_tx(bar, 32768u + (P.scalar_gate ? 0u : 32768u));
     tma_tile(sbase + P_K, &maps.k, h, t0, bar);
     tma_tile(sbase + P_Q, &maps.q, h, t0, bar);
@@ -514,21 +408,329 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
   load_beta(P, beta, t0, len, j);
   cp_commit();
   cp_wait_all();
-  bar_wait(bar, 0, err);
+  bar_wait(bar, parity, err);
   if (len < kC) {  // rows past the sequence end hold the next tokens: clear them
     zero_tail(sm + P_K, len);
     zero_tail(sm + P_Q, len);
   }
   __syncthreads();
+}
+
+// One CTA per (chunk, value head) slot; a slot with a block wider than kSpanMax
+// is listed in W.wide_rec (status word 3 counts them) for kda_prep_tc_fix.
+__global__ void __launch_bounds__(kThr, 3)
+kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps) {
+  extern __shared__ unsigned char smraw[];
+  unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const int c_idx = blockIdx.x, j = blockIdx.y;
+  const int4 ch = W.chunk[c_idx];
+  if (ch.x < 0) return;  // unused chunk slot
+  const int t0 = ch.y, len = ch.z;
+  const int HV = P.HV, h = j / (HV / P.H);
+  const int tid = threadIdx.x;
+  const size_t slot = (size_t)c_idx * HV + j;
+  float *beta = (float *)(sm + P_BETA);
+  uint64_t *bar = (uint64_t *)(sm + P_MISC);
+  KDA_PT_DECL;
+
+  if (tid == 0) {
+    bar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  load_slot(P, maps, sm, bar, 0u, err, t0, len, h, j);
   KDA_PT(0);
 
   unsigned char *rec = W.tc_tiles + slot * kTileRecord;
-  const int wide = phase_a(sm, len, beta, rec, P.l2norm);
-  if (wide && tid == 0) atomicAdd(W.flags + 3, 1);  // status word 3: slots on the exact diagonal path
+  if (phase_a(sm, len, beta, rec, P.l2norm)) {
+    if (tid == 0) W.wide_rec[atomicAdd(W.flags + 3, 1)] = (int)slot;
+    return;
+  }
   KDA_PT(2);
-  phase_b(sm, beta, rec, wide, P, t0, len, h, j);
+  phase_b(sm, beta, rec);
   KDA_PT(10);
   KDA_PT_FLUSH;
+}
+
+// ---- the exact path for slots with a wide block ----
+
+// Phase (a) of the fix-up: phase_a with the block's first row as the row
+// reference Gr and its last row as the column reference Gc on every channel,
+// so that e1, e2 and every off-diagonal factor are <= 1.
+__device__ __forceinline__ void fix_phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec,
+                                            bool l2n) {
+  const int tid = threadIdx.x;
+  float *G = (float *)(sm + P_G);
+  float *vec = (float *)(sm + P_VEC);
+  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
+  if (tid < kD) {
+    const int c = tid;
+    float col[kC];
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < kC; ++r) col[r] = G[r * kGT + c];
+#pragma unroll
+    for (int r = 0; r < kC; ++r) {
+      if (r < len) s += col[r];
+      col[r] = s;
+    }
+#pragma unroll
+    for (int r = 0; r < kC; ++r) G[r * kGT + c] = col[r];
+    const float gl = s;
+    reinterpret_cast<float *>(rec + kRecGAML)[c] = exp2f(gl);
+    float gref[4], gend[4];
+#pragma unroll
+    for (int R = 0; R < 4; ++R) {  // rows past len hold G_last
+      gref[R] = col[16 * R];
+      gend[R] = col[16 * R + 15];
+      vec[(W_GREF + R) * kD + c] = gref[R];
+      vec[(W_CREF + R) * kD + c] = gend[R];
+      vec[(W_LAM + R) * kD + c] = exp2f(gl - gend[R]);
+    }
+    int p = 0;  // D_RI = 2^(Gr(R) - Gc(I)) for the pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+#pragma unroll
+    for (int R = 1; R < 4; ++R)
+#pragma unroll
+      for (int I = 0; I < R; ++I) vec[(W_D + p++) * kD + c] = exp2f(gref[R] - gend[I]);
+  }
+  __syncthreads();
+  {
+    const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4, R = rg >> 2;
+    float gref[8], eref[8], lam[8];
+    uint4 kc[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 4) {
+      *reinterpret_cast<float4 *>(gref + e) = *reinterpret_cast<const float4 *>(vec + (W_GREF + R) * kD + c0 + e);
+      *reinterpret_cast<float4 *>(lam + e) = *reinterpret_cast<const float4 *>(vec + (W_LAM + R) * kD + c0 + e);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) eref[e] = ex2(gref[e]);
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = rg * 4 + rr;
+      const uint32_t off = sw_chunk(r, jj, kC);
+      float kv[8], qv[8], g[8], e1[8], e2[8], o[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + P_K + off), kv);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + P_Q + off), qv);
+      if (l2n) l2norm_row16(kv, qv);
+      *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGT + c0);
+      *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + 4);
+      *reinterpret_cast<float4 *>(e2) = *reinterpret_cast<const float4 *>(vec + (W_CREF + R) * kD + c0);
+      *reinterpret_cast<float4 *>(e2 + 4) = *reinterpret_cast<const float4 *>(vec + (W_CREF + R) * kD + c0 + 4);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        e1[e] = ex2(g[e] - gref[e]);  // <= 1
+        e2[e] = ex2(e2[e] - g[e]);    // <= 1
+      }
+      const float br = beta[r];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
+      *reinterpret_cast<uint4 *>(sm + P_K + off) = pack8(o);  // Kr
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
+      kc[rr] = pack8(o);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = br * kv[e] * (e1[e] * eref[e]);
+      *reinterpret_cast<uint4 *>(rec + kRecBK + off) = pack8(o);  // Bk
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = kv[e] * (e2[e] * lam[e]);
+      *reinterpret_cast<uint4 *>(rec + kRecKH + off) = pack8(o);  // Khat
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
+      *reinterpret_cast<uint4 *>(sm + P_Q + off) = pack8(o);  // Qr
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] *= eref[e];
+      *reinterpret_cast<uint4 *>(rec + kRecQG + off) = pack8(o);  // Qg
+    }
+    __syncthreads();  // G is dead: its upper half takes Kc
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) *reinterpret_cast<uint4 *>(sm + P_KC + sw_chunk(rg * 4 + rr, jj, kC)) = kc[rr];
+  }
+  __syncthreads();
+}
+
+// One diagonal block (R, R) of a slot whose decay span defeats the block
+// factors: L_ri = beta_r sum_c k_rc k_ic 2^(G_rc - G_ic) (i < r) and
+// Aqk_ri = sum_c q~_rc k_ic 2^(G_rc - G_ic) (i <= r) from the raw rows (L2-
+// normalised with l2n), the decay between tokens i and r formed as the running
+// product of the per-token decays 2^g_s, s = i+1 .. r: exact for any gate, it
+// only underflows where the true factor does.  One warp; lane l holds channels
+// 4l .. 4l+3.  Writes the block's L (fp32, Lf) and Aqk (bf16, rec), zeros above
+// the diagonal and past len.
+__device__ __noinline__ void diag_direct(const Problem &P, int t0, int len, int h, int j, int R, const float *beta,
+                                         float *Lf, unsigned char *rec) {
+  const int lane = threadIdx.x & 31, c0 = lane * 4;
+  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
+  const __nv_bfloat16 *kp = (const __nv_bfloat16 *)P.k, *qp = (const __nv_bfloat16 *)P.q;
+  auto ld4 = [&](const __nv_bfloat16 *base, int r, float (&x)[4]) {  // row r of the chunk, this lane's channels
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(base + ((size_t)(t0 + r) * P.H + h) * kD + c0));
+    const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  };
+  // inverse row norms of the q/k L2-norm prologue: row 16R + r's are kept by lane r
+  float nk = 1.f, nq = 1.f;
+  if (P.l2norm) {
+    for (int r = 0; r < 16; ++r) {
+      float sk = 0.f, sq = 0.f;
+      if (16 * R + r < len) {
+        float a[4], b[4];
+        ld4(kp, 16 * R + r, a);
+        ld4(qp, 16 * R + r, b);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sk = fmaf(a[e], a[e], sk);
+          sq = fmaf(b[e], b[e], sq);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      }
+      if (lane == r) {
+        nk = 1.0f / sqrtf(sk + kL2NormEps);
+        nq = 1.0f / sqrtf(sq + kL2NormEps);
+      }
+    }
+  }
+  for (int i = 0; i < 16 && 16 * R + i < len; ++i) {
+    const int ti = 16 * R + i;
+    float ki[4], F[4] = {1.f, 1.f, 1.f, 1.f};
+    ld4(kp, ti, ki);
+    const float nki = __shfl_sync(0xffffffffu, nk, i);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ki[e] *= nki;
+    for (int r = i; r < 16 && 16 * R + r < len; ++r) {
+      const int tr = 16 * R + r;
+      if (r > i) {  // F *= 2^g of token tr
+        const size_t row = (size_t)(t0 + tr) * P.HV + j;
+        if (P.scalar_gate) {
+          const float a = exp2f(__ldg(P.g + row));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) F[e] *= a;
+        } else {
+          const float4 g4 = __ldg(reinterpret_cast<const float4 *>(P.g + row * kD + c0));
+          F[0] *= exp2f(g4.x); F[1] *= exp2f(g4.y); F[2] *= exp2f(g4.z); F[3] *= exp2f(g4.w);
+        }
+      }
+      float kr[4], qr[4];
+      ld4(kp, tr, kr);
+      ld4(qp, tr, qr);
+      const float nkr = __shfl_sync(0xffffffffu, nk, r), nqr = __shfl_sync(0xffffffffu, nq, r) * qscale;
+      float sL = 0.f, sQ = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float f = ki[e] * F[e];
+        sL = fmaf(kr[e] * nkr, f, sL);
+        sQ = fmaf(qr[e] * nqr, f, sQ);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sL += __shfl_xor_sync(0xffffffffu, sL, o);
+        sQ += __shfl_xor_sync(0xffffffffu, sQ, o);
+      }
+      if (lane == 0) {
+        Lf[fsw(tr, ti)] = r > i ? beta[tr] * sL : 0.f;
+        *reinterpret_cast<__nv_bfloat16 *>(rec + kRecAQK + sw_off(tr, ti, kC)) = __float2bfloat16_rn(sQ);
+      }
+    }
+  }
+  for (int e = lane; e < 256; e += 32) {  // the rest of the block: above the diagonal, or past len
+    const int r = e >> 4, i = e & 15, tr = 16 * R + r, ti = 16 * R + i;
+    if (i > r || tr >= len || ti >= len) {
+      Lf[fsw(tr, ti)] = 0.f;
+      *reinterpret_cast<__nv_bfloat16 *>(rec + kRecAQK + sw_off(tr, ti, kC)) = __float2bfloat16_rn(0.f);
+    }
+  }
+}
+
+// Phase (b) of the fix-up: the off-diagonal Gram blocks on the block factors,
+// the diagonal ones by diag_direct (warps 4..7), then the inverse.
+__device__ __forceinline__ void fix_phase_b(unsigned char *sm, const float *beta, unsigned char *rec,
+                                            const Problem &P, int t0, int len, int h, int j) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_u32(sm);
+  const float *vec = (const float *)(sm + P_VEC);
+  float *Lf = (float *)(sm + P_G);
+  for (int p = warp; p < 10; p += 8) {
+    const int R = p >= 6 ? 3 : p >= 3 ? 2 : p >= 1 ? 1 : 0, I = p - R * (R + 1) / 2;
+    if (I == R) continue;
+    const float *Dv = vec + (W_D + R * (R - 1) / 2 + I) * kD;
+    float accL[2][4] = {}, accQ[2][4] = {};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t ak[4], aq[4], b[4];
+      {
+        const int row = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8, jj = 2 * s + (lane >> 4);
+        ldsm_x4(sbase + P_K + sw_chunk(row, jj, kC), ak[0], ak[1], ak[2], ak[3]);
+        ldsm_x4(sbase + P_Q + sw_chunk(row, jj, kC), aq[0], aq[1], aq[2], aq[3]);
+      }
+      {
+        const int mi = lane >> 3;
+        const int row = 16 * I + (lane & 7) + (mi >> 1) * 8, jj = 2 * s + (mi & 1);
+        ldsm_x4(sbase + P_KC + sw_chunk(row, jj, kC), b[0], b[1], b[2], b[3]);
+      }
+      const int c0 = 16 * s + (lane & 3) * 2;
+      const float2 d01 = *reinterpret_cast<const float2 *>(Dv + c0);
+      const float2 d89 = *reinterpret_cast<const float2 *>(Dv + c0 + 8);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 f = unpack_bf16(b[t]);
+        b[t] = (t & 1) ? pack_bf16(f.x * d89.x, f.y * d89.y) : pack_bf16(f.x * d01.x, f.y * d01.y);
+      }
+      mma16816(accL[0], ak, b[0], b[1]);
+      mma16816(accL[1], ak, b[2], b[3]);
+      mma16816(accQ[0], aq, b[0], b[1]);
+      mma16816(accQ[1], aq, b[2], b[3]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * R + (lane >> 2) + hh * 8;
+        const int i = 16 * I + nt * 8 + (lane & 3) * 2;
+        const float br = beta[r];
+        *reinterpret_cast<float2 *>(Lf + fsw(r, i)) = make_float2(br * accL[nt][2 * hh], br * accL[nt][2 * hh + 1]);
+        *reinterpret_cast<uint32_t *>(rec + kRecAQK + sw_off(r, i, kC)) = pack_bf16(accQ[nt][2 * hh], accQ[nt][2 * hh + 1]);
+      }
+    }
+  }
+  if (tid < 6 * 32) {  // Aqk blocks above the diagonal (R < I) are zero
+    const int b = tid >> 5, w = tid & 31;
+    const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
+    *reinterpret_cast<uint4 *>(rec + kRecAQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
+  }
+  if (warp >= 4) diag_direct(P, t0, len, h, j, warp - 4, beta, Lf, rec);
+  __syncthreads();
+  invert_store(sm, rec);
+}
+
+// kda_prep_tc_fix: the slots kda_prep_tc listed, walked by the CTAs, on the
+// exact path (with none listed every CTA reads the count and leaves).
+__global__ void __launch_bounds__(kThr, 3)
+kda_prep_tc_fix_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps) {
+  extern __shared__ unsigned char smraw[];
+  unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const int nfix = *(volatile const int *)(W.flags + 3);
+  if ((int)blockIdx.x >= nfix) return;
+  float *beta = (float *)(sm + P_BETA);
+  uint64_t *bar = (uint64_t *)(sm + P_MISC);
+  if (threadIdx.x == 0) {
+    bar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  uint32_t parity = 0;
+  for (int i = blockIdx.x; i < nfix; i += gridDim.x, parity ^= 1u) {
+    const int s = W.wide_rec[i];
+    const int c_idx = s / P.HV, j = s % P.HV, h = j / (P.HV / P.H);
+    const int4 ch = W.chunk[c_idx];
+    load_slot(P, maps, sm, bar, parity, err, ch.y, ch.z, h, j);
+    unsigned char *rec = W.tc_tiles + (size_t)s * kTileRecord;
+    fix_phase_a(sm, ch.z, beta, rec, P.l2norm);
+    fix_phase_b(sm, beta, rec, P, ch.y, ch.z, h, j);
+    __syncthreads();  // the shared tiles are free for the next slot
+  }
 }
 
 }  // namespace
@@ -538,8 +740,16 @@ KDA_PT_EXPORT(kda_debug_prep_phase_cycles)
 cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps, int *err, cudaStream_t s) {
   if (P.NC == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kda_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kda_prep_tc_fix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+  int nsm = 0;
+  if (e == cudaSuccess) e = sm_count(&nsm);
   if (e != cudaSuccess) return e;
   KDA_LAUNCH("kda_prep_tc", s, kda_prep_tc_kernel<<<dim3(P.NC, P.HV), kThr, P_SMEM, s>>>(P, W, err, maps));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t slots = (int64_t)P.NC * P.HV;
+  const unsigned grid = (unsigned)(slots < nsm ? slots : nsm);
+  KDA_LAUNCH("kda_prep_tc_fix", s, kda_prep_tc_fix_kernel<<<grid, kThr, P_SMEM, s>>>(P, W, err, maps));
   return cudaGetLastError();
 }
 

@@ -106,7 +106,7 @@ typedef struct kda_inputs {
   int N;            /* logical sequences: B when cu_seqlens is NULL, else len(cu_seqlens)-1   */
   kda_dtype dtype;  /* element type of q, k, v, o, dO, dq, dk, dv                            */
   const void *q, *k, *v;
-  const float *g;           /* per-token log2 decay (typically <= 0)                         */
+  const float *g;           /* per-token log2 decay: any finite value <= 0                    */
   const float *beta;        /* per (token, value head) write strength                        */
   const float *h0;          /* initial states [N][HV][K][V], or NULL for zeros               */
   const int32_t *cu_seqlens;/* device [N+1] packed offsets, or NULL for a dense batch         */
@@ -213,16 +213,24 @@ kda_status kda_state_compose(const float *M, const float *h, const float *c, flo
                              int V, int transpose, void *stream);
 
 /* Device status words of a call.  Every chunked call (forward, backward, any
- * variant) writes three int32 words into its workspace, at byte offset
+ * variant) writes five int32 words into its workspace, at byte offset
  * kda_status_offset() (the same for every workspace of the problem):
  *   [0] the number of 64-token chunks mapped;
  *   [1] nonzero if cu_seqlens was malformed (decreasing, negative or past the
  *       token axis): those sequences were treated as empty;
  *   [2] nonzero if a bounded device wait gave up (a copy or product never
- *       completed): the call's results are invalid.  Word 2 is cleared at the
- *       start of every call.
- * The library never reads them on the host: copy them out after the call (in
- * stream order) to check.  Returns SIZE_MAX for an invalid problem. */
+ *       completed): the call's results are invalid;
+ *   [3] the (chunk, value head) slots whose forward records took the exact
+ *       path for strong decays, and
+ *   [4] those whose per-chunk gradients took it (tensor-core path only).  The
+ *       kernels split each pairwise decay 2^(G_r - G_i) at references inside
+ *       16-token blocks; a block whose decay span (the sum of 15 consecutive
+ *       per-token gates of one channel) exceeds 192 (log2) is recomputed by a
+ *       second, slower launch that forms the block's terms exactly.  Results
+ *       are exact for any gate either way; the words only say where time went.
+ * Words 2, 3 and 4 are cleared at the start of every call.  The library never
+ * reads them on the host: copy them out after the call (in stream order) to
+ * check.  Returns SIZE_MAX for an invalid problem. */
 size_t kda_status_offset(const kda_inputs *in);
 
 /* Static description of a status code. */
@@ -231,10 +239,10 @@ const char *kda_status_string(kda_status s);
 /* Message describing the last failure on the calling thread ("" if none). */
 const char *kda_last_error(void);
 
-/* Library ABI version (major * 100 + minor): 104 (101: kda_inputs gained
+/* Library ABI version (major * 100 + minor): 105 (101: kda_inputs gained
  * `flags`; 102: the forward-context entry points; 103: the final-state-only
  * forward, the start-state-gradient-only backward, kda_chunk_fwd_reuse; 104:
- * kda_status_offset, kda_debug_bounded_wait). */
+ * kda_status_offset, kda_debug_bounded_wait; 105: status words 3 and 4). */
 int kda_version(void);
 
 /* Chunked forward without a caller workspace (no counterpart on the pages).

@@ -4,8 +4,9 @@ to the edges of their range.  Gates far below the workloads' clip at -5 (log2)
 give 16-token blocks whose decay span (the sum of 15 per-token gates) reaches
 hundreds: below the block factors' limit (192) the fast path carries them, above
 it the slot's diagonal blocks take the exact path.  Every case is checked
-against the fp64 oracle at the bf16 tolerances, and the device status word 3
-(slots on the exact path) tells which path ran."""
+against the fp64 oracle at the bf16 tolerances, and the device status words 3
+and 4 (slots the record and gradient kernels sent to the exact path) tell which
+path ran."""
 import zlib
 
 import numpy as np
@@ -45,8 +46,9 @@ def _check(inp, l2=False, expect_exact=None):
     gr = H.gpu_bwd(inp, want_dh0=inp.h0 is not None, l2=l2, status=sb)
     H.check_bwd(inp, gr, H.oracle_bwd(inp, l2=l2), tol["bwd"])
     if expect_exact is not None:
-        # forward: the record kernel; recompute backward: the record kernel again and the gradient kernel
-        assert (sf[3] > 0) == expect_exact and (sb[3] > 0) == expect_exact, (sf, sb)
+        # forward: the record kernel (word 3); recompute backward: the record kernel again and the
+        # gradient kernel (word 4)
+        assert (sf[3] > 0) == expect_exact and (sb[3] > 0) == expect_exact and (sb[4] > 0) == expect_exact, (sf, sb)
     return sf, sb
 
 
@@ -98,7 +100,7 @@ def test_ordinary_gates_stay_on_the_block_factors():
     inp = inputs.make_config(1)
     H.gpu_fwd(inp, status=sf)
     H.gpu_bwd(inp, status=sb)
-    assert sf[3] == 0 and sb[3] == 0, (sf, sb)
+    assert sf[3:] == [0, 0] and sb[3:] == [0, 0], (sf, sb)
 
 
 def test_wide_decays_dense_training_shape_sampled():
@@ -110,7 +112,7 @@ def test_wide_decays_dense_training_shape_sampled():
     sf, sb = [], []
     o, _ = H.gpu_fwd(inp, status=sf)
     gr = H.gpu_bwd(inp, want_dh0=False, status=sb)
-    assert sf[3] > 0 and sb[3] > 0
+    assert sf[3] > 0 and sb[3] > 0 and sb[4] > 0
     flat = lambda x: x.reshape(inp.B * inp.T, *x.shape[2:])  # noqa: E731
     for key in ("dq", "dk", "dv", "dg", "dbeta"):
         assert torch.isfinite(gr[key]).all(), key
