@@ -67,9 +67,29 @@ def algorithmic_flops(cfg, C=64):
     return per * cfg.valid_tokens * cfg.HV
 
 
+# Algorithmic bytes per launch of each tensor-core kernel, per token of the
+# layer: the step's own inputs it reads and outputs it writes (the cost model
+# above, split by kernel; intermediates such as the per-chunk records, saved
+# states and tiles are the implementation's cost and are not counted).  This
+# is what the dominant kernel's roofline divides by its time.
+def kernel_algorithmic_bytes_per_token(name, cfg):
+    e = 2 if cfg.dtype == torch.bfloat16 else 4
+    H, HV, K, V = cfg.H, cfg.HV, cfg.K, cfg.V
+    qk, vv, b = H * K * e, HV * V * e, 4 * HV
+    g = 4 * HV if cfg.g.dim() == 3 else 4 * HV * K
+    table = {
+        "kda_prep_tc": 2 * qk + g + b,                            # reads q, k, g, beta
+        "kda_fwd_tc": 2 * vv,                                     # reads v, writes o
+        "kda_fwd_tc_save": 2 * vv,
+        "kda_bwd_scan_tc": vv,                                    # reads dO
+        "kda_bwd_intra_tc": (2 * qk + vv + g + b + vv) + (2 * qk + vv + g + b),  # q k v g beta dO -> dq dk dv dg dbeta
+    }
+    return table.get(name)
+
+
 # Interface bytes per launch of each kernel (what the kernel must read and
-# write by its own contract), per token of the layer.  Used for the dominant
-# kernel's roofline.
+# write by its own contract, intermediates included), per token of the layer:
+# a diagnostic beside the algorithmic roofline, not a roofline.
 def kernel_bytes_per_token(name, cfg):
     e = 2 if cfg.dtype == torch.bfloat16 else 4
     H, HV, K, V = cfg.H, cfg.HV, cfg.K, cfg.V
@@ -114,9 +134,31 @@ NCU_TRAFFIC = {
         bytes_per_token=1281294592 / 8192,  # 974.5 MB read + 306.8 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_intra.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh",
                  "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="e0b0a192344717a07c01b1fbb5ea461f58c667d9e4fdedaf1608e9063bbb319a",
-        profile="profiles/ncu_full_kernels_B8_T1024_H32_K128.md"),
+        sha256="e0b0a192344717a07c01b1fbb5ea461f58c667d9e4fdedaf1608e9063bbb319a"),
 }
+
+
+def dominant_roofline(name, launch_ms, cfg, toks_launch, peaks):
+    """The dominant kernel's roofline object: achieved = its algorithmic bytes
+    per launch (kernel_algorithmic_bytes_per_token x the tokens one launch
+    covers) / its average launch time, against the measured HBM copy peak.
+    ``interface`` is the same kernel's bytes by its own contract, intermediates
+    included (a diagnostic), and ``traffic`` its ncu DRAM bytes per launch while
+    the capture matches the sources."""
+    abpt = kernel_algorithmic_bytes_per_token(name, cfg)
+    ibpt = kernel_bytes_per_token(name, cfg)
+    sec = launch_ms / 1e3
+    achieved = abpt * toks_launch / sec / 1e9 if abpt else None
+    return dict(kernel=name, bound="hbm", achieved=None if achieved is None else round(achieved, 1),
+                peak=peaks["hbm"], unit="GB/s",
+                frac=None if achieved is None else round(achieved / peaks["hbm"], 4),
+                algorithmic_bytes=None if abpt is None else int(round(abpt * toks_launch)),
+                traffic=measured_traffic(name, toks_launch), launch_ms=round(launch_ms, 4),
+                interface=None if ibpt is None else dict(
+                    bytes=int(round(ibpt * toks_launch)), GBps=round(ibpt * toks_launch / sec / 1e9, 1),
+                    frac=round(ibpt * toks_launch / sec / 1e9 / peaks["hbm"], 4)),
+                peak_source=f"{peaks['src']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["src"] == "measured"
+                else "fallback 6.8 TB/s")
 
 
 def sources_sha256(paths):
@@ -609,15 +651,7 @@ def main():
     per_step = {k: v[0] / steps_split for k, v in split.items()}
     dom = max(split, key=lambda k: split[k][0])
     dom_ms, dom_n = split[dom]
-    bpt = kernel_bytes_per_token(dom, cfg)
-    toks_launch = toks / max(1, args.cp_ranks)  # with context parallelism a launch covers one segment
-    achieved = (bpt * toks_launch / (dom_ms / dom_n / 1e3) / 1e9) if bpt else None
-    roof = dict(kernel=dom, bound="hbm", achieved=None if achieved is None else round(achieved, 1),
-                peak=peaks["hbm"], unit="GB/s",
-                frac=None if achieved is None else round(achieved / peaks["hbm"], 4),
-                traffic=measured_traffic(dom, toks_launch), launch_ms=round(dom_ms / dom_n, 4),
-                peak_source=f"{peaks['src']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["src"] == "measured"
-                else "fallback 6.8 TB/s")
+    roof = dominant_roofline(dom, dom_ms / dom_n, cfg, toks / max(1, args.cp_ranks), peaks)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_step, 4),

@@ -23,7 +23,7 @@ EXPORTS = (
     "kda_launch_count", "kda_timing_enable", "kda_timing_collect", "kda_chunk_fwd_noalloc",
     "kda_state_compose", "kda_chunk_ctx_size", "kda_chunk_fwd_ctx_workspace_size",
     "kda_chunk_bwd_ctx_workspace_size", "kda_chunk_fwd_ctx", "kda_chunk_bwd_ctx", "kda_chunk_fwd_reuse",
-    "kda_status_offset", "kda_debug_bounded_wait",
+    "kda_status_offset", "kda_debug_bounded_wait", "kda_uses_tensor_cores",
 )
 
 
@@ -75,6 +75,8 @@ def load(path: str = LIB_PATH):
             getattr(lib, nm).restype = i
         lib.kda_chunk_bwd_ctx.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_chunk_bwd_ctx.restype = i
+        lib.kda_uses_tensor_cores.argtypes = [P]
+        lib.kda_uses_tensor_cores.restype = ctypes.c_int
         lib.kda_status_offset.argtypes = [P]
         lib.kda_status_offset.restype = sz
         lib.kda_debug_bounded_wait.argtypes = [vp, ctypes.c_longlong, vp]

@@ -82,10 +82,7 @@ kda_status validate(const kda_inputs *in, Problem &P) {
   return KDA_OK;
 }
 
-bool use_tc(const Problem &P) {
-  const char *f = getenv("KDA_FORCE_SIMPLE");
-  return tc_eligible(P) && !(f != nullptr && f[0] == '1');
-}
+bool use_tc(const Problem &P) { return tc_eligible(P); }
 
 // The forward context of the tensor-core path: what a forward keeps for its
 // backward -- the per-chunk records and, per (chunk, value head) slot, the
@@ -440,5 +437,11 @@ const char *kda_status_string(kda_status s) {
 const char *kda_last_error(void) { return g_err; }
 
 int kda_version(void) { return 105; }
+
+int kda_uses_tensor_cores(const kda_inputs *in) {
+  Problem P{};
+  if (validate(in, P) != KDA_OK) return -1;
+  return use_tc(P) ? 1 : 0;
+}
 
 }  // extern "C"

@@ -12,8 +12,11 @@
 //
 // Usage rules:
 //  * The first call on each device looks the array's device address up
-//    (cudaGetSymbolAddress, with that device current) and caches it; make that
-//    first call before any CUDA-graph capture on the device.
+//    (cudaGetSymbolAddress, with that device current) and caches it for the
+//    life of the process; make that first call before any CUDA-graph capture
+//    on the device.  A device reset (cudaDeviceReset, or a reset of the
+//    primary context) after that first call is not supported: the module is
+//    reloaded and the cached address would no longer be the array's.
 //  * Every call shares the one array.  Calls whose work may overlap on the GPU
 //    (different streams, or different host threads, without ordering between
 //    them) race on it; order them on one stream.

@@ -233,6 +233,14 @@ kda_status kda_state_compose(const float *M, const float *h, const float *c, flo
  * check.  Returns SIZE_MAX for an invalid problem. */
 size_t kda_status_offset(const kda_inputs *in);
 
+/* Which kernels a call on these inputs runs: 1 for the tensor-core kernels
+ * (bf16, K = V = 128, with q, k, v and a per-channel g 16-byte aligned), 0 for
+ * the general fp32 kernels (same results, several times slower), -1 if the
+ * problem is invalid.  A bf16 K = V = 128 problem whose inputs are a slice of
+ * a larger tensor starting off a 16-byte boundary runs the general kernels:
+ * this tells the caller so before the call. */
+int kda_uses_tensor_cores(const kda_inputs *in);
+
 /* Static description of a status code. */
 const char *kda_status_string(kda_status s);
 
@@ -252,10 +260,11 @@ int kda_version(void);
  * scratch array that lives inside the library: 4 MiB of device memory per GPU
  * that loads it, held until the process exits.  Same arguments and results as
  * kda_chunk_fwd minus the workspace.  The first call on a device looks up the
- * array's address with that device current; make it before any CUDA-graph
- * capture.  All calls share the one array (it keeps the last call's contents;
- * nothing in it must start at zero), so calls that may overlap on the GPU race:
- * order them on one stream.  A problem whose workspace exceeds 4 MiB is
+ * array's address with that device current and keeps it for the life of the
+ * process; make it before any CUDA-graph capture, and do not reset the device
+ * (cudaDeviceReset) after it.  All calls share the one array (it keeps the
+ * last call's contents; nothing in it must start at zero), so calls that may
+ * overlap on the GPU race: order them on one stream.  A problem whose workspace exceeds 4 MiB is
  * rejected with KDA_ERR_WORKSPACE before anything is launched.  The library
  * allocates nothing on this path. */
 kda_status kda_chunk_fwd_noalloc(const kda_inputs *in, void *o, float *hT, void *stream);

@@ -253,3 +253,14 @@ def test_bounded_wait_probe_validation(lib):
     assert lib.kda_debug_bounded_wait(None, 100, None) == _lib.KDA_ERR_INVALID_ARG
     assert lib.kda_debug_bounded_wait(ctypes.c_void_p(0x1000), 0, None) == _lib.KDA_ERR_INVALID_ARG
     assert lib.kda_debug_bounded_wait(ctypes.c_void_p(0x1000), (1 << 24) + 1, None) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_kernel_family_query(lib):
+    """bf16 K = V = 128 with 16-byte aligned q, k, v, g runs the tensor-core
+    kernels; an fp32 problem, other head dims or a misaligned input the general ones."""
+    s = _inputs(K=128, V=128)
+    assert lib.kda_uses_tensor_cores(ctypes.byref(s)) == 1
+    assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs(K=128, V=128, dtype=_lib.KDA_F32))) == 0
+    assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs())) == 0  # K = V = 64
+    assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs(K=128, V=128, q=0x1002))) == 0
+    assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs(HV=3))) == -1

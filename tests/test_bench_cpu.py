@@ -1,8 +1,9 @@
 """The benchmark's roofline arithmetic, pinned on the host: the algorithmic
-bytes and flops of the dense training layer (per token and value head), the
-interface bytes per token that each tensor-core kernel's roofline divides by,
-and the rule that the measured DRAM traffic is reported only while the
-dominant kernel's sources match its capture."""
+bytes and flops of the dense training layer (per token and value head), each
+tensor-core kernel's share of them (what the dominant kernel's roofline
+divides by), its interface bytes (a diagnostic), and the rule that the
+measured DRAM traffic is reported only while the dominant kernel's sources
+match its capture."""
 import os
 import sys
 
@@ -41,6 +42,34 @@ def test_interface_bytes_per_token_of_the_tensor_core_kernels():
     for name, b in want.items():
         assert bench.kernel_bytes_per_token(name, cfg) == b, name
     assert bench.kernel_bytes_per_token("no_such_kernel", cfg) is None
+
+
+def test_algorithmic_bytes_per_token_of_the_tensor_core_kernels():
+    """The dominant kernel's roofline divides its share of the step's algorithmic
+    bytes: the gradient kernel reads q, k, v, g, beta, dO and writes dq, dk, dv,
+    dg, dbeta -- 90,368 bytes per token of the dense training layer."""
+    cfg = _layer()
+    assert bench.kernel_algorithmic_bytes_per_token("kda_bwd_intra_tc", cfg) == 90368
+    assert bench.kernel_algorithmic_bytes_per_token("kda_prep_tc", cfg) == 2 * 8192 + 16384 + 128
+    assert bench.kernel_algorithmic_bytes_per_token("kda_fwd_tc_save", cfg) == 2 * 8192
+    assert bench.kernel_algorithmic_bytes_per_token("kda_bwd_scan_tc", cfg) == 8192
+    # the forward kernels and the backward kernels together cover the step's bytes once each,
+    # except dO, which the reverse scan and the gradient kernel both read
+    step = bench.algorithmic_bytes(cfg)["per_token_head"] * cfg.HV
+    parts = sum(bench.kernel_algorithmic_bytes_per_token(k, cfg)
+                for k in ("kda_prep_tc", "kda_fwd_tc_save", "kda_bwd_scan_tc", "kda_bwd_intra_tc"))
+    assert parts == step + 8192
+
+
+def test_dominant_roofline_fraction_is_algorithmic_bytes_over_time():
+    cfg = _layer()
+    peaks = dict(hbm=6791.4, src="measured")
+    r = bench.dominant_roofline("kda_bwd_intra_tc", 1.866, cfg, 32768, peaks)
+    assert r["algorithmic_bytes"] == 90368 * 32768
+    assert abs(r["achieved"] - 90368 * 32768 / 1.866e-3 / 1e9) < 0.1
+    assert abs(r["frac"] - r["achieved"] / 6791.4) < 1e-4
+    assert 0.23 < r["frac"] < 0.24  # 2.96 GB in 1.866 ms on 6.79 TB/s
+    assert r["interface"]["bytes"] == 160000 * 32768
 
 
 def test_traffic_is_reported_only_for_the_captured_sources():

@@ -82,6 +82,56 @@ def test_state_relay_two_emulated_ranks(name, kw, dtype, split, keep):
     Hh.assert_rel("dh0", res[0][2][5].numpy(), rg["dh0"], tol["bwd"])
 
 
+def _run_ranks(d, inp, segs, keep=True):
+    world = len(segs)
+    tg = ThreadGather(world)
+    res = [None] * world
+    errors = []
+
+    def rank_fn(rank):
+        try:
+            s = segs[rank]
+            q, k, v, g, beta, do = (x[:, s].contiguous() for x in (d.q, d.k, d.v, d.g, d.beta, d.do))
+            gather = tg.for_rank(rank)
+            o, hT, seg = cp.cp_forward(q, k, v, g, beta, d.h0 if rank == 0 else None, rank, gather,
+                                       keep_context=keep)
+            grads = cp.cp_backward(q, k, v, g, beta, seg if keep else seg.h_start, do,
+                                   d.dhT if rank == world - 1 else None, rank, world, gather)
+            torch.cuda.synchronize()
+            res[rank] = (o.cpu(), hT.cpu(), [t.cpu() for t in grads])
+        except Exception as e:  # surfaced after the join
+            errors.append(e)
+            tg.bar.abort()
+
+    ths = [threading.Thread(target=rank_fn, args=(r,)) for r in range(world)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    assert not errors, errors
+    return res
+
+
+def test_state_relay_two_ranks_long_context_sampled():
+    """The long-context workload (T = 65,536, H = HV = 16, near-1 decays) split
+    between two emulated ranks; the oracle checks sampled value heads of the
+    unsplit sequence at the bf16 tolerances."""
+    inp = inputs.make_config(3)
+    d = inp.to("cuda")
+    half = inp.T // 2
+    res = _run_ranks(d, inp, [slice(0, half), slice(half, inp.T)])
+    tol = Hh.TOL[inp.dtype]
+    for n, hq, js, t0, t1, (ro, rhT), rg in Hh.sample_units(inp, [(0, 3)]):
+        o = torch.cat([res[0][0], res[1][0]], dim=1)[0]
+        Hh.assert_rel("o", o[t0:t1][:, js].double().numpy(), ro[0], tol["fwd"])
+        Hh.assert_rel("hT", res[1][1][n][js].double().numpy(), rhT[0], tol["fwd"])
+        for idx, key in enumerate(("dq", "dk", "dv", "dg", "dbeta")):
+            got = torch.cat([res[0][2][idx], res[1][2][idx]], dim=1)[0]
+            got = got[t0:t1, hq:hq + 1] if key in ("dq", "dk") else got[t0:t1][:, js]
+            Hh.assert_rel(key, got.double().numpy(), rg[key][0], tol["bwd"])
+        Hh.assert_rel("dh0", res[0][2][5][n][js].double().numpy(), rg["dh0"][0], tol["bwd"])
+
+
 @pytest.mark.parametrize("K,V", [(128, 128), (64, 48), (3, 5)])
 @pytest.mark.parametrize("transpose", [False, True])
 def test_state_compose_matches_fp64(K, V, transpose):

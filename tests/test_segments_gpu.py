@@ -53,3 +53,27 @@ def test_chunk_kda_autograd_with_segments():
     for name, a, b in zip(("o", "dq", "dk", "dv", "dg", "dbeta", "dh0"), outs[0], outs[1]):
         rel = ((a - b).norm() / b.norm()).item()
         assert rel < 1e-2, (name, rel)
+
+
+def test_long_context_sixteen_segments_sampled():
+    """The long-context workload (T = 65,536, H = HV = 16, near-1 decays) split
+    into 16 segments: 15 state compositions in each direction, with the
+    transitions on the bf16 tensor-core path.  The oracle checks sampled value
+    heads of the unsplit sequence, at the bf16 tolerances, for o, hT and every
+    gradient."""
+    from gated_delta_rule_42_gb300.segments import chunk_kda_bwd_segmented, chunk_kda_fwd_segmented
+    inp = inputs.make_config(3)
+    d = inp.to("cuda")
+    o, hT, ctx = chunk_kda_fwd_segmented(d.q, d.k, d.v, d.g, d.beta, d.h0, 16, True)
+    dq, dk, dv, dg, db, dh0 = chunk_kda_bwd_segmented(d.q, d.k, d.v, d.g, d.beta, ctx, d.do, d.dhT)
+    torch.cuda.synchronize()
+    tol = H.TOL[inp.dtype]
+    flat = lambda x: x.reshape(inp.B * inp.T, *x.shape[2:]).cpu()  # noqa: E731
+    for n, hq, js, t0, t1, (ro, rhT), rg in H.sample_units(inp, [(0, 5), (0, 12)]):
+        H.assert_rel(f"o[{hq}]", flat(o)[t0:t1][:, js].double().numpy(), ro[0], tol["fwd"])
+        H.assert_rel(f"hT[{hq}]", hT[n][js].cpu().double().numpy(), rhT[0], tol["fwd"])
+        for key, x in (("dq", dq), ("dk", dk)):
+            H.assert_rel(f"{key}[{hq}]", flat(x)[t0:t1, hq:hq + 1].double().numpy(), rg[key][0], tol["bwd"])
+        for key, x in (("dv", dv), ("dg", dg), ("dbeta", db)):
+            H.assert_rel(f"{key}[{hq}]", flat(x)[t0:t1][:, js].double().numpy(), rg[key][0], tol["bwd"])
+        H.assert_rel(f"dh0[{hq}]", dh0[n][js].cpu().double().numpy(), rg["dh0"][0], tol["bwd"])
