@@ -128,11 +128,68 @@ def gate_grad_reduce(dg):
     return np.sum(np.asarray(dg, dtype=np.float64), axis=-1)
 
 
+# The KDA gate inside the op ("[Fix] Use unit KDA gate scale when A_log is
+# omitted", fla-org/flash-linear-attention PR #1294, Summary and Breaking
+# changes; its commit log's "[Fix] Reduce GDN/KDA gate bias gradients before
+# downcasting").  The pages name the pieces -- a decay scale exp(A_log) per
+# value head, unit when A_log is omitted (the same as an explicit zero A_log;
+# an explicit ones tensor reproduces the former exp(1) scale), a gate bias
+# whose gradient is reduced over tokens in fp32, bounded and unbounded gate
+# formulas -- but print no formula.  Reading: with x = a + bias (the raw
+# pre-activation plus a per (value head, channel) bias) and s = exp(A_log),
+#   unbounded: g = -s softplus(x)            (g <= 0)
+#   bounded:   g = lower_bound sigmoid(s x)  (lower_bound < g < 0)
+# and g is the per-token log2 decay the recurrence takes ("kda in torchtitan
+# (training)" calls the output of its bounded gate the per-token log2 decay).
+def _softplus(x):
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def _sigmoid(x):
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def _gate_parts(a, A_log, bias, HV):
+    a = np.asarray(a, dtype=np.float64)
+    s = np.ones(HV) if A_log is None else np.exp(np.asarray(A_log, dtype=np.float64))
+    x = a if bias is None else a + np.asarray(bias, dtype=np.float64)  # bias [HV, K] broadcasts over tokens
+    return x, s[:, None]
+
+
+def kda_gate(a, A_log=None, bias=None, lower_bound=None):
+    """Raw gate pre-activations a [B,T,HV,K] -> per-token log2 decay g."""
+    x, s = _gate_parts(a, A_log, bias, np.shape(a)[2])
+    if lower_bound is None:
+        return -s * _softplus(x)
+    return lower_bound * _sigmoid(s * x)
+
+
+def kda_gate_bwd(a, dg, A_log=None, bias=None, lower_bound=None):
+    """Gradients of the gate given dg = dL/dg: (da [B,T,HV,K], dA_log [HV],
+    dbias [HV,K]); the parameter gradients are sums over every token."""
+    x, s = _gate_parts(a, A_log, bias, np.shape(a)[2])
+    dg = np.asarray(dg, dtype=np.float64)
+    if lower_bound is None:
+        dx = -s * _sigmoid(x)          # d/dx of -s softplus(x)
+        ds = -s * _softplus(x)         # d/dA_log of -exp(A_log) softplus(x)
+    else:
+        sg = _sigmoid(s * x)
+        dx = lower_bound * sg * (1.0 - sg) * s
+        ds = lower_bound * sg * (1.0 - sg) * s * x
+    da = dg * dx
+    return da, np.sum(dg * ds, axis=(0, 1, 3)), np.sum(da, axis=(0, 1))
+
+
 def kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, output_final_state=True, nthreads=0,
-            qk_l2norm=False, scalar_gate=False):
+            qk_l2norm=False, scalar_gate=False, gate=None):
     """Token-by-token KDA forward.  Returns (o [B,T,HV,V], hT [N,HV,K,V] or None).
     With qk_l2norm, q and k rows are normalised first (:func:`l2norm_rows`);
-    with scalar_gate, g is [B,T,HV] (:func:`gate_per_channel`)."""
+    with scalar_gate, g is [B,T,HV] (:func:`gate_per_channel`); with gate (a
+    dict of :func:`kda_gate`'s A_log, bias, lower_bound), g holds the raw
+    pre-activations and the gate makes the decay first."""
+    if gate is not None:
+        g = kda_gate(g, **gate)
     if qk_l2norm:
         q, k = l2norm_rows(q), l2norm_rows(k)
     if scalar_gate:
@@ -153,11 +210,17 @@ def kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, output_final_state=True,
 
 
 def kda_bwd(q, k, v, g, beta, h0, do, dhT, cu_seqlens=None, nthreads=0, qk_l2norm=False,
-            scalar_gate=False):
+            scalar_gate=False, gate=None):
     """Token-by-token KDA backward.  Returns dict dq, dk, dv, dg, dbeta, dh0.
     With qk_l2norm, the gradients of the normalised rows are carried back
     through :func:`l2norm_rows` to the raw q and k; with scalar_gate, g and dg
-    are [B,T,HV] (:func:`gate_grad_reduce`)."""
+    are [B,T,HV] (:func:`gate_grad_reduce`); with gate, dg is the gradient of
+    the raw pre-activations, and dA_log, dbias are added (:func:`kda_gate_bwd`)."""
+    if gate is not None:
+        out = kda_bwd(q, k, v, kda_gate(g, **gate), beta, h0, do, dhT, cu_seqlens, nthreads, qk_l2norm,
+                      scalar_gate)
+        out["dg"], out["dA_log"], out["dbias"] = kda_gate_bwd(g, out["dg"], **gate)
+        return out
     if scalar_gate:
         out = kda_bwd(q, k, v, gate_per_channel(g, np.shape(q)[-1]), beta, h0, do, dhT, cu_seqlens, nthreads,
                       qk_l2norm)

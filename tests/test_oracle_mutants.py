@@ -1,7 +1,8 @@
 """The oracle's pins must catch plausible mistakes.  Each case plants one
 mistake in a copy of the C oracle (on the CPU) and loads it in place of the
-real one, or, for the numpy q/k L2-norm prologue, replaces one of the oracle's
-functions; then it runs the pins, and at least one pin must fail."""
+real one, or, for the numpy q/k L2-norm prologue, the scalar gate and the KDA
+gate, replaces one of the oracle's functions; then it runs the pins, and at
+least one pin must fail."""
 import ctypes
 import os
 import subprocess
@@ -148,4 +149,57 @@ def test_scalar_gate_pins_catch_planted_mistake(attr, fn, monkeypatch):
             pin()
         except AssertionError:
             caught.append(pin.__name__)
+    assert caught, f"no pin caught {fn.__name__}"
+
+
+# The KDA gate lives in numpy too: planted mistakes in its forward and backward.
+def _gate_omitted_scale_e(a, A_log=None, bias=None, lower_bound=None):  # the behaviour the page's fix removed
+    return _REAL_GATE(a, np.ones(np.shape(a)[2]) if A_log is None else A_log, bias, lower_bound)
+
+
+def _gate_bounded_scale_outside(a, A_log=None, bias=None, lower_bound=None):
+    if lower_bound is None:
+        return _REAL_GATE(a, A_log, bias, None)
+    s = 1.0 if A_log is None else np.exp(np.asarray(A_log))[:, None]
+    x = a if bias is None else a + bias
+    return s * lower_bound / (1.0 + np.exp(-x))
+
+
+def _gate_bwd_no_scale(a, dg, A_log=None, bias=None, lower_bound=None):
+    da, dA, db = _REAL_GATE_BWD(a, dg, A_log, bias, lower_bound)
+    s = np.ones((np.shape(a)[2], 1)) if A_log is None else np.exp(np.asarray(A_log))[:, None]
+    return da / s, dA, db / s
+
+
+def _gate_bwd_bias_summed_over_channels(a, dg, A_log=None, bias=None, lower_bound=None):
+    da, dA, db = _REAL_GATE_BWD(a, dg, A_log, bias, lower_bound)
+    return da, dA, np.broadcast_to(np.sum(da, axis=(0, 1, 3))[:, None], db.shape).copy()
+
+
+def _gate_bwd_dA_sign(a, dg, A_log=None, bias=None, lower_bound=None):
+    da, dA, db = _REAL_GATE_BWD(a, dg, A_log, bias, lower_bound)
+    return da, -dA, db
+
+
+_REAL_GATE, _REAL_GATE_BWD = oracle.kda_gate, oracle.kda_gate_bwd
+KDA_GATE_MUTANTS = [("kda_gate", _gate_omitted_scale_e), ("kda_gate", _gate_bounded_scale_outside),
+                    ("kda_gate_bwd", _gate_bwd_no_scale), ("kda_gate_bwd", _gate_bwd_bias_summed_over_channels),
+                    ("kda_gate_bwd", _gate_bwd_dA_sign)]
+
+
+def _kda_gate_pins():
+    return [lambda: pins.test_gate_omitted_A_log_is_zero_A_log_bitwise(None), pins.test_gate_closed_forms,
+            lambda: pins.test_gate_finite_differences(None),
+            lambda: pins.test_gate_finite_differences(-5.0), lambda: pins.test_gate_layer_finite_differences(-3.0)]
+
+
+@pytest.mark.parametrize("attr,fn", KDA_GATE_MUTANTS, ids=[m[1].__name__ for m in KDA_GATE_MUTANTS])
+def test_kda_gate_pins_catch_planted_mistake(attr, fn, monkeypatch):
+    monkeypatch.setattr(oracle, attr, fn)
+    caught = 0
+    for pin in _kda_gate_pins():
+        try:
+            pin()
+        except AssertionError:
+            caught += 1
     assert caught, f"no pin caught {fn.__name__}"

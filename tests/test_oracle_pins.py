@@ -417,3 +417,143 @@ def test_scalar_gate_finite_differences():
         key = "dbeta" if name == "beta" else "dh0" if name == "h0" else "d" + name
         err = np.max(np.abs(fd - gr[key])) / max(1.0, np.max(np.abs(fd)))
         assert err < 1e-7, (name, err)
+
+
+# ---- the KDA gate inside the op (oracle.kda_gate / kda_gate_bwd) ----
+
+def _gate_inputs(rng, T=5, HV=2, K=3):
+    a = 2.0 * rng.standard_normal((1, T, HV, K))
+    A_log = 0.5 * rng.standard_normal(HV)
+    bias = rng.standard_normal((HV, K))
+    return a, A_log, bias
+
+
+@pytest.mark.parametrize("lower_bound", [None, -5.0], ids=["unbounded", "bounded"])
+def test_gate_omitted_A_log_is_zero_A_log_bitwise(lower_bound):
+    """[Fix] Use unit KDA gate scale when A_log is omitted: omitting A_log is the
+    same as passing an explicit zero A_log, for the gate and for the whole layer."""
+    rng = np.random.default_rng(41)
+    a, _, bias = _gate_inputs(rng)
+    z = np.zeros(a.shape[2])
+    assert np.array_equal(oracle.kda_gate(a, None, bias, lower_bound), oracle.kda_gate(a, z, bias, lower_bound))
+    q, k, v, _, beta = rand_problem(rng, 1, a.shape[1], 1, a.shape[2], a.shape[3], 2)
+    h0 = rng.standard_normal((1, a.shape[2], a.shape[3], 2))
+    W, Wh = rng.standard_normal(v.shape), rng.standard_normal(h0.shape)
+    g1 = dict(bias=bias, lower_bound=lower_bound)
+    g2 = dict(A_log=z, bias=bias, lower_bound=lower_bound)
+    o1, h1 = oracle.kda_fwd(q, k, v, a, beta, h0, gate=g1)
+    o2, h2 = oracle.kda_fwd(q, k, v, a, beta, h0, gate=g2)
+    assert np.array_equal(o1, o2) and np.array_equal(h1, h2)
+    r1 = oracle.kda_bwd(q, k, v, a, beta, h0, W, Wh, gate=g1)
+    r2 = oracle.kda_bwd(q, k, v, a, beta, h0, W, Wh, gate=g2)
+    for key in r1:
+        assert np.array_equal(r1[key], r2[key]), key
+
+
+def test_gate_closed_forms():
+    """Values the formulas fix: softplus(0) = ln 2 and sigmoid(0) = 1/2; an
+    explicit ones A_log gives the scale e (the former default); far from 0 the
+    unbounded gate tends to -s x and to 0, the bounded one to its bound and to 0;
+    the bias only shifts the argument; the unbounded gate scales with exp(A_log)."""
+    HV, K = 2, 3
+    zero = np.zeros((1, 1, HV, K))
+    ln2 = math.log(2.0)
+    np.testing.assert_allclose(oracle.kda_gate(zero), -ln2, rtol=1e-15)
+    np.testing.assert_allclose(oracle.kda_gate(zero, np.ones(HV)), -math.e * ln2, rtol=1e-15)
+    np.testing.assert_allclose(oracle.kda_gate(zero, lower_bound=-5.0), -2.5, rtol=1e-15)
+    np.testing.assert_allclose(oracle.kda_gate(zero, np.array([0.3, -1.0]), lower_bound=-5.0), -2.5, rtol=1e-15)
+    big = np.full((1, 1, HV, K), 40.0)
+    A = np.array([0.2, -0.4])
+    per_head = lambda x: np.broadcast_to(np.asarray(x)[:, None], big.shape)  # noqa: E731
+    np.testing.assert_allclose(oracle.kda_gate(big, A), per_head(-np.exp(A) * 40.0), rtol=1e-15)
+    np.testing.assert_allclose(oracle.kda_gate(big, A, lower_bound=-3.0), -3.0, rtol=1e-10)  # within e^(-40 s)
+    np.testing.assert_allclose(oracle.kda_gate(-big, A), per_head(-np.exp(A) * math.exp(-40.0)), rtol=1e-12)
+    np.testing.assert_allclose(oracle.kda_gate(-big, A, lower_bound=-3.0),
+                               per_head(-3.0 * np.exp(-40.0 * np.exp(A))), rtol=1e-10)  # to e^(-40 s)
+    rng = np.random.default_rng(42)
+    a, A_log, bias = _gate_inputs(rng, 4, HV, K)
+    np.testing.assert_allclose(oracle.kda_gate(a, A_log, bias), oracle.kda_gate(a + bias, A_log), rtol=0, atol=0)
+    np.testing.assert_allclose(oracle.kda_gate(a, A_log), np.exp(A_log)[:, None] * oracle.kda_gate(a), rtol=1e-14)
+
+
+def test_gate_ranges():
+    rng = np.random.default_rng(43)
+    a, A_log, bias = _gate_inputs(rng, 50, 2, 4)
+    a *= 5.0
+    gu = oracle.kda_gate(a, A_log, bias)
+    gb = oracle.kda_gate(a, A_log, bias, lower_bound=-4.0)
+    assert np.all(gu < 0) and np.all(gb < 0) and np.all(gb > -4.0)
+
+
+@pytest.mark.parametrize("lower_bound", [None, -5.0], ids=["unbounded", "bounded"])
+def test_gate_finite_differences(lower_bound):
+    """Central differences of L = sum(g W) w.r.t. a, A_log and bias."""
+    rng = np.random.default_rng(44)
+    a, A_log, bias = _gate_inputs(rng)
+    W = rng.standard_normal(a.shape)
+    da, dA, db = oracle.kda_gate_bwd(a, W, A_log, bias, lower_bound)
+    h = 1e-6
+    for arr, ref in ((a, da), (A_log, dA), (bias, db)):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = np.sum(oracle.kda_gate(a, A_log, bias, lower_bound) * W)
+            arr[idx] = old - h
+            lm = np.sum(oracle.kda_gate(a, A_log, bias, lower_bound) * W)
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.max(np.abs(fd - ref)) / max(1.0, np.max(np.abs(fd))) < 1e-8
+
+
+@pytest.mark.parametrize("lower_bound", [None, -3.0], ids=["unbounded", "bounded"])
+def test_gate_layer_finite_differences(lower_bound):
+    """The layer with the gate inside: central differences of the raw gate, A_log
+    and the bias through the whole recurrence (GVA, an empty slot), so the core's
+    dg reaches the gate and the parameter gradients sum over the valid tokens."""
+    rng = np.random.default_rng(45)
+    T, H, HV, K, V = 6, 1, 2, 3, 2
+    q, k, v, _, beta = rand_problem(rng, 1, T, H, HV, K, V)
+    a, A_log, bias = _gate_inputs(rng, T, HV, K)
+    cu = [0, 2, 2, 5]  # an empty slot and a capacity tail (token 5)
+    h0 = rng.standard_normal((3, HV, K, V))
+    W = rng.standard_normal((1, T, HV, V))
+    Wh = rng.standard_normal((3, HV, K, V))
+
+    def loss():
+        gate = dict(A_log=A_log, bias=bias, lower_bound=lower_bound)
+        o, hT = oracle.kda_fwd(q, k, v, a, beta, h0, cu, nthreads=1, gate=gate)
+        return float(np.sum(o[:, :5] * W[:, :5]) + np.sum(hT * Wh))
+
+    gr = oracle.kda_bwd(q, k, v, a, beta, h0, W * (np.arange(T) < 5)[None, :, None, None], Wh, cu, nthreads=1,
+                        gate=dict(A_log=A_log, bias=bias, lower_bound=lower_bound))
+    h = 1e-6
+    for arr, ref in ((a, gr["dg"]), (A_log, gr["dA_log"]), (bias, gr["dbias"])):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = loss()
+            arr[idx] = old - h
+            lm = loss()
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.max(np.abs(fd - ref)) / max(1.0, np.max(np.abs(fd))) < 1e-7
+
+
+@pytest.mark.parametrize("lower_bound", [None, -5.0], ids=["unbounded", "bounded"])
+def test_gate_matches_torch_autograd(lower_bound):
+    """torch.nn.functional's softplus / sigmoid with autograd, in fp64."""
+    rng = np.random.default_rng(46)
+    a, A_log, bias = _gate_inputs(rng)
+    W = rng.standard_normal(a.shape)
+    ta, tA, tb = (torch.tensor(x, requires_grad=True) for x in (a, A_log, bias))
+    s = torch.exp(tA)[:, None]
+    x = ta + tb
+    g = -s * torch.nn.functional.softplus(x) if lower_bound is None else lower_bound * torch.sigmoid(s * x)
+    (g * torch.tensor(W)).sum().backward()
+    np.testing.assert_allclose(oracle.kda_gate(a, A_log, bias, lower_bound), g.detach().numpy(), rtol=1e-14)
+    da, dA, db = oracle.kda_gate_bwd(a, W, A_log, bias, lower_bound)
+    np.testing.assert_allclose(da, ta.grad.numpy(), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dA, tA.grad.numpy(), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(db, tb.grad.numpy(), rtol=1e-12, atol=1e-15)
