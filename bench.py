@@ -258,7 +258,15 @@ class Runner:
         self.dev = device
         d = cfg.to(device)
         self.d = d
-        self.s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, qk_l2norm)
+        gate = None  # the KDA gate inside the op: g holds raw pre-activations
+        self.dA = self.dbias = None
+        if d.meta.get("raw_gate"):
+            from gated_delta_rule_42_gb300.ops import KdaGateParams
+            gate = KdaGateParams(d.A_log, d.g_bias, d.lower_bound)
+            self.dA = None if d.A_log is None else torch.empty_like(d.A_log)
+            self.dbias = None if d.g_bias is None else torch.empty_like(d.g_bias)
+        self.s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, qk_l2norm, gate, self.dA,
+                                    self.dbias)
         s = self.s
         self.o = torch.empty_like(d.v)
         self.hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=device)
@@ -542,6 +550,9 @@ def main():
                     help="the same layer with the q/k L2-norm prologue inside the op")
     ap.add_argument("--scalar-gate", action="store_true",
                     help="the same layer with a scalar gate g [B, T, HV] (the GDN variant)")
+    ap.add_argument("--kda-gate", action="store_true",
+                    help="the same layer with the KDA gate inside the op (raw gate, A_log and bias in, their "
+                         "gradients out; unbounded)")
     ap.add_argument("--cp-ranks", type=int, default=0,
                     help="context parallelism: split every sequence into this many segments and run the state "
                          "relay, the ranks serialized on this GPU (measures the relay's per-rank work)")
@@ -576,7 +587,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    if args.seq_len is not None or args.scalar_gate:  # the same shape with another T, or a scalar gate
+    if args.seq_len is not None or args.scalar_gate or args.kda_gate:  # another T, a scalar gate, the KDA gate
         name, kw = inputs.CONFIGS[args.config]
         if args.seq_len is not None:
             assert kw.get("cu_seqlens") is None and "T" in kw, "--seq-len needs a dense configuration"
@@ -585,6 +596,9 @@ def main():
         if args.scalar_gate:
             kw = dict(kw, scalar_gate=True)
             name = f"{name}_scalar_gate"
+        if args.kda_gate:
+            kw = dict(kw, raw_gate=True)
+            name = f"{name}_kda_gate"
         cfg = inputs.make_inputs(seed=1000 + args.config + 7919 * rank, name=name, **kw)
     else:
         cfg = inputs.make_config(args.config, seed=1000 + args.config + 7919 * rank)
@@ -662,6 +676,7 @@ def main():
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": f"inputs {ab['fwd'] / 1e9:.2f} GB read per step > L2 (no flush)",
                    "qk_l2norm": bool(args.qk_l2norm), "scalar_gate": bool(args.scalar_gate),
+                   "kda_gate": bool(args.kda_gate),
                    "backward": "recompute" if args.recompute else "forward context kept",
                    "forward_context_bytes": int(runner.ctx_bytes),
                    **({"cp_ranks": args.cp_ranks, "cp": "sequences split into cp_ranks segments, state relay, "

@@ -16,6 +16,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUD
 KDA_F32, KDA_BF16 = 0, 1
 KDA_QK_L2NORM = 1  # kda_inputs.flags bit: q/k rows L2-normalised inside the op
 KDA_SCALAR_GATE = 2  # kda_inputs.flags bit: g, dg are [B, T, HV] (one decay per token and value head)
+KDA_GATE_IN_KERNEL = 4  # kda_inputs.flags bit: g holds the raw gate, the op makes the decay (kda_inputs.gate)
 
 EXPORTS = (
     "kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_chunk_bwd_workspace_size",
@@ -27,6 +28,13 @@ EXPORTS = (
 )
 
 
+class KdaGate(ctypes.Structure):
+    _fields_ = [
+        ("A_log", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("lower_bound", ctypes.c_float),
+        ("dA_log", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
+    ]
+
+
 class KdaInputs(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("HV", ctypes.c_int),
@@ -34,6 +42,7 @@ class KdaInputs(ctypes.Structure):
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
         ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
         ("cu_seqlens", ctypes.c_void_p), ("flags", ctypes.c_int),
+        ("gate", ctypes.POINTER(KdaGate)),
     ]
 
 

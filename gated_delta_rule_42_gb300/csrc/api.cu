@@ -40,8 +40,15 @@ kda_status validate(const kda_inputs *in, Problem &P) {
   if (in->HV > 65535) return fail(KDA_ERR_UNSUPPORTED, "HV=%d above 65535", in->HV);
   if (in->dtype != KDA_F32 && in->dtype != KDA_BF16)
     return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)in->dtype);
-  if ((in->flags & ~(int)(KDA_QK_L2NORM | KDA_SCALAR_GATE)) != 0)
+  if ((in->flags & ~(int)(KDA_QK_L2NORM | KDA_SCALAR_GATE | KDA_GATE_IN_KERNEL)) != 0)
     return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", (unsigned)in->flags);
+  if ((in->flags & KDA_GATE_IN_KERNEL) != 0) {
+    if (in->gate == nullptr) return fail(KDA_ERR_INVALID_ARG, "KDA_GATE_IN_KERNEL needs gate parameters");
+    if ((in->flags & KDA_SCALAR_GATE) != 0)
+      return fail(KDA_ERR_UNSUPPORTED, "KDA_GATE_IN_KERNEL is not combined with KDA_SCALAR_GATE");
+    const float lb = in->gate->lower_bound;
+    if (!(lb <= 0.f) || lb < -3.0e38f) return fail(KDA_ERR_INVALID_ARG, "gate lower_bound must be finite and <= 0");
+  }
   const int64_t Ttot = (int64_t)in->B * in->T;
   if (Ttot * (in->HV > in->H ? in->HV : in->H) * kMaxDim >= ((int64_t)1 << 46))
     return fail(KDA_ERR_UNSUPPORTED, "problem too large");
@@ -84,6 +91,13 @@ kda_status validate(const kda_inputs *in, Problem &P) {
 
 bool use_tc(const Problem &P) { return tc_eligible(P); }
 
+// The KDA gate's parameters of a validated call (on == false without KDA_GATE_IN_KERNEL).
+GateArgs gate_args(const kda_inputs *in) {
+  GateArgs ga{nullptr, nullptr, 0.f, false};
+  if ((in->flags & KDA_GATE_IN_KERNEL) != 0) ga = GateArgs{in->gate->A_log, in->gate->bias, in->gate->lower_bound, true};
+  return ga;
+}
+
 // The forward context of the tensor-core path: what a forward keeps for its
 // backward -- the per-chunk records and, per (chunk, value head) slot, the
 // chunk-start state and the X^T, D^T tiles -- so that the backward runs
@@ -107,7 +121,7 @@ size_t ctx_layout(const Problem &P, char *base, Workspace *W) {
 // Workspace regions, in order.  Returns the total size; with base != NULL
 // also fills W.  With with_ctx the regions the forward context holds are
 // left out (ctx_layout points W at them).
-size_t layout(const Problem &P, bool backward, bool with_ctx, char *base, Workspace *W) {
+size_t layout(const Problem &P, bool kgate, bool backward, bool with_ctx, char *base, Workspace *W) {
   const size_t slots = (size_t)P.NC * P.HV;
   const size_t K = P.K, V = P.V, C = kChunk;
   size_t off = 0;
@@ -125,9 +139,13 @@ size_t layout(const Problem &P, bool backward, bool with_ctx, char *base, Worksp
     w.wide_rec = (int *)take(sizeof(int) * (slots > 0 ? slots : 1));
     if (backward) w.wide_grad = (int *)take(sizeof(int) * (slots > 0 ? slots : 1));
   }
-  if (P.scalar_gate && !use_tc(P)) {  // fp32 path: the gate repeated over K (and its per-channel gradient)
+  if ((P.scalar_gate || kgate) && !use_tc(P)) {  // fp32 path: the decay per channel (and its gradient)
     w.gx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
     if (backward) w.dgx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
+  }
+  if (kgate && use_tc(P) && backward) {  // per-slot fp32 partials of the gate's parameter gradients
+    w.gpart_b = (float *)take(sizeof(float) * slots * K);
+    w.gpart_a = (float *)take(sizeof(float) * slots);
   }
   if (use_tc(P)) {
     if (!with_ctx) w.tc_tiles = (unsigned char *)take(kTileRecord * slots);  // per-chunk records of the preparation kernel
@@ -174,9 +192,11 @@ size_t layout(const Problem &P, bool backward, bool with_ctx, char *base, Worksp
 // With a scalar gate the fp32 chunked kernels read the gate repeated over K
 // from the workspace; the tensor-core kernels and the recurrent kernel read
 // the scalars directly.
-cudaError_t gate_per_channel(const Problem &P, const Workspace &W, Problem *Pg, cudaStream_t s) {
-  if (!P.scalar_gate || use_tc(P)) return cudaSuccess;  // the tensor-core kernels broadcast the scalars themselves
-  cudaError_t e = launch_gate_expand(P, W.gx, s);
+// With the KDA gate the fp32 kernels read the decay made from the raw gate; the
+// tensor-core kernels make it themselves.
+cudaError_t gate_per_channel(const Problem &P, const GateArgs &ga, const Workspace &W, Problem *Pg, cudaStream_t s) {
+  if ((!P.scalar_gate && !ga.on) || use_tc(P)) return cudaSuccess;
+  cudaError_t e = ga.on ? launch_kgate_apply(P, ga, W.gx, s) : launch_gate_expand(P, W.gx, s);
   Pg->g = W.gx;
   return e;
 }
@@ -208,6 +228,7 @@ kda_status chunk_fwd(const kda_inputs *in, void *o, float *hT, void *ctx, size_t
   Problem P{};
   kda_status st = validate(in, P);
   if (st != KDA_OK) return st;
+  const GateArgs ga = gate_args(in);
   if (P.Ttot > 0 && o == nullptr && hT == nullptr)
     return fail(KDA_ERR_INVALID_ARG, "o and hT are NULL (o NULL: the final state alone, which needs hT)");
   if (use_tc(P) && ((uintptr_t)o & 15) != 0)
@@ -215,19 +236,19 @@ kda_status chunk_fwd(const kda_inputs *in, void *o, float *hT, void *ctx, size_t
   const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
   with_ctx = need_ctx > 0;
   if ((st = check_ws(need_ctx, ctx, ctx_bytes, "forward context")) != KDA_OK) return st;
-  const size_t need = layout(P, false, with_ctx, nullptr, nullptr);
+  const size_t need = layout(P, ga.on, false, with_ctx, nullptr, nullptr);
   if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
   if (P.N == 0) return KDA_OK;
   Workspace W;
-  layout(P, false, with_ctx, (char *)workspace, &W);
+  layout(P, ga.on, false, with_ctx, (char *)workspace, &W);
   if (with_ctx) ctx_layout(P, (char *)ctx, &W);
   Problem Pg = P;
-  cudaError_t e = gate_per_channel(P, W, &Pg, (cudaStream_t)stream);
+  cudaError_t e = gate_per_channel(P, ga, W, &Pg, (cudaStream_t)stream);
   if (e == cudaSuccess) {
     if (use_tc(P)) {
       // with o NULL a context call computes the final state alone: the context keeps the records only
       const int mode = o != nullptr ? (kFwdOutput | (with_ctx ? kFwdSave : 0)) : 0;
-      e = tc_forward(Pg, W, o, hT, mode, with_ctx && reuse, W.flags + 2, (cudaStream_t)stream);
+      e = tc_forward(Pg, ga, W, o, hT, mode, with_ctx && reuse, W.flags + 2, (cudaStream_t)stream);
     } else {
       Problem Pn = Pg;
       e = normalised_copies(Pg, W, &Pn, (cudaStream_t)stream);
@@ -246,6 +267,7 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
   Problem P{};
   kda_status st = validate(in, P);
   if (st != KDA_OK) return st;
+  const GateArgs ga = gate_args(in);
   // dq .. dbeta all NULL with a dh0: the start-state gradient alone (the reverse scan)
   const bool state_only =
       dq == nullptr && dk == nullptr && dv == nullptr && dg == nullptr && dbeta == nullptr && dh0 != nullptr;
@@ -261,28 +283,30 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
   const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
   with_ctx = need_ctx > 0;
   if ((st = check_ws(need_ctx, ctx, ctx_bytes, "forward context")) != KDA_OK) return st;
-  const size_t need = layout(P, true, with_ctx, nullptr, nullptr);
+  const size_t need = layout(P, ga.on, true, with_ctx, nullptr, nullptr);
   if ((st = check_ws(need, workspace, workspace_bytes)) != KDA_OK) return st;
   if (P.N == 0) return KDA_OK;
   Workspace W;
-  layout(P, true, with_ctx, (char *)workspace, &W);
+  layout(P, ga.on, true, with_ctx, (char *)workspace, &W);
   if (with_ctx) ctx_layout(P, (char *)ctx, &W);  // read only: the context serves any number of backwards
   cudaStream_t s = (cudaStream_t)stream;
+  const kda_gate *gate = in->gate;  // (with KDA_GATE_IN_KERNEL; validated)
   Problem Pg = P;
-  cudaError_t e = gate_per_channel(P, W, &Pg, s);
+  cudaError_t e = gate_per_channel(P, ga, W, &Pg, s);
   // per-channel gate gradient (a scalar gate's dg is summed over K inside the tensor-core kernel)
-  float *dgk = P.scalar_gate && !use_tc(P) ? W.dgx : dg;
+  float *dgk = (P.scalar_gate || ga.on) && !use_tc(P) ? W.dgx : dg;
   if (e == cudaSuccess) {
     if (use_tc(P)) {
       int *err = W.flags + 2;
       // the saved tiles come from the context, or from the states pass (the scan alone needs only the records)
       e = with_ctx     ? launch_chunk_map(Pg, W, s)
-          : state_only ? tc_records(Pg, W, err, s)
-                       : tc_forward(Pg, W, nullptr, nullptr, kFwdSave, false, err, s);
+          : state_only ? tc_records(Pg, ga, W, err, s)
+                       : tc_forward(Pg, ga, W, nullptr, nullptr, kFwdSave, false, err, s);
       if (e == cudaSuccess) e = tc_backward_scan(Pg, W, dO, dhT, dh0, err, s);
       if (!state_only) {
-        if (e == cudaSuccess) e = tc_backward_intra(Pg, W, dO, dv, dq, dk, dgk, dbeta, err, s);
+        if (e == cudaSuccess) e = tc_backward_intra(Pg, ga, W, dO, dv, dq, dk, dgk, dbeta, err, s);
         if (e == cudaSuccess && P.HV != P.H) e = launch_group_reduce(Pg, W.dqp, W.dkp, dq, dk, s);
+        if (e == cudaSuccess && ga.on) e = launch_kgate_param_reduce(Pg, W, gate->dA_log, gate->dbias, s);
       }
     } else {
       Problem Pn = Pg;
@@ -291,6 +315,8 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
     }
   }
   if (e == cudaSuccess && P.scalar_gate && !use_tc(P) && !state_only) e = launch_gate_grad_reduce(P, W.dgx, dg, s);
+  if (e == cudaSuccess && ga.on && !use_tc(P) && !state_only)
+    e = launch_kgate_grad(P, ga, W, W.dgx, dg, gate->dA_log, gate->dbias, s);
   if (e != cudaSuccess) return cuda_fail(e, with_ctx ? "kda_chunk_bwd_ctx" : "kda_chunk_bwd");
   return KDA_OK;
 }
@@ -326,13 +352,13 @@ extern "C" {
 size_t kda_chunk_fwd_workspace_size(const kda_inputs *in) {
   Problem P{};
   if (validate(in, P) != KDA_OK) return 0;
-  return layout(P, false, false, nullptr, nullptr);
+  return layout(P, gate_args(in).on, false, false, nullptr, nullptr);
 }
 
 size_t kda_chunk_bwd_workspace_size(const kda_inputs *in) {
   Problem P{};
   if (validate(in, P) != KDA_OK) return 0;
-  return layout(P, true, false, nullptr, nullptr);
+  return layout(P, gate_args(in).on, true, false, nullptr, nullptr);
 }
 
 kda_status kda_chunk_fwd(const kda_inputs *in, void *o, float *hT, void *workspace,
@@ -352,7 +378,7 @@ size_t kda_status_offset(const kda_inputs *in) {
   if (validate(in, P) != KDA_OK) return ~(size_t)0;
   char *const base = reinterpret_cast<char *>((uintptr_t)1 << 20);  // any aligned address: only offsets are taken
   Workspace W;
-  layout(P, false, false, base, &W);
+  layout(P, gate_args(in).on, false, false, base, &W);
   return (size_t)(reinterpret_cast<char *>(W.flags) - base);  // the same in every workspace layout (it comes first)
 }
 
@@ -365,13 +391,13 @@ size_t kda_chunk_ctx_size(const kda_inputs *in) {
 size_t kda_chunk_fwd_ctx_workspace_size(const kda_inputs *in) {
   Problem P{};
   if (validate(in, P) != KDA_OK) return 0;
-  return layout(P, false, ctx_layout(P, nullptr, nullptr) > 0, nullptr, nullptr);
+  return layout(P, gate_args(in).on, false, ctx_layout(P, nullptr, nullptr) > 0, nullptr, nullptr);
 }
 
 size_t kda_chunk_bwd_ctx_workspace_size(const kda_inputs *in) {
   Problem P{};
   if (validate(in, P) != KDA_OK) return 0;
-  return layout(P, true, ctx_layout(P, nullptr, nullptr) > 0, nullptr, nullptr);
+  return layout(P, gate_args(in).on, true, ctx_layout(P, nullptr, nullptr) > 0, nullptr, nullptr);
 }
 
 kda_status kda_chunk_fwd_ctx(const kda_inputs *in, void *o, float *hT, void *ctx, size_t ctx_bytes,
@@ -397,7 +423,7 @@ kda_status kda_recurrent_fwd(const kda_inputs *in, void *o, float *hT, void *str
   kda_status st = validate(in, P);
   if (st != KDA_OK) return st;
   if (P.Ttot > 0 && o == nullptr) return fail(KDA_ERR_INVALID_ARG, "o is NULL");
-  cudaError_t e = launch_recurrent(P, o, hT, (cudaStream_t)stream);
+  cudaError_t e = launch_recurrent(P, gate_args(in), o, hT, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_recurrent_fwd");
   return KDA_OK;
 }
@@ -436,7 +462,7 @@ const char *kda_status_string(kda_status s) {
 
 const char *kda_last_error(void) { return g_err; }
 
-int kda_version(void) { return 105; }
+int kda_version(void) { return 106; }
 
 int kda_uses_tensor_cores(const kda_inputs *in) {
   Problem P{};

@@ -9,6 +9,11 @@
 //
 // Both kernels are HBM-bound streams: 16-byte stores of the expanded rows;
 // one warp per (token, value head) row for the sum, in a fixed order.
+//
+// The KDA gate (KDA_GATE_IN_KERNEL) reaches the fp32 kernels the same way: the
+// decay made from the raw gate, and the gate's backward after them.  The
+// tensor-core kernels make the decay inside their gate cumsum and leave
+// per-slot partials of the parameter gradients, reduced here.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -51,7 +56,98 @@ __global__ void __launch_bounds__(256) gate_grad_reduce_kernel(Problem P, const 
   if (lane == 0) dg[row] = acc;
 }
 
+// ---- the KDA gate (KDA_GATE_IN_KERNEL) on the fp32 path ----
+
+// gx = kgate(a + bias): the decay the fp32 kernels read, one element per thread step.
+__global__ void __launch_bounds__(256) kgate_apply_kernel(Problem P, GateArgs ga, float *__restrict__ gx) {
+  const int64_t total = P.Ttot * P.HV * P.K;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(e % P.K);
+    const int j = (int)((e / P.K) % P.HV);
+    gx[e] = kgate(P.g[e] + kgate_bias(ga, P.K, j, c), kgate_scale(ga, j), ga.lb);
+  }
+}
+
+// One block per value head j, one thread per channel c: walks the valid tokens
+// chunk by chunk in order, da = dG * dg/dx into the caller's dg, and sums
+// dbias[j][c] = sum_t da and dA_log[j] = sum_{t,c} dG * dg/dA_log in a fixed
+// order (in fp64 on this fp32 path, whose results are held to fp32 accuracy).
+__global__ void __launch_bounds__(128) kgate_grad_kernel(Problem P, GateArgs ga, Workspace W, const float *__restrict__ dgx,
+                                                         float *__restrict__ da, float *__restrict__ dA_log,
+                                                         float *__restrict__ dbias) {
+  __shared__ double red[128];
+  const int j = blockIdx.x, c = threadIdx.x;
+  double pb = 0.0, pa = 0.0;  // fp64 partial sums: these reduce over every valid token
+  if (c < P.K) {
+    const float s = kgate_scale(ga, j), b = kgate_bias(ga, P.K, j, c);
+    for (int ci = 0; ci < P.NC; ++ci) {
+      const int4 ch = W.chunk[ci];
+      if (ch.x < 0) break;  // the valid chunks come first
+      for (int r = 0; r < ch.z; ++r) {
+        const size_t e = ((size_t)(ch.y + r) * P.HV + j) * P.K + c;
+        const float2 d = kgate_grad(P.g[e] + b, s, ga.lb);
+        const float v = dgx[e];
+        da[e] = v * d.x;
+        pb += (double)(v * d.x);
+        pa += (double)v * (double)d.y;
+      }
+    }
+    if (dbias != nullptr) dbias[(size_t)j * P.K + c] = (float)pb;
+  }
+  red[c] = pa;
+  __syncthreads();
+  if (c == 0 && dA_log != nullptr) {
+    double t = 0.0;
+    for (int i = 0; i < P.K; ++i) t += red[i];
+    dA_log[j] = (float)t;
+  }
+}
+
+// Tensor-core path: dbias[j][c] and dA_log[j] from the per-slot partials the
+// gradient kernel left (slot = chunk * HV + j), summed over the valid chunks in
+// order.
+__global__ void __launch_bounds__(128) kgate_param_reduce_kernel(Problem P, Workspace W, float *__restrict__ dA_log,
+                                                                 float *__restrict__ dbias) {
+  const int j = blockIdx.x, c = threadIdx.x;
+  float pb = 0.f, pa = 0.f;
+  for (int ci = 0; ci < P.NC; ++ci) {
+    if (W.chunk[ci].x < 0) break;
+    const size_t slot = (size_t)ci * P.HV + j;
+    if (c < P.K) pb += W.gpart_b[slot * P.K + c];
+    pa += W.gpart_a[slot];
+  }
+  if (c < P.K && dbias != nullptr) dbias[(size_t)j * P.K + c] = pb;
+  if (c == 0 && dA_log != nullptr) dA_log[j] = pa;
+}
+
 }  // namespace
+
+cudaError_t launch_kgate_apply(const Problem &P, const GateArgs &ga, float *gx, cudaStream_t s) {
+  const int64_t total = P.Ttot * P.HV * P.K;
+  if (total == 0) return cudaSuccess;
+  int nsm = 0;
+  cudaError_t e = sm_count(&nsm);
+  if (e != cudaSuccess) return e;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)nsm * 8) blocks = (int64_t)nsm * 8;
+  KDA_LAUNCH("kgate_apply_kernel", s, kgate_apply_kernel<<<(unsigned)blocks, 256, 0, s>>>(P, ga, gx));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kgate_grad(const Problem &P, const GateArgs &ga, const Workspace &W, const float *dgx, float *da,
+                              float *dA_log, float *dbias, cudaStream_t s) {
+  if (P.NC == 0) return cudaSuccess;
+  KDA_LAUNCH("kgate_grad_kernel", s, kgate_grad_kernel<<<P.HV, 128, 0, s>>>(P, ga, W, dgx, da, dA_log, dbias));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kgate_param_reduce(const Problem &P, const Workspace &W, float *dA_log, float *dbias,
+                                      cudaStream_t s) {
+  if ((dA_log == nullptr && dbias == nullptr) || P.NC == 0) return cudaSuccess;
+  KDA_LAUNCH("kgate_param_reduce_kernel", s,
+             kgate_param_reduce_kernel<<<P.HV, 128, 0, s>>>(P, W, dA_log, dbias));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gate_expand(const Problem &P, float *gx, cudaStream_t s) {
   const int64_t rows = P.Ttot * P.HV;

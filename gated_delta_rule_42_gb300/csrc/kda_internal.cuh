@@ -75,9 +75,41 @@ struct Workspace {
   __nv_bfloat16 *tc_dx;     // [slot] 16 KB: dX = A^T dD [64][V], swizzled operand tile
   // fp32 path with the q/k L2-norm prologue: normalised copies of q, k (dtype, [Ttot][H][K])
   void *qn, *kn;
-  // scalar gate: the gate repeated over K, and the per-channel gate gradient (fp32, [Ttot][HV][K])
+  // scalar gate: the gate repeated over K, and the per-channel gate gradient (fp32, [Ttot][HV][K]);
+  // with the KDA gate on the fp32 path: the decay made from the raw gate, and its gradient
   float *gx, *dgx;
+  // KDA gate, tensor-core backward: per-slot fp32 partials of dbias [slot][K] and dA_log [slot]
+  float *gpart_b, *gpart_a;
 };
+
+// ---- the KDA gate inside the op (KDA_GATE_IN_KERNEL) ----
+// With x = a + bias and s = exp(A_log): unbounded g = -s softplus(x), bounded
+// (lower bound lb < 0) g = lb sigmoid(s x); g is the per-token log2 decay.
+// Its parameters travel beside the Problem, to the kernels that make the decay.
+struct GateArgs {
+  const float *A_log, *bias;  // [HV] and [HV][K], or NULL (unit scale / no bias)
+  float lb;                   // < 0: the bounded gate; 0: the unbounded one
+  bool on;                    // g holds the raw gate pre-activations
+};
+__device__ __forceinline__ float kgate_softplus(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
+__device__ __forceinline__ float kgate_sigmoid(float y) { return 1.f / (1.f + expf(-y)); }
+__device__ __forceinline__ float kgate_scale(const GateArgs &ga, int j) {
+  return ga.A_log != nullptr ? expf(ga.A_log[j]) : 1.f;
+}
+__device__ __forceinline__ float kgate_bias(const GateArgs &ga, int K, int j, int c) {
+  return ga.bias != nullptr ? ga.bias[(size_t)j * K + c] : 0.f;
+}
+__device__ __forceinline__ float kgate(float x, float s, float lb) {
+  return lb < 0.f ? lb * kgate_sigmoid(s * x) : -s * kgate_softplus(x);
+}
+// (dg/dx, dg/dA_log) at x
+__device__ __forceinline__ float2 kgate_grad(float x, float s, float lb) {
+  if (lb < 0.f) {
+    const float sg = kgate_sigmoid(s * x), t = lb * sg * (1.f - sg) * s;
+    return make_float2(t, t * x);
+  }
+  return make_float2(-s * kgate_sigmoid(x), -s * kgate_softplus(x));
+}
 
 // --- element access -------------------------------------------------------
 __device__ __forceinline__ float ldf(const float *p, int64_t i) { return p[i]; }
@@ -128,9 +160,10 @@ cudaError_t simple_forward(const Problem &P, const Workspace &W, void *o, float 
 cudaError_t simple_backward(const Problem &P, const Workspace &W, const void *dO,
                             const float *dhT, void *dq, void *dk, void *dv, float *dg,
                             float *dbeta, float *dh0, bool state_only, cudaStream_t s);
-cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t s);
+cudaError_t launch_recurrent(const Problem &P, const GateArgs &ga, void *o, float *hT, cudaStream_t s);
 // Per-chunk records (tc_prep.cu): one CTA per (chunk, value head) slot.
-cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps, int *err, cudaStream_t s);
+cudaError_t tc_prepare(const Problem &P, const GateArgs &ga, const Workspace &W, const TmaMaps &maps, int *err,
+                       cudaStream_t s);
 // bf16, K = V = 128 tensor-core forward: the records into W.tc_tiles (unless
 // records_ready: W.tc_tiles already holds them for these q, k, g, beta), then
 // the state chain.  mode is kFwdOutput (o, hT), kFwdSave (no output: per
@@ -138,14 +171,14 @@ cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps
 // W.tc_hs / tc_xt / tc_dt for the backward), both bits, or 0 (hT alone).
 constexpr int kFwdOutput = 1, kFwdSave = 2;
 // The chunk map and the records alone (what the reverse scan needs).
-cudaError_t tc_records(const Problem &P, const Workspace &W, int *err, cudaStream_t s);
-cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, bool records_ready,
-                       int *err, cudaStream_t s);
+cudaError_t tc_records(const Problem &P, const GateArgs &ga, const Workspace &W, int *err, cudaStream_t s);
+cudaError_t tc_forward(const Problem &P, const GateArgs &ga, const Workspace &W, void *o, float *hT, int mode,
+                       bool records_ready, int *err, cudaStream_t s);
 cudaError_t tc_backward_scan(const Problem &P, const Workspace &W, const void *dO, const float *dhT,
                              float *dh0, int *err, cudaStream_t s);
 // Per-chunk gradients: tcgen05 products and the gradient chain in one kernel.
-cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *dO, void *dv, void *dq, void *dk,
-                              float *dg, float *dbeta, int *err, cudaStream_t s);
+cudaError_t tc_backward_intra(const Problem &P, const GateArgs &ga, const Workspace &W, const void *dO, void *dv,
+                              void *dq, void *dk, float *dg, float *dbeta, int *err, cudaStream_t s);
 // dq = (group sum of dqp) / sqrt(K), dk = group sum of dkp, over the HV/H value heads
 // q/k L2-norm prologue (l2norm.cu): normalised copies of the raw rows, and the
 // partial reduction fused with the backward through the normalisation.
@@ -159,6 +192,14 @@ cudaError_t launch_state_compose(const float *M, const float *h, const float *c,
 // per-channel gradient summed over K.
 cudaError_t launch_gate_expand(const Problem &P, float *gx, cudaStream_t s);
 cudaError_t launch_gate_grad_reduce(const Problem &P, const float *dgx, float *dg, cudaStream_t s);
+// KDA gate (gate.cu): the fp32 path's decay from the raw gate; its backward (da
+// from the per-channel dg, dA_log and dbias over the valid tokens); and the
+// tensor-core path's reduction of the per-slot partials.
+cudaError_t launch_kgate_apply(const Problem &P, const GateArgs &ga, float *gx, cudaStream_t s);
+cudaError_t launch_kgate_grad(const Problem &P, const GateArgs &ga, const Workspace &W, const float *dgx, float *da,
+                              float *dA_log, float *dbias, cudaStream_t s);
+cudaError_t launch_kgate_param_reduce(const Problem &P, const Workspace &W, float *dA_log, float *dbias,
+                                      cudaStream_t s);
 cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                 cudaStream_t s);
 // true when the tensor-core kernels handle this problem

@@ -23,7 +23,7 @@ constexpr int kThreadsR = 2 * kCols; // a lane pair holds one column (half the c
 
 template <typename Tin, int KHALF>
 __global__ void __launch_bounds__(kThreadsR)
-recurrent_kernel(Problem P, Tin *__restrict__ o, float *__restrict__ hT) {
+recurrent_kernel(Problem P, GateArgs ga, Tin *__restrict__ o, float *__restrict__ hT) {
   const int n = blockIdx.x, j = blockIdx.y;
   const int half = threadIdx.x & 1, x = blockIdx.z * kCols + (threadIdx.x >> 1);
   const int K = P.K, V = P.V, HV = P.HV, H = P.H, h = j / (HV / H);
@@ -56,7 +56,9 @@ recurrent_kernel(Problem P, Tin *__restrict__ o, float *__restrict__ hT) {
         const int64_t e = (t * H + h) * K + c;
         kv = ldf(k, e);
         qv = ldf(q, e);
-        av = exp2f(P.scalar_gate ? P.g[t * HV + j] : P.g[(t * HV + j) * K + c]);
+        const float gv = P.scalar_gate ? P.g[t * HV + j] : P.g[(t * HV + j) * K + c];
+        // the KDA gate inside the op: the decay from the raw gate
+        av = exp2f(ga.on ? kgate(gv + kgate_bias(ga, K, j, c), kgate_scale(ga, j), ga.lb) : gv);
       }
       sk[c] = kv;
       sq[c] = qv;
@@ -99,20 +101,20 @@ recurrent_kernel(Problem P, Tin *__restrict__ o, float *__restrict__ hT) {
 }
 
 template <typename Tin>
-cudaError_t run(const Problem &P, void *o, float *hT, cudaStream_t s) {
+cudaError_t run(const Problem &P, const GateArgs &ga, void *o, float *hT, cudaStream_t s) {
   if (P.N == 0) return cudaSuccess;
   const dim3 grid(P.N, P.HV, (P.V + kCols - 1) / kCols);
   if (P.K <= 64)
-    KDA_LAUNCH("recurrent_kernel", s, recurrent_kernel<Tin, 32><<<grid, kThreadsR, 0, s>>>(P, (Tin *)o, hT));
+    KDA_LAUNCH("recurrent_kernel", s, recurrent_kernel<Tin, 32><<<grid, kThreadsR, 0, s>>>(P, ga, (Tin *)o, hT));
   else
-    KDA_LAUNCH("recurrent_kernel", s, recurrent_kernel<Tin, 64><<<grid, kThreadsR, 0, s>>>(P, (Tin *)o, hT));
+    KDA_LAUNCH("recurrent_kernel", s, recurrent_kernel<Tin, 64><<<grid, kThreadsR, 0, s>>>(P, ga, (Tin *)o, hT));
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_recurrent(const Problem &P, void *o, float *hT, cudaStream_t s) {
-  return P.bf16 ? run<__nv_bfloat16>(P, o, hT, s) : run<float>(P, o, hT, s);
+cudaError_t launch_recurrent(const Problem &P, const GateArgs &ga, void *o, float *hT, cudaStream_t s) {
+  return P.bf16 ? run<__nv_bfloat16>(P, ga, o, hT, s) : run<float>(P, ga, o, hT, s);
 }
 
 }  // namespace kda

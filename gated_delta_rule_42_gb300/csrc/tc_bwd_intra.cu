@@ -77,7 +77,9 @@ constexpr uint32_t C_BETA = 218112;   // beta [64]
 constexpr uint32_t C_RB = 218368;     // dbeta partials [4][64] (before them: inverse row norms of the L2-norm prologue)
 constexpr uint32_t C_RED = 219392;    // sum_v dX v [64], d(2^G_last) [128]
 constexpr uint32_t C_MISC = 220160;   // mbarriers (loads S, P1, P2, raw k/q, products), tmem slot
-constexpr uint32_t C_SMEM = 220224 + 1024;
+constexpr uint32_t C_GPB = 220224;    // KDA gate: the dg scan's dbias partials [8 segments][128]
+constexpr uint32_t C_GPA = 224320;    //           and dA_log partials [512 threads]
+constexpr uint32_t C_SMEM = 226368 + 1024;
 static_assert(C_SMEM <= 232448, "one CTA per SM (227 KB)");
 // Widest per-channel decay span (log2) of a 16-token block that the middle
 // references carry (e1, e2 within 2^(+-kSpanMax / 2)); a slot with a wider
@@ -329,9 +331,11 @@ __device__ __forceinline__ Opnd opnd(float Kr, float Qr, float Kc, float g, floa
 // (token, head) row, from the inverse norms r of the decay-tile pass and row dots y . dy that a
 // first pass over the assembly's formulas forms, so dq and dk leave as bf16 in one pass.
 // kFix: the fix-up launch, over the slots the first launch listed (status word 4 counts them).
-template <bool kScalarGate, bool kL2, bool kFix>
+// kGate: the KDA gate inside the op (g holds the raw gate a): the cumsum makes the decay, and
+// the dg scan writes da = dG dg/da and per-slot partials of dbias and dA_log (W.gpart_*).
+template <bool kScalarGate, bool kL2, bool kFix, bool kGate>
 __global__ void __launch_bounds__(kCT, 1)
-kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps) {
+kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps, GateArgs ga) {
   const int nfix = kFix ? *(volatile const int *)(W.flags + 4) : 0;
   if (kFix && (int)blockIdx.x >= nfix) return;
   extern __shared__ unsigned char smraw[];
@@ -491,6 +495,12 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       float col[kC];
 #pragma unroll
       for (int r = 0; r < kC; ++r) col[r] = G[r * kGLD + c];
+      if (kGate) {  // the decay from the raw gate
+        const float sc = kgate_scale(ga, j), b = kgate_bias(ga, kD, j, c);
+#pragma unroll
+        for (int r = 0; r < kC; ++r)
+          if (r < len) col[r] = kgate(col[r] + b, sc, ga.lb);
+      }
 #pragma unroll
       for (int r = 0; r < kC; ++r) {
         if (r < len) s += col[r];
@@ -957,6 +967,8 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       }
       issue_gate_beta<kScalarGate>(sbase, sm, P, beta, nxt);
     }
+    float2 gpb = make_float2(0.f, 0.f);  // kGate: this thread's dbias partials (its column pair)
+    float gpa = 0.f;                      //        and dA_log partial
     {  // dg = reverse cumsum of dG: thread = one column pair, one 8-row segment (8 segments)
       const int c = 2 * (tid & 63), seg = tid >> 6, mid = len >> 1;
       // dG of (r, c) and (r, c + 1): Q parts in the Kr hi / lo slots of the pair, P parts in the
@@ -1024,8 +1036,25 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
           for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
           if (lane == k) sg_part = t;
         } else if (r < len) {
-          *reinterpret_cast<float2 *>(args.dg + ((size_t)(t0 + r) * HV + j) * kD + c) = v;
+          const size_t e = ((size_t)(t0 + r) * HV + j) * kD + c;
+          if (kGate) {  // da = dG dg/da; the parameter gradients' partials
+            const float2 a2 = __ldg(reinterpret_cast<const float2 *>(P.g + e));
+            const float sc = kgate_scale(ga, j);
+            const float2 d0 = kgate_grad(a2.x + kgate_bias(ga, kD, j, c), sc, ga.lb);
+            const float2 d1 = kgate_grad(a2.y + kgate_bias(ga, kD, j, c + 1), sc, ga.lb);
+            const float2 da = make_float2(v.x * d0.x, v.y * d1.x);
+            *reinterpret_cast<float2 *>(args.dg + e) = da;
+            gpb.x += da.x;
+            gpb.y += da.y;
+            gpa = fmaf(v.x, d0.y, fmaf(v.y, d1.y, gpa));
+          } else {
+            *reinterpret_cast<float2 *>(args.dg + e) = v;
+          }
         }
+      }
+      if (kGate) {
+        *reinterpret_cast<float2 *>(sm + C_GPB + (uint32_t)(seg * kD + c) * 4u) = gpb;
+        reinterpret_cast<float *>(sm + C_GPA)[tid] = gpa;
       }
     }
     KDA_PT(12);
@@ -1040,6 +1069,23 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
     }
     const bool all_ok = __syncthreads_and(ok) != 0;
     KDA_PT(7);
+    if (kGate) {  // the slot's partials, summed in a fixed order: dbias per channel, dA_log per slot
+      if (tid < kD) {
+        const float *gp = reinterpret_cast<const float *>(sm + C_GPB);
+        float t = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) t += gp[s * kD + tid];
+        W.gpart_b[cur.slot * kD + tid] = t;
+      } else if (warp == kD / 32) {
+        const float *gp = reinterpret_cast<const float *>(sm + C_GPA);
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < kCT / 32; ++i) t += gp[lane + 32 * i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) W.gpart_a[cur.slot] = t;
+      }
+    }
     if (tid < kC && tid < len)
       args.dbeta[(size_t)(t0 + tid) * HV + j] = red[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
     if (kScalarGate) {  // the two warps of each 8-row segment add their halves of the 128 channels
@@ -1082,24 +1128,25 @@ KDA_PT_EXPORT(kda_debug_intra_phase_cycles)
 
 // The per-chunk gradients, then the fix-up launch over the slots with a wide
 // decay span (none, usually: every CTA reads the count and leaves).
-template <bool kSG, bool kL2>
-cudaError_t launch_intra(const Problem &P, const Workspace &W, const IntraArgs &a, const TmaMaps &maps, unsigned grid,
-                         cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, false>,
+template <bool kSG, bool kL2, bool kGate>
+cudaError_t launch_intra(const Problem &P, const GateArgs &ga, const Workspace &W, const IntraArgs &a,
+                         const TmaMaps &maps, unsigned grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, false, kGate>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C_SMEM);
+    e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, true, kGate>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_tc_kernel<kSG, kL2, false><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
+  KDA_LAUNCH("kda_bwd_intra_tc", s,
+             kda_bwd_intra_tc_kernel<kSG, kL2, false, kGate><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   KDA_LAUNCH("kda_bwd_intra_tc_fix", s,
-             kda_bwd_intra_tc_kernel<kSG, kL2, true><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps));
+             kda_bwd_intra_tc_kernel<kSG, kL2, true, kGate><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
   return cudaGetLastError();
 }
 
-cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *dO, void *dv, void *dq, void *dk,
-                              float *dg, float *dbeta, int *err, cudaStream_t s) {
+cudaError_t tc_backward_intra(const Problem &P, const GateArgs &ga, const Workspace &W, const void *dO, void *dv,
+                              void *dq, void *dk, float *dg, float *dbeta, int *err, cudaStream_t s) {
   if (P.NC == 0) return cudaSuccess;
   // fp32 partials when several value heads share a q/k head (reduced, and with the L2-norm
   // prologue normalised, per q/k head afterwards); with HV = H the L2-norm backward is fused
@@ -1113,9 +1160,12 @@ cudaError_t tc_backward_intra(const Problem &P, const Workspace &W, const void *
   if ((e = sm_count(&nsm)) != cudaSuccess) return e;
   const int64_t slots = (int64_t)P.NC * P.HV;
   const unsigned grid = (unsigned)(slots < nsm ? slots : nsm);  // one CTA per SM, persistent over the slots
-  if (P.scalar_gate) return fuse_l2 ? launch_intra<true, true>(P, W, a, maps, grid, s)
-                                    : launch_intra<true, false>(P, W, a, maps, grid, s);
-  return fuse_l2 ? launch_intra<false, true>(P, W, a, maps, grid, s) : launch_intra<false, false>(P, W, a, maps, grid, s);
+  if (P.scalar_gate) return fuse_l2 ? launch_intra<true, true, false>(P, ga, W, a, maps, grid, s)
+                                    : launch_intra<true, false, false>(P, ga, W, a, maps, grid, s);
+  if (ga.on) return fuse_l2 ? launch_intra<false, true, true>(P, ga, W, a, maps, grid, s)
+                              : launch_intra<false, false, true>(P, ga, W, a, maps, grid, s);
+  return fuse_l2 ? launch_intra<false, true, false>(P, ga, W, a, maps, grid, s)
+                 : launch_intra<false, false, false>(P, ga, W, a, maps, grid, s);
 }
 
 }  // namespace kda

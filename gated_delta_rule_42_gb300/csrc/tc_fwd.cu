@@ -320,17 +320,17 @@ cudaError_t launch_fwd(const char *name, const Problem &P, const Workspace &W, c
   return cudaGetLastError();
 }
 
-cudaError_t tc_records(const Problem &P, const Workspace &W, int *err, cudaStream_t s) {
+cudaError_t tc_records(const Problem &P, const GateArgs &ga, const Workspace &W, int *err, cudaStream_t s) {
   cudaError_t e = launch_chunk_map(P, W, s);
   if (e != cudaSuccess || P.N == 0) return e;
   TmaMaps maps;
   if ((e = make_tma_maps(P, P.v, nullptr, &maps)) != cudaSuccess) return e;
-  return tc_prepare(P, W, maps, err, s);
+  return tc_prepare(P, ga, W, maps, err, s);
 }
 
-cudaError_t tc_forward(const Problem &P, const Workspace &W, void *o, float *hT, int mode, bool records_ready,
-                       int *err, cudaStream_t s) {
-  cudaError_t e = records_ready ? launch_chunk_map(P, W, s) : tc_records(P, W, err, s);
+cudaError_t tc_forward(const Problem &P, const GateArgs &ga, const Workspace &W, void *o, float *hT, int mode,
+                       bool records_ready, int *err, cudaStream_t s) {
+  cudaError_t e = records_ready ? launch_chunk_map(P, W, s) : tc_records(P, ga, W, err, s);
   if (e != cudaSuccess || P.N == 0) return e;
   FwdArgs a{(__nv_bfloat16 *)o, hT, err};
   TmaMaps maps;

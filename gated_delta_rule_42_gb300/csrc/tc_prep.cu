@@ -98,7 +98,9 @@ __device__ __forceinline__ void l2norm_row16(float (&kv)[8], float (&qv)[8]) {
 // memory (rec).  With l2n, the k and q rows are L2-normalised first.  Ends
 // with a __syncthreads.  Returns nonzero (every thread, right after the
 // cumsum) when a block's span exceeds kSpanMax: the slot is left to the fix-up.
-__device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec, bool l2n) {
+template <bool kGate>
+__device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec, bool l2n,
+                                       const GateArgs &ga) {
   const int tid = threadIdx.x;
   int wide_c = 0;
   float *G = (float *)(sm + P_G);
@@ -110,6 +112,12 @@ __device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *
     float s = 0.f;
 #pragma unroll
     for (int r = 0; r < kC; ++r) col[r] = G[r * kGT + c];
+    if (kGate) {  // the decay from the raw gate (KDA_GATE_IN_KERNEL); value head blockIdx.y
+      const float sc = kgate_scale(ga, blockIdx.y), b = kgate_bias(ga, kD, blockIdx.y, c);
+#pragma unroll
+      for (int r = 0; r < kC; ++r)
+        if (r < len) col[r] = kgate(col[r] + b, sc, ga.lb);
+    }
 #pragma unroll
     for (int r = 0; r < kC; ++r) {
       if (r < len) s += col[r];
@@ -418,8 +426,9 @@ __device__ __forceinline__ void load_slot(const Problem &P, const TmaMaps &maps,
 
 // One CTA per (chunk, value head) slot; a slot with a block wider than kSpanMax
 // is listed in W.wide_rec (status word 3 counts them) for kda_prep_tc_fix.
+template <bool kGate>
 __global__ void __launch_bounds__(kThr, 3)
-kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps) {
+kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps, GateArgs ga) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const int c_idx = blockIdx.x, j = blockIdx.y;
@@ -442,7 +451,7 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
   KDA_PT(0);
 
   unsigned char *rec = W.tc_tiles + slot * kTileRecord;
-  if (phase_a(sm, len, beta, rec, P.l2norm)) {
+  if (phase_a<kGate>(sm, len, beta, rec, P.l2norm, ga)) {
     if (tid == 0) W.wide_rec[atomicAdd(W.flags + 3, 1)] = (int)slot;
     return;
   }
@@ -458,7 +467,7 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
 // reference Gr and its last row as the column reference Gc on every channel,
 // so that e1, e2 and every off-diagonal factor are <= 1.
 __device__ __forceinline__ void fix_phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec,
-                                            bool l2n) {
+                                            bool l2n, const GateArgs &ga, int j) {
   const int tid = threadIdx.x;
   float *G = (float *)(sm + P_G);
   float *vec = (float *)(sm + P_VEC);
@@ -469,6 +478,12 @@ __device__ __forceinline__ void fix_phase_a(unsigned char *sm, int len, const fl
     float s = 0.f;
 #pragma unroll
     for (int r = 0; r < kC; ++r) col[r] = G[r * kGT + c];
+    if (ga.on) {  // the decay from the raw gate (KDA_GATE_IN_KERNEL)
+      const float sc = kgate_scale(ga, j), b = kgate_bias(ga, kD, j, c);
+#pragma unroll
+      for (int r = 0; r < kC; ++r)
+        if (r < len) col[r] = kgate(col[r] + b, sc, ga.lb);
+    }
 #pragma unroll
     for (int r = 0; r < kC; ++r) {
       if (r < len) s += col[r];
@@ -553,12 +568,13 @@ __device__ __forceinline__ void fix_phase_a(unsigned char *sm, int len, const fl
 // factors: L_ri = beta_r sum_c k_rc k_ic 2^(G_rc - G_ic) (i < r) and
 // Aqk_ri = sum_c q~_rc k_ic 2^(G_rc - G_ic) (i <= r) from the raw rows (L2-
 // normalised with l2n), the decay between tokens i and r formed as the running
-// product of the per-token decays 2^g_s, s = i+1 .. r: exact for any gate, it
-// only underflows where the true factor does.  One warp; lane l holds channels
+// product of the per-token decays 2^g_s, s = i+1 .. r (g made from the raw gate
+// with the KDA gate inside the op): exact for any gate, it only underflows
+// where the true factor does.  One warp; lane l holds channels
 // 4l .. 4l+3.  Writes the block's L (fp32, Lf) and Aqk (bf16, rec), zeros above
 // the diagonal and past len.
-__device__ __noinline__ void diag_direct(const Problem &P, int t0, int len, int h, int j, int R, const float *beta,
-                                         float *Lf, unsigned char *rec) {
+__device__ __noinline__ void diag_direct(const Problem &P, const GateArgs &ga, int t0, int len, int h, int j, int R,
+                                         const float *beta, float *Lf, unsigned char *rec) {
   const int lane = threadIdx.x & 31, c0 = lane * 4;
   constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
   const __nv_bfloat16 *kp = (const __nv_bfloat16 *)P.k, *qp = (const __nv_bfloat16 *)P.q;
@@ -609,7 +625,14 @@ __device__ __noinline__ void diag_direct(const Problem &P, int t0, int len, int 
 #pragma unroll
           for (int e = 0; e < 4; ++e) F[e] *= a;
         } else {
-          const float4 g4 = __ldg(reinterpret_cast<const float4 *>(P.g + row * kD + c0));
+          float4 g4 = __ldg(reinterpret_cast<const float4 *>(P.g + row * kD + c0));
+          if (ga.on) {  // the KDA gate: g holds the raw pre-activations
+            const float sc = kgate_scale(ga, j);
+            g4.x = kgate(g4.x + kgate_bias(ga, kD, j, c0), sc, ga.lb);
+            g4.y = kgate(g4.y + kgate_bias(ga, kD, j, c0 + 1), sc, ga.lb);
+            g4.z = kgate(g4.z + kgate_bias(ga, kD, j, c0 + 2), sc, ga.lb);
+            g4.w = kgate(g4.w + kgate_bias(ga, kD, j, c0 + 3), sc, ga.lb);
+          }
           F[0] *= exp2f(g4.x); F[1] *= exp2f(g4.y); F[2] *= exp2f(g4.z); F[3] *= exp2f(g4.w);
         }
       }
@@ -647,7 +670,7 @@ __device__ __noinline__ void diag_direct(const Problem &P, int t0, int len, int 
 // Phase (b) of the fix-up: the off-diagonal Gram blocks on the block factors,
 // the diagonal ones by diag_direct (warps 4..7), then the inverse.
 __device__ __forceinline__ void fix_phase_b(unsigned char *sm, const float *beta, unsigned char *rec,
-                                            const Problem &P, int t0, int len, int h, int j) {
+                                            const Problem &P, const GateArgs &ga, int t0, int len, int h, int j) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(sm);
   const float *vec = (const float *)(sm + P_VEC);
@@ -700,7 +723,7 @@ __device__ __forceinline__ void fix_phase_b(unsigned char *sm, const float *beta
     const int R = (b < 3) ? 0 : (b < 5 ? 1 : 2), I = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
     *reinterpret_cast<uint4 *>(rec + kRecAQK + sw_chunk(16 * R + (w >> 1), 2 * I + (w & 1), kC)) = make_uint4(0, 0, 0, 0);
   }
-  if (warp >= 4) diag_direct(P, t0, len, h, j, warp - 4, beta, Lf, rec);
+  if (warp >= 4) diag_direct(P, ga, t0, len, h, j, warp - 4, beta, Lf, rec);
   __syncthreads();
   invert_store(sm, rec);
 }
@@ -708,7 +731,7 @@ __device__ __forceinline__ void fix_phase_b(unsigned char *sm, const float *beta
 // kda_prep_tc_fix: the slots kda_prep_tc listed, walked by the CTAs, on the
 // exact path (with none listed every CTA reads the count and leaves).
 __global__ void __launch_bounds__(kThr, 3)
-kda_prep_tc_fix_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps) {
+kda_prep_tc_fix_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps, GateArgs ga) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const int nfix = *(volatile const int *)(W.flags + 3);
@@ -727,8 +750,8 @@ kda_prep_tc_fix_kernel(Problem P, Workspace W, int *err, const __grid_constant__
     const int4 ch = W.chunk[c_idx];
     load_slot(P, maps, sm, bar, parity, err, ch.y, ch.z, h, j);
     unsigned char *rec = W.tc_tiles + (size_t)s * kTileRecord;
-    fix_phase_a(sm, ch.z, beta, rec, P.l2norm);
-    fix_phase_b(sm, beta, rec, P, ch.y, ch.z, h, j);
+    fix_phase_a(sm, ch.z, beta, rec, P.l2norm, ga, j);
+    fix_phase_b(sm, beta, rec, P, ga, ch.y, ch.z, h, j);
     __syncthreads();  // the shared tiles are free for the next slot
   }
 }
@@ -737,19 +760,21 @@ kda_prep_tc_fix_kernel(Problem P, Workspace W, int *err, const __grid_constant__
 
 KDA_PT_EXPORT(kda_debug_prep_phase_cycles)
 
-cudaError_t tc_prepare(const Problem &P, const Workspace &W, const TmaMaps &maps, int *err, cudaStream_t s) {
+cudaError_t tc_prepare(const Problem &P, const GateArgs &ga, const Workspace &W, const TmaMaps &maps, int *err,
+                       cudaStream_t s) {
   if (P.NC == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kda_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+  auto fast = ga.on ? kda_prep_tc_kernel<true> : kda_prep_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(fast, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kda_prep_tc_fix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   int nsm = 0;
   if (e == cudaSuccess) e = sm_count(&nsm);
   if (e != cudaSuccess) return e;
-  KDA_LAUNCH("kda_prep_tc", s, kda_prep_tc_kernel<<<dim3(P.NC, P.HV), kThr, P_SMEM, s>>>(P, W, err, maps));
+  KDA_LAUNCH("kda_prep_tc", s, fast<<<dim3(P.NC, P.HV), kThr, P_SMEM, s>>>(P, W, err, maps, ga));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t slots = (int64_t)P.NC * P.HV;
   const unsigned grid = (unsigned)(slots < nsm ? slots : nsm);
-  KDA_LAUNCH("kda_prep_tc_fix", s, kda_prep_tc_fix_kernel<<<grid, kThr, P_SMEM, s>>>(P, W, err, maps));
+  KDA_LAUNCH("kda_prep_tc_fix", s, kda_prep_tc_fix_kernel<<<grid, kThr, P_SMEM, s>>>(P, W, err, maps, ga));
   return cudaGetLastError();
 }
 

@@ -67,6 +67,18 @@ class KdaInputs:
     output_final_state: bool
     seed: int
     meta: dict = field(default_factory=dict)
+    # KDA gate inside the op: g then holds raw pre-activations, with these parameters
+    A_log: Optional[torch.Tensor] = None     # [HV] fp32
+    g_bias: Optional[torch.Tensor] = None    # [HV, K] fp32
+    lower_bound: Optional[float] = None      # None: the unbounded gate
+
+    @property
+    def gate(self) -> Optional[dict]:
+        """The oracle's gate parameters (fp64 numpy), or None without the gate."""
+        if not self.meta.get("raw_gate"):
+            return None
+        c = (lambda x: None if x is None else x.detach().cpu().to(torch.float64).numpy())
+        return dict(A_log=c(self.A_log), bias=c(self.g_bias), lower_bound=self.lower_bound)
 
     @property
     def N(self) -> int:
@@ -92,7 +104,7 @@ class KdaInputs:
             self.name, self.B, self.T, self.H, self.HV, self.K, self.V, self.dtype,
             mv(self.q), mv(self.k), mv(self.v), mv(self.g), mv(self.beta), mv(self.h0),
             mv(self.do), mv(self.dhT), mv(self.cu_seqlens), self.output_final_state,
-            self.seed, dict(self.meta))
+            self.seed, dict(self.meta), mv(self.A_log), mv(self.g_bias), self.lower_bound)
 
     def f64(self) -> dict:
         """Exact fp64 copies (numpy) of every input, as the oracle consumes them.
@@ -175,12 +187,17 @@ def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.
                 cu_seqlens=None, lengths_fn=None, h0: bool = True, final_state: bool = True,
                 dhT: Optional[bool] = None, g_mean: float = 0.0, seed: int = 0,
                 name: str = "custom", scalar_gate: bool = False, g_std: float = 1.0,
-                g_lo: float = -5.0) -> KdaInputs:
+                g_lo: float = -5.0, raw_gate: bool = False, A_log: Optional[bool] = None,
+                g_bias: Optional[bool] = None, lower_bound: Optional[float] = None) -> KdaInputs:
     """Draw one problem.  ``cu_seqlens`` may be a list of offsets (B must be 1);
     ``lengths_fn(rng)`` may instead return the offsets from the generator.
     ``scalar_gate`` draws g as [B, T, HV] (one decay per token and value head).
     The gate is clip(-softplus(N(g_mean, g_std)), g_lo, 0); the workloads keep
-    the defaults (std 1, clip at -5), the strong-decay cases widen both."""
+    the defaults (std 1, clip at -5), the strong-decay cases widen both.
+    ``raw_gate`` draws g as raw pre-activations N(g_mean, g_std) for the KDA
+    gate inside the op instead, and then (after every other draw) A_log ~
+    0.5 N(0, 1) [HV] and g_bias ~ 0.5 N(0, 1) [HV, K] unless A_log / g_bias is
+    False; ``lower_bound`` selects the bounded gate."""
     rng = np.random.Generator(np.random.PCG64(seed))
     cu = None
     if lengths_fn is not None:
@@ -196,8 +213,8 @@ def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.
     k = _l2_rows(_normal(rng, (B, T, H, K)))
     v = _normal(rng, (B, T, HV, V))
     beta = _sigmoid(_normal(rng, (B, T, HV)))
-    g = _neg_softplus_clipped(_normal(rng, (B, T, HV) if scalar_gate else (B, T, HV, K), mean=g_mean, std=g_std),
-                              lo=g_lo)
+    graw = _normal(rng, (B, T, HV) if scalar_gate else (B, T, HV, K), mean=g_mean, std=g_std)
+    g = graw if raw_gate else _neg_softplus_clipped(graw, lo=g_lo)
     h0_t = _normal(rng, (N, HV, K, V), std=0.1) if h0 else None
     do = _normal(rng, (B, T, HV, V))
     if dhT is None:
@@ -207,6 +224,13 @@ def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.
     def t(x, dt):
         return torch.from_numpy(x).to(dt)
 
+    A_t = bias_t = None
+    if raw_gate:
+        if A_log is not False:
+            A_t = torch.from_numpy(_normal(rng, (HV,), std=0.5))
+        if g_bias is not False:
+            bias_t = torch.from_numpy(_normal(rng, (HV, K), std=0.5))
+
     return KdaInputs(
         name=name, B=B, T=T, H=H, HV=HV, K=K, V=V, dtype=dtype,
         q=t(q, dtype), k=t(k, dtype), v=t(v, dtype),
@@ -215,7 +239,8 @@ def make_inputs(*, B: int, T: int, H: int, HV: int, K: int, V: int, dtype=torch.
         do=t(do, dtype),
         dhT=None if dhT_t is None else torch.from_numpy(dhT_t),
         cu_seqlens=None if cu is None else torch.from_numpy(cu.astype(np.int32)),
-        output_final_state=final_state, seed=seed)
+        output_final_state=final_state, seed=seed, meta=dict(raw_gate=raw_gate),
+        A_log=A_t, g_bias=bias_t, lower_bound=lower_bound)
 
 
 def _packed_varlen_offsets(rng: np.random.Generator) -> np.ndarray:

@@ -21,7 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["chunk_kda", "recurrent_kda", "chunk_kda_fwd", "chunk_kda_bwd", "chunk_kda_fwd_ctx",
-           "chunk_kda_bwd_ctx", "chunk_kda_bwd_state", "chunk_kda_fwd_reuse", "make_inputs_struct"]
+           "chunk_kda_bwd_ctx", "chunk_kda_bwd_state", "chunk_kda_fwd_reuse", "make_inputs_struct", "KdaGateParams"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -41,10 +41,27 @@ def _check_tensor(name, t, dtype, device, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None, use_qk_l2norm=False):
+class KdaGateParams:
+    """The KDA gate inside the op (KDA_GATE_IN_KERNEL): ``g`` then holds the raw
+    gate pre-activations a and the op makes the per-token log2 decay itself,
+    g = -exp(A_log) softplus(a + bias) (unbounded, ``lower_bound`` None) or
+    g = lower_bound sigmoid(exp(A_log) (a + bias)) (bounded, lower_bound < 0).
+    A_log [HV] and bias [HV, K] are fp32 device tensors or None (an omitted
+    A_log is a unit scale, the same as zeros)."""
+
+    def __init__(self, A_log=None, bias=None, lower_bound=None):
+        self.A_log, self.bias = A_log, bias
+        self.lower_bound = 0.0 if lower_bound is None else float(lower_bound)
+
+
+def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None, use_qk_l2norm=False,
+                       gate: Optional[KdaGateParams] = None, dA_log=None, dbias=None):
     """Validate the tensors and build the C ``kda_inputs`` struct.  With
     use_qk_l2norm the library L2-normalises every q and k row itself; a gate of
-    shape [B, T, HV] (instead of [B, T, HV, K]) is the scalar-gate variant."""
+    shape [B, T, HV] (instead of [B, T, HV, K]) is the scalar-gate variant;
+    ``gate`` (:class:`KdaGateParams`) makes the op apply the KDA gate to the raw
+    gate in ``g``, and a backward writes its parameter gradients into dA_log,
+    dbias when they are given."""
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
     B, T, H, K = q.shape
@@ -75,6 +92,25 @@ def make_inputs_struct(q, k, v, g, beta, initial_state=None, cu_seqlens=None, us
     s.h0 = None if initial_state is None else initial_state.data_ptr()
     s.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
     s.flags = (_lib.KDA_QK_L2NORM if use_qk_l2norm else 0) | (_lib.KDA_SCALAR_GATE if scalar_gate else 0)
+    if gate is not None:
+        if scalar_gate:
+            raise ValueError("the KDA gate takes a per-channel raw gate [B, T, HV, K]")
+        if gate.A_log is not None:
+            _check_tensor("A_log", gate.A_log, torch.float32, dev, (HV,))
+        if gate.bias is not None:
+            _check_tensor("gate bias", gate.bias, torch.float32, dev, (HV, K))
+        for name, t, shape in (("dA_log", dA_log, (HV,)), ("dbias", dbias, (HV, K))):
+            if t is not None:
+                _check_tensor(name, t, torch.float32, dev, shape)
+        gs = _lib.KdaGate()
+        gs.A_log = None if gate.A_log is None else gate.A_log.data_ptr()
+        gs.bias = None if gate.bias is None else gate.bias.data_ptr()
+        gs.lower_bound = gate.lower_bound
+        gs.dA_log = None if dA_log is None else dA_log.data_ptr()
+        gs.dbias = None if dbias is None else dbias.data_ptr()
+        s.gate = ctypes.pointer(gs)
+        s._gate_ref = gs  # keeps the struct alive with s
+        s.flags |= _lib.KDA_GATE_IN_KERNEL
     return s
 
 
@@ -100,11 +136,12 @@ def _output(v, need_output, output_final_state):
 
 def chunk_kda_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_final_state=False,
                   workspace: Optional[torch.Tensor] = None, use_qk_l2norm: bool = False,
-                  need_output: bool = True) -> Tuple[Optional[torch.Tensor], Optional[torch.Tensor]]:
+                  need_output: bool = True,
+                  gate: Optional[KdaGateParams] = None) -> Tuple[Optional[torch.Tensor], Optional[torch.Tensor]]:
     """Chunked forward (no autograd).  need_output=False: the final state alone
     (o is None), without the output work."""
     lib = _lib.load()
-    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm, gate)
     o = _output(v, need_output, output_final_state)
     hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
           if output_final_state else None)
@@ -118,9 +155,12 @@ def chunk_kda_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_
 
 def chunk_kda_bwd(q, k, v, g, beta, initial_state, cu_seqlens, do, dht,
                   workspace: Optional[torch.Tensor] = None, need_dh0: bool = True,
-                  use_qk_l2norm: bool = False):
+                  use_qk_l2norm: bool = False, gate: Optional[KdaGateParams] = None):
+    """Chunked backward with recompute.  Returns (dq, dk, dv, dg, dbeta, dh0) and,
+    with ``gate``, also (dA_log or None, dbias or None)."""
     lib = _lib.load()
-    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    dA, dbias = _gate_grads(gate, v)
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm, gate, dA, dbias)
     _check_tensor("do", do, q.dtype, q.device, tuple(v.shape))
     if dht is not None:
         _check_tensor("dht", dht, torch.float32, q.device, (s.N, s.HV, s.K, s.V))
@@ -138,11 +178,20 @@ def chunk_kda_bwd(q, k, v, g, beta, initial_state, cu_seqlens, do, dht,
     _lib.check(lib, lib.kda_chunk_bwd(ctypes.byref(s), _ptr(do), _ptr(dht), _ptr(dq), _ptr(dk),
                                       _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), wp, wb,
                                       _stream(q.device)))
-    return dq, dk, dv, dg, db, dh0
+    return (dq, dk, dv, dg, db, dh0) + (() if gate is None else (dA, dbias))
+
+
+def _gate_grads(gate, v):
+    """Output tensors for the gate's parameter gradients (None for an omitted parameter)."""
+    if gate is None:
+        return None, None
+    dA = None if gate.A_log is None else torch.empty_like(gate.A_log)  # [HV]
+    dbias = None if gate.bias is None else torch.empty_like(gate.bias)
+    return dA, dbias
 
 
 def chunk_kda_fwd_ctx(q, k, v, g, beta, initial_state=None, cu_seqlens=None, output_final_state=False,
-                      use_qk_l2norm: bool = False, need_output: bool = True):
+                      use_qk_l2norm: bool = False, need_output: bool = True, gate: Optional[KdaGateParams] = None):
     """Forward that also returns the forward context (a uint8 device tensor,
     empty on the general path) for :func:`chunk_kda_bwd_ctx`: the per-chunk
     records, chunk-start states and X^T, D^T tiles the backward would otherwise
@@ -150,7 +199,7 @@ def chunk_kda_fwd_ctx(q, k, v, g, beta, initial_state=None, cu_seqlens=None, out
     records only (a backward then needs :func:`chunk_kda_fwd_reuse` with output
     first).  Returns (o or None, final_state or None, context)."""
     lib = _lib.load()
-    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm, gate)
     o = _output(v, need_output, output_final_state)
     hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
           if output_final_state else None)
@@ -186,11 +235,12 @@ def chunk_kda_fwd_reuse(q, k, v, g, beta, initial_state, cu_seqlens, kctx, outpu
 
 
 def chunk_kda_bwd_ctx(q, k, v, g, beta, initial_state, cu_seqlens, kctx, do, dht, need_dh0: bool = True,
-                      use_qk_l2norm: bool = False):
+                      use_qk_l2norm: bool = False, gate: Optional[KdaGateParams] = None):
     """Backward on the context :func:`chunk_kda_fwd_ctx` returned for the same
     inputs (it is only read).  Same results as :func:`chunk_kda_bwd`."""
     lib = _lib.load()
-    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    dA, dbias = _gate_grads(gate, v)
+    s = make_inputs_struct(q, k, v, g, beta, initial_state, cu_seqlens, use_qk_l2norm, gate, dA, dbias)
     _check_tensor("do", do, q.dtype, q.device, tuple(v.shape))
     if dht is not None:
         _check_tensor("dht", dht, torch.float32, q.device, (s.N, s.HV, s.K, s.V))
@@ -208,7 +258,7 @@ def chunk_kda_bwd_ctx(q, k, v, g, beta, initial_state, cu_seqlens, kctx, do, dht
     _lib.check(lib, lib.kda_chunk_bwd_ctx(ctypes.byref(s), cp, cb, _ptr(do), _ptr(dht), _ptr(dq), _ptr(dk),
                                           _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), wp, wb,
                                           _stream(q.device)))
-    return dq, dk, dv, dg, db, dh0
+    return (dq, dk, dv, dg, db, dh0) + (() if gate is None else (dA, dbias))
 
 
 def chunk_kda_bwd_state(q, k, v, g, beta, initial_state, cu_seqlens, do, dht, kctx=None,
@@ -242,32 +292,37 @@ def chunk_kda_bwd_state(q, k, v, g, beta, initial_state, cu_seqlens, do, dht, kc
 class ChunkKDAFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, use_qk_l2norm,
-                keep_context):
+                keep_context, use_gate, A_log, g_bias, lower_bound):
+        gate = KdaGateParams(A_log, g_bias, lower_bound) if use_gate else None
         if keep_context:
             o, hT, ctx.kctx = chunk_kda_fwd_ctx(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
-                                                use_qk_l2norm=use_qk_l2norm)
+                                                use_qk_l2norm=use_qk_l2norm, gate=gate)
         else:
             o, hT = chunk_kda_fwd(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
-                                  use_qk_l2norm=use_qk_l2norm)
+                                  use_qk_l2norm=use_qk_l2norm, gate=gate)
             ctx.kctx = None
-        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens, A_log, g_bias)
         ctx.has_h0 = initial_state is not None
         ctx.l2 = use_qk_l2norm
+        ctx.use_gate, ctx.lower_bound = use_gate, lower_bound
         return o, hT
 
     @staticmethod
     def backward(ctx, do, dht):
-        q, k, v, g, beta, h0, cu = ctx.saved_tensors
+        q, k, v, g, beta, h0, cu, A_log, g_bias = ctx.saved_tensors
         do = do.contiguous()
         dht = None if dht is None else dht.contiguous()
+        gate = KdaGateParams(A_log, g_bias, ctx.lower_bound) if ctx.use_gate else None
         if ctx.kctx is not None:
-            dq, dk, dv, dg, db, dh0 = chunk_kda_bwd_ctx(q, k, v, g, beta, h0, cu, ctx.kctx, do, dht,
-                                                        need_dh0=ctx.has_h0, use_qk_l2norm=ctx.l2)
+            out = chunk_kda_bwd_ctx(q, k, v, g, beta, h0, cu, ctx.kctx, do, dht, need_dh0=ctx.has_h0,
+                                    use_qk_l2norm=ctx.l2, gate=gate)
             ctx.kctx = None  # the context's memory goes back as soon as the backward is enqueued
         else:
-            dq, dk, dv, dg, db, dh0 = chunk_kda_bwd(q, k, v, g, beta, h0, cu, do, dht,
-                                                    need_dh0=ctx.has_h0, use_qk_l2norm=ctx.l2)
-        return dq, dk, dv, dg, db, dh0, None, None, None, None
+            out = chunk_kda_bwd(q, k, v, g, beta, h0, cu, do, dht, need_dh0=ctx.has_h0, use_qk_l2norm=ctx.l2,
+                                gate=gate)
+        dq, dk, dv, dg, db, dh0 = out[:6]
+        dA, dbias = out[6:] if gate is not None else (None, None)
+        return dq, dk, dv, dg, db, dh0, None, None, None, None, None, dA, dbias, None
 
 
 class SegmentedChunkKDAFunction(torch.autograd.Function):
@@ -293,7 +348,8 @@ class SegmentedChunkKDAFunction(torch.autograd.Function):
 
 
 def chunk_kda(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, output_final_state=False,
-              use_qk_l2norm=False, keep_context=True, segments=1):
+              use_qk_l2norm=False, keep_context=True, segments=1, use_gate_in_kernel=False, A_log=None,
+              g_bias=None, lower_bound=None):
     """Chunked KDA forward (with autograd).  Returns (o, final_state or None).
     use_qk_l2norm: L2-normalise every q and k row inside the op (its backward
     included).  keep_context: the forward keeps its per-chunk intermediates
@@ -302,24 +358,30 @@ def chunk_kda(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, output_f
     recompute.  The gradients are the same either way.  segments > 1 (dense
     batches only): every sequence runs as that many segments at once, joined by
     the state relay -- for a few long sequences, whose chunk chains alone would
-    leave most SMs idle (see :mod:`.segments`)."""
+    leave most SMs idle (see :mod:`.segments`).  use_gate_in_kernel: ``g`` holds
+    the raw gate and the op applies the KDA gate with A_log [HV], g_bias [HV, K]
+    and lower_bound (:class:`KdaGateParams`); gradients reach a, A_log and g_bias."""
     if segments > 1:
         if cu_seqlens is not None:
             raise ValueError("segments > 1 splits dense batches only")
+        if use_gate_in_kernel:
+            raise ValueError("segments > 1 takes the per-token decay (use_gate_in_kernel=False)")
         return SegmentedChunkKDAFunction.apply(q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
                                                segments)
     return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state,
-                                  use_qk_l2norm, keep_context)
+                                  use_qk_l2norm, keep_context, use_gate_in_kernel, A_log, g_bias, lower_bound)
 
 
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
-                  output_final_state=False, use_qk_l2norm=False):
+                  output_final_state=False, use_qk_l2norm=False, use_gate_in_kernel=False, A_log=None,
+                  g_bias=None, lower_bound=None):
     """Token-by-token KDA forward for inference (fp32 arithmetic).  Rejects
     inputs that require grad: train through :func:`chunk_kda`."""
-    if any(t is not None and t.requires_grad for t in (q, k, v, gate, beta, initial_state)):
+    if any(t is not None and t.requires_grad for t in (q, k, v, gate, beta, initial_state, A_log, g_bias)):
         raise RuntimeError("recurrent_kda is inference-only; use chunk_kda for training")
     lib = _lib.load()
-    s = make_inputs_struct(q, k, v, gate, beta, initial_state, cu_seqlens, use_qk_l2norm)
+    gp = KdaGateParams(A_log, g_bias, lower_bound) if use_gate_in_kernel else None
+    s = make_inputs_struct(q, k, v, gate, beta, initial_state, cu_seqlens, use_qk_l2norm, gp)
     o = torch.empty_like(v)
     hT = (torch.empty((s.N, s.HV, s.K, s.V), dtype=torch.float32, device=q.device)
           if output_final_state else None)

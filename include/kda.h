@@ -94,8 +94,31 @@ enum {
    * omitted" (fla-org/flash-linear-attention PR #1294, commit log), of which
    * KDA's per-channel gate is the generalisation.  dg is the sum over K of the
    * per-channel gradients. */
-  KDA_SCALAR_GATE = 2
+  KDA_SCALAR_GATE = 2,
+  /* KDA gate inside the op: `g` holds the raw gate pre-activations a (same
+   * layout, fp32) and `gate` the gate's parameters; the op makes the per-token
+   * log2 decay itself, with x = a + bias and s = exp(A_log):
+   *   unbounded (lower_bound == 0):  g = -s softplus(x)
+   *   bounded   (lower_bound  < 0):  g = lower_bound sigmoid(s x)
+   * An omitted A_log is a unit scale, the same as an explicit zero A_log
+   * ("[Fix] Use unit KDA gate scale when A_log is omitted",
+   * fla-org/flash-linear-attention PR #1294, Summary and Breaking changes; the
+   * page prints no formula: the two above are this library's reading).  The
+   * backward's dg is then the gradient w.r.t. a, and the gate's parameter
+   * gradients are summed over every valid token in fp32 (that page's commit
+   * log: gate bias gradients reduced in fp32 before any downcast).  Not
+   * combined with KDA_SCALAR_GATE (KDA_ERR_UNSUPPORTED). */
+  KDA_GATE_IN_KERNEL = 4
 };
+
+/* Parameters of the KDA gate (KDA_GATE_IN_KERNEL); DEVICE pointers. */
+typedef struct kda_gate {
+  const float *A_log; /* [HV] log of the decay scale, or NULL: unit scale (the same as zeros) */
+  const float *bias;  /* [HV][K] added to a, or NULL                                       */
+  float lower_bound;  /* 0: the unbounded gate; < 0: the bounded gate (finite)              */
+  float *dA_log;      /* backward output [HV] (fp32), or NULL                                */
+  float *dbias;       /* backward output [HV][K] (fp32), or NULL                             */
+} kda_gate;
 
 /* Problem description shared by every entry point.  Zero-initialise it: a
  * zero flags field keeps the plain behaviour. */
@@ -110,7 +133,9 @@ typedef struct kda_inputs {
   const float *beta;        /* per (token, value head) write strength                        */
   const float *h0;          /* initial states [N][HV][K][V], or NULL for zeros               */
   const int32_t *cu_seqlens;/* device [N+1] packed offsets, or NULL for a dense batch         */
-  int flags;                /* KDA_QK_L2NORM | KDA_SCALAR_GATE or 0; other bits: INVALID_ARG */
+  int flags;                /* KDA_QK_L2NORM | KDA_SCALAR_GATE | KDA_GATE_IN_KERNEL, or 0;   */
+                            /* other bits: KDA_ERR_INVALID_ARG                                 */
+  const kda_gate *gate;     /* host pointer; required with KDA_GATE_IN_KERNEL, else ignored   */
 } kda_inputs;
 
 /* Bytes of device workspace kda_chunk_fwd needs for this problem (256-byte
@@ -247,10 +272,11 @@ const char *kda_status_string(kda_status s);
 /* Message describing the last failure on the calling thread ("" if none). */
 const char *kda_last_error(void);
 
-/* Library ABI version (major * 100 + minor): 105 (101: kda_inputs gained
+/* Library ABI version (major * 100 + minor): 106 (101: kda_inputs gained
  * `flags`; 102: the forward-context entry points; 103: the final-state-only
  * forward, the start-state-gradient-only backward, kda_chunk_fwd_reuse; 104:
- * kda_status_offset, kda_debug_bounded_wait; 105: status words 3 and 4). */
+ * kda_status_offset, kda_debug_bounded_wait; 105: status words 3 and 4,
+ * kda_uses_tensor_cores; 106: KDA_GATE_IN_KERNEL and kda_inputs.gate). */
 int kda_version(void);
 
 /* Chunked forward without a caller workspace (no counterpart on the pages).

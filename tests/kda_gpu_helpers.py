@@ -35,12 +35,18 @@ def status_words(lib, s, ws, wp):
     return ws[base:base + 20].cpu().numpy().view(np.int32).tolist()
 
 
+def gate_params(d):
+    """The KDA gate's parameters of inputs ``d`` (on the device), or None."""
+    from gated_delta_rule_42_gb300.ops import KdaGateParams
+    return KdaGateParams(d.A_log, d.g_bias, d.lower_bound) if d.meta.get("raw_gate") else None
+
+
 def gpu_fwd(inp, dev="cuda", lib=None, l2=False, status=None):
     """kda_chunk_fwd on the inputs (moved to dev); returns CPU o, hT.  l2: the
     q/k L2-norm prologue flag.  A ``status`` list receives the call's status words."""
     lib = lib or _lib.load()
     d = inp.to(dev)
-    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2, gate_params(d))
     o = _nan_like(d.v.shape, d.dtype, dev)
     hT = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if inp.output_final_state else None
     need = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s))
@@ -56,12 +62,18 @@ def gpu_fwd(inp, dev="cuda", lib=None, l2=False, status=None):
 
 
 def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True, l2=False, status=None):
+    """kda_chunk_bwd; with the KDA gate the dict also holds dA_log and dbias."""
     lib = lib or _lib.load()
     d = inp.to(dev)
-    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
+    gp = gate_params(d)
+    dA = None if gp is None or d.A_log is None else _nan_like(d.A_log.shape, torch.float32, dev)
+    dbias = None if gp is None or d.g_bias is None else _nan_like(d.g_bias.shape, torch.float32, dev)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2, gp, dA, dbias)
     out = dict(dq=_nan_like(d.q.shape, d.dtype, dev), dk=_nan_like(d.k.shape, d.dtype, dev),
                dv=_nan_like(d.v.shape, d.dtype, dev), dg=_nan_like(d.g.shape, torch.float32, dev),
                dbeta=_nan_like(d.beta.shape, torch.float32, dev))
+    if gp is not None:
+        out["dA_log"], out["dbias"] = dA, dbias
     out["dh0"] = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if want_dh0 else None
     need = lib.kda_chunk_bwd_workspace_size(ctypes.byref(s))
     ws, wp, wb = _poisoned_ws(need, dev)
@@ -82,7 +94,7 @@ def gpu_bwd(inp, dev="cuda", lib=None, want_dh0=True, l2=False, status=None):
 def gpu_recurrent(inp, dev="cuda", lib=None, l2=False):
     lib = lib or _lib.load()
     d = inp.to(dev)
-    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2)
+    s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, l2, gate_params(d))
     o = _nan_like(d.v.shape, d.dtype, dev)
     hT = _nan_like((s.N, s.HV, s.K, s.V), torch.float32, dev) if inp.output_final_state else None
     st = lib.kda_recurrent_fwd(ctypes.byref(s), ctypes.c_void_p(o.data_ptr()),
@@ -97,14 +109,14 @@ def oracle_fwd(inp, l2=False):
     f = inp.f64()
     cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
     return oracle.kda_fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], cu, True, qk_l2norm=l2,
-                          scalar_gate=f["g"].ndim == 3)
+                          scalar_gate=f["g"].ndim == 3, gate=inp.gate)
 
 
 def oracle_bwd(inp, l2=False):
     f = inp.f64()
     cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
     return oracle.kda_bwd(f["q"], f["k"], f["v"], f["g"], f["beta"], f["h0"], f["do"], f["dhT"], cu,
-                          qk_l2norm=l2, scalar_gate=f["g"].ndim == 3)
+                          qk_l2norm=l2, scalar_gate=f["g"].ndim == 3, gate=inp.gate)
 
 
 def valid_mask(inp):
@@ -154,6 +166,9 @@ def check_bwd(inp, gr, ref, tol):
         if (~m).any():
             assert torch.isnan(gr[key].reshape(inp.B * inp.T, -1)[torch.from_numpy(~m)]).all(), \
                 f"{key}: tail written"
+    for key in ("dA_log", "dbias"):  # the KDA gate's parameter gradients
+        if gr.get(key) is not None:
+            errs[key] = assert_rel(key, gr[key].numpy(), ref[key], tol)
     if gr.get("dh0") is not None:
         errs["dh0"] = assert_rel("dh0", gr["dh0"].numpy(), ref["dh0"], tol)
         for n in empty_slots(inp):
