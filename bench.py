@@ -550,6 +550,8 @@ def main():
                     help="the same layer with the q/k L2-norm prologue inside the op")
     ap.add_argument("--scalar-gate", action="store_true",
                     help="the same layer with a scalar gate g [B, T, HV] (the GDN variant)")
+    ap.add_argument("--head-dim", type=int, default=None, choices=(64, 128),
+                    help="the same layer with K = V = this head dim (64: the pages' benchmark head dim)")
     ap.add_argument("--kda-gate", action="store_true",
                     help="the same layer with the KDA gate inside the op (raw gate, A_log and bias in, their "
                          "gradients out; unbounded)")
@@ -587,8 +589,11 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    if args.seq_len is not None or args.scalar_gate or args.kda_gate:  # another T, a scalar gate, the KDA gate
+    if args.seq_len is not None or args.scalar_gate or args.kda_gate or args.head_dim:  # a variant of the layer
         name, kw = inputs.CONFIGS[args.config]
+        if args.head_dim and args.head_dim != kw["K"]:
+            kw = dict(kw, K=args.head_dim, V=args.head_dim)
+            name = name.replace(f"K{inputs.CONFIGS[args.config][1]['K']}", f"K{args.head_dim}")
         if args.seq_len is not None:
             assert kw.get("cu_seqlens") is None and "T" in kw, "--seq-len needs a dense configuration"
             kw = dict(kw, T=args.seq_len)

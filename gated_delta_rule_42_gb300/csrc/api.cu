@@ -107,7 +107,7 @@ GateArgs gate_args(const kda_inputs *in) {
 size_t ctx_layout(const Problem &P, char *base, Workspace *W) {
   if (!use_tc(P)) return 0;
   const size_t slots = (size_t)P.NC * P.HV;
-  const size_t rec = align256(kTileRecord * slots), hs = align256(2 * slots * P.K * P.V);
+  const size_t rec = align256(kTileRecord * slots), hs = align256(2 * slots * kMaxDim * kMaxDim);
   const size_t t16 = align256(16384 * slots);
   if (base != nullptr && W != nullptr) {
     W->tc_tiles = (unsigned char *)base;
@@ -144,20 +144,20 @@ size_t layout(const Problem &P, bool kgate, bool backward, bool with_ctx, char *
     if (backward) w.dgx = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
   }
   if (kgate && use_tc(P) && backward) {  // per-slot fp32 partials of the gate's parameter gradients
-    w.gpart_b = (float *)take(sizeof(float) * slots * K);
+    w.gpart_b = (float *)take(sizeof(float) * slots * kMaxDim);
     w.gpart_a = (float *)take(sizeof(float) * slots);
   }
   if (use_tc(P)) {
     if (!with_ctx) w.tc_tiles = (unsigned char *)take(kTileRecord * slots);  // per-chunk records of the preparation kernel
     if (backward) {  // tensor-core backward: per-slot tiles passed between its kernels
       if (!with_ctx) {
-        w.tc_hs = (__nv_bfloat16 *)take(2 * slots * K * V);
+        w.tc_hs = (__nv_bfloat16 *)take(2 * slots * kMaxDim * kMaxDim);
         w.tc_xt = (unsigned char *)take(16384 * slots);
         w.tc_dt = (unsigned char *)take(16384 * slots);
       }
-      w.tc_dh = (__nv_bfloat16 *)take(2 * slots * K * V);
-      w.tc_dd = (__nv_bfloat16 *)take(2 * slots * C * V);
-      w.tc_dx = (__nv_bfloat16 *)take(2 * slots * C * V);
+      w.tc_dh = (__nv_bfloat16 *)take(2 * slots * kMaxDim * kMaxDim);  // 128-wide tiles (a 64-wide head padded)
+      w.tc_dd = (__nv_bfloat16 *)take(2 * slots * C * kMaxDim);
+      w.tc_dx = (__nv_bfloat16 *)take(2 * slots * C * kMaxDim);
       if (P.HV != P.H) {  // fp32 dq, dk partials, reduced (and normalised) per q/k head afterwards
         w.dqp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
         w.dkp = (float *)take(sizeof(float) * (size_t)P.Ttot * P.HV * K);
@@ -232,7 +232,7 @@ kda_status chunk_fwd(const kda_inputs *in, void *o, float *hT, void *ctx, size_t
   if (P.Ttot > 0 && o == nullptr && hT == nullptr)
     return fail(KDA_ERR_INVALID_ARG, "o and hT are NULL (o NULL: the final state alone, which needs hT)");
   if (use_tc(P) && ((uintptr_t)o & 15) != 0)
-    return fail(KDA_ERR_INVALID_ARG, "o must be 16-byte aligned (bf16, K = V = 128 path)");
+    return fail(KDA_ERR_INVALID_ARG, "o must be 16-byte aligned (bf16 tensor-core path)");
   const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
   with_ctx = need_ctx > 0;
   if ((st = check_ws(need_ctx, ctx, ctx_bytes, "forward context")) != KDA_OK) return st;
@@ -278,7 +278,7 @@ kda_status chunk_bwd(const kda_inputs *in, const void *ctx, size_t ctx_bytes, bo
   if (use_tc(P)) {  // the tensor-core kernels load dO by TMA and store the gradients in 4-16 byte vectors
     const char *bad = ((uintptr_t)dO & 15) ? "dO" : ((uintptr_t)dq & 15) ? "dq" : ((uintptr_t)dk & 15) ? "dk"
                       : ((uintptr_t)dv & 15) ? "dv" : (!P.scalar_gate && ((uintptr_t)dg & 15)) ? "dg" : nullptr;
-    if (bad != nullptr) return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned (bf16, K = V = 128 path)", bad);
+    if (bad != nullptr) return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned (bf16 tensor-core path)", bad);
   }
   const size_t need_ctx = with_ctx ? ctx_layout(P, nullptr, nullptr) : 0;
   with_ctx = need_ctx > 0;

@@ -104,20 +104,34 @@ __global__ void __launch_bounds__(128) kgate_grad_kernel(Problem P, GateArgs ga,
 }
 
 // Tensor-core path: dbias[j][c] and dA_log[j] from the per-slot partials the
-// gradient kernel left (slot = chunk * HV + j), summed over the valid chunks in
-// order.
-__global__ void __launch_bounds__(128) kgate_param_reduce_kernel(Problem P, Workspace W, float *__restrict__ dA_log,
+// gradient kernel left (slot = chunk * HV + j, rows 128 wide), summed over the
+// valid chunks in a fixed order.  Block (j, 32 channels): warp w sums the
+// chunks w, w + 8, ..., then the 8 warp sums are added in order; block y = 0
+// also sums the dA_log partials the same way over its 256 threads.
+__global__ void __launch_bounds__(256) kgate_param_reduce_kernel(Problem P, Workspace W, float *__restrict__ dA_log,
                                                                  float *__restrict__ dbias) {
-  const int j = blockIdx.x, c = threadIdx.x;
-  float pb = 0.f, pa = 0.f;
-  for (int ci = 0; ci < P.NC; ++ci) {
-    if (W.chunk[ci].x < 0) break;
-    const size_t slot = (size_t)ci * P.HV + j;
-    if (c < P.K) pb += W.gpart_b[slot * P.K + c];
-    pa += W.gpart_a[slot];
+  __shared__ float part[8][32];
+  __shared__ float pa_s[256];
+  const int j = blockIdx.x, lane = threadIdx.x & 31, w = threadIdx.x >> 5, c = blockIdx.y * 32 + lane;
+  const int nch = *(volatile const int *)W.flags;  // chunks mapped: the valid chunks come first
+  float pb = 0.f;
+  for (int ci = w; ci < nch; ci += 8) pb += W.gpart_b[((size_t)ci * P.HV + j) * kMaxDim + c];
+  part[w][lane] = pb;
+  float pa = 0.f;
+  if (blockIdx.y == 0)
+    for (int ci = threadIdx.x; ci < nch; ci += 256) pa += W.gpart_a[(size_t)ci * P.HV + j];
+  pa_s[threadIdx.x] = pa;
+  __syncthreads();
+  if (w == 0 && c < P.K && dbias != nullptr) {
+    float t = 0.f;
+    for (int i = 0; i < 8; ++i) t += part[i][lane];
+    dbias[(size_t)j * P.K + c] = t;
   }
-  if (c < P.K && dbias != nullptr) dbias[(size_t)j * P.K + c] = pb;
-  if (c == 0 && dA_log != nullptr) dA_log[j] = pa;
+  if (blockIdx.y == 0 && threadIdx.x == 32 && dA_log != nullptr) {
+    float t = 0.f;
+    for (int i = 0; i < 256; ++i) t += pa_s[i];
+    dA_log[j] = t;
+  }
 }
 
 }  // namespace
@@ -145,7 +159,7 @@ cudaError_t launch_kgate_param_reduce(const Problem &P, const Workspace &W, floa
                                       cudaStream_t s) {
   if ((dA_log == nullptr && dbias == nullptr) || P.NC == 0) return cudaSuccess;
   KDA_LAUNCH("kgate_param_reduce_kernel", s,
-             kgate_param_reduce_kernel<<<P.HV, 128, 0, s>>>(P, W, dA_log, dbias));
+             kgate_param_reduce_kernel<<<dim3(P.HV, (P.K + 31) / 32), 256, 0, s>>>(P, W, dA_log, dbias));
   return cudaGetLastError();
 }
 

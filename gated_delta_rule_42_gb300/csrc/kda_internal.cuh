@@ -110,6 +110,23 @@ __device__ __forceinline__ float2 kgate_grad(float x, float s, float lb) {
   }
   return make_float2(-s * kgate_sigmoid(x), -s * kgate_softplus(x));
 }
+// The same on the hardware exponential and logarithm (the bf16 tensor-core
+// path, whose results are held to bf16 accuracy; terms they drop are below
+// 2^-24 of the ones they keep).
+__device__ __forceinline__ float kgate_softplus_fast(float x) {
+  return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
+}
+__device__ __forceinline__ float kgate_sigmoid_fast(float y) { return __fdividef(1.f, 1.f + __expf(-y)); }
+__device__ __forceinline__ float kgate_fast(float x, float s, float lb) {
+  return lb < 0.f ? lb * kgate_sigmoid_fast(s * x) : -s * kgate_softplus_fast(x);
+}
+__device__ __forceinline__ float2 kgate_grad_fast(float x, float s, float lb) {
+  if (lb < 0.f) {
+    const float sg = kgate_sigmoid_fast(s * x), t = lb * sg * (1.f - sg) * s;
+    return make_float2(t, t * x);
+  }
+  return make_float2(-s * kgate_sigmoid_fast(x), -s * kgate_softplus_fast(x));
+}
 
 // --- element access -------------------------------------------------------
 __device__ __forceinline__ float ldf(const float *p, int64_t i) { return p[i]; }
@@ -202,12 +219,12 @@ cudaError_t launch_kgate_param_reduce(const Problem &P, const Workspace &W, floa
                                       cudaStream_t s);
 cudaError_t launch_group_reduce(const Problem &P, const float *dqp, const float *dkp, void *dq, void *dk,
                                 cudaStream_t s);
-// true when the tensor-core kernels handle this problem
-// The tensor-core kernels: bf16, K = V = 128, and q, k, v (and a per-channel g)
-// 16-byte aligned, since they arrive by TMA; other problems run the fp32 kernels.
+// The tensor-core kernels: bf16, K and V each 64 or 128 (a 64-wide head runs in
+// the 128-wide tiles, zero-padded), and q, k, v (and a per-channel g) 16-byte
+// aligned, since they arrive by TMA; other problems run the fp32 kernels.
 inline bool tc_eligible(const Problem &P) {
   const uintptr_t a = (uintptr_t)P.q | (uintptr_t)P.k | (uintptr_t)P.v | (P.scalar_gate ? 0 : (uintptr_t)P.g);
-  return P.bf16 && P.K == 128 && P.V == 128 && (a & 15) == 0;
+  return P.bf16 && (P.K == 64 || P.K == 128) && (P.V == 64 || P.V == 128) && (a & 15) == 0;
 }
 
 }  // namespace kda

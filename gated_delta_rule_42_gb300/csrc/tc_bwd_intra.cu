@@ -265,7 +265,7 @@ __device__ __forceinline__ void issue_gate_beta(uint32_t sbase, unsigned char *s
       *reinterpret_cast<float4 *>(G + r * kGLD + c4) = make_float4(x[u], x[u], x[u], x[u]);
     }
   } else {
-    load_gate<kCT>(sbase + C_G, P.g, q.t0, q.len, P.HV, q.j);
+    load_gate<kCT>(sbase + C_G, P.g, q.t0, q.len, P.HV, q.j, P.K);
   }
   if (tid < kC) {
     if (tid < q.len) cp4(smem_u32(beta + tid), P.beta + (size_t)(q.t0 + tid) * P.HV + q.j);
@@ -286,9 +286,10 @@ __device__ __forceinline__ float hilo(const unsigned char *tile, int a, int b) {
 __device__ __forceinline__ float2 raw_row(const Problem &P, const IntraArgs &a, int t0, int h, int t, int c,
                                           const float *rb, bool is_q) {
   (void)a;
+  if (c >= P.K) return make_float2(0.f, 0.f);  // channels past a 64-wide head
   const __nv_bfloat16 *base = (const __nv_bfloat16 *)(is_q ? P.q : P.k);
-  const float2 x = unpack_bf16(__ldg(reinterpret_cast<const unsigned int *>(base + ((size_t)(t0 + t) * P.H + h) * kD + c)));
-  float s = is_q ? 0.08838834764831845f : 1.f;
+  const float2 x = unpack_bf16(__ldg(reinterpret_cast<const unsigned int *>(base + ((size_t)(t0 + t) * P.H + h) * P.K + c)));
+  float s = is_q ? head_qscale(P.K) : 1.f;
   if (P.l2norm) s *= rb[(is_q ? kC : 0) + t];
   return make_float2(x.x * s, x.y * s);
 }
@@ -352,7 +353,7 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
   uint64_t *bar_s = (uint64_t *)(sm + C_MISC), *bar_p1 = bar_s + 1, *bar_p2 = bar_s + 2;
   uint64_t *bar_kq = bar_s + 3, *bar = bar_s + 4;
   uint32_t *tslot = (uint32_t *)(sm + C_MISC + 40);
-  constexpr float qscale = 0.08838834764831845f;
+  const float qscale = head_qscale(P.K);  // 1/sqrt(K)
   KDA_PT_DECL;
 
   if (tid == 0) {
@@ -446,7 +447,8 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
         const uint2 xv = *reinterpret_cast<const uint2 *>(sm + I_V + sw_off(r, v0, kC));
         const float2 d01 = unpack_bf16(xd.x), d23 = unpack_bf16(xd.y);
         const float2 v01 = unpack_bf16(xv.x), v23 = unpack_bf16(xv.y);
-        *reinterpret_cast<uint2 *>(args.dv + ((size_t)(t0 + r) * HV + j) * kD + v0) =
+        if (v0 < P.V)  // (a 64-wide head: the padded columns are not stored)
+          *reinterpret_cast<uint2 *>(args.dv + ((size_t)(t0 + r) * HV + j) * P.V + v0) =
             make_uint2(pack_bf16(br * d01.x, br * d01.y), pack_bf16(br * d23.x, br * d23.y));
         part = d01.x * v01.x + d01.y * v01.y + d23.x * v23.x + d23.y * v23.y;
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
@@ -488,6 +490,10 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       }
     }
     // ---- G, block references, decay tiles Kr, Qr, Kc (hi/lo) ----
+    if (kGate) {  // the decay from the raw gate
+      kgate_tile<kCT>(G, kGLD, len, P.K, j, ga);
+      __syncthreads();
+    }
     int wide_c = 0;
     if (tid < kD) {
       const int c = tid;
@@ -495,12 +501,6 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
       float col[kC];
 #pragma unroll
       for (int r = 0; r < kC; ++r) col[r] = G[r * kGLD + c];
-      if (kGate) {  // the decay from the raw gate
-        const float sc = kgate_scale(ga, j), b = kgate_bias(ga, kD, j, c);
-#pragma unroll
-        for (int r = 0; r < kC; ++r)
-          if (r < len) col[r] = kgate(col[r] + b, sc, ga.lb);
-      }
 #pragma unroll
       for (int r = 0; r < kC; ++r) {
         if (r < len) s += col[r];
@@ -923,22 +923,22 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
             *krl_p = __float_as_uint(qv[1]);
             *qrh_p = __float_as_uint(pv[0]);
             *qrl_p = __float_as_uint(pv[1]);
-            if (r < len) {
+            if (r < len && c < P.K) {  // (a 64-wide head: the padded channels are not stored)
               const size_t tok = (size_t)(t0 + r);
               if (kL2) {  // dx = r (dy - y (y . dy)), y_q = Qr / e1 / qscale, y_k = Kr / e1
                 const float rk = rb[r], rq = rb[kC + r], dq_dot = dotq[hh] / qscale;
-                __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
-                __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
+                __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * P.K + c;
+                __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * P.K + c;
                 *reinterpret_cast<uint32_t *>(pq) = pack_bf16(rq * (dq2[0] * qscale - yq[0] * dq_dot),
                                                             rq * (dq2[1] * qscale - yq[1] * dq_dot));
                 *reinterpret_cast<uint32_t *>(pk) = pack_bf16(rk * (dk2[0] - yk[0] * dotk[hh]), rk * (dk2[1] - yk[1] * dotk[hh]));
               } else if (args.partial) {
-                float *pq = (float *)args.dq + (tok * HV + j) * kD + c, *pk = (float *)args.dk + (tok * HV + j) * kD + c;
+                float *pq = (float *)args.dq + (tok * HV + j) * P.K + c, *pk = (float *)args.dk + (tok * HV + j) * P.K + c;
                 *reinterpret_cast<float2 *>(pq) = make_float2(dq2[0], dq2[1]);  // scaled in the group reduction
                 *reinterpret_cast<float2 *>(pk) = make_float2(dk2[0], dk2[1]);
               } else {
-                __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * kD + c;
-                __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * kD + c;
+                __nv_bfloat16 *pq = (__nv_bfloat16 *)args.dq + (tok * H + h) * P.K + c;
+                __nv_bfloat16 *pk = (__nv_bfloat16 *)args.dk + (tok * H + h) * P.K + c;
                 *reinterpret_cast<uint32_t *>(pq) = pack_bf16(dq2[0] * qscale, dq2[1] * qscale);
                 *reinterpret_cast<uint32_t *>(pk) = pack_bf16(dk2[0], dk2[1]);
               }
@@ -1035,13 +1035,13 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
           if (lane == k) sg_part = t;
-        } else if (r < len) {
-          const size_t e = ((size_t)(t0 + r) * HV + j) * kD + c;
+        } else if (r < len && c < P.K) {  // (a 64-wide head: the padded channels are not stored)
+          const size_t e = ((size_t)(t0 + r) * HV + j) * P.K + c;
           if (kGate) {  // da = dG dg/da; the parameter gradients' partials
             const float2 a2 = __ldg(reinterpret_cast<const float2 *>(P.g + e));
             const float sc = kgate_scale(ga, j);
-            const float2 d0 = kgate_grad(a2.x + kgate_bias(ga, kD, j, c), sc, ga.lb);
-            const float2 d1 = kgate_grad(a2.y + kgate_bias(ga, kD, j, c + 1), sc, ga.lb);
+            const float2 d0 = kgate_grad_fast(a2.x + kgate_bias(ga, P.K, j, c), sc, ga.lb);
+            const float2 d1 = kgate_grad_fast(a2.y + kgate_bias(ga, P.K, j, c + 1), sc, ga.lb);
             const float2 da = make_float2(v.x * d0.x, v.y * d1.x);
             *reinterpret_cast<float2 *>(args.dg + e) = da;
             gpb.x += da.x;

@@ -75,13 +75,14 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const float *__restrict__ dhT, fl
   const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
   uint32_t phase = 0, ld_par = 0;
 
-  float dreg[64];  // dh'[cown][64 * vhalf + x]
+  float dreg[64];  // dh'[cown][64 * vhalf + x]; rows past K and columns past V (a 64-wide head) stay zero
+  const bool hlive = cown < P.K && 64 * vhalf < P.V;
   {
-    const size_t base = (((size_t)n * HV + j) * kD + cown) * kD + 64 * vhalf;
+    const size_t base = (((size_t)n * HV + j) * P.K + cown) * P.V + 64 * vhalf;
 #pragma unroll
     for (int x = 0; x < 64; x += 4) {
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (dhT != nullptr) t = *reinterpret_cast<const float4 *>(dhT + base + x);
+      if (dhT != nullptr && hlive) t = *reinterpret_cast<const float4 *>(dhT + base + x);
       dreg[x] = t.x; dreg[x + 1] = t.y; dreg[x + 2] = t.z; dreg[x + 3] = t.w;
     }
   }
@@ -207,8 +208,8 @@ kda_bwd_scan_tc_kernel(Problem P, Workspace W, const float *__restrict__ dhT, fl
     fence_after();
   }
 
-  if (dh0 != nullptr) {
-    float *dst = dh0 + (((size_t)n * HV + j) * kD + cown) * kD + 64 * vhalf;
+  if (dh0 != nullptr && hlive) {
+    float *dst = dh0 + (((size_t)n * HV + j) * P.K + cown) * P.V + 64 * vhalf;
 #pragma unroll
     for (int x = 0; x < 64; x += 4)
       *reinterpret_cast<float4 *>(dst + x) = make_float4(dreg[x], dreg[x + 1], dreg[x + 2], dreg[x + 3]);

@@ -66,10 +66,25 @@ static __shared__ long long kda_pt_acc[33];  // [32] = time of the last stamp
 #endif
 
 constexpr int kC = 64;     // chunk
-constexpr int kD = 128;    // K = V
+constexpr int kD = 128;    // the tiles' K = V (a 64-wide head is zero-padded to it)
 constexpr int kThr = 256;  // 8 warps
 constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile of the per-chunk gradient kernel
 constexpr int kGT = 128;   // row stride of the TMA-loaded gate tile (dense rows)
+
+// The KDA gate over a chunk's [64][ld] gate tile in shared memory (raw
+// pre-activations in, the per-token log2 decay out), elementwise over the
+// block's NT threads: rows < len, channels < K (the rest is never summed).
+template <int NT>
+__device__ __forceinline__ void kgate_tile(float *G, int ld, int len, int K, int j, const GateArgs &ga) {
+  static_assert(NT % 128 == 0, "each thread keeps one channel");
+  const int c = threadIdx.x & 127;
+  if (c >= K) return;
+  const float sc = kgate_scale(ga, j), b = kgate_bias(ga, K, j, c);
+  for (int r = threadIdx.x >> 7; r < len; r += NT / 128) G[r * ld + c] = kgate_fast(G[r * ld + c] + b, sc, ga.lb);
+}
+
+// 1 / sqrt(K) for the head dims of the tensor-core path (64 or 128), exactly.
+__host__ __device__ __forceinline__ float head_qscale(int K) { return K == 64 ? 0.125f : 0.08838834764831845f; }
 
 // rows of the per-channel vector table of the per-chunk gradient kernel: G_last,
 // 2^G_last, the row references Gr(R) and 2^Gr(R), the block-pair factors D_RI,
@@ -121,14 +136,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Asynchronous loads of one chunk's gate rows ([tokens][HV][128] fp32) into a
-// [64][kGLD] tile; rows at or past len are zeroed.
+// Asynchronous loads of one chunk's gate rows ([tokens][HV][K] fp32, K = 64 or
+// 128) into a [64][kGLD] tile; rows at or past len and channels past K are zeroed.
 template <int NT = kThr>
-__device__ __forceinline__ void load_gate(uint32_t tile, const float *g, int t0, int len, int HV, int j) {
+__device__ __forceinline__ void load_gate(uint32_t tile, const float *g, int t0, int len, int HV, int j, int K) {
   for (int it = threadIdx.x; it < kC * 32; it += NT) {
     const int r = it >> 5, jj = it & 31;
     const uint32_t dst = tile + (uint32_t)(r * kGLD + jj * 4) * 4u;
-    if (r < len) cp16(dst, g + ((size_t)(t0 + r) * HV + j) * kD + jj * 4);
+    if (r < len && jj * 4 < K) cp16(dst, g + ((size_t)(t0 + r) * HV + j) * K + jj * 4);
     else st_zero16(dst);
   }
 }

@@ -95,13 +95,14 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
   uint32_t phase = 0, phase_o = 0, ld_par = 0;
   KDA_PT_DECL;
 
-  float hreg[64];  // h[cown][64 * vhalf + x]
+  float hreg[64];  // h[cown][64 * vhalf + x]; rows past K and columns past V (a 64-wide head) stay zero
+  const bool hlive = cown < P.K && 64 * vhalf < P.V;
   {
-    const size_t base = (((size_t)n * HV + j) * kD + cown) * kD + 64 * vhalf;
+    const size_t base = (((size_t)n * HV + j) * P.K + cown) * P.V + 64 * vhalf;
 #pragma unroll
     for (int x = 0; x < 64; x += 4) {
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (P.h0 != nullptr) t = *reinterpret_cast<const float4 *>(P.h0 + base + x);
+      if (P.h0 != nullptr && hlive) t = *reinterpret_cast<const float4 *>(P.h0 + base + x);
       hreg[x] = t.x; hreg[x + 1] = t.y; hreg[x + 2] = t.z; hreg[x + 3] = t.w;
     }
   }
@@ -279,9 +280,10 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
       __syncthreads();
       fence_after();
       const uint4 *Os = (const uint4 *)(sm + S_H);
-      for (int it = tid; it < len * 16; it += kThr) {
-        const int r = it >> 4, jj = it & 15;
-        *reinterpret_cast<uint4 *>(args.o + ((size_t)(t0 + r) * HV + j) * kD + jj * 8) = Os[r * 16 + jj];
+      const int vq = P.V >> 3;  // 16-byte chunks of an output row (the padded columns are not stored)
+      for (int it = tid; it < len * vq; it += kThr) {
+        const int r = it / vq, jj = it - r * vq;
+        *reinterpret_cast<uint4 *>(args.o + ((size_t)(t0 + r) * HV + j) * P.V + jj * 8) = Os[r * 16 + jj];
       }
     }
     fence_before();
@@ -290,8 +292,8 @@ kda_fwd_tc_kernel(Problem P, Workspace W, FwdArgs args, const __grid_constant__ 
     KDA_PT(6);
   }
 
-  if (args.hT != nullptr) {
-    float *dst = args.hT + (((size_t)n * HV + j) * kD + cown) * kD + 64 * vhalf;
+  if (args.hT != nullptr && hlive) {
+    float *dst = args.hT + (((size_t)n * HV + j) * P.K + cown) * P.V + 64 * vhalf;
 #pragma unroll
     for (int x = 0; x < 64; x += 4)
       *reinterpret_cast<float4 *>(dst + x) = make_float4(hreg[x], hreg[x + 1], hreg[x + 2], hreg[x + 3]);

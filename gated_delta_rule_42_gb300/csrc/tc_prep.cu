@@ -100,24 +100,21 @@ __device__ __forceinline__ void l2norm_row16(float (&kv)[8], float (&qv)[8]) {
 // cumsum) when a block's span exceeds kSpanMax: the slot is left to the fix-up.
 template <bool kGate>
 __device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec, bool l2n,
-                                       const GateArgs &ga) {
+                                       const GateArgs &ga, float qscale, int K) {
   const int tid = threadIdx.x;
   int wide_c = 0;
   float *G = (float *)(sm + P_G);
   float *vec = (float *)(sm + P_VEC);
-  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
+  if (kGate) {  // the decay from the raw gate (KDA_GATE_IN_KERNEL); value head blockIdx.y
+    kgate_tile<kThr>(G, kGT, len, K, blockIdx.y, ga);
+    __syncthreads();
+  }
   if (tid < kD) {  // one thread per channel (a warp reads 32 consecutive channels: no bank conflicts)
     const int c = tid;
     float col[kC];
     float s = 0.f;
 #pragma unroll
     for (int r = 0; r < kC; ++r) col[r] = G[r * kGT + c];
-    if (kGate) {  // the decay from the raw gate (KDA_GATE_IN_KERNEL); value head blockIdx.y
-      const float sc = kgate_scale(ga, blockIdx.y), b = kgate_bias(ga, kD, blockIdx.y, c);
-#pragma unroll
-      for (int r = 0; r < kC; ++r)
-        if (r < len) col[r] = kgate(col[r] + b, sc, ga.lb);
-    }
 #pragma unroll
     for (int r = 0; r < kC; ++r) {
       if (r < len) s += col[r];
@@ -451,7 +448,7 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
   KDA_PT(0);
 
   unsigned char *rec = W.tc_tiles + slot * kTileRecord;
-  if (phase_a<kGate>(sm, len, beta, rec, P.l2norm, ga)) {
+  if (phase_a<kGate>(sm, len, beta, rec, P.l2norm, ga, head_qscale(P.K), P.K)) {
     if (tid == 0) W.wide_rec[atomicAdd(W.flags + 3, 1)] = (int)slot;
     return;
   }
@@ -467,23 +464,21 @@ kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ Tma
 // reference Gr and its last row as the column reference Gc on every channel,
 // so that e1, e2 and every off-diagonal factor are <= 1.
 __device__ __forceinline__ void fix_phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec,
-                                            bool l2n, const GateArgs &ga, int j) {
+                                            bool l2n, const GateArgs &ga, int j, int K) {
   const int tid = threadIdx.x;
   float *G = (float *)(sm + P_G);
   float *vec = (float *)(sm + P_VEC);
-  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
+  if (ga.on) {  // the decay from the raw gate (KDA_GATE_IN_KERNEL)
+    kgate_tile<kThr>(G, kGT, len, K, j, ga);
+    __syncthreads();
+  }
+  const float qscale = head_qscale(K);
   if (tid < kD) {
     const int c = tid;
     float col[kC];
     float s = 0.f;
 #pragma unroll
     for (int r = 0; r < kC; ++r) col[r] = G[r * kGT + c];
-    if (ga.on) {  // the decay from the raw gate (KDA_GATE_IN_KERNEL)
-      const float sc = kgate_scale(ga, j), b = kgate_bias(ga, kD, j, c);
-#pragma unroll
-      for (int r = 0; r < kC; ++r)
-        if (r < len) col[r] = kgate(col[r] + b, sc, ga.lb);
-    }
 #pragma unroll
     for (int r = 0; r < kC; ++r) {
       if (r < len) s += col[r];
@@ -576,10 +571,12 @@ __device__ __forceinline__ void fix_phase_a(unsigned char *sm, int len, const fl
 __device__ __noinline__ void diag_direct(const Problem &P, const GateArgs &ga, int t0, int len, int h, int j, int R,
                                          const float *beta, float *Lf, unsigned char *rec) {
   const int lane = threadIdx.x & 31, c0 = lane * 4;
-  constexpr float qscale = 0.08838834764831845f;  // 1/sqrt(128)
+  const float qscale = head_qscale(P.K);
   const __nv_bfloat16 *kp = (const __nv_bfloat16 *)P.k, *qp = (const __nv_bfloat16 *)P.q;
+  const bool live = c0 < P.K;  // channels past K (a zero-padded 64-wide head) stay zero
   auto ld4 = [&](const __nv_bfloat16 *base, int r, float (&x)[4]) {  // row r of the chunk, this lane's channels
-    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(base + ((size_t)(t0 + r) * P.H + h) * kD + c0));
+    const uint2 u = live ? __ldg(reinterpret_cast<const uint2 *>(base + ((size_t)(t0 + r) * P.H + h) * P.K + c0))
+                         : make_uint2(0u, 0u);
     const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y);
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
   };
@@ -624,14 +621,14 @@ __device__ __noinline__ void diag_direct(const Problem &P, const GateArgs &ga, i
           const float a = exp2f(__ldg(P.g + row));
 #pragma unroll
           for (int e = 0; e < 4; ++e) F[e] *= a;
-        } else {
-          float4 g4 = __ldg(reinterpret_cast<const float4 *>(P.g + row * kD + c0));
+        } else if (live) {
+          float4 g4 = __ldg(reinterpret_cast<const float4 *>(P.g + row * P.K + c0));
           if (ga.on) {  // the KDA gate: g holds the raw pre-activations
             const float sc = kgate_scale(ga, j);
-            g4.x = kgate(g4.x + kgate_bias(ga, kD, j, c0), sc, ga.lb);
-            g4.y = kgate(g4.y + kgate_bias(ga, kD, j, c0 + 1), sc, ga.lb);
-            g4.z = kgate(g4.z + kgate_bias(ga, kD, j, c0 + 2), sc, ga.lb);
-            g4.w = kgate(g4.w + kgate_bias(ga, kD, j, c0 + 3), sc, ga.lb);
+            g4.x = kgate_fast(g4.x + kgate_bias(ga, P.K, j, c0), sc, ga.lb);
+            g4.y = kgate_fast(g4.y + kgate_bias(ga, P.K, j, c0 + 1), sc, ga.lb);
+            g4.z = kgate_fast(g4.z + kgate_bias(ga, P.K, j, c0 + 2), sc, ga.lb);
+            g4.w = kgate_fast(g4.w + kgate_bias(ga, P.K, j, c0 + 3), sc, ga.lb);
           }
           F[0] *= exp2f(g4.x); F[1] *= exp2f(g4.y); F[2] *= exp2f(g4.z); F[3] *= exp2f(g4.w);
         }
@@ -750,7 +747,7 @@ kda_prep_tc_fix_kernel(Problem P, Workspace W, int *err, const __grid_constant__
     const int4 ch = W.chunk[c_idx];
     load_slot(P, maps, sm, bar, parity, err, ch.y, ch.z, h, j);
     unsigned char *rec = W.tc_tiles + (size_t)s * kTileRecord;
-    fix_phase_a(sm, ch.z, beta, rec, P.l2norm, ga, j);
+    fix_phase_a(sm, ch.z, beta, rec, P.l2norm, ga, j, P.K);
     fix_phase_b(sm, beta, rec, P, ga, ch.y, ch.z, h, j);
     __syncthreads();  // the shared tiles are free for the next slot
   }

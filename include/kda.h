@@ -34,10 +34,12 @@
  *   g, dg          [B][T][HV][K]     fp32  ([B][T][HV] with KDA_SCALAR_GATE)
  *   beta, dbeta    [B][T][HV]        fp32
  *   h0,hT,dhT,dh0  [N][HV][K][V]     fp32
- * The bf16 K = V = 128 problems run the tensor-core kernels when q, k, v and g
- * are 16-byte aligned (they arrive by TMA); otherwise the general kernels run,
- * with the same results.  On the tensor-core path o, dO, dq, dk, dv and (per-
- * channel gate) dg must be 16-byte aligned too (KDA_ERR_INVALID_ARG otherwise).
+ * bf16 problems with K and V each 64 or 128 run the tensor-core kernels when
+ * q, k, v and g are 16-byte aligned (they arrive by TMA; a 64-wide head runs
+ * zero-padded in the 128-wide tiles); otherwise the general kernels run, with
+ * the same results (kda_uses_tensor_cores() tells which).  On the tensor-core
+ * path o, dO, dq, dk, dv and (per-channel gate) dg must be 16-byte aligned too
+ * (KDA_ERR_INVALID_ARG otherwise).
  * Value head j reads query/key head j / (HV/H) (contiguous groups).
  * dq and dk are summed over the HV/H value heads that share a q/k head.
  *
@@ -125,7 +127,7 @@ typedef struct kda_gate {
 typedef struct kda_inputs {
   int B, T;         /* batch and (padded) tokens per batch row; B must be 1 with cu_seqlens */
   int H, HV;        /* query/key heads and value heads; HV must be a multiple of H          */
-  int K, V;         /* key and value head dims: 1..128 each (bf16 fast path: K = V = 128)    */
+  int K, V;         /* key and value head dims: 1..128 each (tensor cores: 64 or 128, bf16)   */
   int N;            /* logical sequences: B when cu_seqlens is NULL, else len(cu_seqlens)-1   */
   kda_dtype dtype;  /* element type of q, k, v, o, dO, dq, dk, dv                            */
   const void *q, *k, *v;
@@ -259,11 +261,11 @@ kda_status kda_state_compose(const float *M, const float *h, const float *c, flo
 size_t kda_status_offset(const kda_inputs *in);
 
 /* Which kernels a call on these inputs runs: 1 for the tensor-core kernels
- * (bf16, K = V = 128, with q, k, v and a per-channel g 16-byte aligned), 0 for
- * the general fp32 kernels (same results, several times slower), -1 if the
- * problem is invalid.  A bf16 K = V = 128 problem whose inputs are a slice of
- * a larger tensor starting off a 16-byte boundary runs the general kernels:
- * this tells the caller so before the call. */
+ * (bf16, K and V each 64 or 128, with q, k, v and a per-channel g 16-byte
+ * aligned), 0 for the general fp32 kernels (same results, several times
+ * slower), -1 if the problem is invalid.  A bf16 problem whose inputs are a
+ * slice of a larger tensor starting off a 16-byte boundary runs the general
+ * kernels: this tells the caller so before the call. */
 int kda_uses_tensor_cores(const kda_inputs *in);
 
 /* Static description of a status code. */

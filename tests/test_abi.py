@@ -102,10 +102,10 @@ def test_l2norm_flag_workspace(lib):
     of q and k (two more [T][H][K] buffers); the bf16 tensor-core path
     normalises in its kernels, and with HV = H fuses the norm's backward into
     the gradient kernel, so its workspace does not change."""
-    s0 = _inputs(K=64, V=64)
-    s1 = _inputs(K=64, V=64, flags=_lib.KDA_QK_L2NORM)
+    s0 = _inputs(K=64, V=64, dtype=_lib.KDA_F32)
+    s1 = _inputs(K=64, V=64, dtype=_lib.KDA_F32, flags=_lib.KDA_QK_L2NORM)
     extra = lib.kda_chunk_fwd_workspace_size(ctypes.byref(s1)) - lib.kda_chunk_fwd_workspace_size(ctypes.byref(s0))
-    assert extra >= 2 * 128 * 2 * 64 * 2
+    assert extra >= 2 * 128 * 2 * 64 * 4
     t0 = _inputs(K=128, V=128, HV=2)
     t1 = _inputs(K=128, V=128, HV=2, flags=_lib.KDA_QK_L2NORM)
     assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(t1)) == lib.kda_chunk_fwd_workspace_size(ctypes.byref(t0))
@@ -155,8 +155,10 @@ def test_forward_context_sizes(lib):
     bc = lib.kda_chunk_bwd_ctx_workspace_size(ctypes.byref(s))
     assert f - fc == _a256(66048 * slots)
     assert b - bc == ctx
-    for kw in (dict(K=64, V=64), dict(K=128, V=128, dtype=_lib.KDA_F32), dict(K=128, V=128, v=0x1008)):
-        g = _inputs(T=200, **kw)                # general path: fp32, K != 128, or a misaligned v
+    # a 64-wide head runs in the same 128-wide tiles: the same context
+    assert lib.kda_chunk_ctx_size(ctypes.byref(_inputs(K=64, V=64, T=200))) == ctx
+    for kw in (dict(K=96, V=96), dict(K=128, V=128, dtype=_lib.KDA_F32), dict(K=128, V=128, v=0x1008)):
+        g = _inputs(T=200, **kw)                # general path: fp32, K not 64 or 128, or a misaligned v
         assert lib.kda_chunk_ctx_size(ctypes.byref(g)) == 0
         assert lib.kda_chunk_fwd_ctx_workspace_size(ctypes.byref(g)) == lib.kda_chunk_fwd_workspace_size(ctypes.byref(g))
         assert lib.kda_chunk_bwd_ctx_workspace_size(ctypes.byref(g)) == lib.kda_chunk_bwd_workspace_size(ctypes.byref(g))
@@ -177,7 +179,7 @@ def test_forward_context_checks(lib):
         st = lib.kda_chunk_bwd_ctx(ctypes.byref(s), ctx, nbytes, fake[0], None, *fake[1:6], None, ws, 1 << 30, None)
         assert st == _lib.KDA_ERR_WORKSPACE, lib.kda_last_error()
     # a general-path problem keeps nothing: a NULL context is fine up to the workspace check
-    g = _inputs(K=64, V=64)
+    g = _inputs(K=64, V=64, dtype=_lib.KDA_F32)
     st = lib.kda_chunk_fwd_ctx(ctypes.byref(g), o, None, None, 0, None, 0, None)
     assert st == _lib.KDA_ERR_WORKSPACE and b"workspace is NULL" in lib.kda_last_error()
 
@@ -256,11 +258,12 @@ def test_bounded_wait_probe_validation(lib):
 
 
 def test_kernel_family_query(lib):
-    """bf16 K = V = 128 with 16-byte aligned q, k, v, g runs the tensor-core
-    kernels; an fp32 problem, other head dims or a misaligned input the general ones."""
-    s = _inputs(K=128, V=128)
-    assert lib.kda_uses_tensor_cores(ctypes.byref(s)) == 1
+    """bf16 with K and V each 64 or 128 and 16-byte aligned q, k, v, g runs the
+    tensor-core kernels; an fp32 problem, other head dims or a misaligned input
+    the general ones."""
+    for K, V in ((128, 128), (64, 64), (64, 128), (128, 64)):
+        assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs(K=K, V=V))) == 1, (K, V)
     assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs(K=128, V=128, dtype=_lib.KDA_F32))) == 0
-    assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs())) == 0  # K = V = 64
+    assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs(K=96, V=96))) == 0
     assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs(K=128, V=128, q=0x1002))) == 0
     assert lib.kda_uses_tensor_cores(ctypes.byref(_inputs(HV=3))) == -1

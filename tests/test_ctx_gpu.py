@@ -40,7 +40,8 @@ CASES = [
     ("tc_l2norm", dict(B=1, T=200, H=1, HV=2, K=128, V=128), True, False),
     ("tc_l2norm_fused", dict(B=1, T=200, H=2, HV=2, K=128, V=128), True, True),
     ("tc_scalar_gate", dict(B=1, T=190, H=2, HV=4, K=128, V=128, scalar_gate=True), False, True),
-    ("general_bf16_k64", dict(B=1, T=150, H=1, HV=2, K=64, V=64), False, True),
+    ("tc_bf16_k64", dict(B=1, T=150, H=1, HV=2, K=64, V=64), False, True),
+    ("general_bf16_k96", dict(B=1, T=150, H=1, HV=2, K=96, V=96), False, True),
     ("general_fp32", dict(B=1, T=100, H=1, HV=2, K=128, V=128, dtype=torch.float32), False, True),
 ]
 
@@ -53,7 +54,7 @@ def test_context_pair_matches_recompute_bitwise(name, kw, l2, states):
     inp = inputs.make_inputs(dtype=dtype, seed=zlib.crc32(name.encode()) % 1000, name=name, **kw, **extra)
     want_dh0 = inp.h0 is not None
     o, hT, grads, nctx = H.gpu_fwd_bwd_ctx(inp, l2=l2, want_dh0=want_dh0, backwards=2)
-    tc = dtype == torch.bfloat16 and kw["K"] == 128 and kw["V"] == 128
+    tc = dtype == torch.bfloat16 and kw["K"] in (64, 128) and kw["V"] in (64, 128)
     assert (nctx > 0) == tc
     o2, hT2 = H.gpu_fwd(inp, l2=l2)
     _same("o", o, o2)
