@@ -61,6 +61,20 @@ static_assert(T_YR == T_XR + 64, "xr and yr are one N = 128 product");
 constexpr uint32_t CK_DA = C_DAB, CK_DAQK = C_DAB + 8192;
 static_assert(CK_DAQK + 8192 + LO128 <= C_XB, "dA/dL and dAqk with their lo twins");
 constexpr float kLn2 = 0.69314718055994530942f;
+// The gate tile arrives by TMA with group P2: dense [64][128] fp32 rows (rows
+// past the chunk hold other tokens until the cumsum overwrites them).
+constexpr int kGD = kGT;
+constexpr uint32_t kBytesG = kC * kD * 4u;
+static_assert(kC * kGD * 4 <= C_A - C_G, "the dense gate tile fits the padded one's place");
+// beta of a slot (cp.async from 64 threads; zero past len)
+__device__ __forceinline__ void issue_beta(float *beta, const Problem &P, const Slot &q) {
+  const int tid = threadIdx.x;
+  if (tid < kC) {
+    if (tid < q.len) cp4(smem_u32(beta + tid), P.beta + (size_t)(q.t0 + tid) * P.HV + q.j);
+    else beta[tid] = 0.f;
+  }
+  cp_commit();
+}
 // Rows of the vector table this kernel uses: G_last, 2^G_last, m, 2^m,
 // 2^(G_last - m); the dg scan's block totals (Q, P, Khat term) x 4 blocks go to
 // twelve rows it leaves free.
@@ -159,12 +173,13 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     if (tid == 0) {
       mbar_expect_tx(bar_s, kBytesS);
       mbar_expect_tx(bar_p1, kBytesP1);
-      mbar_expect_tx(bar_p2, kBytesP2);
+      mbar_expect_tx(bar_p2, kBytesP2 + kBytesG);
       for (int i = 0; i < kCopiesS; ++i) copy_s(i, sbase, W, maps, cur, bar_s);
       for (int i = 0; i < kCopiesP1; ++i) copy_p1(i, sbase, W, maps, cur, bar_p1);
       for (int i = 0; i < kCopiesP2; ++i) copy_p2(i, sbase, W, maps, cur, bar_p2);
+      tma_load3(sbase + C_G, &maps.g, 0, cur.j, cur.t0, bar_p2);
     }
-    issue_gate_beta<false>(sbase, sm, P, beta, cur);
+    issue_beta(beta, P, cur);
   }
   for (uint32_t it = 0; have; ++it) {
     const uint32_t par = it & 1u;
@@ -181,7 +196,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
         const int r = 64 + len + (it2 >> 4), q = it2 & 15;
         *reinterpret_cast<uint4 *>(sm + I_STK + sw_chunk(r, q, 192)) = make_uint4(0, 0, 0, 0);
       }
-    cp_wait_all();  // G, beta
+    cp_wait_all();  // beta
     fence_async_smem();
     fence_before();
     __syncthreads();
@@ -245,7 +260,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     KDA_PT(0);
 
     // ---- raw k, q rows; dA, dAqk out of TMEM as hi/lo tiles; the gate; G and the reference ----
-    if (tid == 0) {
+    if (tid == 0) {  // (into the dh' and v tiles, dead now)
       fence_async_smem();
       mbar_expect_tx(bar_kq, 32768u);
       tma_tile(sbase + C_KRAW, &maps.k, h, t0, bar_kq);
@@ -273,7 +288,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       }
     }
     if (kGate) {  // the decay from the raw gate
-      kgate_tile<kCT>(G, kGLD, len, P.K, j, ga);
+      kgate_tile<kCT>(G, kGD, len, P.K, j, ga);
       __syncthreads();
     }
     int wide_c = 0;
@@ -282,14 +297,14 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       float s = 0.f;
       float col[kC];
 #pragma unroll
-      for (int r = 0; r < kC; ++r) col[r] = G[r * kGLD + c];
+      for (int r = 0; r < kC; ++r) col[r] = G[r * kGD + c];
 #pragma unroll
       for (int r = 0; r < kC; ++r) {
         if (r < len) s += col[r];
         col[r] = s;
       }
 #pragma unroll
-      for (int r = 0; r < kC; ++r) G[r * kGLD + c] = col[r];
+      for (int r = 0; r < kC; ++r) G[r * kGD + c] = col[r];
       const float gl = s, m = 0.5f * (col[0] + gl);  // rows past len hold G_last
       wide_c = !(col[0] - gl <= kChunkSpan);        // (NaN-safe)
       vec[V_GL * kD + c] = gl;
@@ -341,7 +356,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float g = G[r * kGLD + c0 + e];
+          const float g = G[r * kGD + c0 + e];
           e1[e] = ex2(g - mv[e]);  // within 2^(+-kChunkSpan/2)
           e2[e] = ex2(mv[e] - g);
         }
@@ -476,6 +491,8 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     float qv[16], pv[16], bp[16];  // dG's Q and P parts, dbeta partials of the 16 rows
     float cq = 0.f;                // sum over the rows of dKhat k khat
     const bool cin = c < P.K;      // (a 64-wide head: the padded channels are not stored)
+    const bool odd = (lane & 1) != 0;
+    const int cp = c & ~1;         // the channel pair a store covers
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4) {
       float tb[4], tg[4], th[4], tx[4], ty[4], tz[4];  // -dBk, dQg, dKhat, xr, yr, xyi
@@ -490,7 +507,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
                                      make_float2(bf_at(sm + C_KR + LO128, o0), bf_at(sm + C_KR + LO128, o1)));
         const float2 Qr = __fadd2_rn(make_float2(bf_at(sm + C_QR, o0), bf_at(sm + C_QR, o1)),
                                      make_float2(bf_at(sm + C_QR + LO128, o0), bf_at(sm + C_QR + LO128, o1)));
-        const float2 d = __fadd2_rn(make_float2(G[r * kGLD + c], G[(r + 1) * kGLD + c]), ngm);  // G - m
+        const float2 d = __fadd2_rn(make_float2(G[r * kGD + c], G[(r + 1) * kGD + c]), ngm);  // G - m
         const float2 e1 = make_float2(ex2(d.x), ex2(d.y)), e2 = make_float2(ex2(-d.x), ex2(-d.y));
         const float2 Kc = __fmul2_rn(__fmul2_rn(Kr, e2), e2);
         const float2 br = u == 0 ? make_float2(b4.x, b4.y) : make_float2(b4.z, b4.w);
@@ -519,20 +536,32 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
         cq += (in0 ? kht.x : 0.f) + (in1 ? kht.y : 0.f);
         bp[t] = bq.x;
         bp[t + 1] = bq.y;
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          if ((w ? in1 : in0) && cin) {
-            const size_t tok = (size_t)(t0 + r + w);
-            const float vq = w ? dq2.y : dq2.x, vk = w ? dk2.y : dk2.x;
-            if (args.partial) {
-              ((float *)args.dq)[(tok * HV + j) * P.K + c] = vq;  // scaled in the group reduction
-              ((float *)args.dk)[(tok * HV + j) * P.K + c] = vk;
+        {  // lanes (c, c + 1) trade one value: the even lane stores row r, the odd lane row r + 1,
+           // each as the channel pair (c & ~1, c | 1)
+          const float gq = __shfl_xor_sync(0xffffffffu, odd ? dq2.x : dq2.y, 1);
+          const float gk = __shfl_xor_sync(0xffffffffu, odd ? dk2.x : dk2.y, 1);
+          const float2 pq = odd ? make_float2(gq, dq2.y) : make_float2(dq2.x, gq);
+          const float2 pk = odd ? make_float2(gk, dk2.y) : make_float2(dk2.x, gk);
+          if ((odd ? in1 : in0) && cin) {
+            const size_t tok = (size_t)(t0 + r + (odd ? 1 : 0));
+            if (args.partial) {  // (scaled in the group reduction)
+              *reinterpret_cast<float2 *>((float *)args.dq + (tok * HV + j) * P.K + cp) = pq;
+              *reinterpret_cast<float2 *>((float *)args.dk + (tok * HV + j) * P.K + cp) = pk;
             } else {
-              ((__nv_bfloat16 *)args.dq)[(tok * H + h) * P.K + c] = __float2bfloat16_rn(vq * qscale);
-              ((__nv_bfloat16 *)args.dk)[(tok * H + h) * P.K + c] = __float2bfloat16_rn(vk);
+              *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dq + (tok * H + h) * P.K + cp) =
+                  pack_bf16(pq.x * qscale, pq.y * qscale);
+              *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dk + (tok * H + h) * P.K + cp) = pack_bf16(pk.x, pk.y);
             }
           }
         }
+      }
+    }
+    float ar[16];  // kGate: the raw gate of this thread's rows, for the dg scan (loaded before it)
+    if (kGate) {
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int r = 16 * R + t;
+        ar[t] = (r < len && cin) ? __ldg(P.g + ((size_t)(t0 + r) * HV + j) * P.K + c) : 0.f;
       }
     }
     KDA_PT(9);
@@ -558,15 +587,16 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     KDA_PT(10);
     if (more) {  // the next slot's remaining inputs into the dead tiles; its G and beta
       if (tid == 0) {
-        mbar_expect_tx(bar_p2, kBytesP2);
+        mbar_expect_tx(bar_p2, kBytesP2 + kBytesG);
         mbar_expect_tx(bar_s, kBytesS);
       }
-      if (lane == 0 && warp >= 1 && warp <= kCopiesP2 + kCopiesS) {
+      if (lane == 0 && warp >= 1 && warp <= kCopiesP2 + kCopiesS + 1) {
         fence_async_smem();
         if (warp <= kCopiesP2) copy_p2(warp - 1, sbase, W, maps, nxt, bar_p2);
-        else copy_s(warp - 1 - kCopiesP2, sbase, W, maps, nxt, bar_s);
+        else if (warp <= kCopiesP2 + kCopiesS) copy_s(warp - 1 - kCopiesP2, sbase, W, maps, nxt, bar_s);
+        else tma_load3(sbase + C_G, &maps.g, 0, nxt.j, nxt.t0, bar_p2);
       }
-      issue_gate_beta<false>(sbase, sm, P, beta, nxt);
+      issue_beta(beta, P, nxt);
     }
     float gpb = 0.f, gpa = 0.f;  // kGate: this thread's dbias and dA_log partials
     {  // dg = reverse cumsum of dG over the chunk (G in log2 units)
@@ -600,30 +630,38 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       float qs = qoff, ps = poff + kLn2 * ks;
       const float sc = kGate ? kgate_scale(ga, j) : 0.f, gb = kGate && cin ? kgate_bias(ga, P.K, j, c) : 0.f;
 #pragma unroll
-      for (int t = 15; t >= 0; --t) {
-        const int r = 16 * R + t;
-        const bool hi = r >= mid;
-        qs += qv[t];
-        if (hi) ps += pv[t];
-        const float v = qs + carried + (hi ? ps : pv[t]);
-        if (r < len && cin) {
-          const size_t e = ((size_t)(t0 + r) * HV + j) * P.K + c;
+      for (int p2 = 7; p2 >= 0; --p2) {
+        float vv[2];
+#pragma unroll
+        for (int w = 1; w >= 0; --w) {
+          const int t = 2 * p2 + w, r = 16 * R + t;
+          const bool hi = r >= mid;
+          qs += qv[t];
+          if (hi) ps += pv[t];
+          float v = qs + carried + (hi ? ps : pv[t]);
           if (kGate) {  // da = dG dg/da; the parameter gradients' partials
-            const float2 d = kgate_grad_fast(__ldg(P.g + e) + gb, sc, ga.lb);
-            const float da = v * d.x;
-            args.dg[e] = da;
-            gpb += da;
-            gpa = fmaf(v, d.y, gpa);
-          } else {
-            args.dg[e] = v;
+            const float2 d = kgate_grad_fast(ar[t] + gb, sc, ga.lb);
+            const bool use = r < len && cin;
+            gpb += use ? v * d.x : 0.f;
+            gpa = use ? fmaf(v, d.y, gpa) : gpa;
+            v *= d.x;
           }
+          vv[w] = v;
         }
+        // lanes (c, c + 1) trade one value and store rows 2 p2 (even lane), 2 p2 + 1 (odd lane)
+        const float got = __shfl_xor_sync(0xffffffffu, odd ? vv[0] : vv[1], 1);
+        const int rs = 16 * R + 2 * p2 + (odd ? 1 : 0);
+        if (rs < len && cin)
+          *reinterpret_cast<float2 *>(args.dg + ((size_t)(t0 + rs) * HV + j) * P.K + cp) =
+              odd ? make_float2(got, vv[1]) : make_float2(vv[0], got);
       }
     }
     KDA_PT(12);
     if (kGate) {
       reinterpret_cast<float *>(sm + C_GPB)[R * kD + c] = gpb;
-      reinterpret_cast<float *>(sm + C_GPA)[tid] = gpa;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gpa += __shfl_xor_sync(0xffffffffu, gpa, o);
+      if (lane == 0) reinterpret_cast<float *>(sm + C_GPA)[warp] = gpa;
     }
     const bool all_ok = __syncthreads_and(ok) != 0;
     KDA_PT(7);
@@ -631,13 +669,10 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       if (tid < kD) {
         const float *gp = reinterpret_cast<const float *>(sm + C_GPB);
         W.gpart_b[cur.slot * kD + tid] = gp[tid] + gp[kD + tid] + gp[2 * kD + tid] + gp[3 * kD + tid];
-      } else if (warp == kD / 32) {
-        const float *gp = reinterpret_cast<const float *>(sm + C_GPA);
-        float t = 0.f;
+      } else if (warp == kD / 32) {  // the 16 warp sums
+        float t = lane < kCT / 32 ? reinterpret_cast<const float *>(sm + C_GPA)[lane] : 0.f;
 #pragma unroll
-        for (int i = 0; i < kCT / 32; ++i) t += gp[lane + 32 * i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
         if (lane == 0) W.gpart_a[cur.slot] = t;
       }
     }

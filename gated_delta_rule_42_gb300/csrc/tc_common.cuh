@@ -80,7 +80,15 @@ __device__ __forceinline__ void kgate_tile(float *G, int ld, int len, int K, int
   const int c = threadIdx.x & 127;
   if (c >= K) return;
   const float sc = kgate_scale(ga, j), b = kgate_bias(ga, K, j, c);
-  for (int r = threadIdx.x >> 7; r < len; r += NT / 128) G[r * ld + c] = kgate_fast(G[r * ld + c] + b, sc, ga.lb);
+  if (NT >= 512) {  // few rows per thread: all of them at once
+#pragma unroll
+    for (int i = 0; i < kC / (NT / 128); ++i) {
+      const int r = (threadIdx.x >> 7) + i * (NT / 128);
+      if (r < len) G[r * ld + c] = kgate_fast(G[r * ld + c] + b, sc, ga.lb);
+    }
+  } else {
+    for (int r = threadIdx.x >> 7; r < len; r += NT / 128) G[r * ld + c] = kgate_fast(G[r * ld + c] + b, sc, ga.lb);
+  }
 }
 
 // 1 / sqrt(K) for the head dims of the tensor-core path (64 or 128), exactly.
