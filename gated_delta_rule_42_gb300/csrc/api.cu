@@ -137,6 +137,7 @@ size_t layout(const Problem &P, bool kgate, bool backward, bool with_ctx, char *
   w.flags = (int *)take(sizeof(int) * 8);
   if (use_tc(P)) {  // slots the record / gradient kernel leaves to its exact-path fix-up launch
     w.wide_rec = (int *)take(sizeof(int) * (slots > 0 ? slots : 1));
+    w.wide_crec = (int *)take(sizeof(int) * (slots > 0 ? slots : 1));
     if (backward) {
       w.wide_grad = (int *)take(sizeof(int) * (slots > 0 ? slots : 1));
       w.wide_cgrad = (int *)take(sizeof(int) * (slots > 0 ? slots : 1));

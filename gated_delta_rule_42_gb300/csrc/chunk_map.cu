@@ -29,6 +29,7 @@ chunk_map_kernel(const int32_t *__restrict__ cu, int B, int T, int N, int64_t Tt
     flags[3] = 0;  // and its counts of slots on the exact (wide-decay) path
     flags[4] = 0;
     flags[5] = 0;  // and on the block-reference path (wide chunk span)
+    flags[6] = 0;
   }
   __syncthreads();
   for (int base = 0; base < N; base += kMapThreads) {

@@ -50,10 +50,12 @@ struct Workspace {
   int4 *chunk;   // [NC]
   int *flags;    // [0] = number of chunks, [1] = malformed-offsets flag, [2] = a bounded wait gave up,
                  // [3], [4] = (chunk, value head) slots the record / gradient kernel sent to the exact
-                 // path for a wide decay span, listed in wide_rec / wide_grad; [5] = slots the
-                 // chunk-reference gradient kernel left to the block-reference one (wide_cgrad)
+                 // path for a wide decay span, listed in wide_rec / wide_grad; [5], [6] = slots the
+                 // chunk-reference gradient / record kernel left to the block-reference one
+                 // (wide_cgrad / wide_crec)
   int *wide_rec, *wide_grad;  // [NC * HV] slot lists of the fix-up launches
   int *wide_cgrad;            // [NC * HV] slots the chunk-reference gradient kernel left (flags[5])
+  int *wide_crec;             // [NC * HV] slots the chunk-reference record kernel left (flags[6])
   float *G;      // [slot][64][K]   chunk-local inclusive gate cumsum
   float *Aqk;    // [slot][64][64]  lower (incl. diagonal) decayed q~ k^T
   float *A;      // [slot][64][64]  (I + L)^-1

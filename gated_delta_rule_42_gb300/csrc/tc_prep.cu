@@ -1,11 +1,11 @@
-// Per-chunk preparation of the bf16 chunked KDA forward (K = V = 128, chunk 64):
-// everything a chunk step needs that does not depend on v or on the carried
-// state, for every (chunk, value head) slot in parallel.
+// Per-chunk preparation of the bf16 chunked KDA forward (K, V = 64 or 128, chunk
+// 64): everything a chunk step needs that does not depend on v or on the
+// carried state, for every (chunk, value head) slot in parallel.
 //
-// One CTA per slot (three per SM: 75 KB of shared memory, no tensor memory):
+// One CTA per slot (three per SM: 75 KB of shared memory):
 //  (a) chunk-local cumsum G of the log2 gate and the decay-scaled tiles;
-//  (b) the decayed Gram blocks L (strictly lower, beta-scaled) and Aqk (lower)
-//      on 16x16 warp MMAs, and A = (I + L)^-1 in fp32;
+//  (b) the decayed Gram blocks L (strictly lower, beta-scaled) and Aqk (lower),
+//      and A = (I + L)^-1 in fp32;
 // and writes the slot's tile record: Bk = beta k 2^G, Qg = q~ 2^G,
 // Khat = k 2^(G_last - G), Aqk and A (bf16, swizzled operand tiles) and
 // 2^G_last (fp32 [K]).  The sequential state kernel and the reverse scan load
@@ -19,22 +19,26 @@
 // stay factored as A and Bk: the state kernel forms w h and u with tensor-core
 // products.
 //
-// Decay scaling.  2^(G_r - G_i) is split per channel at references inside
-// the 16-token blocks: row r of block R carries e1 = 2^(G_r - Gr(R)) (tiles Kr,
-// Qr), column i of block I carries e2 = 2^(Gc(I) - G_i) (tile Kc), and between
-// blocks (R > I) the factor D_RI = 2^(Gr(R) - Gc(I)) <= 1 goes onto the column
-// fragments in registers.  kda_prep_tc puts both references in the middle of
-// each block's range, so e1 and e2 stay within 2^(+-kSpanMax/2) as long as the
-// block's decay span (G at its first row minus G at its last) is at most
-// kSpanMax, and a diagonal block needs no factor at all.  A slot with a wider
-// block (per-token gates averaging below about -12.8, log2) is listed instead
-// and left to kda_prep_tc_fix, which takes each block's first row as Gr and
-// its last as Gc on every channel: e1, e2 <= 1, so the off-diagonal products
-// only underflow where the true product does, and it forms the diagonal blocks
-// exactly from the raw rows, the decay between tokens i and r as the running
-// product of the per-token decays (diag_direct).  Chunk-level tiles:
-// Bk = beta k e1 2^Gr, Qg = q~ e1 2^Gr and Khat = k e2 2^(G_last - Gc); terms
-// below 2^-30 of the largest may flush to zero.
+// Decay scaling: three kernels, each exact where it runs.
+//  - kda_prep_chunk_tc (every slot) splits 2^(G_r - G_i) at the middle m of each
+//    channel's range over the chunk: rows carry e1 = 2^(G_r - m) (tiles Kr, Qr),
+//    columns e2 = 2^(m - G_i) (tile Kc), and L, Aqk are one tcgen05 product.
+//    It needs every channel's chunk span G_first - G_last <= kChunkSpan.
+//  - The block-reference kernel (kda_prep_tc_list, over the slots with a wider
+//    span) splits at references inside the 16-token blocks: row r of block R
+//    carries e1 = 2^(G_r - Gr(R)), column i of block I e2 = 2^(Gc(I) - G_i), and
+//    between blocks (R > I) the factor D_RI = 2^(Gr(R) - Gc(I)) <= 1 goes onto the
+//    column fragments of 16x16 warp MMAs.  Both references sit in the middle of
+//    the block's range, so e1 and e2 stay within 2^(+-kSpanMax/2) while the
+//    block's span is at most kSpanMax; a diagonal block needs no factor.
+//  - kda_prep_tc_fix (a slot with a wider block: per-token gates averaging below
+//    about -12.8, log2) takes each block's first row as Gr and its last as Gc on
+//    every channel: e1, e2 <= 1, so the off-diagonal products only underflow
+//    where the true product does, and it forms the diagonal blocks exactly from
+//    the raw rows, the decay between tokens i and r as the running product of the
+//    per-token decays (diag_direct).  Chunk-level tiles there: Bk = beta k e1
+//    2^Gr, Qg = q~ e1 2^Gr and Khat = k e2 2^(G_last - Gc); terms below 2^-30 of
+//    the largest may flush to zero.
 #include "tc_common.cuh"
 
 namespace kda {
@@ -100,13 +104,13 @@ __device__ __forceinline__ void l2norm_row16(float (&kv)[8], float (&qv)[8]) {
 // cumsum) when a block's span exceeds kSpanMax: the slot is left to the fix-up.
 template <bool kGate>
 __device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *beta, unsigned char *rec, bool l2n,
-                                       const GateArgs &ga, float qscale, int K) {
+                                       const GateArgs &ga, float qscale, int K, int j) {
   const int tid = threadIdx.x;
   int wide_c = 0;
   float *G = (float *)(sm + P_G);
   float *vec = (float *)(sm + P_VEC);
   if (kGate) {  // the decay from the raw gate (KDA_GATE_IN_KERNEL); value head blockIdx.y
-    kgate_tile<kThr>(G, kGT, len, K, blockIdx.y, ga);
+    kgate_tile<kThr>(G, kGT, len, K, j, ga);
     __syncthreads();
   }
   if (tid < kD) {  // one thread per channel (a warp reads 32 consecutive channels: no bank conflicts)
@@ -421,41 +425,236 @@ __device__ __forceinline__ void load_slot(const Problem &P, const TmaMaps &maps,
   __syncthreads();
 }
 
-// One CTA per (chunk, value head) slot; a slot with a block wider than kSpanMax
-// is listed in W.wide_rec (status word 3 counts them) for kda_prep_tc_fix.
+// ---- one decay reference per chunk: the Gram products on tcgen05 ----
+
+// Shared memory of the chunk-reference kernel: the map above, with [Kr; Qr] as one
+// 128-row operand in place of k and q (the two 64-column sub-tiles of 128 rows at
+// P_K and P_K + 16 KB), a second mbarrier and the tensor-memory slot.
+constexpr uint32_t P_BAR2 = P_MISC + 8, P_TSLOT = P_MISC + 16;
+constexpr uint32_t P_SMEM_C = P_MISC + 32 + 1024;
+static_assert(P_SMEM_C + 1024 <= 233472 / 3, "three CTAs per SM");
+static_assert(P_K + 32768 == P_G, "[Kr; Qr] fills the k and q tiles");
+// Widest per-channel decay span (log2) of a chunk that one middle reference carries.
+constexpr float kChunkSpan = 192.f;
+constexpr uint32_t kTmemCols = 64;  // [L | Aqk] rows (M = 128) x 64 columns, per CTA
+
+// One CTA per (chunk, value head) slot, with the pairwise decay 2^(G_r - G_i) split
+// at the middle m of each channel's range over the chunk: e1 = 2^(G_r - m) on
+// the rows (Kr, Qr), e2 = 2^(m - G_i) on the columns (Kc), both within
+// 2^(+-kChunkSpan/2) when every channel's span G_first - G_last is at most
+// kChunkSpan.  Then L and Aqk are one tcgen05 product [Kr; Qr] Kc^T (M = 128,
+// N = 64, K = 128, fp32 in tensor memory) with no per-block factor.  A slot
+// whose span is wider is listed (W.wide_crec, status word 6) for the
+// block-reference kernel below.
 template <bool kGate>
 __global__ void __launch_bounds__(kThr, 3)
-kda_prep_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps, GateArgs ga) {
+kda_prep_chunk_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps, GateArgs ga) {
   extern __shared__ unsigned char smraw[];
   unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(sm);
   const int c_idx = blockIdx.x, j = blockIdx.y;
   const int4 ch = W.chunk[c_idx];
   if (ch.x < 0) return;  // unused chunk slot
   const int t0 = ch.y, len = ch.z;
   const int HV = P.HV, h = j / (HV / P.H);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t slot = (size_t)c_idx * HV + j;
   float *beta = (float *)(sm + P_BETA);
-  uint64_t *bar = (uint64_t *)(sm + P_MISC);
+  float *G = (float *)(sm + P_G);
+  float *vec = (float *)(sm + P_VEC);
+  uint64_t *bar = (uint64_t *)(sm + P_MISC), *bar_mma = (uint64_t *)(sm + P_BAR2);
+  uint32_t *tslot = (uint32_t *)(sm + P_TSLOT);
   KDA_PT_DECL;
 
   if (tid == 0) {
     bar_init(bar, 1);
+    bar_init(bar_mma, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(tslot, kTmemCols);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tslot;
+  load_slot(P, maps, sm, bar, 0u, err, t0, len, h, j);
+  KDA_PT(0);
+  unsigned char *rec = W.tc_tiles + slot * kTileRecord;
+  const float qscale = head_qscale(P.K);
+
+  // ---- G, 2^G_last and the reference m = (G_first + G_last) / 2 per channel ----
+  if (kGate) {  // the decay from the raw gate (KDA_GATE_IN_KERNEL)
+    kgate_tile<kThr>(G, kGT, len, P.K, j, ga);
+    __syncthreads();
+  }
+  int wide_c = 0;
+  if (tid < kD) {
+    const int c = tid;
+    float col[kC];
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < kC; ++r) col[r] = G[r * kGT + c];
+#pragma unroll
+    for (int r = 0; r < kC; ++r) {
+      if (r < len) s += col[r];
+      col[r] = s;
+    }
+#pragma unroll
+    for (int r = 0; r < kC; ++r) G[r * kGT + c] = col[r];
+    const float gl = s, m = 0.5f * (col[0] + gl);  // rows past len hold G_last
+    wide_c = !(col[0] - gl <= kChunkSpan);        // (NaN-safe)
+    reinterpret_cast<float *>(rec + kRecGAML)[c] = exp2f(gl);
+    vec[W_GREF * kD + c] = m;
+    vec[W_EREF * kD + c] = exp2f(m);
+    vec[W_LAM * kD + c] = exp2f(gl - m);
+  }
+  const bool wide = __syncthreads_or(wide_c) != 0;
+  KDA_PT(1);
+  if (wide) {  // left to the block-reference kernel
+    if (tid == 0) W.wide_crec[atomicAdd(W.flags + 6, 1)] = (int)slot;
+  } else {
+    // ---- tiles: thread = 8 channels (one 16-byte chunk) of 4 rows, a half-warp per row.
+    // [Kr; Qr] takes k's and q's place row by row: Kr row r's two sub-tile chunks land on
+    // k's row r (channels 0..63) and q's row r (channels 0..63), Qr's on k's and q's row r
+    // (channels 64..127) -- all held by the half-warp that reads row r, so a warp barrier
+    // between its reads and its writes suffices. ----
+    {
+      const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4;
+      float mv[8], em[8], lm[8];
+#pragma unroll
+      for (int e = 0; e < 8; e += 4) {
+        *reinterpret_cast<float4 *>(mv + e) = *reinterpret_cast<const float4 *>(vec + W_GREF * kD + c0 + e);
+        *reinterpret_cast<float4 *>(em + e) = *reinterpret_cast<const float4 *>(vec + W_EREF * kD + c0 + e);
+        *reinterpret_cast<float4 *>(lm + e) = *reinterpret_cast<const float4 *>(vec + W_LAM * kD + c0 + e);
+      }
+      uint4 kc[4];  // Kc rows, written once every thread has read its G values
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = rg * 4 + rr;
+        const uint32_t off = sw_chunk(r, jj, kC);
+        float kv[8], qv[8], g[8], e1[8], e2[8], o[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sm + P_K + off), kv);
+        unpack8(*reinterpret_cast<const uint4 *>(sm + P_Q + off), qv);
+        __syncwarp();  // the half-warp has read row r of k and q
+        if (P.l2norm) l2norm_row16(kv, qv);
+        *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGT + c0);
+        *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGT + c0 + 4);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          e1[e] = ex2(g[e] - mv[e]);  // within 2^(+-kChunkSpan/2)
+          e2[e] = ex2(mv[e] - g[e]);
+        }
+        const float br = beta[r];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
+        *reinterpret_cast<uint4 *>(sm + P_K + sw_chunk(r, jj, 2 * kC)) = pack8(o);  // Kr: rows 0..63
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] *= br * em[e];
+        *reinterpret_cast<uint4 *>(rec + kRecBK + off) = pack8(o);  // Bk = beta k 2^G
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
+        kc[rr] = pack8(o);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] *= lm[e];
+        *reinterpret_cast<uint4 *>(rec + kRecKH + off) = pack8(o);  // Khat = k 2^(G_last - G)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
+        *reinterpret_cast<uint4 *>(sm + P_K + sw_chunk(kC + r, jj, 2 * kC)) = pack8(o);  // Qr: rows 64..127
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] *= em[e];
+        *reinterpret_cast<uint4 *>(rec + kRecQG + off) = pack8(o);  // Qg = q~ 2^G
+      }
+      __syncthreads();  // G is dead: its upper half takes Kc
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) *reinterpret_cast<uint4 *>(sm + P_KC + sw_chunk(rg * 4 + rr, jj, kC)) = kc[rr];
+    }
+    fence_async_smem();  // [Kr; Qr] and Kc are read by the tensor core next
+    fence_before();
+    __syncthreads();
+    fence_after();
+    KDA_PT(2);
+    // ---- [L~ | Aqk][m][i] = sum_c [Kr; Qr][m][c] Kc[i][c]   (M = 128, N = 64, K = 128) ----
+    if (tid == 0) {
+      const uint32_t id = idesc(128, 64, 0, 0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma(tmem, desc_k16(sbase + P_K, k, 2 * kC), desc_k16(sbase + P_KC, k, kC), id, k > 0);
+      commit(bar_mma);
+    }
+    bar_wait(bar_mma, 0u, err);
+    fence_after();
+    {  // warp: lane quarter w % 4 (rows 32 (w % 4) ..), columns 32 (w / 4) ..; L to fp32 shared
+       // memory for the inverse (beta-scaled, strictly lower), Aqk (lower) to the record
+      const int q4 = warp & 3, c32 = 32 * (warp >> 2), m = 32 * q4 + lane;
+      float x[32];
+      tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)c32, x);
+      float *Lf = (float *)(sm + P_G);  // G is dead
+      if (m < kC) {
+        const int r = m;
+        const float br = beta[r];
+#pragma unroll
+        for (int i4 = 0; i4 < 32; i4 += 4) {
+          const int i = c32 + i4;
+          *reinterpret_cast<float4 *>(Lf + fsw(r, i)) =
+              make_float4(i < r ? br * x[i4] : 0.f, i + 1 < r ? br * x[i4 + 1] : 0.f, i + 2 < r ? br * x[i4 + 2] : 0.f,
+                          i + 3 < r ? br * x[i4 + 3] : 0.f);
+        }
+      } else {
+        const int r = m - kC;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = (c32 + 8 * t + e <= r) ? x[8 * t + e] : 0.f;
+          *reinterpret_cast<uint4 *>(rec + kRecAQK + sw_chunk(r, (c32 >> 3) + t, kC)) = pack8(y);
+        }
+      }
+    }
+    fence_before();
+    __syncthreads();
+    KDA_PT(4);
+    invert_store(sm, rec);
+  }
+  KDA_PT(10);
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    tmem_free(tmem, kTmemCols);
+  }
+  KDA_PT_FLUSH;
+}
+
+// The block-reference record kernel (phases (a) and (b) above) over the slots the
+// chunk-reference kernel listed (status word 6), walked by the CTAs; a slot with a
+// wide 16-token block goes on to the exact fix-up list (status word 3).
+template <bool kGate>
+__global__ void __launch_bounds__(kThr, 3)
+kda_prep_tc_list_kernel(Problem P, Workspace W, int *err, const __grid_constant__ TmaMaps maps, GateArgs ga) {
+  extern __shared__ unsigned char smraw[];
+  unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const int nlist = *(volatile const int *)(W.flags + 6);
+  if ((int)blockIdx.x >= nlist) return;
+  float *beta = (float *)(sm + P_BETA);
+  uint64_t *bar = (uint64_t *)(sm + P_MISC);
+  if (threadIdx.x == 0) {
+    bar_init(bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
-  load_slot(P, maps, sm, bar, 0u, err, t0, len, h, j);
-  KDA_PT(0);
-
-  unsigned char *rec = W.tc_tiles + slot * kTileRecord;
-  if (phase_a<kGate>(sm, len, beta, rec, P.l2norm, ga, head_qscale(P.K), P.K)) {
-    if (tid == 0) W.wide_rec[atomicAdd(W.flags + 3, 1)] = (int)slot;
-    return;
+  uint32_t parity = 0;
+  for (int i = blockIdx.x; i < nlist; i += gridDim.x, parity ^= 1u) {
+    const int s = W.wide_crec[i];
+    const int c_idx = s / P.HV, j = s % P.HV, h = j / (P.HV / P.H);
+    const int4 ch = W.chunk[c_idx];
+    load_slot(P, maps, sm, bar, parity, err, ch.y, ch.z, h, j);
+    unsigned char *rec = W.tc_tiles + (size_t)s * kTileRecord;
+    if (phase_a<kGate>(sm, ch.z, beta, rec, P.l2norm, ga, head_qscale(P.K), P.K, j)) {
+      if (threadIdx.x == 0) W.wide_rec[atomicAdd(W.flags + 3, 1)] = s;
+    } else {
+      phase_b(sm, beta, rec);
+    }
+    __syncthreads();  // the shared tiles are free for the next slot
   }
-  KDA_PT(2);
-  phase_b(sm, beta, rec);
-  KDA_PT(10);
-  KDA_PT_FLUSH;
 }
 
 // ---- the exact path for slots with a wide block ----
@@ -760,17 +959,23 @@ KDA_PT_EXPORT(kda_debug_prep_phase_cycles)
 cudaError_t tc_prepare(const Problem &P, const GateArgs &ga, const Workspace &W, const TmaMaps &maps, int *err,
                        cudaStream_t s) {
   if (P.NC == 0) return cudaSuccess;
-  auto fast = ga.on ? kda_prep_tc_kernel<true> : kda_prep_tc_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(fast, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+  // the chunk-reference kernel over every slot, the block-reference kernel over the
+  // slots it left, the exact fix-up over those with a wide block
+  auto fast = ga.on ? kda_prep_chunk_tc_kernel<true> : kda_prep_chunk_tc_kernel<false>;
+  auto list = ga.on ? kda_prep_tc_list_kernel<true> : kda_prep_tc_list_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(fast, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM_C);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(list, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kda_prep_tc_fix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   int nsm = 0;
   if (e == cudaSuccess) e = sm_count(&nsm);
   if (e != cudaSuccess) return e;
-  KDA_LAUNCH("kda_prep_tc", s, fast<<<dim3(P.NC, P.HV), kThr, P_SMEM, s>>>(P, W, err, maps, ga));
+  KDA_LAUNCH("kda_prep_tc", s, fast<<<dim3(P.NC, P.HV), kThr, P_SMEM_C, s>>>(P, W, err, maps, ga));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t slots = (int64_t)P.NC * P.HV;
-  const unsigned grid = (unsigned)(slots < nsm ? slots : nsm);
+  const unsigned grid = (unsigned)(slots < nsm ? slots : nsm), grid3 = (unsigned)(slots < 3 * nsm ? slots : 3 * nsm);
+  KDA_LAUNCH("kda_prep_tc_block", s, list<<<grid3, kThr, P_SMEM, s>>>(P, W, err, maps, ga));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   KDA_LAUNCH("kda_prep_tc_fix", s, kda_prep_tc_fix_kernel<<<grid, kThr, P_SMEM, s>>>(P, W, err, maps, ga));
   return cudaGetLastError();
 }
