@@ -466,7 +466,7 @@ const char *kda_status_string(kda_status s) {
 
 const char *kda_last_error(void) { return g_err; }
 
-int kda_version(void) { return 106; }
+int kda_version(void) { return 107; }
 
 int kda_uses_tensor_cores(const kda_inputs *in) {
   Problem P{};

@@ -240,7 +240,7 @@ kda_status kda_state_compose(const float *M, const float *h, const float *c, flo
                              int V, int transpose, void *stream);
 
 /* Device status words of a call.  Every chunked call (forward, backward, any
- * variant) writes five int32 words into its workspace, at byte offset
+ * variant) writes seven int32 words into its workspace, at byte offset
  * kda_status_offset() (the same for every workspace of the problem):
  *   [0] the number of 64-token chunks mapped;
  *   [1] nonzero if cu_seqlens was malformed (decreasing, negative or past the
@@ -249,13 +249,18 @@ kda_status kda_state_compose(const float *M, const float *h, const float *c, flo
  *       completed): the call's results are invalid;
  *   [3] the (chunk, value head) slots whose forward records took the exact
  *       path for strong decays, and
- *   [4] those whose per-chunk gradients took it (tensor-core path only).  The
- *       kernels split each pairwise decay 2^(G_r - G_i) at references inside
- *       16-token blocks; a block whose decay span (the sum of 15 consecutive
- *       per-token gates of one channel) exceeds 192 (log2) is recomputed by a
- *       second, slower launch that forms the block's terms exactly.  Results
- *       are exact for any gate either way; the words only say where time went.
- * Words 2, 3 and 4 are cleared at the start of every call.  The library never
+ *   [4] those whose per-chunk gradients took it;
+ *   [5] the slots whose per-chunk gradients took the 16-token block path, and
+ *   [6] those whose forward records took it (tensor-core path only for 3..6).
+ *       The kernels split each pairwise decay 2^(G_r - G_i) of a chunk at one
+ *       reference per channel, the middle of the channel's range over the
+ *       chunk; a chunk whose decay span (the sum of 63 consecutive per-token
+ *       gates of one channel) exceeds 192 (log2) is recomputed by a second
+ *       launch with references inside its 16-token blocks, and a block whose
+ *       span (15 gates) exceeds 192 by a third, slower launch that forms the
+ *       block's terms exactly.  Results are exact for any gate either way;
+ *       the words only say where time went.
+ * Words 2 to 6 are cleared at the start of every call.  The library never
  * reads them on the host: copy them out after the call (in stream order) to
  * check.  Returns SIZE_MAX for an invalid problem. */
 size_t kda_status_offset(const kda_inputs *in);
@@ -274,11 +279,12 @@ const char *kda_status_string(kda_status s);
 /* Message describing the last failure on the calling thread ("" if none). */
 const char *kda_last_error(void);
 
-/* Library ABI version (major * 100 + minor): 106 (101: kda_inputs gained
+/* Library ABI version (major * 100 + minor): 107 (101: kda_inputs gained
  * `flags`; 102: the forward-context entry points; 103: the final-state-only
  * forward, the start-state-gradient-only backward, kda_chunk_fwd_reuse; 104:
  * kda_status_offset, kda_debug_bounded_wait; 105: status words 3 and 4,
- * kda_uses_tensor_cores; 106: KDA_GATE_IN_KERNEL and kda_inputs.gate). */
+ * kda_uses_tensor_cores; 106: KDA_GATE_IN_KERNEL and kda_inputs.gate; 107:
+ * status words 5 and 6). */
 int kda_version(void);
 
 /* Chunked forward without a caller workspace (no counterpart on the pages).

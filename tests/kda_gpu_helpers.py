@@ -29,10 +29,10 @@ def _poisoned_ws(nbytes, dev):
 
 
 def status_words(lib, s, ws, wp):
-    """The five int32 status words a call left in its workspace (after a sync)."""
+    """The seven int32 status words a call left in its workspace (after a sync)."""
     off = lib.kda_status_offset(ctypes.byref(s))
     base = wp.value - ws.data_ptr() + off
-    return ws[base:base + 20].cpu().numpy().view(np.int32).tolist()
+    return ws[base:base + 28].cpu().numpy().view(np.int32).tolist()
 
 
 def gate_params(d):

@@ -1,12 +1,13 @@
 """GPU parity for strong decays: the tensor-core kernels split each pairwise
-decay 2^(G_r - G_i) into per-block factors, and these cases drive those factors
-to the edges of their range.  Gates far below the workloads' clip at -5 (log2)
-give 16-token blocks whose decay span (the sum of 15 per-token gates) reaches
-hundreds: below the block factors' limit (192) the fast path carries them, above
-it the slot's diagonal blocks take the exact path.  Every case is checked
-against the fp64 oracle at the bf16 tolerances, and the device status words 3
-and 4 (slots the record and gradient kernels sent to the exact path) tell which
-path ran."""
+decay 2^(G_r - G_i) into factors at references inside the chunk, and these
+cases drive those factors to the edges of their range.  A chunk whose decay
+span (per channel, G at its first row minus G at its last) is at most 192
+(log2) runs on one middle reference per chunk; a wider one goes to the
+16-token block-reference kernels (status words 6 for the records, 5 for the
+gradients); a 16-token block wider than 192 goes on to the exact path (words 3
+and 4).  Gates far below the workloads' clip at -5 (log2) reach every path.
+Every case is checked against the fp64 oracle at the bf16 tolerances, and the
+status words tell which paths ran."""
 import zlib
 
 import numpy as np
@@ -31,13 +32,13 @@ VARLEN_GVA = dict(B=1, T=700, H=2, HV=4, K=128, V=128, cu_seqlens=[0, 0, 3, 260,
 # name, gate (mean, std, clip) of clip(-softplus(N(mean, std)), clip, 0), problem, exact path expected
 CASES = [
     ("softplus_N2_2_clip30", (2.0, 2.0, -30.0), VARLEN_GVA, False),
-    ("strong_N6_3_clip40", (6.0, 3.0, -40.0), VARLEN_GVA, False),  # spans up to ~140: the fast path's upper range
-    ("wide_N16_4_clip60", (16.0, 4.0, -60.0), VARLEN_GVA, True),   # spans ~240: the exact path
+    ("strong_N6_3_clip40", (6.0, 3.0, -40.0), VARLEN_GVA, False),  # block spans up to ~140: block references
+    ("wide_N16_4_clip60", (16.0, 4.0, -60.0), VARLEN_GVA, True),   # block spans ~240: the exact path
     ("wide_dense_hv_eq_h", (16.0, 4.0, -60.0), dict(B=2, T=200, H=2, HV=2, K=128, V=128), True),
 ]
 
 
-def _check(inp, l2=False, expect_exact=None):
+def _check(inp, l2=False, expect_exact=None, expect_block=None):
     tol = H.TOL[inp.dtype]
     sf, sb = [], []
     o, hT = H.gpu_fwd(inp, l2=l2, status=sf)
@@ -49,6 +50,14 @@ def _check(inp, l2=False, expect_exact=None):
         # forward: the record kernel (word 3); recompute backward: the record kernel again and the
         # gradient kernel (word 4)
         assert (sf[3] > 0) == expect_exact and (sb[3] > 0) == expect_exact and (sb[4] > 0) == expect_exact, (sf, sb)
+    # the gradients run the chunk-reference kernel first except with a scalar gate or the
+    # fused L2-norm backward (HV = H), where the block-reference kernel takes every slot
+    chunk_grad = not (inp.g.dim() == 3 or (l2 and inp.HV == inp.H))  # (a scalar gate is [B, T, HV])
+    if expect_block is not None:  # the block-reference kernels: records (word 6), gradients (word 5)
+        assert (sf[6] > 0) == expect_block and (sb[6] > 0) == expect_block, (sf, sb)
+        assert not chunk_grad or (sb[5] > 0) == expect_block, (sf, sb)
+    if expect_exact:  # a slot on the exact path went through the block-reference kernel first
+        assert sf[6] >= sf[3] and sb[6] >= sb[3] and (not chunk_grad or sb[5] >= sb[4]), (sf, sb)
     return sf, sb
 
 
@@ -57,7 +66,16 @@ def test_strong_decays(name, gate, kw, exact):
     mu, sd, lo = gate
     inp = inputs.make_inputs(dtype=torch.bfloat16, seed=zlib.crc32(name.encode()) % 1000, name=name,
                              g_mean=mu, g_std=sd, g_lo=lo, **kw)
-    _check(inp, expect_exact=exact)
+    _check(inp, expect_exact=exact, expect_block=None if name.startswith("softplus") else True)
+
+
+def test_chunk_wide_block_narrow_takes_the_block_reference_path_only():
+    """Per-token gates near -4 (log2): every chunk spans ~250 (> 192) while every
+    16-token block spans ~60, so each slot goes to the block-reference kernels and
+    none to the exact path."""
+    inp = inputs.make_inputs(dtype=torch.bfloat16, seed=67, name="chunk_wide", g_mean=4.0, g_std=0.3, g_lo=-8.0,
+                             **VARLEN_GVA)
+    _check(inp, expect_exact=False, expect_block=True)
 
 
 def _unnormalised(inp, seed):
@@ -95,12 +113,12 @@ def test_hard_resets_in_a_few_channels():
     _check(inp, expect_exact=True)
 
 
-def test_ordinary_gates_stay_on_the_block_factors():
+def test_ordinary_gates_stay_on_the_chunk_references():
     sf, sb = [], []
     inp = inputs.make_config(1)
     H.gpu_fwd(inp, status=sf)
     H.gpu_bwd(inp, status=sb)
-    assert sf[3:] == [0, 0] and sb[3:] == [0, 0], (sf, sb)
+    assert sf[3:] == [0, 0, 0, 0] and sb[3:] == [0, 0, 0, 0], (sf, sb)
 
 
 def test_wide_decays_dense_training_shape_sampled():

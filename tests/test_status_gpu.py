@@ -1,6 +1,6 @@
 """GPU: the device status words a call leaves in its workspace (chunks mapped,
 malformed offsets, a bounded wait that gave up, slots on the exact wide-decay
-path) and the bounded-wait path
+path, slots on the block-reference path) and the bounded-wait path
 itself, exercised by a probe that waits on an mbarrier nothing completes.
 Nothing here faults, traps or hangs the GPU: malformed offsets are handled by
 the chunk map as empty sequences, and the probe's wait is bounded."""
@@ -27,7 +27,7 @@ def lib():
 
 def _words(ws, wp, off):
     base = wp.value - ws.data_ptr()
-    return ws[base + off: base + off + 20].cpu().numpy().view(np.int32).tolist()
+    return ws[base + off: base + off + 28].cpu().numpy().view(np.int32).tolist()
 
 
 def _run_fwd_bwd(lib, d, s):
@@ -54,7 +54,7 @@ def test_status_words_after_clean_calls(lib, K, dtype):
     s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens)
     fwd, bwd, _, _ = _run_fwd_bwd(lib, d, s)
     chunks = 3 + 3  # 130 and 170 tokens
-    assert fwd == [chunks, 0, 0, 0, 0] and bwd == [chunks, 0, 0, 0, 0]
+    assert fwd == [chunks, 0, 0, 0, 0, 0, 0] and bwd == [chunks, 0, 0, 0, 0, 0, 0]
 
 
 def test_malformed_offsets_are_flagged_and_treated_as_empty(lib):
@@ -67,7 +67,7 @@ def test_malformed_offsets_are_flagged_and_treated_as_empty(lib):
     cu = torch.tensor([0, 100, 400, 300], dtype=torch.int32, device="cuda")
     s = make_inputs_struct(d.q, d.k, d.v, d.g, d.beta, d.h0, cu)
     fwd, bwd, o, g = _run_fwd_bwd(lib, d, s)
-    assert fwd == [2, 1, 0, 0, 0] and bwd == [2, 1, 0, 0, 0]
+    assert fwd == [2, 1, 0, 0, 0, 0, 0] and bwd == [2, 1, 0, 0, 0, 0, 0]
     assert torch.isfinite(o[:, :100]).all() and all(torch.isfinite(x[:, :100]).all() for x in g)
 
 
