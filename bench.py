@@ -125,16 +125,28 @@ def kernel_bytes_per_token(name, cfg):
     return table.get(name)
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
-# kernel from one ncu --set full capture, per token of the captured launch, with
-# the SHA-256 of the sources the kernel was built from at capture time.  The
-# value is reported only while those sources are unchanged.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the step's
+# kernels, each from its own one-kernel ncu --set full capture on the dense layer
+# at T = 1024, per token of the captured launch, with the SHA-256 of the sources
+# the kernel was built from at capture time.  A value is reported only while
+# those sources are unchanged.
 NCU_TRAFFIC = {
     "kda_bwd_intra_tc": dict(
-        bytes_per_token=1281294592 / 8192,  # 974.5 MB read + 306.8 MB written, B=8 T=1024 H=HV=32
-        sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_intra.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh",
-                 "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="e0b0a192344717a07c01b1fbb5ea461f58c667d9e4fdedaf1608e9063bbb319a"),
+        bytes_per_token=1282299392 / 8192,  # 974.3 MB read + 308.0 MB written, B=8 T=1024 H=HV=32
+        sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_chunk.cu", "gated_delta_rule_42_gb300/csrc/tc_intra.cuh", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
+        sha256="64811d10a74f805bee872f2b5c83dcaefce7588564d78555b219d602f581c5ad"),
+    "kda_prep_tc": dict(
+        bytes_per_token=493784064 / 8192,  # 270.6 MB read + 223.2 MB written, B=8 T=1024 H=HV=32
+        sources=("gated_delta_rule_42_gb300/csrc/tc_prep.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
+        sha256="a391e31c176d0906a92b747c39a0a983d38f17e4cbace7852bdd1e243bb80dcb"),
+    "kda_fwd_tc_save": dict(
+        bytes_per_token=624922368 / 8192,  # 339.2 MB read + 285.8 MB written, B=8 T=1024 H=HV=32
+        sources=("gated_delta_rule_42_gb300/csrc/tc_fwd.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
+        sha256="88c527df14544aa8eaafca0eb372e1ce3377af9cd7f84b9919bfa5466caf9c1b"),
+    "kda_bwd_scan_tc": dict(
+        bytes_per_token=559956224 / 8192,  # 337.7 MB read + 222.3 MB written, B=8 T=1024 H=HV=32
+        sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_scan.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
+        sha256="da1ee511eec4127d68a680db53ef9fb5b01fdf26335150453d55ef709d32f409"),
 }
 
 
@@ -168,6 +180,24 @@ def sources_sha256(paths):
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def step_traffic(split, steps_split, tokens):
+    """The step's DRAM bytes from the per-kernel captures: the sum over the
+    kernels that take more than 1 % of the step's kernel time (the rest are a
+    few-microsecond chunk map and empty fix-up launches) of their traffic per
+    launch x launches per step; None unless every one of them has a capture
+    that matches its sources."""
+    total_ms = sum(v[0] for v in split.values())
+    total = 0.0
+    for name, (ms_k, n_k) in split.items():
+        if ms_k < 0.01 * total_ms:
+            continue
+        t = measured_traffic(name, tokens)
+        if t is None:
+            return None
+        total += t * n_k / steps_split
+    return int(round(total))
 
 
 def measured_traffic(name, tokens):
@@ -670,7 +700,15 @@ def main():
     per_step = {k: v[0] / steps_split for k, v in split.items()}
     dom = max(split, key=lambda k: split[k][0])
     dom_ms, dom_n = split[dom]
+    # the captures are of the dense layer's kernels (K = V = 128, the gate as given, no L2-norm
+    # prologue): their traffic per token holds for this workload and its length variants only
+    captured = (cfg.K == 128 and cfg.V == 128 and cfg.H == 32 and cfg.HV == 32 and not args.qk_l2norm
+                and not args.scalar_gate and not args.kda_gate and not args.recompute and args.cp_ranks == 1
+                and args.segments == 1)
     roof = dominant_roofline(dom, dom_ms / dom_n, cfg, toks / max(1, args.cp_ranks), peaks)
+    if not captured:
+        roof["traffic"] = None
+    traffic = step_traffic(split, steps_split, toks) if captured else None
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_step, 4),
@@ -694,6 +732,8 @@ def main():
                           "roofline_ms": round(roof_s * 1e3, 4),
                           "achieved_GBps": round(ab["total"] / (ms_step / 1e3) / 1e9, 1),
                           "frac": round(roof_s / (ms_step / 1e3), 4),
+                          "traffic": traffic,
+                          "traffic_vs_algorithmic": None if traffic is None else round(traffic / ab["total"], 3),
                           "peaks": {"hbm_gbs": peaks["hbm"], "bf16_tflops": peaks["bf16"],
                                     "source": peaks["src"]}},
         "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(per_step.items(), key=lambda x: -x[1])},

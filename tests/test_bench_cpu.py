@@ -1,9 +1,9 @@
 """The benchmark's roofline arithmetic, pinned on the host: the algorithmic
 bytes and flops of the dense training layer (per token and value head), each
 tensor-core kernel's share of them (what the dominant kernel's roofline
-divides by), its interface bytes (a diagnostic), and the rule that the
-measured DRAM traffic is reported only while the dominant kernel's sources
-match its capture."""
+divides by), its interface bytes (a diagnostic), and the rule that measured
+DRAM traffic (the dominant kernel's, and the step's sum over its kernels) is
+reported only while each kernel's sources match its capture."""
 import os
 import sys
 
@@ -79,4 +79,17 @@ def test_traffic_is_reported_only_for_the_captured_sources():
     assert (got is not None) == current
     if current:  # the capture's own size gives back its bytes
         assert abs(got - t["bytes_per_token"] * 8192) <= 1
-    assert bench.measured_traffic("kda_prep_tc", 8192) is None  # no capture recorded for it
+    assert bench.measured_traffic("chunk_map_kernel", 8192) is None  # no capture recorded for it
+
+
+def test_step_traffic_needs_a_capture_for_every_kernel_that_matters():
+    split = {"kda_bwd_intra_tc": (15.6, 10), "kda_prep_tc": (5.6, 10), "kda_fwd_tc_save": (4.2, 10),
+             "kda_bwd_scan_tc": (3.6, 10), "chunk_map_kernel": (0.16, 20)}
+    current = all(bench.sources_sha256(bench.NCU_TRAFFIC[k]["sources"]) == bench.NCU_TRAFFIC[k]["sha256"]
+                  for k in ("kda_bwd_intra_tc", "kda_prep_tc", "kda_fwd_tc_save", "kda_bwd_scan_tc"))
+    got = bench.step_traffic(split, 10, 8192)
+    assert (got is not None) == current
+    if current:  # one launch of each per step; the chunk map (under 1 % of the time) is left out
+        want = sum(bench.NCU_TRAFFIC[k]["bytes_per_token"] * 8192 for k in list(split)[:4])
+        assert abs(got - want) <= 4
+    assert bench.step_traffic(dict(split, other_kernel=(5.0, 10)), 10, 8192) is None
