@@ -75,10 +75,29 @@ __device__ __forceinline__ void issue_beta(float *beta, const Problem &P, const 
   }
   cp_commit();
 }
+// Scalar gate (one decay per token and value head): the scalars of a slot's rows
+// (zero past len), loaded into registers by every thread ...
+constexpr int kSgIt = kC * 32 / kCT;  // float4 stores of the gate tile per thread
+__device__ __forceinline__ void sg_load(float (&x)[kSgIt], const Problem &P, const Slot &q) {
+#pragma unroll
+  for (int u = 0; u < kSgIt; ++u) {
+    const int r = (int)(threadIdx.x + u * kCT) >> 5;
+    x[u] = r < q.len ? P.g[(size_t)(q.t0 + r) * P.HV + q.j] : 0.f;
+  }
+}
+// ... and repeated over the 128 channels of the gate tile once the tile is free.
+__device__ __forceinline__ void sg_store(float *G, const float (&x)[kSgIt]) {
+#pragma unroll
+  for (int u = 0; u < kSgIt; ++u) {
+    const int it = threadIdx.x + u * kCT, r = it >> 5, c4 = (it & 31) * 4;
+    *reinterpret_cast<float4 *>(G + r * kGD + c4) = make_float4(x[u], x[u], x[u], x[u]);
+  }
+}
 // Rows of the vector table this kernel uses: G_last, 2^G_last, m, 2^m,
 // 2^(G_last - m); the dg scan's block totals (Q, P, Khat term) x 4 blocks go to
 // twelve rows it leaves free.
 constexpr int V_M = V_RREF, V_EM = V_EREF, V_LM = V_LAM;
+constexpr int V_SG = V_RREF + 1;  // kSG: dg row sums [4 channel quarters][64 rows] (two vector rows)
 __device__ __forceinline__ int tot_row(int kind, int R) {
   const int k = 4 * kind + R;
   return k < 6 ? V_D + k : V_LAM + 2 + (k - 6);
@@ -133,7 +152,9 @@ __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-template <bool kGate>
+// kGate: the KDA gate inside the op; kSG: one decay per (token, value head), dg summed over
+// the channels (the two are not combined).
+template <bool kGate, bool kSG>
 __global__ void __launch_bounds__(kCT, 1)
 kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps,
                               GateArgs ga) {
@@ -173,11 +194,16 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     if (tid == 0) {
       mbar_expect_tx(bar_s, kBytesS);
       mbar_expect_tx(bar_p1, kBytesP1);
-      mbar_expect_tx(bar_p2, kBytesP2 + kBytesG);
+      mbar_expect_tx(bar_p2, kBytesP2 + (kSG ? 0u : kBytesG));
       for (int i = 0; i < kCopiesS; ++i) copy_s(i, sbase, W, maps, cur, bar_s);
       for (int i = 0; i < kCopiesP1; ++i) copy_p1(i, sbase, W, maps, cur, bar_p1);
       for (int i = 0; i < kCopiesP2; ++i) copy_p2(i, sbase, W, maps, cur, bar_p2);
-      tma_load3(sbase + C_G, &maps.g, 0, cur.j, cur.t0, bar_p2);
+      if (!kSG) tma_load3(sbase + C_G, &maps.g, 0, cur.j, cur.t0, bar_p2);
+    }
+    if (kSG) {
+      float x[kSgIt];
+      sg_load(x, P, cur);
+      sg_store(G, x);
     }
     issue_beta(beta, P, cur);
   }
@@ -354,11 +380,13 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
             qv[e] *= rq;
           }
         }
+        float g[8];  // (two 16-byte reads: a half-warp reads one whole row, free of bank conflicts)
+        *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGD + c0);
+        *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGD + c0 + 4);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float g = G[r * kGD + c0 + e];
-          e1[e] = ex2(g - mv[e]);  // within 2^(+-kChunkSpan/2)
-          e2[e] = ex2(mv[e] - g);
+          e1[e] = ex2(g[e] - mv[e]);  // within 2^(+-kChunkSpan/2)
+          e2[e] = ex2(mv[e] - g[e]);
         }
         uint4 hi, lo;
 #pragma unroll
@@ -587,10 +615,10 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     KDA_PT(10);
     if (more) {  // the next slot's remaining inputs into the dead tiles; its G and beta
       if (tid == 0) {
-        mbar_expect_tx(bar_p2, kBytesP2 + kBytesG);
+        mbar_expect_tx(bar_p2, kBytesP2 + (kSG ? 0u : kBytesG));
         mbar_expect_tx(bar_s, kBytesS);
       }
-      if (lane == 0 && warp >= 1 && warp <= kCopiesP2 + kCopiesS + 1) {
+      if (lane == 0 && warp >= 1 && warp <= kCopiesP2 + kCopiesS + (kSG ? 0 : 1)) {
         fence_async_smem();
         if (warp <= kCopiesP2) copy_p2(warp - 1, sbase, W, maps, nxt, bar_p2);
         else if (warp <= kCopiesP2 + kCopiesS) copy_s(warp - 1 - kCopiesP2, sbase, W, maps, nxt, bar_s);
@@ -598,6 +626,8 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       }
       issue_beta(beta, P, nxt);
     }
+    float sgx[kSgIt];  // kSG: the next slot's scalars, stored into the gate tile at the end of the slot
+    if (kSG && more) sg_load(sgx, P, nxt);
     float gpb = 0.f, gpa = 0.f;  // kGate: this thread's dbias and dA_log partials
     {  // dg = reverse cumsum of dG over the chunk (G in log2 units)
       float qoff = 0.f, poff = 0.f, ppre = 0.f, ks = 0.f;
@@ -629,6 +659,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       const float carried = kLn2 * vec[V_GAML * kD + c] * red[64 + c];
       float qs = qoff, ps = poff + kLn2 * ks;
       const float sc = kGate ? kgate_scale(ga, j) : 0.f, gb = kGate && cin ? kgate_bias(ga, P.K, j, c) : 0.f;
+      float sgr[16];  // kSG: this thread's dg of each row, summed over the channels below
 #pragma unroll
       for (int p2 = 7; p2 >= 0; --p2) {
         float vv[2];
@@ -647,13 +678,19 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
             v *= d.x;
           }
           vv[w] = v;
+          if (kSG) sgr[t] = (r < len && cin) ? v : 0.f;
         }
-        // lanes (c, c + 1) trade one value and store rows 2 p2 (even lane), 2 p2 + 1 (odd lane)
-        const float got = __shfl_xor_sync(0xffffffffu, odd ? vv[0] : vv[1], 1);
-        const int rs = 16 * R + 2 * p2 + (odd ? 1 : 0);
-        if (rs < len && cin)
-          *reinterpret_cast<float2 *>(args.dg + ((size_t)(t0 + rs) * HV + j) * P.K + cp) =
-              odd ? make_float2(got, vv[1]) : make_float2(vv[0], got);
+        if (!kSG) {  // lanes (c, c + 1) trade one value and store rows 2 p2 (even lane), 2 p2 + 1 (odd lane)
+          const float got = __shfl_xor_sync(0xffffffffu, odd ? vv[0] : vv[1], 1);
+          const int rs = 16 * R + 2 * p2 + (odd ? 1 : 0);
+          if (rs < len && cin)
+            *reinterpret_cast<float2 *>(args.dg + ((size_t)(t0 + rs) * HV + j) * P.K + cp) =
+                odd ? make_float2(got, vv[1]) : make_float2(vv[0], got);
+        }
+      }
+      if (kSG) {  // the sum over the warp's 32 channels of each row, then over the 4 quarters below
+        const float v = rows16_sum(sgr);
+        if ((lane & 1) == 0) vec[V_SG * kD + quarter * kC + 16 * R + (lane >> 1)] = v;
       }
     }
     KDA_PT(12);
@@ -678,6 +715,13 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     }
     if (tid < kC && tid < len)
       args.dbeta[(size_t)(t0 + tid) * HV + j] = red[tid] + rb[tid] + rb[kC + tid] + rb[2 * kC + tid] + rb[3 * kC + tid];
+    if (kSG) {
+      if (tid < kC && tid < len) {
+        const float *sp = vec + V_SG * kD;
+        args.dg[(size_t)(t0 + tid) * HV + j] = sp[tid] + sp[kC + tid] + sp[2 * kC + tid] + sp[3 * kC + tid];
+      }
+      if (more) sg_store(G, sgx);  // (the gate tile is dead; the loop top publishes it)
+    }
     KDA_PT(8);
     if (!all_ok) {  // a wait gave up (error flag set): let the copies already issued land, then stop
       if (more) {
@@ -709,20 +753,22 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
 
 KDA_PT_EXPORT(kda_debug_intra_chunk_phase_cycles)
 
+template <bool kGate, bool kSG>
+cudaError_t launch_chunk(const Problem &P, const GateArgs &ga, const Workspace &W, const IntraArgs &a,
+                         const TmaMaps &maps, unsigned grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_chunk_tc_kernel<kGate, kSG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
+  if (e != cudaSuccess) return e;
+  KDA_LAUNCH("kda_bwd_intra_tc", s,
+             kda_bwd_intra_chunk_tc_kernel<kGate, kSG><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_intra_chunk(const Problem &P, const GateArgs &ga, const Workspace &W, const IntraArgs &a,
                                const TmaMaps &maps, unsigned grid, cudaStream_t s) {
-  if (ga.on) {
-    cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_chunk_tc_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
-    if (e != cudaSuccess) return e;
-    KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_chunk_tc_kernel<true><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_chunk_tc_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
-    if (e != cudaSuccess) return e;
-    KDA_LAUNCH("kda_bwd_intra_tc", s, kda_bwd_intra_chunk_tc_kernel<false><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
-  }
-  return cudaGetLastError();
+  if (P.scalar_gate) return launch_chunk<false, true>(P, ga, W, a, maps, grid, s);
+  return ga.on ? launch_chunk<true, false>(P, ga, W, a, maps, grid, s)
+               : launch_chunk<false, false>(P, ga, W, a, maps, grid, s);
 }
 
 }  // namespace kda

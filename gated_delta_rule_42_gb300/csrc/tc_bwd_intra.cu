@@ -933,7 +933,7 @@ KDA_PT_EXPORT(kda_debug_intra_phase_cycles)
 template <bool kSG, bool kL2, bool kGate>
 cudaError_t launch_intra(const Problem &P, const GateArgs &ga, const Workspace &W, const IntraArgs &a,
                          const TmaMaps &maps, unsigned grid, cudaStream_t s) {
-  constexpr bool kChunk = !kSG && !kL2;
+  constexpr bool kChunk = !kL2;
   constexpr int kFirst = kChunk ? kChunkWideList : kAllSlots;
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, kFirst, kGate>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
