@@ -98,6 +98,45 @@ __device__ __forceinline__ void sg_store(float *G, const float (&x)[kSgIt]) {
 // twelve rows it leaves free.
 constexpr int V_M = V_RREF, V_EM = V_EREF, V_LM = V_LAM;
 constexpr int V_SG = V_RREF + 1;  // kSG: dg row sums [4 channel quarters][64 rows] (two vector rows)
+// kL2 (the fused L2-norm backward): the rows' inverse norms (k rows 0..63, q rows 64..127)
+// in a vector row, and the row dots y . dy of q and of k as [64 rows][4 channel quarters]
+// tables in the KDA gate's partials area (written there only after the dg scan)
+constexpr int V_RN = V_RREF + 3;
+static_assert(V_RN < V_EREF, "a free vector row");
+constexpr uint32_t C_DOTQ = C_GPB, C_DOTK = C_GPB + 1024;
+static_assert(C_DOTK + 1024 <= C_GPA, "the dot tables fit the partials area");
+// Sum of v[t] over the warp's 32 lanes for each of 4 rows t: on return lanes 8t .. 8t + 7
+// hold row t's sum.
+__device__ __forceinline__ float rows4_sum(float (&v)[4]) {
+  const int lane = threadIdx.x & 31;
+  {
+    const bool up = (lane & 16) != 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool up = (lane & 8) != 0;
+    const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float t = v[0];
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
+}
+// An fp32 value parked as two 16-bit halves in a hi/lo tile pair's slots (and read back).
+__device__ __forceinline__ void park32(unsigned char *tile, uint32_t lo_off, uint32_t off, float x) {
+  const uint32_t b = __float_as_uint(x);
+  *reinterpret_cast<uint16_t *>(tile + off) = (uint16_t)(b >> 16);
+  *reinterpret_cast<uint16_t *>(tile + lo_off + off) = (uint16_t)(b & 0xffffu);
+}
+__device__ __forceinline__ float unpark32(const unsigned char *tile, uint32_t lo_off, uint32_t off) {
+  return __uint_as_float(((uint32_t)*reinterpret_cast<const uint16_t *>(tile + off) << 16) |
+                         (uint32_t)*reinterpret_cast<const uint16_t *>(tile + lo_off + off));
+}
 __device__ __forceinline__ int tot_row(int kind, int R) {
   const int k = 4 * kind + R;
   return k < 6 ? V_D + k : V_LAM + 2 + (k - 6);
@@ -153,8 +192,11 @@ __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
 }
 
 // kGate: the KDA gate inside the op; kSG: one decay per (token, value head), dg summed over
-// the channels (the two are not combined).
-template <bool kGate, bool kSG>
+// the channels (the two are not combined); kL2: the q/k L2-norm prologue with HV = H, its
+// backward dx = r (dy - y (y . dy)) fused: a first pass over the assembly parks each
+// element's dy and y in the thread's own tile slots and forms the row dots, a second pass
+// after a barrier stores dq, dk.
+template <bool kGate, bool kSG, bool kL2>
 __global__ void __launch_bounds__(kCT, 1)
 kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps,
                               GateArgs ga) {
@@ -379,6 +421,10 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
             kv[e] *= rk;
             qv[e] *= rq;
           }
+          if (kL2 && jj == 0) {  // the rows' inverse norms, for the fused backward
+            vec[V_RN * kD + r] = rk;
+            vec[V_RN * kD + kC + r] = rq;
+          }
         }
         float g[8];  // (two 16-byte reads: a half-warp reads one whole row, free of bank conflicts)
         *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGD + c0);
@@ -527,6 +573,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       tmem_ld6x4(tq + (uint32_t)(16 * R + 4 * s4), tb, tg, th, tx, ty, tz);
       if (s4 == 1) KDA_PT(18);
       const float4 b4 = *reinterpret_cast<const float4 *>(beta + 16 * R + 4 * s4);
+      float dq4[4], dk4[4];  // kL2: y . dy of the quad's rows over this thread's channel
 #pragma unroll
       for (int u = 0; u < 4; u += 2) {
         const int t = 4 * s4 + u, r = 16 * R + t;  // rows r, r + 1
@@ -564,7 +611,21 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
         cq += (in0 ? kht.x : 0.f) + (in1 ? kht.y : 0.f);
         bp[t] = bq.x;
         bp[t + 1] = bq.y;
-        {  // lanes (c, c + 1) trade one value: the even lane stores row r, the odd lane row r + 1,
+        if (kL2) {  // first pass: park dy (dq2, dk2) and y (Qr e2 = q~ normalised, Kr e2 = k normalised)
+          const float2 yq = __fmul2_rn(Qr, e2), yk = __fmul2_rn(Kr, e2);
+          park32(sm + C_KC, LO128, o0, dq2.x);
+          park32(sm + C_KC, LO128, o1, dq2.y);
+          park32(sm + C_QR, LO128, o0, yq.x);
+          park32(sm + C_QR, LO128, o1, yq.y);
+          park32(sm + C_KR, LO128, o0, yk.x);
+          park32(sm + C_KR, LO128, o1, yk.y);
+          G[r * kGD + c] = dk2.x;
+          G[(r + 1) * kGD + c] = dk2.y;
+          dq4[u] = yq.x * dq2.x;
+          dq4[u + 1] = yq.y * dq2.y;
+          dk4[u] = yk.x * dk2.x;
+          dk4[u + 1] = yk.y * dk2.y;
+        } else {  // lanes (c, c + 1) trade one value: the even lane stores row r, the odd lane row r + 1,
            // each as the channel pair (c & ~1, c | 1)
           const float gq = __shfl_xor_sync(0xffffffffu, odd ? dq2.x : dq2.y, 1);
           const float gk = __shfl_xor_sync(0xffffffffu, odd ? dk2.x : dk2.y, 1);
@@ -581,6 +642,14 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
               *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dk + (tok * H + h) * P.K + cp) = pack_bf16(pk.x, pk.y);
             }
           }
+        }
+      }
+      if (kL2) {  // the quad's row dots over the warp's 32 channels, into [row][quarter] tables
+        const float tqd = rows4_sum(dq4), tkd = rows4_sum(dk4);
+        if ((lane & 7) == 0) {
+          const int row = 16 * R + 4 * s4 + (lane >> 3);
+          reinterpret_cast<float *>(sm + C_DOTQ)[row * 4 + quarter] = tqd;
+          reinterpret_cast<float *>(sm + C_DOTK)[row * 4 + quarter] = tkd;
         }
       }
     }
@@ -613,6 +682,40 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     fence_before();
     __syncthreads();  // every read of the tiles, G and beta is done; the totals are published
     KDA_PT(10);
+    if (kL2) {  // second pass: dq, dk = r (dy - y (y . dy)) from the parked values and the row dots
+#pragma unroll
+      for (int p2 = 0; p2 < 8; ++p2) {
+        const int r = 16 * R + 2 * p2;
+        const uint32_t o0 = sw_off(r, c, kC), o1 = sw_off(r + 1, c, kC);
+        const float4 dqa = *reinterpret_cast<const float4 *>(sm + C_DOTQ + r * 16);
+        const float4 dqb = *reinterpret_cast<const float4 *>(sm + C_DOTQ + (r + 1) * 16);
+        const float4 dka = *reinterpret_cast<const float4 *>(sm + C_DOTK + r * 16);
+        const float4 dkb = *reinterpret_cast<const float4 *>(sm + C_DOTK + (r + 1) * 16);
+        const float2 dotq = make_float2(dqa.x + dqa.y + dqa.z + dqa.w, dqb.x + dqb.y + dqb.z + dqb.w);
+        const float2 dotk = make_float2(dka.x + dka.y + dka.z + dka.w, dkb.x + dkb.y + dkb.z + dkb.w);
+        const float2 rk = make_float2(vec[V_RN * kD + r], vec[V_RN * kD + r + 1]);
+        const float2 rq = make_float2(vec[V_RN * kD + kC + r], vec[V_RN * kD + kC + r + 1]);
+        const float2 dq2 = make_float2(unpark32(sm + C_KC, LO128, o0), unpark32(sm + C_KC, LO128, o1));
+        const float2 yq = make_float2(unpark32(sm + C_QR, LO128, o0), unpark32(sm + C_QR, LO128, o1));
+        const float2 yk = make_float2(unpark32(sm + C_KR, LO128, o0), unpark32(sm + C_KR, LO128, o1));
+        const float2 dk2 = make_float2(G[r * kGD + c], G[(r + 1) * kGD + c]);
+        // dq = rq (qscale dq2 - (yq / qscale) (y . dy)), dk = rk (dk2 - yk (y . dy)) (yq carries qscale)
+        const float iqs = 1.f / qscale;
+        const float2 fq = make_float2(rq.x * (qscale * dq2.x - yq.x * iqs * dotq.x),
+                                      rq.y * (qscale * dq2.y - yq.y * iqs * dotq.y));
+        const float2 fk = make_float2(rk.x * (dk2.x - yk.x * dotk.x), rk.y * (dk2.y - yk.y * dotk.y));
+        const float gq = __shfl_xor_sync(0xffffffffu, odd ? fq.x : fq.y, 1);
+        const float gk = __shfl_xor_sync(0xffffffffu, odd ? fk.x : fk.y, 1);
+        const float2 pq = odd ? make_float2(gq, fq.y) : make_float2(fq.x, gq);
+        const float2 pk = odd ? make_float2(gk, fk.y) : make_float2(fk.x, gk);
+        if (r + (odd ? 1 : 0) < len && cin) {
+          const size_t tok = (size_t)(t0 + r + (odd ? 1 : 0));
+          *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dq + (tok * H + h) * P.K + cp) = pack_bf16(pq.x, pq.y);
+          *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dk + (tok * H + h) * P.K + cp) = pack_bf16(pk.x, pk.y);
+        }
+      }
+      __syncthreads();  // every parked value is read: the tiles are dead
+    }
     if (more) {  // the next slot's remaining inputs into the dead tiles; its G and beta
       if (tid == 0) {
         mbar_expect_tx(bar_p2, kBytesP2 + (kSG ? 0u : kBytesG));
@@ -753,22 +856,30 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
 
 KDA_PT_EXPORT(kda_debug_intra_chunk_phase_cycles)
 
-template <bool kGate, bool kSG>
+template <bool kGate, bool kSG, bool kL2>
 cudaError_t launch_chunk(const Problem &P, const GateArgs &ga, const Workspace &W, const IntraArgs &a,
                          const TmaMaps &maps, unsigned grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_chunk_tc_kernel<kGate, kSG>,
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_chunk_tc_kernel<kGate, kSG, kL2>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
   KDA_LAUNCH("kda_bwd_intra_tc", s,
-             kda_bwd_intra_chunk_tc_kernel<kGate, kSG><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
+             kda_bwd_intra_chunk_tc_kernel<kGate, kSG, kL2><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
   return cudaGetLastError();
+}
+
+template <bool kL2>
+cudaError_t launch_chunk_l2(const Problem &P, const GateArgs &ga, const Workspace &W, const IntraArgs &a,
+                            const TmaMaps &maps, unsigned grid, cudaStream_t s) {
+  if (P.scalar_gate) return launch_chunk<false, true, kL2>(P, ga, W, a, maps, grid, s);
+  return ga.on ? launch_chunk<true, false, kL2>(P, ga, W, a, maps, grid, s)
+               : launch_chunk<false, false, kL2>(P, ga, W, a, maps, grid, s);
 }
 
 cudaError_t launch_intra_chunk(const Problem &P, const GateArgs &ga, const Workspace &W, const IntraArgs &a,
                                const TmaMaps &maps, unsigned grid, cudaStream_t s) {
-  if (P.scalar_gate) return launch_chunk<false, true>(P, ga, W, a, maps, grid, s);
-  return ga.on ? launch_chunk<true, false>(P, ga, W, a, maps, grid, s)
-               : launch_chunk<false, false>(P, ga, W, a, maps, grid, s);
+  // the L2-norm backward is fused when the q/k head's gradients come from one value head
+  return (P.l2norm && !a.partial) ? launch_chunk_l2<true>(P, ga, W, a, maps, grid, s)
+                                  : launch_chunk_l2<false>(P, ga, W, a, maps, grid, s);
 }
 
 }  // namespace kda

@@ -925,30 +925,22 @@ kda_bwd_intra_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_con
 
 KDA_PT_EXPORT(kda_debug_intra_phase_cycles)
 
-// The per-chunk gradients: the chunk-reference kernel over every slot (without
-// a scalar gate or the fused L2-norm backward), this kernel over the slots it
-// left (or over every slot), then the exact fix-up over the slots with a wide
-// 16-token block (none, usually: the CTAs of a list launch read its count and
-// leave).
+// The per-chunk gradients: the chunk-reference kernel over every slot, this kernel
+// over the slots it left (a wide chunk span), then the exact fix-up over the slots
+// with a wide 16-token block (none, usually: the CTAs of a list launch read its
+// count and leave).
 template <bool kSG, bool kL2, bool kGate>
 cudaError_t launch_intra(const Problem &P, const GateArgs &ga, const Workspace &W, const IntraArgs &a,
                          const TmaMaps &maps, unsigned grid, cudaStream_t s) {
-  constexpr bool kChunk = !kL2;
-  constexpr int kFirst = kChunk ? kChunkWideList : kAllSlots;
-  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, kFirst, kGate>,
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, kChunkWideList, kGate>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kda_bwd_intra_tc_kernel<kSG, kL2, kFixList, kGate>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  if (kChunk) {
-    if ((e = launch_intra_chunk(P, ga, W, a, maps, grid, s)) != cudaSuccess) return e;
-    KDA_LAUNCH("kda_bwd_intra_tc_block", s,
-               kda_bwd_intra_tc_kernel<kSG, kL2, kFirst, kGate><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
-  } else {
-    KDA_LAUNCH("kda_bwd_intra_tc", s,
-               kda_bwd_intra_tc_kernel<kSG, kL2, kFirst, kGate><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
-  }
+  if ((e = launch_intra_chunk(P, ga, W, a, maps, grid, s)) != cudaSuccess) return e;
+  KDA_LAUNCH("kda_bwd_intra_tc_block", s,
+             kda_bwd_intra_tc_kernel<kSG, kL2, kChunkWideList, kGate><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   KDA_LAUNCH("kda_bwd_intra_tc_fix", s,
              kda_bwd_intra_tc_kernel<kSG, kL2, kFixList, kGate><<<grid, kCT, C_SMEM, s>>>(P, W, a, maps, ga));

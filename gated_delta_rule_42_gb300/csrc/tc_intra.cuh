@@ -228,9 +228,9 @@ __device__ __forceinline__ void issue_gate_beta(uint32_t sbase, unsigned char *s
 
 }  // namespace intra
 
-// The chunk-reference kernel over every slot of the chunk table (any gate; not
-// the fused L2-norm backward): it lists the slots whose chunk decay span is too
-// wide for it in W.wide_cgrad (status word 5) for the block-reference kernel.
+// The chunk-reference kernel over every slot of the chunk table: it lists the
+// slots whose chunk decay span is too wide for it in W.wide_cgrad (status word 5)
+// for the block-reference kernel.
 cudaError_t launch_intra_chunk(const Problem &P, const GateArgs &ga, const Workspace &W, const intra::IntraArgs &a,
                                const TmaMaps &maps, unsigned grid, cudaStream_t s);
 
