@@ -159,3 +159,24 @@ def test_chunk_kda_autograd_reaches_the_gate_parameters():
         if key in ("dq", "dk", "dv", "dg", "dbeta"):
             got, want = got.reshape(inp.T, -1)[m], want.reshape(inp.T, -1)[m]
         assert torch.equal(got, want), key
+
+
+@pytest.mark.parametrize("hv,lb", [(2, None), (4, -5.0)], ids=["fused_norm_bwd_unbounded", "gva_partials_bounded"])
+def test_kda_gate_with_l2norm_prologue(hv, lb):
+    """The KDA gate and the q/k L2-norm prologue together, on raw (unnormalised)
+    q, k rows: with HV = H the norm's backward is fused into the gradient kernel,
+    with HV > H it runs on the per-value-head partials afterwards."""
+    import numpy as np
+    inp = _inp("gate_l2", dict(B=1, T=300, H=2, HV=hv, K=128, V=128, cu_seqlens=[0, 0, 130, 300]), torch.bfloat16,
+               lb, {}, seed=86 + hv)
+    rng = np.random.default_rng(87)
+    for name in ("q", "k"):  # rows of norm e^N(0, 0.7): the prologue has something to undo
+        x = getattr(inp, name)
+        f = torch.from_numpy(np.exp(rng.normal(0.0, 0.7, size=x.shape[:-1] + (1,))))
+        setattr(inp, name, (x.to(torch.float64) * f).to(inp.dtype))
+    tol = H.TOL[inp.dtype]
+    o, hT = H.gpu_fwd(inp, l2=True)
+    ro, rhT = H.oracle_fwd(inp, l2=True)
+    H.check_fwd(inp, o, hT, ro, rhT, tol["fwd"])
+    gr = H.gpu_bwd(inp, l2=True)
+    H.check_bwd(inp, gr, H.oracle_bwd(inp, l2=True), tol["bwd"])
