@@ -252,8 +252,12 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
   for (uint32_t it = 0; have; ++it) {
     const uint32_t par = it & 1u;
     const int t0 = cur.t0, len = cur.len, j = cur.j, h = cur.h;
-    Slot nn;
-    const bool more2 = get_slot<kAllSlots>(P, W, s_idx + 2 * (int64_t)gridDim.x, 0, nn);
+    // the chunk-table entry of the slot after next: loaded now, decoded at the end of the
+    // slot (nothing waits for the load in between)
+    const int64_t s_n2 = s_idx + 2 * (int64_t)gridDim.x;
+    const bool in_n2 = s_n2 < (int64_t)P.NC * HV;
+    const int c_n2 = in_n2 ? (int)(s_n2 / HV) : 0;
+    const int4 ent_n2 = W.chunk[c_n2];
     bool ok = true;  // every bounded wait of this thread succeeded
     KDA_PT(13);
     ok &= bar_wait(bar_s, par, args.err);
@@ -839,8 +843,12 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     }
     cur = nxt;
     have = more;
-    nxt = nn;
-    more = more2;
+    nxt.j = (int)(s_n2 - (int64_t)c_n2 * HV);
+    nxt.h = nxt.j / (HV / H);
+    nxt.t0 = ent_n2.y;
+    nxt.len = ent_n2.z;
+    nxt.slot = (size_t)s_n2;
+    more = in_n2 && ent_n2.x >= 0;
     s_idx += gridDim.x;
   }  // slot loop
   fence_before();
