@@ -132,9 +132,9 @@ def kernel_bytes_per_token(name, cfg):
 # those sources are unchanged.
 NCU_TRAFFIC = {
     "kda_bwd_intra_tc": dict(
-        bytes_per_token=1282299392 / 8192,  # 974.3 MB read + 308.0 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=1282072064 / 8192,  # 974.3 MB read + 307.8 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_chunk.cu", "gated_delta_rule_42_gb300/csrc/tc_intra.cuh", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="64811d10a74f805bee872f2b5c83dcaefce7588564d78555b219d602f581c5ad"),
+        sha256="b72319c6c15e3e8bbafde0eebdd8e8dc9e881e3fb966ac19d8fe00307ee198af"),
     "kda_prep_tc": dict(
         bytes_per_token=493784064 / 8192,  # 270.6 MB read + 223.2 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_prep.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
