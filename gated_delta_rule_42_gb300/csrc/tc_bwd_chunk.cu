@@ -515,7 +515,8 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
           mma16816(acc[1], al, b[2], b[3]);
         }
       }
-      __syncthreads();  // every warp has read dA: its tiles become dL
+      // (every read of dA, by the T phase, ended at the barrier before this phase: its tiles
+      // become dL without another)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -684,7 +685,10 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       if ((lane & 1) == 0) rb[quarter * kC + 16 * R + (lane >> 1)] = v;
     }
     fence_before();
-    __syncthreads();  // every read of the tiles, G and beta is done; the totals are published
+    // every read of the tiles, G and beta is done; the totals are published; every wait of
+    // the slot is behind, so its outcome is known here (the KDA gate and the scalar gate
+    // reduce theirs at the end of the slot, where their sums need a barrier anyway)
+    bool all_ok = __syncthreads_and(ok) != 0;
     KDA_PT(10);
     if (kL2) {  // second pass: dq, dk = r (dy - y (y . dy)) from the parked values and the row dots
 #pragma unroll
@@ -807,7 +811,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       for (int o = 16; o > 0; o >>= 1) gpa += __shfl_xor_sync(0xffffffffu, gpa, o);
       if (lane == 0) reinterpret_cast<float *>(sm + C_GPA)[warp] = gpa;
     }
-    const bool all_ok = __syncthreads_and(ok) != 0;
+    if (kGate || kSG) all_ok = __syncthreads_and(ok) != 0;
     KDA_PT(7);
     if (kGate) {  // the slot's partials, summed in a fixed order: dbias per channel, dA_log per slot
       if (tid < kD) {
