@@ -132,9 +132,9 @@ def kernel_bytes_per_token(name, cfg):
 # those sources are unchanged.
 NCU_TRAFFIC = {
     "kda_bwd_intra_tc": dict(
-        bytes_per_token=1282072064 / 8192,  # 974.3 MB read + 307.8 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=1282380032 / 8192,  # 974.3 MB read + 308.1 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_chunk.cu", "gated_delta_rule_42_gb300/csrc/tc_intra.cuh", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="b72319c6c15e3e8bbafde0eebdd8e8dc9e881e3fb966ac19d8fe00307ee198af"),
+        sha256="5dc08a1915124138a9f8d926e8cbe4e5a5a10bd7b8a9f555a9d5148d2cc1946f"),
     "kda_prep_tc": dict(
         bytes_per_token=493784064 / 8192,  # 270.6 MB read + 223.2 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_prep.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
