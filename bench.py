@@ -222,42 +222,67 @@ def load_peaks():
 
 # --------------------------------------------------------------------------
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks / throttle reasons sampled during the timed region: every
+    20 ms, each sample stamped on arrival; only the samples that arrive between
+    begin() and end() (plus one interval) count, or the first one after begin()
+    when the region is shorter than an interval."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (arrival time, line)
+        self.t_begin = self.t_end = None
 
     def start(self):
+        """Start sampling and wait (up to 3 s) until the first sample arrives."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.INTERVAL_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
+            t_stop = time.monotonic() + 3.0
+            while not self.lines and time.monotonic() < t_stop and self.proc.poll() is None:
+                time.sleep(0.005)
         except Exception:
             self.proc = None
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def begin(self):
+        self.t_begin = time.monotonic()
+
+    def end(self):
+        self.t_end = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return None
+        if self.t_end is not None:  # let the sample that covers the region's end arrive
+            time.sleep(2 * self.INTERVAL_MS / 1e3)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        lines = list(self.lines)
+        if self.t_begin is not None and self.t_end is not None:
+            lag = self.INTERVAL_MS / 1e3
+            inside = [ln for t, ln in lines if self.t_begin <= t <= self.t_end + lag]
+            after = [ln for t, ln in lines if t >= self.t_begin]
+            lines = inside if inside else after[:1]
+        else:
+            lines = [ln for _, ln in lines]
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -272,7 +297,7 @@ class ClockSampler:
         if not sm:
             return None
         return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons),
-                    samples=len(sm))
+                    samples=len(sm), interval_ms=self.INTERVAL_MS)
 
 
 # --------------------------------------------------------------------------
@@ -658,7 +683,9 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    clocks.begin()
     ms = timed(runner.step, args.steps, runner.stream)
+    clocks.end()
     if dist:
         dist.barrier()
     launches = runner.lib.kda_launch_count() - n0

@@ -93,3 +93,33 @@ def test_step_traffic_needs_a_capture_for_every_kernel_that_matters():
         want = sum(bench.NCU_TRAFFIC[k]["bytes_per_token"] * 8192 for k in list(split)[:4])
         assert abs(got - want) <= 4
     assert bench.step_traffic(dict(split, other_kernel=(5.0, 10)), 10, 8192) is None
+
+
+def test_clock_sampler_keeps_the_samples_of_the_timed_region():
+    """Samples count only when they arrive between begin() and end() plus one
+    interval (or, for a region shorter than an interval, the first one after
+    begin()); a slowdown reason outside the region is not reported."""
+    class _Proc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    def line(mhz, hw="Not Active"):
+        return f"0, {mhz}, 2070, 900.0, 0x0, {hw}, Not Active, Not Active, Not Active"
+
+    s = bench.ClockSampler(0)
+    s.proc = _Proc()
+    s.INTERVAL_MS = 0  # (no wait for a last sample in the test)
+    s.t_begin, s.t_end = 10.0, 10.1
+    s.lines = [(9.9, line(1200, "Active")), (10.02, line(2070)), (10.07, line(2065)), (10.5, line(1000, "Active"))]
+    got = s.stop()
+    assert got["samples"] == 2 and got["sm_mhz"] == 2067.5 and got["reasons"] == []
+    s2 = bench.ClockSampler(0)
+    s2.proc = _Proc()
+    s2.INTERVAL_MS = 0
+    s2.t_begin, s2.t_end = 10.0, 10.001
+    s2.lines = [(9.9, line(1200)), (10.03, line(2070, "Active")), (10.06, line(2060))]
+    got = s2.stop()
+    assert got["samples"] == 1 and got["sm_mhz"] == 2070 and got["reasons"] == ["hw_slowdown"]
