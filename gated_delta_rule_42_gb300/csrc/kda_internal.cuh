@@ -69,7 +69,7 @@ struct Workspace {
   float *dqp;    // [Ttot][HV][K]   per-value-head dq~ partials
   float *dkp;    // [Ttot][HV][K]
   float *dw;     // [slot][64][K]
-  // tensor-core backward (bf16, K = V = 128), per (chunk, value head) slot
+  // tensor-core backward (bf16, K, V = 64 or 128 in 128-wide tiles), per (chunk, value head) slot
   __nv_bfloat16 *tc_hs;     // [slot] 32 KB: chunk-start state h [K][V], swizzled operand tile (forward recompute)
   unsigned char *tc_tiles;  // [slot] kTileRecord bytes: the per-chunk record (kRec* offsets)
   unsigned char *tc_xt;     // [slot] 16 KB: swizzled X^T tile [V][64]
@@ -185,7 +185,7 @@ cudaError_t launch_recurrent(const Problem &P, const GateArgs &ga, void *o, floa
 // Per-chunk records (tc_prep.cu): one CTA per (chunk, value head) slot.
 cudaError_t tc_prepare(const Problem &P, const GateArgs &ga, const Workspace &W, const TmaMaps &maps, int *err,
                        cudaStream_t s);
-// bf16, K = V = 128 tensor-core forward: the records into W.tc_tiles (unless
+// bf16 tensor-core forward (K, V = 64 or 128): the records into W.tc_tiles (unless
 // records_ready: W.tc_tiles already holds them for these q, k, g, beta), then
 // the state chain.  mode is kFwdOutput (o, hT), kFwdSave (no output: per
 // (chunk, value head) slot the chunk-start state and the X^T, D^T tiles go to

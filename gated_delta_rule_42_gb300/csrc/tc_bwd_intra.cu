@@ -1,7 +1,11 @@
-// Per-chunk gradients of the bf16 chunked KDA backward (K = V = 128): the
-// tensor-core products and the gradient chain in one kernel.
+// Per-chunk gradients of the bf16 chunked KDA backward on 16-token block
+// references: the tensor-core products and the gradient chain in one kernel.
+// It runs over the slots the chunk-reference kernel (tc_bwd_chunk.cu) lists,
+// those whose chunk decay span is too wide for one reference per chunk, and its
+// fix-up launch over the slots with a 16-token block too wide for it in turn.
+// (K, V = 64 run in the 128-wide tiles, zero-padded.)
 //
-// Persistent: one CTA (16 warps) per SM walks the (chunk, value head) slots,
+// Persistent: one CTA (16 warps) per SM walks its slots,
 // and loads the next slot's inputs into tiles as soon as the current slot's
 // work leaves them dead (three groups, below), so most of each slot's loads
 // overlap the previous slot's chain and assembly.  Inputs: the

@@ -1,4 +1,4 @@
-// Reverse state-gradient scan of the bf16 chunked KDA backward (K = V = 128).
+// Reverse state-gradient scan of the bf16 chunked KDA backward (K, V = 64 or 128).
 //
 // One CTA walks the chunks of one (sequence, value head) from last to first,
 // holding dh' -- the gradient of the chunk-END state -- in fp32 registers

@@ -1,4 +1,4 @@
-// Shared pieces of the bf16 tensor-core KDA kernels (K = V = 128, chunk 64):
+// Shared pieces of the bf16 tensor-core KDA kernels (K, V = 64 or 128 in 128-wide tiles, chunk 64):
 // the asynchronous loads and bulk copies, the phase-timing hooks and the
 // operand-descriptor helpers.
 //

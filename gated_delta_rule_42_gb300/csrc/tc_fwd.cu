@@ -1,4 +1,4 @@
-// Sequential bf16 chunked KDA forward on the sm_103a tensor cores (K = V = 128).
+// Sequential bf16 chunked KDA forward on the sm_103a tensor cores (K, V = 64 or 128).
 //
 // One CTA walks the chunks of one (sequence, value head) in order, keeping the
 // fp32 state h[K][V] in registers (thread = key channel c, half the value

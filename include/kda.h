@@ -169,7 +169,7 @@ kda_status kda_chunk_bwd(const kda_inputs *in, const void *dO, const float *dhT,
 
 /* ---- forward context: the backward without its recompute (no counterpart on
  * the pages, which leave open what a forward keeps for its backward) ----
- * On the tensor-core path (bf16, K = V = 128, aligned q/k/v/g) the backward
+ * On the tensor-core path (bf16, K, V = 64 or 128, aligned q/k/v/g) the backward
  * first re-runs two forward kernels: the per-chunk record kernel and the
  * state chain that saves every chunk's start state.  kda_chunk_fwd_ctx writes
  * those results into a caller-owned context buffer while it computes o, and
