@@ -202,6 +202,62 @@ __device__ __forceinline__ int phase_a(unsigned char *sm, int len, const float *
   return 0;
 }
 
+
+// ---- 16x16 warp MMAs on fp32 operands split into hi + lo bf16 (the inverse's merges) ----
+// Row strides of the fp32 scratch tiles (row-major), chosen so that the fragment loads
+// and stores below are free of bank conflicts.
+constexpr int kTs16 = 20, kTs8 = 12;
+__device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16(x.x, x.y);
+  const float2 h = unpack_bf16(hi);
+  lo = pack_bf16(x.x - h.x, x.y - h.y);
+}
+// A fragment (m16n8k16, rows r0 .., columns k0 ..) of an fp32 [64][64] fsw tile, as hi / lo.
+__device__ __forceinline__ void frag_a_f32(const float *M, int r0, int k0, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  split2(*reinterpret_cast<const float2 *>(M + fsw(r0 + g, k0 + 2 * q)), hi[0], lo[0]);
+  split2(*reinterpret_cast<const float2 *>(M + fsw(r0 + g + 8, k0 + 2 * q)), hi[1], lo[1]);
+  split2(*reinterpret_cast<const float2 *>(M + fsw(r0 + g, k0 + 2 * q + 8)), hi[2], lo[2]);
+  split2(*reinterpret_cast<const float2 *>(M + fsw(r0 + g + 8, k0 + 2 * q + 8)), hi[3], lo[3]);
+}
+// B fragment (element (k, n) = M[k0 + k][n0 + n], k < 16, n < 8) of an fp32 fsw tile.
+__device__ __forceinline__ void frag_b_fsw(const float *M, int k0, int n0, uint32_t (&hi)[2], uint32_t (&lo)[2]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int k = k0 + 2 * q + 8 * h;
+    split2(make_float2(M[fsw(k, n0 + g)], M[fsw(k + 1, n0 + g)]), hi[h], lo[h]);
+  }
+}
+// The same from a row-major fp32 scratch tile of row stride ld.
+__device__ __forceinline__ void frag_b_rm(const float *M, int ld, int k0, int n0, uint32_t (&hi)[2],
+                                          uint32_t (&lo)[2]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int k = k0 + 2 * q + 8 * h;
+    split2(make_float2(M[k * ld + n0 + g], M[(k + 1) * ld + n0 + g]), hi[h], lo[h]);
+  }
+}
+__device__ __forceinline__ void mma3x(float (&c)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                      const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+  mma16816(c, ah, bh[0], bh[1]);
+  mma16816(c, ah, bl[0], bl[1]);
+  mma16816(c, al, bh[0], bh[1]);
+}
+// C fragment (rows r0 + g, r0 + g + 8; columns c0 + 2q, + 1) into a row-major scratch tile ...
+__device__ __forceinline__ void store_c(float *M, int ld, int r0, int c0, const float (&c)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  *reinterpret_cast<float2 *>(M + (r0 + g) * ld + c0 + 2 * q) = make_float2(c[0], c[1]);
+  *reinterpret_cast<float2 *>(M + (r0 + g + 8) * ld + c0 + 2 * q) = make_float2(c[2], c[3]);
+}
+// ... or, negated, into an fp32 fsw tile.
+__device__ __forceinline__ void store_c_fsw_neg(float *M, int r0, int c0, const float (&c)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  *reinterpret_cast<float2 *>(M + fsw(r0 + g, c0 + 2 * q)) = make_float2(-c[0], -c[1]);
+  *reinterpret_cast<float2 *>(M + fsw(r0 + g + 8, c0 + 2 * q)) = make_float2(-c[2], -c[3]);
+}
+
 // The inverse A = (I + L)^-1 of L (fp32 in shared memory, strictly lower) and
 // its bf16 record tile.  Begins after a __syncthreads that published L.
 __device__ __forceinline__ void invert_store(unsigned char *sm, unsigned char *rec) {
@@ -244,72 +300,67 @@ __device__ __forceinline__ void invert_store(unsigned char *sm, unsigned char *r
   KDA_PT(5);
   // Off-diagonal blocks, 32-blocked: A = [[A1, 0], [A21, A2]] with A21 = -A2 L21 A1,
   // where A1 = [[D0, 0], [-D1 L10 D0, D1]] and A2 likewise from D2, D3 (D_R the
-  // diagonal-block inverses above).  Each thread forms 1 x 4 row segments.
-  for (int e = tid; e < 2 * 64; e += kThr) {  // T_b = L_{R,R-1} D_{R-1} for R = 1, 3
-    const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // diagonal-block inverses above).  The products run on 16x16 warp MMAs with each
+  // fp32 operand split into a hi and a lo bf16 (hi*hi + hi*lo + lo*hi: about 16
+  // mantissa bits, far below the bf16 rounding of the record), each chain inside one
+  // warp: A_{R,R-1} = -D_R (L_{R,R-1} D_{R-1}) for R = 1, 3 on warps 0 and 1, then
+  // column block w (8 columns) of A21 = -A2 (L21 A1) on warp w < 4.
+  if (warp < 2) {
+    const int R = 2 * warp + 1;
+    float *Ts = Tf + warp * 16 * kTs16;  // L_{R,R-1} D_{R-1}, row-major [16][kTs16]
+    uint32_t ah[4], al[4];
+    frag_a_f32(Lf, 16 * R, 16 * (R - 1), ah, al);
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float l = Lf[fsw(16 * R + rr, 16 * (R - 1) + m)];
-      const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(16 * (R - 1) + m, 16 * (R - 1) + i4));
-      acc.x = fmaf(l, a.x, acc.x); acc.y = fmaf(l, a.y, acc.y);
-      acc.z = fmaf(l, a.z, acc.z); acc.w = fmaf(l, a.w, acc.w);
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t bh[2], bl[2];
+      frag_b_fsw(Af, 16 * (R - 1), 16 * (R - 1) + 8 * nt, bh, bl);
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      mma3x(c, ah, al, bh, bl);
+      store_c(Ts, kTs16, 0, 8 * nt, c);
     }
-    *reinterpret_cast<float4 *>(Tf + (b * 16 + rr) * 16 + i4) = acc;
+    __syncwarp();
+    frag_a_f32(Af, 16 * R, 16 * R, ah, al);  // D_R
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t bh[2], bl[2];
+      frag_b_rm(Ts, kTs16, 0, 8 * nt, bh, bl);
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      mma3x(c, ah, al, bh, bl);
+      store_c_fsw_neg(Af, 16 * R, 16 * (R - 1) + 8 * nt, c);
+    }
   }
   __syncthreads();
   KDA_PT(6);
-  for (int e = tid; e < 2 * 64; e += kThr) {  // A_{R,R-1} = -D_R T_b
-    const int b = e >> 6, R = 2 * b + 1, rr = (e >> 2) & 15, i4 = (e & 3) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (warp < 4) {
+    float *Ts = Tf + 2 * 16 * kTs16 + warp * 32 * kTs8;  // column block w of L21 A1, [32][kTs8]
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float l = Af[fsw(16 * R + rr, 16 * R + m)];
-      const float4 t = *reinterpret_cast<const float4 *>(Tf + (b * 16 + m) * 16 + i4);
-      acc.x = fmaf(l, t.x, acc.x); acc.y = fmaf(l, t.y, acc.y);
-      acc.z = fmaf(l, t.z, acc.z); acc.w = fmaf(l, t.w, acc.w);
-    }
-    *reinterpret_cast<float4 *>(Af + fsw(16 * R + rr, 16 * (R - 1) + i4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-  }
-  __syncthreads();
-  KDA_PT(7);
-  if (tid < 128) {  // 32 x 32 products as 2 x 4 register tiles (rows rg, rg + 16) on four warps
-    const int rg = tid >> 3, c4 = (tid & 7) * 4;
-    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {  // T2 = L21 A1  (A1 lower triangular: zeros above)
-      const float4 a = *reinterpret_cast<const float4 *>(Af + fsw(m, c4));
+    for (int mt = 0; mt < 2; ++mt) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float l = Lf[fsw(32 + rg + 16 * k, m)];
-        acc[k].x = fmaf(l, a.x, acc[k].x); acc[k].y = fmaf(l, a.y, acc[k].y);
-        acc[k].z = fmaf(l, a.z, acc[k].z); acc[k].w = fmaf(l, a.w, acc[k].w);
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        frag_a_f32(Lf, 32 + 16 * mt, 16 * ks, ah, al);  // L21
+        frag_b_fsw(Af, 16 * ks, 8 * warp, bh, bl);    // A1 (its upper block is zero)
+        mma3x(c, ah, al, bh, bl);
       }
+      store_c(Ts, kTs8, 16 * mt, 0, c);
     }
+    __syncwarp();
 #pragma unroll
-    for (int k = 0; k < 2; ++k) *reinterpret_cast<float4 *>(Tf + (rg + 16 * k) * 32 + c4) = acc[k];
+    for (int mt = 0; mt < 2; ++mt) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        frag_a_f32(Af, 32 + 16 * mt, 32 + 16 * ks, ah, al);  // A2
+        frag_b_rm(Ts, kTs8, 16 * ks, 0, bh, bl);
+        mma3x(c, ah, al, bh, bl);
+      }
+      store_c_fsw_neg(Af, 32 + 16 * mt, 8 * warp, c);
+    }
   }
   __syncthreads();
   KDA_PT(8);
-  if (tid < 128) {
-    const int rg = tid >> 3, c4 = (tid & 7) * 4;
-    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {  // A21 = -A2 T2
-      const float4 t = *reinterpret_cast<const float4 *>(Tf + m * 32 + c4);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float l = Af[fsw(32 + rg + 16 * k, 32 + m)];
-        acc[k].x = fmaf(l, t.x, acc[k].x); acc[k].y = fmaf(l, t.y, acc[k].y);
-        acc[k].z = fmaf(l, t.z, acc[k].z); acc[k].w = fmaf(l, t.w, acc[k].w);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-      *reinterpret_cast<float4 *>(Af + fsw(32 + rg + 16 * k, c4)) = make_float4(-acc[k].x, -acc[k].y, -acc[k].z, -acc[k].w);
-  }
-  __syncthreads();
-  KDA_PT(9);
   for (int e = tid; e < kC * kC / 8; e += kThr) {  // A -> bf16 tile, 16-byte chunks
     const int r = e >> 3, jj = e & 7;
     float x[8];
