@@ -32,7 +32,10 @@
 //                                                                   with the dG_last term)
 //   dbeta = sum_v dX v + sum_c (dBk k Gamma + k e1 xr)
 // and runs the reverse cumsum dg of its channel over its rows in registers, the
-// block totals exchanged in shared memory.  These are the intra-chunk backward
+// block totals exchanged in shared memory.  Between the first products and the
+// chain the CTA splits in two groups of 8 warps: one turns dA into T = A^T dA and
+// dL = -tril_{-1}(T A^T) on warp MMAs while the other loads raw k and q, runs
+// the gate's cumsum and builds the decayed tiles.  These are the intra-chunk backward
 // steps of FLA's chunk_bwd_dqkwg / chunk_bwd_dv_local / prepare_wy_repr_bwd
 // ("[Fix] Use unit KDA gate scale when A_log is omitted",
 // fla-org/flash-linear-attention PR #1294, commit log); the inputs and their
@@ -60,6 +63,28 @@ static_assert(T_YR == T_XR + 64, "xr and yr are one N = 128 product");
 // twins 16 KB on.
 constexpr uint32_t CK_DA = C_DAB, CK_DAQK = C_DAB + 8192;
 static_assert(CK_DAQK + 8192 + LO128 <= C_XB, "dA/dL and dAqk with their lo twins");
+// From the products to the chain the CTA runs as two groups of 8 warps (named barriers 1
+// and 2): raw k and q land in the Kr and Qr hi tiles' places, so the second group's tiles
+// and the first group's dA, dAqk, T, dL and X tiles are disjoint.
+constexpr int kGroupWarps = 8;
+constexpr int kBarChainGroup = 1, kBarTileGroup = 2;
+constexpr uint32_t CK_KRAW = C_KR, CK_QRAW = C_QR;
+static_assert(C_KC + 2 * 16384 <= CK_DA && CK_DAQK + 8192 + LO128 <= C_XB && C_T + 16384 <= C_G,
+              "the two groups' tiles are disjoint");
+// Barrier among the 256 threads of one group.
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(kGroupWarps * 32) : "memory");
+}
+// The same, returning whether any of the group's threads passed a nonzero v.
+__device__ __forceinline__ bool group_sync_or(int id, int v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v), "r"(id), "r"(kGroupWarps * 32)
+      : "memory");
+  return r != 0;
+}
 constexpr float kLn2 = 0.69314718055994530942f;
 // The gate tile arrives by TMA with group P2: dense [64][128] fp32 rows (rows
 // past the chunk hold other tokens until the cumsum overwrites them).
@@ -331,165 +356,207 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     __syncthreads();  // products in TMEM; the operand tiles are dead
     KDA_PT(0);
 
-    // ---- raw k, q rows; dA, dAqk out of TMEM as hi/lo tiles; the gate; G and the reference ----
-    if (tid == 0) {  // (into the dh' and v tiles, dead now)
-      fence_async_smem();
-      mbar_expect_tx(bar_kq, 32768u);
-      tma_tile(sbase + C_KRAW, &maps.k, h, t0, bar_kq);
-      tma_tile(sbase + C_QRAW, &maps.q, h, t0, bar_kq);
-    }
-    {
-      // Z: lanes 0..63 (r), cols 64..127 (i) = dAqk[r][i]; lanes 64..127 (m), cols 0..63 (i) = dA[m][i]
-      const int cg = warp >> 2, row = 32 * (quarter & 1) + lane;
-      const bool qk = quarter < 2;
-      float x[16];
-      tmem_ld16(tq + T_Z + (qk ? 64u : 0u) + (uint32_t)(16 * cg), x);
+    // ---- two warp groups until the chain: warps 0..7 take dA and dAqk out of TMEM and run
+    // T = A^T dA and dL; warps 8..15 load the raw k, q rows and build G, the reference and the
+    // decayed tiles.  Their tiles are disjoint: the raw rows land in the Kr and Qr hi tiles'
+    // places (dead product operands), each 16-byte chunk rewritten by the thread that read it. ----
+    if (warp < kGroupWarps) {
+      {  // Z: lanes 0..63 (r), cols 64..127 (i) = dAqk[r][i]; lanes 64..127 (m), cols 0..63 (i) = dA[m][i]
+        const int ch = warp >> 2, row = 32 * (quarter & 1) + lane;  // ch: the column half
+        const bool qk = quarter < 2;
+        float x[32];
+        tmem_ld32(tq + T_Z + (qk ? 64u : 0u) + (uint32_t)(32 * ch), x);
 #pragma unroll
-      for (int hx = 0; hx < 2; ++hx) {
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int col = 16 * cg + 8 * hx + e;
-          y[e] = (qk && col > row) ? 0.f : x[8 * hx + e];  // dAqk[r][i] is a gradient of Aqk only where i <= r
-        }
-        uint4 hi, lo;
-        split8(y, hi, lo);
-        const uint32_t off = sw_chunk(row, 2 * cg + hx, kC);
-        *reinterpret_cast<uint4 *>(sm + (qk ? CK_DAQK : CK_DA) + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + (qk ? CK_DAQK : CK_DA) + LO128 + off) = lo;
-      }
-    }
-    if (kGate) {  // the decay from the raw gate
-      kgate_tile<kCT>(G, kGD, len, P.K, j, ga);
-      __syncthreads();
-    }
-    int wide_c = 0;
-    if (tid < kD) {
-      const int c = tid;
-      float s = 0.f;
-      float col[kC];
-#pragma unroll
-      for (int r = 0; r < kC; ++r) col[r] = G[r * kGD + c];
-#pragma unroll
-      for (int r = 0; r < kC; ++r) {
-        if (r < len) s += col[r];
-        col[r] = s;
-      }
-#pragma unroll
-      for (int r = 0; r < kC; ++r) G[r * kGD + c] = col[r];
-      const float gl = s, m = 0.5f * (col[0] + gl);  // rows past len hold G_last
-      wide_c = !(col[0] - gl <= kChunkSpan);        // (NaN-safe)
-      vec[V_GL * kD + c] = gl;
-      vec[V_GAML * kD + c] = exp2f(gl);
-      vec[V_M * kD + c] = m;
-      vec[V_EM * kD + c] = exp2f(m);
-      vec[V_LM * kD + c] = exp2f(gl - m);
-    }
-    ok &= bar_wait(bar_kq, par, args.err);  // raw k, q
-    if (len < kC) {  // rows past the sequence end hold other tokens: clear them
-      zero_tail<kCT>(sm + C_KRAW, len);
-      zero_tail<kCT>(sm + C_QRAW, len);
-    }
-    // a channel's decay span is wider than one reference carries: list the slot
-    // for the block-reference kernel (whose results replace this launch's)
-    if (__syncthreads_or(wide_c) != 0 && tid == 0) W.wide_cgrad[atomicAdd(W.flags + 5, 1)] = (int)cur.slot;
-    KDA_PT(1);
-    {  // the decayed hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2
-      const int jj = tid & 15, c0 = jj * 8, rg = tid >> 4;  // two rows per thread
-      float mv[8];
-#pragma unroll
-      for (int e = 0; e < 8; e += 4)
-        *reinterpret_cast<float4 *>(mv + e) = *reinterpret_cast<const float4 *>(vec + V_M * kD + c0 + e);
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int r = rg * 2 + rr;
-        const uint32_t off = sw_chunk(r, jj, kC);
-        float kv[8], qv[8], o[8], e1[8], e2[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sm + C_KRAW + off), kv);  // raw k, q (zero past len)
-        unpack8(*reinterpret_cast<const uint4 *>(sm + C_QRAW + off), qv);
-        if (P.l2norm) {  // q/k L2-norm prologue (value-head partials: its backward runs per q/k head afterwards)
-          float sk = 0.f, sq = 0.f;
+        for (int hx = 0; hx < 4; ++hx) {
+          float y[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            sk = fmaf(kv[e], kv[e], sk);
-            sq = fmaf(qv[e], qv[e], sq);
+            const int col = 32 * ch + 8 * hx + e;
+            y[e] = (qk && col > row) ? 0.f : x[8 * hx + e];  // dAqk[r][i] is a gradient of Aqk only where i <= r
           }
+          uint4 hi, lo;
+          split8(y, hi, lo);
+          const uint32_t off = sw_chunk(row, 4 * ch + hx, kC);
+          *reinterpret_cast<uint4 *>(sm + (qk ? CK_DAQK : CK_DA) + off) = hi;
+          *reinterpret_cast<uint4 *>(sm + (qk ? CK_DAQK : CK_DA) + LO128 + off) = lo;
+        }
+      }
+      group_sync(kBarChainGroup);
+      KDA_PT(1);
+      // ---- T = A^T dA  (T[r][m] = sum_i' A[i'][r] dA[i'][m]); a warp: 16 rows, 32 columns ----
+      const int mt = warp >> 1, nh = warp & 1;
+      {
+        float acc[4][4] = {};
 #pragma unroll
-          for (int o2 = 1; o2 < 16; o2 <<= 1) {
-            sk += __shfl_xor_sync(0xffffffffu, sk, o2);
-            sq += __shfl_xor_sync(0xffffffffu, sq, o2);
+        for (int s = 0; s < 4; ++s) {
+          uint32_t a[4];
+          lda_t(sbase + C_A, kC, 16 * mt, 16 * s, a);  // element (r, i') = A[i'][r]
+#pragma unroll
+          for (int qq = 0; qq < 2; ++qq) {
+            uint32_t bh[4], bl[4];
+            ldb_t(sbase + CK_DA, kC, 32 * nh + 16 * qq, 16 * s, bh);  // element (i', m) = dA[i'][m]
+            ldb_t(sbase + CK_DA + LO128, kC, 32 * nh + 16 * qq, 16 * s, bl);
+            mma16816(acc[2 * qq], a, bh[0], bh[1]);
+            mma16816(acc[2 * qq], a, bl[0], bl[1]);
+            mma16816(acc[2 * qq + 1], a, bh[2], bh[3]);
+            mma16816(acc[2 * qq + 1], a, bl[2], bl[3]);
           }
-          const float rk = 1.0f / sqrtf(sk + kL2NormEps), rq = 1.0f / sqrtf(sq + kL2NormEps);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r = 16 * mt + (lane >> 2) + 8 * hh, m = 32 * nh + 8 * nt + (lane & 3) * 2;
+            st_split2(sm + C_T, LO64, r, m, kC, acc[nt][2 * hh], acc[nt][2 * hh + 1]);
+          }
+      }
+      group_sync(kBarChainGroup);  // (every read of dA has ended: its tiles become dL)
+      KDA_PT(3);
+      // ---- dL = -tril_{-1}(T A^T); X = beta dL.  A warp: the 16-column blocks nh and nh + 2
+      // of its 16 rows; the blocks above the diagonal are zero (no product, zeros stored). ----
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const int nq = nh + 2 * qq;
+        float acc[2][4] = {};
+        if (nq <= mt) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            uint32_t ah[4], al[4], b[4];
+            lda(sbase + C_T, kC, 16 * mt, 16 * s, ah);  // element (r, m) = T[r][m]
+            lda(sbase + C_T + LO64, kC, 16 * mt, 16 * s, al);
+            ldb(sbase + C_A, kC, 16 * nq, 16 * s, b);  // element (m, i) = A[i][m]
+            mma16816(acc[0], ah, b[0], b[1]);
+            mma16816(acc[0], al, b[0], b[1]);
+            mma16816(acc[1], ah, b[2], b[3]);
+            mma16816(acc[1], al, b[2], b[3]);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r = 16 * mt + (lane >> 2) + 8 * hh, i = 16 * nq + 8 * nt + (lane & 3) * 2;
+            const float d0 = (i < r) ? -acc[nt][2 * hh] : 0.f, d1 = (i + 1 < r) ? -acc[nt][2 * hh + 1] : 0.f;
+            st_split2(sm + CK_DA, LO128, r, i, kC, d0, d1);
+            st_split2(sm + C_XB, LO64, r, i, kC, beta[r] * d0, beta[r] * d1);
+          }
+      }
+    } else {
+      const int tb = tid - kGroupWarps * 32;  // 0..255
+      if (tb == 0) {  // raw k, q
+        fence_async_smem();
+        mbar_expect_tx(bar_kq, 32768u);
+        tma_tile(sbase + CK_KRAW, &maps.k, h, t0, bar_kq);
+        tma_tile(sbase + CK_QRAW, &maps.q, h, t0, bar_kq);
+      }
+      if (kGate) {  // the decay from the raw gate
+        kgate_tile<kGroupWarps * 32>(G, kGD, len, P.K, j, ga, tb);
+        group_sync(kBarTileGroup);
+      }
+      int wide_c = 0;
+      if (tb < kD) {  // G and the reference m = (G_first + G_last) / 2 per channel
+        const int c = tb;
+        float s = 0.f;
+        float col[kC];
+#pragma unroll
+        for (int r = 0; r < kC; ++r) col[r] = G[r * kGD + c];
+#pragma unroll
+        for (int r = 0; r < kC; ++r) {
+          if (r < len) s += col[r];
+          col[r] = s;
+        }
+#pragma unroll
+        for (int r = 0; r < kC; ++r) G[r * kGD + c] = col[r];
+        const float gl = s, m = 0.5f * (col[0] + gl);  // rows past len hold G_last
+        wide_c = !(col[0] - gl <= kChunkSpan);        // (NaN-safe)
+        vec[V_GL * kD + c] = gl;
+        vec[V_GAML * kD + c] = exp2f(gl);
+        vec[V_M * kD + c] = m;
+        vec[V_EM * kD + c] = exp2f(m);
+        vec[V_LM * kD + c] = exp2f(gl - m);
+      }
+      ok &= bar_wait(bar_kq, par, args.err);  // raw k, q
+      if (len < kC)  // rows past the sequence end hold other tokens: clear them
+        for (int it2 = tb; it2 < (kC - len) * 16; it2 += kGroupWarps * 32) {
+          const int r = len + (it2 >> 4), q = it2 & 15;
+          const uint32_t off = (q >> 3) * 8192 + r * 128 + (q & 7) * 16;
+          *reinterpret_cast<uint4 *>(sm + CK_KRAW + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4 *>(sm + CK_QRAW + off) = make_uint4(0, 0, 0, 0);
+        }
+      // a channel's decay span is wider than one reference carries: list the slot for the
+      // block-reference kernel (whose results replace this launch's)
+      if (group_sync_or(kBarTileGroup, wide_c) && tb == 0) W.wide_cgrad[atomicAdd(W.flags + 5, 1)] = (int)cur.slot;
+      {  // the decayed hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2; a half-warp per row
+        const int jj = tb & 15, c0 = jj * 8, rg = tb >> 4;  // four rows per thread
+        float mv[8];
+#pragma unroll
+        for (int e = 0; e < 8; e += 4)
+          *reinterpret_cast<float4 *>(mv + e) = *reinterpret_cast<const float4 *>(vec + V_M * kD + c0 + e);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = rg * 4 + rr;
+          const uint32_t off = sw_chunk(r, jj, kC);
+          float kv[8], qv[8], o[8], e1[8], e2[8];
+          unpack8(*reinterpret_cast<const uint4 *>(sm + CK_KRAW + off), kv);  // raw k, q (zero past len)
+          unpack8(*reinterpret_cast<const uint4 *>(sm + CK_QRAW + off), qv);
+          if (P.l2norm) {  // q/k L2-norm prologue (value-head partials: its backward runs per q/k head afterwards)
+            float sk = 0.f, sq = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              sk = fmaf(kv[e], kv[e], sk);
+              sq = fmaf(qv[e], qv[e], sq);
+            }
+#pragma unroll
+            for (int o2 = 1; o2 < 16; o2 <<= 1) {
+              sk += __shfl_xor_sync(0xffffffffu, sk, o2);
+              sq += __shfl_xor_sync(0xffffffffu, sq, o2);
+            }
+            const float rk = 1.0f / sqrtf(sk + kL2NormEps), rq = 1.0f / sqrtf(sq + kL2NormEps);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              kv[e] *= rk;
+              qv[e] *= rq;
+            }
+            if (kL2 && jj == 0) {  // the rows' inverse norms, for the fused backward
+              vec[V_RN * kD + r] = rk;
+              vec[V_RN * kD + kC + r] = rq;
+            }
+          }
+          float g[8];  // (two 16-byte reads: a half-warp reads one whole row, free of bank conflicts)
+          *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGD + c0);
+          *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGD + c0 + 4);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            kv[e] *= rk;
-            qv[e] *= rq;
+            e1[e] = ex2(g[e] - mv[e]);  // within 2^(+-kChunkSpan/2)
+            e2[e] = ex2(mv[e] - g[e]);
           }
-          if (kL2 && jj == 0) {  // the rows' inverse norms, for the fused backward
-            vec[V_RN * kD + r] = rk;
-            vec[V_RN * kD + kC + r] = rq;
-          }
+          uint4 hi, lo;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
+          split8(o, hi, lo);
+          *reinterpret_cast<uint4 *>(sm + C_KR + off) = hi;  // (over the raw k chunk read above)
+          *reinterpret_cast<uint4 *>(sm + C_KR + LO128 + off) = lo;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
+          split8(o, hi, lo);
+          *reinterpret_cast<uint4 *>(sm + C_QR + off) = hi;  // (over the raw q chunk read above)
+          *reinterpret_cast<uint4 *>(sm + C_QR + LO128 + off) = lo;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
+          split8(o, hi, lo);
+          *reinterpret_cast<uint4 *>(sm + C_KC + off) = hi;
+          *reinterpret_cast<uint4 *>(sm + C_KC + LO128 + off) = lo;
         }
-        float g[8];  // (two 16-byte reads: a half-warp reads one whole row, free of bank conflicts)
-        *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(G + r * kGD + c0);
-        *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(G + r * kGD + c0 + 4);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          e1[e] = ex2(g[e] - mv[e]);  // within 2^(+-kChunkSpan/2)
-          e2[e] = ex2(mv[e] - g[e]);
-        }
-        uint4 hi, lo;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
-        split8(o, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + C_KR + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + C_KR + LO128 + off) = lo;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
-        split8(o, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + C_QR + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + C_QR + LO128 + off) = lo;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
-        split8(o, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + C_KC + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + C_KC + LO128 + off) = lo;
       }
     }
-    fence_async_smem();  // Kr, Qr, Kc and dAqk^T are read by the tensor core from the dL phase on
+    fence_async_smem();  // Kr, Qr, Kc, dAqk, dL and X are read by the tensor core next
     fence_before();
     __syncthreads();
-    KDA_PT(2);
-    // ---- T = A^T dA  (T[r][m] = sum_i' A[i'][r] dA[i'][m]) ----
-    const int mt = warp >> 2, nq = warp & 3;  // 16-row block, 16-column quarter
-    {
-      float acc[2][4] = {};
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        uint32_t a[4], bh[4], bl[4];
-        lda_t(sbase + C_A, kC, 16 * mt, 16 * s, a);  // element (r, i') = A[i'][r]
-        ldb_t(sbase + CK_DA, kC, 16 * nq, 16 * s, bh);  // element (i', m) = dA[i'][m]
-        ldb_t(sbase + CK_DA + LO128, kC, 16 * nq, 16 * s, bl);
-        mma16816(acc[0], a, bh[0], bh[1]);
-        mma16816(acc[0], a, bl[0], bl[1]);
-        mma16816(acc[1], a, bh[2], bh[3]);
-        mma16816(acc[1], a, bl[2], bl[3]);
-      }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * mt + (lane >> 2) + 8 * hh, m = 16 * nq + 8 * nt + (lane & 3) * 2;
-          st_split2(sm + C_T, LO64, r, m, kC, acc[nt][2 * hh], acc[nt][2 * hh + 1]);
-        }
-    }
-    __syncthreads();
-    KDA_PT(3);
-    // ---- dL = -tril_{-1}(T A^T); X = beta dL.  The blocks above the diagonal are zero: their
-    // warps skip the product, and warp 3 (block (0, 3)) issues the yi term of the chain. ----
+    fence_after();
+    KDA_PT(4);
+    // ---- the chain, from one thread (a commit tracks the products its own thread issued) ----
     if (tid == 96) {
-      fence_after();
-      const uint32_t id_yi = idesc(128, 64, 1, 1);
+      const uint32_t id_yi = idesc(128, 64, 1, 1), id_xyr = idesc(128, 128, 1, 0), id_xi = idesc(128, 64, 1, 1);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
 #pragma unroll
@@ -499,43 +566,6 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
           mma(tmem + T_XYI, desc_mn(sbase + C_QR + la, s, 8192), desc_mn(sbase + CK_DAQK + lb, s, 8192), id_yi,
               (s > 0 || p > 0) ? 1u : 0u);
         }
-    }
-    {
-      float acc[2][4] = {};
-      if (nq <= mt) {
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          uint32_t ah[4], al[4], b[4];
-          lda(sbase + C_T, kC, 16 * mt, 16 * s, ah);  // element (r, m) = T[r][m]
-          lda(sbase + C_T + LO64, kC, 16 * mt, 16 * s, al);
-          ldb(sbase + C_A, kC, 16 * nq, 16 * s, b);  // element (m, i) = A[i][m]
-          mma16816(acc[0], ah, b[0], b[1]);
-          mma16816(acc[0], al, b[0], b[1]);
-          mma16816(acc[1], ah, b[2], b[3]);
-          mma16816(acc[1], al, b[2], b[3]);
-        }
-      }
-      // (every read of dA, by the T phase, ended at the barrier before this phase: its tiles
-      // become dL without another)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * mt + (lane >> 2) + 8 * hh, i = 16 * nq + 8 * nt + (lane & 3) * 2;
-          const float d0 = (i < r) ? -acc[nt][2 * hh] : 0.f, d1 = (i + 1 < r) ? -acc[nt][2 * hh + 1] : 0.f;
-          st_split2(sm + CK_DA, LO128, r, i, kC, d0, d1);
-          st_split2(sm + C_XB, LO64, r, i, kC, beta[r] * d0, beta[r] * d1);
-        }
-    }
-    fence_async_smem();  // the chain tiles are read by the tensor core next
-    fence_before();
-    __syncthreads();
-    fence_after();
-    KDA_PT(4);
-    // ---- the X and dL terms of the chain, from the thread that issued the dAqk terms (a
-    // commit tracks the products its own thread issued) ----
-    if (tid == 96) {
-      const uint32_t id_xyr = idesc(128, 128, 1, 0), id_xi = idesc(128, 64, 1, 1);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
 #pragma unroll

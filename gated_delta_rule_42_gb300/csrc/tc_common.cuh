@@ -72,23 +72,29 @@ constexpr int kGLD = 132;  // padded fp32 row stride of the gate tile of the per
 constexpr int kGT = 128;   // row stride of the TMA-loaded gate tile (dense rows)
 
 // The KDA gate over a chunk's [64][ld] gate tile in shared memory (raw
-// pre-activations in, the per-token log2 decay out), elementwise over the
-// block's NT threads: rows < len, channels < K (the rest is never summed).
+// pre-activations in, the per-token log2 decay out), elementwise over NT
+// threads (t: the calling thread's index among them): rows < len, channels < K
+// (the rest is never summed).
 template <int NT>
-__device__ __forceinline__ void kgate_tile(float *G, int ld, int len, int K, int j, const GateArgs &ga) {
+__device__ __forceinline__ void kgate_tile(float *G, int ld, int len, int K, int j, const GateArgs &ga, int t) {
   static_assert(NT % 128 == 0, "each thread keeps one channel");
-  const int c = threadIdx.x & 127;
+  const int c = t & 127;
   if (c >= K) return;
   const float sc = kgate_scale(ga, j), b = kgate_bias(ga, K, j, c);
   if (NT >= 512) {  // few rows per thread: all of them at once
 #pragma unroll
     for (int i = 0; i < kC / (NT / 128); ++i) {
-      const int r = (threadIdx.x >> 7) + i * (NT / 128);
+      const int r = (t >> 7) + i * (NT / 128);
       if (r < len) G[r * ld + c] = kgate_fast(G[r * ld + c] + b, sc, ga.lb);
     }
   } else {
-    for (int r = threadIdx.x >> 7; r < len; r += NT / 128) G[r * ld + c] = kgate_fast(G[r * ld + c] + b, sc, ga.lb);
+    for (int r = t >> 7; r < len; r += NT / 128) G[r * ld + c] = kgate_fast(G[r * ld + c] + b, sc, ga.lb);
   }
+}
+// The same over the whole CTA (NT threads).
+template <int NT = kThr>
+__device__ __forceinline__ void kgate_tile(float *G, int ld, int len, int K, int j, const GateArgs &ga) {
+  kgate_tile<NT>(G, ld, len, K, j, ga, (int)threadIdx.x);
 }
 
 // 1 / sqrt(K) for the head dims of the tensor-core path (64 or 128), exactly.
