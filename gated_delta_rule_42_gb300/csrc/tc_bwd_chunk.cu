@@ -68,7 +68,11 @@ static_assert(CK_DAQK + 8192 + LO128 <= C_XB, "dA/dL and dAqk with their lo twin
 // and the first group's dA, dAqk, T, dL and X tiles are disjoint.
 constexpr int kGroupWarps = 8;
 constexpr int kBarChainGroup = 1, kBarTileGroup = 2;
-constexpr uint32_t CK_KRAW = C_KR, CK_QRAW = C_QR;
+// Raw k and q land in the Kr hi and lo tiles' places once the products that read them (the
+// dh' D^T and Z operands D^T and X^T) are done; the decayed-tile pass rewrites each 16-byte
+// chunk in the thread that read it.
+constexpr uint32_t CK_KRAW = C_KR, CK_QRAW = C_KR + LO128;
+static_assert(CK_KRAW == I_XT && CK_QRAW == I_DT, "raw k, q over the X^T and D^T operands");
 static_assert(C_KC + 2 * 16384 <= CK_DA && CK_DAQK + 8192 + LO128 <= C_XB && C_T + 16384 <= C_G,
               "the two groups' tiles are disjoint");
 // Barrier among the 256 threads of one group.
@@ -237,13 +241,14 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
   float *rb = (float *)(sm + C_RB);
   float *red = (float *)(sm + C_RED);  // [0, 64): sum_v dX v; [64, 192): d(2^G_last)
   uint64_t *bar_s = (uint64_t *)(sm + C_MISC), *bar_p1 = bar_s + 1, *bar_p2 = bar_s + 2;
-  uint64_t *bar_kq = bar_s + 3, *bar = bar_s + 4;
+  uint64_t *bar_kq = bar_s + 3, *bar = bar_s + 4, *bar_g = bar_s + 6;  // (bar_s + 5 holds the tmem slot)
   uint32_t *tslot = (uint32_t *)(sm + C_MISC + 40);
   const float qscale = head_qscale(P.K);  // 1/sqrt(K)
   KDA_PT_DECL;
 
   if (tid == 0) {
     for (int b = 0; b < 5; ++b) bar_init(bar_s + b, 1);
+    bar_init(bar_g, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
@@ -303,10 +308,6 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     // ---- tensor-core products, transposed (M = 128 channels or rows of [X; D]) ----
     if (tid == 0) {
       const uint32_t idk = idesc(128, 128, 0, 0), idd = idesc(128, 64, 0, 1), idz = idesc(128, 128, 0, 1);
-      // [(h dX^T) | (h dO^T)][c][n] = sum_v h[c][v] [dX; dO][n][v]   (K = 128 v; T_DQG = T_NBK + 64)
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma(tmem + T_NBK, desc_k16(sbase + I_H, k, kD), desc_k16(sbase + I_STK, k, 192), idk, k > 0);
       // (dh' D^T)[c][r] = sum_v dh'[c][v] D[r][v]   (D^T is stored [v][r]: an MN-major B)
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -315,7 +316,20 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         mma(tmem + T_Z, desc_k16(sbase + I_STK + 64 * 128, k, 192), desc_mn(sbase + I_XT, k, 16384), idz, k > 0);
+      commit(bar_g);  // X^T and D^T are read: raw k, q may land there
+      // [(h dX^T) | (h dO^T)][c][n] = sum_v h[c][v] [dX; dO][n][v]   (K = 128 v; T_DQG = T_NBK + 64)
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma(tmem + T_NBK, desc_k16(sbase + I_H, k, kD), desc_k16(sbase + I_STK, k, 192), idk, k > 0);
       commit(bar);
+      if (bar_wait(bar_g, par, args.err)) {  // raw k, q
+        fence_async_smem();
+        mbar_expect_tx(bar_kq, 32768u);
+        tma_tile(sbase + CK_KRAW, &maps.k, h, t0, bar_kq);
+        tma_tile(sbase + CK_QRAW, &maps.q, h, t0, bar_kq);
+      } else {
+        ok = false;
+      }
     }
     // meanwhile (warp 0 only issues the products): warps 4..7 d(2^G_last)[c] =
     // sum_v dh'[c][v] h[c][v]; warps 1..3, 8..15 dv = beta dX and sum_v dX v
@@ -441,14 +455,9 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
             st_split2(sm + C_XB, LO64, r, i, kC, beta[r] * d0, beta[r] * d1);
           }
       }
+      KDA_PT(22);
     } else {
       const int tb = tid - kGroupWarps * 32;  // 0..255
-      if (tb == 0) {  // raw k, q
-        fence_async_smem();
-        mbar_expect_tx(bar_kq, 32768u);
-        tma_tile(sbase + CK_KRAW, &maps.k, h, t0, bar_kq);
-        tma_tile(sbase + CK_QRAW, &maps.q, h, t0, bar_kq);
-      }
       if (kGate) {  // the decay from the raw gate
         kgate_tile<kGroupWarps * 32>(G, kGD, len, P.K, j, ga, tb);
         group_sync(kBarTileGroup);
@@ -475,7 +484,9 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
         vec[V_EM * kD + c] = exp2f(m);
         vec[V_LM * kD + c] = exp2f(gl - m);
       }
+      KDA_PT(19);
       ok &= bar_wait(bar_kq, par, args.err);  // raw k, q
+      KDA_PT(20);
       if (len < kC)  // rows past the sequence end hold other tokens: clear them
         for (int it2 = tb; it2 < (kC - len) * 16; it2 += kGroupWarps * 32) {
           const int r = len + (it2 >> 4), q = it2 & 15;
@@ -486,6 +497,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       // a channel's decay span is wider than one reference carries: list the slot for the
       // block-reference kernel (whose results replace this launch's)
       if (group_sync_or(kBarTileGroup, wide_c) && tb == 0) W.wide_cgrad[atomicAdd(W.flags + 5, 1)] = (int)cur.slot;
+      KDA_PT(21);
       {  // the decayed hi/lo tiles Kr = k e1, Qr = q~ e1, Kc = k e2; a half-warp per row
         const int jj = tb & 15, c0 = jj * 8, rg = tb >> 4;  // four rows per thread
         float mv[8];
@@ -534,12 +546,12 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = kv[e] * e1[e];
           split8(o, hi, lo);
-          *reinterpret_cast<uint4 *>(sm + C_KR + off) = hi;  // (over the raw k chunk read above)
-          *reinterpret_cast<uint4 *>(sm + C_KR + LO128 + off) = lo;
+          *reinterpret_cast<uint4 *>(sm + C_KR + off) = hi;          // (over the raw k chunk read above)
+          *reinterpret_cast<uint4 *>(sm + C_KR + LO128 + off) = lo;  // (over the raw q chunk read above)
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = qv[e] * qscale * e1[e];
           split8(o, hi, lo);
-          *reinterpret_cast<uint4 *>(sm + C_QR + off) = hi;  // (over the raw q chunk read above)
+          *reinterpret_cast<uint4 *>(sm + C_QR + off) = hi;
           *reinterpret_cast<uint4 *>(sm + C_QR + LO128 + off) = lo;
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = kv[e] * e2[e];
@@ -548,6 +560,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
           *reinterpret_cast<uint4 *>(sm + C_KC + LO128 + off) = lo;
         }
       }
+      KDA_PT(23);
     }
     fence_async_smem();  // Kr, Qr, Kc, dAqk, dL and X are read by the tensor core next
     fence_before();

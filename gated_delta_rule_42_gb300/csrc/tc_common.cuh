@@ -22,7 +22,10 @@ using namespace umma;
 #ifdef KDA_PHASE_TIMING
 static __device__ long long kda_phase_cycles[32];
 static __shared__ long long kda_pt_acc[33];  // [32] = time of the last stamp
-#define KDA_PT_ON (threadIdx.x == 0)
+#ifndef KDA_PT_TID
+#define KDA_PT_TID 0  // the thread whose timeline is recorded
+#endif
+#define KDA_PT_ON (threadIdx.x == KDA_PT_TID)
 #define KDA_PT_DECL                                             \
   do {                                                          \
     if (KDA_PT_ON) {                                            \
