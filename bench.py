@@ -132,21 +132,21 @@ def kernel_bytes_per_token(name, cfg):
 # those sources are unchanged.
 NCU_TRAFFIC = {
     "kda_bwd_intra_tc": dict(
-        bytes_per_token=1282380032 / 8192,  # 974.3 MB read + 308.1 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=1282971648 / 8192,  # 974.3 MB read + 308.7 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_chunk.cu", "gated_delta_rule_42_gb300/csrc/tc_intra.cuh", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="5dc08a1915124138a9f8d926e8cbe4e5a5a10bd7b8a9f555a9d5148d2cc1946f"),
+        sha256="2ceb37b15769b237d4fdf6d5b506abb1b4e4d4c79cf60ce18b1186ec0b87ad06"),
     "kda_prep_tc": dict(
-        bytes_per_token=493784064 / 8192,  # 270.6 MB read + 223.2 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=512473856 / 8192,  # 271.0 MB read + 241.5 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_prep.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="a391e31c176d0906a92b747c39a0a983d38f17e4cbace7852bdd1e243bb80dcb"),
+        sha256="4ead00db5b17147d97749679830f43945dcd04f9f84a5c236afb3c7cbda103d6"),
     "kda_fwd_tc_save": dict(
-        bytes_per_token=624922368 / 8192,  # 339.2 MB read + 285.8 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=624946432 / 8192,  # 339.1 MB read + 285.9 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_fwd.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="88c527df14544aa8eaafca0eb372e1ce3377af9cd7f84b9919bfa5466caf9c1b"),
+        sha256="fae778c4ab025e760bca5f5321e1e0cfcc7c54cd81732da36474481e1753f12f"),
     "kda_bwd_scan_tc": dict(
-        bytes_per_token=559956224 / 8192,  # 337.7 MB read + 222.3 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=560227584 / 8192,  # 337.7 MB read + 222.5 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_scan.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="da1ee511eec4127d68a680db53ef9fb5b01fdf26335150453d55ef709d32f409"),
+        sha256="fa160889992d5989fb10277ed479daa765b8d06e9c96eaea678e6017847af27e"),
 }
 
 

@@ -64,8 +64,10 @@ static_assert(T_YR == T_XR + 64, "xr and yr are one N = 128 product");
 constexpr uint32_t CK_DA = C_DAB, CK_DAQK = C_DAB + 8192;
 static_assert(CK_DAQK + 8192 + LO128 <= C_XB, "dA/dL and dAqk with their lo twins");
 // From the products to the chain the CTA runs as two groups of 8 warps (named barriers 1
-// and 2): raw k and q land in the Kr and Qr hi tiles' places, so the second group's tiles
-// and the first group's dA, dAqk, T, dL and X tiles are disjoint.
+// and 2): raw k and q land in the Kr hi and lo tiles' places, so the second group's tiles
+// and the first group's dA, dAqk, T, dL and X tiles are disjoint.  A few loops of the two
+// groups stay rolled ("#pragma unroll 1"): the kernel's code is large, and with the KDA
+// gate's code inside it an unrolled version spent most of its stalls on instruction fetch.
 constexpr int kGroupWarps = 8;
 constexpr int kBarChainGroup = 1, kBarTileGroup = 2;
 // Raw k and q land in the Kr hi and lo tiles' places once the products that read them (the
@@ -372,8 +374,12 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
 
     // ---- two warp groups until the chain: warps 0..7 take dA and dAqk out of TMEM and run
     // T = A^T dA and dL; warps 8..15 load the raw k, q rows and build G, the reference and the
-    // decayed tiles.  Their tiles are disjoint: the raw rows land in the Kr and Qr hi tiles'
+    // decayed tiles.  Their tiles are disjoint: the raw rows land in the Kr hi and lo tiles'
     // places (dead product operands), each 16-byte chunk rewritten by the thread that read it. ----
+    if (kGate) {  // the decay from the raw gate, on every warp before the groups part
+      kgate_tile<kCT>(G, kGD, len, P.K, j, ga);
+      __syncthreads();
+    }
     if (warp < kGroupWarps) {
       {  // Z: lanes 0..63 (r), cols 64..127 (i) = dAqk[r][i]; lanes 64..127 (m), cols 0..63 (i) = dA[m][i]
         const int ch = warp >> 2, row = 32 * (quarter & 1) + lane;  // ch: the column half
@@ -401,7 +407,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       const int mt = warp >> 1, nh = warp & 1;
       {
         float acc[4][4] = {};
-#pragma unroll
+#pragma unroll 1
         for (int s = 0; s < 4; ++s) {
           uint32_t a[4];
           lda_t(sbase + C_A, kC, 16 * mt, 16 * s, a);  // element (r, i') = A[i'][r]
@@ -428,12 +434,12 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       KDA_PT(3);
       // ---- dL = -tril_{-1}(T A^T); X = beta dL.  A warp: the 16-column blocks nh and nh + 2
       // of its 16 rows; the blocks above the diagonal are zero (no product, zeros stored). ----
-#pragma unroll
+#pragma unroll 1
       for (int qq = 0; qq < 2; ++qq) {
         const int nq = nh + 2 * qq;
         float acc[2][4] = {};
         if (nq <= mt) {
-#pragma unroll
+#pragma unroll 1
           for (int s = 0; s < 4; ++s) {
             uint32_t ah[4], al[4], b[4];
             lda(sbase + C_T, kC, 16 * mt, 16 * s, ah);  // element (r, m) = T[r][m]
@@ -458,10 +464,6 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       KDA_PT(22);
     } else {
       const int tb = tid - kGroupWarps * 32;  // 0..255
-      if (kGate) {  // the decay from the raw gate
-        kgate_tile<kGroupWarps * 32>(G, kGD, len, P.K, j, ga, tb);
-        group_sync(kBarTileGroup);
-      }
       int wide_c = 0;
       if (tb < kD) {  // G and the reference m = (G_first + G_last) / 2 per channel
         const int c = tb;
@@ -504,8 +506,8 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
 #pragma unroll
         for (int e = 0; e < 8; e += 4)
           *reinterpret_cast<float4 *>(mv + e) = *reinterpret_cast<const float4 *>(vec + V_M * kD + c0 + e);
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
+#pragma unroll 1
+        for (int rr = 0; rr < 4; ++rr) {  // (rolled: the kernel's code stays within the instruction cache)
           const int r = rg * 4 + rr;
           const uint32_t off = sw_chunk(r, jj, kC);
           float kv[8], qv[8], o[8], e1[8], e2[8];

@@ -578,7 +578,7 @@ kda_prep_chunk_tc_kernel(Problem P, Workspace W, int *err, const __grid_constant
         *reinterpret_cast<float4 *>(lm + e) = *reinterpret_cast<const float4 *>(vec + W_LAM * kD + c0 + e);
       }
       uint4 kc[4];  // Kc rows, written once every thread has read its G values
-#pragma unroll
+#pragma unroll 1    // (rolled: the kernel's code stays small; unrolled it stalled on instruction fetch)
       for (int rr = 0; rr < 4; ++rr) {
         const int r = rg * 4 + rr;
         const uint32_t off = sw_chunk(r, jj, kC);
