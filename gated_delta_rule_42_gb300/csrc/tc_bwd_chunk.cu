@@ -158,15 +158,42 @@ __device__ __forceinline__ float rows4_sum(float (&v)[4]) {
   for (int o = 4; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
   return t;
 }
-// An fp32 value parked as two 16-bit halves in a hi/lo tile pair's slots (and read back).
-__device__ __forceinline__ void park32(unsigned char *tile, uint32_t lo_off, uint32_t off, float x) {
-  const uint32_t b = __float_as_uint(x);
-  *reinterpret_cast<uint16_t *>(tile + off) = (uint16_t)(b >> 16);
-  *reinterpret_cast<uint16_t *>(tile + lo_off + off) = (uint16_t)(b & 0xffffu);
+// kL2: four values per row parked in tensor memory, in the columns of this thread's lane the
+// assembly has just read (T_NBK, T_DQG, T_DKH, T_XR + row): each (lane, column) belongs to
+// one thread, which reads it back after the CTA barrier.  Four consecutive rows at a time.
+__device__ __forceinline__ void tmem_park4x4(uint32_t t, const float (&a)[4], const float (&b)[4],
+                                             const float (&c)[4], const float (&d)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%4,%5,%6,%7};\n"
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%1], {%8,%9,%10,%11};\n"
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%2], {%12,%13,%14,%15};\n"
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%3], {%16,%17,%18,%19};\n" ::"r"(t + T_NBK),
+      "r"(t + T_DQG), "r"(t + T_DKH), "r"(t + T_XR), "r"(__float_as_uint(a[0])), "r"(__float_as_uint(a[1])),
+      "r"(__float_as_uint(a[2])), "r"(__float_as_uint(a[3])), "r"(__float_as_uint(b[0])), "r"(__float_as_uint(b[1])),
+      "r"(__float_as_uint(b[2])), "r"(__float_as_uint(b[3])), "r"(__float_as_uint(c[0])), "r"(__float_as_uint(c[1])),
+      "r"(__float_as_uint(c[2])), "r"(__float_as_uint(c[3])), "r"(__float_as_uint(d[0])), "r"(__float_as_uint(d[1])),
+      "r"(__float_as_uint(d[2])), "r"(__float_as_uint(d[3]))
+      : "memory");
 }
-__device__ __forceinline__ float unpark32(const unsigned char *tile, uint32_t lo_off, uint32_t off) {
-  return __uint_as_float(((uint32_t)*reinterpret_cast<const uint16_t *>(tile + off) << 16) |
-                         (uint32_t)*reinterpret_cast<const uint16_t *>(tile + lo_off + off));
+__device__ __forceinline__ void tmem_unpark4x4(uint32_t t, float (&a)[4], float (&b)[4], float (&c)[4], float (&d)[4]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%16];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%4,%5,%6,%7}, [%17];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%8,%9,%10,%11}, [%18];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%12,%13,%14,%15}, [%19];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(t + T_NBK), "r"(t + T_DQG), "r"(t + T_DKH), "r"(t + T_XR)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[4 + i]);
+    c[i] = __uint_as_float(r[8 + i]);
+    d[i] = __uint_as_float(r[12 + i]);
+  }
 }
 __device__ __forceinline__ int tot_row(int kind, int R) {
   const int k = 4 * kind + R;
@@ -225,8 +252,8 @@ __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
 // kGate: the KDA gate inside the op; kSG: one decay per (token, value head), dg summed over
 // the channels (the two are not combined); kL2: the q/k L2-norm prologue with HV = H, its
 // backward dx = r (dy - y (y . dy)) fused: a first pass over the assembly parks each
-// element's dy and y in the thread's own tile slots and forms the row dots, a second pass
-// after a barrier stores dq, dk.
+// element's dy and y in tensor-memory columns it has read and forms the row dots, a second
+// pass after a barrier (and after the next slot's last loads are issued) stores dq, dk.
 template <bool kGate, bool kSG, bool kL2>
 __global__ void __launch_bounds__(kCT, 1)
 kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __grid_constant__ TmaMaps maps,
@@ -624,6 +651,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       if (s4 == 1) KDA_PT(18);
       const float4 b4 = *reinterpret_cast<const float4 *>(beta + 16 * R + 4 * s4);
       float dq4[4], dk4[4];  // kL2: y . dy of the quad's rows over this thread's channel
+      float pdq[4], pyq[4], pyk[4], pdk[4];  // kL2: dy and y of the quad's rows, parked below
 #pragma unroll
       for (int u = 0; u < 4; u += 2) {
         const int t = 4 * s4 + u, r = 16 * R + t;  // rows r, r + 1
@@ -663,14 +691,14 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
         bp[t + 1] = bq.y;
         if (kL2) {  // first pass: park dy (dq2, dk2) and y (Qr e2 = q~ normalised, Kr e2 = k normalised)
           const float2 yq = __fmul2_rn(Qr, e2), yk = __fmul2_rn(Kr, e2);
-          park32(sm + C_KC, LO128, o0, dq2.x);
-          park32(sm + C_KC, LO128, o1, dq2.y);
-          park32(sm + C_QR, LO128, o0, yq.x);
-          park32(sm + C_QR, LO128, o1, yq.y);
-          park32(sm + C_KR, LO128, o0, yk.x);
-          park32(sm + C_KR, LO128, o1, yk.y);
-          G[r * kGD + c] = dk2.x;
-          G[(r + 1) * kGD + c] = dk2.y;
+          pdq[u] = dq2.x;
+          pdq[u + 1] = dq2.y;
+          pyq[u] = yq.x;
+          pyq[u + 1] = yq.y;
+          pyk[u] = yk.x;
+          pyk[u + 1] = yk.y;
+          pdk[u] = dk2.x;
+          pdk[u + 1] = dk2.y;
           dq4[u] = yq.x * dq2.x;
           dq4[u + 1] = yq.y * dq2.y;
           dk4[u] = yk.x * dk2.x;
@@ -695,6 +723,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
         }
       }
       if (kL2) {  // the quad's row dots over the warp's 32 channels, into [row][quarter] tables
+        tmem_park4x4(tq + (uint32_t)(16 * R + 4 * s4), pdq, pyq, pyk, pdk);
         const float tqd = rows4_sum(dq4), tkd = rows4_sum(dk4);
         if ((lane & 7) == 0) {
           const int row = 16 * R + 4 * s4 + (lane >> 3);
@@ -729,46 +758,13 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       const float v = rows16_sum(bp);
       if ((lane & 1) == 0) rb[quarter * kC + 16 * R + (lane >> 1)] = v;
     }
+    if (kL2) asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
     fence_before();
     // every read of the tiles, G and beta is done; the totals are published; every wait of
     // the slot is behind, so its outcome is known here (the KDA gate and the scalar gate
     // reduce theirs at the end of the slot, where their sums need a barrier anyway)
     bool all_ok = __syncthreads_and(ok) != 0;
     KDA_PT(10);
-    if (kL2) {  // second pass: dq, dk = r (dy - y (y . dy)) from the parked values and the row dots
-#pragma unroll
-      for (int p2 = 0; p2 < 8; ++p2) {
-        const int r = 16 * R + 2 * p2;
-        const uint32_t o0 = sw_off(r, c, kC), o1 = sw_off(r + 1, c, kC);
-        const float4 dqa = *reinterpret_cast<const float4 *>(sm + C_DOTQ + r * 16);
-        const float4 dqb = *reinterpret_cast<const float4 *>(sm + C_DOTQ + (r + 1) * 16);
-        const float4 dka = *reinterpret_cast<const float4 *>(sm + C_DOTK + r * 16);
-        const float4 dkb = *reinterpret_cast<const float4 *>(sm + C_DOTK + (r + 1) * 16);
-        const float2 dotq = make_float2(dqa.x + dqa.y + dqa.z + dqa.w, dqb.x + dqb.y + dqb.z + dqb.w);
-        const float2 dotk = make_float2(dka.x + dka.y + dka.z + dka.w, dkb.x + dkb.y + dkb.z + dkb.w);
-        const float2 rk = make_float2(vec[V_RN * kD + r], vec[V_RN * kD + r + 1]);
-        const float2 rq = make_float2(vec[V_RN * kD + kC + r], vec[V_RN * kD + kC + r + 1]);
-        const float2 dq2 = make_float2(unpark32(sm + C_KC, LO128, o0), unpark32(sm + C_KC, LO128, o1));
-        const float2 yq = make_float2(unpark32(sm + C_QR, LO128, o0), unpark32(sm + C_QR, LO128, o1));
-        const float2 yk = make_float2(unpark32(sm + C_KR, LO128, o0), unpark32(sm + C_KR, LO128, o1));
-        const float2 dk2 = make_float2(G[r * kGD + c], G[(r + 1) * kGD + c]);
-        // dq = rq (qscale dq2 - (yq / qscale) (y . dy)), dk = rk (dk2 - yk (y . dy)) (yq carries qscale)
-        const float iqs = 1.f / qscale;
-        const float2 fq = make_float2(rq.x * (qscale * dq2.x - yq.x * iqs * dotq.x),
-                                      rq.y * (qscale * dq2.y - yq.y * iqs * dotq.y));
-        const float2 fk = make_float2(rk.x * (dk2.x - yk.x * dotk.x), rk.y * (dk2.y - yk.y * dotk.y));
-        const float gq = __shfl_xor_sync(0xffffffffu, odd ? fq.x : fq.y, 1);
-        const float gk = __shfl_xor_sync(0xffffffffu, odd ? fk.x : fk.y, 1);
-        const float2 pq = odd ? make_float2(gq, fq.y) : make_float2(fq.x, gq);
-        const float2 pk = odd ? make_float2(gk, fk.y) : make_float2(fk.x, gk);
-        if (r + (odd ? 1 : 0) < len && cin) {
-          const size_t tok = (size_t)(t0 + r + (odd ? 1 : 0));
-          *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dq + (tok * H + h) * P.K + cp) = pack_bf16(pq.x, pq.y);
-          *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dk + (tok * H + h) * P.K + cp) = pack_bf16(pk.x, pk.y);
-        }
-      }
-      __syncthreads();  // every parked value is read: the tiles are dead
-    }
     if (more) {  // the next slot's remaining inputs into the dead tiles; its G and beta
       if (tid == 0) {
         mbar_expect_tx(bar_p2, kBytesP2 + (kSG ? 0u : kBytesG));
@@ -781,6 +777,45 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
         else tma_load3(sbase + C_G, &maps.g, 0, nxt.j, nxt.t0, bar_p2);
       }
       issue_beta(beta, P, nxt);
+    }
+    if (kL2) {  // second pass: dq, dk = r (dy - y (y . dy)) from the parked values and the row dots
+      fence_after();
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float pdq[4], pyq[4], pyk[4], pdk[4];
+        tmem_unpark4x4(tq + (uint32_t)(16 * R + 4 * q4), pdq, pyq, pyk, pdk);
+#pragma unroll
+        for (int u = 0; u < 4; u += 2) {
+          const int r = 16 * R + 4 * q4 + u;
+          const float4 dqa = *reinterpret_cast<const float4 *>(sm + C_DOTQ + r * 16);
+          const float4 dqb = *reinterpret_cast<const float4 *>(sm + C_DOTQ + (r + 1) * 16);
+          const float4 dka = *reinterpret_cast<const float4 *>(sm + C_DOTK + r * 16);
+          const float4 dkb = *reinterpret_cast<const float4 *>(sm + C_DOTK + (r + 1) * 16);
+          const float2 dotq = make_float2(dqa.x + dqa.y + dqa.z + dqa.w, dqb.x + dqb.y + dqb.z + dqb.w);
+          const float2 dotk = make_float2(dka.x + dka.y + dka.z + dka.w, dkb.x + dkb.y + dkb.z + dkb.w);
+          const float2 rk = make_float2(vec[V_RN * kD + r], vec[V_RN * kD + r + 1]);
+          const float2 rq = make_float2(vec[V_RN * kD + kC + r], vec[V_RN * kD + kC + r + 1]);
+          const float2 dq2 = make_float2(pdq[u], pdq[u + 1]), yq = make_float2(pyq[u], pyq[u + 1]);
+          const float2 yk = make_float2(pyk[u], pyk[u + 1]), dk2 = make_float2(pdk[u], pdk[u + 1]);
+          // dq = rq (qscale dq2 - (yq / qscale) (y . dy)), dk = rk (dk2 - yk (y . dy)) (yq carries qscale)
+          const float iqs = 1.f / qscale;
+          const float2 fq = make_float2(rq.x * (qscale * dq2.x - yq.x * iqs * dotq.x),
+                                        rq.y * (qscale * dq2.y - yq.y * iqs * dotq.y));
+          const float2 fk = make_float2(rk.x * (dk2.x - yk.x * dotk.x), rk.y * (dk2.y - yk.y * dotk.y));
+          const float gq = __shfl_xor_sync(0xffffffffu, odd ? fq.x : fq.y, 1);
+          const float gk = __shfl_xor_sync(0xffffffffu, odd ? fk.x : fk.y, 1);
+          const float2 pq = odd ? make_float2(gq, fq.y) : make_float2(fq.x, gq);
+          const float2 pk = odd ? make_float2(gk, fk.y) : make_float2(fk.x, gk);
+          if (r + (odd ? 1 : 0) < len && cin) {
+            const size_t tok = (size_t)(t0 + r + (odd ? 1 : 0));
+            *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dq + (tok * H + h) * P.K + cp) =
+                pack_bf16(pq.x, pq.y);
+            *reinterpret_cast<uint32_t *>((__nv_bfloat16 *)args.dk + (tok * H + h) * P.K + cp) = pack_bf16(pk.x, pk.y);
+          }
+        }
+      }
+      // (the KDA gate's partials go where the dot tables are, after the dg scan)
+      if (kGate) __syncthreads();
     }
     float sgx[kSgIt];  // kSG: the next slot's scalars, stored into the gate tile at the end of the slot
     if (kSG && more) sg_load(sgx, P, nxt);
