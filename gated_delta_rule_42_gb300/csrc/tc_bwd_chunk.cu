@@ -195,6 +195,16 @@ __device__ __forceinline__ void tmem_unpark4x4(uint32_t t, float (&a)[4], float 
     d[i] = __uint_as_float(r[12 + i]);
   }
 }
+// (dg/dx, dg/dA_log) of the KDA gate at x on the hardware exponential, logarithm and
+// reciprocal (bf16-path accuracy).  The unbounded form g = -s softplus(x) takes both from
+// one exponential e = exp(-|x|): sigmoid(x) = (x >= 0 ? 1 : e) / (1 + e) and
+// softplus(x) = max(x, 0) + ln(1 + e); the bounded form g = lb sigmoid(s x) as before.
+__device__ __forceinline__ float2 gate_grad(float x, float s, float lb) {
+  if (lb < 0.f) return kgate_grad_fast(x, s, lb);
+  const float e = __expf(-fabsf(x)), r = __fdividef(1.f, 1.f + e);
+  const float sg = x >= 0.f ? r : e * r, sp = fmaxf(x, 0.f) + __logf(1.f + e);
+  return make_float2(-s * sg, -s * sp);
+}
 __device__ __forceinline__ int tot_row(int kind, int R) {
   const int k = 4 * kind + R;
   return k < 6 ? V_D + k : V_LAM + 2 + (k - 6);
@@ -318,6 +328,11 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     const int c_n2 = in_n2 ? (int)(s_n2 / HV) : 0;
     const int4 ent_n2 = W.chunk[c_n2];
     bool ok = true;  // every bounded wait of this thread succeeded
+    float gsc = 0.f, gbias = 0.f;  // kGate: the slot's gate scale and the bias of channel tid % 128
+    if (kGate) {  // (loaded here: the gate pass and the dg scan use them thousands of cycles on)
+      gsc = kgate_scale(ga, j);
+      gbias = (tid & 127) < P.K ? kgate_bias(ga, P.K, j, tid & 127) : 0.f;
+    }
     KDA_PT(13);
     ok &= bar_wait(bar_s, par, args.err);
     ok &= bar_wait(bar_p1, par, args.err);
@@ -403,8 +418,16 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
     // T = A^T dA and dL; warps 8..15 load the raw k, q rows and build G, the reference and the
     // decayed tiles.  Their tiles are disjoint: the raw rows land in the Kr hi and lo tiles'
     // places (dead product operands), each 16-byte chunk rewritten by the thread that read it. ----
-    if (kGate) {  // the decay from the raw gate, on every warp before the groups part
-      kgate_tile<kCT>(G, kGD, len, P.K, j, ga);
+    if (kGate) {  // the decay from the raw gate, on every warp before the groups part: channel
+                  // tid % 128, rows tid / 128 + 4 i
+      const int cg = tid & 127;
+      if (cg < P.K) {
+#pragma unroll
+        for (int i = 0; i < kC / 4; ++i) {
+          const int r = (tid >> 7) + 4 * i;
+          if (r < len) G[r * kGD + cg] = kgate_fast(G[r * kGD + cg] + gbias, gsc, ga.lb);
+        }
+      }
       __syncthreads();
     }
     if (warp < kGroupWarps) {
@@ -849,7 +872,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
       KDA_PT(17);
       const float carried = kLn2 * vec[V_GAML * kD + c] * red[64 + c];
       float qs = qoff, ps = poff + kLn2 * ks;
-      const float sc = kGate ? kgate_scale(ga, j) : 0.f, gb = kGate && cin ? kgate_bias(ga, P.K, j, c) : 0.f;
+      const float sc = gsc, gb = cin ? gbias : 0.f;  // (c == tid % 128: the channel whose bias it loaded)
       float sgr[16];  // kSG: this thread's dg of each row, summed over the channels below
 #pragma unroll
       for (int p2 = 7; p2 >= 0; --p2) {
@@ -862,7 +885,7 @@ kda_bwd_intra_chunk_tc_kernel(Problem P, Workspace W, IntraArgs args, const __gr
           if (hi) ps += pv[t];
           float v = qs + carried + (hi ? ps : pv[t]);
           if (kGate) {  // da = dG dg/da; the parameter gradients' partials
-            const float2 d = kgate_grad_fast(ar[t] + gb, sc, ga.lb);
+            const float2 d = gate_grad(ar[t] + gb, sc, ga.lb);
             const bool use = r < len && cin;
             gpb += use ? v * d.x : 0.f;
             gpa = use ? fmaf(v, d.y, gpa) : gpa;
