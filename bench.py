@@ -132,9 +132,9 @@ def kernel_bytes_per_token(name, cfg):
 # those sources are unchanged.
 NCU_TRAFFIC = {
     "kda_bwd_intra_tc": dict(
-        bytes_per_token=1282525952 / 8192,  # 974.3 MB read + 308.2 MB written, B=8 T=1024 H=HV=32
+        bytes_per_token=1282263552 / 8192,  # 974.3 MB read + 308.0 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_bwd_chunk.cu", "gated_delta_rule_42_gb300/csrc/tc_intra.cuh", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
-        sha256="a2474a4da988ff150f81d784031b8b8b7f675f609c2ef3aa9e20f596b8863ff3"),
+        sha256="4581ef8aa45c4e51f08b58124c6303e06625a71ded908159970c1f09398680c1"),
     "kda_prep_tc": dict(
         bytes_per_token=512473856 / 8192,  # 271.0 MB read + 241.5 MB written, B=8 T=1024 H=HV=32
         sources=("gated_delta_rule_42_gb300/csrc/tc_prep.cu", "gated_delta_rule_42_gb300/csrc/tc_common.cuh", "gated_delta_rule_42_gb300/csrc/umma.cuh", "gated_delta_rule_42_gb300/csrc/kda_internal.cuh"),
