@@ -117,6 +117,7 @@ def kernel_bytes_per_token(name, cfg):
         "simple_bwd_intra_kernel": 3 * qk - qk + vv + vv + b + f32K + 2 * cc + 2 * hh + 2 * f32V
         + vv + b + g + 2 * f32K + 2 * f32K,
         "group_reduce_kernel": 2 * f32K + 2 * qk,
+        "group_reduce4_kernel": 2 * f32K + 2 * qk,
         "group_reduce_l2norm_kernel": 2 * f32K + 4 * qk,
         "l2norm_rows_kernel": 4 * qk,
         "gate_expand_kernel": 4 * HV + f32K,
